@@ -1,0 +1,203 @@
+"""CPU oracle for the Mixture-of-Experts FFN layer forward — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline / reference legs may
+import this package.  The product library (``libmoe.so`` and its Python binding) never imports
+it, and the two share no code: this wrapper loads ``liboracle.so`` built from
+``moe_oracle.cpp`` with the host C++ compiler.
+
+Arrays are numpy, C-contiguous; bf16 tensors travel as ``uint16`` bit patterns.
+The arithmetic, its sources and its readings of the pages are documented in ``moe_oracle.cpp``.
+Every function here is pinned by ``tests/test_oracle_pins.py`` (closed forms, a hand-worked
+example, library routines, a float64 brute force and the layer's invariants).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# -ffp-contract=off: no fused multiply-add contraction, so x86 and Arm builds round alike.
+CXXFLAGS = ["-O3", "-std=c++17", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared"]
+
+
+def build(src: str = _SRC, out: str = _LIB, extra: list[str] | None = None) -> str:
+    """Compile the oracle shared library (``g++``).  Returns the path of the built library."""
+    cmd = ["g++", *CXXFLAGS, *(extra or []), src, "-o", out + ".tmp"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    os.replace(out + ".tmp", out)
+    return out
+
+
+def _needs_build() -> bool:
+    return not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+
+
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_F32P = ctypes.POINTER(ctypes.c_float)
+_U16P = ctypes.POINTER(ctypes.c_uint16)
+_INT = ctypes.c_int
+
+_SIGS = {
+    "oracle_num_threads": ([], _INT),
+    "oracle_route": ([_F32P, _INT, _INT, _INT, _I32P, _F32P], _INT),
+    "oracle_permute": ([_I32P, _INT, _INT, _INT, _I32P, _I32P, _I32P, _I32P], _INT),
+    "oracle_gather_rows": ([_U16P, _I32P, _INT, _INT, _U16P], None),
+    "oracle_gateup_swiglu": ([_U16P, _I32P, _INT, _U16P, _INT, _INT, _F32P], None),
+    "oracle_down": ([_F32P, _I32P, _INT, _U16P, _INT, _INT, _F32P], None),
+    "oracle_down_bf16": ([_U16P, _I32P, _INT, _U16P, _INT, _INT, _F32P], None),
+    "oracle_combine": ([_F32P, _F32P, _I32P, _INT, _INT, _INT, _F32P], None),
+    "oracle_forward": ([_U16P, _F32P, _U16P, _U16P, _INT, _INT, _INT, _INT, _INT, _F32P], _INT),
+    "oracle_forward_tokens": ([_U16P, _F32P, _U16P, _U16P, _INT, _INT, _INT, _INT, _INT, _I32P, _INT,
+                               _F32P], _INT),
+}
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            if _needs_build():
+                build()
+            _lib = load_library(_LIB)
+    return _lib
+
+
+def _p(a: np.ndarray, ptype):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ptype)
+
+
+def _c(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+class Oracle:
+    """Thin numpy wrapper over one loaded oracle library (the default one, or a test's build)."""
+
+    def __init__(self, library: ctypes.CDLL | None = None):
+        self.L = library if library is not None else lib()
+
+    def num_threads(self) -> int:
+        return int(self.L.oracle_num_threads())
+
+    def route(self, logits, k):
+        logits = _c(logits, np.float32)
+        T, E = logits.shape
+        idx = np.empty((T, k), np.int32)
+        w = np.empty((T, k), np.float32)
+        rc = self.L.oracle_route(_p(logits, _F32P), T, E, k, _p(idx, _I32P), _p(w, _F32P))
+        if rc:
+            raise ValueError(f"oracle_route rejected the shape (rc={rc})")
+        return idx, w
+
+    def permute(self, idx, E):
+        idx = _c(idx, np.int32)
+        T, k = idx.shape
+        counts = np.empty(E, np.int32)
+        offsets = np.empty(E + 1, np.int32)
+        src = np.empty(T * k, np.int32)
+        dest = np.empty((T, k), np.int32)
+        rc = self.L.oracle_permute(_p(idx, _I32P), T, E, k, _p(counts, _I32P), _p(offsets, _I32P),
+                                   _p(src, _I32P), _p(dest, _I32P))
+        if rc:
+            raise ValueError(f"oracle_permute rejected its input (rc={rc})")
+        return counts, offsets, src, dest
+
+    def gather_rows(self, x_bits, src):
+        x_bits = _c(x_bits, np.uint16)
+        src = _c(src, np.int32)
+        M, d = src.shape[0], x_bits.shape[1]
+        out = np.empty((M, d), np.uint16)
+        self.L.oracle_gather_rows(_p(x_bits, _U16P), _p(src, _I32P), M, d, _p(out, _U16P))
+        return out
+
+    def gateup_swiglu(self, x_perm_bits, offsets, wgu_bits):
+        x_perm_bits = _c(x_perm_bits, np.uint16)
+        offsets = _c(offsets, np.int32)
+        wgu_bits = _c(wgu_bits, np.uint16)
+        E, d, f2 = wgu_bits.shape
+        f = f2 // 2
+        M = x_perm_bits.shape[0]
+        h = np.zeros((M, f), np.float32)
+        self.L.oracle_gateup_swiglu(_p(x_perm_bits, _U16P), _p(offsets, _I32P), E,
+                                    _p(wgu_bits, _U16P), d, f, _p(h, _F32P))
+        return h
+
+    def down(self, h, offsets, wd_bits):
+        offsets = _c(offsets, np.int32)
+        wd_bits = _c(wd_bits, np.uint16)
+        E, f, d = wd_bits.shape
+        M = h.shape[0]
+        y = np.zeros((M, d), np.float32)
+        if h.dtype == np.uint16:
+            h = _c(h, np.uint16)
+            self.L.oracle_down_bf16(_p(h, _U16P), _p(offsets, _I32P), E, _p(wd_bits, _U16P), d, f,
+                                    _p(y, _F32P))
+        else:
+            h = _c(h, np.float32)
+            self.L.oracle_down(_p(h, _F32P), _p(offsets, _I32P), E, _p(wd_bits, _U16P), d, f,
+                               _p(y, _F32P))
+        return y
+
+    def combine(self, y, w, dest):
+        y = _c(y, np.float32)
+        w = _c(w, np.float32)
+        dest = _c(dest, np.int32)
+        T, k = dest.shape
+        d = y.shape[1]
+        out = np.empty((T, d), np.float32)
+        self.L.oracle_combine(_p(y, _F32P), _p(w, _F32P), _p(dest, _I32P), T, d, k, _p(out, _F32P))
+        return out
+
+    def forward(self, x_bits, logits, wgu_bits, wd_bits, k):
+        x_bits = _c(x_bits, np.uint16)
+        logits = _c(logits, np.float32)
+        wgu_bits = _c(wgu_bits, np.uint16)
+        wd_bits = _c(wd_bits, np.uint16)
+        T, d = x_bits.shape
+        E, _, f2 = wgu_bits.shape
+        out = np.empty((T, d), np.float32)
+        rc = self.L.oracle_forward(_p(x_bits, _U16P), _p(logits, _F32P), _p(wgu_bits, _U16P),
+                                   _p(wd_bits, _U16P), T, d, f2 // 2, E, k, _p(out, _F32P))
+        if rc:
+            raise ValueError(f"oracle_forward failed (rc={rc})")
+        return out
+
+    def forward_tokens(self, x_bits, logits, wgu_bits, wd_bits, k, tokens):
+        x_bits = _c(x_bits, np.uint16)
+        logits = _c(logits, np.float32)
+        wgu_bits = _c(wgu_bits, np.uint16)
+        wd_bits = _c(wd_bits, np.uint16)
+        tokens = _c(tokens, np.int32)
+        T, d = x_bits.shape
+        E, _, f2 = wgu_bits.shape
+        out = np.empty((tokens.shape[0], d), np.float32)
+        rc = self.L.oracle_forward_tokens(_p(x_bits, _U16P), _p(logits, _F32P), _p(wgu_bits, _U16P),
+                                          _p(wd_bits, _U16P), T, d, f2 // 2, E, k,
+                                          _p(tokens, _I32P), tokens.shape[0], _p(out, _F32P))
+        if rc:
+            raise ValueError(f"oracle_forward_tokens failed (rc={rc})")
+        return out
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to float32 (exact)."""
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)

@@ -1,0 +1,289 @@
+// moe_oracle.cpp — plain, slow, CPU reference of one Mixture-of-Experts FFN layer forward.
+//
+// TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline
+// and reference legs may load this library.  The product path (libmoe.so) never calls it, and
+// this file shares no code, header, table or helper with the CUDA library.
+//
+// What the layer computes (the plain definition, step by step):
+//   1. route    top-k experts per token from fp32 router logits; weights = softmax over all
+//               experts, restricted to the chosen k and renormalised to sum to 1.
+//   2. permute  group the (token, slot) assignments by expert (counting sort: expert, then
+//               ascending token), giving counts, offsets, src (row -> token), dest (token,slot -> row).
+//   3. gate+up  for every permuted row: g = x.W_gate[e], u = x.W_up[e] (fp32 accumulate),
+//               h = silu(g) * u, silu(z) = z / (1 + exp(-z)).  h stays fp32 here.
+//   4. down     y = h.W_down[e] (fp32 accumulate).
+//   5. combine  out[t] = sum_j w[t,j] * y[dest[t,j]], j in slot order, fp32.
+//
+// Sources:
+//   * Stage order dispatch -> linear1 -> SwiGLU -> linear2 -> combine: DeepGEMM PR #304 write-up
+//     (itsolotime.com), section 1.1 "the core of the problem: the NVLink bottleneck in MoE inference".
+//   * SwiGLU between a fused gate/up projection and the down projection, with the gate/up
+//     pre-activations kept out of global memory: "Triton-MoE-Dispatch-Kernel erreicht 131 % von
+//     Megablocks" (lumeric.app), the article body.
+//   * Rearrange -> GroupGEMM -> weighted-average reduce: the HPC-Ops operator-library page
+//     (ntfzh.com), its FusedMoE paragraph.
+//   * Top-k routing done on the device inside the MoE kernel: "Triton MoE 核心擊敗 Megablocks"
+//     (setupai.cc), section 技術深入 (technical deep dive), the dynamic-routing bullet.
+//   The pages never define the router function.  Reading adopted here for every workload:
+//   softmax over all E logits, keep the k largest logits (ties -> lower expert index; the slot
+//   order is descending logit), renormalise the kept probabilities to sum to 1.
+//
+// Precision: every floating-point step is fp32 from the same bf16 inputs (bf16 -> fp32 is exact).
+// The layer's definition fixes fp32 accumulation; this file is built with -ffp-contract=off so the
+// x86 and Arm builds round identically.
+//
+// Parity pins: every function below is pinned by CPU tests that do not reuse this code
+// (tests/test_oracle_pins.py): a hand-worked 4-token example with closed-form outputs, the
+// E=1/k=1 dense SwiGLU FFN against numpy matmul, a float64 brute-force per-token dense FFN,
+// numpy stable argsort for routing and the permutation, and the layer's invariants.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <numeric>
+#include <vector>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+// bf16 is the upper half of an IEEE fp32 word, so widening is a 16-bit shift (exact).
+inline float bf16_to_f32(uint16_t b) {
+    uint32_t u = static_cast<uint32_t>(b) << 16;
+    float f;
+    std::memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+inline float silu(float z) { return z / (1.0f + std::exp(-z)); }
+
+// One permuted row through expert e: g, u over i = 0..d-1 ascending; h = silu(g) * u.
+void gateup_row(const float* x, const uint16_t* Wgu_e, int d, int f, float* h, float* g, float* u) {
+    for (int n = 0; n < f; ++n) { g[n] = 0.0f; u[n] = 0.0f; }
+    for (int i = 0; i < d; ++i) {
+        const float xi = x[i];
+        const uint16_t* wrow = Wgu_e + static_cast<size_t>(i) * 2 * f;   // row i of [d, 2f]
+        for (int n = 0; n < f; ++n) {
+            g[n] += xi * bf16_to_f32(wrow[n]);          // gate: columns 0 .. f-1
+            u[n] += xi * bf16_to_f32(wrow[f + n]);      // up:   columns f .. 2f-1
+        }
+    }
+    for (int n = 0; n < f; ++n) h[n] = silu(g[n]) * u[n];
+}
+
+// y = h . W_down[e], n = 0..f-1 ascending.
+void down_row(const float* h, const uint16_t* Wd_e, int d, int f, float* y) {
+    for (int m = 0; m < d; ++m) y[m] = 0.0f;
+    for (int n = 0; n < f; ++n) {
+        const float hn = h[n];
+        const uint16_t* wrow = Wd_e + static_cast<size_t>(n) * d;       // row n of [f, d]
+        for (int m = 0; m < d; ++m) y[m] += hn * bf16_to_f32(wrow[m]);
+    }
+}
+
+bool valid_shape(int T, int E, int k) { return T >= 0 && E >= 1 && k >= 1 && k <= E; }
+
+}  // namespace
+
+extern "C" {
+
+// Threads OpenMP will use in the parallel loops below.
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+// Step 1, route.  logits [T,E] fp32 row-major -> idx [T,k] int32, w [T,k] fp32.
+// Returns 0, or -1 on a bad shape.
+int oracle_route(const float* logits, int T, int E, int k, int32_t* idx, float* w) {
+    if (!valid_shape(T, E, k)) return -1;
+    std::vector<int> order(E);
+    std::vector<float> p(E);
+    for (int t = 0; t < T; ++t) {
+        const float* l = logits + static_cast<size_t>(t) * E;
+        // Sort expert ids by logit, largest first; stable, so equal logits keep ascending id.
+        std::iota(order.begin(), order.end(), 0);
+        std::stable_sort(order.begin(), order.end(), [l](int a, int b) { return l[a] > l[b]; });
+        // Full softmax over all E experts.
+        float mx = l[0];
+        for (int e = 1; e < E; ++e) mx = std::max(mx, l[e]);
+        float Z = 0.0f;
+        for (int e = 0; e < E; ++e) { p[e] = std::exp(l[e] - mx); Z += p[e]; }
+        for (int e = 0; e < E; ++e) p[e] /= Z;
+        // Keep the first k in slot order, renormalise.
+        float s = 0.0f;
+        for (int j = 0; j < k; ++j) s += p[order[j]];
+        for (int j = 0; j < k; ++j) {
+            idx[static_cast<size_t>(t) * k + j] = order[j];
+            w[static_cast<size_t>(t) * k + j] = p[order[j]] / s;
+        }
+    }
+    return 0;
+}
+
+// Step 2, permute: counting sort of the T*k assignments by expert, tokens ascending within an
+// expert.  counts [E], offsets [E+1] (exclusive scan), src [T*k] (row -> token),
+// dest [T,k] ((token, slot) -> row).  Returns 0, -1 on a bad shape, -2 if idx holds an id
+// outside [0,E) or repeats an expert within one token.
+int oracle_permute(const int32_t* idx, int T, int E, int k,
+                   int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest) {
+    if (!valid_shape(T, E, k)) return -1;
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            const int e = idx[static_cast<size_t>(t) * k + j];
+            if (e < 0 || e >= E) return -2;
+            for (int jj = 0; jj < j; ++jj)
+                if (idx[static_cast<size_t>(t) * k + jj] == e) return -2;
+        }
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (size_t a = 0; a < static_cast<size_t>(T) * k; ++a) counts[idx[a]] += 1;
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    std::vector<int32_t> cursor(offsets, offsets + E);
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            const int e = idx[static_cast<size_t>(t) * k + j];
+            const int r = cursor[e]++;
+            src[r] = t;
+            dest[static_cast<size_t>(t) * k + j] = r;
+        }
+    return 0;
+}
+
+// x_perm[r] = x[src[r]] for r < M (a bf16 row copy).
+void oracle_gather_rows(const uint16_t* x, const int32_t* src, int M, int d, uint16_t* x_perm) {
+    for (int r = 0; r < M; ++r)
+        std::memcpy(x_perm + static_cast<size_t>(r) * d, x + static_cast<size_t>(src[r]) * d,
+                    sizeof(uint16_t) * d);
+}
+
+// Step 3, gate+up with SwiGLU over the permuted rows 0..offsets[E]-1 of x_perm [M,d] bf16.
+// W_gate_up [E, d, 2f] bf16 (gate columns 0..f-1, up columns f..2f-1) -> h [M, f] fp32.
+void oracle_gateup_swiglu(const uint16_t* x_perm, const int32_t* offsets, int E,
+                          const uint16_t* Wgu, int d, int f, float* h) {
+    for (int e = 0; e < E; ++e) {
+        const uint16_t* We = Wgu + static_cast<size_t>(e) * d * 2 * f;
+#pragma omp parallel
+        {
+            std::vector<float> x(d), g(f), u(f);
+#pragma omp for schedule(dynamic, 1)
+            for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
+                for (int i = 0; i < d; ++i) x[i] = bf16_to_f32(x_perm[static_cast<size_t>(r) * d + i]);
+                gateup_row(x.data(), We, d, f, h + static_cast<size_t>(r) * f, g.data(), u.data());
+            }
+        }
+    }
+}
+
+// Step 4, down projection over rows 0..offsets[E]-1: y [M, d] = h [M, f] . W_down[e] [f, d].
+void oracle_down(const float* h, const int32_t* offsets, int E, const uint16_t* Wd, int d, int f,
+                 float* y) {
+    for (int e = 0; e < E; ++e) {
+        const uint16_t* We = Wd + static_cast<size_t>(e) * f * d;
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int r = offsets[e]; r < offsets[e + 1]; ++r)
+            down_row(h + static_cast<size_t>(r) * f, We, d, f, y + static_cast<size_t>(r) * d);
+    }
+}
+
+// Step 4 with a bf16 h operand (for checking the down-projection stage on its own).
+void oracle_down_bf16(const uint16_t* h_bf16, const int32_t* offsets, int E, const uint16_t* Wd,
+                      int d, int f, float* y) {
+    for (int e = 0; e < E; ++e) {
+        const uint16_t* We = Wd + static_cast<size_t>(e) * f * d;
+#pragma omp parallel
+        {
+            std::vector<float> h(f);
+#pragma omp for schedule(dynamic, 1)
+            for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
+                for (int n = 0; n < f; ++n) h[n] = bf16_to_f32(h_bf16[static_cast<size_t>(r) * f + n]);
+                down_row(h.data(), We, d, f, y + static_cast<size_t>(r) * d);
+            }
+        }
+    }
+}
+
+// Step 5, combine: out[t] = sum over slots j = 0..k-1 (ascending) of w[t,j] * y[dest[t,j]].
+void oracle_combine(const float* y, const float* w, const int32_t* dest, int T, int d, int k,
+                    float* out) {
+#pragma omp parallel for
+    for (int t = 0; t < T; ++t) {
+        float* o = out + static_cast<size_t>(t) * d;
+        for (int m = 0; m < d; ++m) o[m] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const float wj = w[static_cast<size_t>(t) * k + j];
+            const float* yr = y + static_cast<size_t>(dest[static_cast<size_t>(t) * k + j]) * d;
+            for (int m = 0; m < d; ++m) o[m] += wj * yr[m];
+        }
+    }
+}
+
+// The whole layer: steps 1-5 in order.  x [T,d] bf16, logits [T,E] fp32, W_gate_up [E,d,2f] bf16,
+// W_down [E,f,d] bf16 -> out [T,d] fp32.  Returns 0 or a negative code from route/permute.
+int oracle_forward(const uint16_t* x, const float* logits, const uint16_t* Wgu, const uint16_t* Wd,
+                   int T, int d, int f, int E, int k, float* out) {
+    if (!valid_shape(T, E, k) || d < 1 || f < 1) return -1;
+    const size_t M = static_cast<size_t>(T) * k;
+    std::vector<int32_t> idx(M), counts(E), offsets(E + 1), src(M), dest(M);
+    std::vector<float> w(M);
+    int rc = oracle_route(logits, T, E, k, idx.data(), w.data());
+    if (rc) return rc;
+    rc = oracle_permute(idx.data(), T, E, k, counts.data(), offsets.data(), src.data(), dest.data());
+    if (rc) return rc;
+    std::vector<uint16_t> x_perm(M * d);
+    oracle_gather_rows(x, src.data(), static_cast<int>(M), d, x_perm.data());
+    std::vector<float> h(M * f), y(M * d);
+    oracle_gateup_swiglu(x_perm.data(), offsets.data(), E, Wgu, d, f, h.data());
+    oracle_down(h.data(), offsets.data(), E, Wd, d, f, y.data());
+    oracle_combine(y.data(), w.data(), dest.data(), T, d, k, out);
+    return 0;
+}
+
+// The layer's output for a chosen subset of tokens only (out_rows [ntok, d] fp32).  Every token's
+// output depends only on its own logits and x row, so this is the same definition restricted to
+// those tokens: route the token, run each chosen expert's FFN on its x row, combine in slot order.
+// Used to check full-size workloads on sampled tokens.  Returns 0 or a negative code.
+int oracle_forward_tokens(const uint16_t* x, const float* logits, const uint16_t* Wgu,
+                          const uint16_t* Wd, int T, int d, int f, int E, int k,
+                          const int32_t* tokens, int ntok, float* out_rows) {
+    if (!valid_shape(T, E, k) || d < 1 || f < 1) return -1;
+    for (int s = 0; s < ntok; ++s)
+        if (tokens[s] < 0 || tokens[s] >= T) return -1;
+    const size_t npairs = static_cast<size_t>(ntok) * k;
+    std::vector<int32_t> idx(npairs);
+    std::vector<float> w(npairs), ys(npairs * d);
+    for (int s = 0; s < ntok; ++s)
+        oracle_route(logits + static_cast<size_t>(tokens[s]) * E, 1, E, k, idx.data() + s * k,
+                     w.data() + s * k);
+#pragma omp parallel
+    {
+        std::vector<float> xr(d), g(f), u(f), h(f);
+#pragma omp for schedule(dynamic, 1)
+        for (long long q = 0; q < static_cast<long long>(npairs); ++q) {
+            const int s = static_cast<int>(q / k);
+            const int e = idx[q];
+            const uint16_t* xt = x + static_cast<size_t>(tokens[s]) * d;
+            for (int i = 0; i < d; ++i) xr[i] = bf16_to_f32(xt[i]);
+            gateup_row(xr.data(), Wgu + static_cast<size_t>(e) * d * 2 * f, d, f, h.data(), g.data(),
+                       u.data());
+            down_row(h.data(), Wd + static_cast<size_t>(e) * f * d, d, f, ys.data() + q * d);
+        }
+    }
+    for (int s = 0; s < ntok; ++s) {
+        float* o = out_rows + static_cast<size_t>(s) * d;
+        for (int m = 0; m < d; ++m) o[m] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const float wj = w[static_cast<size_t>(s) * k + j];
+            const float* yr = ys.data() + (static_cast<size_t>(s) * k + j) * d;
+            for (int m = 0; m < d; ++m) o[m] += wj * yr[m];
+        }
+    }
+    return 0;
+}
+
+}  // extern "C"

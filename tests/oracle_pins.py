@@ -1,0 +1,274 @@
+"""Pins for the CPU oracle: checks against facts that do not come from the oracle itself.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises ``AssertionError`` when the oracle disagrees
+with a closed form, a hand-worked example, a library routine (numpy / scipy) or a float64
+brute force written here from the layer's definition.  ``test_oracle_pins.py`` runs them on the
+real oracle; ``test_oracle_mutants.py`` runs them on deliberately broken copies of the oracle
+and expects each copy to fail at least one pin.
+
+The layer (per token t, chosen experts e_j, weights w_j):
+    out[t] = sum_j w_j * ( silu(x W_gate[e_j]) * (x W_up[e_j]) ) W_down[e_j]
+with W_gate_up[e] = [W_gate[e] | W_up[e]] ([d, 2f]) and silu(z) = z * sigmoid(z).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+from scipy.special import expit, softmax
+
+from oracle import bf16_bits_to_f32
+
+
+def sigma(z: float) -> float:
+    return 1.0 / (1.0 + math.exp(-z))
+
+
+def f32_to_bf16_bits(a) -> np.ndarray:
+    """Round float32 values to bf16 (round to nearest even) and return the bit patterns."""
+    u = np.ascontiguousarray(a, np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+# --------------------------------------------------------------------------------------------
+# Hand-worked example: E = 3 experts, top-2, d = f = 2, T = 4 tokens.
+#   W_gate[e] = a_e * I with a = (1, 2, 0.5);  W_up[e] = I;  W_down[e] = c_e * I with c = (1, 0.5, -1)
+#   so expert e maps x to y_i = c_e * silu(a_e x_i) * x_i = c_e * a_e * x_i^2 * sigma(a_e x_i).
+#   Per expert: e0: y_i = x_i^2 sigma(x_i);  e1: y_i = x_i^2 sigma(2 x_i);  e2: y_i = -x_i^2 sigma(x_i/2) / 2.
+# Tokens (x; logits) and the hand derivation:
+#   t0 x=[1,-1];  logits [0,0,0]: three-way tie -> lowest ids first: idx [0,1], w [1/2, 1/2].
+#       e0 -> [s(1), s(-1)], e1 -> [s(2), s(-2)]  => out = [(s1+s2)/2, (s(-1)+s(-2))/2]
+#   t1 x=[2,0];   logits [1,0,2]: order e2 (2) > e0 (1) > e1 (0): idx [2,0];
+#       w = softmax over {2,1} = [s(1), s(-1)].  e2 -> [-2 s(1), 0], e0 -> [4 s(2), 0]
+#       => out = [-2 s(1)^2 + 4 s(-1) s(2), 0]
+#   t2 x=[1,2];   logits [0,1,1]: tie for first between e1, e2 -> idx [1,2], w [1/2,1/2].
+#       e1 -> [s(2), 4 s(4)], e2 -> [-s(1/2)/2, -2 s(1)]  => out = [(s2 - s(1/2)/2)/2, 2 s(4) - s(1)]
+#   t3 x=[-2,1];  logits [3,1,1]: e0 first, tie e1/e2 for second -> idx [0,1];
+#       w = softmax over {3,1} = [s(2), s(-2)].  e0 -> [4 s(-2), s(1)], e1 -> [4 s(-4), s(2)]
+#       => out = [4 s(2) s(-2) + 4 s(-2) s(-4), s(2) s(1) + s(-2) s(2)]
+#   Counting sort by expert then token: e0 <- t0,t1,t3 (rows 0,1,2); e1 <- t0,t2,t3 (rows 3,4,5);
+#   e2 <- t1,t2 (rows 6,7).  counts [3,3,2], offsets [0,3,6,8], src [0,1,3,0,2,3,1,2],
+#   dest [[0,3],[6,1],[4,7],[2,5]].
+# Every weight and x value is exactly representable in bf16.
+# --------------------------------------------------------------------------------------------
+HAND_X = np.array([[1, -1], [2, 0], [1, 2], [-2, 1]], np.float32)
+HAND_LOGITS = np.array([[0, 0, 0], [1, 0, 2], [0, 1, 1], [3, 1, 1]], np.float32)
+HAND_A = (1.0, 2.0, 0.5)
+HAND_C = (1.0, 0.5, -1.0)
+
+
+def hand_weights():
+    E, d, f = 3, 2, 2
+    wgu = np.zeros((E, d, 2 * f), np.float32)
+    wd = np.zeros((E, f, d), np.float32)
+    for e in range(E):
+        wgu[e, :, :f] = HAND_A[e] * np.eye(2)
+        wgu[e, :, f:] = np.eye(2)
+        wd[e] = HAND_C[e] * np.eye(2)
+    return f32_to_bf16_bits(wgu), f32_to_bf16_bits(wd)
+
+
+def hand_expected():
+    s = sigma
+    idx = np.array([[0, 1], [2, 0], [1, 2], [0, 1]], np.int32)
+    w = np.array([[0.5, 0.5], [s(1), s(-1)], [0.5, 0.5], [s(2), s(-2)]])
+    out = np.array([
+        [(s(1) + s(2)) / 2, (s(-1) + s(-2)) / 2],
+        [-2 * s(1) ** 2 + 4 * s(-1) * s(2), 0.0],
+        [(s(2) - s(0.5) / 2) / 2, 2 * s(4) - s(1)],
+        [4 * s(2) * s(-2) + 4 * s(-2) * s(-4), s(2) * s(1) + s(-2) * s(2)],
+    ])
+    counts = np.array([3, 3, 2], np.int32)
+    offsets = np.array([0, 3, 6, 8], np.int32)
+    src = np.array([0, 1, 3, 0, 2, 3, 1, 2], np.int32)
+    dest = np.array([[0, 3], [6, 1], [4, 7], [2, 5]], np.int32)
+    return idx, w, out, counts, offsets, src, dest
+
+
+def pin_hand_example(O):
+    idx_e, w_e, out_e, counts_e, offsets_e, src_e, dest_e = hand_expected()
+    x_bits = f32_to_bf16_bits(HAND_X)
+    wgu, wd = hand_weights()
+    idx, w = O.route(HAND_LOGITS, 2)
+    assert np.array_equal(idx, idx_e), (idx, idx_e)
+    np.testing.assert_allclose(w, w_e, rtol=1e-6, atol=0)
+    counts, offsets, src, dest = O.permute(idx, 3)
+    assert np.array_equal(counts, counts_e)
+    assert np.array_equal(offsets, offsets_e)
+    assert np.array_equal(src, src_e)
+    assert np.array_equal(dest, dest_e)
+    out = O.forward(x_bits, HAND_LOGITS, wgu, wd, 2)
+    np.testing.assert_allclose(out, out_e, rtol=1e-6, atol=1e-7)
+    out_rows = O.forward_tokens(x_bits, HAND_LOGITS, wgu, wd, 2, np.array([3, 0], np.int32))
+    np.testing.assert_allclose(out_rows, out_e[[3, 0]], rtol=1e-6, atol=1e-7)
+
+
+# --------------------------------------------------------------------------------------------
+# Random small layers and a float64 brute force written from the definition: per token, pick the
+# k largest logits (stable, lower id first on ties), softmax-renormalise, run each chosen
+# expert's dense SwiGLU FFN in float64 with numpy matmuls, and sum.  No permutation.
+# --------------------------------------------------------------------------------------------
+def random_layer(rng, T, d, f, E, tie_logits=False):
+    if tie_logits:
+        logits = rng.integers(0, 3, size=(T, E)).astype(np.float32)
+    else:
+        logits = rng.standard_normal((T, E)).astype(np.float32)
+    x_bits = f32_to_bf16_bits(rng.standard_normal((T, d)).astype(np.float32))
+    wgu_bits = f32_to_bf16_bits((0.3 * rng.standard_normal((E, d, 2 * f))).astype(np.float32))
+    wd_bits = f32_to_bf16_bits((0.3 * rng.standard_normal((E, f, d))).astype(np.float32))
+    return logits, x_bits, wgu_bits, wd_bits
+
+
+def brute_force_forward(logits, x_bits, wgu_bits, wd_bits, k):
+    T, E = logits.shape
+    f = wgu_bits.shape[2] // 2
+    x = bf16_bits_to_f32(x_bits).astype(np.float64)
+    wgu = bf16_bits_to_f32(wgu_bits).astype(np.float64)
+    wd = bf16_bits_to_f32(wd_bits).astype(np.float64)
+    out = np.zeros((T, x.shape[1]))
+    for t in range(T):
+        chosen = np.argsort(-logits[t].astype(np.float64), kind="stable")[:k]
+        p = softmax(logits[t].astype(np.float64))
+        wts = p[chosen] / p[chosen].sum()
+        for e, wt in zip(chosen, wts):
+            g = x[t] @ wgu[e][:, :f]
+            u = x[t] @ wgu[e][:, f:]
+            out[t] += wt * ((g * expit(g) * u) @ wd[e])
+    return out
+
+
+BRUTE_SHAPES = [  # (T, d, f, E, k, tie_logits)
+    (16, 32, 24, 6, 2, False),
+    (9, 16, 32, 5, 3, True),
+    (12, 8, 8, 4, 4, False),
+    (7, 24, 16, 6, 1, True),
+    (1, 32, 32, 3, 2, False),
+]
+
+
+def pin_brute_force(O, seed=1234):
+    rng = np.random.default_rng(seed)
+    for T, d, f, E, k, ties in BRUTE_SHAPES:
+        logits, x_bits, wgu, wd = random_layer(rng, T, d, f, E, ties)
+        ref = brute_force_forward(logits, x_bits, wgu, wd, k)
+        out = O.forward(x_bits, logits, wgu, wd, k)
+        err = np.abs(out - ref).max()
+        assert err <= 1e-5 * max(1.0, np.abs(ref).max()), (T, d, f, E, k, err)
+        tok = np.arange(T - 1, -1, -2, dtype=np.int32)
+        rows = O.forward_tokens(x_bits, logits, wgu, wd, k, tok)
+        err = np.abs(rows - ref[tok]).max()
+        assert err <= 1e-5 * max(1.0, np.abs(ref).max()), ("tokens", T, d, f, E, k, err)
+
+
+def pin_dense_e1_k1(O, seed=7):
+    """E = 1, k = 1: the layer is the dense SwiGLU FFN silu(x Wg) * (x Wu) @ Wd (numpy matmul)."""
+    rng = np.random.default_rng(seed)
+    T, d, f = 10, 48, 40
+    logits, x_bits, wgu_bits, wd_bits = random_layer(rng, T, d, f, 1)
+    x = bf16_bits_to_f32(x_bits).astype(np.float64)
+    wg = bf16_bits_to_f32(wgu_bits[0, :, :f]).astype(np.float64)
+    wu = bf16_bits_to_f32(wgu_bits[0, :, f:]).astype(np.float64)
+    wd = bf16_bits_to_f32(wd_bits[0]).astype(np.float64)
+    g = x @ wg
+    ref = (g * expit(g) * (x @ wu)) @ wd
+    out = O.forward(x_bits, logits, wgu_bits, wd_bits, 1)
+    assert np.abs(out - ref).max() <= 1e-5 * np.abs(ref).max()
+    _, w = O.route(logits, 1)
+    assert np.all(w == 1.0)
+
+
+def pin_route_library(O, seed=11):
+    """Top-k ids equal numpy's stable argsort of -logits; weights equal scipy's softmax renormalised."""
+    rng = np.random.default_rng(seed)
+    for T, E, k, ties in [(64, 8, 2, False), (50, 7, 3, True), (33, 40, 8, False), (20, 256, 8, True),
+                          (5, 5, 5, False), (17, 6, 6, True)]:
+        logits = (rng.integers(0, 4, (T, E)) if ties else rng.standard_normal((T, E))).astype(np.float32)
+        idx, w = O.route(logits, k)
+        ref_idx = np.argsort(-logits.astype(np.float64), axis=1, kind="stable")[:, :k]
+        assert np.array_equal(idx, ref_idx), (T, E, k)
+        p = softmax(logits.astype(np.float64), axis=1)
+        pk = np.take_along_axis(p, ref_idx, axis=1)
+        np.testing.assert_allclose(w, pk / pk.sum(axis=1, keepdims=True), rtol=1e-6, atol=0)
+        np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-6)
+        if k == E:  # all experts kept: the weights are the full softmax
+            np.testing.assert_allclose(np.take_along_axis(w, np.argsort(idx, axis=1), 1), p,
+                                       rtol=1e-6, atol=0)
+
+
+def pin_permute_library(O, seed=5):
+    """The permutation equals numpy's stable argsort of the flattened expert ids."""
+    rng = np.random.default_rng(seed)
+    for T, E, k in [(40, 8, 2), (31, 16, 4), (1, 3, 3), (64, 256, 8), (25, 1, 1)]:
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        counts, offsets, src, dest = O.permute(idx, E)
+        flat = idx.reshape(-1)
+        order = np.argsort(flat, kind="stable")
+        assert np.array_equal(counts, np.bincount(flat, minlength=E))
+        assert np.array_equal(offsets, np.concatenate([[0], np.cumsum(counts)]))
+        assert np.array_equal(src, order // k)
+        ref_dest = np.empty(T * k, np.int64)
+        ref_dest[order] = np.arange(T * k)
+        assert np.array_equal(dest.reshape(-1), ref_dest)
+
+
+def pin_invariants(O, seed=3):
+    """Layer invariants on a random layer: counts sum to T*k, src/dest are inverse bijections,
+    each row lies in its expert's segment, tokens ascend within a segment, weights sum to 1."""
+    rng = np.random.default_rng(seed)
+    T, E, k = 57, 9, 3
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    idx, w = O.route(logits, k)
+    assert all(len(set(r)) == k for r in idx.tolist())
+    assert np.all(np.diff(np.take_along_axis(logits, idx, 1), axis=1) <= 0)
+    np.testing.assert_allclose(w.sum(1), 1.0, atol=1e-6, rtol=0)
+    counts, offsets, src, dest = O.permute(idx, E)
+    assert counts.sum() == T * k and np.all(np.diff(offsets) >= 0)
+    for t in range(T):
+        for j in range(k):
+            r = dest[t, j]
+            assert src[r] == t
+            assert offsets[idx[t, j]] <= r < offsets[idx[t, j] + 1]
+    for e in range(E):
+        seg = src[offsets[e]:offsets[e + 1]]
+        assert np.all(np.diff(seg) > 0)
+    assert np.array_equal(np.sort(dest.reshape(-1)), np.arange(T * k))
+
+
+def pin_stages(O, seed=9):
+    """The stage entry points compose to the one-call forward, and each stage matches its own
+    library-routine statement (gather = fancy indexing, down = per-row matmul in float64,
+    combine = weighted sum of gathered rows)."""
+    rng = np.random.default_rng(seed)
+    T, d, f, E, k = 13, 16, 24, 4, 2
+    logits, x_bits, wgu, wd = random_layer(rng, T, d, f, E)
+    idx, w = O.route(logits, k)
+    counts, offsets, src, dest = O.permute(idx, E)
+    xp = O.gather_rows(x_bits, src)
+    assert np.array_equal(xp, x_bits[src])
+    h = O.gateup_swiglu(xp, offsets, wgu)
+    expert_of_row = np.repeat(np.arange(E), counts)
+    xpf = bf16_bits_to_f32(xp).astype(np.float64)
+    wguf = bf16_bits_to_f32(wgu).astype(np.float64)
+    g_ref = np.stack([xpf[r] @ wguf[expert_of_row[r]][:, :f] for r in range(T * k)])
+    u_ref = np.stack([xpf[r] @ wguf[expert_of_row[r]][:, f:] for r in range(T * k)])
+    h_ref = g_ref * expit(g_ref) * u_ref
+    assert np.abs(h - h_ref).max() <= 1e-5 * np.abs(h_ref).max()
+    y = O.down(h, offsets, wd)
+    wdf = bf16_bits_to_f32(wd).astype(np.float64)
+    y_ref = np.stack([h[r].astype(np.float64) @ wdf[expert_of_row[r]] for r in range(T * k)])
+    assert np.abs(y - y_ref).max() <= 1e-5 * np.abs(y_ref).max()
+    hb = f32_to_bf16_bits(h)
+    y16 = O.down(hb, offsets, wd)
+    y16_ref = np.stack([bf16_bits_to_f32(hb[r]).astype(np.float64) @ wdf[expert_of_row[r]]
+                        for r in range(T * k)])
+    assert np.abs(y16 - y16_ref).max() <= 1e-5 * np.abs(y16_ref).max()
+    out = O.combine(y, w, dest)
+    out_ref = np.einsum("tk,tkd->td", w.astype(np.float64), y.astype(np.float64)[dest])
+    assert np.abs(out - out_ref).max() <= 1e-6 * np.abs(out_ref).max()
+    full = O.forward(x_bits, logits, wgu, wd, k)
+    assert np.array_equal(full, out)
+
+
+ALL_PINS = [pin_hand_example, pin_brute_force, pin_dense_e1_k1, pin_route_library,
+            pin_permute_library, pin_invariants, pin_stages]
