@@ -1,0 +1,426 @@
+"""Benchmark of the MoE layer forward on GB300: prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole layer (route -> permute -> gate+up/SwiGLU GEMM -> down GEMM ->
+combine) over one batch of seeded synthetic input.  Default workload: the Mixtral-8x7B-shaped
+decode-like batch (T=32, d=4096, f=14336, E=8, top-2).
+
+ours (default):
+  value        tokens/s with inputs resident in HBM: K steps of moe_forward, CUDA events around each
+               step on its stream, L2 flushed (512 MB write) between steps outside the events.
+  roofline     the dominant kernel: its algorithmic bytes (or FLOPs) per launch / its mean duration,
+               from a second K-step loop that calls the five stage entry points with events between
+               them (the same kernels moe_forward launches).
+  e2e          tokens/s through moe_forward_host: x and logits copied from page-locked host memory,
+               the layer, out copied back — all inside the timed region.
+  cpu_baseline the CPU oracle on a bounded sample of the same workload (rank 0, N=1 only).
+reference:
+  the CPU oracle as the reference arm: each step is the oracle's forward on a bounded token
+  sample of the same workload, timed on the host cores.
+Under torchrun (N > 1) each rank runs an independent replica of the layer on its own GPU (the
+layer has no cross-rank exchange); value = tokens of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_grouped_fp32_gb300.workloads import WORKLOADS, Workload, bf16_bits, make_inputs  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and TFLOP/s, % of roofline (1×GB300), T=32..4096"
+DEFAULT_WORKLOAD = "mixtral_t32"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ("route", "permute", "gateup_swiglu", "down", "combine")
+KERNEL_NAMES = {"route": "route_kernel", "permute": "permute_kernel",
+                "gateup_swiglu": "grouped_gemm_kernel<0>", "down": "grouped_gemm_kernel<1>",
+                "combine": "combine_kernel"}
+
+# DRAM traffic (read + write bytes per launch) from ncu captures, keyed by (workload, stage), valid
+# only while the kernel source hashes to the recorded value; see profiles/.
+MEASURED_TRAFFIC: dict = {}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------------------------
+# Algorithmic work per stage (what the layer must move / compute, not what the kernels happen to)
+# ----------------------------------------------------------------------------------------------
+def stage_work(w: Workload, n_active: int) -> dict:
+    T, d, f, E, k = w.T, w.d, w.f, w.E, w.k
+    M = T * k
+    return {
+        "route": {"bytes": T * E * 4 + M * 8, "flops": 0},
+        "permute": {"bytes": M * 4 + T * d * 2 + M * d * 2 + (E + E + 1 + 2 * M) * 4, "flops": 0},
+        "gateup_swiglu": {"bytes": n_active * d * 2 * f * 2 + M * d * 2 + M * f * 2, "flops": 4 * M * d * f},
+        "down": {"bytes": n_active * f * d * 2 + M * f * 2 + M * d * 4, "flops": 2 * M * d * f},
+        "combine": {"bytes": M * d * 4 + M * 8 + T * d * 2, "flops": 2 * M * d},
+    }
+
+
+def layer_work(w: Workload, n_active: int) -> dict:
+    return {"bytes": n_active * 3 * w.d * w.f * 2 + w.T * w.d * 2 + w.T * w.E * 4 + w.T * w.d * 2,
+            "flops": 6 * w.T * w.k * w.d * w.f}
+
+
+# ----------------------------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ----------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5:
+            time.sleep(0.01)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        t0, t1 = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (0, 1e30)
+        rows = [ln for (t, ln) in self.lines if t0 - 0.05 <= t <= t1 + 0.05] or [ln for _, ln in self.lines[-3:]]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------------
+# Our arm
+# ----------------------------------------------------------------------------------------------
+def run_ours(args, w: Workload, rank: int, world: int, dist):
+    from mixture_experts_grouped_fp32_gb300 import moe
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    moe.load()
+
+    logits, x, wgu, wd = make_inputs(w, seed=args.seed + rank, weight_device=str(dev))
+    x_d, l_d = x.to(dev), logits.to(dev)
+    ws = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k) + moe.host_staging_size(w.T, w.d, w.E),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty(w.T, w.d, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        moe.forward(x_d, l_d, wgu, wd, w.k, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if moe.get_device_error(ws) != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    v = moe.workspace_views(ws, w.T, w.d, w.f, w.E, w.k)
+    counts = v["counts"].cpu().numpy()
+    n_active = int((counts > 0).sum())
+
+    # ---- timed region: K steps of moe_forward --------------------------------------------------
+    sampler = ClockSampler(local) if rank == 0 or world > 1 else None
+    if sampler:
+        sampler.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    if sampler:
+        sampler.mark()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = statistics.mean(step_ms)
+    ms_max = ms
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    clocks = sampler.stop() if sampler else None
+
+    # ---- per-stage timing: the five stage entry points, events between launches ---------------
+    idx, wts = v["idx"], v["w"]
+    counts_d, offs, src, dest, xp, h, y = (v["counts"], v["offsets"], v["src"], v["dest"], v["x_perm"],
+                                          v["h"], v["y_perm"])
+    st = v["status"]
+    calls = [
+        lambda: moe.route(l_d, w.k, idx=idx, w=wts),
+        lambda: moe.permute(idx, x_d, w.E, status=st, out=(counts_d, offs, src, dest, xp)),
+        lambda: moe.grouped_gemm_gateup_swiglu(xp, wgu, offs, h=h, status=st),
+        lambda: moe.grouped_gemm_down(h, wd, offs, y_perm=y, status=st),
+        lambda: moe.combine(y, wts, dest, out=out, status=st),
+    ]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        sev[i][0].record(stream)
+        for j, c in enumerate(calls):
+            c()
+            sev[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    stage_ms = {name: statistics.mean(sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(args.steps))
+                for j, name in enumerate(STAGES)}
+    staged_step_ms = statistics.mean(sev[i][0].elapsed_time(sev[i][5]) for i in range(args.steps))
+
+    # ---- e2e through moe_forward_host ---------------------------------------------------------
+    xh, lh = x.pin_memory(), logits.pin_memory()
+    oh = torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory()
+    for _ in range(max(1, args.warmup)):
+        moe.forward_host(xh, lh, wgu, wd, w.k, oh, ws)
+    torch.cuda.synchronize(dev)
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        eev[i][0].record(stream)
+        moe.forward_host(xh, lh, wgu, wd, w.k, oh, ws)
+        eev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
+    if moe.get_device_error(ws) != 0:
+        raise RuntimeError("device status word set during the timed region")
+
+    peaks, peak_src = load_peaks()
+    sw = stage_work(w, n_active)
+    lw = layer_work(w, n_active)
+    dom = max(("gateup_swiglu", "down"), key=lambda n: stage_ms[n])
+    dom_ms = stage_ms[dom]
+    t_mem = sw[dom]["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_cmp = sw[dom]["flops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_cmp > t_mem:
+        achieved = sw[dom]["flops"] / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        achieved = sw[dom]["bytes"] / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = MEASURED_TRAFFIC.get((w.name, dom))
+    roof.update({"kernel": KERNEL_NAMES[dom], "peak_source": peak_src + " (burst)",
+                 "algorithmic_per_launch": sw[dom]["flops"] if roof["bound"] == "tensor" else sw[dom]["bytes"],
+                 "launch_ms": round(dom_ms, 4)})
+    layer_roof_ms = 1e3 * max(lw["bytes"] / (peaks["hbm_gbs"] * 1e9), lw["flops"] / (peaks["bf16_tflops"] * 1e12))
+
+    tokens = w.T * world
+    return {
+        "ms": ms_max, "tokens": tokens, "t_wall": t_wall, "clocks": clocks, "stage_ms": stage_ms,
+        "staged_step_ms": staged_step_ms, "e2e_ms": e2e_ms, "roofline": roof, "layer": lw,
+        "layer_roof_ms": layer_roof_ms, "n_active": n_active, "max_load": int(counts.max()),
+        "host_weights": (wgu, wd), "inputs": (logits, x), "step_ms_p10_p90": (
+            float(np.percentile(step_ms, 10)), float(np.percentile(step_ms, 90))),
+        "peak_src": peak_src, "peaks": peaks,
+    }
+
+
+# ----------------------------------------------------------------------------------------------
+# Oracle timing (CPU baseline and the reference arm)
+# ----------------------------------------------------------------------------------------------
+def oracle_sample_runner(w: Workload, logits, x, wgu, wd):
+    import oracle as oracle_pkg
+    O = oracle_pkg.Oracle()
+    xb = bf16_bits(x)
+    ln = logits.numpy()
+    wgub, wdb = bf16_bits(wgu), bf16_bits(wd)
+
+    def run(S: int) -> float:
+        t0 = time.perf_counter()
+        O.forward(xb[:S], ln[:S], wgub, wdb, w.k)
+        return time.perf_counter() - t0
+
+    return O, run
+
+
+def pick_sample(run, T: int, budget_s: float) -> int:
+    """Largest token count S <= T whose oracle forward should take about budget_s."""
+    S = min(T, 2)
+    t = max(run(S), 1e-4)
+    while S < T and t < budget_s / 4:
+        S = min(T, S * 4)
+        t = max(run(S), 1e-4)
+    S = max(1, min(T, int(S * budget_s / t)))
+    return S
+
+
+def cpu_baseline(w, logits, x, wgu, wd, budget_s: float):
+    O, run = oracle_sample_runner(w, logits, x, wgu, wd)
+    S = pick_sample(run, w.T, budget_s)
+    dt = run(S)
+    return {"value": round(S / dt, 3), "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
+            "sample": f"oracle forward (route, permute, gate+up/SwiGLU, down, combine) on the first {S} of "
+                      f"{w.T} tokens of the same seeded batch, full weights, {dt:.1f} s"}
+
+
+def run_reference(args, w: Workload, rank: int, world: int):
+    if rank != 0:
+        return None
+    logits, x, wgu, wd = make_inputs(w, seed=args.seed, weight_device="cuda" if torch.cuda.is_available() else "cpu")
+    wgu, wd = wgu.cpu(), wd.cpu()
+    O, run = oracle_sample_runner(w, logits, x, wgu, wd)
+    n = args.steps + args.warmup
+    per_step = max(0.5, min(20.0, 150.0 / max(1, n)))
+    S = pick_sample(run, w.T, per_step)
+    for _ in range(args.warmup):
+        run(S)
+    times = [run(S) for _ in range(args.steps)]
+    ms = 1e3 * statistics.mean(times)
+    value = S / (ms * 1e-3)
+    sample = (f"each step: oracle forward on the first {S} of {w.T} tokens of the seeded batch, full weights, "
+              f"{O.num_threads()} host threads")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded)", "config": config_of(w, args),
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def config_of(w: Workload, args) -> dict:
+    return {"workload": w.name, "T": w.T, "d_model": w.d, "d_ff": w.f, "experts": w.E, "top_k": w.k,
+            "logit_bias": list(w.bias), "seed": args.seed, "parallelism": "replicas",
+            "l2": "flushed between steps (512 MB write); weights of the active experts exceed L2"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0, help="oracle CPU-baseline sample size, seconds")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    w = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        line = run_reference(args, w, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    r = run_ours(args, w, rank, world, dist)
+    if rank == 0:
+        tok_s = r["tokens"] / (r["ms"] * 1e-3)
+        tflops = r["layer"]["flops"] * world / (r["ms"] * 1e-3) / 1e12
+        line = {
+            "metric": METRIC, "value": round(tok_s, 2), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"], 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded)", "config": config_of(w, args),
+            "tflops": round(tflops, 2),
+            "layer_roofline": {"ms": round(r["layer_roof_ms"], 4), "frac": round(r["layer_roof_ms"] / r["ms"], 4),
+                               "bytes": r["layer"]["bytes"], "flops": r["layer"]["flops"],
+                               "peaks": r["peak_src"]},
+            "roofline": r["roofline"],
+            "stage_ms": {k: round(v, 4) for k, v in r["stage_ms"].items()},
+            "staged_step_ms": round(r["staged_step_ms"], 4),
+            "step_ms_p10_p90": [round(v, 4) for v in r["step_ms_p10_p90"]],
+            "active_experts": r["n_active"], "max_expert_load": r["max_load"],
+            "e2e": {"value": round(w.T / (r["e2e_ms"] * 1e-3), 2), "unit": "tokens/s",
+                    "h2d_bytes_per_step": w.T * w.d * 2 + w.T * w.E * 4, "d2h_bytes_per_step": w.T * w.d * 2,
+                    "ms_per_step": round(r["e2e_ms"], 4)},
+            "gpu_launches": 5 * args.steps,
+            "clocks": r["clocks"],
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            logits, x = r["inputs"]
+            wgu, wd = (t.cpu() for t in r["host_weights"])
+            line["cpu_baseline"] = cpu_baseline(w, logits, x, wgu, wd, args.cpu_budget_s)
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,168 @@
+/* moe.h — C ABI of libmoe.so: the forward pass of one Mixture-of-Experts FFN layer on a GB300
+ * (sm_103a).
+ *
+ * The layer, in five stream-ordered steps (one kernel launch each):
+ *   route    -> top-k experts and their weights per token
+ *   permute  -> group the (token, slot) assignments by expert, copy x rows into that order
+ *   gate+up  -> grouped BF16 GEMM x_perm . [W_gate | W_up] per expert, SwiGLU fused in the
+ *               epilogue, so the gate/up pre-activations never reach global memory
+ *   down     -> grouped BF16 GEMM h . W_down per expert
+ *   combine  -> out[t] = sum_j w[t,j] * y_perm[dest[t,j]]
+ * Stage order: DeepGEMM PR #304 write-up (itsolotime.com), section 1.1 (dispatch -> linear1 ->
+ * SwiGLU -> linear2 -> combine) and the HPC-Ops page (ntfzh.com), FusedMoE paragraph
+ * (rearrange -> GroupGEMM -> weighted-average reduce).  Gate+up fusion with SwiGLU kept on chip:
+ * "Triton-MoE-Dispatch-Kernel erreicht 131 % von Megablocks" (lumeric.app), article body.
+ *
+ * Conventions for every call
+ *   - Tensors are row-major and contiguous.  "bf16" buffers hold IEEE bfloat16 values
+ *     (passed as void*); fp32 buffers are float; index buffers are int32_t.
+ *   - Unless a parameter says "host", every pointer is a DEVICE pointer (cudaMalloc, or a torch
+ *     CUDA tensor's data_ptr()) owned by the caller.  The library allocates no device memory,
+ *     never frees anything and keeps no pointer after a call returns.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls enqueue work on it
+ *     and return without synchronising, except moe_get_device_error, which reads back.
+ *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code.  On any error nothing is launched
+ *     and moe_last_error_string() (per calling thread) says why.
+ *   - Shape limits: 1 <= E <= 256, 1 <= top_k <= min(E, 8), T >= 0 (T = 0 launches nothing),
+ *     d and f multiples of 64 in [64, 65536], T * top_k < 2^31 and every buffer < 2^31 rows.
+ *   - Only devices of compute capability 10.3 (GB300) are supported: MOE_ERR_UNSUPPORTED else.
+ *   - Device-side checks (an expert id outside [0,E), offsets that are not a valid segmentation,
+ *     a dest row out of range, a pipeline wait that exceeded its time limit) never fault: the
+ *     kernel skips the offending access and ORs a MOE_STATUS_* bit into the caller's status
+ *     word, which moe_get_device_error reads.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1) /* null pointer, bad shape or limit */
+#define MOE_ERR_UNSUPPORTED (-2) /* not a compute-capability 10.3 device */
+#define MOE_ERR_WORKSPACE (-3)   /* workspace missing or smaller than moe_workspace_size() */
+#define MOE_ERR_CUDA (-4)        /* a CUDA runtime/driver call or a launch failed */
+
+/* Bits of the device status word (int32). */
+#define MOE_STATUS_BAD_EXPERT_ID 0x1 /* permute: an id outside [0,E) or repeated within a token */
+#define MOE_STATUS_BAD_OFFSETS 0x2   /* grouped GEMM: offsets not 0 <= ... nondecreasing <= M */
+#define MOE_STATUS_BAD_DEST 0x4      /* combine: a dest row outside [0, T*top_k) */
+#define MOE_STATUS_WAIT_TIMEOUT 0x8  /* grouped GEMM: a pipeline wait gave up after ~1 s */
+
+typedef void* moe_stream_t; /* a cudaStream_t */
+
+/* Bytes of scratch that moe_forward needs for this shape (256-byte aligned pieces: status word,
+ * idx, w, counts, offsets, src, dest, x_perm bf16 [T*k,d], h bf16 [T*k,f], y_perm fp32 [T*k,d]).
+ * Returns 0 for an invalid shape. */
+MOE_API size_t moe_workspace_size(int T, int d, int f, int E, int top_k);
+
+/* Byte offsets of moe_forward's intermediates inside the workspace, in this order: status, idx,
+ * w, counts, offsets, src, dest, x_perm, h, y_perm, total (11 values written to offsets_out).
+ * Lets a caller inspect the intermediates of a moe_forward call.  Returns MOE_OK or
+ * MOE_ERR_INVALID_ARG. */
+MOE_API int moe_workspace_layout(int T, int d, int f, int E, int top_k, size_t* offsets_out);
+
+/* Step 1 — top-k routing.  Per token t: the top_k largest of logits[t, 0..E-1] (equal logits:
+ * lower expert id first) in slot order of descending logit, and w[t,j] = the softmax over all E
+ * logits restricted to the chosen experts and renormalised to sum to 1, all in fp32.
+ *   logits [T,E] fp32 in;  idx [T,top_k] int32 out;  w [T,top_k] fp32 out.
+ * Routing on the device with no host synchronisation: "Triton MoE 核心擊敗 Megablocks"
+ * (setupai.cc), section 技術深入, the dynamic-routing bullet.  The pages do not define the
+ * router function; softmax-then-top-k-renormalised is the reading used throughout.
+ * Logits must be finite (NaN/inf are outside the contract). */
+MOE_API int moe_route(const float* logits, int T, int E, int top_k, int32_t* idx, float* w,
+              moe_stream_t stream);
+
+/* Step 2 — permute ("dispatch", the data rearrangement before the grouped GEMM).  Groups the
+ * T*top_k assignments by expert, tokens ascending within an expert (a stable counting sort, so
+ * the result is unique and bit-exact):
+ *   idx [T,top_k] int32 in;  x [T,d] bf16 in;
+ *   counts [E] int32 out (assignments per expert);  offsets [E+1] int32 out (exclusive scan;
+ *   expert e owns rows offsets[e] .. offsets[e+1]-1);  src [T*top_k] int32 out (row -> token);
+ *   dest [T,top_k] int32 out ((token, slot) -> row);  x_perm [T*top_k, d] bf16 out (x_perm[r] =
+ *   x[src[r]]);  status: device int32 or NULL, gets MOE_STATUS_BAD_EXPERT_ID.
+ * DeepGEMM PR #304 write-up, section 3.1 (m-grouped contiguous layout: activations contiguous by
+ * token, grouped per expert); HPC-Ops page, FusedMoE paragraph (the preceding rearrangement). */
+MOE_API int moe_permute(const int32_t* idx, const void* x, int T, int d, int E, int top_k,
+                int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest, void* x_perm,
+                int32_t* status, moe_stream_t stream);
+
+/* Step 3 — grouped gate+up GEMM with the SwiGLU epilogue.  For every expert e and row r in
+ * [offsets[e], offsets[e+1]):  g = x_perm[r] . W_gate_up[e][:, 0:f],  u = x_perm[r] .
+ * W_gate_up[e][:, f:2f] (fp32 accumulation on the tensor cores), h[r] = bf16(silu(g) * u),
+ * silu(z) = z / (1 + exp(-z)).  g and u live only in tensor memory.
+ *   x_perm [M,d] bf16 in;  w_gate_up [E,d,2f] bf16 in;  offsets [E+1] int32 in (device);
+ *   M = rows of x_perm and h;  h [M,f] bf16 out (rows past offsets[E] untouched);
+ *   status: device int32 or NULL (MOE_STATUS_BAD_OFFSETS, MOE_STATUS_WAIT_TIMEOUT).
+ * "Triton-MoE-Dispatch-Kernel erreicht 131 % von Megablocks" (lumeric.app), article body;
+ * block-scheduled grouped GEMM over variable expert batches: "Triton MoE 核心擊敗 Megablocks",
+ * section 關鍵要點; persistent kernel hiding prologue/epilogue: HPC-Ops page. */
+MOE_API int moe_grouped_gemm_gateup_swiglu(const void* x_perm, const void* w_gate_up,
+                                   const int32_t* offsets, int M, int d, int f, int E, void* h,
+                                   int32_t* status, moe_stream_t stream);
+
+/* Step 4 — grouped down-projection GEMM: y_perm[r] = h[r] . W_down[e] (fp32 accumulation) for
+ * r in expert e's segment.
+ *   h [M,f] bf16 in;  w_down [E,f,d] bf16 in;  offsets [E+1] int32 in;  y_perm [M,d] fp32 out;
+ *   status as for step 3.
+ * DeepGEMM PR #304 write-up, section 1.1 ("linear2"); HPC-Ops page (GroupGEMM). */
+MOE_API int moe_grouped_gemm_down(const void* h, const void* w_down, const int32_t* offsets, int M, int d,
+                          int f, int E, float* y_perm, int32_t* status, moe_stream_t stream);
+
+/* Step 5 — weighted combine (unpermute): out[t] = bf16( sum_{j=0..top_k-1} w[t,j] *
+ * y_perm[dest[t,j]] ), fp32 sums in slot order; no atomics, so the result is deterministic.
+ *   y_perm [T*top_k, d] fp32 in;  w [T,top_k] fp32 in;  dest [T,top_k] int32 in;
+ *   out [T,d] bf16 out;  status: device int32 or NULL (MOE_STATUS_BAD_DEST).
+ * DeepGEMM PR #304 write-up, section 1.1 ("combine"); HPC-Ops page (weighted-average reduce). */
+MOE_API int moe_combine(const float* y_perm, const float* w, const int32_t* dest, int T, int d, int top_k,
+                void* out, int32_t* status, moe_stream_t stream);
+
+/* The whole layer in one call: steps 1-5 as five kernel launches on `stream`, intermediates
+ * carved from `workspace` (device, >= moe_workspace_size() bytes, 256-byte aligned).
+ *   x [T,d] bf16;  logits [T,E] fp32;  w_gate_up [E,d,2f] bf16;  w_down [E,f,d] bf16;
+ *   out [T,d] bf16.
+ * The status word at the start of the workspace is reset by the first kernel of every call and
+ * can be read with moe_get_device_error(workspace, ...) after the stream has run the call. */
+MOE_API int moe_forward(const void* x, const float* logits, const void* w_gate_up, const void* w_down,
+                int T, int d, int f, int E, int top_k, void* out, void* workspace,
+                size_t workspace_bytes, moe_stream_t stream);
+
+/* moe_forward with the per-call tensors in HOST memory: x_host [T,d] bf16 and logits_host [T,E]
+ * fp32 are copied to the device, the layer runs, and out [T,d] bf16 is copied back to out_host,
+ * all enqueued on `stream` (cudaMemcpyAsync; page-locked host buffers make the copies
+ * asynchronous).  The caller synchronises the stream before reading out_host.  x and logits are
+ * staged in the workspace, which must hold moe_workspace_size() + moe_host_staging_size() bytes;
+ * out is staged there too.  Weights stay device pointers. */
+MOE_API size_t moe_host_staging_size(int T, int d, int E);
+MOE_API int moe_forward_host(const void* x_host, const float* logits_host, const void* w_gate_up,
+                     const void* w_down, int T, int d, int f, int E, int top_k, void* out_host,
+                     void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Reads (synchronously: cudaMemcpy) a device status word — a stage call's `status` pointer, or
+ * the workspace of moe_forward — into *code (0 = no device-side error). */
+MOE_API int moe_get_device_error(const void* status_or_workspace, int32_t* code);
+
+/* Number of kernel launches one moe_forward call makes (5). */
+MOE_API int moe_forward_launch_count(void);
+
+/* Message for the last non-OK return on the calling thread ("" if none). */
+MOE_API const char* moe_last_error_string(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+MOE_API int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,312 @@
+// moe_api.cu — the extern "C" entry points declared in include/moe.h: argument checks (before
+// any CUDA call), device checks, workspace carving and the stream-ordered launches.
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int ok() {
+    g_err[0] = '\0';
+    return MOE_OK;
+}
+
+constexpr int kMaxE = 256, kMaxK = 8, kMaxDim = 65536;
+
+bool dim_ok(int v) { return v >= 64 && v <= kMaxDim && v % 64 == 0; }
+
+int check_shape(int T, int d, int f, int E, int k, bool need_f) {
+    if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d must be >= 0", T);
+    if (E < 1 || E > kMaxE) return fail(MOE_ERR_INVALID_ARG, "E = %d outside [1, %d]", E, kMaxE);
+    if (k < 1 || k > E || k > kMaxK)
+        return fail(MOE_ERR_INVALID_ARG, "top_k = %d outside [1, min(E=%d, %d)]", k, E, kMaxK);
+    if (d != -1 && !dim_ok(d))
+        return fail(MOE_ERR_INVALID_ARG, "d = %d must be a multiple of 64 in [64, %d]", d, kMaxDim);
+    if (need_f && !dim_ok(f))
+        return fail(MOE_ERR_INVALID_ARG, "f = %d must be a multiple of 64 in [64, %d]", f, kMaxDim);
+    if (static_cast<long long>(T) * k >= (1ll << 31))
+        return fail(MOE_ERR_INVALID_ARG, "T * top_k = %lld must be < 2^31", static_cast<long long>(T) * k);
+    return MOE_OK;
+}
+
+struct DevInfo {
+    int major = 0, minor = 0, sms = 0;
+    bool init = false;
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+// Current device must be compute capability 10.3; fills the SM count.
+int check_device(int* num_sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(MOE_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DevInfo& di = g_dev[dev];
+    if (!di.init) {
+        if ((e = cudaDeviceGetAttribute(&di.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return fail(MOE_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        di.init = true;
+    }
+    if (di.major != 10 || di.minor != 3)
+        return fail(MOE_ERR_UNSUPPORTED, "device %d is sm_%d%d; libmoe is built for sm_103a only", dev,
+                    di.major, di.minor);
+    *num_sms = di.sms;
+    return MOE_OK;
+}
+
+int launched(cudaError_t e, const char* what) {
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+// moe_forward's workspace: 256-byte aligned pieces in this order.
+struct Layout {
+    size_t status, idx, w, counts, offsets, src, dest, x_perm, h, y_perm, total;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+Layout layout(int T, int d, int f, int E, int k) {
+    const size_t M = static_cast<size_t>(T) * k;
+    Layout L;
+    size_t o = 0;
+    L.status = o; o += 256;
+    L.idx = o; o = align256(o + M * 4);
+    L.w = o; o = align256(o + M * 4);
+    L.counts = o; o = align256(o + static_cast<size_t>(E) * 4);
+    L.offsets = o; o = align256(o + static_cast<size_t>(E + 1) * 4);
+    L.src = o; o = align256(o + M * 4);
+    L.dest = o; o = align256(o + M * 4);
+    L.x_perm = o; o = align256(o + M * d * 2);
+    L.h = o; o = align256(o + M * f * 2);
+    L.y_perm = o; o = align256(o + M * d * 4);
+    L.total = o;
+    return L;
+}
+
+template <class P>
+P* at(void* base, size_t off) {
+    return reinterpret_cast<P*>(static_cast<char*>(base) + off);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int run_layer(const void* x, const float* logits, const void* wgu, const void* wd, int T, int d, int f,
+              int E, int k, void* out, void* ws, int num_sms, cudaStream_t s) {
+    const Layout L = layout(T, d, f, E, k);
+    int32_t* status = at<int32_t>(ws, L.status);
+    int32_t* idx = at<int32_t>(ws, L.idx);
+    float* w = at<float>(ws, L.w);
+    int32_t* counts = at<int32_t>(ws, L.counts);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* src = at<int32_t>(ws, L.src);
+    int32_t* dest = at<int32_t>(ws, L.dest);
+    auto* x_perm = at<__nv_bfloat16>(ws, L.x_perm);
+    auto* h = at<__nv_bfloat16>(ws, L.h);
+    float* y = at<float>(ws, L.y_perm);
+    const int M = T * k;
+    cudaError_t e;
+    if ((e = launch_route(logits, T, E, k, idx, w, status, s)) != cudaSuccess) return launched(e, "route");
+    if ((e = launch_permute(idx, static_cast<const __nv_bfloat16*>(x), T, d, E, k, counts, offsets, src,
+                            dest, x_perm, status, num_sms, s)) != cudaSuccess)
+        return launched(e, "permute");
+    const char* why = "";
+    GemmArgs g1{x_perm, wgu, offsets, M, d, f, E, h, status};
+    if ((e = launch_grouped_gemm(0, g1, num_sms, s, &why)) != cudaSuccess)
+        return fail(MOE_ERR_CUDA, "gate+up GEMM: %s (%s)", why, cudaGetErrorString(e));
+    GemmArgs g2{h, wd, offsets, M, f, d, E, y, status};
+    if ((e = launch_grouped_gemm(1, g2, num_sms, s, &why)) != cudaSuccess)
+        return fail(MOE_ERR_CUDA, "down GEMM: %s (%s)", why, cudaGetErrorString(e));
+    if ((e = launch_combine(y, w, dest, T, d, k, static_cast<__nv_bfloat16*>(out), status, s)) != cudaSuccess)
+        return launched(e, "combine");
+    return ok();
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_version(void) { return 100; }
+
+int moe_forward_launch_count(void) { return 5; }
+
+const char* moe_last_error_string(void) { return g_err; }
+
+size_t moe_workspace_size(int T, int d, int f, int E, int top_k) {
+    if (check_shape(T, d, f, E, top_k, true) != MOE_OK) return 0;
+    return layout(T, d, f, E, top_k).total;
+}
+
+int moe_workspace_layout(int T, int d, int f, int E, int top_k, size_t* offsets_out) {
+    int rc = check_shape(T, d, f, E, top_k, true);
+    if (rc) return rc;
+    if (!offsets_out) return fail(MOE_ERR_INVALID_ARG, "moe_workspace_layout: null pointer");
+    const Layout L = layout(T, d, f, E, top_k);
+    const size_t v[11] = {L.status, L.idx, L.w, L.counts, L.offsets, L.src, L.dest, L.x_perm, L.h, L.y_perm, L.total};
+    for (int i = 0; i < 11; ++i) offsets_out[i] = v[i];
+    return ok();
+}
+
+size_t moe_host_staging_size(int T, int d, int E) {
+    if (T < 0 || d < 1 || E < 1) return 0;
+    return align256(static_cast<size_t>(T) * d * 2) * 2 + align256(static_cast<size_t>(T) * E * 4);
+}
+
+int moe_route(const float* logits, int T, int E, int top_k, int32_t* idx, float* w, moe_stream_t stream) {
+    int rc = check_shape(T, -1, 0, E, top_k, false);
+    if (rc) return rc;
+    if (T == 0) return ok();
+    if (!logits || !idx || !w) return fail(MOE_ERR_INVALID_ARG, "moe_route: null pointer");
+    int sms;
+    if ((rc = check_device(&sms))) return rc;
+    return launched(launch_route(logits, T, E, top_k, idx, w, nullptr, static_cast<cudaStream_t>(stream)),
+                    "route");
+}
+
+int moe_permute(const int32_t* idx, const void* x, int T, int d, int E, int top_k, int32_t* counts,
+                int32_t* offsets, int32_t* src, int32_t* dest, void* x_perm, int32_t* status,
+                moe_stream_t stream) {
+    int rc = check_shape(T, d, 0, E, top_k, false);
+    if (rc) return rc;
+    if (T == 0) return ok();
+    if (!idx || !x || !counts || !offsets || !src || !dest || !x_perm)
+        return fail(MOE_ERR_INVALID_ARG, "moe_permute: null pointer");
+    if (!aligned16(x) || !aligned16(x_perm))
+        return fail(MOE_ERR_INVALID_ARG, "moe_permute: x and x_perm must be 16-byte aligned");
+    int sms;
+    if ((rc = check_device(&sms))) return rc;
+    return launched(launch_permute(idx, static_cast<const __nv_bfloat16*>(x), T, d, E, top_k, counts,
+                                   offsets, src, dest, static_cast<__nv_bfloat16*>(x_perm), status, sms,
+                                   static_cast<cudaStream_t>(stream)),
+                    "permute");
+}
+
+static int gemm_entry(int kind, const void* A, const void* B, const int32_t* offsets, int M, int d, int f,
+                      int E, void* out, int32_t* status, moe_stream_t stream, const char* name) {
+    int rc = check_shape(0, d, f, E, 1, true);
+    if (rc) return rc;
+    if (M < 0) return fail(MOE_ERR_INVALID_ARG, "%s: M = %d must be >= 0", name, M);
+    if (M == 0) return ok();
+    if (!A || !B || !offsets || !out) return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
+    if (!aligned16(A) || !aligned16(B) || !aligned16(out))
+        return fail(MOE_ERR_INVALID_ARG, "%s: operands must be 16-byte aligned", name);
+    int sms;
+    if ((rc = check_device(&sms))) return rc;
+    GemmArgs g = kind == 0 ? GemmArgs{A, B, offsets, M, d, f, E, out, status}
+                           : GemmArgs{A, B, offsets, M, f, d, E, out, status};
+    const char* why = "";
+    cudaError_t e = launch_grouped_gemm(kind, g, sms, static_cast<cudaStream_t>(stream), &why);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s (%s)", name, why, cudaGetErrorString(e));
+    return ok();
+}
+
+int moe_grouped_gemm_gateup_swiglu(const void* x_perm, const void* w_gate_up, const int32_t* offsets, int M,
+                                   int d, int f, int E, void* h, int32_t* status, moe_stream_t stream) {
+    return gemm_entry(0, x_perm, w_gate_up, offsets, M, d, f, E, h, status, stream,
+                      "moe_grouped_gemm_gateup_swiglu");
+}
+
+int moe_grouped_gemm_down(const void* h, const void* w_down, const int32_t* offsets, int M, int d, int f,
+                          int E, float* y_perm, int32_t* status, moe_stream_t stream) {
+    return gemm_entry(1, h, w_down, offsets, M, d, f, E, y_perm, status, stream, "moe_grouped_gemm_down");
+}
+
+int moe_combine(const float* y_perm, const float* w, const int32_t* dest, int T, int d, int top_k, void* out,
+                int32_t* status, moe_stream_t stream) {
+    int rc = check_shape(T, d, 0, top_k, top_k, false);
+    if (rc) return rc;
+    if (T == 0) return ok();
+    if (!y_perm || !w || !dest || !out) return fail(MOE_ERR_INVALID_ARG, "moe_combine: null pointer");
+    if (!aligned16(y_perm) || !aligned16(out))
+        return fail(MOE_ERR_INVALID_ARG, "moe_combine: y_perm and out must be 16-byte aligned");
+    int sms;
+    if ((rc = check_device(&sms))) return rc;
+    return launched(launch_combine(y_perm, w, dest, T, d, top_k, static_cast<__nv_bfloat16*>(out), status,
+                                   static_cast<cudaStream_t>(stream)),
+                    "combine");
+}
+
+int moe_forward(const void* x, const float* logits, const void* w_gate_up, const void* w_down, int T, int d,
+                int f, int E, int top_k, void* out, void* workspace, size_t workspace_bytes,
+                moe_stream_t stream) {
+    int rc = check_shape(T, d, f, E, top_k, true);
+    if (rc) return rc;
+    if (T == 0) return ok();
+    if (!x || !logits || !w_gate_up || !w_down || !out)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward: null pointer");
+    if (!aligned16(x) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(out))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward: bf16 tensors must be 16-byte aligned");
+    const size_t need = layout(T, d, f, E, top_k).total;
+    if (!workspace || workspace_bytes < need)
+        return fail(MOE_ERR_WORKSPACE, "moe_forward: workspace %zu bytes < %zu needed", workspace_bytes, need);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(MOE_ERR_WORKSPACE, "moe_forward: workspace must be 256-byte aligned");
+    int sms;
+    if ((rc = check_device(&sms))) return rc;
+    return run_layer(x, logits, w_gate_up, w_down, T, d, f, E, top_k, out, workspace, sms,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward_host(const void* x_host, const float* logits_host, const void* w_gate_up, const void* w_down,
+                     int T, int d, int f, int E, int top_k, void* out_host, void* workspace,
+                     size_t workspace_bytes, moe_stream_t stream) {
+    int rc = check_shape(T, d, f, E, top_k, true);
+    if (rc) return rc;
+    if (T == 0) return ok();
+    if (!x_host || !logits_host || !w_gate_up || !w_down || !out_host)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_host: null pointer");
+    const size_t need = layout(T, d, f, E, top_k).total;
+    const size_t stage = moe_host_staging_size(T, d, E);
+    if (!workspace || workspace_bytes < need + stage)
+        return fail(MOE_ERR_WORKSPACE, "moe_forward_host: workspace %zu bytes < %zu needed", workspace_bytes,
+                    need + stage);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(MOE_ERR_WORKSPACE, "moe_forward_host: workspace must be 256-byte aligned");
+    if (!aligned16(w_gate_up) || !aligned16(w_down))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_host: weights must be 16-byte aligned");
+    int sms;
+    if ((rc = check_device(&sms))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t xb = static_cast<size_t>(T) * d * 2, lb = static_cast<size_t>(T) * E * 4;
+    void* x_dev = at<char>(workspace, need);
+    void* out_dev = at<char>(workspace, need + align256(xb));
+    float* logits_dev = at<float>(workspace, need + 2 * align256(xb));
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(logits_dev, logits_host, lb, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return fail(MOE_ERR_CUDA, "moe_forward_host: host-to-device copy: %s", cudaGetErrorString(e));
+    if ((rc = run_layer(x_dev, logits_dev, w_gate_up, w_down, T, d, f, E, top_k, out_dev, workspace, sms, s)))
+        return rc;
+    if ((e = cudaMemcpyAsync(out_host, out_dev, xb, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return fail(MOE_ERR_CUDA, "moe_forward_host: device-to-host copy: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+int moe_get_device_error(const void* status_or_workspace, int32_t* code) {
+    if (!status_or_workspace || !code) return fail(MOE_ERR_INVALID_ARG, "moe_get_device_error: null pointer");
+    cudaError_t e = cudaMemcpy(code, status_or_workspace, sizeof(int32_t), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "moe_get_device_error: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+}  // extern "C"

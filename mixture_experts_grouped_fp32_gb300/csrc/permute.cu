@@ -1,0 +1,141 @@
+// permute.cu — step 2: group the T*k (token, slot) assignments by expert and copy x rows into
+// that order (the "dispatch" / data rearrangement ahead of the grouped GEMM: DeepGEMM PR #304
+// write-up, section 3.1, m-grouped contiguous layout; HPC-Ops page, FusedMoE paragraph).
+//
+// Order: expert ascending, then token ascending — a stable counting sort, so every output is
+// unique and the kernel is bit-exact with any correct implementation.
+//
+// One launch, no grid-wide synchronisation: every block histograms ALL assignments itself (a
+// few tens of KB of idx, read from L2), which gives it both the global offsets and, for its own
+// chunk of tokens, how many earlier tokens chose each expert.  It then ranks its chunk's
+// assignments, writes src/dest, and copies its tokens' x rows to their k destinations with
+// 16-byte vector loads and stores.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kPermThreads = 256;
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 8;
+constexpr int kMaxTokPerBlock = 16;
+
+__global__ void __launch_bounds__(kPermThreads)
+permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int T, int d, int E,
+               int k, int tok_per_block, int32_t* __restrict__ counts,
+               int32_t* __restrict__ offsets, int32_t* __restrict__ src,
+               int32_t* __restrict__ dest, uint4* __restrict__ x_perm,
+               int32_t* __restrict__ status) {
+    __shared__ int tot[kMaxE];      // assignments per expert, all tokens
+    __shared__ int before[kMaxE];   // ... from tokens before this block's chunk
+    __shared__ int off[kMaxE + 1];  // exclusive scan of tot
+    __shared__ int cidx[kMaxTokPerBlock * kMaxK];
+    __shared__ int crow[kMaxTokPerBlock * kMaxK];
+    __shared__ int bad;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < E; e += kPermThreads) {
+        tot[e] = 0;
+        before[e] = 0;
+    }
+    if (tid == 0) bad = 0;
+    __syncthreads();
+
+    const int t0 = blockIdx.x * tok_per_block;
+    const int t1 = min(T, t0 + tok_per_block);
+    const int nA = T * k, a0 = t0 * k;
+
+    // Histogram; warp-uniform trip count so __match_any_sync sees all 32 lanes.
+    for (int base = warp * 32; base < nA; base += kPermThreads) {
+        const int a = base + lane;
+        const int e = a < nA ? __ldg(idx + a) : 0;
+        const bool ok = a < nA && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+        if (a < nA && !ok) bad = 1;
+        const int key = ok ? (e * 2 + (a < a0 ? 1 : 0)) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (ok && lane == __ffs(peers) - 1) {
+            atomicAdd(&tot[e], __popc(peers));
+            if (a < a0) atomicAdd(&before[e], __popc(peers));
+        }
+    }
+    __syncthreads();
+
+    // Exclusive scan of tot over E <= 256 experts by warp 0, 8 experts per lane.
+    if (warp == 0) {
+        const int per = (E + 31) / 32;
+        const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+        int sum = 0;
+        for (int e = e0; e < e1; ++e) sum += tot[e];
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        int run = incl - sum;
+        for (int e = e0; e < e1; ++e) {
+            off[e] = run;
+            run += tot[e];
+        }
+        if (lane == 31) off[E] = incl;
+    }
+    __syncthreads();
+
+    if (blockIdx.x == 0) {
+        for (int e = tid; e < E; e += kPermThreads) counts[e] = tot[e];
+        for (int e = tid; e <= E; e += kPermThreads) offsets[e] = off[e];
+    }
+
+    // Rank this chunk's assignments.  Each expert occurs at most once per token, so the rank of
+    // (t, j) within expert e = number of earlier chunk tokens that chose e.
+    const int nloc = (t1 - t0) * k;
+    if (tid < nloc) cidx[tid] = __ldg(idx + a0 + tid);
+    __syncthreads();
+    if (tid < nloc) {
+        const int e = cidx[tid];
+        const int tl = tid / k;
+        int row = -1;
+        if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) {
+            int rank = 0;
+            for (int i = 0; i < tl * k; ++i) rank += (cidx[i] == e);
+            for (int i = tl * k; i < tl * k + k; ++i)
+                if (i != tid && cidx[i] == e) bad = 1;  // repeated within one token
+            row = off[e] + before[e] + rank;
+            src[row] = t0 + tl;
+        }
+        dest[a0 + tid] = row;
+        crow[tid] = row;
+    }
+    __syncthreads();
+    if (bad && tid == 0) flag_status(status, MOE_STATUS_BAD_EXPERT_ID);
+
+    // Row copies: x[t] -> x_perm[row(t, j)] for each slot j, 16 bytes per access.
+    const int dv = d / 8;  // uint4 per row
+    const int nvec = (t1 - t0) * dv;
+#pragma unroll 4
+    for (int i = tid; i < nvec; i += kPermThreads) {
+        const int tl = i / dv, v = i - tl * dv;
+        const uint4 val = __ldg(x + static_cast<size_t>(t0 + tl) * dv + v);
+        for (int j = 0; j < k; ++j) {
+            const int r = crow[tl * k + j];
+            if (r >= 0) x_perm[static_cast<size_t>(r) * dv + v] = val;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
+                           int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest,
+                           __nv_bfloat16* x_perm, int32_t* status, int num_sms, cudaStream_t s) {
+    // About two blocks per SM for the row copies, at most kMaxTokPerBlock tokens per block.
+    int tpb = (T + 2 * num_sms - 1) / (2 * num_sms);
+    tpb = tpb < 1 ? 1 : (tpb > kMaxTokPerBlock ? kMaxTokPerBlock : tpb);
+    const int blocks = (T + tpb - 1) / tpb;
+    permute_kernel<<<blocks, kPermThreads, 0, s>>>(
+        idx, reinterpret_cast<const uint4*>(x), T, d, E, k, tpb, counts, offsets, src, dest,
+        reinterpret_cast<uint4*>(x_perm), status);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,262 @@
+"""ctypes binding of ``libmoe.so`` (declared in ``include/moe.h``): argument marshalling only.
+
+Every function takes torch CUDA tensors, passes their ``data_ptr()`` and the current CUDA
+stream to the C entry point of the same name, and raises ``MoeError`` on a non-zero return.
+All arithmetic happens in the library's kernels; there is no Python or CPU fallback — if the
+library has not been built, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+_SIGS = {
+    "moe_version": ([], _I),
+    "moe_forward_launch_count": ([], _I),
+    "moe_last_error_string": ([], ctypes.c_char_p),
+    "moe_workspace_size": ([_I, _I, _I, _I, _I], _SZ),
+    "moe_workspace_layout": ([_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _I),
+    "moe_host_staging_size": ([_I, _I, _I], _SZ),
+    "moe_route": ([_P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_permute": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_grouped_gemm_gateup_swiglu": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "moe_grouped_gemm_down": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_forward": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
+    "moe_forward_host": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
+    "moe_get_device_error": ([_P, ctypes.POINTER(ctypes.c_int32)], _I),
+}
+
+WS_FIELDS = ("status", "idx", "w", "counts", "offsets", "src", "dest", "x_perm", "h", "y_perm", "total")
+
+STATUS_BAD_EXPERT_ID = 0x1
+STATUS_BAD_OFFSETS = 0x2
+STATUS_BAD_DEST = 0x4
+STATUS_WAIT_TIMEOUT = 0x8
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} returned {code}: {msg}")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load ``libmoe.so`` (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it with "
+                                   "`python -m mixture_experts_grouped_fp32_gb300.build`")
+            lib = ctypes.CDLL(path)
+            for name, (args, res) in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def _call(name: str, *args) -> None:
+    L = load()
+    rc = getattr(L, name)(*args)
+    if rc != 0:
+        raise MoeError(name, rc, L.moe_last_error_string().decode())
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else stream
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> None:
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor "
+                         f"(got {t.dtype}, cuda={t.is_cuda}, contiguous={t.is_contiguous()})")
+
+
+def workspace_size(T: int, d: int, f: int, E: int, top_k: int) -> int:
+    return int(load().moe_workspace_size(T, d, f, E, top_k))
+
+
+def workspace_layout(T: int, d: int, f: int, E: int, top_k: int) -> dict:
+    out = (_SZ * 11)()
+    _call("moe_workspace_layout", T, d, f, E, top_k, out)
+    return dict(zip(WS_FIELDS, [int(v) for v in out]))
+
+
+def host_staging_size(T: int, d: int, E: int) -> int:
+    return int(load().moe_host_staging_size(T, d, E))
+
+
+def forward_launch_count() -> int:
+    return int(load().moe_forward_launch_count())
+
+
+def route(logits: torch.Tensor, top_k: int, idx=None, w=None, stream=None):
+    _dev(logits, torch.float32, "logits")
+    T, E = logits.shape
+    idx = idx if idx is not None else torch.empty(T, top_k, dtype=torch.int32, device=logits.device)
+    w = w if w is not None else torch.empty(T, top_k, dtype=torch.float32, device=logits.device)
+    _call("moe_route", _ptr(logits), T, E, top_k, _ptr(idx), _ptr(w), _stream(stream))
+    return idx, w
+
+
+def permute(idx: torch.Tensor, x: torch.Tensor, E: int, status: torch.Tensor | None = None, stream=None,
+            out: tuple | None = None):
+    """Returns (counts, offsets, src, dest, x_perm); ``out`` may supply those five buffers."""
+    _dev(idx, torch.int32, "idx")
+    _dev(x, torch.bfloat16, "x")
+    T, k = idx.shape
+    d = x.shape[1]
+    dev = x.device
+    if out is not None:
+        counts, offsets, src, dest, x_perm = out
+    else:
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+        offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        src = torch.empty(T * k, dtype=torch.int32, device=dev)
+        dest = torch.empty(T, k, dtype=torch.int32, device=dev)
+        x_perm = torch.empty(T * k, d, dtype=torch.bfloat16, device=dev)
+    _call("moe_permute", _ptr(idx), _ptr(x), T, d, E, k, _ptr(counts), _ptr(offsets), _ptr(src),
+          _ptr(dest), _ptr(x_perm), _ptr(status), _stream(stream))
+    return counts, offsets, src, dest, x_perm
+
+
+def grouped_gemm_gateup_swiglu(x_perm, w_gate_up, offsets, h=None, status=None, stream=None):
+    _dev(x_perm, torch.bfloat16, "x_perm")
+    _dev(w_gate_up, torch.bfloat16, "w_gate_up")
+    _dev(offsets, torch.int32, "offsets")
+    M, d = x_perm.shape
+    E, _, f2 = w_gate_up.shape
+    h = h if h is not None else torch.empty(M, f2 // 2, dtype=torch.bfloat16, device=x_perm.device)
+    _call("moe_grouped_gemm_gateup_swiglu", _ptr(x_perm), _ptr(w_gate_up), _ptr(offsets), M, d, f2 // 2, E,
+          _ptr(h), _ptr(status), _stream(stream))
+    return h
+
+
+def grouped_gemm_down(h, w_down, offsets, y_perm=None, status=None, stream=None):
+    _dev(h, torch.bfloat16, "h")
+    _dev(w_down, torch.bfloat16, "w_down")
+    _dev(offsets, torch.int32, "offsets")
+    M, f = h.shape
+    E, _, d = w_down.shape
+    y_perm = y_perm if y_perm is not None else torch.empty(M, d, dtype=torch.float32, device=h.device)
+    _call("moe_grouped_gemm_down", _ptr(h), _ptr(w_down), _ptr(offsets), M, d, f, E, _ptr(y_perm),
+          _ptr(status), _stream(stream))
+    return y_perm
+
+
+def combine(y_perm, w, dest, out=None, status=None, stream=None):
+    _dev(y_perm, torch.float32, "y_perm")
+    _dev(w, torch.float32, "w")
+    _dev(dest, torch.int32, "dest")
+    T, k = dest.shape
+    d = y_perm.shape[1]
+    out = out if out is not None else torch.empty(T, d, dtype=torch.bfloat16, device=y_perm.device)
+    _call("moe_combine", _ptr(y_perm), _ptr(w), _ptr(dest), T, d, k, _ptr(out), _ptr(status), _stream(stream))
+    return out
+
+
+def forward(x, logits, w_gate_up, w_down, top_k, out=None, workspace=None, stream=None):
+    """One call for the whole layer (five kernel launches).  Returns ``out`` bf16 [T, d]."""
+    _dev(x, torch.bfloat16, "x")
+    _dev(logits, torch.float32, "logits")
+    _dev(w_gate_up, torch.bfloat16, "w_gate_up")
+    _dev(w_down, torch.bfloat16, "w_down")
+    T, d = x.shape
+    E, _, f2 = w_gate_up.shape
+    if workspace is None:
+        workspace = torch.empty(workspace_size(T, d, f2 // 2, E, top_k), dtype=torch.uint8, device=x.device)
+    out = out if out is not None else torch.empty(T, d, dtype=torch.bfloat16, device=x.device)
+    _call("moe_forward", _ptr(x), _ptr(logits), _ptr(w_gate_up), _ptr(w_down), T, d, f2 // 2, E, top_k,
+          _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    return out
+
+
+def forward_host(x_host, logits_host, w_gate_up, w_down, top_k, out_host, workspace, stream=None):
+    """The layer with x, logits and out in (page-locked) host memory; copies are enqueued on the
+    stream together with the five kernels.  Synchronise the stream before reading ``out_host``."""
+    for t, n in ((x_host, "x_host"), (logits_host, "logits_host"), (out_host, "out_host")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous host tensor")
+    _dev(w_gate_up, torch.bfloat16, "w_gate_up")
+    _dev(w_down, torch.bfloat16, "w_down")
+    T, d = x_host.shape
+    E, _, f2 = w_gate_up.shape
+    _call("moe_forward_host", _ptr(x_host), _ptr(logits_host), _ptr(w_gate_up), _ptr(w_down), T, d, f2 // 2, E,
+          top_k, _ptr(out_host), _ptr(workspace), workspace.numel(), _stream(stream))
+    return out_host
+
+
+def get_device_error(status_or_workspace: torch.Tensor) -> int:
+    code = ctypes.c_int32(0)
+    _call("moe_get_device_error", _ptr(status_or_workspace), ctypes.byref(code))
+    return int(code.value)
+
+
+def workspace_views(ws: torch.Tensor, T: int, d: int, f: int, E: int, top_k: int) -> dict:
+    """Typed views of moe_forward's intermediates inside ``ws`` (for inspection and tests)."""
+    L = workspace_layout(T, d, f, E, top_k)
+    M = T * top_k
+
+    def view(name, n, dtype, shape):
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return ws[L[name]:L[name] + nbytes].view(dtype).view(*shape)
+
+    return {
+        "status": view("status", 1, torch.int32, (1,)),
+        "idx": view("idx", M, torch.int32, (T, top_k)),
+        "w": view("w", M, torch.float32, (T, top_k)),
+        "counts": view("counts", E, torch.int32, (E,)),
+        "offsets": view("offsets", E + 1, torch.int32, (E + 1,)),
+        "src": view("src", M, torch.int32, (M,)),
+        "dest": view("dest", M, torch.int32, (T, top_k)),
+        "x_perm": view("x_perm", M * d, torch.bfloat16, (M, d)),
+        "h": view("h", M * f, torch.bfloat16, (M, f)),
+        "y_perm": view("y_perm", M * d, torch.float32, (M, d)),
+    }
+
+
+class MoELayer:
+    """A Mixture-of-Experts FFN layer whose weights and workspace live on one GPU.
+
+    ``layer(x, logits)`` runs the five-kernel forward on the current stream and returns bf16
+    [T, d]; the workspace grows on demand and is reused across calls."""
+
+    def __init__(self, w_gate_up: torch.Tensor, w_down: torch.Tensor, top_k: int):
+        _dev(w_gate_up, torch.bfloat16, "w_gate_up")
+        _dev(w_down, torch.bfloat16, "w_down")
+        self.w_gate_up, self.w_down, self.top_k = w_gate_up, w_down, top_k
+        self.E, self.d, f2 = w_gate_up.shape
+        self.f = f2 // 2
+        self._ws = torch.empty(0, dtype=torch.uint8, device=w_gate_up.device)
+
+    def workspace(self, T: int) -> torch.Tensor:
+        need = workspace_size(T, self.d, self.f, self.E, self.top_k)
+        if self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.w_gate_up.device)
+        return self._ws
+
+    def __call__(self, x: torch.Tensor, logits: torch.Tensor, out: torch.Tensor | None = None):
+        return forward(x, logits, self.w_gate_up, self.w_down, self.top_k, out=out,
+                       workspace=self.workspace(x.shape[0]))

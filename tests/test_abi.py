@@ -1,0 +1,137 @@
+"""libmoe.so without a GPU: it loads, exports every symbol include/moe.h declares, and rejects
+bad arguments with the documented codes before making any CUDA call.  CPU only."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_grouped_fp32_gb300 import build, moe
+    if not os.path.exists(moe.LIB_PATH):
+        build.build()
+    return moe.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)
+
+
+def test_header_declares_the_stage_calls():
+    names = set(declared_symbols())
+    for n in ["moe_route", "moe_permute", "moe_grouped_gemm_gateup_swiglu", "moe_grouped_gemm_down",
+              "moe_combine", "moe_forward"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_launch_count(lib):
+    assert lib.moe_version() >= 100
+    assert lib.moe_forward_launch_count() == 5
+
+
+def _err(lib):
+    return lib.moe_last_error_string().decode()
+
+
+def test_workspace_layout_matches_the_documented_order(lib):
+    from mixture_experts_grouped_fp32_gb300 import moe
+    T, d, f, E, k = 300, 512, 768, 8, 2
+    L = moe.workspace_layout(T, d, f, E, k)
+    M = T * k
+
+    def up(v):
+        return (v + 255) // 256 * 256
+
+    expect, o = {}, 0
+    for name, nbytes in [("status", 256), ("idx", M * 4), ("w", M * 4), ("counts", E * 4),
+                         ("offsets", (E + 1) * 4), ("src", M * 4), ("dest", M * 4),
+                         ("x_perm", M * d * 2), ("h", M * f * 2), ("y_perm", M * d * 4)]:
+        expect[name] = o
+        o = up(o + nbytes)
+    expect["total"] = o
+    assert L == expect
+    assert moe.workspace_size(T, d, f, E, k) == o
+    assert moe.workspace_size(T, 100, f, E, k) == 0  # invalid shape
+
+
+@pytest.mark.parametrize("args,fragment", [
+    ((-1, 64, 128, 8, 2), "T = -1"),
+    ((4, 64, 128, 0, 1), "E = 0"),
+    ((4, 64, 128, 257, 2), "E = 257"),
+    ((4, 64, 128, 8, 9), "top_k = 9"),
+    ((4, 64, 128, 4, 5), "top_k = 5"),
+    ((4, 96, 128, 8, 2), "d = 96"),
+    ((4, 64, 100, 8, 2), "f = 100"),
+])
+def test_forward_rejects_bad_shapes(lib, args, fragment):
+    T, d, f, E, k = args
+    p = ctypes.c_void_p(1 << 20)
+    rc = lib.moe_forward(p, p, p, p, T, d, f, E, k, p, p, 1 << 40, None)
+    assert rc == -1
+    assert fragment in _err(lib)
+
+
+def test_forward_rejects_null_and_small_workspace(lib):
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.moe_forward(None, p, p, p, 4, 64, 128, 8, 2, p, p, 1 << 40, None) == -1
+    assert lib.moe_forward(p, p, p, p, 4, 64, 128, 8, 2, p, p, 16, None) == -3
+    assert "workspace" in _err(lib)
+    assert lib.moe_forward(p, p, p, p, 4, 64, 128, 8, 2, p, ctypes.c_void_p((1 << 20) + 16), 1 << 40,
+                           None) == -3
+    assert lib.moe_forward(p, p, ctypes.c_void_p((1 << 20) + 2), p, 4, 64, 128, 8, 2, p, p, 1 << 40,
+                           None) == -1
+
+
+def test_stage_calls_reject_bad_arguments(lib):
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.moe_route(None, 4, 8, 2, p, p, None) == -1
+    assert lib.moe_route(p, 4, 8, 0, p, p, None) == -1
+    assert lib.moe_permute(p, None, 4, 64, 8, 2, p, p, p, p, p, None, None) == -1
+    assert lib.moe_permute(p, ctypes.c_void_p((1 << 20) + 8), 4, 64, 8, 2, p, p, p, p, p, None, None) == -1
+    assert lib.moe_grouped_gemm_gateup_swiglu(p, p, None, 8, 64, 128, 8, p, None, None) == -1
+    assert lib.moe_grouped_gemm_gateup_swiglu(p, p, p, -1, 64, 128, 8, p, None, None) == -1
+    assert lib.moe_grouped_gemm_down(p, p, p, 8, 64, 96, 8, p, None, None) == -1
+    assert lib.moe_combine(p, p, p, 4, 64, 0, p, None, None) == -1
+    assert lib.moe_get_device_error(None, None) == -1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    # T = 0 (and M = 0) launch nothing and succeed, so they need no device.
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.moe_forward(p, p, p, p, 0, 64, 128, 8, 2, p, p, 1 << 40, None) == 0
+    assert lib.moe_route(p, 0, 8, 2, p, p, None) == 0
+    assert lib.moe_permute(p, p, 0, 64, 8, 2, p, p, p, p, p, None, None) == 0
+    assert lib.moe_grouped_gemm_down(p, p, p, 0, 64, 128, 8, p, None, None) == 0
+    assert lib.moe_combine(p, p, p, 0, 64, 2, p, None, None) == 0
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    from mixture_experts_grouped_fp32_gb300 import moe
+    saved = moe._lib
+    moe._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="missing"):
+            moe.load(str(tmp_path / "libmoe.so"))
+    finally:
+        moe._lib = saved
+
+
+def test_product_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "mixture_experts_grouped_fp32_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "from oracle" not in text, fn
+                assert "liboracle" not in text and "moe_oracle" not in text, fn

@@ -1,0 +1,52 @@
+"""GPU parity at the full workload sizes, in the launch configuration bench.py times
+(moe_forward, one call, five launches).  Routing and the permutation are compared in full and bit
+for bit; the layer output is compared on sampled tokens that the oracle computes one by one
+(first, last, random, and tokens routed to the busiest expert)."""
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+from gpu_cases import assert_close, assert_layer_close, to_np_bits  # noqa: E402
+
+from mixture_experts_grouped_fp32_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+FULL = ["mixtral_t32", "mixtral_t512", "mixtral_t512_skew40", "mixtral_t4096", "deepseek_t2048"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_forward(oracle, name):
+    from mixture_experts_grouped_fp32_gb300 import moe
+    w = WORKLOADS[name]
+    dev = torch.device("cuda")
+    logits, x, wgu, wd = make_inputs(w, seed=0, weight_device="cuda")
+    ws = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k), dtype=torch.uint8, device=dev)
+    out = moe.forward(x.to(dev), logits.to(dev), wgu, wd, w.k, workspace=ws)
+    torch.cuda.synchronize()
+    assert moe.get_device_error(ws) == 0
+    v = moe.workspace_views(ws, w.T, w.d, w.f, w.E, w.k)
+
+    ln = logits.numpy()
+    idx, wt = oracle.route(ln, w.k)
+    counts, offsets, src, dest = oracle.permute(idx, w.E)
+    assert np.array_equal(v["idx"].cpu().numpy(), idx)
+    assert_close(v["w"].cpu().numpy(), wt, 1e-6, 0, "route weights")
+    assert np.array_equal(v["counts"].cpu().numpy(), counts)
+    assert np.array_equal(v["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(v["src"].cpu().numpy(), src)
+    assert np.array_equal(v["dest"].cpu().numpy(), dest)
+    xb = to_np_bits(x)
+    assert np.array_equal(to_np_bits(v["x_perm"].cpu()), xb[src])
+
+    rng = np.random.default_rng(1)
+    hot = int(np.argmax(counts))
+    hot_tokens = src[offsets[hot]:offsets[hot + 1]]
+    sample = np.unique(np.concatenate([[0, w.T - 1], rng.integers(0, w.T, 6),
+                                       rng.choice(hot_tokens, min(4, hot_tokens.size), replace=False)]))
+    ref = oracle.forward_tokens(xb, ln, to_np_bits(wgu), to_np_bits(wd), w.k, sample.astype(np.int32))
+    got = out[torch.from_numpy(sample).to(dev)].float().cpu().numpy()
+    assert_layer_close(got, ref, f"{name} sampled tokens {sample.tolist()}")

@@ -1,0 +1,250 @@
+"""GPU parity: every step of the CUDA path against the CPU oracle on the same seeded inputs,
+through the C ABI (libmoe.so via its ctypes binding).  Sizes here finish in seconds on the oracle
+while spanning several tiles, ragged expert segments, partial N tiles, more work items than
+SMs (so the persistent loop wraps its pipeline and both accumulators), and the degenerate cases.
+"""
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+from gpu_cases import (assert_close, assert_layer_close, case_inputs, from_np_bits,  # noqa: E402
+                       random_bf16, to_np_bits)
+
+from mixture_experts_grouped_fp32_gb300.workloads import WORKLOADS, Workload  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_grouped_fp32_gb300 import moe as m
+    m.load()
+    return m
+
+
+# (name, Workload) — the layer shapes checked end to end against the oracle's full forward.
+CASES = [
+    WORKLOADS["tiny"],
+    Workload("ragged_multi_tile", 300, 512, 768, 8, 2),
+    Workload("many_items_per_cta", 4096, 256, 2048, 2, 1),
+    Workload("partial_n_tiles_k_eq_e", 37, 192, 320, 4, 4),
+    Workload("zipf_skew_zero_token_experts", 256, 256, 384, 64, 6, ("zipf", 1.2)),
+    Workload("one_hot_expert", 200, 128, 256, 8, 1, ("hot0", 40.0)),
+    Workload("single_token", 1, 128, 128, 8, 2),
+    Workload("dense_e1_k1", 70, 128, 192, 1, 1),
+    Workload("minimal_dims", 50, 64, 64, 3, 2),
+    Workload("deepseek_like_wide_d", 40, 1024, 256, 32, 8, ("zipf", 1.2)),
+]
+
+
+def _forward_and_views(moe, w, logits, x, wgu, wd):
+    dev = torch.device(DEV)
+    ws = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k), dtype=torch.uint8, device=dev)
+    ws.fill_(0xFF)  # NaN-ish sentinel everywhere: every consumed intermediate must be written
+    out = moe.forward(x.to(dev), logits.to(dev), wgu.to(dev), wd.to(dev), w.k, workspace=ws)
+    torch.cuda.synchronize()
+    return out, moe.workspace_views(ws, w.T, w.d, w.f, w.E, w.k), ws
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_forward_matches_oracle(moe, oracle, w):
+    logits, x, wgu, wd = case_inputs(w, seed=0)
+    out, v, ws = _forward_and_views(moe, w, logits, x, wgu, wd)
+    assert moe.get_device_error(ws) == 0
+    ln = logits.numpy()
+    idx, wt = oracle.route(ln, w.k)
+    counts, offsets, src, dest = oracle.permute(idx, w.E)
+    assert np.array_equal(v["idx"].cpu().numpy(), idx)
+    assert_close(v["w"].cpu().numpy(), wt, 1e-6, 0, "route weights")
+    assert np.array_equal(v["counts"].cpu().numpy(), counts)
+    assert np.array_equal(v["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(v["src"].cpu().numpy(), src)
+    assert np.array_equal(v["dest"].cpu().numpy(), dest)
+    assert np.array_equal(to_np_bits(v["x_perm"].cpu()), to_np_bits(x)[src])
+    ref = oracle.forward(to_np_bits(x), ln, to_np_bits(wgu), to_np_bits(wd), w.k)
+    assert_layer_close(out.float().cpu().numpy(), ref, w.name)
+
+
+def test_forward_is_deterministic(moe):
+    w = Workload("det", 300, 512, 768, 8, 2)
+    logits, x, wgu, wd = case_inputs(w, seed=3)
+    a, _, _ = _forward_and_views(moe, w, logits, x, wgu, wd)
+    b, _, _ = _forward_and_views(moe, w, logits, x, wgu, wd)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ------------------------------------------------------------------------------------------
+# Stage by stage, each stage fed seeded inputs (never the CUDA path's own outputs).
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("T,E,k,ties", [(4096, 8, 2, False), (513, 256, 8, False), (333, 64, 6, True),
+                                        (77, 5, 5, True), (1, 8, 1, False), (1000, 33, 3, False),
+                                        (64, 8, 2, True)])
+def test_route_parity(moe, oracle, T, E, k, ties):
+    g = torch.Generator("cpu").manual_seed(T * 7 + E)
+    logits = (torch.randint(0, 2, (T, E), generator=g).float() if ties
+              else torch.randn(T, E, generator=g))
+    idx, w = moe.route(logits.to(DEV), k)
+    torch.cuda.synchronize()
+    ridx, rw = oracle.route(logits.numpy(), k)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert_close(w.cpu().numpy(), rw, 1e-6, 0, "route weights")
+
+
+@pytest.mark.parametrize("T,d,E,k", [(4096, 4096, 8, 2), (2048, 256, 256, 8), (37, 64, 4, 4), (1, 128, 8, 2),
+                                     (999, 192, 64, 6)])
+def test_permute_parity(moe, oracle, T, d, E, k):
+    g = torch.Generator("cpu").manual_seed(T + d)
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).int()
+    x = random_bf16((T, d), seed=T)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    counts, offsets, src, dest, x_perm = moe.permute(idx.to(DEV), x.to(DEV), E, status=status)
+    torch.cuda.synchronize()
+    rc, ro, rs, rd = oracle.permute(idx.numpy(), E)
+    assert int(status.item()) == 0
+    assert np.array_equal(counts.cpu().numpy(), rc)
+    assert np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(src.cpu().numpy(), rs)
+    assert np.array_equal(dest.cpu().numpy(), rd)
+    assert np.array_equal(to_np_bits(x_perm.cpu()), oracle.gather_rows(to_np_bits(x), rs))
+
+
+def _segments(oracle, T, E, k, seed, bias=("none", 0.0)):
+    from mixture_experts_grouped_fp32_gb300.workloads import draw_routing
+    logits, _ = draw_routing(T, 64, E, seed, bias)
+    idx, _ = oracle.route(logits.numpy(), k)
+    counts, offsets, _, _ = oracle.permute(idx, E)
+    return offsets
+
+
+GEMM_CASES = [  # (T, d, f, E, k, bias)
+    (300, 512, 768, 8, 2, ("none", 0.0)),
+    (4096, 256, 2048, 2, 1, ("none", 0.0)),
+    (37, 192, 320, 4, 4, ("none", 0.0)),
+    (256, 256, 384, 64, 6, ("zipf", 1.2)),
+    (200, 128, 256, 8, 1, ("hot0", 40.0)),
+]
+
+
+@pytest.mark.parametrize("T,d,f,E,k,bias", GEMM_CASES)
+def test_gateup_swiglu_parity(moe, oracle, T, d, f, E, k, bias):
+    offsets = _segments(oracle, T, E, k, seed=11, bias=bias)
+    M = T * k
+    x_perm = random_bf16((M, d), seed=5)
+    _, _, wgu, _ = case_inputs(Workload("g", 1, d, f, E, 1), seed=2)
+    extra = 3  # rows past offsets[E] must stay untouched
+    h = torch.full((M + extra, f), float("nan"), dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    xp = torch.cat([x_perm, torch.zeros(extra, d, dtype=torch.bfloat16)]).to(DEV)
+    moe.grouped_gemm_gateup_swiglu(xp, wgu.to(DEV), torch.from_numpy(offsets).to(DEV), h=h, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.gateup_swiglu(to_np_bits(x_perm), offsets, to_np_bits(wgu))
+    got = h[:M].float().cpu().numpy()
+    assert np.isfinite(got).all(), "some h rows were not written"
+    assert torch.isnan(h[M:].float()).all(), "rows past offsets[E] were written"
+    assert float(np.abs(got - ref).max()) <= 1e-2 * float(np.abs(ref).max())
+    assert_close(got, ref, 2.0 ** -7, 2e-3, "h")
+
+
+@pytest.mark.parametrize("T,d,f,E,k,bias", GEMM_CASES)
+def test_down_parity(moe, oracle, T, d, f, E, k, bias):
+    offsets = _segments(oracle, T, E, k, seed=12, bias=bias)
+    M = T * k
+    h = random_bf16((M, f), seed=6, scale=0.5)
+    _, _, _, wd = case_inputs(Workload("g", 1, d, f, E, 1), seed=4)
+    y = torch.full((M, d), float("nan"), dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    moe.grouped_gemm_down(h.to(DEV), wd.to(DEV), torch.from_numpy(offsets).to(DEV), y_perm=y, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.down(to_np_bits(h), offsets, to_np_bits(wd))
+    got = y.cpu().numpy()
+    assert np.isfinite(got).all(), "some y rows were not written"
+    assert_close(got, ref, 1e-3, 1e-4, "y_perm")
+
+
+@pytest.mark.parametrize("T,d,E,k", [(4096, 4096, 8, 2), (2048, 7168, 256, 8), (37, 192, 4, 4), (1, 64, 3, 1)])
+def test_combine_parity(moe, oracle, T, d, E, k):
+    g = torch.Generator("cpu").manual_seed(T + k)
+    logits = torch.randn(T, E, generator=g)
+    idx, w = oracle.route(logits.numpy(), k)
+    _, _, _, dest = oracle.permute(idx, E)
+    y = torch.randn(T * k, d, generator=g)
+    out = moe.combine(y.to(DEV), torch.from_numpy(w).to(DEV), torch.from_numpy(dest).to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.combine(y.numpy(), w, dest)
+    assert_close(out.float().cpu().numpy(), ref, 2.0 ** -8, 1e-6, "combine")
+
+
+# ------------------------------------------------------------------------------------------
+# Device-side checks: bad data drives no out-of-bounds access; the status word says what.
+# ------------------------------------------------------------------------------------------
+def test_status_flags_bad_expert_ids(moe):
+    idx = torch.tensor([[0, 1], [2, 9], [3, 3]], dtype=torch.int32, device=DEV)
+    x = torch.zeros(3, 64, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    moe.permute(idx, x, 4, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & moe.STATUS_BAD_EXPERT_ID
+
+
+def test_status_flags_bad_offsets(moe):
+    E, d, f = 4, 64, 128
+    x_perm = torch.zeros(16, d, dtype=torch.bfloat16, device=DEV)
+    wgu = torch.zeros(E, d, 2 * f, dtype=torch.bfloat16, device=DEV)
+    h = torch.zeros(16, f, dtype=torch.bfloat16, device=DEV)
+    for bad in ([0, 5, 3, 8, 16], [0, 4, 8, 12, 17]):  # decreasing; past M
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        offs = torch.tensor(bad, dtype=torch.int32, device=DEV)
+        moe.grouped_gemm_gateup_swiglu(x_perm, wgu, offs, h=h, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) & moe.STATUS_BAD_OFFSETS
+
+
+def test_status_flags_bad_dest(moe):
+    y = torch.ones(4, 64, dtype=torch.float32, device=DEV)
+    w = torch.full((2, 2), 0.5, dtype=torch.float32, device=DEV)
+    dest = torch.tensor([[0, 1], [2, 4]], dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = moe.combine(y, w, dest, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & moe.STATUS_BAD_DEST
+    assert torch.allclose(out[0].float(), torch.ones(64, device=DEV))
+
+
+def test_forward_host_matches_forward(moe):
+    w = Workload("host", 97, 256, 512, 8, 2)
+    logits, x, wgu, wd = case_inputs(w, seed=9)
+    dev = torch.device(DEV)
+    wgu_d, wd_d = wgu.to(dev), wd.to(dev)
+    ref = moe.forward(x.to(dev), logits.to(dev), wgu_d, wd_d, w.k)
+    ws = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k) + moe.host_staging_size(w.T, w.d, w.E),
+                     dtype=torch.uint8, device=dev)
+    xh, lh = x.pin_memory(), logits.pin_memory()
+    oh = torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory()
+    moe.forward_host(xh, lh, wgu_d, wd_d, w.k, oh, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))
+
+
+def test_forward_makes_five_launches(moe):
+    w = WORKLOADS["tiny"]
+    logits, x, wgu, wd = case_inputs(w)
+    dev = torch.device(DEV)
+    args = (x.to(dev), logits.to(dev), wgu.to(dev), wd.to(dev), w.k)
+    ws = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k), dtype=torch.uint8, device=dev)
+    moe.forward(*args, workspace=ws)
+    torch.cuda.synchronize()
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        moe.forward(*args, workspace=ws)
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events() if str(e.device_type).endswith("CUDA") and "_kernel" in e.name]
+    if not names:
+        pytest.skip("profiler recorded no CUDA kernels on this build")
+    assert len(names) == moe.forward_launch_count() == 5, names
