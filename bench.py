@@ -25,7 +25,6 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -50,9 +49,31 @@ KERNEL_NAMES = {"route": "route_kernel", "permute": "permute_kernel",
                 "gateup_swiglu": "grouped_gemm_kernel<0>", "down": "grouped_gemm_kernel<1>",
                 "combine": "combine_kernel"}
 
-# DRAM traffic (read + write bytes per launch) from ncu captures, keyed by (workload, stage), valid
-# only while the kernel source hashes to the recorded value; see profiles/.
-MEASURED_TRAFFIC: dict = {}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum per launch) from ncu captures of the
+# kernel source with the recorded hash (profiles/grouped_gemm_*.md); reported only while the GEMM
+# source still hashes to that value, else null.
+MEASURED_TRAFFIC = {
+    ("mixtral_t32", "gateup_swiglu"): (1884495616, "ab1644aa9a1bc078"),
+    ("mixtral_t32", "down"): (944644096, "ab1644aa9a1bc078"),
+    ("mixtral_t4096", "gateup_swiglu"): (2193298432, "ab1644aa9a1bc078"),
+    ("mixtral_t4096", "down"): (1535353344, "ab1644aa9a1bc078"),
+}
+GEMM_SOURCES = ("mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm.cu",
+                "mixture_experts_grouped_fp32_gb300/csrc/tcgen05.cuh")
+
+
+def gemm_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for p in GEMM_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, stage: str):
+    rec = MEASURED_TRAFFIC.get((workload, stage))
+    return rec[0] if rec and rec[1] == gemm_source_hash() else None
 
 
 def load_peaks():
@@ -155,6 +176,21 @@ class ClockSampler:
 # ----------------------------------------------------------------------------------------------
 # Our arm
 # ----------------------------------------------------------------------------------------------
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The largest of every rank's value (the slowest replica sets the whole job's time)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    on = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=on)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput of independent replicas: all ranks' tokens over the slowest rank's time."""
+    return tokens_per_rank * world / (ms_max * 1e-3)
+
+
 def run_ours(args, w: Workload, rank: int, world: int, dist):
     from mixture_experts_grouped_fp32_gb300 import moe
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -207,11 +243,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         sampler.mark()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     ms = statistics.mean(step_ms)
-    ms_max = ms
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist, dev)
     clocks = sampler.stop() if sampler else None
 
     # ---- per-stage timing: the five stage entry points, events between launches ---------------
@@ -271,15 +303,14 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         achieved = sw[dom]["bytes"] / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = MEASURED_TRAFFIC.get((w.name, dom))
+    roof["traffic"] = measured_traffic(w.name, dom)
     roof.update({"kernel": KERNEL_NAMES[dom], "peak_source": peak_src + " (burst)",
                  "algorithmic_per_launch": sw[dom]["flops"] if roof["bound"] == "tensor" else sw[dom]["bytes"],
                  "launch_ms": round(dom_ms, 4)})
     layer_roof_ms = 1e3 * max(lw["bytes"] / (peaks["hbm_gbs"] * 1e9), lw["flops"] / (peaks["bf16_tflops"] * 1e12))
 
-    tokens = w.T * world
     return {
-        "ms": ms_max, "tokens": tokens, "t_wall": t_wall, "clocks": clocks, "stage_ms": stage_ms,
+        "ms": ms_max, "tokens_per_rank": w.T, "t_wall": t_wall, "clocks": clocks, "stage_ms": stage_ms,
         "staged_step_ms": staged_step_ms, "e2e_ms": e2e_ms, "roofline": roof, "layer": lw,
         "layer_roof_ms": layer_roof_ms, "n_active": n_active, "max_load": int(counts.max()),
         "host_weights": (wgu, wd), "inputs": (logits, x), "step_ms_p10_p90": (
@@ -390,7 +421,7 @@ def main():
         dist.init_process_group("nccl")
     r = run_ours(args, w, rank, world, dist)
     if rank == 0:
-        tok_s = r["tokens"] / (r["ms"] * 1e-3)
+        tok_s = job_tokens_per_s(r["tokens_per_rank"], world, r["ms"])
         tflops = r["layer"]["flops"] * world / (r["ms"] * 1e-3) / 1e12
         line = {
             "metric": METRIC, "value": round(tok_s, 2), "unit": "tokens/s", "n_gpus": world,

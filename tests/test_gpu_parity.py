@@ -232,19 +232,47 @@ def test_forward_host_matches_forward(moe):
     assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))
 
 
-def test_forward_makes_five_launches(moe):
+def _cudart():
+    import ctypes
+    import glob
+    try:
+        return ctypes.CDLL("libcudart.so.13")
+    except OSError:
+        for c in glob.glob(os.path.join(os.path.dirname(torch.__file__), "..", "nvidia", "*", "lib",
+                                        "libcudart.so*")):
+            return ctypes.CDLL(c)
+    return None
+
+
+def test_forward_is_five_kernels_and_graph_capturable(moe):
+    """Capture one moe_forward in a CUDA graph: the runtime counts exactly five kernel nodes, and
+    replaying the graph reproduces the eager result bit for bit."""
+    import ctypes
     w = WORKLOADS["tiny"]
     logits, x, wgu, wd = case_inputs(w)
     dev = torch.device(DEV)
     args = (x.to(dev), logits.to(dev), wgu.to(dev), wd.to(dev), w.k)
     ws = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k), dtype=torch.uint8, device=dev)
-    moe.forward(*args, workspace=ws)
+    eager = moe.forward(*args, workspace=ws).clone()
+    out = torch.zeros_like(eager)
     torch.cuda.synchronize()
-    from torch.profiler import ProfilerActivity, profile
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
-        moe.forward(*args, workspace=ws)
-        torch.cuda.synchronize()
-    names = [e.name for e in prof.events() if str(e.device_type).endswith("CUDA") and "_kernel" in e.name]
-    if not names:
-        pytest.skip("profiler recorded no CUDA kernels on this build")
-    assert len(names) == moe.forward_launch_count() == 5, names
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.forward(*args, out=out, workspace=ws)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    rt = _cudart()
+    if rt is None or not hasattr(g, "raw_cuda_graph"):
+        pytest.skip("no libcudart / raw_cuda_graph to count graph nodes")
+    n = ctypes.c_size_t(0)
+    assert rt.cudaGraphGetNodes(ctypes.c_void_p(g.raw_cuda_graph()), None, ctypes.byref(n)) == 0
+    nodes = (ctypes.c_void_p * n.value)()
+    assert rt.cudaGraphGetNodes(ctypes.c_void_p(g.raw_cuda_graph()), nodes, ctypes.byref(n)) == 0
+    kinds = []
+    for i in range(n.value):
+        t = ctypes.c_int(-1)
+        assert rt.cudaGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) == 0
+        kinds.append(t.value)
+    # cudaGraphNodeTypeKernel == 0
+    assert kinds.count(0) == moe.forward_launch_count() == 5, kinds
