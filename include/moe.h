@@ -148,6 +148,32 @@ MOE_API int moe_forward_host(const void* x_host, const float* logits_host, const
                      const void* w_down, int T, int d, int f, int E, int top_k, void* out_host,
                      void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* Size of the fixed scratch array that moe_forward_noalloc uses (64 MiB). */
+#define MOE_NOALLOC_SCRATCH_BYTES (64ull * 1024ull * 1024ull)
+
+/* moe_forward without a caller-provided workspace and without allocating anything.
+ * The pages have no counterpart to this call; it exists for callers that cannot allocate device
+ * memory when they run the layer: code that runs while a stream is being captured into a CUDA
+ * graph (allocation is not allowed there), inference servers whose device memory is carved up in
+ * advance so that no extra pool is available, and plugins inside a host framework whose
+ * allocator they cannot reach.  Such callers pass only the layer's inputs and output.
+ *   x [T,d] bf16, logits [T,E] fp32, w_gate_up [E,d,2f] bf16, w_down [E,f,d] bf16 in;
+ *   out [T,d] bf16 out — device pointers, same meaning and layout as moe_forward.
+ * The intermediates live in one file-scope device array of MOE_NOALLOC_SCRATCH_BYTES that every
+ * GPU loading this library holds until the process exits.  Shapes whose moe_workspace_size()
+ * exceeds it are rejected with MOE_ERR_WORKSPACE (e.g. the Mixtral-8x7B shape fits up to
+ * T = 512 tokens with top-2).  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture.  All calls on a device share the one array and it keeps the last call's contents
+ * (every intermediate is rewritten before it is read; the status word is reset by the first
+ * kernel), so calls whose work overlaps on the GPU — on different streams, or from different
+ * threads without ordering — race with each other: serialise them.  The device status word is
+ * kept inside the array and is not readable through moe_get_device_error.
+ * Returns MOE_OK or an MOE_ERR_* code as moe_forward does. */
+MOE_API int moe_forward_noalloc(const void* x, const float* logits, const void* w_gate_up,
+                                const void* w_down, int T, int d, int f, int E, int top_k,
+                                void* out, moe_stream_t stream);
+
 /* Reads (synchronously: cudaMemcpy) a device status word — a stage call's `status` pointer, or
  * the workspace of moe_forward — into *code (0 = no device-side error). */
 MOE_API int moe_get_device_error(const void* status_or_workspace, int32_t* code);

@@ -142,6 +142,33 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
 }  // namespace
 }  // namespace moe
 
+// Scratch of moe_forward_noalloc: one fixed device array per GPU, never allocated at run time.
+static __device__ __align__(256) unsigned char moe_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+namespace moe {
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of moe_noalloc_scratch on device `dev` (current), looked up once per device.
+// In host code the array's name is only a host-side handle, never a device address.
+int noalloc_scratch(int dev, void** out) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, moe_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return fail(MOE_ERR_CUDA, "moe_forward_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
 using namespace moe;
 
 extern "C" {
@@ -300,6 +327,32 @@ int moe_forward_host(const void* x_host, const float* logits_host, const void* w
     if ((e = cudaMemcpyAsync(out_host, out_dev, xb, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "moe_forward_host: device-to-host copy: %s", cudaGetErrorString(e));
     return ok();
+}
+
+int moe_forward_noalloc(const void* x, const float* logits, const void* w_gate_up, const void* w_down, int T,
+                        int d, int f, int E, int top_k, void* out, moe_stream_t stream) {
+    int rc = check_shape(T, d, f, E, top_k, true);
+    if (rc) return rc;
+    if (T == 0) return ok();
+    if (!x || !logits || !w_gate_up || !w_down || !out)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_noalloc: null pointer");
+    if (!aligned16(x) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(out))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_noalloc: bf16 tensors must be 16-byte aligned");
+    const size_t need = layout(T, d, f, E, top_k).total;
+    if (need > MOE_NOALLOC_SCRATCH_BYTES)
+        return fail(MOE_ERR_WORKSPACE,
+                    "moe_forward_noalloc: this shape needs %zu bytes of scratch, more than the fixed %llu; "
+                    "use moe_forward with a workspace",
+                    need, static_cast<unsigned long long>(MOE_NOALLOC_SCRATCH_BYTES));
+    int sms;
+    if ((rc = check_device(&sms))) return rc;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    void* ws = nullptr;
+    if ((rc = noalloc_scratch(dev, &ws))) return rc;
+    return run_layer(x, logits, w_gate_up, w_down, T, d, f, E, top_k, out, ws, sms,
+                     static_cast<cudaStream_t>(stream));
 }
 
 int moe_get_device_error(const void* status_or_workspace, int32_t* code) {
