@@ -62,7 +62,8 @@ extern "C" {
 typedef void* moe_stream_t; /* a cudaStream_t */
 
 /* Bytes of scratch that moe_forward needs for this shape (256-byte aligned pieces: status word,
- * idx, w, counts, offsets, src, dest, x_perm bf16 [T*k,d], h bf16 [T*k,f], y_perm fp32 [T*k,d]).
+ * idx, w, counts, offsets, src, dest, x_perm bf16 [T*k,d], h bf16 [T*k,f], y_perm fp32
+ * [moe_down_ksplit(), T*k, d]).
  * Returns 0 for an invalid shape. */
 MOE_API size_t moe_workspace_size(int T, int d, int f, int E, int top_k);
 
@@ -106,26 +107,39 @@ MOE_API int moe_permute(const int32_t* idx, const void* x, int T, int d, int E, 
  *   status: device int32 or NULL (MOE_STATUS_BAD_OFFSETS, MOE_STATUS_WAIT_TIMEOUT).
  * "Triton-MoE-Dispatch-Kernel erreicht 131 % von Megablocks" (lumeric.app), article body;
  * block-scheduled grouped GEMM over variable expert batches: "Triton MoE 核心擊敗 Megablocks",
- * section 關鍵要點; persistent kernel hiding prologue/epilogue: HPC-Ops page. */
+ * section 關鍵要點; persistent kernel hiding prologue/epilogue: HPC-Ops page.
+ * Experts with at most 64 rows (environment MOE_GEMM_SWAP_MAX overrides; 0 = never) run with
+ * A and B swapped — weights as the tensor-core M operand, the expert's rows as N — as in
+ * "dynamic swap A/B" of the DeepGEMM PR #304 write-up, section 3.2; results are the same. */
 MOE_API int moe_grouped_gemm_gateup_swiglu(const void* x_perm, const void* w_gate_up,
                                    const int32_t* offsets, int M, int d, int f, int E, void* h,
                                    int32_t* status, moe_stream_t stream);
 
 /* Step 4 — grouped down-projection GEMM: y_perm[r] = h[r] . W_down[e] (fp32 accumulation) for
- * r in expert e's segment.
- *   h [M,f] bf16 in;  w_down [E,f,d] bf16 in;  offsets [E+1] int32 in;  y_perm [M,d] fp32 out;
- *   status as for step 3.
+ * r in expert e's segment.  With ksplit > 1 the reduction over f is split into ksplit contiguous
+ * ranges of 64-wide blocks and y_perm receives ksplit partial sums, slice s at y_perm + s*M*d;
+ * y_perm[r] is their sum (moe_combine adds them in slice order).  A slice past the end of f holds
+ * zeros.
+ *   h [M,f] bf16 in;  w_down [E,f,d] bf16 in;  offsets [E+1] int32 in;  ksplit in [1, 8];
+ *   y_perm [ksplit, M, d] fp32 out;  status as for step 3.
  * DeepGEMM PR #304 write-up, section 1.1 ("linear2"); HPC-Ops page (GroupGEMM). */
 MOE_API int moe_grouped_gemm_down(const void* h, const void* w_down, const int32_t* offsets, int M, int d,
-                          int f, int E, float* y_perm, int32_t* status, moe_stream_t stream);
+                          int f, int E, int ksplit, float* y_perm, int32_t* status, moe_stream_t stream);
+
+/* The ksplit that moe_forward uses for the down projection of this layer shape (2 when the
+ * down projection has between one and two waves of 128x256 work items on a 152-SM GPU, else 1);
+ * 0 for an invalid shape.  The environment variable MOE_DOWN_KSPLIT, if set, overrides it. */
+MOE_API int moe_down_ksplit(int T, int d, int f, int E, int top_k);
 
 /* Step 5 — weighted combine (unpermute): out[t] = bf16( sum_{j=0..top_k-1} w[t,j] *
  * y_perm[dest[t,j]] ), fp32 sums in slot order; no atomics, so the result is deterministic.
- *   y_perm [T*top_k, d] fp32 in;  w [T,top_k] fp32 in;  dest [T,top_k] int32 in;
- *   out [T,d] bf16 out;  status: device int32 or NULL (MOE_STATUS_BAD_DEST).
+ * y_perm may hold ksplit partial slices from moe_grouped_gemm_down; each row is the sum of its
+ * slices, added in slice order.
+ *   y_perm [ksplit, T*top_k, d] fp32 in;  w [T,top_k] fp32 in;  dest [T,top_k] int32 in;
+ *   ksplit in [1, 8];  out [T,d] bf16 out;  status: device int32 or NULL (MOE_STATUS_BAD_DEST).
  * DeepGEMM PR #304 write-up, section 1.1 ("combine"); HPC-Ops page (weighted-average reduce). */
 MOE_API int moe_combine(const float* y_perm, const float* w, const int32_t* dest, int T, int d, int top_k,
-                void* out, int32_t* status, moe_stream_t stream);
+                int ksplit, void* out, int32_t* status, moe_stream_t stream);
 
 /* The whole layer in one call: steps 1-5 as five kernel launches on `stream`, intermediates
  * carved from `workspace` (device, >= moe_workspace_size() bytes, 256-byte aligned).
@@ -162,7 +176,7 @@ MOE_API int moe_forward_host(const void* x_host, const float* logits_host, const
  * The intermediates live in one file-scope device array of MOE_NOALLOC_SCRATCH_BYTES that every
  * GPU loading this library holds until the process exits.  Shapes whose moe_workspace_size()
  * exceeds it are rejected with MOE_ERR_WORKSPACE (e.g. the Mixtral-8x7B shape fits up to
- * T = 512 tokens with top-2).  The first call on a device looks up the array's device address
+ * T = 256 tokens with top-2).  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream
  * capture.  All calls on a device share the one array and it keeps the last call's contents
  * (every intermediate is rewritten before it is read; the status word is reset by the first

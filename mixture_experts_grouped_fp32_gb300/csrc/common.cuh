@@ -14,19 +14,53 @@ __device__ __forceinline__ void flag_status(int32_t* status, int32_t bit) {
     if (status) atomicOr(status, bit);
 }
 
+// Programmatic dependent launch.  Every kernel of the layer calls pdl_wait() before its first
+// global-memory access, which waits for the previous kernel in the stream to finish and its
+// writes to become visible (a no-op when the launch had no programmatic dependency); so the
+// stream order of all reads and writes is kept, while the launch and the shared-memory /
+// tensor-memory set-up of a kernel overlap the tail of the one before.  pdl_trigger() lets the
+// next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Launchers (defined next to their kernels).  All return cudaGetLastError() of the launch.
+// Kernels of the layer, as bits of the programmatic-launch mask.
+enum PdlKernel { kPdlRoute = 1, kPdlPermute = 2, kPdlGateUp = 4, kPdlDown = 8, kPdlCombine = 16 };
+
+// Whether a kernel is launched with the programmatic-stream-serialization attribute (see
+// pdl_wait).  The environment variable MOE_PDL, a bit mask of PdlKernel, overrides the default.
+bool pdl_enabled(int kernel_bit);
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(int kernel_bit, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled(kernel_bit) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Launchers (defined next to their kernels).  All return the launch's error code.
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                          int32_t* status_reset, cudaStream_t s);
 cudaError_t launch_permute(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
                            int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest,
                            __nv_bfloat16* x_perm, int32_t* status, int num_sms, cudaStream_t s);
 cudaError_t launch_combine(const float* y, const float* w, const int32_t* dest, int T, int d, int k,
-                           __nv_bfloat16* out, int32_t* status, cudaStream_t s);
+                           int ksplit, __nv_bfloat16* out, int32_t* status, cudaStream_t s);
+
+// Largest number of K slices the down projection may be split into.
+constexpr int kMaxKSplit = 8;
 
 // Grouped GEMMs.  `kind` selects the fused gate+up+SwiGLU (0) or the down projection (1).
 struct GemmArgs {
@@ -34,8 +68,10 @@ struct GemmArgs {
     const void* B;         // W_gate_up [E,K,2N] or W_down [E,K,N], bf16
     const int32_t* offsets;  // [E+1]
     int M, K, N, E;        // N = output features (f for gate+up, d for down)
-    void* out;             // h [M,N] bf16 or y_perm [M,N] fp32
+    void* out;             // h [M,N] bf16, or y_perm [ksplit, M, N] fp32 partial sums
     int32_t* status;
+    int ksplit;            // K slices (down only; 1 = no split)
+    int swap_max;          // experts with at most this many rows use the swapped orientation
 };
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                 const char** why);

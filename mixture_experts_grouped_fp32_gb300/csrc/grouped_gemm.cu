@@ -5,30 +5,44 @@
 //           (K = d), h[r] = bf16(silu(g) * u).  The fp32 g and u exist only in tensor memory —
 //           the gate/up fusion that keeps the SwiGLU intermediate out of global memory
 //           ("Triton-MoE-Dispatch-Kernel erreicht 131 % von Megablocks", lumeric.app).
-//   kind 1, down: y_perm[r] = h[r] . W_down[e] (K = f), fp32 out.
+//   kind 1, down: y_perm[r] = h[r] . W_down[e] (K = f), fp32 out, optionally split over K into
+//           `ksplit` partial slices that the combine step adds in a fixed order.
 //
 // Work decomposition ("block-scheduled grouped GEMM for variable expert batches":
 // "Triton MoE 核心擊敗 Megablocks", setupai.cc, section 關鍵要點).  Expert e's rows form
-// ceil(count_e / 128) M-tiles; each (expert, N-tile, M-tile) is one work item of identical cost
-// (same K, full 128x256 MMA tile), so a static round-robin over a persistent grid of one CTA per
-// SM balances any expert skew up to one item.  Items are numbered expert-major, then N-tile,
-// then M-tile, so CTAs that run together share a weight tile (in L2) and an expert's activation
-// rows stay L2-resident while its N-tiles sweep ("persistent cache-aware" strategy:
-// "Triton-Optimierter BF16 Grouped GEMM Kernel beschleunigt MoE-Modelle", meineki.news).  The
-// persistent kernel overlaps one tile's epilogue with the next tile's main loop through two
-// tensor-memory accumulators (HPC-Ops page: persistent kernels hide prologue/epilogue cost).
+// ceil(count_e / 128) M-tiles; each (expert, N-tile, M-tile, K-slice) is one work item, and items
+// of one launch all cost the same weight bytes, so a static round-robin over a persistent grid of
+// one CTA per SM balances any expert skew to within one item.  Items are numbered expert-major,
+// then N-tile, M-tile, K-slice, so CTAs that run together share a weight tile (in L2) and an
+// expert's activation rows stay L2-resident while its N-tiles sweep ("persistent cache-aware"
+// strategy: "Triton-Optimierter BF16 Grouped GEMM Kernel beschleunigt MoE-Modelle",
+// meineki.news).  Two tensor-memory accumulators let one item's epilogue overlap the next item's
+// main loop (HPC-Ops page: persistent kernels hide prologue/epilogue cost).
+//
+// Two operand orientations, chosen per item from the expert's row count on the device:
+//   normal   UMMA M = 128 activation rows, N = 256 weight columns (the expert has > swap_max rows)
+//   swap-AB  UMMA M = 128 weight columns, N = the expert's rows rounded up to 16 (<= swap_max):
+//            the weights become the A operand so a small expert costs an N=16..128 MMA instead
+//            of a mostly empty 128-row tile, and only ceil(rows/32) 32-row activation boxes are
+//            loaded (DeepGEMM write-up, section 3.2, "dynamic swap A/B": B^T . A^T puts the large,
+//            regular weight dimension on the UMMA M side).
 //
 // Roles (warp specialisation as in the DeepGEMM write-up, section 1.2, technique 2, without the
 // communication role): warp 0 lane 0 issues TMA loads into a 4-stage ring; warp 1 owns tensor
-// memory and lane 0 issues tcgen05.mma; warps 2-5 (128 threads, one accumulator row each) run
+// memory and lane 0 issues tcgen05.mma; warps 2-5 (128 threads, one accumulator lane each) run
 // the epilogue.  Every wait is bounded (1 s) and reports MOE_STATUS_WAIT_TIMEOUT instead of
 // hanging.
 //
-// Shared-memory operand layouts (128-byte swizzle, as written by TMA with SWIZZLE_128B):
-//   A (activations, K-major): 128 rows x 64 K, row pitch 128 B, 8-row groups 1024 B apart.
-//   B (weights [K, N] with N contiguous, i.e. MN-major): four 64-column boxes of 64 K-rows,
-//     8 KB apart; inside a box, K-row pitch 128 B, 8-row groups 1024 B apart.
-//   UMMA: M = 128, N = 256, K = 16 per instruction, fp32 accumulator = 256 TMEM columns.
+// Shared-memory stage (128-byte swizzle, as written by TMA with SWIZZLE_128B), 48 KB:
+//   activations, K-major: up to 128 rows x 64 K, row pitch 128 B, 8-row groups 1024 B apart.
+//   weights ([K, N] with N contiguous, i.e. MN-major): four 64-column boxes of 64 K-rows, 8 KB
+//     apart; inside a box, K-row pitch 128 B, 8-row groups 1024 B apart.  For kind 0 the boxes
+//     hold gate columns n0..n0+127 then up columns f+n0..f+n0+127.
+//   normal mode: one M=128 x N=256 MMA per 16-deep K step into a 256-column fp32 accumulator
+//     (kind 0: columns 0-127 gate, 128-255 up).
+//   swap mode: two M=128 x N=rows16 MMAs per K step, weight boxes 0-1 and 2-3 as A, into
+//     accumulator columns [0, N) and [128, 128+N) (kind 0: gate and up; kind 1: output columns
+//     n0..n0+127 and n0+128..n0+255).
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -37,11 +51,13 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;                         // tile rows = UMMA M
+constexpr int BM = 128;                         // activation rows per M-tile
 constexpr int BK = 64;                          // K per stage (one 128-byte swizzle row)
 constexpr int UMMA_K = 16;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int A_BOX32_ROWS = 32;                // activation box height in swap mode
+constexpr int A_BOX32_BYTES = A_BOX32_ROWS * BK * 2;  // 4 KB
 constexpr int B_BOX_N = 64;
 constexpr int B_BOXES = 4;
 constexpr int B_BOX_BYTES = B_BOX_N * BK * 2;   // 8 KB
@@ -53,6 +69,7 @@ constexpr int NUM_ACC = 2;
 constexpr int TMEM_COLS = NUM_ACC * ACC_COLS;   // 512
 constexpr int NUM_THREADS = 192;
 constexpr int MAX_E = 256;
+constexpr int SWAP_MAX_ROWS = 128;              // swap mode needs N = rows16 <= 128
 // The whole opt-in shared memory of an SM: one CTA per SM, and any descriptor mistake would
 // still read inside this CTA's own allocation.
 constexpr int SMEM_BYTES = 232448;
@@ -72,10 +89,12 @@ struct Ctl {
 static_assert(STAGES * STAGE_BYTES + 1024 + sizeof(Ctl) <= SMEM_BYTES, "shared memory budget");
 
 struct Item {
-    int e, n_tile, m_tile, row0, rows;
+    int e, n_tile, m_tile, kslice, row0, rows;
+    bool swap;
 };
 
-__device__ __forceinline__ Item decode_item(const Ctl& c, int E, int i) {
+// Items of expert e: ceil(count / BM) M-tiles x n_tiles x ksplit, ordered N-tile, M-tile, K-slice.
+__device__ __forceinline__ Item decode_item(const Ctl& c, int E, int ksplit, int swap_max, int i) {
     int lo = 0, hi = E;  // item_start[lo] <= i < item_start[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -86,10 +105,14 @@ __device__ __forceinline__ Item decode_item(const Ctl& c, int E, int i) {
     const int cnt = c.seg[lo + 1] - c.seg[lo];
     const int mt = (cnt + BM - 1) / BM;
     const int j = i - c.item_start[lo];
-    it.n_tile = j / mt;
-    it.m_tile = j - it.n_tile * mt;
+    const int per_n = mt * ksplit;
+    it.n_tile = j / per_n;
+    const int r = j - it.n_tile * per_n;
+    it.m_tile = r / ksplit;
+    it.kslice = r - it.m_tile * ksplit;
     it.row0 = c.seg[lo] + it.m_tile * BM;
     it.rows = min(BM, cnt - it.m_tile * BM);
+    it.swap = cnt <= swap_max;
     return it;
 }
 
@@ -102,13 +125,19 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return g / (1.0f + __expf(-g)) * u;
 }
 
-// KIND 0: gate+up+SwiGLU (output tile = 128 h columns, B boxes = gate n0, n0+64, up f+n0, f+n0+64)
-// KIND 1: down             (output tile = 256 y columns, B boxes = n0 + 64 q)
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+    __nv_bfloat16 b = __float2bfloat16_rn(v);
+    return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// KIND 0: gate+up+SwiGLU (output tile = 128 h columns; weight boxes gate n0, n0+64, up f+n0, f+n0+64)
+// KIND 1: down             (output tile = 256 y columns; weight boxes n0 + 64 q)
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const int32_t* __restrict__ offsets, int M, int K, int N, int E,
-                    void* __restrict__ out, int32_t* __restrict__ status) {
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
+                    const __grid_constant__ CUtensorMap tmB, const int32_t* __restrict__ offsets, int M,
+                    int K, int N, int E, int ksplit, int swap_max, void* __restrict__ out,
+                    int32_t* __restrict__ status) {
     constexpr int BN_OUT = KIND == 0 ? 128 : 256;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -119,6 +148,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_tiles = (N + BN_OUT - 1) / BN_OUT;
     const int num_kb = K / BK;
+    const int kb_per = (num_kb + ksplit - 1) / ksplit;  // K blocks per slice (host: no empty slice)
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -136,12 +166,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmA32);
         ptx::prefetch_tensormap(&tmB);
     }
     if (warp == 1) {
         ptx::tmem_alloc(&c.tmem_base, TMEM_COLS);
         ptx::tmem_relinquish();
     }
+    // Everything above touched only this CTA's shared and tensor memory; from here on global
+    // memory written by the previous kernel is read, so wait for it (programmatic launch).
+    pdl_wait();
+    pdl_trigger();
     if (warp == 2) {
         // Validate offsets and build the per-expert item prefix (8 experts per lane).
         for (int e = lane; e <= E; e += 32) c.seg[e] = __ldg(offsets + e);
@@ -152,9 +187,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         ok = __all_sync(0xffffffffu, ok);
         const int per = (E + 31) / 32;
         const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+        const int per_tile = n_tiles * ksplit;
         int sum = 0;
         if (ok)
-            for (int e = e0; e < e1; ++e) sum += ((c.seg[e + 1] - c.seg[e] + BM - 1) / BM) * n_tiles;
+            for (int e = e0; e < e1; ++e) sum += ((c.seg[e + 1] - c.seg[e] + BM - 1) / BM) * per_tile;
         int incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -164,7 +200,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         int run = incl - sum;
         for (int e = e0; e < e1; ++e) {
             c.item_start[e] = run;
-            if (ok) run += ((c.seg[e + 1] - c.seg[e] + BM - 1) / BM) * n_tiles;
+            if (ok) run += ((c.seg[e + 1] - c.seg[e] + BM - 1) / BM) * per_tile;
         }
         if (lane == 31) {
             c.item_start[E] = incl;
@@ -188,10 +224,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint32_t stage = 0, phase = 0;
         bool aborted = false;
         for (int i = blockIdx.x; i < total && !aborted; i += gridDim.x) {
-            const Item it = decode_item(c, E, i);
+            const Item it = decode_item(c, E, ksplit, swap_max, i);
             const int n0 = it.n_tile * BN_OUT;
             const int brow = it.e * K;
-            for (int kb = 0; kb < num_kb; ++kb) {
+            const int nbox32 = (it.rows + A_BOX32_ROWS - 1) / A_BOX32_ROWS;
+            const uint32_t tx = it.swap ? B_BYTES + nbox32 * A_BOX32_BYTES : STAGE_BYTES;
+            const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!ptx::mbar_wait(&c.empty[stage], phase ^ 1u, abort_flag)) {
                     raise_abort(c, status);
                     aborted = true;
@@ -199,8 +238,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 uint8_t* sa = tiles + stage * STAGE_BYTES;
                 uint8_t* sb = sa + A_BYTES;
-                ptx::mbar_arrive_expect_tx(&c.full[stage], STAGE_BYTES);
-                ptx::tma_load_2d(sa, &tmA, &c.full[stage], kb * BK, it.row0, pol_act);
+                ptx::mbar_arrive_expect_tx(&c.full[stage], tx);
+                if (it.swap) {
+                    for (int q = 0; q < nbox32; ++q)
+                        ptx::tma_load_2d(sa + q * A_BOX32_BYTES, &tmA32, &c.full[stage], kb * BK,
+                                         it.row0 + q * A_BOX32_ROWS, pol_act);
+                } else {
+                    ptx::tma_load_2d(sa, &tmA, &c.full[stage], kb * BK, it.row0, pol_act);
+                }
 #pragma unroll
                 for (int q = 0; q < B_BOXES; ++q) {
                     int col;
@@ -219,17 +264,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------ MMA issuer ------------------------------
-        constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, UMMA_N, /*a_mn=*/0, /*b_mn=*/1);
+        constexpr uint32_t idesc_normal = ptx::idesc_bf16_f32(BM, UMMA_N, /*a_mn=*/0, /*b_mn=*/1);
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool aborted = false;
         for (int i = blockIdx.x; i < total && !aborted; i += gridDim.x) {
+            const Item it = decode_item(c, E, ksplit, swap_max, i);
+            const uint32_t ntok = (static_cast<uint32_t>(it.rows) + 15u) & ~15u;
+            const uint32_t idesc_swap = ptx::idesc_bf16_f32(BM, ntok, /*a_mn=*/1, /*b_mn=*/0);
+            const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
             if (!ptx::mbar_wait(&c.tempty[acc], acc_phase ^ 1u, abort_flag)) {
                 raise_abort(c, status);
                 break;
             }
             ptx::tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-            for (int kb = 0; kb < num_kb; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!ptx::mbar_wait(&c.full[stage], phase, abort_flag)) {
                     raise_abort(c, status);
                     aborted = true;
@@ -237,14 +286,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 ptx::tc_fence_after();
                 const uint32_t sa = ptx::smem_u32(tiles + stage * STAGE_BYTES);
-                const uint64_t a_desc = ptx::smem_desc_sw128(sa, 16, 1024);
-                const uint64_t b_desc = ptx::smem_desc_sw128(sa + A_BYTES, B_BOX_BYTES, 1024);
+                // Activations: K-major, +32 B per 16 K.  Weights: MN-major (atoms 8 KB apart along
+                // N/M, 8-row K groups 1 KB apart), +16 rows * 128 B = 2 KB per 16 K.
+                const uint64_t act_desc = ptx::smem_desc_sw128(sa, 16, 1024);
+                const uint64_t wgt_desc = ptx::smem_desc_sw128(sa + A_BYTES, B_BOX_BYTES, 1024);
+                const uint64_t wgt_hi_desc = ptx::smem_desc_sw128(sa + A_BYTES + 2 * B_BOX_BYTES, B_BOX_BYTES, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                    // K-major A: +32 bytes per 16 K; MN-major B: +16 rows * 128 bytes per 16 K.
-                    ptx::mma_bf16_ss(d_tmem, a_desc + static_cast<uint64_t>((kk * 32) >> 4),
-                                     b_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc,
-                                     (kb | kk) != 0 ? 1u : 0u);
+                    const uint32_t accum = (kb != kb0 || kk != 0) ? 1u : 0u;
+                    const uint64_t a_off = static_cast<uint64_t>((kk * 32) >> 4);
+                    const uint64_t w_off = static_cast<uint64_t>((kk * 2048) >> 4);
+                    if (it.swap) {
+                        ptx::mma_bf16_ss(d_tmem, wgt_desc + w_off, act_desc + a_off, idesc_swap, accum);
+                        ptx::mma_bf16_ss(d_tmem + 128, wgt_hi_desc + w_off, act_desc + a_off, idesc_swap, accum);
+                    } else {
+                        ptx::mma_bf16_ss(d_tmem, act_desc + a_off, wgt_desc + w_off, idesc_normal, accum);
+                    }
                 }
                 ptx::mma_commit(&c.empty[stage]);  // frees the stage once these MMAs finish
                 if (++stage == STAGES) {
@@ -265,56 +322,92 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int r_local = quarter * 32 + lane;
         uint32_t acc = 0, acc_phase = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x) {
-            const Item it = decode_item(c, E, i);
+            const Item it = decode_item(c, E, ksplit, swap_max, i);
             if (!ptx::mbar_wait(&c.tfull[acc], acc_phase, abort_flag)) {
                 raise_abort(c, status);
                 break;
             }
             ptx::tc_fence_after();
-            const bool row_ok = r_local < it.rows;
-            const size_t grow = static_cast<size_t>(it.row0 + r_local);
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * ACC_COLS;
             const int n0 = it.n_tile * BN_OUT;
-            if (KIND == 0) {
-                __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(out);
+            // A K-slice past the last K block (ksplit not dividing K evenly) contributes zeros.
+            const bool kfull = it.kslice * kb_per < num_kb;
+            if (it.swap) {
+                // Accumulator lane = weight column (n0 + r_local [+128]), accumulator column = row.
+                const int nchunk = (it.rows + 31) / 32;
+                const int col0 = n0 + r_local;
 #pragma unroll 1
-                for (int cc = 0; cc < BN_OUT / 32; ++cc) {
-                    uint32_t g[32], u[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + cc * 32, g);
-                    ptx::tmem_ld_32x32b_x32(taddr + 128 + cc * 32, u);
+                for (int cc = 0; cc < nchunk; ++cc) {
+                    uint32_t a0[32], a1[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + cc * 32, a0);
+                    ptx::tmem_ld_32x32b_x32(taddr + 128 + cc * 32, a1);
                     ptx::tmem_ld_wait();
-                    const int col = n0 + cc * 32;
-                    if (row_ok && col < N) {
-                        uint4* dst = reinterpret_cast<uint4*>(h + grow * N + col);
+                    const int nrow = min(32, it.rows - cc * 32);
+                    const size_t row_base = static_cast<size_t>(it.row0 + cc * 32);
+                    if (KIND == 0) {
+                        uint16_t* h = reinterpret_cast<uint16_t*>(out);
+                        if (col0 < N) {
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 o;
-                            o.x = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 0]), __uint_as_float(u[8 * v + 0])),
-                                              silu_mul(__uint_as_float(g[8 * v + 1]), __uint_as_float(u[8 * v + 1])));
-                            o.y = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 2]), __uint_as_float(u[8 * v + 2])),
-                                              silu_mul(__uint_as_float(g[8 * v + 3]), __uint_as_float(u[8 * v + 3])));
-                            o.z = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 4]), __uint_as_float(u[8 * v + 4])),
-                                              silu_mul(__uint_as_float(g[8 * v + 5]), __uint_as_float(u[8 * v + 5])));
-                            o.w = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 6]), __uint_as_float(u[8 * v + 6])),
-                                              silu_mul(__uint_as_float(g[8 * v + 7]), __uint_as_float(u[8 * v + 7])));
-                            dst[v] = o;
+                            for (int j = 0; j < 32; ++j)
+                                if (j < nrow)
+                                    h[(row_base + j) * N + col0] =
+                                        bf16_bits(silu_mul(__uint_as_float(a0[j]), __uint_as_float(a1[j])));
                         }
+                    } else {
+                        float* y = reinterpret_cast<float*>(out) + static_cast<size_t>(it.kslice) * M * N;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nrow) {
+                                if (col0 < N) y[(row_base + j) * N + col0] = (kfull ? __uint_as_float(a0[j]) : 0.0f);
+                                if (col0 + 128 < N) y[(row_base + j) * N + col0 + 128] = (kfull ? __uint_as_float(a1[j]) : 0.0f);
+                            }
                     }
                 }
             } else {
-                float* y = reinterpret_cast<float*>(out);
+                // Accumulator lane = row (row0 + r_local), accumulator column = output column.
+                const bool row_ok = r_local < it.rows;
+                const size_t grow = static_cast<size_t>(it.row0 + r_local);
+                if (KIND == 0) {
+                    __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(out);
 #pragma unroll 1
-                for (int cc = 0; cc < BN_OUT / 32; ++cc) {
-                    uint32_t v32[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + cc * 32, v32);
-                    ptx::tmem_ld_wait();
-                    const int col = n0 + cc * 32;
-                    if (row_ok && col < N) {
-                        float4* dst = reinterpret_cast<float4*>(y + grow * N + col);
+                    for (int cc = 0; cc < BN_OUT / 32; ++cc) {
+                        uint32_t g[32], u[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + cc * 32, g);
+                        ptx::tmem_ld_32x32b_x32(taddr + 128 + cc * 32, u);
+                        ptx::tmem_ld_wait();
+                        const int col = n0 + cc * 32;
+                        if (row_ok && col < N) {
+                            uint4* dst = reinterpret_cast<uint4*>(h + grow * N + col);
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            dst[v] = make_float4(__uint_as_float(v32[4 * v]), __uint_as_float(v32[4 * v + 1]),
-                                                 __uint_as_float(v32[4 * v + 2]), __uint_as_float(v32[4 * v + 3]));
+                            for (int v = 0; v < 4; ++v) {
+                                uint32_t p[4];
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    p[q] = pack_bf16x2(
+                                        silu_mul(__uint_as_float(g[8 * v + 2 * q]), __uint_as_float(u[8 * v + 2 * q])),
+                                        silu_mul(__uint_as_float(g[8 * v + 2 * q + 1]),
+                                                 __uint_as_float(u[8 * v + 2 * q + 1])));
+                                dst[v] = make_uint4(p[0], p[1], p[2], p[3]);
+                            }
+                        }
+                    }
+                } else {
+                    float* y = reinterpret_cast<float*>(out) + static_cast<size_t>(it.kslice) * M * N;
+#pragma unroll 1
+                    for (int cc = 0; cc < BN_OUT / 32; ++cc) {
+                        uint32_t v32[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + cc * 32, v32);
+                        ptx::tmem_ld_wait();
+                        const int col = n0 + cc * 32;
+                        if (row_ok && col < N) {
+                            float4* dst = reinterpret_cast<float4*>(y + grow * N + col);
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                dst[v] = make_float4((kfull ? __uint_as_float(v32[4 * v]) : 0.0f),
+                                                     (kfull ? __uint_as_float(v32[4 * v + 1]) : 0.0f),
+                                                     (kfull ? __uint_as_float(v32[4 * v + 2]) : 0.0f),
+                                                     (kfull ? __uint_as_float(v32[4 * v + 3]) : 0.0f));
+                        }
                     }
                 }
             }
@@ -391,22 +484,27 @@ cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const ch
         }
         attr_set[dev] = true;
     }
-    CUtensorMap mA, mB;
+    CUtensorMap mA, mA32, mB;
     const uint64_t bcols = KIND == 0 ? 2ull * a.N : static_cast<uint64_t>(a.N);
-    if (!make_map(&mA, a.A, a.K, a.M, BM) ||
+    if (!make_map(&mA, a.A, a.K, a.M, BM) || !make_map(&mA32, a.A, a.K, a.M, A_BOX32_ROWS) ||
         !make_map(&mB, a.B, bcols, static_cast<uint64_t>(a.E) * a.K, BK)) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or bad operand)";
         return cudaErrorInvalidValue;
     }
-    grouped_gemm_kernel<KIND><<<num_sms, NUM_THREADS, SMEM_BYTES, s>>>(
-        mA, mB, a.offsets, a.M, a.K, a.N, a.E, a.out, a.status);
-    return cudaGetLastError();
+    const int swap_max = a.swap_max < 0 ? 0 : (a.swap_max > SWAP_MAX_ROWS ? SWAP_MAX_ROWS : a.swap_max);
+    const int ksplit = KIND == 0 ? 1 : a.ksplit;
+    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_kernel<KIND>, dim3(num_sms), dim3(NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB,
+                    a.offsets, a.M, a.K, a.N, a.E, ksplit, swap_max, a.out, a.status);
 }
 
 }  // namespace
 
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                 const char** why) {
+    if (a.ksplit < 1 || a.ksplit > kMaxKSplit || (kind == 0 && a.ksplit != 1)) {
+        *why = "ksplit must be 1 for gate+up and in [1, 8] for down";
+        return cudaErrorInvalidValue;
+    }
     return kind == 0 ? launch_kind<0>(a, num_sms, s, why) : launch_kind<1>(a, num_sms, s, why);
 }
 

@@ -1,6 +1,7 @@
 // moe_api.cu — the extern "C" entry points declared in include/moe.h: argument checks (before
 // any CUDA call), device checks, workspace carving and the stream-ordered launches.
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <mutex>
 
@@ -76,6 +77,56 @@ int launched(cudaError_t e, const char* what) {
     return ok();
 }
 
+}  // namespace
+
+// Default: every launch but the permute's.  Measured on GB300 (ms per layer, all five = 0.4197 at
+// Mixtral T=32 against 0.4277 with none; but a programmatic permute launch costs the DeepSeek-
+// shaped layer 0.09 ms: 2.545 with only that bit against 2.454 with none).
+bool pdl_enabled(int kernel_bit) {
+    static const int mask = [] {
+        const char* v = std::getenv("MOE_PDL");
+        return v ? std::atoi(v) : (kPdlRoute | kPdlGateUp | kPdlDown | kPdlCombine);
+    }();
+    return (mask & kernel_bit) != 0;
+}
+
+namespace {
+
+// Experts with at most this many rows run the grouped GEMMs in the swapped orientation (weights
+// as the UMMA M operand).  Per 64-deep K block the swapped MMAs read 32 KB of weights plus
+// 256 B per row from shared memory against 48 KB for the normal 128x256 tile, so swapping pays
+// below ~64 rows; measured on GB300 (Mixtral shape, T=512): 64 -> 0.574 ms/layer, 128 ->
+// 0.589 ms.  MOE_GEMM_SWAP_MAX overrides it: 0 turns swapping off, values above 128 clamp to 128.
+int swap_max_rows() {
+    const char* v = std::getenv("MOE_GEMM_SWAP_MAX");
+    int x = v ? std::atoi(v) : 64;
+    return x < 0 ? 0 : (x > 128 ? 128 : x);
+}
+
+// K slices for the down projection of a layer shape.  The down GEMM has d/256 N-tiles per M-tile.
+// When that gives between one and two waves of work items on a 152-SM GB300, the last wave runs
+// on a fraction of the SMs; splitting K in two evens it out (Mixtral shape, T=512: down GEMM
+// 0.209 -> 0.179 ms).  Below one wave each item streams its own weight tile and the SMs in use
+// already saturate HBM, and a split only adds partial-sum traffic (T=32: 0.138 -> 0.142 ms);
+// above two waves the tail is small.  MOE_DOWN_KSPLIT overrides the choice.  The result never
+// leaves a slice without K blocks.
+int down_ksplit(int T, int d, int f, int E, int k) {
+    const long long M = static_cast<long long>(T) * k;
+    const int num_kb = f / 64;
+    int S;
+    if (const char* v = std::getenv("MOE_DOWN_KSPLIT")) {
+        S = std::atoi(v);
+    } else {
+        const long long mtiles = (M + 127) / 128 + (M < E ? M : E);
+        const long long items = mtiles * ((d + 255) / 256);
+        S = (items >= 152 && items < 304) ? 2 : 1;
+    }
+    const int cap = num_kb < kMaxKSplit ? num_kb : kMaxKSplit;
+    S = S < 1 ? 1 : (S > cap ? cap : S);
+    const int per = (num_kb + S - 1) / S;
+    return (num_kb + per - 1) / per;
+}
+
 // moe_forward's workspace: 256-byte aligned pieces in this order.
 struct Layout {
     size_t status, idx, w, counts, offsets, src, dest, x_perm, h, y_perm, total;
@@ -96,7 +147,7 @@ Layout layout(int T, int d, int f, int E, int k) {
     L.dest = o; o = align256(o + M * 4);
     L.x_perm = o; o = align256(o + M * d * 2);
     L.h = o; o = align256(o + M * f * 2);
-    L.y_perm = o; o = align256(o + M * d * 4);
+    L.y_perm = o; o = align256(o + static_cast<size_t>(down_ksplit(T, d, f, E, k)) * M * d * 4);
     L.total = o;
     return L;
 }
@@ -128,13 +179,15 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
                             dest, x_perm, status, num_sms, s)) != cudaSuccess)
         return launched(e, "permute");
     const char* why = "";
-    GemmArgs g1{x_perm, wgu, offsets, M, d, f, E, h, status};
+    const int swap_max = swap_max_rows(), ksplit = down_ksplit(T, d, f, E, k);
+    GemmArgs g1{x_perm, wgu, offsets, M, d, f, E, h, status, 1, swap_max};
     if ((e = launch_grouped_gemm(0, g1, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "gate+up GEMM: %s (%s)", why, cudaGetErrorString(e));
-    GemmArgs g2{h, wd, offsets, M, f, d, E, y, status};
+    GemmArgs g2{h, wd, offsets, M, f, d, E, y, status, ksplit, swap_max};
     if ((e = launch_grouped_gemm(1, g2, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "down GEMM: %s (%s)", why, cudaGetErrorString(e));
-    if ((e = launch_combine(y, w, dest, T, d, k, static_cast<__nv_bfloat16*>(out), status, s)) != cudaSuccess)
+    if ((e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) !=
+        cudaSuccess)
         return launched(e, "combine");
     return ok();
 }
@@ -194,6 +247,11 @@ int moe_workspace_layout(int T, int d, int f, int E, int top_k, size_t* offsets_
     return ok();
 }
 
+int moe_down_ksplit(int T, int d, int f, int E, int top_k) {
+    if (check_shape(T, d, f, E, top_k, true) != MOE_OK) return 0;
+    return down_ksplit(T, d, f, E, top_k);
+}
+
 size_t moe_host_staging_size(int T, int d, int E) {
     if (T < 0 || d < 1 || E < 1) return 0;
     return align256(static_cast<size_t>(T) * d * 2) * 2 + align256(static_cast<size_t>(T) * E * 4);
@@ -229,18 +287,20 @@ int moe_permute(const int32_t* idx, const void* x, int T, int d, int E, int top_
 }
 
 static int gemm_entry(int kind, const void* A, const void* B, const int32_t* offsets, int M, int d, int f,
-                      int E, void* out, int32_t* status, moe_stream_t stream, const char* name) {
+                      int E, int ksplit, void* out, int32_t* status, moe_stream_t stream, const char* name) {
     int rc = check_shape(0, d, f, E, 1, true);
     if (rc) return rc;
     if (M < 0) return fail(MOE_ERR_INVALID_ARG, "%s: M = %d must be >= 0", name, M);
+    if (ksplit < 1 || ksplit > kMaxKSplit)
+        return fail(MOE_ERR_INVALID_ARG, "%s: ksplit = %d outside [1, %d]", name, ksplit, kMaxKSplit);
     if (M == 0) return ok();
     if (!A || !B || !offsets || !out) return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
     if (!aligned16(A) || !aligned16(B) || !aligned16(out))
         return fail(MOE_ERR_INVALID_ARG, "%s: operands must be 16-byte aligned", name);
     int sms;
     if ((rc = check_device(&sms))) return rc;
-    GemmArgs g = kind == 0 ? GemmArgs{A, B, offsets, M, d, f, E, out, status}
-                           : GemmArgs{A, B, offsets, M, f, d, E, out, status};
+    GemmArgs g = kind == 0 ? GemmArgs{A, B, offsets, M, d, f, E, out, status, 1, swap_max_rows()}
+                           : GemmArgs{A, B, offsets, M, f, d, E, out, status, ksplit, swap_max_rows()};
     const char* why = "";
     cudaError_t e = launch_grouped_gemm(kind, g, sms, static_cast<cudaStream_t>(stream), &why);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s (%s)", name, why, cudaGetErrorString(e));
@@ -249,26 +309,28 @@ static int gemm_entry(int kind, const void* A, const void* B, const int32_t* off
 
 int moe_grouped_gemm_gateup_swiglu(const void* x_perm, const void* w_gate_up, const int32_t* offsets, int M,
                                    int d, int f, int E, void* h, int32_t* status, moe_stream_t stream) {
-    return gemm_entry(0, x_perm, w_gate_up, offsets, M, d, f, E, h, status, stream,
+    return gemm_entry(0, x_perm, w_gate_up, offsets, M, d, f, E, 1, h, status, stream,
                       "moe_grouped_gemm_gateup_swiglu");
 }
 
 int moe_grouped_gemm_down(const void* h, const void* w_down, const int32_t* offsets, int M, int d, int f,
-                          int E, float* y_perm, int32_t* status, moe_stream_t stream) {
-    return gemm_entry(1, h, w_down, offsets, M, d, f, E, y_perm, status, stream, "moe_grouped_gemm_down");
+                          int E, int ksplit, float* y_perm, int32_t* status, moe_stream_t stream) {
+    return gemm_entry(1, h, w_down, offsets, M, d, f, E, ksplit, y_perm, status, stream, "moe_grouped_gemm_down");
 }
 
-int moe_combine(const float* y_perm, const float* w, const int32_t* dest, int T, int d, int top_k, void* out,
-                int32_t* status, moe_stream_t stream) {
+int moe_combine(const float* y_perm, const float* w, const int32_t* dest, int T, int d, int top_k, int ksplit,
+                void* out, int32_t* status, moe_stream_t stream) {
     int rc = check_shape(T, d, 0, top_k, top_k, false);
     if (rc) return rc;
     if (T == 0) return ok();
     if (!y_perm || !w || !dest || !out) return fail(MOE_ERR_INVALID_ARG, "moe_combine: null pointer");
+    if (ksplit < 1 || ksplit > kMaxKSplit)
+        return fail(MOE_ERR_INVALID_ARG, "moe_combine: ksplit = %d outside [1, %d]", ksplit, kMaxKSplit);
     if (!aligned16(y_perm) || !aligned16(out))
         return fail(MOE_ERR_INVALID_ARG, "moe_combine: y_perm and out must be 16-byte aligned");
     int sms;
     if ((rc = check_device(&sms))) return rc;
-    return launched(launch_combine(y_perm, w, dest, T, d, top_k, static_cast<__nv_bfloat16*>(out), status,
+    return launched(launch_combine(y_perm, w, dest, T, d, top_k, ksplit, static_cast<__nv_bfloat16*>(out), status,
                                    static_cast<cudaStream_t>(stream)),
                     "combine");
 }

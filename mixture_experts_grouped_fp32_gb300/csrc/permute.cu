@@ -34,6 +34,8 @@ permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int
     __shared__ int bad;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();
+    pdl_trigger();
     for (int e = tid; e < E; e += kPermThreads) {
         tot[e] = 0;
         before[e] = 0;
@@ -132,10 +134,9 @@ cudaError_t launch_permute(const int32_t* idx, const __nv_bfloat16* x, int T, in
     int tpb = (T + 2 * num_sms - 1) / (2 * num_sms);
     tpb = tpb < 1 ? 1 : (tpb > kMaxTokPerBlock ? kMaxTokPerBlock : tpb);
     const int blocks = (T + tpb - 1) / tpb;
-    permute_kernel<<<blocks, kPermThreads, 0, s>>>(
-        idx, reinterpret_cast<const uint4*>(x), T, d, E, k, tpb, counts, offsets, src, dest,
-        reinterpret_cast<uint4*>(x_perm), status);
-    return cudaGetLastError();
+    return launch_k(kPdlPermute, permute_kernel, dim3(blocks), dim3(kPermThreads), 0, s, idx,
+                    reinterpret_cast<const uint4*>(x), T, d, E, k, tpb, counts, offsets, src, dest,
+                    reinterpret_cast<uint4*>(x_perm), status);
 }
 
 }  // namespace moe

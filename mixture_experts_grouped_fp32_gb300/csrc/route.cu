@@ -30,6 +30,8 @@ template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx,
              float* __restrict__ w, int32_t* __restrict__ status_reset) {
+    pdl_wait();
+    pdl_trigger();
     if (status_reset != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *status_reset = 0;
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
@@ -104,14 +106,13 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx,
                          int32_t* status_reset, cudaStream_t s) {
     const dim3 grid((T + kRouteWarps - 1) / kRouteWarps), block(kRouteWarps * 32);
     if (E <= 32)
-        route_kernel<1><<<grid, block, 0, s>>>(logits, T, E, k, idx, w, status_reset);
+        return launch_k(kPdlRoute, route_kernel<1>, grid, block, 0, s, logits, T, E, k, idx, w, status_reset);
     else if (E <= 64)
-        route_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, idx, w, status_reset);
+        return launch_k(kPdlRoute, route_kernel<2>, grid, block, 0, s, logits, T, E, k, idx, w, status_reset);
     else if (E <= 128)
-        route_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, idx, w, status_reset);
+        return launch_k(kPdlRoute, route_kernel<4>, grid, block, 0, s, logits, T, E, k, idx, w, status_reset);
     else
-        route_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, idx, w, status_reset);
-    return cudaGetLastError();
+        return launch_k(kPdlRoute, route_kernel<8>, grid, block, 0, s, logits, T, E, k, idx, w, status_reset);
 }
 
 }  // namespace moe

@@ -29,8 +29,10 @@ _SIGS = {
     "moe_route": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_permute": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_gateup_swiglu": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
-    "moe_grouped_gemm_down": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
-    "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_grouped_gemm_down": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
+    "moe_down_ksplit": ([_I, _I, _I, _I, _I], _I),
+    "moe_combine": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "moe_forward_noalloc": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "moe_forward": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "moe_forward_host": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "moe_get_device_error": ([_P, ctypes.POINTER(ctypes.c_int32)], _I),
@@ -154,26 +156,41 @@ def grouped_gemm_gateup_swiglu(x_perm, w_gate_up, offsets, h=None, status=None, 
     return h
 
 
-def grouped_gemm_down(h, w_down, offsets, y_perm=None, status=None, stream=None):
+def down_ksplit(T: int, d: int, f: int, E: int, top_k: int) -> int:
+    """K slices moe_forward uses for the down projection of this shape."""
+    return int(load().moe_down_ksplit(T, d, f, E, top_k))
+
+
+def grouped_gemm_down(h, w_down, offsets, y_perm=None, status=None, stream=None, ksplit: int = 1):
+    """y_perm [ksplit, M, d] fp32 partial sums (a [M, d] view when ksplit == 1)."""
     _dev(h, torch.bfloat16, "h")
     _dev(w_down, torch.bfloat16, "w_down")
     _dev(offsets, torch.int32, "offsets")
     M, f = h.shape
     E, _, d = w_down.shape
-    y_perm = y_perm if y_perm is not None else torch.empty(M, d, dtype=torch.float32, device=h.device)
-    _call("moe_grouped_gemm_down", _ptr(h), _ptr(w_down), _ptr(offsets), M, d, f, E, _ptr(y_perm),
+    if y_perm is None:
+        y_perm = torch.empty(ksplit, M, d, dtype=torch.float32, device=h.device)
+        if ksplit == 1:
+            y_perm = y_perm[0]
+    if y_perm.numel() < ksplit * M * d:
+        raise ValueError("y_perm must hold ksplit * M * d floats")
+    _call("moe_grouped_gemm_down", _ptr(h), _ptr(w_down), _ptr(offsets), M, d, f, E, ksplit, _ptr(y_perm),
           _ptr(status), _stream(stream))
     return y_perm
 
 
-def combine(y_perm, w, dest, out=None, status=None, stream=None):
+def combine(y_perm, w, dest, out=None, status=None, stream=None, ksplit: int = 1):
+    """y_perm is [T*k, d] or [ksplit, T*k, d] partial sums; out bf16 [T, d]."""
     _dev(y_perm, torch.float32, "y_perm")
     _dev(w, torch.float32, "w")
     _dev(dest, torch.int32, "dest")
     T, k = dest.shape
-    d = y_perm.shape[1]
+    d = y_perm.shape[-1]
+    if y_perm.numel() < ksplit * T * k * d:
+        raise ValueError("y_perm must hold ksplit * T * k * d floats")
     out = out if out is not None else torch.empty(T, d, dtype=torch.bfloat16, device=y_perm.device)
-    _call("moe_combine", _ptr(y_perm), _ptr(w), _ptr(dest), T, d, k, _ptr(out), _ptr(status), _stream(stream))
+    _call("moe_combine", _ptr(y_perm), _ptr(w), _ptr(dest), T, d, k, ksplit, _ptr(out), _ptr(status),
+          _stream(stream))
     return out
 
 
@@ -218,6 +235,7 @@ def workspace_views(ws: torch.Tensor, T: int, d: int, f: int, E: int, top_k: int
     """Typed views of moe_forward's intermediates inside ``ws`` (for inspection and tests)."""
     L = workspace_layout(T, d, f, E, top_k)
     M = T * top_k
+    S = down_ksplit(T, d, f, E, top_k)
 
     def view(name, n, dtype, shape):
         nbytes = n * torch.empty((), dtype=dtype).element_size()
@@ -233,7 +251,8 @@ def workspace_views(ws: torch.Tensor, T: int, d: int, f: int, E: int, top_k: int
         "dest": view("dest", M, torch.int32, (T, top_k)),
         "x_perm": view("x_perm", M * d, torch.bfloat16, (M, d)),
         "h": view("h", M * f, torch.bfloat16, (M, f)),
-        "y_perm": view("y_perm", M * d, torch.float32, (M, d)),
+        "y_perm": view("y_perm", S * M * d, torch.float32, (S, M, d)),
+        "ksplit": S,
     }
 
 

@@ -53,10 +53,12 @@ def test_workspace_layout_matches_the_documented_order(lib):
     def up(v):
         return (v + 255) // 256 * 256
 
+    S = moe.down_ksplit(T, d, f, E, k)
+    assert 1 <= S <= 8
     expect, o = {}, 0
     for name, nbytes in [("status", 256), ("idx", M * 4), ("w", M * 4), ("counts", E * 4),
                          ("offsets", (E + 1) * 4), ("src", M * 4), ("dest", M * 4),
-                         ("x_perm", M * d * 2), ("h", M * f * 2), ("y_perm", M * d * 4)]:
+                         ("x_perm", M * d * 2), ("h", M * f * 2), ("y_perm", S * M * d * 4)]:
         expect[name] = o
         o = up(o + nbytes)
     expect["total"] = o
@@ -101,8 +103,11 @@ def test_stage_calls_reject_bad_arguments(lib):
     assert lib.moe_permute(p, ctypes.c_void_p((1 << 20) + 8), 4, 64, 8, 2, p, p, p, p, p, None, None) == -1
     assert lib.moe_grouped_gemm_gateup_swiglu(p, p, None, 8, 64, 128, 8, p, None, None) == -1
     assert lib.moe_grouped_gemm_gateup_swiglu(p, p, p, -1, 64, 128, 8, p, None, None) == -1
-    assert lib.moe_grouped_gemm_down(p, p, p, 8, 64, 96, 8, p, None, None) == -1
-    assert lib.moe_combine(p, p, p, 4, 64, 0, p, None, None) == -1
+    assert lib.moe_grouped_gemm_down(p, p, p, 8, 64, 96, 8, 1, p, None, None) == -1
+    assert lib.moe_grouped_gemm_down(p, p, p, 8, 64, 128, 8, 9, p, None, None) == -1
+    assert "ksplit" in _err(lib)
+    assert lib.moe_combine(p, p, p, 4, 64, 0, 1, p, None, None) == -1
+    assert lib.moe_combine(p, p, p, 4, 64, 2, 0, p, None, None) == -1
     assert lib.moe_get_device_error(None, None) == -1
 
 
@@ -112,8 +117,8 @@ def test_empty_batch_is_a_no_op(lib):
     assert lib.moe_forward(p, p, p, p, 0, 64, 128, 8, 2, p, p, 1 << 40, None) == 0
     assert lib.moe_route(p, 0, 8, 2, p, p, None) == 0
     assert lib.moe_permute(p, p, 0, 64, 8, 2, p, p, p, p, p, None, None) == 0
-    assert lib.moe_grouped_gemm_down(p, p, p, 0, 64, 128, 8, p, None, None) == 0
-    assert lib.moe_combine(p, p, p, 0, 64, 2, p, None, None) == 0
+    assert lib.moe_grouped_gemm_down(p, p, p, 0, 64, 128, 8, 1, p, None, None) == 0
+    assert lib.moe_combine(p, p, p, 0, 64, 2, 1, p, None, None) == 0
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path):
@@ -135,3 +140,24 @@ def test_product_package_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in text and "from oracle" not in text, fn
                 assert "liboracle" not in text and "moe_oracle" not in text, fn
+
+
+def test_down_ksplit_policy(lib):
+    """Few tokens -> the down projection is split over K; many tokens -> no split; never an empty
+    slice; the environment override is honoured and clamped."""
+    from mixture_experts_grouped_fp32_gb300 import moe
+    assert moe.down_ksplit(32, 4096, 14336, 8, 2) == 1
+    assert moe.down_ksplit(512, 4096, 14336, 8, 2) == 2
+    assert moe.down_ksplit(4096, 4096, 14336, 8, 2) == 1
+    assert moe.down_ksplit(2048, 7168, 2048, 256, 8) == 1
+    for T, d, f, E, k in [(1, 64, 64, 8, 2), (64, 256, 512, 8, 2), (37, 192, 320, 4, 4), (512, 4096, 14336, 8, 2)]:
+        S = moe.down_ksplit(T, d, f, E, k)
+        nkb = f // 64
+        per = -(-nkb // S)
+        assert 1 <= S <= min(8, nkb) and (S - 1) * per < nkb
+    os.environ["MOE_DOWN_KSPLIT"] = "3"
+    try:
+        assert moe.down_ksplit(4096, 4096, 14336, 8, 2) == 3
+        assert moe.down_ksplit(4, 64, 128, 8, 2) == 2  # clamped to f/64 = 2 K blocks
+    finally:
+        del os.environ["MOE_DOWN_KSPLIT"]

@@ -51,8 +51,22 @@ def _forward_and_views(moe, w, logits, x, wgu, wd):
     return out, moe.workspace_views(ws, w.T, w.d, w.f, w.E, w.k), ws
 
 
+# GEMM path variants: the default policy (small experts swapped, few-token down GEMM split over
+# K), every expert in the normal orientation, and a forced 3-way K split.
+MODES = {"default": {}, "noswap": {"MOE_GEMM_SWAP_MAX": "0"}, "ksplit3": {"MOE_DOWN_KSPLIT": "3"}}
+
+
+@pytest.fixture(params=sorted(MODES))
+def mode(request, monkeypatch):
+    for k in ("MOE_GEMM_SWAP_MAX", "MOE_DOWN_KSPLIT"):
+        monkeypatch.delenv(k, raising=False)
+    for k, v in MODES[request.param].items():
+        monkeypatch.setenv(k, v)
+    return request.param
+
+
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
-def test_forward_matches_oracle(moe, oracle, w):
+def test_forward_matches_oracle(moe, oracle, w, mode):
     logits, x, wgu, wd = case_inputs(w, seed=0)
     out, v, ws = _forward_and_views(moe, w, logits, x, wgu, wd)
     assert moe.get_device_error(ws) == 0
@@ -130,8 +144,10 @@ GEMM_CASES = [  # (T, d, f, E, k, bias)
 ]
 
 
+@pytest.mark.parametrize("swap_max", ["128", "0"])
 @pytest.mark.parametrize("T,d,f,E,k,bias", GEMM_CASES)
-def test_gateup_swiglu_parity(moe, oracle, T, d, f, E, k, bias):
+def test_gateup_swiglu_parity(moe, oracle, T, d, f, E, k, bias, swap_max, monkeypatch):
+    monkeypatch.setenv("MOE_GEMM_SWAP_MAX", swap_max)
     offsets = _segments(oracle, T, E, k, seed=11, bias=bias)
     M = T * k
     x_perm = random_bf16((M, d), seed=5)
@@ -151,33 +167,44 @@ def test_gateup_swiglu_parity(moe, oracle, T, d, f, E, k, bias):
     assert_close(got, ref, 2.0 ** -7, 2e-3, "h")
 
 
+@pytest.mark.parametrize("swap_max,ksplit", [("128", 1), ("0", 1), ("128", 3), ("0", 5), ("128", 8)])
 @pytest.mark.parametrize("T,d,f,E,k,bias", GEMM_CASES)
-def test_down_parity(moe, oracle, T, d, f, E, k, bias):
+def test_down_parity(moe, oracle, T, d, f, E, k, bias, swap_max, ksplit, monkeypatch):
+    monkeypatch.setenv("MOE_GEMM_SWAP_MAX", swap_max)
     offsets = _segments(oracle, T, E, k, seed=12, bias=bias)
     M = T * k
     h = random_bf16((M, f), seed=6, scale=0.5)
     _, _, _, wd = case_inputs(Workload("g", 1, d, f, E, 1), seed=4)
-    y = torch.full((M, d), float("nan"), dtype=torch.float32, device=DEV)
+    y = torch.full((ksplit, M, d), float("nan"), dtype=torch.float32, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    moe.grouped_gemm_down(h.to(DEV), wd.to(DEV), torch.from_numpy(offsets).to(DEV), y_perm=y, status=status)
+    moe.grouped_gemm_down(h.to(DEV), wd.to(DEV), torch.from_numpy(offsets).to(DEV), y_perm=y, status=status,
+                          ksplit=ksplit)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     ref = oracle.down(to_np_bits(h), offsets, to_np_bits(wd))
-    got = y.cpu().numpy()
+    parts = y.cpu().numpy()
+    assert np.isfinite(parts).all(), "some partial-sum rows were not written"
+    got = parts[0].copy()
+    for s_ in range(1, ksplit):  # slice order, as the combine step adds them
+        got += parts[s_]
     assert np.isfinite(got).all(), "some y rows were not written"
     assert_close(got, ref, 1e-3, 1e-4, "y_perm")
 
 
-@pytest.mark.parametrize("T,d,E,k", [(4096, 4096, 8, 2), (2048, 7168, 256, 8), (37, 192, 4, 4), (1, 64, 3, 1)])
-def test_combine_parity(moe, oracle, T, d, E, k):
+@pytest.mark.parametrize("T,d,E,k,ksplit", [(4096, 4096, 8, 2, 1), (2048, 7168, 256, 8, 1), (37, 192, 4, 4, 1),
+                                             (1, 64, 3, 1, 1), (32, 4096, 8, 2, 5), (300, 512, 8, 2, 8)])
+def test_combine_parity(moe, oracle, T, d, E, k, ksplit):
     g = torch.Generator("cpu").manual_seed(T + k)
     logits = torch.randn(T, E, generator=g)
     idx, w = oracle.route(logits.numpy(), k)
     _, _, _, dest = oracle.permute(idx, E)
-    y = torch.randn(T * k, d, generator=g)
-    out = moe.combine(y.to(DEV), torch.from_numpy(w).to(DEV), torch.from_numpy(dest).to(DEV))
+    y = torch.randn(ksplit, T * k, d, generator=g)
+    out = moe.combine(y.to(DEV), torch.from_numpy(w).to(DEV), torch.from_numpy(dest).to(DEV), ksplit=ksplit)
     torch.cuda.synchronize()
-    ref = oracle.combine(y.numpy(), w, dest)
+    ysum = y[0].numpy().copy()
+    for s_ in range(1, ksplit):  # the partial slices are added in slice order before weighting
+        ysum += y[s_].numpy()
+    ref = oracle.combine(ysum, w, dest)
     assert_close(out.float().cpu().numpy(), ref, 2.0 ** -8, 1e-6, "combine")
 
 
@@ -247,7 +274,6 @@ def _cudart():
 def test_forward_is_five_kernels_and_graph_capturable(moe):
     """Capture one moe_forward in a CUDA graph: the runtime counts exactly five kernel nodes, and
     replaying the graph reproduces the eager result bit for bit."""
-    import ctypes
     w = WORKLOADS["tiny"]
     logits, x, wgu, wd = case_inputs(w)
     dev = torch.device(DEV)
@@ -256,23 +282,42 @@ def test_forward_is_five_kernels_and_graph_capturable(moe):
     eager = moe.forward(*args, workspace=ws).clone()
     out = torch.zeros_like(eager)
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
+    try:
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+    except TypeError:  # a torch without keep_graph: replay still checked, nodes not counted
+        g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         moe.forward(*args, out=out, workspace=ws)
+    raw = None
+    try:
+        raw = g.raw_cuda_graph()
+    except (AttributeError, RuntimeError):
+        pass
+    kinds = _graph_node_types(raw) if raw else None
+    if raw is not None and hasattr(g, "instantiate"):
+        g.instantiate()
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
-    rt = _cudart()
-    if rt is None or not hasattr(g, "raw_cuda_graph"):
+    if kinds is None:
         pytest.skip("no libcudart / raw_cuda_graph to count graph nodes")
+    # cudaGraphNodeTypeKernel == 0
+    assert kinds.count(0) == moe.forward_launch_count() == 5, kinds
+
+
+def _graph_node_types(raw):
+    import ctypes
+    rt = _cudart()
+    if rt is None:
+        return None
+    g = ctypes.c_void_p(raw)
     n = ctypes.c_size_t(0)
-    assert rt.cudaGraphGetNodes(ctypes.c_void_p(g.raw_cuda_graph()), None, ctypes.byref(n)) == 0
+    assert rt.cudaGraphGetNodes(g, None, ctypes.byref(n)) == 0
     nodes = (ctypes.c_void_p * n.value)()
-    assert rt.cudaGraphGetNodes(ctypes.c_void_p(g.raw_cuda_graph()), nodes, ctypes.byref(n)) == 0
+    assert rt.cudaGraphGetNodes(g, nodes, ctypes.byref(n)) == 0
     kinds = []
     for i in range(n.value):
         t = ctypes.c_int(-1)
         assert rt.cudaGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) == 0
         kinds.append(t.value)
-    # cudaGraphNodeTypeKernel == 0
-    assert kinds.count(0) == moe.forward_launch_count() == 5, kinds
+    return kinds
