@@ -62,6 +62,7 @@ MEASURED_TRAFFIC = {
     ("mixtral_t4096", "down"): (1545403784, "c1456f64356fe32c"),
 }
 GEMM_SOURCES = ("mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm.cu",
+                "mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm_2sm.cu",
                 "mixture_experts_grouped_fp32_gb300/csrc/tcgen05.cuh")
 
 

@@ -1,6 +1,7 @@
 // common.cuh — small shared pieces of the MoE kernels (status bits, bf16 packing, launchers).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -72,8 +73,16 @@ struct GemmArgs {
     int32_t* status;
     int ksplit;            // K slices (down only; 1 = no split)
     int swap_max;          // experts with at most this many rows use the swapped orientation
+    int pair;              // 1: run on SM pairs (cta_group::2, normal orientation only)
 };
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                 const char** why);
+cudaError_t launch_grouped_gemm_pair(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
+                                     const char** why);
+
+// 2-D bf16 tensor map over [rows, cols] (cols contiguous), box = [box_rows, 64 cols], 128-byte
+// swizzle; false if the driver's encoder is unavailable or rejects the operand.
+bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                          uint32_t box_rows);
 
 }  // namespace moe

@@ -442,34 +442,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 // ---------------------------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // ---------------------------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// 2-D bf16 tensor [rows, cols] (cols contiguous), box = [box_rows, 64 cols], 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
-    auto enc = get_encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {64, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int KIND>
 cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const char** why) {
     static bool attr_set[64] = {};
@@ -486,8 +458,8 @@ cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const ch
     }
     CUtensorMap mA, mA32, mB;
     const uint64_t bcols = KIND == 0 ? 2ull * a.N : static_cast<uint64_t>(a.N);
-    if (!make_map(&mA, a.A, a.K, a.M, BM) || !make_map(&mA32, a.A, a.K, a.M, A_BOX32_ROWS) ||
-        !make_map(&mB, a.B, bcols, static_cast<uint64_t>(a.E) * a.K, BK)) {
+    if (!make_tensor_map_bf16(&mA, a.A, a.K, a.M, BM) || !make_tensor_map_bf16(&mA32, a.A, a.K, a.M, A_BOX32_ROWS) ||
+        !make_tensor_map_bf16(&mB, a.B, bcols, static_cast<uint64_t>(a.E) * a.K, BK)) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or bad operand)";
         return cudaErrorInvalidValue;
     }
@@ -499,12 +471,41 @@ cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const ch
 
 }  // namespace
 
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous), box = [box_rows, 64 cols], 128-byte swizzle.
+bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                 const char** why) {
     if (a.ksplit < 1 || a.ksplit > kMaxKSplit || (kind == 0 && a.ksplit != 1)) {
         *why = "ksplit must be 1 for gate+up and in [1, 8] for down";
         return cudaErrorInvalidValue;
     }
+    if (a.pair && num_sms >= 2) return launch_grouped_gemm_pair(kind, a, num_sms, s, why);
     return kind == 0 ? launch_kind<0>(a, num_sms, s, why) : launch_kind<1>(a, num_sms, s, why);
 }
 

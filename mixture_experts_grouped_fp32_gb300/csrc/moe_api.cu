@@ -103,6 +103,15 @@ int swap_max_rows() {
     return x < 0 ? 0 : (x > 128 ? 128 : x);
 }
 
+// Whether the grouped GEMMs run on SM pairs (tcgen05 cta_group::2, 256-row tiles).  Chosen when
+// the average expert has at least 128 rows (M >= 128 E): then most items are full tiles and sibling
+// M-tiles share one weight load; decode-sized batches and many-expert layers keep the 1-SM kernel
+// with its swapped orientation for small experts.  MOE_GEMM_2SM=0/1 overrides.
+int use_pair(long long M, int E) {
+    if (const char* v = std::getenv("MOE_GEMM_2SM")) return v[0] == '1' ? 1 : 0;
+    return M >= 128ll * E ? 1 : 0;
+}
+
 // K slices for the down projection of a layer shape.  The down GEMM has d/256 N-tiles per M-tile.
 // When that gives between one and two waves of work items on a 152-SM GB300, the last wave runs
 // on a fraction of the SMs; splitting K in two evens it out (Mixtral shape, T=512: down GEMM
@@ -180,10 +189,11 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
         return launched(e, "permute");
     const char* why = "";
     const int swap_max = swap_max_rows(), ksplit = down_ksplit(T, d, f, E, k);
-    GemmArgs g1{x_perm, wgu, offsets, M, d, f, E, h, status, 1, swap_max};
+    const int pair = use_pair(M, E);
+    GemmArgs g1{x_perm, wgu, offsets, M, d, f, E, h, status, 1, swap_max, pair};
     if ((e = launch_grouped_gemm(0, g1, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "gate+up GEMM: %s (%s)", why, cudaGetErrorString(e));
-    GemmArgs g2{h, wd, offsets, M, f, d, E, y, status, ksplit, swap_max};
+    GemmArgs g2{h, wd, offsets, M, f, d, E, y, status, ksplit, swap_max, pair};
     if ((e = launch_grouped_gemm(1, g2, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "down GEMM: %s (%s)", why, cudaGetErrorString(e));
     if ((e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) !=
@@ -299,8 +309,9 @@ static int gemm_entry(int kind, const void* A, const void* B, const int32_t* off
         return fail(MOE_ERR_INVALID_ARG, "%s: operands must be 16-byte aligned", name);
     int sms;
     if ((rc = check_device(&sms))) return rc;
-    GemmArgs g = kind == 0 ? GemmArgs{A, B, offsets, M, d, f, E, out, status, 1, swap_max_rows()}
-                           : GemmArgs{A, B, offsets, M, f, d, E, out, status, ksplit, swap_max_rows()};
+    const int pair = use_pair(M, E);
+    GemmArgs g = kind == 0 ? GemmArgs{A, B, offsets, M, d, f, E, out, status, 1, swap_max_rows(), pair}
+                           : GemmArgs{A, B, offsets, M, f, d, E, out, status, ksplit, swap_max_rows(), pair};
     const char* why = "";
     cudaError_t e = launch_grouped_gemm(kind, g, sms, static_cast<cudaStream_t>(stream), &why);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s (%s)", name, why, cudaGetErrorString(e));

@@ -51,14 +51,17 @@ def _forward_and_views(moe, w, logits, x, wgu, wd):
     return out, moe.workspace_views(ws, w.T, w.d, w.f, w.E, w.k), ws
 
 
-# GEMM path variants: the default policy (small experts swapped, few-token down GEMM split over
-# K), every expert in the normal orientation, and a forced 3-way K split.
-MODES = {"default": {}, "noswap": {"MOE_GEMM_SWAP_MAX": "0"}, "ksplit3": {"MOE_DOWN_KSPLIT": "3"}}
+# GEMM path variants: the default policy (small experts swapped on the 1-SM kernel, SM pairs when
+# the average expert has >= 128 rows, few-token down GEMM split over K), the 1-SM kernel with every
+# expert in the normal orientation, the SM-pair kernel for every shape, and a forced 3-way K split.
+MODES = {"default": {}, "noswap": {"MOE_GEMM_SWAP_MAX": "0", "MOE_GEMM_2SM": "0"},
+         "pair": {"MOE_GEMM_2SM": "1"}, "ksplit3": {"MOE_DOWN_KSPLIT": "3"}}
+ENV_KNOBS = ("MOE_GEMM_SWAP_MAX", "MOE_DOWN_KSPLIT", "MOE_GEMM_2SM")
 
 
 @pytest.fixture(params=sorted(MODES))
 def mode(request, monkeypatch):
-    for k in ("MOE_GEMM_SWAP_MAX", "MOE_DOWN_KSPLIT"):
+    for k in ENV_KNOBS:
         monkeypatch.delenv(k, raising=False)
     for k, v in MODES[request.param].items():
         monkeypatch.setenv(k, v)
@@ -144,10 +147,11 @@ GEMM_CASES = [  # (T, d, f, E, k, bias)
 ]
 
 
-@pytest.mark.parametrize("swap_max", ["128", "0"])
+@pytest.mark.parametrize("swap_max,pair", [("128", "0"), ("0", "0"), ("64", "1")])
 @pytest.mark.parametrize("T,d,f,E,k,bias", GEMM_CASES)
-def test_gateup_swiglu_parity(moe, oracle, T, d, f, E, k, bias, swap_max, monkeypatch):
+def test_gateup_swiglu_parity(moe, oracle, T, d, f, E, k, bias, swap_max, pair, monkeypatch):
     monkeypatch.setenv("MOE_GEMM_SWAP_MAX", swap_max)
+    monkeypatch.setenv("MOE_GEMM_2SM", pair)
     offsets = _segments(oracle, T, E, k, seed=11, bias=bias)
     M = T * k
     x_perm = random_bf16((M, d), seed=5)
@@ -167,10 +171,12 @@ def test_gateup_swiglu_parity(moe, oracle, T, d, f, E, k, bias, swap_max, monkey
     assert_close(got, ref, 2.0 ** -7, 2e-3, "h")
 
 
-@pytest.mark.parametrize("swap_max,ksplit", [("128", 1), ("0", 1), ("128", 3), ("0", 5), ("128", 8)])
+@pytest.mark.parametrize("swap_max,ksplit,pair", [("128", 1, "0"), ("0", 1, "0"), ("128", 3, "0"), ("0", 5, "0"),
+                                                  ("128", 8, "0"), ("64", 1, "1"), ("64", 3, "1")])
 @pytest.mark.parametrize("T,d,f,E,k,bias", GEMM_CASES)
-def test_down_parity(moe, oracle, T, d, f, E, k, bias, swap_max, ksplit, monkeypatch):
+def test_down_parity(moe, oracle, T, d, f, E, k, bias, swap_max, ksplit, pair, monkeypatch):
     monkeypatch.setenv("MOE_GEMM_SWAP_MAX", swap_max)
+    monkeypatch.setenv("MOE_GEMM_2SM", pair)
     offsets = _segments(oracle, T, E, k, seed=12, bias=bias)
     M = T * k
     h = random_bf16((M, f), seed=6, scale=0.5)
