@@ -126,8 +126,9 @@ MOE_API int moe_grouped_gemm_gateup_swiglu(const void* x_perm, const void* w_gat
 MOE_API int moe_grouped_gemm_down(const void* h, const void* w_down, const int32_t* offsets, int M, int d,
                           int f, int E, int ksplit, float* y_perm, int32_t* status, moe_stream_t stream);
 
-/* The ksplit that moe_forward uses for the down projection of this layer shape (2 when the
- * down projection has between one and two waves of 128x256 work items on a 152-SM GPU, else 1);
+/* The ksplit that moe_forward uses for the down projection of this layer shape (2 when the 1-SM
+ * kernel runs and the down projection has between one and two waves of 128x256 work items on a
+ * 152-SM GPU, else 1);
  * 0 for an invalid shape.  The environment variable MOE_DOWN_KSPLIT, if set, overrides it. */
 MOE_API int moe_down_ksplit(int T, int d, int f, int E, int top_k);
 
@@ -176,7 +177,7 @@ MOE_API int moe_forward_host(const void* x_host, const float* logits_host, const
  * The intermediates live in one file-scope device array of MOE_NOALLOC_SCRATCH_BYTES that every
  * GPU loading this library holds until the process exits.  Shapes whose moe_workspace_size()
  * exceeds it are rejected with MOE_ERR_WORKSPACE (e.g. the Mixtral-8x7B shape fits up to
- * T = 256 tokens with top-2).  The first call on a device looks up the array's device address
+ * T = 629 tokens with top-2).  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream
  * capture.  All calls on a device share the one array and it keeps the last call's contents
  * (every intermediate is rewritten before it is read; the status word is reset by the first

@@ -62,6 +62,9 @@ WORKLOADS = {
                  note="Mixtral-8x7B-shaped layer, large batch T=4096"),
         Workload("deepseek_t2048", 2048, 7168, 2048, 256, 8, ("zipf", 1.2),
                  note="DeepSeek-V3-shaped routed experts, Zipf(1.2)-skewed loads, T=2048"),
+        Workload("deepseek_e32_t256", 256, 7168, 2048, 32, 8, ("zipf", 1.2),
+                 note="profiling-scale DeepSeek-V3-shaped layer: same expert shapes and skew, "
+                      "32 experts (2.8 GB of weights, small enough for a full ncu capture)"),
     ]
 }
 

@@ -147,7 +147,8 @@ def test_down_ksplit_policy(lib):
     slice; the environment override is honoured and clamped."""
     from mixture_experts_grouped_fp32_gb300 import moe
     assert moe.down_ksplit(32, 4096, 14336, 8, 2) == 1
-    assert moe.down_ksplit(512, 4096, 14336, 8, 2) == 2
+    assert moe.down_ksplit(512, 4096, 14336, 8, 2) == 1  # SM-pair kernel: unsplit
+    assert moe.down_ksplit(256, 4096, 14336, 8, 2) == 2  # 1-SM kernel, 1-2 waves of items
     assert moe.down_ksplit(4096, 4096, 14336, 8, 2) == 1
     assert moe.down_ksplit(2048, 7168, 2048, 256, 8) == 1
     for T, d, f, E, k in [(1, 64, 64, 8, 2), (64, 256, 512, 8, 2), (37, 192, 320, 4, 4), (512, 4096, 14336, 8, 2)]:
