@@ -54,12 +54,16 @@ KERNEL_NAMES = {"route": "route_kernel", "permute": "permute_kernel",
 # kernel source with the recorded hash (profiles/grouped_gemm_*.md); reported only while the GEMM
 # source still hashes to that value, else null.
 MEASURED_TRAFFIC = {
-    ("mixtral_t32", "gateup_swiglu"): (1884890384, "c1456f64356fe32c"),
-    ("mixtral_t32", "down"): (944694816, "c1456f64356fe32c"),
-    ("mixtral_t512", "gateup_swiglu"): (1917549360, "c1456f64356fe32c"),
-    ("mixtral_t512", "down"): (996471376, "c1456f64356fe32c"),
-    ("mixtral_t4096", "gateup_swiglu"): (2175459632, "c1456f64356fe32c"),
-    ("mixtral_t4096", "down"): (1545403784, "c1456f64356fe32c"),
+    ("mixtral_t32", "gateup_swiglu"): (1884524288, "6e81f169663e49ee"),
+    ("mixtral_t32", "down"): (944738312, "6e81f169663e49ee"),
+    ("mixtral_t512", "gateup_swiglu"): (1917243192, "6e81f169663e49ee"),
+    ("mixtral_t512", "down"): (982807992, "6e81f169663e49ee"),
+    ("mixtral_t4096", "gateup_swiglu"): (3750712520, "6e81f169663e49ee"),
+    ("mixtral_t4096", "down"): (2027564816, "6e81f169663e49ee"),
+    ("deepseek_t2048", "gateup_swiglu"): (7458951424, "6e81f169663e49ee"),
+    ("deepseek_t2048", "down"): (4063171840, "6e81f169663e49ee"),
+    ("deepseek_e32_t256", "gateup_swiglu"): (1919886096, "6e81f169663e49ee"),
+    ("deepseek_e32_t256", "down"): (1008913104, "6e81f169663e49ee"),
 }
 GEMM_SOURCES = ("mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm.cu",
                 "mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm_2sm.cu",
@@ -311,7 +315,10 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = measured_traffic(w.name, dom)
-    roof.update({"kernel": KERNEL_NAMES[dom], "peak_source": peak_src + " (burst)",
+    kname = KERNEL_NAMES[dom]
+    if moe.gemm_pair_mode(w.T, w.E, w.k) == 1:
+        kname = kname.replace("grouped_gemm_kernel", "grouped_gemm_2sm_kernel")
+    roof.update({"kernel": kname, "peak_source": peak_src + " (burst)",
                  "algorithmic_per_launch": sw[dom]["flops"] if roof["bound"] == "tensor" else sw[dom]["bytes"],
                  "launch_ms": round(dom_ms, 4)})
     layer_roof_ms = 1e3 * max(lw["bytes"] / (peaks["hbm_gbs"] * 1e9), lw["flops"] / (peaks["bf16_tflops"] * 1e12))

@@ -126,6 +126,12 @@ MOE_API int moe_grouped_gemm_gateup_swiglu(const void* x_perm, const void* w_gat
 MOE_API int moe_grouped_gemm_down(const void* h, const void* w_down, const int32_t* offsets, int M, int d,
                           int f, int E, int ksplit, float* y_perm, int32_t* status, moe_stream_t stream);
 
+/* 1 if moe_forward runs the grouped GEMMs of this layer shape on SM pairs (tcgen05 cta_group::2,
+ * 256-row tiles; chosen when T*top_k >= 128*E, i.e. the average expert holds >= 128 rows), 0 if
+ * on single SMs (128-row tiles, experts with <= 64 rows swapped), -1 for an invalid shape.  The
+ * environment variable MOE_GEMM_2SM=0/1 overrides the choice.  Results are the same either way. */
+MOE_API int moe_gemm_pair_mode(int T, int E, int top_k);
+
 /* The ksplit that moe_forward uses for the down projection of this layer shape (2 when the 1-SM
  * kernel runs and the down projection has between one and two waves of 128x256 work items on a
  * 152-SM GPU, else 1);

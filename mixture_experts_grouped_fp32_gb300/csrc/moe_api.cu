@@ -259,6 +259,11 @@ int moe_workspace_layout(int T, int d, int f, int E, int top_k, size_t* offsets_
     return ok();
 }
 
+int moe_gemm_pair_mode(int T, int E, int top_k) {
+    if (check_shape(T, -1, 0, E, top_k, false) != MOE_OK) return -1;
+    return use_pair(static_cast<long long>(T) * top_k, E);
+}
+
 int moe_down_ksplit(int T, int d, int f, int E, int top_k) {
     if (check_shape(T, d, f, E, top_k, true) != MOE_OK) return 0;
     return down_ksplit(T, d, f, E, top_k);

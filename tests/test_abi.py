@@ -162,3 +162,12 @@ def test_down_ksplit_policy(lib):
         assert moe.down_ksplit(4, 64, 128, 8, 2) == 2  # clamped to f/64 = 2 K blocks
     finally:
         del os.environ["MOE_DOWN_KSPLIT"]
+
+
+def test_gemm_pair_mode_policy(lib):
+    from mixture_experts_grouped_fp32_gb300 import moe
+    assert moe.gemm_pair_mode(4096, 8, 2) == 1    # 1024 rows per expert on average
+    assert moe.gemm_pair_mode(512, 8, 2) == 1     # 128
+    assert moe.gemm_pair_mode(32, 8, 2) == 0      # 8
+    assert moe.gemm_pair_mode(2048, 256, 8) == 0  # 64
+    assert moe.gemm_pair_mode(4, 8, 9) == -1
