@@ -19,6 +19,7 @@ constexpr int kPermThreads = 256;
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;
 constexpr int kMaxTokPerBlock = 16;
+constexpr int kCopyBatch = 4;
 
 __global__ void __launch_bounds__(kPermThreads)
 permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int T, int d, int E,
@@ -47,17 +48,48 @@ permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int
     const int t1 = min(T, t0 + tok_per_block);
     const int nA = T * k, a0 = t0 * k;
 
-    // Histogram; warp-uniform trip count so __match_any_sync sees all 32 lanes.
-    for (int base = warp * 32; base < nA; base += kPermThreads) {
-        const int a = base + lane;
-        const int e = a < nA ? __ldg(idx + a) : 0;
-        const bool ok = a < nA && static_cast<unsigned>(e) < static_cast<unsigned>(E);
-        if (a < nA && !ok) bad = 1;
-        const int key = ok ? (e * 2 + (a < a0 ? 1 : 0)) : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, key);
-        if (ok && lane == __ffs(peers) - 1) {
-            atomicAdd(&tot[e], __popc(peers));
-            if (a < a0) atomicAdd(&before[e], __popc(peers));
+    // Histogram of all assignments (tot) and of those before this block's chunk (before).
+    if (E <= 32) {
+        // Few experts: lanes collide often, so aggregate equal ids within the warp first.  The
+        // trip count is warp-uniform so __match_any_sync sees all 32 lanes.
+        for (int base = warp * 32; base < nA; base += kPermThreads) {
+            const int a = base + lane;
+            const int e = a < nA ? __ldg(idx + a) : 0;
+            const bool ok = a < nA && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+            if (a < nA && !ok) bad = 1;
+            const int key = ok ? (e * 2 + (a < a0 ? 1 : 0)) : -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, key);
+            if (ok && lane == __ffs(peers) - 1) {
+                atomicAdd(&tot[e], __popc(peers));
+                if (a < a0) atomicAdd(&before[e], __popc(peers));
+            }
+        }
+    } else {
+        // Many experts: collisions are rare; 16-byte loads of four ids, plain shared atomics.
+        const bool vec = (reinterpret_cast<uintptr_t>(idx) & 15u) == 0;
+        const int n4 = vec ? nA / 4 : 0;
+        for (int q = tid; q < n4; q += kPermThreads) {
+            const int4 v = __ldg(reinterpret_cast<const int4*>(idx) + q);
+            const int ev[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = 4 * q + u, e = ev[u];
+                if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) {
+                    atomicAdd(&tot[e], 1);
+                    if (a < a0) atomicAdd(&before[e], 1);
+                } else {
+                    bad = 1;
+                }
+            }
+        }
+        for (int a = 4 * n4 + tid; a < nA; a += kPermThreads) {
+            const int e = __ldg(idx + a);
+            if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) {
+                atomicAdd(&tot[e], 1);
+                if (a < a0) atomicAdd(&before[e], 1);
+            } else {
+                bad = 1;
+            }
         }
     }
     __syncthreads();
@@ -111,16 +143,31 @@ permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int
     __syncthreads();
     if (bad && tid == 0) flag_status(status, MOE_STATUS_BAD_EXPERT_ID);
 
-    // Row copies: x[t] -> x_perm[row(t, j)] for each slot j, 16 bytes per access.
+    // Row copies: x[t] -> x_perm[row(t, j)] for each slot j, 16 bytes per access.  Each thread
+    // first issues kCopyBatch independent loads, then their k stores each, so that enough reads
+    // are in flight to cover the memory latency.
     const int dv = d / 8;  // uint4 per row
     const int nvec = (t1 - t0) * dv;
-#pragma unroll 4
-    for (int i = tid; i < nvec; i += kPermThreads) {
-        const int tl = i / dv, v = i - tl * dv;
-        const uint4 val = __ldg(x + static_cast<size_t>(t0 + tl) * dv + v);
-        for (int j = 0; j < k; ++j) {
-            const int r = crow[tl * k + j];
-            if (r >= 0) x_perm[static_cast<size_t>(r) * dv + v] = val;
+    for (int base = tid; base < nvec; base += kPermThreads * kCopyBatch) {
+        uint4 val[kCopyBatch];
+#pragma unroll
+        for (int u = 0; u < kCopyBatch; ++u) {
+            const int i = base + u * kPermThreads;
+            if (i < nvec) {
+                const int tl = i / dv, v = i - tl * dv;
+                val[u] = __ldg(x + static_cast<size_t>(t0 + tl) * dv + v);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyBatch; ++u) {
+            const int i = base + u * kPermThreads;
+            if (i < nvec) {
+                const int tl = i / dv, v = i - tl * dv;
+                for (int j = 0; j < k; ++j) {
+                    const int r = crow[tl * k + j];
+                    if (r >= 0) x_perm[static_cast<size_t>(r) * dv + v] = val[u];
+                }
+            }
         }
     }
 }
@@ -130,8 +177,8 @@ permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int
 cudaError_t launch_permute(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
                            int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest,
                            __nv_bfloat16* x_perm, int32_t* status, int num_sms, cudaStream_t s) {
-    // About two blocks per SM for the row copies, at most kMaxTokPerBlock tokens per block.
-    int tpb = (T + 2 * num_sms - 1) / (2 * num_sms);
+    // About four blocks per SM for the row copies, at most kMaxTokPerBlock tokens per block.
+    int tpb = (T + 4 * num_sms - 1) / (4 * num_sms);
     tpb = tpb < 1 ? 1 : (tpb > kMaxTokPerBlock ? kMaxTokPerBlock : tpb);
     const int blocks = (T + tpb - 1) / tpb;
     return launch_k(kPdlPermute, permute_kernel, dim3(blocks), dim3(kPermThreads), 0, s, idx,
