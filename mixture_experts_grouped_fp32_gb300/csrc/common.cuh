@@ -74,6 +74,7 @@ struct GemmArgs {
     int ksplit;            // K slices (down only; 1 = no split)
     int swap_max;          // experts with at most this many rows use the swapped orientation
     int pair;              // 1: run on SM pairs (cta_group::2, normal orientation only)
+    int inject_stall = 0;  // test hook (1-SM kernel): make one pipeline wait run out, see moe_api.cu
 };
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                 const char** why);

@@ -136,7 +136,7 @@ template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
                     const __grid_constant__ CUtensorMap tmB, const int32_t* __restrict__ offsets, int M,
-                    int K, int N, int E, int ksplit, int swap_max, void* __restrict__ out,
+                    int K, int N, int E, int ksplit, int swap_max, int inject_stall, void* __restrict__ out,
                     int32_t* __restrict__ status) {
     constexpr int BN_OUT = KIND == 0 ? 128 : 256;
     extern __shared__ uint8_t smem_raw[];
@@ -238,7 +238,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 uint8_t* sa = tiles + stage * STAGE_BYTES;
                 uint8_t* sb = sa + A_BYTES;
-                ptx::mbar_arrive_expect_tx(&c.full[stage], tx);
+                // Failure-detection test hook: CTA 0 arms its first stage for 16 bytes more than its
+                // copies bring, so that stage never completes and the MMA thread's bounded wait
+                // must expire (status MOE_STATUS_WAIT_TIMEOUT).
+                const uint32_t extra = (inject_stall && blockIdx.x == 0 && filled_mask == 0) ? 16u : 0u;
+                ptx::mbar_arrive_expect_tx(&c.full[stage], tx + extra);
                 if (it.swap) {
                     for (int q = 0; q < nbox32; ++q)
                         ptx::tma_load_2d(sa + q * A_BOX32_BYTES, &tmA32, &c.full[stage], kb * BK,
@@ -465,8 +469,9 @@ cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const ch
     }
     const int swap_max = a.swap_max < 0 ? 0 : (a.swap_max > SWAP_MAX_ROWS ? SWAP_MAX_ROWS : a.swap_max);
     const int ksplit = KIND == 0 ? 1 : a.ksplit;
-    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_kernel<KIND>, dim3(num_sms), dim3(NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB,
-                    a.offsets, a.M, a.K, a.N, a.E, ksplit, swap_max, a.out, a.status);
+    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_kernel<KIND>, dim3(num_sms), dim3(NUM_THREADS),
+                    SMEM_BYTES, s, mA, mA32, mB, a.offsets, a.M, a.K, a.N, a.E, ksplit, swap_max, a.inject_stall,
+                    a.out, a.status);
 }
 
 }  // namespace
@@ -505,7 +510,7 @@ cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaSt
         *why = "ksplit must be 1 for gate+up and in [1, 8] for down";
         return cudaErrorInvalidValue;
     }
-    if (a.pair && num_sms >= 2) return launch_grouped_gemm_pair(kind, a, num_sms, s, why);
+    if (a.pair && num_sms >= 2 && !a.inject_stall) return launch_grouped_gemm_pair(kind, a, num_sms, s, why);
     return kind == 0 ? launch_kind<0>(a, num_sms, s, why) : launch_kind<1>(a, num_sms, s, why);
 }
 

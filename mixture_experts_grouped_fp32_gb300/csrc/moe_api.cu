@@ -112,6 +112,15 @@ int use_pair(long long M, int E) {
     return M >= 128ll * E ? 1 : 0;
 }
 
+// Failure-detection test hook, off unless the environment sets MOE_INJECT_STALL=1: the next
+// grouped-GEMM launches run on the 1-SM kernel with one pipeline stage armed for bytes that never
+// arrive, so a bounded wait expires (~1 s), the kernel reports MOE_STATUS_WAIT_TIMEOUT in the
+// status word, releases its tensor memory and returns.  Nothing faults, traps or hangs.
+int inject_stall() {
+    const char* v = std::getenv("MOE_INJECT_STALL");
+    return (v && v[0] == '1') ? 1 : 0;
+}
+
 // K slices for the down projection of a layer shape.  The down GEMM has d/256 N-tiles per M-tile.
 // When that gives between one and two waves of work items on a 152-SM GB300, the last wave runs
 // on a fraction of the SMs; splitting K in two evens it out (Mixtral shape, T=512: down GEMM
@@ -319,6 +328,7 @@ static int gemm_entry(int kind, const void* A, const void* B, const int32_t* off
     const int pair = use_pair(M, E);
     GemmArgs g = kind == 0 ? GemmArgs{A, B, offsets, M, d, f, E, out, status, 1, swap_max_rows(), pair}
                            : GemmArgs{A, B, offsets, M, f, d, E, out, status, ksplit, swap_max_rows(), pair};
+    g.inject_stall = inject_stall();
     const char* why = "";
     cudaError_t e = launch_grouped_gemm(kind, g, sms, static_cast<cudaStream_t>(stream), &why);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s (%s)", name, why, cudaGetErrorString(e));
