@@ -54,16 +54,18 @@ KERNEL_NAMES = {"route": "route_kernel", "permute": "permute_kernel",
 # kernel source with the recorded hash (profiles/grouped_gemm_*.md); reported only while the GEMM
 # source still hashes to that value, else null.
 MEASURED_TRAFFIC = {
-    ("mixtral_t32", "gateup_swiglu"): (1884524288, "6e81f169663e49ee"),
-    ("mixtral_t32", "down"): (944738312, "6e81f169663e49ee"),
-    ("mixtral_t512", "gateup_swiglu"): (1917243192, "6e81f169663e49ee"),
-    ("mixtral_t512", "down"): (982807992, "6e81f169663e49ee"),
-    ("mixtral_t4096", "gateup_swiglu"): (3750712520, "6e81f169663e49ee"),
-    ("mixtral_t4096", "down"): (2027564816, "6e81f169663e49ee"),
-    ("deepseek_t2048", "gateup_swiglu"): (7458951424, "6e81f169663e49ee"),
-    ("deepseek_t2048", "down"): (4063171840, "6e81f169663e49ee"),
-    ("deepseek_e32_t256", "gateup_swiglu"): (1919886096, "6e81f169663e49ee"),
-    ("deepseek_e32_t256", "down"): (1008913104, "6e81f169663e49ee"),
+    ("mixtral_t32", "gateup_swiglu"): (1884468992, "c849555c80d424e9"),
+    ("mixtral_t32", "down"): (944722688, "c849555c80d424e9"),
+    ("mixtral_t512", "gateup_swiglu"): (1917358080, "c849555c80d424e9"),
+    ("mixtral_t512", "down"): (982794496, "c849555c80d424e9"),
+    ("mixtral_t512_skew40", "gateup_swiglu"): (1918835456, "c849555c80d424e9"),
+    ("mixtral_t512_skew40", "down"): (983391232, "c849555c80d424e9"),
+    ("mixtral_t4096", "gateup_swiglu"): (2628528640, "c849555c80d424e9"),
+    ("mixtral_t4096", "down"): (1527778304, "c849555c80d424e9"),
+    ("deepseek_t2048", "gateup_swiglu"): (8076621056, "c849555c80d424e9"),
+    ("deepseek_t2048", "down"): (4063829248, "c849555c80d424e9"),
+    ("deepseek_e32_t256", "gateup_swiglu"): (1920173312, "c849555c80d424e9"),
+    ("deepseek_e32_t256", "down"): (1008944128, "c849555c80d424e9"),
 }
 GEMM_SOURCES = ("mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm.cu",
                 "mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm_2sm.cu",
@@ -316,8 +318,10 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = measured_traffic(w.name, dom)
     kname = KERNEL_NAMES[dom]
-    if moe.gemm_pair_mode(w.T, w.E, w.k) == 1:
-        kname = kname.replace("grouped_gemm_kernel", "grouped_gemm_2sm_kernel")
+    pair_mode = moe.gemm_pair_mode(w.T, w.d, w.f, w.E, w.k, 0 if dom == "gateup_swiglu" else 1)
+    if pair_mode >= 1:  # SM-pair kernel, template <KIND, swapping form>
+        kname = kname.replace("grouped_gemm_kernel", "grouped_gemm_2sm_kernel").replace(
+            ">", ", true>" if pair_mode == 2 else ", false>")
     roof.update({"kernel": kname, "peak_source": peak_src + " (burst)",
                  "algorithmic_per_launch": sw[dom]["flops"] if roof["bound"] == "tensor" else sw[dom]["bytes"],
                  "launch_ms": round(dom_ms, 4)})

@@ -126,11 +126,21 @@ MOE_API int moe_grouped_gemm_gateup_swiglu(const void* x_perm, const void* w_gat
 MOE_API int moe_grouped_gemm_down(const void* h, const void* w_down, const int32_t* offsets, int M, int d,
                           int f, int E, int ksplit, float* y_perm, int32_t* status, moe_stream_t stream);
 
-/* 1 if moe_forward runs the grouped GEMMs of this layer shape on SM pairs (tcgen05 cta_group::2,
- * 256-row tiles; chosen when T*top_k >= 128*E, i.e. the average expert holds >= 128 rows), 0 if
- * on single SMs (128-row tiles, experts with <= 64 rows swapped), -1 for an invalid shape.  The
- * environment variable MOE_GEMM_2SM=0/1 overrides the choice.  Results are the same either way. */
-MOE_API int moe_gemm_pair_mode(int T, int E, int top_k);
+/* Which grouped-GEMM kernel moe_forward (and the stage calls) run for this layer shape, for the
+ * gate+up GEMM (kind 0) or the down GEMM (kind 1):
+ *   0  single SMs: 128-row tiles, experts with <= 64 rows swapped (weights as the UMMA M operand);
+ *   1  SM pairs (tcgen05 cta_group::2), 256-row tiles only;
+ *   2  SM pairs that also run small experts, and the short remainders of larger ones, swapped
+ *      (M = 256 weight columns x N = rows; up to 64 or 128 rows, by the shared-memory layout the
+ *      kernel picks on the device from the row counts);
+ *  -1  invalid shape or kind.
+ * Policy: with T*top_k >= 128*E (the average expert holds >= 128 rows) SM pairs, mode 1 for the
+ * down GEMM below 512 rows per expert and mode 2 otherwise; gate+up also runs in mode 2 from 32
+ * rows per expert when E * ceil(f/256) >= 608 (many-expert layers); else mode 0.
+ * The environment variable MOE_GEMM_2SM=0/1/2 overrides both GEMMs, MOE_GEMM_2SM_DOWN the down
+ * GEMM alone, MOE_GEMM_PAIR_SWAP_MAX the swap threshold of mode 2 (0..128).  Results agree with
+ * the oracle in every mode. */
+MOE_API int moe_gemm_pair_mode(int T, int d, int f, int E, int top_k, int kind);
 
 /* The ksplit that moe_forward uses for the down projection of this layer shape (2 when the 1-SM
  * kernel runs and the down projection has between one and two waves of 128x256 work items on a

@@ -73,7 +73,9 @@ struct GemmArgs {
     int32_t* status;
     int ksplit;            // K slices (down only; 1 = no split)
     int swap_max;          // experts with at most this many rows use the swapped orientation
-    int pair;              // 1: run on SM pairs (cta_group::2, normal orientation only)
+    int pair;              // 0: 1-SM kernel; 1: SM pairs (cta_group::2), normal orientation only;
+                           // 2: SM pairs with experts of at most pair_swap_max rows swapped
+    int pair_swap_max = 0; // swap threshold of the SM-pair kernel (pair == 2), at most 256
     int inject_stall = 0;  // test hook (1-SM kernel): make one pipeline wait run out, see moe_api.cu
 };
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,

@@ -1,15 +1,54 @@
 // grouped_gemm_2sm.cu — the two grouped GEMMs of the MoE layer on pairs of SMs (tcgen05
 // cta_group::2), for launches whose experts hold 128 rows or more on average.
 //
-// Same operation and item order as grouped_gemm.cu (normal orientation only), but each work
-// item is a 256-row tile computed by a cluster of two CTAs on two SMs:
-//   * CTA r of the pair owns activation rows row0 + 128 r .. +127 (its M-tile) and loads them;
-//   * the 256 weight columns of the tile are split: each CTA loads its 128-column half;
-//   * one thread of CTA 0 issues M=256 x N=256 UMMAs that read both CTAs' shared memory and
-//     accumulate CTA r's 128 rows into CTA r's tensor memory.
-// Per 64-deep K block each SM thus fills 32 KB of shared memory (16 KB rows + 16 KB half weights)
-// instead of 48 KB, and the weight tile is fetched once for both M-tiles.  Sibling M-tiles of an
-// expert share one weight load instead of two.
+// Same operations as grouped_gemm.cu, but every work item is computed by a cluster of two CTAs
+// on two SMs, and one thread of CTA 0 issues M=256 UMMAs that read both CTAs' shared memory and
+// accumulate into both CTAs' tensor memory.  Two item orientations:
+//
+//   normal  a 256-row tile of one expert: CTA r owns activation rows row0 + 128 r .. +127 (its
+//           M-tile) and loads them, plus its 128-column half of the tile's 256 weight columns;
+//           UMMA M = 256 rows x N = 256 weight columns (kind 0: gate and up of 128 h columns).
+//           Per 64-deep K block each SM fills 32 KB of shared memory instead of the 1-SM tile's
+//           48 KB, and the two M-tiles share one weight load.
+//   swap    a chunk of at most C rows of one expert with the operands swapped (DeepGEMM write-up,
+//           section 3.2, "dynamic swap A/B"): the weights are the UMMA A operand, M = 256 weight
+//           columns (CTA r loads columns n0 + 128 r .. +127), and the tokens are B, N = rows
+//           rounded up to 16 (CTA r loads its N/2 rows).  Kind 0 issues two such UMMAs per K step,
+//           gate into accumulator columns [0, N) and up into [128, 128 + N), so an item covers 256
+//           h columns and one tensor-memory lane holds the gate and up value of one column; kind 1
+//           issues one, covering 256 y columns.  The MMA work is the chunk's rows, not a 256-row
+//           tile, so a small expert streams its weights with the tensor pipe mostly idle.
+//
+// The normal-only form (SWAPCAP false) runs six 32 KB pipeline stages.  The swapping form picks
+// one of two shared-memory layouts on the device, from the expert row counts, identically in
+// every CTA:
+//   layout A  six 32 KB stages plus a 4 KB token buffer each: chunks of C = 64 rows;
+//   layout B  five 40 KB stages (32 KB + 8 KB of tokens): chunks of C = 128 rows, one stage fewer.
+// Layout B is taken when more experts have 65..128 rows (swapped only under B) than there are
+// normal 256-row tiles (each slowed by the shallower pipeline); measured on the Mixtral shape at
+// T=512: near-uniform 103..147-row experts run best under A, a skewed batch with seven 74..104-row
+// experts under B.
+//   count <= min(swap_max, C)    one swapped chunk;
+//   otherwise                    256-row normal tiles; a remainder of at most C rows past the last
+//                                full tile becomes one swapped chunk, a larger one one more (partly
+//                                empty) normal tile.
+//
+// Schedule.  Items are numbered expert-major; inside an expert by 256-column super tile s (kind 0:
+// the normal N-tiles 2s and 2s+1, kind 1: N-tile s), then normal items (N-tile, pair, K-slice), then
+// the swapped chunk (K-slice) — items that read the same weight columns run at about the same time
+// and share them through L2.  A static round-robin over the persistent grid of CTA pairs balances
+// skewed loads ("Triton MoE 核心擊敗 Megablocks", setupai.cc, section 關鍵要點, block-scheduled
+// grouped GEMM).  In the swapping form of kind 0 a swapped item reads 512 weight columns and a
+// normal one 256, so there one schedule slot is either a swapped item or the two normal items of
+// N-tiles 2s and 2s+1 for one M-tile pair, run back to back: every slot streams the same weight
+// bytes and the round-robin stays balanced.
+//
+// Shared-memory stage (1024-byte aligned regions, 128-byte swizzle as written by TMA):
+//   X (16 KB)  normal: the CTA's 128 activation rows x 64 K (K-major);
+//              swap: weight boxes 0-1 (MN-major, 64 columns each, 8 KB apart)
+//   Y (16 KB)  normal: the CTA's two weight boxes; swap: weight boxes 2-3 (kind 0: up)
+//   T (4/8 KB) swap only: the CTA's N/2 token rows x 64 K (K-major), as 32-row boxes; after the
+//              six stages in layout A, after X and Y of the stage in layout B.
 //
 // Synchronisation across the pair:
 //   full[s]   lives in CTA 0: its producer arms it with the bytes of both CTAs; both producers'
@@ -27,43 +66,128 @@ namespace {
 constexpr int BM = 128;          // rows per CTA (M-tile)
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 6;
-constexpr int A_BYTES = BM * BK * 2;             // 16 KB
+constexpr int A_BYTES = BM * BK * 2;             // 16 KB: region X
 constexpr int B_BOX_BYTES = 64 * BK * 2;         // 8 KB
-constexpr int BH_BOXES = 2;                      // weight boxes per CTA (half of the tile)
-constexpr int BH_BYTES = BH_BOXES * B_BOX_BYTES; // 16 KB
-constexpr int STAGE_BYTES = A_BYTES + BH_BYTES;  // 32 KB
-constexpr int PAIR_STAGE_BYTES = 2 * STAGE_BYTES;
+constexpr int BH_BOXES = 2;                      // weight boxes per CTA in the normal orientation
+constexpr int REGION_Y = A_BYTES;                // 16 KB
+constexpr int TOK_BOX_ROWS = 32;                 // token box height in the swapped orientation
+constexpr int TOK_BOX_BYTES = TOK_BOX_ROWS * BK * 2;  // 4 KB
+constexpr int NORMAL_CTA_BYTES = A_BYTES + BH_BOXES * B_BOX_BYTES;  // 32 KB per CTA per stage
+constexpr int STAGES_MAX = 6;
+// Layout A: six 32 KB stages, then six 4 KB token buffers.  Layout B: five 40 KB stages.
+constexpr int A_TOK_BASE = STAGES_MAX * NORMAL_CTA_BYTES;      // 192 KB
+constexpr int B_STAGE_BYTES = NORMAL_CTA_BYTES + 2 * TOK_BOX_BYTES;  // 40 KB
+constexpr int B_STAGES = 5;
+constexpr int TILES_BYTES = A_TOK_BASE + STAGES_MAX * TOK_BOX_BYTES;  // 216 KB
+static_assert(B_STAGES * B_STAGE_BYTES <= TILES_BYTES, "layout B fits the tile area");
 constexpr int ACC_COLS = 256;
 constexpr int NUM_ACC = 2;
 constexpr int TMEM_COLS = NUM_ACC * ACC_COLS;
 constexpr int NUM_THREADS = 192;
 constexpr int MAX_E = 256;
 constexpr int SMEM_BYTES = 232448;
+constexpr int SUPER_N = 256;                     // output columns of a swapped item
+constexpr int PAIR_SWAP_MAX_ROWS = 128;
 constexpr uint16_t BOTH_CTAS = 0x3;
 
+template <bool SWAPCAP>
+struct Cfg {
+    static constexpr int TILES = SWAPCAP ? TILES_BYTES : STAGES_MAX * NORMAL_CTA_BYTES;
+};
+
 struct Ctl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[STAGES_MAX];
+    uint64_t empty[STAGES_MAX];
     uint64_t tfull[NUM_ACC];
     uint64_t tempty[NUM_ACC];
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
     int total_items;
+    int layout_b;  // swapping form: 1 = layout B (five 40 KB stages, 128-row chunks)
     int seg[MAX_E + 1];
     int item_start[MAX_E + 1];
 };
-static_assert(STAGES * STAGE_BYTES + 1024 + sizeof(Ctl) <= SMEM_BYTES, "shared memory budget");
+static_assert(Cfg<true>::TILES + 1024 + sizeof(Ctl) <= SMEM_BYTES, "shared memory budget");
 
-struct PairItem {
-    int e, n_tile, kslice, row0, rows;  // row0/rows: this CTA's M-tile (rows may be <= 0)
+// Pipeline geometry of one launch (uniform across the grid).
+struct Ring {
+    int nst, stride, chunk;  // stages, stage stride in bytes, swapped-chunk rows (C)
+    __device__ __forceinline__ uint32_t tok_off(int s) const {
+        return chunk > 64 ? static_cast<uint32_t>(s * stride + NORMAL_CTA_BYTES)
+                          : static_cast<uint32_t>(A_TOK_BASE + s * TOK_BOX_BYTES);
+    }
+};
+template <bool SWAPCAP>
+__device__ __forceinline__ Ring make_ring(int layout_b) {
+    if (SWAPCAP && layout_b) return Ring{B_STAGES, B_STAGE_BYTES, 128};
+    return Ring{STAGES_MAX, NORMAL_CTA_BYTES, 64};
+}
+
+// How an expert's rows split into normal 256-row pair tiles (np) and at most one swapped chunk
+// (ns, starting at row sbase of the expert).
+struct RowSplit {
+    int np, ns, sbase;
+};
+template <bool SWAPCAP>
+__device__ __forceinline__ RowSplit split_rows(int cnt, int swap_max, int chunk) {
+    RowSplit s{0, 0, 0};
+    if (cnt <= 0) return s;
+    if (!SWAPCAP) {
+        s.np = (cnt + 2 * BM - 1) / (2 * BM);
+    } else if (cnt <= min(swap_max, chunk)) {
+        s.ns = 1;
+    } else {
+        s.np = cnt / (2 * BM);
+        const int rem = cnt - 2 * BM * s.np;
+        if (rem > chunk || (rem > 0 && s.np == 0)) {
+            ++s.np;
+        } else if (rem > 0) {
+            s.ns = 1;
+            s.sbase = 2 * BM * s.np;
+        }
+    }
+    return s;
+}
+
+// Column tiling of one launch.  Normal N-tiles are BN_OUT output columns (kind 0: 128 h columns,
+// kind 1: 256 y columns); R of them make one 256-column super tile; the last super tile may hold
+// fewer (r_last).
+template <int KIND>
+struct Tiling {
+    int n_super, r_last;
+    static constexpr int BN_OUT = KIND == 0 ? 128 : 256;
+    static constexpr int R = SUPER_N / BN_OUT;
+    __device__ __forceinline__ explicit Tiling(int N) {
+        const int n_tiles = (N + BN_OUT - 1) / BN_OUT;
+        n_super = (n_tiles + R - 1) / R;
+        r_last = n_tiles - R * (n_super - 1);
+    }
 };
 
-// Items of expert e: ceil(ceil(count / 128) / 2) M-tile pairs x n_tiles x ksplit, ordered N-tile,
-// pair, K-slice.
-__device__ __forceinline__ PairItem decode_pair_item(const Ctl& c, int E, int ksplit, int rank, int i) {
-    int lo = 0, hi = E;
+// Whether one schedule slot holds the normal items of a whole super tile (see the header).
+template <int KIND, bool SWAPCAP>
+struct Sched {
+    static constexpr bool GROUP = SWAPCAP && KIND == 0;
+};
+
+template <int KIND, bool SWAPCAP>
+__device__ __forceinline__ int expert_items(int cnt, const Tiling<KIND>& t, int ksplit, int swap_max, int chunk) {
+    const RowSplit s = split_rows<SWAPCAP>(cnt, swap_max, chunk);
+    if (Sched<KIND, SWAPCAP>::GROUP) return t.n_super * (s.np + s.ns) * ksplit;
+    return ((t.n_super - 1) * (Tiling<KIND>::R * s.np + s.ns) + (t.r_last * s.np + s.ns)) * ksplit;
+}
+
+struct PairItem {
+    int e, n_tile, kslice, row0, rows;  // normal: this CTA's M-tile (rows may be <= 0)
+    int swap, ntok;                     // swap: row0/rows = the chunk, ntok = rows rounded to 16
+    int nsub;                           // items in this slot: N-tiles n_tile .. n_tile + nsub - 1
+};
+
+template <int KIND, bool SWAPCAP>
+__device__ __forceinline__ PairItem decode_pair_item(const Ctl& c, const Tiling<KIND>& t, int E, int ksplit,
+                                                     int swap_max, int chunk, int rank, int i) {
+    int lo = 0, hi = E;  // item_start[lo] <= i < item_start[lo + 1]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if (c.item_start[mid] <= i) lo = mid; else hi = mid;
@@ -71,16 +195,37 @@ __device__ __forceinline__ PairItem decode_pair_item(const Ctl& c, int E, int ks
     PairItem it;
     it.e = lo;
     const int cnt = c.seg[lo + 1] - c.seg[lo];
-    const int pairs = ((cnt + BM - 1) / BM + 1) / 2;
+    const RowSplit s = split_rows<SWAPCAP>(cnt, swap_max, chunk);
+    constexpr int R = Tiling<KIND>::R;
+    constexpr bool GROUP = Sched<KIND, SWAPCAP>::GROUP;
+    const int per_full = ((GROUP ? 1 : R) * s.np + s.ns) * ksplit;
     const int j = i - c.item_start[lo];
-    const int per_n = pairs * ksplit;
-    it.n_tile = j / per_n;
-    const int r = j - it.n_tile * per_n;
-    const int mpair = r / ksplit;
-    it.kslice = r - mpair * ksplit;
-    const int mtile = 2 * mpair + rank;
-    it.row0 = c.seg[lo] + mtile * BM;
-    it.rows = min(BM, cnt - mtile * BM);
+    const int st = min(j / per_full, t.n_super - 1);
+    const int r = j - st * per_full;
+    const int rs = st == t.n_super - 1 ? t.r_last : R;
+    const int n_normal = (GROUP ? 1 : rs) * s.np * ksplit;
+    it.nsub = 1;
+    if (r < n_normal) {
+        const int per_n = s.np * ksplit;
+        const int ntl = r / per_n;  // 0 when GROUP
+        const int rr = r - ntl * per_n;
+        const int mpair = rr / ksplit;
+        it.kslice = rr - mpair * ksplit;
+        it.n_tile = R * st + ntl;
+        if (GROUP) it.nsub = rs;
+        const int mtile = 2 * mpair + rank;
+        it.row0 = c.seg[lo] + mtile * BM;
+        it.rows = min(BM, cnt - mtile * BM);
+        it.swap = 0;
+        it.ntok = 0;
+    } else {
+        it.kslice = r - n_normal;  // the only chunk
+        it.n_tile = st;
+        it.row0 = c.seg[lo] + s.sbase;
+        it.rows = min(chunk, cnt - s.sbase);
+        it.swap = 1;
+        it.ntok = (it.rows + 15) & ~15;
+    }
     return it;
 }
 
@@ -93,28 +238,35 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return g / (1.0f + __expf(-g)) * u;
 }
 
-template <int KIND>
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+    __nv_bfloat16 b = __float2bfloat16_rn(v);
+    return *reinterpret_cast<uint16_t*>(&b);
+}
+
+template <int KIND, bool SWAPCAP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const int32_t* __restrict__ offsets, int M, int K, int N, int E, int ksplit,
-                        void* __restrict__ out, int32_t* __restrict__ status) {
-    constexpr int BN_OUT = KIND == 0 ? 128 : 256;  // output columns of a tile
+grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
+                        const __grid_constant__ CUtensorMap tmB, const int32_t* __restrict__ offsets, int M,
+                        int K, int N, int E, int ksplit, int swap_max, void* __restrict__ out,
+                        int32_t* __restrict__ status) {
+    constexpr int BN_OUT = Tiling<KIND>::BN_OUT;
+    constexpr int SW_BOXES = KIND == 0 ? 4 : 2;  // weight boxes per CTA in a swapped item
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     uint8_t* tiles = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    Ctl& c = *reinterpret_cast<Ctl*>(tiles + STAGES * STAGE_BYTES);
+    Ctl& c = *reinterpret_cast<Ctl*>(tiles + Cfg<SWAPCAP>::TILES);
     const volatile int* abort_flag = &c.abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = static_cast<int>(ptx::cluster_ctarank());
     const bool leader = rank == 0;
     const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
-    const int n_tiles = (N + BN_OUT - 1) / BN_OUT;
+    const Tiling<KIND> tiling(N);
     const int num_kb = K / BK;
     const int kb_per = (num_kb + ksplit - 1) / ksplit;
 
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < STAGES_MAX; ++s) {
             ptx::mbar_init(&c.full[s], 1);
             ptx::mbar_init(&c.empty[s], 1);
         }
@@ -129,6 +281,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
     }
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tmA);
+        if (SWAPCAP) ptx::prefetch_tensormap(&tmA32);
         ptx::prefetch_tensormap(&tmB);
     }
     if (warp == 1) {
@@ -146,10 +299,28 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         ok = __all_sync(0xffffffffu, ok);
         const int per = (E + 31) / 32;
         const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-        const int per_tile = n_tiles * ksplit;
+        // Layout choice (swapping form): B when experts that only B swaps (65..128 rows)
+        // outnumber the normal 256-row tiles B would slow down.
+        int layout_b = 0;
+        if (SWAPCAP && ok) {
+            int mid = 0, tiles_b = 0;
+            for (int e = e0; e < e1; ++e) {
+                const int cnt = c.seg[e + 1] - c.seg[e];
+                mid += (cnt > 64 && cnt <= min(swap_max, 128)) ? 1 : 0;
+                tiles_b += split_rows<SWAPCAP>(cnt, swap_max, 128).np;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                mid += __shfl_xor_sync(0xffffffffu, mid, o);
+                tiles_b += __shfl_xor_sync(0xffffffffu, tiles_b, o);
+            }
+            layout_b = mid > tiles_b ? 1 : 0;
+        }
+        const int chunk = make_ring<SWAPCAP>(layout_b).chunk;
         int sum = 0;
         if (ok)
-            for (int e = e0; e < e1; ++e) sum += (((c.seg[e + 1] - c.seg[e] + BM - 1) / BM + 1) / 2) * per_tile;
+            for (int e = e0; e < e1; ++e)
+                sum += expert_items<KIND, SWAPCAP>(c.seg[e + 1] - c.seg[e], tiling, ksplit, swap_max, chunk);
         int incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -159,11 +330,12 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         int run = incl - sum;
         for (int e = e0; e < e1; ++e) {
             c.item_start[e] = run;
-            if (ok) run += (((c.seg[e + 1] - c.seg[e] + BM - 1) / BM + 1) / 2) * per_tile;
+            if (ok) run += expert_items<KIND, SWAPCAP>(c.seg[e + 1] - c.seg[e], tiling, ksplit, swap_max, chunk);
         }
         if (lane == 31) {
             c.item_start[E] = incl;
             c.total_items = incl;
+            c.layout_b = layout_b;
         }
         if (!ok && lane == 0 && leader) flag_status(status, MOE_STATUS_BAD_OFFSETS);
     }
@@ -174,57 +346,89 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
 
     const uint32_t tmem_base = c.tmem_base;
     const int total = c.total_items;
-    uint32_t fill_parity[STAGES];
+    const Ring ring = make_ring<SWAPCAP>(c.layout_b);
+    const int chunk = ring.chunk;
+    uint32_t fill_parity[STAGES_MAX];
     int filled_mask = 0;
 
     if (warp == 0 && lane == 0) {
         // ------------------------------ TMA producer (both CTAs) ------------------------------
         const uint64_t pol_act = ptx::policy_evict_last();
         const uint64_t pol_wgt = ptx::policy_evict_normal();
-        uint32_t stage = 0, phase = 0;
+        int stage = 0;
+        uint32_t phase = 0;
         bool aborted = false;
         for (int i = pair_id; i < total && !aborted; i += num_pairs) {
-            const PairItem it = decode_pair_item(c, E, ksplit, rank, i);
-            const int n0 = it.n_tile * BN_OUT;
+          const PairItem slot = decode_pair_item<KIND, SWAPCAP>(c, tiling, E, ksplit, swap_max, chunk, rank, i);
+          for (int sub = 0; sub < slot.nsub && !aborted; ++sub) {
+            PairItem it = slot;
+            it.n_tile += sub;
             const int brow = it.e * K;
             const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
+            // Swapped items: this CTA's token rows start N/2 into the chunk for CTA 1.
+            const int half = it.ntok >> 1;
+            const int ntb = (half + TOK_BOX_ROWS - 1) / TOK_BOX_ROWS;  // 1 (layout A) or up to 2 (B)
+            const uint32_t pair_tx = it.swap ? 2u * (SW_BOXES * B_BOX_BYTES + ntb * TOK_BOX_BYTES)
+                                             : 2u * NORMAL_CTA_BYTES;
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (!ptx::mbar_wait(&c.empty[stage], phase ^ 1u, abort_flag)) {
                     raise_abort(c, status);
                     aborted = true;
                     break;
                 }
-                uint8_t* sa = tiles + stage * STAGE_BYTES;
-                uint8_t* sb = sa + A_BYTES;
+                uint8_t* sa = tiles + stage * ring.stride;
                 const uint32_t full_leader = ptx::map_to_cta(ptx::smem_u32(&c.full[stage]), 0);
-                if (leader) ptx::mbar_arrive_expect_tx(&c.full[stage], PAIR_STAGE_BYTES);
-                ptx::tma_load_2d_pair(sa, &tmA, full_leader, kb * BK, it.row0, pol_act);
+                if (leader) ptx::mbar_arrive_expect_tx(&c.full[stage], pair_tx);
+                if (SWAPCAP && it.swap) {
+                    const int n0 = it.n_tile * SUPER_N + 128 * rank;
+                    uint8_t* st = tiles + ring.tok_off(stage);
+                    for (int q = 0; q < ntb; ++q)
+                        ptx::tma_load_2d_pair(st + q * TOK_BOX_BYTES, &tmA32, full_leader, kb * BK,
+                                              it.row0 + rank * half + q * TOK_BOX_ROWS, pol_act);
 #pragma unroll
-                for (int q = 0; q < BH_BOXES; ++q) {
-                    // kind 0: CTA r holds gate columns n0+64r.. and up columns f+n0+64r..;
-                    // kind 1: CTA r holds output columns n0+128r .. n0+128r+127.
-                    const int col = KIND == 0 ? (q == 0 ? n0 + 64 * rank : N + n0 + 64 * rank)
-                                              : n0 + 128 * rank + 64 * q;
-                    ptx::tma_load_2d_pair(sb + q * B_BOX_BYTES, &tmB, full_leader, col, brow + kb * BK, pol_wgt);
+                    for (int q = 0; q < SW_BOXES; ++q) {
+                        // kind 0: gate n0, n0+64, up f+n0, f+n0+64; kind 1: n0, n0+64.
+                        const int col = (KIND == 0 && q >= 2) ? N + n0 + 64 * (q - 2) : n0 + 64 * (q & 1);
+                        ptx::tma_load_2d_pair(sa + q * B_BOX_BYTES, &tmB, full_leader, col, brow + kb * BK,
+                                              pol_wgt);
+                    }
+                } else {
+                    const int n0 = it.n_tile * BN_OUT;
+                    ptx::tma_load_2d_pair(sa, &tmA, full_leader, kb * BK, it.row0, pol_act);
+#pragma unroll
+                    for (int q = 0; q < BH_BOXES; ++q) {
+                        // kind 0: CTA r holds gate columns n0+64r.. and up columns f+n0+64r..;
+                        // kind 1: CTA r holds output columns n0+128r .. n0+128r+127.
+                        const int col = KIND == 0 ? (q == 0 ? n0 + 64 * rank : N + n0 + 64 * rank)
+                                                  : n0 + 128 * rank + 64 * q;
+                        ptx::tma_load_2d_pair(sa + REGION_Y + q * B_BOX_BYTES, &tmB, full_leader, col,
+                                              brow + kb * BK, pol_wgt);
+                    }
                 }
                 fill_parity[stage] = phase;
                 filled_mask |= 1 << stage;
-                if (++stage == STAGES) {
+                if (++stage == ring.nst) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
+          }
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------ pair MMA issuer (CTA 0) ------------------------------
-        constexpr uint32_t idesc = ptx::idesc_bf16_f32(2 * BM, ACC_COLS, /*a_mn=*/0, /*b_mn=*/1);
-        uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+        constexpr uint32_t idesc_normal = ptx::idesc_bf16_f32(2 * BM, ACC_COLS, /*a_mn=*/0, /*b_mn=*/1);
+        int stage = 0;
+        uint32_t phase = 0, acc = 0, acc_phase = 0;
         bool aborted = false;
         for (int i = pair_id; i < total && !aborted; i += num_pairs) {
-            const PairItem it = decode_pair_item(c, E, ksplit, rank, i);
+          const PairItem slot = decode_pair_item<KIND, SWAPCAP>(c, tiling, E, ksplit, swap_max, chunk, rank, i);
+          for (int sub = 0; sub < slot.nsub && !aborted; ++sub) {
+            const PairItem& it = slot;
+            const uint32_t idesc_swap = ptx::idesc_bf16_f32(2 * BM, static_cast<uint32_t>(it.ntok), 1, 0);
             const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
             if (!ptx::mbar_wait(&c.tempty[acc], acc_phase ^ 1u, abort_flag)) {
                 raise_abort(c, status);
+                aborted = true;
                 break;
             }
             ptx::tc_fence_after();
@@ -236,16 +440,33 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t sa = ptx::smem_u32(tiles + stage * STAGE_BYTES);
-                const uint64_t a_desc = ptx::smem_desc_sw128(sa, 16, 1024);
-                const uint64_t b_desc = ptx::smem_desc_sw128(sa + A_BYTES, B_BOX_BYTES, 1024);
+                const uint32_t sa = ptx::smem_u32(tiles + stage * ring.stride);
+                if (SWAPCAP && it.swap) {
+                    // Weights MN-major (A, 64-column atoms 8 KB apart), tokens K-major (B).
+                    const uint64_t wx_desc = ptx::smem_desc_sw128(sa, B_BOX_BYTES, 1024);
+                    const uint64_t wy_desc = ptx::smem_desc_sw128(sa + REGION_Y, B_BOX_BYTES, 1024);
+                    const uint64_t tok_desc = ptx::smem_desc_sw128(ptx::smem_u32(tiles + ring.tok_off(stage)), 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                    ptx::mma_bf16_ss_pair(d_tmem, a_desc + static_cast<uint64_t>((kk * 32) >> 4),
-                                          b_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc,
-                                          (kb != kb0 || kk != 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint32_t accum = (kb != kb0 || kk != 0) ? 1u : 0u;
+                        const uint64_t w_off = static_cast<uint64_t>((kk * 2048) >> 4);
+                        const uint64_t t_off = static_cast<uint64_t>((kk * 32) >> 4);
+                        ptx::mma_bf16_ss_pair(d_tmem, wx_desc + w_off, tok_desc + t_off, idesc_swap, accum);
+                        if (KIND == 0)
+                            ptx::mma_bf16_ss_pair(d_tmem + 128, wy_desc + w_off, tok_desc + t_off, idesc_swap,
+                                                  accum);
+                    }
+                } else {
+                    const uint64_t a_desc = ptx::smem_desc_sw128(sa, 16, 1024);
+                    const uint64_t b_desc = ptx::smem_desc_sw128(sa + REGION_Y, B_BOX_BYTES, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                        ptx::mma_bf16_ss_pair(d_tmem, a_desc + static_cast<uint64_t>((kk * 32) >> 4),
+                                              b_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc_normal,
+                                              (kb != kb0 || kk != 0) ? 1u : 0u);
+                }
                 ptx::mma_commit_pair(&c.empty[stage], BOTH_CTAS);
-                if (++stage == STAGES) {
+                if (++stage == ring.nst) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -256,65 +477,102 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 acc = 0;
                 acc_phase ^= 1u;
             }
+          }
         }
     } else if (warp >= 2) {
         // ------------------------------ epilogue (both CTAs) ------------------------------
         const int quarter = warp & 3;
         const int r_local = quarter * 32 + lane;
         uint32_t acc = 0, acc_phase = 0;
-        for (int i = pair_id; i < total; i += num_pairs) {
-            const PairItem it = decode_pair_item(c, E, ksplit, rank, i);
+        bool aborted = false;
+        for (int i = pair_id; i < total && !aborted; i += num_pairs) {
+          const PairItem slot = decode_pair_item<KIND, SWAPCAP>(c, tiling, E, ksplit, swap_max, chunk, rank, i);
+          for (int sub = 0; sub < slot.nsub; ++sub) {
+            PairItem it = slot;
+            it.n_tile += sub;
             if (!ptx::mbar_wait(&c.tfull[acc], acc_phase, abort_flag)) {
                 raise_abort(c, status);
+                aborted = true;
                 break;
             }
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * ACC_COLS;
-            const int n0 = it.n_tile * BN_OUT;
             const bool kfull = it.kslice * kb_per < num_kb;  // an empty K slice contributes zeros
-            const bool row_ok = r_local < it.rows;
-            const size_t grow = static_cast<size_t>(it.row0 + r_local);
-            if (KIND == 0) {
-                // Accumulator columns: [gate n0..+63 | up n0..+63 | gate n0+64..+127 | up n0+64..+127].
-                __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(out);
+            if (SWAPCAP && it.swap) {
+                // Accumulator lane = weight column col0 of this CTA's half, accumulator column = row.
+                const int col0 = it.n_tile * SUPER_N + 128 * rank + r_local;
+                const int nchunk = (it.rows + 31) / 32;
 #pragma unroll 1
-                for (int cc = 0; cc < BN_OUT / 32; ++cc) {
-                    const uint32_t gcol = (cc < 2 ? 32 * cc : 128 + 32 * (cc - 2));
-                    uint32_t g[32], u[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + gcol, g);
-                    ptx::tmem_ld_32x32b_x32(taddr + gcol + 64, u);
+                for (int cc = 0; cc < nchunk; ++cc) {
+                    uint32_t a0[32], a1[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + cc * 32, a0);
+                    if (KIND == 0) ptx::tmem_ld_32x32b_x32(taddr + 128 + cc * 32, a1);
                     ptx::tmem_ld_wait();
-                    const int col = n0 + cc * 32;
-                    if (row_ok && col < N) {
-                        uint4* dst = reinterpret_cast<uint4*>(h + grow * N + col);
+                    const int nrow = min(32, it.rows - cc * 32);
+                    const size_t row_base = static_cast<size_t>(it.row0 + cc * 32);
+                    if (col0 < N) {
+                        if (KIND == 0) {
+                            uint16_t* h = reinterpret_cast<uint16_t*>(out);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint32_t p[4];
+                            for (int j = 0; j < 32; ++j)
+                                if (j < nrow)
+                                    h[(row_base + j) * N + col0] =
+                                        bf16_bits(silu_mul(__uint_as_float(a0[j]), __uint_as_float(a1[j])));
+                        } else {
+                            float* y = reinterpret_cast<float*>(out) + static_cast<size_t>(it.kslice) * M * N;
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                p[q] = pack_bf16x2(
-                                    silu_mul(__uint_as_float(g[8 * v + 2 * q]), __uint_as_float(u[8 * v + 2 * q])),
-                                    silu_mul(__uint_as_float(g[8 * v + 2 * q + 1]), __uint_as_float(u[8 * v + 2 * q + 1])));
-                            dst[v] = make_uint4(p[0], p[1], p[2], p[3]);
+                            for (int j = 0; j < 32; ++j)
+                                if (j < nrow) y[(row_base + j) * N + col0] = kfull ? __uint_as_float(a0[j]) : 0.0f;
                         }
                     }
                 }
             } else {
-                float* y = reinterpret_cast<float*>(out) + static_cast<size_t>(it.kslice) * M * N;
+                const int n0 = it.n_tile * BN_OUT;
+                const bool row_ok = r_local < it.rows;
+                const size_t grow = static_cast<size_t>(it.row0 + r_local);
+                if (KIND == 0) {
+                    // Accumulator columns: [gate n0..+63 | up n0..+63 | gate n0+64..+127 | up n0+64..+127].
+                    __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(out);
 #pragma unroll 1
-                for (int cc = 0; cc < BN_OUT / 32; ++cc) {
-                    uint32_t v32[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + cc * 32, v32);
-                    ptx::tmem_ld_wait();
-                    const int col = n0 + cc * 32;
-                    if (row_ok && col < N) {
-                        float4* dst = reinterpret_cast<float4*>(y + grow * N + col);
+                    for (int cc = 0; cc < BN_OUT / 32; ++cc) {
+                        const uint32_t gcol = (cc < 2 ? 32 * cc : 128 + 32 * (cc - 2));
+                        uint32_t g[32], u[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + gcol, g);
+                        ptx::tmem_ld_32x32b_x32(taddr + gcol + 64, u);
+                        ptx::tmem_ld_wait();
+                        const int col = n0 + cc * 32;
+                        if (row_ok && col < N) {
+                            uint4* dst = reinterpret_cast<uint4*>(h + grow * N + col);
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            dst[v] = make_float4(kfull ? __uint_as_float(v32[4 * v]) : 0.0f,
-                                                 kfull ? __uint_as_float(v32[4 * v + 1]) : 0.0f,
-                                                 kfull ? __uint_as_float(v32[4 * v + 2]) : 0.0f,
-                                                 kfull ? __uint_as_float(v32[4 * v + 3]) : 0.0f);
+                            for (int v = 0; v < 4; ++v) {
+                                uint32_t p[4];
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    p[q] = pack_bf16x2(
+                                        silu_mul(__uint_as_float(g[8 * v + 2 * q]), __uint_as_float(u[8 * v + 2 * q])),
+                                        silu_mul(__uint_as_float(g[8 * v + 2 * q + 1]),
+                                                 __uint_as_float(u[8 * v + 2 * q + 1])));
+                                dst[v] = make_uint4(p[0], p[1], p[2], p[3]);
+                            }
+                        }
+                    }
+                } else {
+                    float* y = reinterpret_cast<float*>(out) + static_cast<size_t>(it.kslice) * M * N;
+#pragma unroll 1
+                    for (int cc = 0; cc < BN_OUT / 32; ++cc) {
+                        uint32_t v32[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + cc * 32, v32);
+                        ptx::tmem_ld_wait();
+                        const int col = n0 + cc * 32;
+                        if (row_ok && col < N) {
+                            float4* dst = reinterpret_cast<float4*>(y + grow * N + col);
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                dst[v] = make_float4(kfull ? __uint_as_float(v32[4 * v]) : 0.0f,
+                                                     kfull ? __uint_as_float(v32[4 * v + 1]) : 0.0f,
+                                                     kfull ? __uint_as_float(v32[4 * v + 2]) : 0.0f,
+                                                     kfull ? __uint_as_float(v32[4 * v + 3]) : 0.0f);
+                        }
                     }
                 }
             }
@@ -325,6 +583,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 acc = 0;
                 acc_phase ^= 1u;
             }
+          }
         }
     }
 
@@ -334,7 +593,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
     if (warp == 0 && lane == 0 && c.abort_flag) {
         if (leader) {
             // CTA 0's full barriers count both CTAs' copies: wait for every stage filled so far.
-            for (int s = 0; s < STAGES; ++s)
+            for (int s = 0; s < STAGES_MAX; ++s)
                 if (filled_mask & (1 << s)) ptx::mbar_wait_ns(&c.full[s], fill_parity[s], 100000000ull);
         } else {
             const uint64_t t0 = ptx::globaltimer_ns();  // give this CTA's own copies time to land
@@ -353,13 +612,13 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
     ptx::cluster_sync();
 }
 
-template <int KIND>
+template <int KIND, bool SWAPCAP>
 cudaError_t launch_pair_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const char** why) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_2sm_kernel<KIND>,
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_2sm_kernel<KIND, SWAPCAP>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) {
             *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
@@ -367,25 +626,30 @@ cudaError_t launch_pair_kind(const GemmArgs& a, int num_sms, cudaStream_t s, con
         }
         attr_set[dev] = true;
     }
-    CUtensorMap mA, mB;
+    CUtensorMap mA, mA32, mB;
     const uint64_t bcols = KIND == 0 ? 2ull * a.N : static_cast<uint64_t>(a.N);
     if (!make_tensor_map_bf16(&mA, a.A, a.K, a.M, BM) ||
+        !make_tensor_map_bf16(&mA32, a.A, a.K, a.M, TOK_BOX_ROWS) ||
         !make_tensor_map_bf16(&mB, a.B, bcols, static_cast<uint64_t>(a.E) * a.K, BK)) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or bad operand)";
         return cudaErrorInvalidValue;
     }
     const int grid = num_sms & ~1;  // whole CTA pairs
     const int ksplit = KIND == 0 ? 1 : a.ksplit;
-    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_2sm_kernel<KIND>, dim3(grid),
-                    dim3(NUM_THREADS), SMEM_BYTES, s, mA, mB, a.offsets, a.M, a.K, a.N, a.E, ksplit, a.out,
-                    a.status);
+    const int swap_max = a.pair_swap_max < 0 ? 0 : (a.pair_swap_max > PAIR_SWAP_MAX_ROWS ? PAIR_SWAP_MAX_ROWS
+                                                                                      : a.pair_swap_max);
+    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_2sm_kernel<KIND, SWAPCAP>, dim3(grid),
+                    dim3(NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB, a.offsets, a.M, a.K, a.N, a.E, ksplit,
+                    swap_max, a.out, a.status);
 }
 
 }  // namespace
 
 cudaError_t launch_grouped_gemm_pair(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                      const char** why) {
-    return kind == 0 ? launch_pair_kind<0>(a, num_sms, s, why) : launch_pair_kind<1>(a, num_sms, s, why);
+    if (a.pair == 2)
+        return kind == 0 ? launch_pair_kind<0, true>(a, num_sms, s, why) : launch_pair_kind<1, true>(a, num_sms, s, why);
+    return kind == 0 ? launch_pair_kind<0, false>(a, num_sms, s, why) : launch_pair_kind<1, false>(a, num_sms, s, why);
 }
 
 }  // namespace moe

@@ -103,13 +103,36 @@ int swap_max_rows() {
     return x < 0 ? 0 : (x > 128 ? 128 : x);
 }
 
-// Whether the grouped GEMMs run on SM pairs (tcgen05 cta_group::2, 256-row tiles).  Chosen when
-// the average expert has at least 128 rows (M >= 128 E): then most items are full tiles and sibling
-// M-tiles share one weight load; decode-sized batches and many-expert layers keep the 1-SM kernel
-// with its swapped orientation for small experts.  MOE_GEMM_2SM=0/1 overrides.
-int use_pair(long long M, int E) {
-    if (const char* v = std::getenv("MOE_GEMM_2SM")) return v[0] == '1' ? 1 : 0;
-    return M >= 128ll * E ? 1 : 0;
+// Which grouped-GEMM kernel a layer shape runs on, per GEMM (kind 0 gate+up with N = f output
+// columns, 1 down with N = d): 0 the 1-SM kernel (128-row tiles, experts with <= swap_max_rows()
+// rows swapped), 1 the SM-pair kernel with 256-row tiles only, 2 the SM-pair kernel that also
+// swaps small experts and the short remainders of large ones.
+//   * average expert >= 128 rows (M >= 128 E): SM pairs, so sibling M-tiles share one weight load;
+//     mode 2, except the down GEMM below 512 rows per expert, measured faster in mode 1;
+//   * gate+up, 32..127 rows per expert on average, and at least 608 schedule slots (E x N/256:
+//     eight rounds over GB300's 76 SM pairs): mode 2 — many-expert layers mix a few large experts,
+//     which pair tiles run faster, with many small ones, which stream swapped (DeepSeek-V3 shape:
+//     gate+up 1.458 -> 1.415 ms); with fewer slots the round-robin's last round runs mostly empty
+//     (a 32-expert layer of the same shape: 0.289 -> 0.340 ms);
+//   * otherwise the 1-SM kernel.
+// MOE_GEMM_2SM=0/1/2 overrides both GEMMs, MOE_GEMM_2SM_DOWN the down GEMM alone.
+int use_pair(long long M, int E, int N, int kind) {
+    auto parse = [](const char* v) { return v[0] == '2' ? 2 : (v[0] == '1' ? 1 : 0); };
+    if (kind == 1)
+        if (const char* v = std::getenv("MOE_GEMM_2SM_DOWN")) return parse(v);
+    if (const char* v = std::getenv("MOE_GEMM_2SM")) return parse(v);
+    if (M >= 128ll * E) return (kind == 1 && M < 512ll * E) ? 1 : 2;
+    if (kind == 0 && M >= 32ll * E && static_cast<long long>(E) * ((N + 255) / 256) >= 608) return 2;
+    return 0;
+}
+
+// Swap threshold of the SM-pair kernel in mode 2: experts with at most this many rows run as one
+// swapped chunk (further capped on the device at 64 or 128 rows by the shared-memory layout the
+// kernel picks).  MOE_GEMM_PAIR_SWAP_MAX overrides (clamped to [0, 128]).
+int pair_swap_max_rows() {
+    const char* v = std::getenv("MOE_GEMM_PAIR_SWAP_MAX");
+    int x = v ? std::atoi(v) : 128;
+    return x < 0 ? 0 : (x > 128 ? 128 : x);
 }
 
 // Failure-detection test hook, off unless the environment sets MOE_INJECT_STALL=1: the next
@@ -134,7 +157,7 @@ int down_ksplit(int T, int d, int f, int E, int k) {
     int S;
     if (const char* v = std::getenv("MOE_DOWN_KSPLIT")) {
         S = std::atoi(v);
-    } else if (use_pair(M, E)) {
+    } else if (use_pair(M, E, d, 1)) {
         S = 1;  // 256-row pair items: measured best unsplit (Mixtral T=512: 0.510 ms/layer vs 0.524 at 2)
     } else {
         const long long mtiles = (M + 127) / 128 + (M < E ? M : E);
@@ -200,11 +223,10 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
         return launched(e, "permute");
     const char* why = "";
     const int swap_max = swap_max_rows(), ksplit = down_ksplit(T, d, f, E, k);
-    const int pair = use_pair(M, E);
-    GemmArgs g1{x_perm, wgu, offsets, M, d, f, E, h, status, 1, swap_max, pair};
+    GemmArgs g1{x_perm, wgu, offsets, M, d, f, E, h, status, 1, swap_max, use_pair(M, E, f, 0), pair_swap_max_rows()};
     if ((e = launch_grouped_gemm(0, g1, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "gate+up GEMM: %s (%s)", why, cudaGetErrorString(e));
-    GemmArgs g2{h, wd, offsets, M, f, d, E, y, status, ksplit, swap_max, pair};
+    GemmArgs g2{h, wd, offsets, M, f, d, E, y, status, ksplit, swap_max, use_pair(M, E, d, 1), pair_swap_max_rows()};
     if ((e = launch_grouped_gemm(1, g2, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "down GEMM: %s (%s)", why, cudaGetErrorString(e));
     if ((e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) !=
@@ -268,9 +290,9 @@ int moe_workspace_layout(int T, int d, int f, int E, int top_k, size_t* offsets_
     return ok();
 }
 
-int moe_gemm_pair_mode(int T, int E, int top_k) {
-    if (check_shape(T, -1, 0, E, top_k, false) != MOE_OK) return -1;
-    return use_pair(static_cast<long long>(T) * top_k, E);
+int moe_gemm_pair_mode(int T, int d, int f, int E, int top_k, int kind) {
+    if (check_shape(T, d, f, E, top_k, true) != MOE_OK || (kind != 0 && kind != 1)) return -1;
+    return use_pair(static_cast<long long>(T) * top_k, E, kind == 0 ? f : d, kind);
 }
 
 int moe_down_ksplit(int T, int d, int f, int E, int top_k) {
@@ -325,9 +347,10 @@ static int gemm_entry(int kind, const void* A, const void* B, const int32_t* off
         return fail(MOE_ERR_INVALID_ARG, "%s: operands must be 16-byte aligned", name);
     int sms;
     if ((rc = check_device(&sms))) return rc;
-    const int pair = use_pair(M, E);
+    const int pair = use_pair(M, E, kind == 0 ? f : d, kind);
     GemmArgs g = kind == 0 ? GemmArgs{A, B, offsets, M, d, f, E, out, status, 1, swap_max_rows(), pair}
                            : GemmArgs{A, B, offsets, M, f, d, E, out, status, ksplit, swap_max_rows(), pair};
+    g.pair_swap_max = pair_swap_max_rows();
     g.inject_stall = inject_stall();
     const char* why = "";
     cudaError_t e = launch_grouped_gemm(kind, g, sms, static_cast<cudaStream_t>(stream), &why);

@@ -31,7 +31,7 @@ _SIGS = {
     "moe_grouped_gemm_gateup_swiglu": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gemm_down": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_down_ksplit": ([_I, _I, _I, _I, _I], _I),
-    "moe_gemm_pair_mode": ([_I, _I, _I], _I),
+    "moe_gemm_pair_mode": ([_I, _I, _I, _I, _I, _I], _I),
     "moe_combine": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_forward_noalloc": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "moe_forward": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
@@ -162,9 +162,11 @@ def down_ksplit(T: int, d: int, f: int, E: int, top_k: int) -> int:
     return int(load().moe_down_ksplit(T, d, f, E, top_k))
 
 
-def gemm_pair_mode(T: int, E: int, top_k: int) -> int:
-    """1 if moe_forward runs this shape's grouped GEMMs on SM pairs, 0 if on single SMs."""
-    return int(load().moe_gemm_pair_mode(T, E, top_k))
+def gemm_pair_mode(T: int, d: int, f: int, E: int, top_k: int, kind: int = 0) -> int:
+    """Grouped-GEMM kernel moe_forward picks for this shape and GEMM (kind 0 gate+up, 1 down):
+    0 single SMs, 1 SM pairs with 256-row tiles only, 2 SM pairs that also swap small experts;
+    -1 for an invalid shape."""
+    return int(load().moe_gemm_pair_mode(T, d, f, E, top_k, kind))
 
 
 def grouped_gemm_down(h, w_down, offsets, y_perm=None, status=None, stream=None, ksplit: int = 1):

@@ -18,10 +18,18 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 FULL = ["mixtral_t32", "mixtral_t512", "mixtral_t512_skew40", "mixtral_t4096", "deepseek_t2048"]
 
 
+@pytest.mark.parametrize("path", ["policy", "other"])
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_forward(oracle, name):
+def test_full_size_forward(oracle, name, path, monkeypatch):
+    """`policy`: the GEMM path moe_forward picks for the shape; `other`: another kernel forced
+    (single SMs -> swapping SM pairs -> normal-only SM pairs -> single SMs), so every kernel is
+    checked at full size."""
     from mixture_experts_grouped_fp32_gb300 import moe
     w = WORKLOADS[name]
+    if path == "other":
+        rot = {0: "2", 2: "1", 1: "0"}
+        monkeypatch.setenv("MOE_GEMM_2SM", rot[moe.gemm_pair_mode(w.T, w.d, w.f, w.E, w.k, 0)])
+        monkeypatch.setenv("MOE_GEMM_2SM_DOWN", rot[moe.gemm_pair_mode(w.T, w.d, w.f, w.E, w.k, 1)])
     dev = torch.device("cuda")
     logits, x, wgu, wd = make_inputs(w, seed=0, weight_device="cuda")
     ws = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k), dtype=torch.uint8, device=dev)

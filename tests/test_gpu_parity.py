@@ -39,6 +39,7 @@ CASES = [
     Workload("dense_e1_k1", 70, 128, 192, 1, 1),
     Workload("minimal_dims", 50, 64, 64, 3, 2),
     Workload("deepseek_like_wide_d", 40, 1024, 256, 32, 8, ("zipf", 1.2)),
+    Workload("hot_expert_mid_experts", 700, 256, 512, 8, 2, ("hot0", 2.2)),
 ]
 
 
@@ -53,10 +54,13 @@ def _forward_and_views(moe, w, logits, x, wgu, wd):
 
 # GEMM path variants: the default policy (small experts swapped on the 1-SM kernel, SM pairs when
 # the average expert has >= 128 rows, few-token down GEMM split over K), the 1-SM kernel with every
-# expert in the normal orientation, the SM-pair kernel for every shape, and a forced 3-way K split.
+# expert in the normal orientation, the SM-pair kernel for every shape in its normal-only form and
+# in its swapping form (thresholds 128 and 64 rows), and a forced 3-way K split.
 MODES = {"default": {}, "noswap": {"MOE_GEMM_SWAP_MAX": "0", "MOE_GEMM_2SM": "0"},
-         "pair": {"MOE_GEMM_2SM": "1"}, "ksplit3": {"MOE_DOWN_KSPLIT": "3"}}
-ENV_KNOBS = ("MOE_GEMM_SWAP_MAX", "MOE_DOWN_KSPLIT", "MOE_GEMM_2SM")
+         "pair": {"MOE_GEMM_2SM": "1"}, "pairswap": {"MOE_GEMM_2SM": "2"},
+         "pairswap64": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_SWAP_MAX": "64"},
+         "ksplit3": {"MOE_DOWN_KSPLIT": "3"}}
+ENV_KNOBS = ("MOE_GEMM_SWAP_MAX", "MOE_DOWN_KSPLIT", "MOE_GEMM_2SM", "MOE_GEMM_PAIR_SWAP_MAX", "MOE_GEMM_2SM_DOWN")
 
 
 @pytest.fixture(params=sorted(MODES))
@@ -138,20 +142,34 @@ def _segments(oracle, T, E, k, seed, bias=("none", 0.0)):
     return offsets
 
 
-GEMM_CASES = [  # (T, d, f, E, k, bias)
-    (300, 512, 768, 8, 2, ("none", 0.0)),
-    (4096, 256, 2048, 2, 1, ("none", 0.0)),
-    (37, 192, 320, 4, 4, ("none", 0.0)),
-    (256, 256, 384, 64, 6, ("zipf", 1.2)),
-    (200, 128, 256, 8, 1, ("hot0", 40.0)),
+GEMM_CASES = [  # (T, d, f, E, k, bias); row counts per expert at the seeds used below
+    (300, 512, 768, 8, 2, ("none", 0.0)),     # 62-90 rows each
+    (4096, 256, 2048, 2, 1, ("none", 0.0)),   # ~2048 each: 256-row tiles, one a 1-row remainder
+    (37, 192, 320, 4, 4, ("none", 0.0)),      # 37 each, partial N tiles on both GEMMs
+    (256, 256, 384, 64, 6, ("zipf", 1.2)),    # 250 down to 0 rows
+    (200, 128, 256, 8, 1, ("hot0", 40.0)),    # one expert holds all 200 rows
+    (600, 256, 512, 2, 1, ("none", 0.0)),     # 309 / 291: one 256-row tile plus a short remainder
+    (700, 256, 512, 8, 2, ("hot0", 2.2)),     # ~630 + 96..143: the pair kernel's 40 KB-stage layout
 ]
 
 
-@pytest.mark.parametrize("swap_max,pair", [("128", "0"), ("0", "0"), ("64", "1")])
+def _set_gemm_env(monkeypatch, swap_max, pair):
+    """pair "2:<n>" selects the swapping SM-pair kernel with threshold n."""
+    monkeypatch.setenv("MOE_GEMM_SWAP_MAX", swap_max)
+    mode, _, psm = pair.partition(":")
+    monkeypatch.setenv("MOE_GEMM_2SM", mode)
+    monkeypatch.delenv("MOE_GEMM_2SM_DOWN", raising=False)
+    if psm:
+        monkeypatch.setenv("MOE_GEMM_PAIR_SWAP_MAX", psm)
+    else:
+        monkeypatch.delenv("MOE_GEMM_PAIR_SWAP_MAX", raising=False)
+
+
+@pytest.mark.parametrize("swap_max,pair", [("128", "0"), ("0", "0"), ("64", "1"), ("64", "2:128"),
+                                           ("64", "2:64"), ("64", "2:0")])
 @pytest.mark.parametrize("T,d,f,E,k,bias", GEMM_CASES)
 def test_gateup_swiglu_parity(moe, oracle, T, d, f, E, k, bias, swap_max, pair, monkeypatch):
-    monkeypatch.setenv("MOE_GEMM_SWAP_MAX", swap_max)
-    monkeypatch.setenv("MOE_GEMM_2SM", pair)
+    _set_gemm_env(monkeypatch, swap_max, pair)
     offsets = _segments(oracle, T, E, k, seed=11, bias=bias)
     M = T * k
     x_perm = random_bf16((M, d), seed=5)
@@ -172,11 +190,11 @@ def test_gateup_swiglu_parity(moe, oracle, T, d, f, E, k, bias, swap_max, pair, 
 
 
 @pytest.mark.parametrize("swap_max,ksplit,pair", [("128", 1, "0"), ("0", 1, "0"), ("128", 3, "0"), ("0", 5, "0"),
-                                                  ("128", 8, "0"), ("64", 1, "1"), ("64", 3, "1")])
+                                                  ("128", 8, "0"), ("64", 1, "1"), ("64", 3, "1"), ("64", 1, "2:128"),
+                                                  ("64", 3, "2:64"), ("64", 2, "2:0")])
 @pytest.mark.parametrize("T,d,f,E,k,bias", GEMM_CASES)
 def test_down_parity(moe, oracle, T, d, f, E, k, bias, swap_max, ksplit, pair, monkeypatch):
-    monkeypatch.setenv("MOE_GEMM_SWAP_MAX", swap_max)
-    monkeypatch.setenv("MOE_GEMM_2SM", pair)
+    _set_gemm_env(monkeypatch, swap_max, pair)
     offsets = _segments(oracle, T, E, k, seed=12, bias=bias)
     M = T * k
     h = random_bf16((M, f), seed=6, scale=0.5)
