@@ -8,7 +8,8 @@ decode-like batch (T=32, d=4096, f=14336, E=8, top-2).
 
 ours (default):
   value        tokens/s with inputs resident in HBM: K steps of moe_forward, CUDA events around each
-               step on its stream.  The weights of every workload (>= 2.8 GB) exceed the 129 MB L2,
+               step on its stream (K defaults to ~0.5 s of device time; nvidia-smi samples the SM
+               clock and throttle reasons every 20 ms during that region).  The weights of every workload (>= 2.8 GB) exceed the 129 MB L2,
                so they stream from HBM each step; --flush-l2 also writes 512 MB between steps.
   roofline     the dominant kernel: its algorithmic bytes (or FLOPs) per launch / its mean duration,
                from a second K-step loop that calls the five stage entry points with events between
@@ -26,6 +27,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -53,6 +55,10 @@ KERNEL_NAMES = {"route": "route_kernel", "permute": "permute_kernel",
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum per launch) from ncu captures of the
 # kernel source with the recorded hash (profiles/grouped_gemm_*.md); reported only while the GEMM
 # source still hashes to that value, else null.
+# Default timed region (no --steps): about this much device time, within these step counts.
+AUTO_TIMED_S = 0.5
+AUTO_STEPS_MIN, AUTO_STEPS_MAX = 50, 4000
+
 MEASURED_TRAFFIC = {
     ("mixtral_t32", "gateup_swiglu"): (1884468992, "c849555c80d424e9"),
     ("mixtral_t32", "down"): (944722688, "c849555c80d424e9"),
@@ -224,6 +230,17 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     torch.cuda.synchronize(dev)
     if moe.get_device_error(ws) != 0:
         raise RuntimeError("device status word set during warm-up")
+    if args.steps is None:
+        # No --steps: time enough steps for ~0.5 s of device work, so that the clock sampler
+        # (20 ms period) sees the timed region ~25 times; every rank takes the same K.
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(3):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        est = max_over_ranks(e0.elapsed_time(e1) / 3, dist, dev)
+        args.steps = int(min(AUTO_STEPS_MAX, max(AUTO_STEPS_MIN, math.ceil(AUTO_TIMED_S * 1e3 / est))))
 
     v = moe.workspace_views(ws, w.T, w.d, w.f, w.E, w.k)
     counts = v["counts"].cpu().numpy()
@@ -413,7 +430,8 @@ def config_of(w: Workload, args) -> dict:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for ~0.5 s of device time, 50..4000; 20 for --impl reference)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -431,6 +449,8 @@ def main():
     w = WORKLOADS[args.workload]
 
     if args.impl == "reference":
+        if args.steps is None:
+            args.steps = 20
         line = run_reference(args, w, rank, world)
         if line is not None:
             print(json.dumps(line), flush=True)

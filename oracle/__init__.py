@@ -58,6 +58,10 @@ _SIGS = {
     "oracle_forward": ([_U16P, _F32P, _U16P, _U16P, _INT, _INT, _INT, _INT, _INT, _F32P], _INT),
     "oracle_forward_tokens": ([_U16P, _F32P, _U16P, _U16P, _INT, _INT, _INT, _INT, _INT, _I32P, _INT,
                                _F32P], _INT),
+    "oracle_route_grouped": ([_F32P, _F32P, _INT, _INT, _INT, _INT, _INT, ctypes.c_float, _I32P, _F32P], _INT),
+    "oracle_forward_routed": ([_U16P, _I32P, _F32P, _U16P, _U16P, _INT, _INT, _INT, _INT, _INT, _F32P], _INT),
+    "oracle_forward_tokens_routed": ([_U16P, _I32P, _F32P, _U16P, _U16P, _INT, _INT, _INT, _INT, _INT, _I32P,
+                                      _INT, _F32P], _INT),
 }
 
 
@@ -195,6 +199,56 @@ class Oracle:
                                           _p(tokens, _I32P), tokens.shape[0], _p(out, _F32P))
         if rc:
             raise ValueError(f"oracle_forward_tokens failed (rc={rc})")
+        return out
+
+    def route_grouped(self, logits, bias, k, n_group, topk_group, scale=1.0):
+        """DeepSeek-V3 router: sigmoid affinities, selection bias, group-limited top-k."""
+        logits = _c(logits, np.float32)
+        bias = _c(bias, np.float32)
+        T, E = logits.shape
+        assert bias.shape == (E,)
+        idx = np.empty((T, k), np.int32)
+        w = np.empty((T, k), np.float32)
+        rc = self.L.oracle_route_grouped(_p(logits, _F32P), _p(bias, _F32P), T, E, k, n_group, topk_group,
+                                         float(scale), _p(idx, _I32P), _p(w, _F32P))
+        if rc:
+            raise ValueError(f"oracle_route_grouped rejected the shape (rc={rc})")
+        return idx, w
+
+    def forward_routed(self, x_bits, idx, w, wgu_bits, wd_bits):
+        """Steps 2-5 of the layer for a given routing idx/w [T,k]."""
+        x_bits = _c(x_bits, np.uint16)
+        idx = _c(idx, np.int32)
+        w = _c(w, np.float32)
+        wgu_bits = _c(wgu_bits, np.uint16)
+        wd_bits = _c(wd_bits, np.uint16)
+        T, d = x_bits.shape
+        E, _, f2 = wgu_bits.shape
+        k = idx.shape[1]
+        out = np.empty((T, d), np.float32)
+        rc = self.L.oracle_forward_routed(_p(x_bits, _U16P), _p(idx, _I32P), _p(w, _F32P), _p(wgu_bits, _U16P),
+                                          _p(wd_bits, _U16P), T, d, f2 // 2, E, k, _p(out, _F32P))
+        if rc:
+            raise ValueError(f"oracle_forward_routed failed (rc={rc})")
+        return out
+
+    def forward_tokens_routed(self, x_bits, idx_rows, w_rows, wgu_bits, wd_bits, tokens):
+        """The layer's output for the sampled tokens, given their routing idx_rows/w_rows [ntok,k]."""
+        x_bits = _c(x_bits, np.uint16)
+        idx_rows = _c(idx_rows, np.int32)
+        w_rows = _c(w_rows, np.float32)
+        wgu_bits = _c(wgu_bits, np.uint16)
+        wd_bits = _c(wd_bits, np.uint16)
+        tokens = _c(tokens, np.int32)
+        T, d = x_bits.shape
+        E, _, f2 = wgu_bits.shape
+        k = idx_rows.shape[1]
+        out = np.empty((tokens.shape[0], d), np.float32)
+        rc = self.L.oracle_forward_tokens_routed(_p(x_bits, _U16P), _p(idx_rows, _I32P), _p(w_rows, _F32P),
+                                                 _p(wgu_bits, _U16P), _p(wd_bits, _U16P), T, d, f2 // 2, E, k,
+                                                 _p(tokens, _I32P), tokens.shape[0], _p(out, _F32P))
+        if rc:
+            raise ValueError(f"oracle_forward_tokens_routed failed (rc={rc})")
         return out
 
 

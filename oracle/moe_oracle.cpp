@@ -27,6 +27,9 @@
 //   The pages never define the router function.  Reading adopted here for every workload:
 //   softmax over all E logits, keep the k largest logits (ties -> lower expert index; the slot
 //   order is descending logit), renormalise the kept probabilities to sum to 1.
+//   A second router, DeepSeek-V3's (the pages only name that model), follows the DeepSeek-V3
+//   Technical Report: sigmoid affinities, a selection-only bias, group-limited top-k, normalised
+//   and scaled gating values (oracle_route_grouped).
 //
 // Precision: every floating-point step is fp32 from the same bf16 inputs (bf16 -> fp32 is exact).
 // The layer's definition fixes fp32 accumulation; this file is built with -ffp-contract=off so the
@@ -121,6 +124,64 @@ int oracle_route(const float* logits, int T, int E, int k, int32_t* idx, float* 
         for (int j = 0; j < k; ++j) {
             idx[static_cast<size_t>(t) * k + j] = order[j];
             w[static_cast<size_t>(t) * k + j] = p[order[j]] / s;
+        }
+    }
+    return 0;
+}
+
+// Step 1, second router: DeepSeek-V3's sigmoid gating with a selection bias and group-limited
+// top-k (DeepSeek-V3 Technical Report, section 2.1.2: the affinity s = sigmoid(logit); the bias b
+// of auxiliary-loss-free load balancing enters only the choice of experts; the gating values are
+// the chosen experts' s normalised to sum to 1; the node-limited routing paragraph: experts are
+// split into groups and a token may use only the groups with the largest sums of their K_r/M
+// highest scores).  Per token, in fp32:
+//   s[e] = 1 / (1 + exp(-logit[e]))              affinity
+//   c[e] = s[e] + bias[e]                        selection score
+//   group g = experts [g*E/G, (g+1)*E/G); its score = sum of its q largest c, q = max(1, k/topk_group)
+//   keep the topk_group groups with the largest scores (equal scores -> lower group id)
+//   idx = the k experts of the kept groups with the largest c (equal -> lower id), slot order =
+//         descending c
+//   w[j] = scale * s[idx[j]] / sum_j' s[idx[j']]
+// Returns 0, or -1 on a bad shape (E % G != 0, topk_group outside [1, G], k > topk_group * E / G).
+int oracle_route_grouped(const float* logits, const float* bias, int T, int E, int k, int n_group,
+                         int topk_group, float scale, int32_t* idx, float* w) {
+    if (!valid_shape(T, E, k) || n_group < 1 || E % n_group != 0 || topk_group < 1 ||
+        topk_group > n_group || k > topk_group * (E / n_group))
+        return -1;
+    const int gs = E / n_group;
+    const int q = std::min(gs, std::max(1, k / topk_group));
+    std::vector<float> sc(E), c(E), gscore(n_group), tmp(gs);
+    std::vector<int> gorder(n_group), eorder;
+    std::vector<char> kept(n_group);
+    for (int t = 0; t < T; ++t) {
+        const float* l = logits + static_cast<size_t>(t) * E;
+        for (int e = 0; e < E; ++e) {
+            sc[e] = 1.0f / (1.0f + std::exp(-l[e]));
+            c[e] = sc[e] + bias[e];
+        }
+        // Group scores: the q largest selection scores of each group, added largest first.
+        for (int g = 0; g < n_group; ++g) {
+            for (int i = 0; i < gs; ++i) tmp[i] = c[g * gs + i];
+            std::sort(tmp.begin(), tmp.end(), [](float a, float b) { return a > b; });
+            float sum = 0.0f;
+            for (int i = 0; i < q; ++i) sum += tmp[i];
+            gscore[g] = sum;
+        }
+        std::iota(gorder.begin(), gorder.end(), 0);
+        std::stable_sort(gorder.begin(), gorder.end(), [&](int a, int b) { return gscore[a] > gscore[b]; });
+        std::fill(kept.begin(), kept.end(), 0);
+        for (int i = 0; i < topk_group; ++i) kept[gorder[i]] = 1;
+        // Candidates: the kept groups' experts, ascending id; a stable sort by c keeps equal
+        // scores in ascending id.
+        eorder.clear();
+        for (int e = 0; e < E; ++e)
+            if (kept[e / gs]) eorder.push_back(e);
+        std::stable_sort(eorder.begin(), eorder.end(), [&](int a, int b) { return c[a] > c[b]; });
+        float ssum = 0.0f;
+        for (int j = 0; j < k; ++j) ssum += sc[eorder[j]];
+        for (int j = 0; j < k; ++j) {
+            idx[static_cast<size_t>(t) * k + j] = eorder[j];
+            w[static_cast<size_t>(t) * k + j] = scale * (sc[eorder[j]] / ssum);
         }
     }
     return 0;
@@ -223,50 +284,59 @@ void oracle_combine(const float* y, const float* w, const int32_t* dest, int T, 
     }
 }
 
-// The whole layer: steps 1-5 in order.  x [T,d] bf16, logits [T,E] fp32, W_gate_up [E,d,2f] bf16,
-// W_down [E,f,d] bf16 -> out [T,d] fp32.  Returns 0 or a negative code from route/permute.
-int oracle_forward(const uint16_t* x, const float* logits, const uint16_t* Wgu, const uint16_t* Wd,
-                   int T, int d, int f, int E, int k, float* out) {
+// Steps 2-5 for a given routing: idx/w [T,k] (from either router) -> out [T,d] fp32.  x [T,d] bf16,
+// W_gate_up [E,d,2f] bf16, W_down [E,f,d] bf16.  Returns 0 or a negative code from permute.
+int oracle_forward_routed(const uint16_t* x, const int32_t* idx, const float* w, const uint16_t* Wgu,
+                          const uint16_t* Wd, int T, int d, int f, int E, int k, float* out) {
     if (!valid_shape(T, E, k) || d < 1 || f < 1) return -1;
     const size_t M = static_cast<size_t>(T) * k;
-    std::vector<int32_t> idx(M), counts(E), offsets(E + 1), src(M), dest(M);
-    std::vector<float> w(M);
-    int rc = oracle_route(logits, T, E, k, idx.data(), w.data());
-    if (rc) return rc;
-    rc = oracle_permute(idx.data(), T, E, k, counts.data(), offsets.data(), src.data(), dest.data());
+    std::vector<int32_t> counts(E), offsets(E + 1), src(M), dest(M);
+    int rc = oracle_permute(idx, T, E, k, counts.data(), offsets.data(), src.data(), dest.data());
     if (rc) return rc;
     std::vector<uint16_t> x_perm(M * d);
     oracle_gather_rows(x, src.data(), static_cast<int>(M), d, x_perm.data());
     std::vector<float> h(M * f), y(M * d);
     oracle_gateup_swiglu(x_perm.data(), offsets.data(), E, Wgu, d, f, h.data());
     oracle_down(h.data(), offsets.data(), E, Wd, d, f, y.data());
-    oracle_combine(y.data(), w.data(), dest.data(), T, d, k, out);
+    oracle_combine(y.data(), w, dest.data(), T, d, k, out);
     return 0;
 }
 
-// The layer's output for a chosen subset of tokens only (out_rows [ntok, d] fp32).  Every token's
-// output depends only on its own logits and x row, so this is the same definition restricted to
-// those tokens: route the token, run each chosen expert's FFN on its x row, combine in slot order.
-// Used to check full-size workloads on sampled tokens.  Returns 0 or a negative code.
-int oracle_forward_tokens(const uint16_t* x, const float* logits, const uint16_t* Wgu,
-                          const uint16_t* Wd, int T, int d, int f, int E, int k,
-                          const int32_t* tokens, int ntok, float* out_rows) {
+// The whole layer: steps 1-5 in order, with the softmax top-k router.  x [T,d] bf16, logits [T,E]
+// fp32, W_gate_up [E,d,2f] bf16, W_down [E,f,d] bf16 -> out [T,d] fp32.  Returns 0 or a negative
+// code from route/permute.
+int oracle_forward(const uint16_t* x, const float* logits, const uint16_t* Wgu, const uint16_t* Wd,
+                   int T, int d, int f, int E, int k, float* out) {
+    if (!valid_shape(T, E, k) || d < 1 || f < 1) return -1;
+    const size_t M = static_cast<size_t>(T) * k;
+    std::vector<int32_t> idx(M);
+    std::vector<float> w(M);
+    int rc = oracle_route(logits, T, E, k, idx.data(), w.data());
+    if (rc) return rc;
+    return oracle_forward_routed(x, idx.data(), w.data(), Wgu, Wd, T, d, f, E, k, out);
+}
+
+// The layer's output for a chosen subset of tokens only (out_rows [ntok, d] fp32), given those
+// tokens' routing idx_rows/w_rows [ntok, k].  Every token's output depends only on its own routing
+// and x row, so this is the same definition restricted to those tokens: run each chosen expert's
+// FFN on the token's x row, combine in slot order.  Returns 0 or a negative code.
+int oracle_forward_tokens_routed(const uint16_t* x, const int32_t* idx_rows, const float* w_rows,
+                                 const uint16_t* Wgu, const uint16_t* Wd, int T, int d, int f, int E,
+                                 int k, const int32_t* tokens, int ntok, float* out_rows) {
     if (!valid_shape(T, E, k) || d < 1 || f < 1) return -1;
     for (int s = 0; s < ntok; ++s)
         if (tokens[s] < 0 || tokens[s] >= T) return -1;
     const size_t npairs = static_cast<size_t>(ntok) * k;
-    std::vector<int32_t> idx(npairs);
-    std::vector<float> w(npairs), ys(npairs * d);
-    for (int s = 0; s < ntok; ++s)
-        oracle_route(logits + static_cast<size_t>(tokens[s]) * E, 1, E, k, idx.data() + s * k,
-                     w.data() + s * k);
+    for (size_t q = 0; q < npairs; ++q)
+        if (idx_rows[q] < 0 || idx_rows[q] >= E) return -2;
+    std::vector<float> ys(npairs * d);
 #pragma omp parallel
     {
         std::vector<float> xr(d), g(f), u(f), h(f);
 #pragma omp for schedule(dynamic, 1)
         for (long long q = 0; q < static_cast<long long>(npairs); ++q) {
             const int s = static_cast<int>(q / k);
-            const int e = idx[q];
+            const int e = idx_rows[q];
             const uint16_t* xt = x + static_cast<size_t>(tokens[s]) * d;
             for (int i = 0; i < d; ++i) xr[i] = bf16_to_f32(xt[i]);
             gateup_row(xr.data(), Wgu + static_cast<size_t>(e) * d * 2 * f, d, f, h.data(), g.data(),
@@ -278,12 +348,29 @@ int oracle_forward_tokens(const uint16_t* x, const float* logits, const uint16_t
         float* o = out_rows + static_cast<size_t>(s) * d;
         for (int m = 0; m < d; ++m) o[m] = 0.0f;
         for (int j = 0; j < k; ++j) {
-            const float wj = w[static_cast<size_t>(s) * k + j];
+            const float wj = w_rows[static_cast<size_t>(s) * k + j];
             const float* yr = ys.data() + (static_cast<size_t>(s) * k + j) * d;
             for (int m = 0; m < d; ++m) o[m] += wj * yr[m];
         }
     }
     return 0;
+}
+
+// The same with the softmax top-k router: each sampled token is routed from its own logits row.
+int oracle_forward_tokens(const uint16_t* x, const float* logits, const uint16_t* Wgu,
+                          const uint16_t* Wd, int T, int d, int f, int E, int k,
+                          const int32_t* tokens, int ntok, float* out_rows) {
+    if (!valid_shape(T, E, k) || d < 1 || f < 1) return -1;
+    for (int s = 0; s < ntok; ++s)
+        if (tokens[s] < 0 || tokens[s] >= T) return -1;
+    const size_t npairs = static_cast<size_t>(ntok) * k;
+    std::vector<int32_t> idx(npairs);
+    std::vector<float> w(npairs);
+    for (int s = 0; s < ntok; ++s)
+        oracle_route(logits + static_cast<size_t>(tokens[s]) * E, 1, E, k, idx.data() + s * k,
+                     w.data() + s * k);
+    return oracle_forward_tokens_routed(x, idx.data(), w.data(), Wgu, Wd, T, d, f, E, k, tokens, ntok,
+                                        out_rows);
 }
 
 }  // extern "C"

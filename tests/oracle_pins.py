@@ -270,5 +270,127 @@ def pin_stages(O, seed=9):
     assert np.array_equal(full, out)
 
 
+# --------------------------------------------------------------------------------------------
+# The second router (DeepSeek-V3's): s = sigmoid(logit), selection score c = s + bias, experts in
+# G equal groups, group score = sum of the group's q = k / topk_group largest c, keep the
+# topk_group best groups (equal -> lower group), then the k largest c among their experts (equal
+# -> lower id), w = scale * s / sum(s over the chosen).
+# --------------------------------------------------------------------------------------------
+def pin_grouped_hand_example(O):
+    """Hand-worked cases with exact fp32 values (all logits 0, so s = 1/2 everywhere, and
+    dyadic biases).  E = 8 in G = 2 groups {0..3}, {4..7}; topk_group = 1; k = 2 (q = 2); scale 2.5.
+      bias A = [.5, -.25, -.25, -.25, .125, .125, -.5, -.5] -> c = [1, .25, .25, .25, .625, .625, 0, 0]
+        group scores 1 + .25 = 1.25 and .625 + .625 = 1.25: a tie, the lower group (0) is kept;
+        inside it c = 1 first, then a three-way tie at .25 -> id 1.  idx [0, 1], w = 2.5 * [.5, .5].
+      bias B = A with bias[4] = .25 -> group 1 scores .75 + .625 = 1.375 > 1.25: group 1 is kept and
+        idx = [4, 5] although expert 0 has the largest c overall (plain top-2 would give [0, 4]).
+      The bias moves the selection only: w = 2.5 * [.5, .5] = [1.25, 1.25] in both cases."""
+    logits = np.zeros((2, 8), np.float32)
+    bias_a = np.array([.5, -.25, -.25, -.25, .125, .125, -.5, -.5], np.float32)
+    bias_b = bias_a.copy()
+    bias_b[4] = .25
+    idx, w = O.route_grouped(logits, bias_a, 2, 2, 1, 2.5)
+    assert idx.tolist() == [[0, 1], [0, 1]], idx
+    assert w.tolist() == [[1.25, 1.25], [1.25, 1.25]], w
+    idx, w = O.route_grouped(logits, bias_b, 2, 2, 1, 2.5)
+    assert idx.tolist() == [[4, 5], [4, 5]], idx
+    assert w.tolist() == [[1.25, 1.25], [1.25, 1.25]], w
+    # Weights from distinct affinities (no bias, one group, k = 3 of 4): closed form in float64.
+    lg = np.array([[math.log(3.0), 0.0, -math.log(3.0), math.log(7.0)]], np.float32)
+    idx, w = O.route_grouped(lg, np.zeros(4, np.float32), 3, 1, 1, 1.0)
+    assert idx.tolist() == [[3, 0, 1]], idx  # sigma: 7/8 > 3/4 > 1/2 > 1/4
+    ref = np.array([7 / 8, 3 / 4, 1 / 2]) / (7 / 8 + 3 / 4 + 1 / 2)
+    np.testing.assert_allclose(w[0], ref, rtol=1e-6, atol=0)
+
+
+def pin_grouped_reduces_to_topk(O, seed=21):
+    """One group and no bias: sigmoid is increasing, so the chosen ids are the k largest logits —
+    the softmax router's ids (pinned to numpy's argsort above) — and the weights are scipy's
+    expit of those logits, normalised and scaled."""
+    rng = np.random.default_rng(seed)
+    for T, E, k, scale in [(40, 8, 2, 1.0), (25, 64, 6, 2.5), (16, 256, 8, 2.5), (9, 5, 5, 0.5)]:
+        logits = rng.standard_normal((T, E)).astype(np.float32)
+        idx, w = O.route_grouped(logits, np.zeros(E, np.float32), k, 1, 1, scale)
+        ref_idx, _ = O.route(logits, k)
+        assert np.array_equal(idx, np.argsort(-logits.astype(np.float64), axis=1, kind="stable")[:, :k])
+        assert np.array_equal(idx, ref_idx)
+        s = expit(np.take_along_axis(logits, idx, 1).astype(np.float64))
+        np.testing.assert_allclose(w, scale * s / s.sum(1, keepdims=True), rtol=1e-6, atol=0)
+
+
+def grouped_brute_force(logits, bias, k, G, topk_group, scale):
+    """float64 brute force over every set of topk_group groups and every k-subset of their experts.
+    Returns (idx, w, margin): margin = the smallest score gap a decision rested on, so callers can
+    skip decisions that float32 rounding could flip."""
+    import itertools
+    T, E = logits.shape
+    gs = E // G
+    q = min(gs, max(1, k // topk_group))
+    idx = np.empty((T, k), np.int64)
+    w = np.empty((T, k))
+    margin = np.empty(T)
+    for t in range(T):
+        s = 1.0 / (1.0 + np.exp(-logits[t].astype(np.float64)))
+        c = s + bias.astype(np.float64)
+        gsc = [sum(sorted(c[g * gs:(g + 1) * gs], reverse=True)[:q]) for g in range(G)]
+        best = max(itertools.combinations(range(G), topk_group), key=lambda gg: sum(gsc[g] for g in gg))
+        allowed = [e for e in range(E) if e // gs in best]
+        pick = max(itertools.combinations(allowed, k), key=lambda es: sum(c[e] for e in es))
+        pick = sorted(pick, key=lambda e: -c[e])
+        idx[t] = pick
+        w[t] = scale * s[pick] / s[pick].sum()
+        kept_g = sorted(gsc[g] for g in best)
+        rest_g = [gsc[g] for g in range(G) if g not in best]
+        rest_e = [c[e] for e in allowed if e not in pick]
+        gaps = [kept_g[0] - max(rest_g)] if rest_g else [1.0]
+        gaps += [min(c[pick]) - max(rest_e)] if rest_e else []
+        gaps += list(-np.diff(c[pick]))
+        margin[t] = min(gaps)
+    return idx, w, margin
+
+
+def pin_grouped_brute_force(O, seed=23):
+    """Random layers against the float64 brute force: the same groups, ids and slot order, and
+    the same weights to 1e-6, wherever the decision margin is wider than float32 rounding."""
+    rng = np.random.default_rng(seed)
+    checked = 0
+    for T, E, k, G, tg, scale in [(30, 8, 2, 2, 1, 2.5), (30, 16, 4, 4, 2, 1.0), (20, 16, 3, 4, 3, 1.5),
+                                  (20, 12, 4, 3, 2, 2.5), (10, 32, 8, 8, 4, 2.5)]:
+        logits = rng.standard_normal((T, E)).astype(np.float32)
+        bias = (0.2 * rng.standard_normal(E)).astype(np.float32)
+        idx, w = O.route_grouped(logits, bias, k, G, tg, scale)
+        ref_idx, ref_w, margin = grouped_brute_force(logits, bias, k, G, tg, scale)
+        ok = margin > 1e-5
+        assert ok.mean() > 0.9
+        assert np.array_equal(idx[ok], ref_idx[ok]), (T, E, k, G, tg)
+        np.testing.assert_allclose(w[ok], ref_w[ok], rtol=1e-6, atol=0)
+        checked += int(ok.sum())
+    assert checked > 100
+
+
+def pin_grouped_invariants(O, seed=29):
+    """DeepSeek-V3-shaped routing (E = 256, 8 groups of 32, 4 groups kept, top-8): distinct ids
+    from at most 4 groups, weights summing to the scale, weights proportional to sigmoid(logit),
+    and no unchosen expert of a kept group beating a chosen one on s + bias."""
+    rng = np.random.default_rng(seed)
+    T, E, k, G, tg, scale = 64, 256, 8, 8, 4, 2.5
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    bias = (0.1 * rng.standard_normal(E)).astype(np.float32)
+    idx, w = O.route_grouped(logits, bias, k, G, tg, scale)
+    s = expit(logits.astype(np.float64))
+    c = s + bias
+    for t in range(T):
+        ids = idx[t].tolist()
+        assert len(set(ids)) == k and all(0 <= e < E for e in ids)
+        groups = {e // 32 for e in ids}
+        assert len(groups) <= tg
+        np.testing.assert_allclose(w[t].sum(), scale, rtol=1e-6)
+        np.testing.assert_allclose(w[t] / w[t].sum(), s[t, ids] / s[t, ids].sum(), rtol=1e-6)
+        assert np.all(np.diff(c[t, ids]) <= 1e-7)  # slot order: descending selection score
+        kept = [e for e in range(E) if e // 32 in groups and e not in ids]
+        assert max(c[t, kept]) <= min(c[t, ids]) + 1e-7
+
+
 ALL_PINS = [pin_hand_example, pin_brute_force, pin_dense_e1_k1, pin_route_library,
-            pin_permute_library, pin_invariants, pin_stages]
+            pin_permute_library, pin_invariants, pin_stages, pin_grouped_hand_example,
+            pin_grouped_reduces_to_topk, pin_grouped_brute_force, pin_grouped_invariants]

@@ -35,6 +35,17 @@ MUTANTS = {
     "down_wrong_expert": ("const uint16_t* We = Wd + static_cast<size_t>(e) * f * d;\n#pragma omp parallel for",
                           "const uint16_t* We = Wd + static_cast<size_t>((e + 1) % E) * f * d;\n#pragma omp parallel for"),
     "gather_wrong_row": ("x + static_cast<size_t>(src[r]) * d,", "x + static_cast<size_t>(src[M - 1 - r]) * d,"),
+    # the DeepSeek-V3 router
+    "grouped_bias_in_weights": ("w[static_cast<size_t>(t) * k + j] = scale * (sc[eorder[j]] / ssum);",
+                                "w[static_cast<size_t>(t) * k + j] = scale * (c[eorder[j]] / ssum);"),
+    "grouped_no_bias": ("c[e] = sc[e] + bias[e];", "c[e] = sc[e];"),
+    "grouped_top1_group_score": ("const int q = std::min(gs, std::max(1, k / topk_group));", "const int q = 1;"),
+    "grouped_no_group_limit": ("for (int i = 0; i < topk_group; ++i) kept[gorder[i]] = 1;",
+                               "for (int i = 0; i < n_group; ++i) kept[gorder[i]] = 1;"),
+    "grouped_no_scale": ("= scale * (sc[eorder[j]] / ssum);", "= (sc[eorder[j]] / ssum);"),
+    "grouped_group_ties_higher": ("return gscore[a] > gscore[b]; });",
+                                  "return gscore[a] > gscore[b] || (gscore[a] == gscore[b] && a > b); });"),
+    "grouped_affinity_sign": ("sc[e] = 1.0f / (1.0f + std::exp(-l[e]));", "sc[e] = 1.0f / (1.0f + std::exp(l[e]));"),
 }
 
 _CHILD = textwrap.dedent("""
