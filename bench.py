@@ -41,7 +41,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from mixture_experts_grouped_fp32_gb300.workloads import WORKLOADS, Workload, bf16_bits, make_inputs  # noqa: E402
+from mixture_experts_grouped_fp32_gb300.workloads import (WORKLOADS, Workload, bf16_bits, draw_router_bias,  # noqa: E402
+                                                          make_inputs)
 
 METRIC = "MoE-layer tokens/s and TFLOP/s, % of roofline (1×GB300), T=32..4096"
 DEFAULT_WORKLOAD = "mixtral_t32"
@@ -222,8 +223,15 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if args.flush_l2 else None
     stream = torch.cuda.current_stream(dev)
 
+    grouped = w.router[0] == "grouped"
+    bias_d = draw_router_bias(w, seed=args.seed + rank).to(dev)
+
     def step():
-        moe.forward(x_d, l_d, wgu, wd, w.k, out=out, workspace=ws)
+        if grouped:  # DeepSeek-V3's router as step 1
+            _, G, tg, scale, _ = w.router
+            moe.forward_grouped(x_d, l_d, bias_d, wgu, wd, w.k, G, tg, scale, out=out, workspace=ws)
+        else:
+            moe.forward(x_d, l_d, wgu, wd, w.k, out=out, workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -280,7 +288,8 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
                                           v["h"], v["y_perm"])
     st = v["status"]
     calls = [
-        lambda: moe.route(l_d, w.k, idx=idx, w=wts),
+        (lambda: moe.route_grouped(l_d, bias_d, w.k, *w.router[1:4], idx=idx, w=wts)) if grouped else
+        (lambda: moe.route(l_d, w.k, idx=idx, w=wts)),
         lambda: moe.permute(idx, x_d, w.E, status=st, out=(counts_d, offs, src, dest, xp)),
         lambda: moe.grouped_gemm_gateup_swiglu(xp, wgu, offs, h=h, status=st),
         lambda: moe.grouped_gemm_down(h, wd, offs, y_perm=y, status=st, ksplit=v["ksplit"]),
@@ -301,17 +310,29 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     staged_step_ms = statistics.mean(sev[i][0].elapsed_time(sev[i][5]) for i in range(args.steps))
 
     # ---- e2e through moe_forward_host ---------------------------------------------------------
+    # (grouped router: the same host->device copies, moe_forward_grouped and the copy back, each
+    # enqueued on the stream by the binding)
     xh, lh = x.pin_memory(), logits.pin_memory()
     oh = torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        if grouped:
+            x_d.copy_(xh, non_blocking=True)
+            l_d.copy_(lh, non_blocking=True)
+            step()
+            oh.copy_(out, non_blocking=True)
+        else:
+            moe.forward_host(xh, lh, wgu, wd, w.k, oh, ws)
+
     for _ in range(max(1, args.warmup)):
-        moe.forward_host(xh, lh, wgu, wd, w.k, oh, ws)
+        e2e_step()
     torch.cuda.synchronize(dev)
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps):
         if flush is not None:
             flush.zero_()
         eev[i][0].record(stream)
-        moe.forward_host(xh, lh, wgu, wd, w.k, oh, ws)
+        e2e_step()
         eev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
@@ -357,16 +378,21 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
 # ----------------------------------------------------------------------------------------------
 # Oracle timing (CPU baseline and the reference arm)
 # ----------------------------------------------------------------------------------------------
-def oracle_sample_runner(w: Workload, logits, x, wgu, wd):
+def oracle_sample_runner(w: Workload, logits, x, wgu, wd, seed: int = 0):
     import oracle as oracle_pkg
     O = oracle_pkg.Oracle()
     xb = bf16_bits(x)
     ln = logits.numpy()
     wgub, wdb = bf16_bits(wgu), bf16_bits(wd)
+    bias = draw_router_bias(w, seed).numpy()
 
     def run(S: int) -> float:
         t0 = time.perf_counter()
-        O.forward(xb[:S], ln[:S], wgub, wdb, w.k)
+        if w.router[0] == "grouped":
+            idx, wts = O.route_grouped(ln[:S], bias, w.k, *w.router[1:4])
+            O.forward_routed(xb[:S], idx, wts, wgub, wdb)
+        else:
+            O.forward(xb[:S], ln[:S], wgub, wdb, w.k)
         return time.perf_counter() - t0
 
     return O, run
@@ -383,8 +409,8 @@ def pick_sample(run, T: int, budget_s: float) -> int:
     return S
 
 
-def cpu_baseline(w, logits, x, wgu, wd, budget_s: float):
-    O, run = oracle_sample_runner(w, logits, x, wgu, wd)
+def cpu_baseline(w, logits, x, wgu, wd, budget_s: float, seed: int = 0):
+    O, run = oracle_sample_runner(w, logits, x, wgu, wd, seed)
     S = pick_sample(run, w.T, budget_s)
     dt = run(S)
     return {"value": round(S / dt, 3), "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
@@ -397,7 +423,7 @@ def run_reference(args, w: Workload, rank: int, world: int):
         return None
     logits, x, wgu, wd = make_inputs(w, seed=args.seed, weight_device="cuda" if torch.cuda.is_available() else "cpu")
     wgu, wd = wgu.cpu(), wd.cpu()
-    O, run = oracle_sample_runner(w, logits, x, wgu, wd)
+    O, run = oracle_sample_runner(w, logits, x, wgu, wd, args.seed)
     n = args.steps + args.warmup
     per_step = max(0.5, min(20.0, 150.0 / max(1, n)))
     S = pick_sample(run, w.T, per_step)
@@ -421,7 +447,7 @@ def run_reference(args, w: Workload, rank: int, world: int):
 
 def config_of(w: Workload, args) -> dict:
     return {"workload": w.name, "T": w.T, "d_model": w.d, "d_ff": w.f, "experts": w.E, "top_k": w.k,
-            "logit_bias": list(w.bias), "seed": args.seed, "parallelism": "replicas",
+            "logit_bias": list(w.bias), "router": list(w.router), "seed": args.seed, "parallelism": "replicas",
             "l2": ("flushed between steps (512 MB write, outside the step events)" if args.flush_l2 else
                    "not flushed: inputs larger than L2 (the active experts' weights, >= 2.8 GB, stream "
                    "from HBM every step; L2 is 129 MB)")}
@@ -488,7 +514,7 @@ def main():
         if world == 1 and not args.no_cpu_baseline:
             logits, x = r["inputs"]
             wgu, wd = (t.cpu() for t in r["host_weights"])
-            line["cpu_baseline"] = cpu_baseline(w, logits, x, wgu, wd, args.cpu_budget_s)
+            line["cpu_baseline"] = cpu_baseline(w, logits, x, wgu, wd, args.cpu_budget_s, args.seed)
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

@@ -84,6 +84,25 @@ MOE_API int moe_workspace_layout(int T, int d, int f, int E, int top_k, size_t* 
 MOE_API int moe_route(const float* logits, int T, int E, int top_k, int32_t* idx, float* w,
               moe_stream_t stream);
 
+/* Step 1, second router — DeepSeek-V3's gating (DeepSeek-V3 Technical Report, section 2.1.2; the
+ * pages only name that model, so the definition comes from its report).  Per token, in fp32:
+ *   s[e] = 1 / (1 + exp(-logits[t,e]))      affinity
+ *   c[e] = s[e] + bias[e]                   selection score (the auxiliary-loss-free balancing bias
+ *                                           steers the choice only)
+ *   the E experts form n_group equal groups (experts g*E/n_group ..); a group's score is the sum of
+ *   its q = max(1, top_k / topk_group) largest c (the report's node-limited routing); the topk_group
+ *   best groups are kept (equal scores: lower group first);
+ *   idx[t,.] = the top_k largest c among the kept groups' experts (equal: lower id first), in slot
+ *   order of descending c;  w[t,j] = scale * s[idx[t,j]] / sum_j' s[idx[t,j']] (sum in slot order).
+ *   logits [T,E] fp32 in;  bias [E] fp32 in;  idx [T,top_k] int32 out;  w [T,top_k] fp32 out.
+ * DeepSeek-V3's own setting: E = 256, n_group = 8, topk_group = 4, top_k = 8, scale = 2.5.
+ * Requires 1 <= n_group <= 32 dividing E, 1 <= topk_group <= n_group, top_k <= topk_group * E /
+ * n_group, scale > 0 (else MOE_ERR_INVALID_ARG).  The selection compares fp32 values computed with
+ * the GPU's expf: a choice between scores within a few ulp of each other may differ from a CPU
+ * evaluation of the same formula; either choice is a valid top-k. */
+MOE_API int moe_route_grouped(const float* logits, const float* bias, int T, int E, int top_k, int n_group,
+                      int topk_group, float scale, int32_t* idx, float* w, moe_stream_t stream);
+
 /* Step 2 — permute ("dispatch", the data rearrangement before the grouped GEMM).  Groups the
  * T*top_k assignments by expert, tokens ascending within an expert (a stable counting sort, so
  * the result is unique and bit-exact):
@@ -167,6 +186,14 @@ MOE_API int moe_combine(const float* y_perm, const float* w, const int32_t* dest
 MOE_API int moe_forward(const void* x, const float* logits, const void* w_gate_up, const void* w_down,
                 int T, int d, int f, int E, int top_k, void* out, void* workspace,
                 size_t workspace_bytes, moe_stream_t stream);
+
+/* moe_forward with DeepSeek-V3's router (moe_route_grouped) as step 1; steps 2-5 as in
+ * moe_forward, with the same workspace (moe_workspace_size) and five launches.  bias [E] fp32 and
+ * n_group, topk_group, scale as for moe_route_grouped. */
+MOE_API int moe_forward_grouped(const void* x, const float* logits, const float* bias, const void* w_gate_up,
+                        const void* w_down, int T, int d, int f, int E, int top_k, int n_group,
+                        int topk_group, float scale, void* out, void* workspace, size_t workspace_bytes,
+                        moe_stream_t stream);
 
 /* moe_forward with the per-call tensors in HOST memory: x_host [T,d] bf16 and logits_host [T,E]
  * fp32 are copied to the device, the layer runs, and out [T,d] bf16 is copied back to out_host,

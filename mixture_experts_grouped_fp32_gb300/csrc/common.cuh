@@ -54,6 +54,9 @@ cudaError_t launch_k(int kernel_bit, void (*kernel)(KArgs...), dim3 grid, dim3 b
 // Launchers (defined next to their kernels).  All return the launch's error code.
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                          int32_t* status_reset, cudaStream_t s);
+cudaError_t launch_route_grouped(const float* logits, const float* bias, int T, int E, int k, int n_group,
+                                 int topk_group, float scale, int32_t* idx, float* w, int32_t* status_reset,
+                                 cudaStream_t s);
 cudaError_t launch_permute(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
                            int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest,
                            __nv_bfloat16* x_perm, int32_t* status, int num_sms, cudaStream_t s);
@@ -75,7 +78,8 @@ struct GemmArgs {
     int swap_max;          // experts with at most this many rows use the swapped orientation
     int pair;              // 0: 1-SM kernel; 1: SM pairs (cta_group::2), normal orientation only;
                            // 2: SM pairs with experts of at most pair_swap_max rows swapped
-    int pair_swap_max = 0; // swap threshold of the SM-pair kernel (pair == 2), at most 256
+    int pair_swap_max = 0; // swap threshold of the SM-pair kernel (pair == 2), at most 128
+    int pair_layout = 0;   // SM-pair kernel's shared-memory layout: 0 chosen on the device, 1 A, 2 B
     int inject_stall = 0;  // test hook (1-SM kernel): make one pipeline wait run out, see moe_api.cu
 };
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,

@@ -24,10 +24,12 @@
 // every CTA:
 //   layout A  six 32 KB stages plus a 4 KB token buffer each: chunks of C = 64 rows;
 //   layout B  five 40 KB stages (32 KB + 8 KB of tokens): chunks of C = 128 rows, one stage fewer.
-// Layout B is taken when more experts have 65..128 rows (swapped only under B) than there are
-// normal 256-row tiles (each slowed by the shallower pipeline); measured on the Mixtral shape at
-// T=512: near-uniform 103..147-row experts run best under A, a skewed batch with seven 74..104-row
-// experts under B.
+// Layout B is taken when some experts have 65..128 rows (swapped only under B) and they number
+// at least a quarter of the normal 256-row tiles (each slowed by the shallower pipeline).  Under
+// sustained load the GPU runs at its power cap, and a swapped expert's smaller MMA work raises the
+// clock for everything: Mixtral shape, T=512 (3 such experts, 5 tiles) 0.544 -> 0.533 ms/layer
+// with B, a skewed batch (7 experts, 2 tiles) 0.584 -> 0.523; the DeepSeek-V3 shape (5 experts,
+// 61 tiles) runs best under A (2.416 vs 2.451 ms).
 //   count <= min(swap_max, C)    one swapped chunk;
 //   otherwise                    256-row normal tiles; a remainder of at most C rows past the last
 //                                full tile becomes one swapped chunk, a larger one one more (partly
@@ -247,7 +249,7 @@ template <int KIND, bool SWAPCAP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
                         const __grid_constant__ CUtensorMap tmB, const int32_t* __restrict__ offsets, int M,
-                        int K, int N, int E, int ksplit, int swap_max, void* __restrict__ out,
+                        int K, int N, int E, int ksplit, int swap_max, int layout_mode, void* __restrict__ out,
                         int32_t* __restrict__ status) {
     constexpr int BN_OUT = Tiling<KIND>::BN_OUT;
     constexpr int SW_BOXES = KIND == 0 ? 4 : 2;  // weight boxes per CTA in a swapped item
@@ -299,8 +301,8 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         ok = __all_sync(0xffffffffu, ok);
         const int per = (E + 31) / 32;
         const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-        // Layout choice (swapping form): B when experts that only B swaps (65..128 rows)
-        // outnumber the normal 256-row tiles B would slow down.
+        // Layout choice (swapping form): B when there are experts that only B swaps (65..128
+        // rows) and they number at least a quarter of the normal 256-row tiles B slows down.
         int layout_b = 0;
         if (SWAPCAP && ok) {
             int mid = 0, tiles_b = 0;
@@ -314,8 +316,9 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 mid += __shfl_xor_sync(0xffffffffu, mid, o);
                 tiles_b += __shfl_xor_sync(0xffffffffu, tiles_b, o);
             }
-            layout_b = mid > tiles_b ? 1 : 0;
+            layout_b = (mid > 0 && 4 * mid >= tiles_b) ? 1 : 0;
         }
+        if (SWAPCAP && layout_mode != 0) layout_b = layout_mode == 2 ? 1 : 0;  // host override
         const int chunk = make_ring<SWAPCAP>(layout_b).chunk;
         int sum = 0;
         if (ok)
@@ -640,7 +643,7 @@ cudaError_t launch_pair_kind(const GemmArgs& a, int num_sms, cudaStream_t s, con
                                                                                       : a.pair_swap_max);
     return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_2sm_kernel<KIND, SWAPCAP>, dim3(grid),
                     dim3(NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB, a.offsets, a.M, a.K, a.N, a.E, ksplit,
-                    swap_max, a.out, a.status);
+                    swap_max, a.pair_layout, a.out, a.status);
 }
 
 }  // namespace

@@ -129,6 +129,14 @@ int use_pair(long long M, int E, int N, int kind) {
 // Swap threshold of the SM-pair kernel in mode 2: experts with at most this many rows run as one
 // swapped chunk (further capped on the device at 64 or 128 rows by the shared-memory layout the
 // kernel picks).  MOE_GEMM_PAIR_SWAP_MAX overrides (clamped to [0, 128]).
+// Shared-memory layout of the swapping SM-pair kernel: 0 = chosen on the device from the row
+// counts (default), 1 = layout A (six stages), 2 = layout B (five stages, 128-row chunks).
+// MOE_GEMM_PAIR_LAYOUT overrides; a measurement knob.
+int pair_layout() {
+    const char* v = std::getenv("MOE_GEMM_PAIR_LAYOUT");
+    return v ? (v[0] == 'A' || v[0] == '1' ? 1 : (v[0] == 'B' || v[0] == '2' ? 2 : 0)) : 0;
+}
+
 int pair_swap_max_rows() {
     const char* v = std::getenv("MOE_GEMM_PAIR_SWAP_MAX");
     int x = v ? std::atoi(v) : 128;
@@ -202,8 +210,33 @@ P* at(void* base, size_t off) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The router of a layer: the softmax top-k router when `grouped` is false, else DeepSeek-V3's
+// (sigmoid affinity, selection bias, group-limited top-k, scaled weights).
+struct Router {
+    bool grouped = false;
+    const float* bias = nullptr;
+    int n_group = 1, topk_group = 1;
+    float scale = 1.0f;
+};
+
+int check_router(const Router& r, int E, int k, const char* name) {
+    if (!r.grouped) return MOE_OK;
+    if (!r.bias) return fail(MOE_ERR_INVALID_ARG, "%s: null bias", name);
+    if (r.n_group < 1 || r.n_group > 32 || E % r.n_group != 0)
+        return fail(MOE_ERR_INVALID_ARG, "%s: n_group = %d must divide E = %d and lie in [1, 32]", name, r.n_group, E);
+    if (r.topk_group < 1 || r.topk_group > r.n_group)
+        return fail(MOE_ERR_INVALID_ARG, "%s: topk_group = %d outside [1, n_group = %d]", name, r.topk_group,
+                    r.n_group);
+    if (k > r.topk_group * (E / r.n_group))
+        return fail(MOE_ERR_INVALID_ARG, "%s: top_k = %d exceeds the %d experts of the kept groups", name, k,
+                    r.topk_group * (E / r.n_group));
+    if (!(r.scale > 0.0f) || r.scale > 3.0e38f)
+        return fail(MOE_ERR_INVALID_ARG, "%s: scale must be a positive finite number", name);
+    return MOE_OK;
+}
+
 int run_layer(const void* x, const float* logits, const void* wgu, const void* wd, int T, int d, int f,
-              int E, int k, void* out, void* ws, int num_sms, cudaStream_t s) {
+              int E, int k, void* out, void* ws, int num_sms, cudaStream_t s, const Router& router = Router()) {
     const Layout L = layout(T, d, f, E, k);
     int32_t* status = at<int32_t>(ws, L.status);
     int32_t* idx = at<int32_t>(ws, L.idx);
@@ -217,16 +250,21 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
     float* y = at<float>(ws, L.y_perm);
     const int M = T * k;
     cudaError_t e;
-    if ((e = launch_route(logits, T, E, k, idx, w, status, s)) != cudaSuccess) return launched(e, "route");
+    e = router.grouped ? launch_route_grouped(logits, router.bias, T, E, k, router.n_group, router.topk_group,
+                                              router.scale, idx, w, status, s)
+                       : launch_route(logits, T, E, k, idx, w, status, s);
+    if (e != cudaSuccess) return launched(e, "route");
     if ((e = launch_permute(idx, static_cast<const __nv_bfloat16*>(x), T, d, E, k, counts, offsets, src,
                             dest, x_perm, status, num_sms, s)) != cudaSuccess)
         return launched(e, "permute");
     const char* why = "";
     const int swap_max = swap_max_rows(), ksplit = down_ksplit(T, d, f, E, k);
-    GemmArgs g1{x_perm, wgu, offsets, M, d, f, E, h, status, 1, swap_max, use_pair(M, E, f, 0), pair_swap_max_rows()};
+    GemmArgs g1{x_perm, wgu, offsets, M, d, f, E, h, status, 1, swap_max, use_pair(M, E, f, 0), pair_swap_max_rows(),
+                pair_layout()};
     if ((e = launch_grouped_gemm(0, g1, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "gate+up GEMM: %s (%s)", why, cudaGetErrorString(e));
-    GemmArgs g2{h, wd, offsets, M, f, d, E, y, status, ksplit, swap_max, use_pair(M, E, d, 1), pair_swap_max_rows()};
+    GemmArgs g2{h, wd, offsets, M, f, d, E, y, status, ksplit, swap_max, use_pair(M, E, d, 1), pair_swap_max_rows(),
+                pair_layout()};
     if ((e = launch_grouped_gemm(1, g2, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "down GEMM: %s (%s)", why, cudaGetErrorString(e));
     if ((e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) !=
@@ -316,6 +354,26 @@ int moe_route(const float* logits, int T, int E, int top_k, int32_t* idx, float*
                     "route");
 }
 
+int moe_route_grouped(const float* logits, const float* bias, int T, int E, int top_k, int n_group,
+                      int topk_group, float scale, int32_t* idx, float* w, moe_stream_t stream) {
+    int rc = check_shape(T, -1, 0, E, top_k, false);
+    if (rc) return rc;
+    Router r;
+    r.grouped = true;
+    r.bias = bias;
+    r.n_group = n_group;
+    r.topk_group = topk_group;
+    r.scale = scale;
+    if ((rc = check_router(r, E, top_k, "moe_route_grouped"))) return rc;
+    if (T == 0) return ok();
+    if (!logits || !idx || !w) return fail(MOE_ERR_INVALID_ARG, "moe_route_grouped: null pointer");
+    int sms;
+    if ((rc = check_device(&sms))) return rc;
+    return launched(launch_route_grouped(logits, bias, T, E, top_k, n_group, topk_group, scale, idx, w, nullptr,
+                                         static_cast<cudaStream_t>(stream)),
+                    "route_grouped");
+}
+
 int moe_permute(const int32_t* idx, const void* x, int T, int d, int E, int top_k, int32_t* counts,
                 int32_t* offsets, int32_t* src, int32_t* dest, void* x_perm, int32_t* status,
                 moe_stream_t stream) {
@@ -351,6 +409,7 @@ static int gemm_entry(int kind, const void* A, const void* B, const int32_t* off
     GemmArgs g = kind == 0 ? GemmArgs{A, B, offsets, M, d, f, E, out, status, 1, swap_max_rows(), pair}
                            : GemmArgs{A, B, offsets, M, f, d, E, out, status, ksplit, swap_max_rows(), pair};
     g.pair_swap_max = pair_swap_max_rows();
+    g.pair_layout = pair_layout();
     g.inject_stall = inject_stall();
     const char* why = "";
     cudaError_t e = launch_grouped_gemm(kind, g, sms, static_cast<cudaStream_t>(stream), &why);
@@ -405,6 +464,35 @@ int moe_forward(const void* x, const float* logits, const void* w_gate_up, const
     if ((rc = check_device(&sms))) return rc;
     return run_layer(x, logits, w_gate_up, w_down, T, d, f, E, top_k, out, workspace, sms,
                      static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward_grouped(const void* x, const float* logits, const float* bias, const void* w_gate_up,
+                        const void* w_down, int T, int d, int f, int E, int top_k, int n_group, int topk_group,
+                        float scale, void* out, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    int rc = check_shape(T, d, f, E, top_k, true);
+    if (rc) return rc;
+    Router r;
+    r.grouped = true;
+    r.bias = bias;
+    r.n_group = n_group;
+    r.topk_group = topk_group;
+    r.scale = scale;
+    if ((rc = check_router(r, E, top_k, "moe_forward_grouped"))) return rc;
+    if (T == 0) return ok();
+    if (!x || !logits || !w_gate_up || !w_down || !out)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_grouped: null pointer");
+    if (!aligned16(x) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(out))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_grouped: bf16 tensors must be 16-byte aligned");
+    const size_t need = layout(T, d, f, E, top_k).total;
+    if (!workspace || workspace_bytes < need)
+        return fail(MOE_ERR_WORKSPACE, "moe_forward_grouped: workspace %zu bytes < %zu needed", workspace_bytes,
+                    need);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(MOE_ERR_WORKSPACE, "moe_forward_grouped: workspace must be 256-byte aligned");
+    int sms;
+    if ((rc = check_device(&sms))) return rc;
+    return run_layer(x, logits, w_gate_up, w_down, T, d, f, E, top_k, out, workspace, sms,
+                     static_cast<cudaStream_t>(stream), r);
 }
 
 int moe_forward_host(const void* x_host, const float* logits_host, const void* w_gate_up, const void* w_down,

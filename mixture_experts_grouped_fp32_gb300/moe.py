@@ -27,6 +27,9 @@ _SIGS = {
     "moe_workspace_layout": ([_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _I),
     "moe_host_staging_size": ([_I, _I, _I], _SZ),
     "moe_route": ([_P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_route_grouped": ([_P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P], _I),
+    "moe_forward_grouped": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _SZ, _P],
+                            _I),
     "moe_permute": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_gateup_swiglu": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gemm_down": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
@@ -124,6 +127,21 @@ def route(logits: torch.Tensor, top_k: int, idx=None, w=None, stream=None):
     return idx, w
 
 
+def route_grouped(logits: torch.Tensor, bias: torch.Tensor, top_k: int, n_group: int, topk_group: int,
+                  scale: float = 1.0, idx=None, w=None, stream=None):
+    """DeepSeek-V3's router (sigmoid affinity, selection bias, group-limited top-k, scaled weights)."""
+    _dev(logits, torch.float32, "logits")
+    _dev(bias, torch.float32, "bias")
+    T, E = logits.shape
+    if bias.shape != (E,):
+        raise ValueError(f"bias must have shape ({E},), got {tuple(bias.shape)}")
+    idx = idx if idx is not None else torch.empty(T, top_k, dtype=torch.int32, device=logits.device)
+    w = w if w is not None else torch.empty(T, top_k, dtype=torch.float32, device=logits.device)
+    _call("moe_route_grouped", _ptr(logits), _ptr(bias), T, E, top_k, n_group, topk_group, float(scale), _ptr(idx),
+          _ptr(w), _stream(stream))
+    return idx, w
+
+
 def permute(idx: torch.Tensor, x: torch.Tensor, E: int, status: torch.Tensor | None = None, stream=None,
             out: tuple | None = None):
     """Returns (counts, offsets, src, dest, x_perm); ``out`` may supply those five buffers."""
@@ -215,6 +233,25 @@ def forward(x, logits, w_gate_up, w_down, top_k, out=None, workspace=None, strea
     out = out if out is not None else torch.empty(T, d, dtype=torch.bfloat16, device=x.device)
     _call("moe_forward", _ptr(x), _ptr(logits), _ptr(w_gate_up), _ptr(w_down), T, d, f2 // 2, E, top_k,
           _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    return out
+
+
+def forward_grouped(x, logits, bias, w_gate_up, w_down, top_k, n_group, topk_group, scale=1.0, out=None,
+                    workspace=None, stream=None):
+    """The layer with DeepSeek-V3's router as step 1 (five kernel launches).  Returns ``out``."""
+    _dev(x, torch.bfloat16, "x")
+    _dev(logits, torch.float32, "logits")
+    _dev(bias, torch.float32, "bias")
+    _dev(w_gate_up, torch.bfloat16, "w_gate_up")
+    _dev(w_down, torch.bfloat16, "w_down")
+    T, d = x.shape
+    E, _, f2 = w_gate_up.shape
+    if workspace is None:
+        workspace = torch.empty(workspace_size(T, d, f2 // 2, E, top_k), dtype=torch.uint8, device=x.device)
+    out = out if out is not None else torch.empty(T, d, dtype=torch.bfloat16, device=x.device)
+    _call("moe_forward_grouped", _ptr(x), _ptr(logits), _ptr(bias), _ptr(w_gate_up), _ptr(w_down), T, d, f2 // 2,
+          E, top_k, n_group, topk_group, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+          _stream(stream))
     return out
 
 

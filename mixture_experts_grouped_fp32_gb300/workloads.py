@@ -13,6 +13,9 @@ Draw recipe (seed s, default 0):
     CPU would take ~15 s; small layers are drawn on the CPU.  A CUDA-drawn tensor is reproducible
     for a given torch build, which is all a parity check needs (both sides read the same tensor).
 
+  * The grouped router's selection bias (DeepSeek-V3 workload only): bias_std * N(0,1) [E] from a
+    CPU generator seeded ``s + 2``.
+
 Workload shapes are those of the pages' benchmarks: a Mixtral-8x7B-shaped MoE layer (d_model
 4096, d_ff 14336, 8 experts, top-2) and a DeepSeek-V3-shaped routed-expert layer (d_model 7168,
 d_ff 2048 per expert, 256 experts, top-8) — "Triton-MoE-Dispatch-Kernel erreicht 131 % von
@@ -41,6 +44,9 @@ class Workload:
     #   ("zipf", s)          + log(r**-s) with rank r = e + 1 (expert 0 most popular)
     bias: tuple = ("none", 0.0)
     note: str = field(default="", compare=False)
+    # Router: ("softmax",) — softmax top-k renormalised; or ("grouped", n_group, topk_group, scale,
+    # bias_std) — DeepSeek-V3's sigmoid router with a selection bias drawn N(0, bias_std^2).
+    router: tuple = ("softmax",)
 
     @property
     def M(self) -> int:
@@ -65,8 +71,21 @@ WORKLOADS = {
         Workload("deepseek_e32_t256", 256, 7168, 2048, 32, 8, ("zipf", 1.2),
                  note="profiling-scale DeepSeek-V3-shaped layer: same expert shapes and skew, "
                       "32 experts (2.8 GB of weights, small enough for a full ncu capture)"),
+        Workload("deepseek_v3_t2048", 2048, 7168, 2048, 256, 8, ("zipf", 1.2),
+                 note="DeepSeek-V3-shaped routed experts with DeepSeek-V3's own router: sigmoid "
+                      "affinities, selection bias, 8 groups of 32 experts, 4 groups kept, scale 2.5",
+                 router=("grouped", 8, 4, 2.5, 0.1)),
     ]
 }
+
+
+def draw_router_bias(w: Workload, seed: int = 0) -> torch.Tensor:
+    """The grouped router's per-expert selection bias, fp32 [E] on the CPU: N(0, bias_std^2) from a
+    generator seeded ``seed + 2`` (zeros for the softmax router, which has none)."""
+    if w.router[0] != "grouped":
+        return torch.zeros(w.E, dtype=torch.float32)
+    g = torch.Generator("cpu").manual_seed(seed + 2)
+    return (torch.randn(w.E, generator=g, dtype=torch.float32) * float(w.router[4])).contiguous()
 
 
 def logit_bias(E: int, bias: tuple) -> torch.Tensor:

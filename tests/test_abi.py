@@ -111,6 +111,22 @@ def test_stage_calls_reject_bad_arguments(lib):
     assert lib.moe_get_device_error(None, None) == -1
 
 
+def test_grouped_router_rejects_bad_groups(lib):
+    p = ctypes.c_void_p(1 << 20)
+    f = ctypes.c_float
+    assert lib.moe_route_grouped(p, None, 4, 256, 8, 8, 4, f(2.5), p, p, None) == -1   # null bias
+    assert "bias" in _err(lib)
+    assert lib.moe_route_grouped(p, p, 4, 256, 8, 7, 4, f(2.5), p, p, None) == -1      # 7 does not divide 256
+    assert lib.moe_route_grouped(p, p, 4, 256, 8, 64, 4, f(2.5), p, p, None) == -1     # more than 32 groups
+    assert lib.moe_route_grouped(p, p, 4, 256, 8, 8, 9, f(2.5), p, p, None) == -1      # topk_group > n_group
+    assert lib.moe_route_grouped(p, p, 4, 16, 8, 8, 2, f(1.0), p, p, None) == -1       # k > 2 groups x 2
+    assert "kept groups" in _err(lib)
+    assert lib.moe_route_grouped(p, p, 4, 256, 8, 8, 4, f(0.0), p, p, None) == -1      # scale
+    assert lib.moe_route_grouped(p, p, 0, 256, 8, 8, 4, f(2.5), p, p, None) == 0       # empty batch
+    assert lib.moe_forward_grouped(p, p, p, p, p, 4, 64, 128, 16, 8, 8, 2, f(1.0), p, p, 1 << 40, None) == -1
+    assert lib.moe_forward_grouped(p, p, p, p, p, 0, 64, 128, 256, 8, 8, 4, f(2.5), p, p, 1 << 40, None) == 0
+
+
 def test_empty_batch_is_a_no_op(lib):
     # T = 0 (and M = 0) launch nothing and succeed, so they need no device.
     p = ctypes.c_void_p(1 << 20)
