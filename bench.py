@@ -372,6 +372,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         "host_weights": (wgu, wd), "inputs": (logits, x), "step_ms_p10_p90": (
             float(np.percentile(step_ms, 10)), float(np.percentile(step_ms, 90))),
         "peak_src": peak_src, "peaks": peaks, "ksplit": v["ksplit"],
+        "launches_per_step": 5 if grouped else moe.forward_launch_count(w.T, w.E, w.k),
     }
 
 
@@ -508,7 +509,7 @@ def main():
             "e2e": {"value": round(w.T / (r["e2e_ms"] * 1e-3), 2), "unit": "tokens/s",
                     "h2d_bytes_per_step": w.T * w.d * 2 + w.T * w.E * 4, "d2h_bytes_per_step": w.T * w.d * 2,
                     "ms_per_step": round(r["e2e_ms"], 4)},
-            "gpu_launches": 5 * args.steps,
+            "gpu_launches": r["launches_per_step"] * args.steps,
             "clocks": r["clocks"],
         }
         if world == 1 and not args.no_cpu_baseline:

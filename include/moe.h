@@ -236,8 +236,12 @@ MOE_API int moe_forward_noalloc(const void* x, const float* logits, const void* 
  * the workspace of moe_forward — into *code (0 = no device-side error). */
 MOE_API int moe_get_device_error(const void* status_or_workspace, int32_t* code);
 
-/* Number of kernel launches one moe_forward call makes (5). */
-MOE_API int moe_forward_launch_count(void);
+/* Number of kernel launches one moe_forward call makes for this shape: 4 when routing and the
+ * permutation run as one kernel (E <= 32 and T*E <= 8192: each block routes every token itself to
+ * build its histogram, so no grid-wide synchronisation is needed), else 5 (route, permute, two
+ * grouped GEMMs, combine); 0 for T = 0; -1 for an invalid shape.  moe_forward_grouped always
+ * makes 5.  The environment variable MOE_FUSE_ROUTE_PERMUTE=0 turns the fusion off. */
+MOE_API int moe_forward_launch_count(int T, int E, int top_k);
 
 /* Message for the last non-OK return on the calling thread ("" if none). */
 MOE_API const char* moe_last_error_string(void);

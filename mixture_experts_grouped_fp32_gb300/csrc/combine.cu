@@ -5,9 +5,13 @@
 // DeepGEMM PR #304 write-up, section 1.1 ("combine"); HPC-Ops page, FusedMoE paragraph (the
 // weighted-average reduce after the GroupGEMM).
 //
-// Gather form: each block owns one token and reads its k rows, so no two blocks write the same
-// output and no atomics are needed — the result is deterministic.  Accesses are 2 x 16-byte fp32
-// loads per slot and one 16-byte bf16 store per 8 output elements, coalesced across the block.
+// Gather form: block (t, c) owns a set of token t's output columns (every gridDim.y-th group of
+// 1024) and reads those columns of the token's k rows, so no two blocks write the same output and
+// no atomics are needed — the result is deterministic.  Each thread owns 8 outputs at a time: it
+// issues all k slots' 2 x 16-byte fp32 loads before adding them in slot order, then one 16-byte
+// bf16 store; accesses are coalesced across the block.  Few tokens split their columns over
+// several blocks so that enough loads are in flight (T=32: 128 blocks instead of 32); many tokens
+// use one block each (T=4096: 4096 blocks of 4 column groups rather than 16384 blocks of one).
 #include "common.cuh"
 
 namespace moe {
@@ -18,7 +22,9 @@ constexpr int kMaxK = 8;
 
 // SPLIT = y_perm holds more than one K slice (kept a template so the common single-slice case
 // has no inner loop between the slot loads).
-template <bool SPLIT>
+// KB = slots held in registers at once (k <= KB): sized to k so that a top-2 layer does not
+// reserve registers for eight slots (which would cost occupancy).
+template <bool SPLIT, int KB>
 __global__ void __launch_bounds__(kCombThreads)
 combine_kernel(const float4* __restrict__ y, const float* __restrict__ w,
                const int32_t* __restrict__ dest, int T, int d, int k, int ksplit, uint4* __restrict__ out,
@@ -39,24 +45,30 @@ combine_kernel(const float4* __restrict__ y, const float* __restrict__ w,
     __syncthreads();
 
     const int dv = d / 8;  // groups of 8 outputs
-    for (int v = tid; v < dv; v += kCombThreads) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < k; ++j) {
-            const int r = rows[j];
-            if (r < 0) continue;
-            const float wj = wts[j];
-            const float4* yr = y + static_cast<size_t>(r) * (d / 4) + 2 * v;
-            float4 a = __ldg(yr), b = __ldg(yr + 1);
-            if (SPLIT)
-            for (int s = 1; s < ksplit; ++s) {
-                const float4* ys = yr + static_cast<size_t>(s) * M * (d / 4);
-                const float4 a2 = __ldg(ys), b2 = __ldg(ys + 1);
-                a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
-                b.x += b2.x; b.y += b2.y; b.z += b2.z; b.w += b2.w;
+    for (int v = blockIdx.y * kCombThreads + tid; v < dv; v += gridDim.y * kCombThreads) {
+        float4 a[KB], b[KB];
+#pragma unroll
+        for (int j = 0; j < KB; ++j)
+            if (j < k && rows[j] >= 0) {
+                const float4* yr = y + static_cast<size_t>(rows[j]) * (d / 4) + 2 * v;
+                a[j] = __ldg(yr);
+                b[j] = __ldg(yr + 1);
+                if (SPLIT)
+                    for (int s = 1; s < ksplit; ++s) {
+                        const float4* ys = yr + static_cast<size_t>(s) * M * (d / 4);
+                        const float4 a2 = __ldg(ys), b2 = __ldg(ys + 1);
+                        a[j].x += a2.x; a[j].y += a2.y; a[j].z += a2.z; a[j].w += a2.w;
+                        b[j].x += b2.x; b[j].y += b2.y; b[j].z += b2.z; b[j].w += b2.w;
+                    }
             }
-            acc[0] += wj * a.x; acc[1] += wj * a.y; acc[2] += wj * a.z; acc[3] += wj * a.w;
-            acc[4] += wj * b.x; acc[5] += wj * b.y; acc[6] += wj * b.z; acc[7] += wj * b.w;
-        }
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < KB; ++j)
+            if (j < k && rows[j] >= 0) {
+                const float wj = wts[j];
+                acc[0] += wj * a[j].x; acc[1] += wj * a[j].y; acc[2] += wj * a[j].z; acc[3] += wj * a[j].w;
+                acc[4] += wj * b[j].x; acc[5] += wj * b[j].y; acc[6] += wj * b[j].z; acc[7] += wj * b[j].w;
+            }
         uint4 o;
         o.x = pack_bf16x2(acc[0], acc[1]);
         o.y = pack_bf16x2(acc[2], acc[3]);
@@ -70,8 +82,16 @@ combine_kernel(const float4* __restrict__ y, const float* __restrict__ w,
 
 cudaError_t launch_combine(const float* y, const float* w, const int32_t* dest, int T, int d, int k,
                            int ksplit, __nv_bfloat16* out, int32_t* status, cudaStream_t s) {
-    auto kernel = ksplit > 1 ? combine_kernel<true> : combine_kernel<false>;
-    return launch_k(kPdlCombine, kernel, dim3(T), dim3(kCombThreads), 0, s, reinterpret_cast<const float4*>(y), w,
+    auto kernel = k <= 2 ? (ksplit > 1 ? combine_kernel<true, 2> : combine_kernel<false, 2>)
+                : k <= 4 ? (ksplit > 1 ? combine_kernel<true, 4> : combine_kernel<false, 4>)
+                         : (ksplit > 1 ? combine_kernel<true, 8> : combine_kernel<false, 8>);
+    // Column groups per token: enough blocks for ~4 per SM on a 152-SM GPU, at most one per
+    // 1024-column group.
+    const int groups = (d / 8 + kCombThreads - 1) / kCombThreads;
+    int split = (4 * 152 + T - 1) / T;
+    split = split < 1 ? 1 : (split > groups ? groups : split);
+    const dim3 grid(T, split);
+    return launch_k(kPdlCombine, kernel, grid, dim3(kCombThreads), 0, s, reinterpret_cast<const float4*>(y), w,
                     dest, T, d, k, ksplit, reinterpret_cast<uint4*>(out), status);
 }
 

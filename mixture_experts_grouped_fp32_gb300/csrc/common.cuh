@@ -60,6 +60,12 @@ cudaError_t launch_route_grouped(const float* logits, const float* bias, int T, 
 cudaError_t launch_permute(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
                            int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest,
                            __nv_bfloat16* x_perm, int32_t* status, int num_sms, cudaStream_t s);
+// Steps 1+2 in one launch (softmax router): only when route_permute_fusable(T, E).
+bool route_permute_fusable(int T, int E);
+cudaError_t launch_route_permute(const float* logits, const __nv_bfloat16* x, int T, int d, int E, int k,
+                                 int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* src,
+                                 int32_t* dest, __nv_bfloat16* x_perm, int32_t* status, int num_sms,
+                                 cudaStream_t s);
 cudaError_t launch_combine(const float* y, const float* w, const int32_t* dest, int T, int d, int k,
                            int ksplit, __nv_bfloat16* out, int32_t* status, cudaStream_t s);
 

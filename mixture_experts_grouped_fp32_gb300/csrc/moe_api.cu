@@ -143,6 +143,15 @@ int pair_swap_max_rows() {
     return x < 0 ? 0 : (x > 128 ? 128 : x);
 }
 
+// Whether moe_forward runs routing and the permutation as one launch (softmax router, E <= 32,
+// T*E <= 8192: every block can afford to route all tokens itself).  MOE_FUSE_ROUTE_PERMUTE=0
+// turns it off.
+bool fuse_route_permute(int T, int E) {
+    const char* v = std::getenv("MOE_FUSE_ROUTE_PERMUTE");
+    if (v && v[0] == '0') return false;
+    return route_permute_fusable(T, E);
+}
+
 // Failure-detection test hook, off unless the environment sets MOE_INJECT_STALL=1: the next
 // grouped-GEMM launches run on the 1-SM kernel with one pipeline stage armed for bytes that never
 // arrive, so a bounded wait expires (~1 s), the kernel reports MOE_STATUS_WAIT_TIMEOUT in the
@@ -250,13 +259,19 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
     float* y = at<float>(ws, L.y_perm);
     const int M = T * k;
     cudaError_t e;
-    e = router.grouped ? launch_route_grouped(logits, router.bias, T, E, k, router.n_group, router.topk_group,
-                                              router.scale, idx, w, status, s)
-                       : launch_route(logits, T, E, k, idx, w, status, s);
-    if (e != cudaSuccess) return launched(e, "route");
-    if ((e = launch_permute(idx, static_cast<const __nv_bfloat16*>(x), T, d, E, k, counts, offsets, src,
-                            dest, x_perm, status, num_sms, s)) != cudaSuccess)
-        return launched(e, "permute");
+    if (!router.grouped && fuse_route_permute(T, E)) {
+        if ((e = launch_route_permute(logits, static_cast<const __nv_bfloat16*>(x), T, d, E, k, idx, w, counts,
+                                      offsets, src, dest, x_perm, status, num_sms, s)) != cudaSuccess)
+            return launched(e, "route+permute");
+    } else {
+        e = router.grouped ? launch_route_grouped(logits, router.bias, T, E, k, router.n_group, router.topk_group,
+                                                  router.scale, idx, w, status, s)
+                           : launch_route(logits, T, E, k, idx, w, status, s);
+        if (e != cudaSuccess) return launched(e, "route");
+        if ((e = launch_permute(idx, static_cast<const __nv_bfloat16*>(x), T, d, E, k, counts, offsets, src,
+                                dest, x_perm, status, num_sms, s)) != cudaSuccess)
+            return launched(e, "permute");
+    }
     const char* why = "";
     const int swap_max = swap_max_rows(), ksplit = down_ksplit(T, d, f, E, k);
     GemmArgs g1{x_perm, wgu, offsets, M, d, f, E, h, status, 1, swap_max, use_pair(M, E, f, 0), pair_swap_max_rows(),
@@ -309,7 +324,11 @@ extern "C" {
 
 int moe_version(void) { return 100; }
 
-int moe_forward_launch_count(void) { return 5; }
+int moe_forward_launch_count(int T, int E, int top_k) {
+    if (check_shape(T, -1, 0, E, top_k, false) != MOE_OK) return -1;
+    if (T == 0) return 0;
+    return fuse_route_permute(T, E) ? 4 : 5;
+}
 
 const char* moe_last_error_string(void) { return g_err; }
 

@@ -20,6 +20,7 @@ constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;
 constexpr int kMaxTokPerBlock = 16;
 constexpr int kCopyBatch = 4;
+constexpr long long kFuseMaxLogits = 8192;  // route+permute fusion: T*E at most this
 
 __global__ void __launch_bounds__(kPermThreads)
 permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int T, int d, int E,
@@ -172,7 +173,176 @@ permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int
     }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Steps 1 and 2 in one launch, for small routing problems (E <= 32, T*E <= kFuseMaxLogits).
+// Every block routes ALL T tokens itself — a thread per token, the softmax router's selection
+// (k largest logits, equal logits -> lower id, slot order descending) — to build the histogram
+// the permutation needs, so no grid-wide synchronisation is required; it writes idx and w only
+// for its own chunk of tokens, then ranks and copies that chunk exactly as permute_kernel does.
+// The redundant routing reads T*E*4 bytes per block from L2 (at most 32 KB).  Measured on the
+// Mixtral shape (ms/layer, fused vs two launches): T=32 0.409 vs 0.413, T=512 0.512 vs 0.516,
+// T=4096 2.007 vs 1.992 — hence the limit T*E <= 8192.
+// ---------------------------------------------------------------------------------------------
+constexpr int kFuseMaxE = 32;
+
+__device__ __forceinline__ bool logit_before(float av, int ai, float bv, int bi) {
+    return av > bv || (av == bv && ai < bi);
+}
+
+__global__ void __launch_bounds__(kPermThreads)
+route_permute_kernel(const float* __restrict__ logits, const uint4* __restrict__ x, int T, int d, int E, int k,
+                     int tok_per_block, int32_t* __restrict__ idx, float* __restrict__ w,
+                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ src,
+                     int32_t* __restrict__ dest, uint4* __restrict__ x_perm, int32_t* __restrict__ status) {
+    __shared__ int tot[kFuseMaxE];
+    __shared__ int before[kFuseMaxE];
+    __shared__ int off[kFuseMaxE + 1];
+    __shared__ int cidx[kMaxTokPerBlock * kMaxK];
+    __shared__ int crow[kMaxTokPerBlock * kMaxK];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();
+    pdl_trigger();
+    if (status != nullptr && blockIdx.x == 0 && tid == 0) *status = 0;  // first kernel of the layer
+    if (tid < E) {
+        tot[tid] = 0;
+        before[tid] = 0;
+    }
+    __syncthreads();
+    const int t0 = blockIdx.x * tok_per_block;
+    const int t1 = min(T, t0 + tok_per_block);
+
+    // Route every token (thread per token); warp-aggregated histogram updates.
+    for (int base = warp * 32; base < T; base += kPermThreads) {
+        const int t = base + lane;
+        const bool active = t < T;
+        int sel[kMaxK];
+        float selv[kMaxK];
+        unsigned used = 0u;
+        const float* row = logits + static_cast<size_t>(active ? t : 0) * E;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            sel[j] = 0;
+            selv[j] = 0.0f;
+            if (j < k) {
+                int bi = -1;
+                float bv = 0.0f;
+                for (int e = 0; e < E; ++e) {
+                    const float v = __ldg(row + e);
+                    if (!(used & (1u << e)) && (bi < 0 || logit_before(v, e, bv, bi))) {
+                        bi = e;
+                        bv = v;
+                    }
+                }
+                used |= 1u << bi;
+                sel[j] = bi;
+                selv[j] = bv;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            if (j < k) {
+                const int key = active ? (sel[j] * 2 + (t < t0 ? 1 : 0)) : -1;
+                const unsigned peers = __match_any_sync(0xffffffffu, key);
+                if (active && lane == __ffs(peers) - 1) {
+                    atomicAdd(&tot[sel[j]], __popc(peers));
+                    if (t < t0) atomicAdd(&before[sel[j]], __popc(peers));
+                }
+            }
+        }
+        if (active && t >= t0 && t < t1) {
+            // Weights of the block's own tokens: softmax restricted to the chosen k.
+            float ex[kMaxK], sum = 0.0f;
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) {
+                ex[j] = 0.0f;
+                if (j < k) {
+                    ex[j] = expf(selv[j] - selv[0]);
+                    sum += ex[j];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j)
+                if (j < k) {
+                    idx[static_cast<size_t>(t) * k + j] = sel[j];
+                    w[static_cast<size_t>(t) * k + j] = ex[j] / sum;
+                    cidx[(t - t0) * k + j] = sel[j];
+                }
+        }
+    }
+    __syncthreads();
+
+    // Exclusive scan of tot (E <= 32: one expert per lane of warp 0).
+    if (warp == 0) {
+        const int v = lane < E ? tot[lane] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        if (lane < E) off[lane] = incl - v;
+        if (lane == 31) off[E] = incl;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        if (tid < E) counts[tid] = tot[tid];
+        if (tid <= E) offsets[tid] = off[tid];
+    }
+
+    // Rank this chunk's assignments (ids are valid by construction) and copy its rows.
+    const int nloc = (t1 - t0) * k, a0 = t0 * k;
+    if (tid < nloc) {
+        const int e = cidx[tid];
+        const int tl = tid / k;
+        int rank = 0;
+        for (int i = 0; i < tl * k; ++i) rank += (cidx[i] == e);
+        const int row = off[e] + before[e] + rank;
+        src[row] = t0 + tl;
+        dest[a0 + tid] = row;
+        crow[tid] = row;
+    }
+    __syncthreads();
+    const int dv = d / 8;
+    const int nvec = (t1 - t0) * dv;
+    for (int base = tid; base < nvec; base += kPermThreads * kCopyBatch) {
+        uint4 val[kCopyBatch];
+#pragma unroll
+        for (int u = 0; u < kCopyBatch; ++u) {
+            const int i = base + u * kPermThreads;
+            if (i < nvec) {
+                const int tl = i / dv, v = i - tl * dv;
+                val[u] = __ldg(x + static_cast<size_t>(t0 + tl) * dv + v);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyBatch; ++u) {
+            const int i = base + u * kPermThreads;
+            if (i < nvec) {
+                const int tl = i / dv, v = i - tl * dv;
+                for (int j = 0; j < k; ++j) x_perm[static_cast<size_t>(crow[tl * k + j]) * dv + v] = val[u];
+            }
+        }
+    }
+}
+
 }  // namespace
+
+bool route_permute_fusable(int T, int E) {
+    return E <= kFuseMaxE && static_cast<long long>(T) * E <= kFuseMaxLogits;
+}
+
+cudaError_t launch_route_permute(const float* logits, const __nv_bfloat16* x, int T, int d, int E, int k,
+                                 int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* src,
+                                 int32_t* dest, __nv_bfloat16* x_perm, int32_t* status, int num_sms,
+                                 cudaStream_t s) {
+    int tpb = (T + 4 * num_sms - 1) / (4 * num_sms);
+    tpb = tpb < 1 ? 1 : (tpb > kMaxTokPerBlock ? kMaxTokPerBlock : tpb);
+    const int blocks = (T + tpb - 1) / tpb;
+    return launch_k(kPdlRoute, route_permute_kernel, dim3(blocks), dim3(kPermThreads), 0, s, logits,
+                    reinterpret_cast<const uint4*>(x), T, d, E, k, tpb, idx, w, counts, offsets, src, dest,
+                    reinterpret_cast<uint4*>(x_perm), status);
+}
 
 cudaError_t launch_permute(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
                            int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest,

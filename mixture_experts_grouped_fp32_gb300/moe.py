@@ -21,7 +21,7 @@ _I = ctypes.c_int
 _SZ = ctypes.c_size_t
 _SIGS = {
     "moe_version": ([], _I),
-    "moe_forward_launch_count": ([], _I),
+    "moe_forward_launch_count": ([_I, _I, _I], _I),
     "moe_last_error_string": ([], ctypes.c_char_p),
     "moe_workspace_size": ([_I, _I, _I, _I, _I], _SZ),
     "moe_workspace_layout": ([_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _I),
@@ -114,8 +114,9 @@ def host_staging_size(T: int, d: int, E: int) -> int:
     return int(load().moe_host_staging_size(T, d, E))
 
 
-def forward_launch_count() -> int:
-    return int(load().moe_forward_launch_count())
+def forward_launch_count(T: int, E: int, top_k: int) -> int:
+    """Kernel launches of one moe_forward call for this shape (4 with route+permute fused, else 5)."""
+    return int(load().moe_forward_launch_count(T, E, top_k))
 
 
 def route(logits: torch.Tensor, top_k: int, idx=None, w=None, stream=None):

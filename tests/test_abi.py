@@ -37,7 +37,18 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_launch_count(lib):
     assert lib.moe_version() >= 100
-    assert lib.moe_forward_launch_count() == 5
+    assert lib.moe_forward_launch_count(32, 8, 2) == 4       # route+permute fused
+    assert lib.moe_forward_launch_count(1024, 8, 2) == 4     # T*E = 8192
+    assert lib.moe_forward_launch_count(1025, 8, 2) == 5
+    assert lib.moe_forward_launch_count(4096, 8, 2) == 5
+    assert lib.moe_forward_launch_count(2048, 256, 8) == 5   # E > 32
+    assert lib.moe_forward_launch_count(0, 8, 2) == 0
+    assert lib.moe_forward_launch_count(4, 8, 9) == -1
+    os.environ["MOE_FUSE_ROUTE_PERMUTE"] = "0"
+    try:
+        assert lib.moe_forward_launch_count(32, 8, 2) == 5
+    finally:
+        del os.environ["MOE_FUSE_ROUTE_PERMUTE"]
 
 
 def _err(lib):

@@ -55,12 +55,14 @@ def _forward_and_views(moe, w, logits, x, wgu, wd):
 # GEMM path variants: the default policy (small experts swapped on the 1-SM kernel, SM pairs when
 # the average expert has >= 128 rows, few-token down GEMM split over K), the 1-SM kernel with every
 # expert in the normal orientation, the SM-pair kernel for every shape in its normal-only form and
-# in its swapping form (thresholds 128 and 64 rows), and a forced 3-way K split.
+# in its swapping form (thresholds 128 and 64 rows), a forced 3-way K split, and routing and the
+# permutation as two launches where the default fuses them (E <= 32).
 MODES = {"default": {}, "noswap": {"MOE_GEMM_SWAP_MAX": "0", "MOE_GEMM_2SM": "0"},
          "pair": {"MOE_GEMM_2SM": "1"}, "pairswap": {"MOE_GEMM_2SM": "2"},
          "pairswap64": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_SWAP_MAX": "64"},
-         "ksplit3": {"MOE_DOWN_KSPLIT": "3"}}
-ENV_KNOBS = ("MOE_GEMM_SWAP_MAX", "MOE_DOWN_KSPLIT", "MOE_GEMM_2SM", "MOE_GEMM_PAIR_SWAP_MAX", "MOE_GEMM_2SM_DOWN")
+         "ksplit3": {"MOE_DOWN_KSPLIT": "3"}, "nofuse": {"MOE_FUSE_ROUTE_PERMUTE": "0"}}
+ENV_KNOBS = ("MOE_GEMM_SWAP_MAX", "MOE_DOWN_KSPLIT", "MOE_GEMM_2SM", "MOE_GEMM_PAIR_SWAP_MAX", "MOE_GEMM_2SM_DOWN",
+             "MOE_FUSE_ROUTE_PERMUTE", "MOE_GEMM_PAIR_LAYOUT")
 
 
 @pytest.fixture(params=sorted(MODES))
@@ -295,9 +297,12 @@ def _cudart():
     return None
 
 
-def test_forward_is_five_kernels_and_graph_capturable(moe):
-    """Capture one moe_forward in a CUDA graph: the runtime counts exactly five kernel nodes, and
-    replaying the graph reproduces the eager result bit for bit."""
+@pytest.mark.parametrize("fuse", ["1", "0"])
+def test_forward_launches_and_graph_capture(moe, fuse, monkeypatch):
+    """Capture one moe_forward in a CUDA graph: the runtime counts exactly the kernel nodes that
+    moe_forward_launch_count() states (4 with route+permute fused, 5 without), and replaying the
+    graph reproduces the eager result bit for bit."""
+    monkeypatch.setenv("MOE_FUSE_ROUTE_PERMUTE", fuse)
     w = WORKLOADS["tiny"]
     logits, x, wgu, wd = case_inputs(w)
     dev = torch.device(DEV)
@@ -326,7 +331,7 @@ def test_forward_is_five_kernels_and_graph_capturable(moe):
     if kinds is None:
         pytest.skip("no libcudart / raw_cuda_graph to count graph nodes")
     # cudaGraphNodeTypeKernel == 0
-    assert kinds.count(0) == moe.forward_launch_count() == 5, kinds
+    assert kinds.count(0) == moe.forward_launch_count(w.T, w.E, w.k) == (4 if fuse == "1" else 5), kinds
 
 
 def _graph_node_types(raw):
