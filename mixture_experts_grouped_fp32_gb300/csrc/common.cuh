@@ -86,6 +86,8 @@ struct GemmArgs {
                            // 2: SM pairs with experts of at most pair_swap_max rows swapped
     int pair_swap_max = 0; // swap threshold of the SM-pair kernel (pair == 2), at most 128
     int pair_layout = 0;   // SM-pair kernel's shared-memory layout: 0 chosen on the device, 1 A, 2 B
+    int pair_split = 0;    // SM-pair kernel (pair == 2): CTA pairs given to normal tiles when the
+                           // kinds are split between pairs; 0 = one round-robin over all slots
     int inject_stall = 0;  // test hook (1-SM kernel): make one pipeline wait run out, see moe_api.cu
 };
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,

@@ -91,6 +91,13 @@ constexpr int SMEM_BYTES = 232448;
 constexpr int SUPER_N = 256;                     // output columns of a swapped item
 constexpr int PAIR_SWAP_MAX_ROWS = 128;
 constexpr uint16_t BOTH_CTAS = 0x3;
+constexpr int kMixedSplit = 1 << 20;  // split_req value selecting the proportional merge
+constexpr int kAutoSplit = 1 << 21;   // split_req value: choose the split on the device
+// Cost model of the automatic split (ns per pipeline stage of one CTA pair, fitted to a sweep of
+// the split on the DeepSeek-V3-shaped gate+up GEMM: 0.373 us per 256x256x64 pair MMA stage of a
+// normal tile at the clock the tile phase runs at, 0.465 us per stage of a swapped chunk, which
+// streams 2 x 32 KB of weights and is bound by the bytes one SM pair keeps in flight).
+constexpr long long kNormalStageNs = 373, kSwapStageNs = 465;
 
 template <bool SWAPCAP>
 struct Cfg {
@@ -107,8 +114,11 @@ struct Ctl {
     int abort_flag;
     int total_items;
     int layout_b;  // swapping form: 1 = layout B (five 40 KB stages, 128-row chunks)
+    int split_p;   // split schedule: pairs [0, split_p) run normal slots, the rest swapped ones; 0 = off
+    int total_normal;
     int seg[MAX_E + 1];
-    int item_start[MAX_E + 1];
+    int item_start[MAX_E + 1];  // round-robin: first slot of each expert; split: first swapped slot
+    int nstart[MAX_E + 1];      // split: first normal slot of each expert
 };
 static_assert(Cfg<true>::TILES + 1024 + sizeof(Ctl) <= SMEM_BYTES, "shared memory budget");
 
@@ -231,6 +241,83 @@ __device__ __forceinline__ PairItem decode_pair_item(const Ctl& c, const Tiling<
     return it;
 }
 
+// Split schedule (swapping form only): the normal slots and the swapped slots are numbered
+// separately, each expert-major.  Normal slot numbering inside an expert: super tile, M-tile pair,
+// K-slice (kind 0: one slot = N-tiles 2s and 2s+1, as in the round-robin order); swapped: super
+// tile, K-slice.
+template <int KIND>
+__device__ __forceinline__ int expert_normal_slots(int cnt, const Tiling<KIND>& t, int ksplit, int swap_max,
+                                                   int chunk) {
+    const RowSplit s = split_rows<true>(cnt, swap_max, chunk);
+    return (KIND == 0 ? t.n_super : (t.n_super - 1) * Tiling<KIND>::R + t.r_last) * s.np * ksplit;
+}
+template <int KIND>
+__device__ __forceinline__ int expert_swap_slots(int cnt, const Tiling<KIND>& t, int ksplit, int swap_max,
+                                                 int chunk) {
+    return t.n_super * split_rows<true>(cnt, swap_max, chunk).ns * ksplit;
+}
+
+template <int KIND>
+__device__ __forceinline__ PairItem decode_split_item(const Ctl& c, const Tiling<KIND>& t, int E, int ksplit,
+                                                      int swap_max, int chunk, int rank, bool normal, int i) {
+    const int* start = normal ? c.nstart : c.item_start;
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (start[mid] <= i) lo = mid; else hi = mid;
+    }
+    PairItem it;
+    it.e = lo;
+    const int cnt = c.seg[lo + 1] - c.seg[lo];
+    const RowSplit s = split_rows<true>(cnt, swap_max, chunk);
+    const int j = i - start[lo];
+    it.nsub = 1;
+    if (normal) {
+        const int per_st = s.np * ksplit;
+        const int st = j / per_st;
+        const int r = j - st * per_st;
+        const int mpair = r / ksplit;
+        it.kslice = r - mpair * ksplit;
+        if (KIND == 0) {
+            it.n_tile = 2 * st;
+            it.nsub = st == t.n_super - 1 ? t.r_last : 2;
+        } else {
+            it.n_tile = st;
+        }
+        const int mtile = 2 * mpair + rank;
+        it.row0 = c.seg[lo] + mtile * BM;
+        it.rows = min(BM, cnt - mtile * BM);
+        it.swap = 0;
+        it.ntok = 0;
+    } else {
+        const int st = j / ksplit;
+        it.kslice = j - st * ksplit;
+        it.n_tile = st;
+        it.row0 = c.seg[lo] + s.sbase;
+        it.rows = min(chunk, cnt - s.sbase);
+        it.swap = 1;
+        it.ntok = (it.rows + 15) & ~15;
+    }
+    return it;
+}
+
+// The slots one CTA pair runs: `count` slots first, first + stride, ... of one numbering.
+struct Walk {
+    int first, stride, count, mode;  // mode 0 round-robin over all slots, 1 normal, 2 swapped,
+                                     // 3 round-robin over the proportional merge of both
+};
+
+// Mixed order (mode 3): the normal and the swapped slots merged in proportion to their counts
+// (n_normal : n_swap), slot i of the merge being normal iff floor((i+1) n / t) > floor(i n / t) —
+// so every CTA pair of the round-robin gets the same share of each kind, and spends time on each
+// in proportion to its work: tensor-bound tiles and weight streams run side by side on the GPU.
+__device__ __forceinline__ void mixed_slot(int i, int n_normal, int n_total, bool* normal, int* idx) {
+    const long long a = static_cast<long long>(i) * n_normal / n_total;
+    const long long b = static_cast<long long>(i + 1) * n_normal / n_total;
+    *normal = b > a;
+    *idx = *normal ? static_cast<int>(a) : i - static_cast<int>(a);
+}
+
 __device__ __forceinline__ void raise_abort(Ctl& c, int32_t* status) {
     *reinterpret_cast<volatile int*>(&c.abort_flag) = 1;
     flag_status(status, MOE_STATUS_WAIT_TIMEOUT);
@@ -249,8 +336,8 @@ template <int KIND, bool SWAPCAP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
                         const __grid_constant__ CUtensorMap tmB, const int32_t* __restrict__ offsets, int M,
-                        int K, int N, int E, int ksplit, int swap_max, int layout_mode, void* __restrict__ out,
-                        int32_t* __restrict__ status) {
+                        int K, int N, int E, int ksplit, int swap_max, int layout_mode, int split_req,
+                        void* __restrict__ out, int32_t* __restrict__ status) {
     constexpr int BN_OUT = Tiling<KIND>::BN_OUT;
     constexpr int SW_BOXES = KIND == 0 ? 4 : 2;  // weight boxes per CTA in a swapped item
     extern __shared__ uint8_t smem_raw[];
@@ -320,24 +407,87 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         }
         if (SWAPCAP && layout_mode != 0) layout_b = layout_mode == 2 ? 1 : 0;  // host override
         const int chunk = make_ring<SWAPCAP>(layout_b).chunk;
+        // Split schedule: only when both kinds of slot exist.
+        int nsum = 0, ssum = 0;
+        if (SWAPCAP && split_req != 0 && ok)
+            for (int e = e0; e < e1; ++e) {
+                const int cnt = c.seg[e + 1] - c.seg[e];
+                nsum += expert_normal_slots<KIND>(cnt, tiling, ksplit, swap_max, chunk);
+                ssum += expert_swap_slots<KIND>(cnt, tiling, ksplit, swap_max, chunk);
+            }
+        int ntot = nsum, stot = ssum;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            ntot += __shfl_xor_sync(0xffffffffu, ntot, o);
+            stot += __shfl_xor_sync(0xffffffffu, stot, o);
+        }
+        // Automatic split: P pairs for the normal tiles, in proportion to the modelled work of each
+        // kind.  Only when each kind is at least 15 % of it (otherwise one round-robin overlaps the
+        // little there is of the other kind well enough), and when most normal-tile stages belong
+        // to experts with two or more pair tiles — those reuse their weights from L2 and are bound
+        // by the tensor pipe; a one-tile expert streams its weights like a swapped chunk, and with
+        // both kinds memory-bound a split only unbalances the bytes (Mixtral T=512: +5 %).
+        int auto_p = 0;
+        if (SWAPCAP && split_req == kAutoSplit && ok) {
+            long long hs = 0, hs_reuse = 0, ls = 0;  // pair-stages: normal tiles, of them reused, swapped
+            const int n_tiles = (N + Tiling<KIND>::BN_OUT - 1) / Tiling<KIND>::BN_OUT;
+            for (int e = e0; e < e1; ++e) {
+                const RowSplit rs = split_rows<true>(c.seg[e + 1] - c.seg[e], swap_max, chunk);
+                const long long h = static_cast<long long>(rs.np) * n_tiles * num_kb;
+                hs += h;
+                hs_reuse += rs.np >= 2 ? h : 0;
+                ls += static_cast<long long>(rs.ns) * tiling.n_super * num_kb;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                hs += __shfl_xor_sync(0xffffffffu, hs, o);
+                hs_reuse += __shfl_xor_sync(0xffffffffu, hs_reuse, o);
+                ls += __shfl_xor_sync(0xffffffffu, ls, o);
+            }
+            const long long wh = hs * kNormalStageNs, wl = ls * kSwapStageNs, wt = wh + wl;
+            if (wt > 0 && 100 * wh >= 15 * wt && 100 * wl >= 15 * wt && 2 * hs_reuse >= hs) {
+                auto_p = static_cast<int>((2 * num_pairs * wh + wt) / (2 * wt));  // rounded
+                auto_p = max(1, min(num_pairs - 1, auto_p));
+            }
+        }
+        const int req = split_req == kAutoSplit ? auto_p : split_req;
+        const bool split = SWAPCAP && req > 0 && ok && ntot > 0 && stot > 0 &&
+                           (num_pairs >= 2 || req == kMixedSplit);
+        // Exclusive scans: round-robin slots into item_start; or normal slots into nstart and
+        // swapped slots into item_start.
         int sum = 0;
-        if (ok)
+        if (ok && !split)
             for (int e = e0; e < e1; ++e)
                 sum += expert_items<KIND, SWAPCAP>(c.seg[e + 1] - c.seg[e], tiling, ksplit, swap_max, chunk);
-        int incl = sum;
+        if (split) sum = ssum;
+        int incl = sum, nincl = nsum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
+            const int nv = __shfl_up_sync(0xffffffffu, nincl, o);
+            if (lane >= o) {
+                incl += v;
+                nincl += nv;
+            }
         }
-        int run = incl - sum;
+        int run = incl - sum, nrun = nincl - nsum;
         for (int e = e0; e < e1; ++e) {
+            const int cnt = c.seg[e + 1] - c.seg[e];
             c.item_start[e] = run;
-            if (ok) run += expert_items<KIND, SWAPCAP>(c.seg[e + 1] - c.seg[e], tiling, ksplit, swap_max, chunk);
+            c.nstart[e] = nrun;
+            if (split) {
+                run += expert_swap_slots<KIND>(cnt, tiling, ksplit, swap_max, chunk);
+                nrun += expert_normal_slots<KIND>(cnt, tiling, ksplit, swap_max, chunk);
+            } else if (ok) {
+                run += expert_items<KIND, SWAPCAP>(cnt, tiling, ksplit, swap_max, chunk);
+            }
         }
         if (lane == 31) {
             c.item_start[E] = incl;
+            c.nstart[E] = nincl;
             c.total_items = incl;
+            c.total_normal = split ? nincl : 0;
+            c.split_p = split ? (req == kMixedSplit ? kMixedSplit : min(req, num_pairs - 1)) : 0;
             c.layout_b = layout_b;
         }
         if (!ok && lane == 0 && leader) flag_status(status, MOE_STATUS_BAD_OFFSETS);
@@ -348,9 +498,21 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
     ptx::tc_fence_after();
 
     const uint32_t tmem_base = c.tmem_base;
-    const int total = c.total_items;
     const Ring ring = make_ring<SWAPCAP>(c.layout_b);
     const int chunk = ring.chunk;
+    Walk walk{pair_id, num_pairs, c.total_items, 0};
+    if (c.split_p == kMixedSplit)
+        walk = Walk{pair_id, num_pairs, c.total_normal + c.total_items, 3};
+    else if (c.split_p > 0)
+        walk = pair_id < c.split_p ? Walk{pair_id, c.split_p, c.total_normal, 1}
+                                   : Walk{pair_id - c.split_p, num_pairs - c.split_p, c.total_items, 2};
+    auto slot_at = [&](int i) {
+        if (walk.mode == 0) return decode_pair_item<KIND, SWAPCAP>(c, tiling, E, ksplit, swap_max, chunk, rank, i);
+        bool normal = walk.mode == 1;
+        int j = i;
+        if (walk.mode == 3) mixed_slot(i, c.total_normal, walk.count, &normal, &j);
+        return decode_split_item<KIND>(c, tiling, E, ksplit, swap_max, chunk, rank, normal, j);
+    };
     uint32_t fill_parity[STAGES_MAX];
     int filled_mask = 0;
 
@@ -361,8 +523,8 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         int stage = 0;
         uint32_t phase = 0;
         bool aborted = false;
-        for (int i = pair_id; i < total && !aborted; i += num_pairs) {
-          const PairItem slot = decode_pair_item<KIND, SWAPCAP>(c, tiling, E, ksplit, swap_max, chunk, rank, i);
+        for (int i = walk.first; i < walk.count && !aborted; i += walk.stride) {
+          const PairItem slot = slot_at(i);
           for (int sub = 0; sub < slot.nsub && !aborted; ++sub) {
             PairItem it = slot;
             it.n_tile += sub;
@@ -423,8 +585,8 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         int stage = 0;
         uint32_t phase = 0, acc = 0, acc_phase = 0;
         bool aborted = false;
-        for (int i = pair_id; i < total && !aborted; i += num_pairs) {
-          const PairItem slot = decode_pair_item<KIND, SWAPCAP>(c, tiling, E, ksplit, swap_max, chunk, rank, i);
+        for (int i = walk.first; i < walk.count && !aborted; i += walk.stride) {
+          const PairItem slot = slot_at(i);
           for (int sub = 0; sub < slot.nsub && !aborted; ++sub) {
             const PairItem& it = slot;
             const uint32_t idesc_swap = ptx::idesc_bf16_f32(2 * BM, static_cast<uint32_t>(it.ntok), 1, 0);
@@ -488,8 +650,8 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         const int r_local = quarter * 32 + lane;
         uint32_t acc = 0, acc_phase = 0;
         bool aborted = false;
-        for (int i = pair_id; i < total && !aborted; i += num_pairs) {
-          const PairItem slot = decode_pair_item<KIND, SWAPCAP>(c, tiling, E, ksplit, swap_max, chunk, rank, i);
+        for (int i = walk.first; i < walk.count && !aborted; i += walk.stride) {
+          const PairItem slot = slot_at(i);
           for (int sub = 0; sub < slot.nsub; ++sub) {
             PairItem it = slot;
             it.n_tile += sub;
@@ -643,7 +805,7 @@ cudaError_t launch_pair_kind(const GemmArgs& a, int num_sms, cudaStream_t s, con
                                                                                       : a.pair_swap_max);
     return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_2sm_kernel<KIND, SWAPCAP>, dim3(grid),
                     dim3(NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB, a.offsets, a.M, a.K, a.N, a.E, ksplit,
-                    swap_max, a.pair_layout, a.out, a.status);
+                    swap_max, a.pair_layout, a.pair_split, a.out, a.status);
 }
 
 }  // namespace

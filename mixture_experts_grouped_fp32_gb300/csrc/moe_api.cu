@@ -137,6 +137,19 @@ int pair_layout() {
     return v ? (v[0] == 'A' || v[0] == '1' ? 1 : (v[0] == 'B' || v[0] == '2' ? 2 : 0)) : 0;
 }
 
+// Schedule of the swapping SM-pair kernel.  Default "auto" (1 << 21): the kernel splits its CTA
+// pairs on the device between the normal tiles and the swapped chunks when both kinds carry much
+// work and the tiles are tensor-bound (DeepSeek-V3 shape, gate+up: 1.394 -> 1.217 ms), else one
+// round-robin over the slots in expert order.  MOE_GEMM_PAIR_SPLIT overrides: 0 = round-robin,
+// P > 0 = P pairs on normal tiles, "mix" = round-robin over both kinds merged in proportion.
+int pair_split() {
+    const char* v = std::getenv("MOE_GEMM_PAIR_SPLIT");
+    if (!v || v[0] == 'a') return 1 << 21;  // chosen on the device
+    if (v[0] == 'm') return 1 << 20;        // proportional merge
+    const int x = std::atoi(v);
+    return x < 0 ? 0 : (x > 1000 ? 1000 : x);
+}
+
 int pair_swap_max_rows() {
     const char* v = std::getenv("MOE_GEMM_PAIR_SWAP_MAX");
     int x = v ? std::atoi(v) : 128;
@@ -275,11 +288,11 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
     const char* why = "";
     const int swap_max = swap_max_rows(), ksplit = down_ksplit(T, d, f, E, k);
     GemmArgs g1{x_perm, wgu, offsets, M, d, f, E, h, status, 1, swap_max, use_pair(M, E, f, 0), pair_swap_max_rows(),
-                pair_layout()};
+                pair_layout(), pair_split()};
     if ((e = launch_grouped_gemm(0, g1, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "gate+up GEMM: %s (%s)", why, cudaGetErrorString(e));
     GemmArgs g2{h, wd, offsets, M, f, d, E, y, status, ksplit, swap_max, use_pair(M, E, d, 1), pair_swap_max_rows(),
-                pair_layout()};
+                pair_layout(), pair_split()};
     if ((e = launch_grouped_gemm(1, g2, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "down GEMM: %s (%s)", why, cudaGetErrorString(e));
     if ((e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) !=
@@ -429,6 +442,7 @@ static int gemm_entry(int kind, const void* A, const void* B, const int32_t* off
                            : GemmArgs{A, B, offsets, M, f, d, E, out, status, ksplit, swap_max_rows(), pair};
     g.pair_swap_max = pair_swap_max_rows();
     g.pair_layout = pair_layout();
+    g.pair_split = pair_split();
     g.inject_stall = inject_stall();
     const char* why = "";
     cudaError_t e = launch_grouped_gemm(kind, g, sms, static_cast<cudaStream_t>(stream), &why);

@@ -55,14 +55,18 @@ def _forward_and_views(moe, w, logits, x, wgu, wd):
 # GEMM path variants: the default policy (small experts swapped on the 1-SM kernel, SM pairs when
 # the average expert has >= 128 rows, few-token down GEMM split over K), the 1-SM kernel with every
 # expert in the normal orientation, the SM-pair kernel for every shape in its normal-only form and
-# in its swapping form (thresholds 128 and 64 rows), a forced 3-way K split, and routing and the
-# permutation as two launches where the default fuses them (E <= 32).
+# in its swapping form (thresholds 128 and 64 rows; and with its CTA pairs split between normal
+# tiles and swapped chunks), a forced 3-way K split, and routing and the permutation as two
+# launches where the default fuses them (E <= 32).
 MODES = {"default": {}, "noswap": {"MOE_GEMM_SWAP_MAX": "0", "MOE_GEMM_2SM": "0"},
-         "pair": {"MOE_GEMM_2SM": "1"}, "pairswap": {"MOE_GEMM_2SM": "2"},
+         "pair": {"MOE_GEMM_2SM": "1"}, "pairswap": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_SPLIT": "0"},
          "pairswap64": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_SWAP_MAX": "64"},
+         "pairsplit": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_SPLIT": "30"},
+         "pairmix": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_SPLIT": "mix"},
+         "pairauto": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_SPLIT": "auto"},
          "ksplit3": {"MOE_DOWN_KSPLIT": "3"}, "nofuse": {"MOE_FUSE_ROUTE_PERMUTE": "0"}}
 ENV_KNOBS = ("MOE_GEMM_SWAP_MAX", "MOE_DOWN_KSPLIT", "MOE_GEMM_2SM", "MOE_GEMM_PAIR_SWAP_MAX", "MOE_GEMM_2SM_DOWN",
-             "MOE_FUSE_ROUTE_PERMUTE", "MOE_GEMM_PAIR_LAYOUT")
+             "MOE_FUSE_ROUTE_PERMUTE", "MOE_GEMM_PAIR_LAYOUT", "MOE_GEMM_PAIR_SPLIT")
 
 
 @pytest.fixture(params=sorted(MODES))
@@ -156,19 +160,24 @@ GEMM_CASES = [  # (T, d, f, E, k, bias); row counts per expert at the seeds used
 
 
 def _set_gemm_env(monkeypatch, swap_max, pair):
-    """pair "2:<n>" selects the swapping SM-pair kernel with threshold n."""
+    """pair "2:<n>" selects the swapping SM-pair kernel with threshold n (and its default,
+    device-chosen schedule), "2:<n>:<p>" fixes the schedule (0 round-robin, p pairs on normal
+    tiles, "mix", "auto")."""
     monkeypatch.setenv("MOE_GEMM_SWAP_MAX", swap_max)
-    mode, _, psm = pair.partition(":")
-    monkeypatch.setenv("MOE_GEMM_2SM", mode)
+    parts = pair.split(":")
+    monkeypatch.setenv("MOE_GEMM_2SM", parts[0])
     monkeypatch.delenv("MOE_GEMM_2SM_DOWN", raising=False)
-    if psm:
-        monkeypatch.setenv("MOE_GEMM_PAIR_SWAP_MAX", psm)
-    else:
-        monkeypatch.delenv("MOE_GEMM_PAIR_SWAP_MAX", raising=False)
+    for name, i in (("MOE_GEMM_PAIR_SWAP_MAX", 1), ("MOE_GEMM_PAIR_SPLIT", 2)):
+        if len(parts) > i:
+            monkeypatch.setenv(name, parts[i])
+        else:
+            monkeypatch.delenv(name, raising=False)
 
 
 @pytest.mark.parametrize("swap_max,pair", [("128", "0"), ("0", "0"), ("64", "1"), ("64", "2:128"),
-                                           ("64", "2:64"), ("64", "2:0")])
+                                           ("64", "2:64"), ("64", "2:0"), ("64", "2:128:40"), ("64", "2:64:1"),
+                                           ("64", "2:128:mix"), ("64", "2:128:auto"),
+                                           ("64", "2:128:0")])
 @pytest.mark.parametrize("T,d,f,E,k,bias", GEMM_CASES)
 def test_gateup_swiglu_parity(moe, oracle, T, d, f, E, k, bias, swap_max, pair, monkeypatch):
     _set_gemm_env(monkeypatch, swap_max, pair)
@@ -193,7 +202,9 @@ def test_gateup_swiglu_parity(moe, oracle, T, d, f, E, k, bias, swap_max, pair, 
 
 @pytest.mark.parametrize("swap_max,ksplit,pair", [("128", 1, "0"), ("0", 1, "0"), ("128", 3, "0"), ("0", 5, "0"),
                                                   ("128", 8, "0"), ("64", 1, "1"), ("64", 3, "1"), ("64", 1, "2:128"),
-                                                  ("64", 3, "2:64"), ("64", 2, "2:0")])
+                                                  ("64", 3, "2:64"), ("64", 2, "2:0"), ("64", 1, "2:128:40"),
+                                                  ("64", 2, "2:64:75"), ("64", 1, "2:128:mix"),
+                                                  ("64", 1, "2:128:auto"), ("64", 1, "2:128:0")])
 @pytest.mark.parametrize("T,d,f,E,k,bias", GEMM_CASES)
 def test_down_parity(moe, oracle, T, d, f, E, k, bias, swap_max, ksplit, pair, monkeypatch):
     _set_gemm_env(monkeypatch, swap_max, pair)
