@@ -61,18 +61,20 @@ AUTO_TIMED_S = 0.5
 AUTO_STEPS_MIN, AUTO_STEPS_MAX = 50, 4000
 
 MEASURED_TRAFFIC = {
-    ("mixtral_t32", "gateup_swiglu"): (1884468992, "c849555c80d424e9"),
-    ("mixtral_t32", "down"): (944722688, "c849555c80d424e9"),
-    ("mixtral_t512", "gateup_swiglu"): (1917358080, "c849555c80d424e9"),
-    ("mixtral_t512", "down"): (982794496, "c849555c80d424e9"),
-    ("mixtral_t512_skew40", "gateup_swiglu"): (1918835456, "c849555c80d424e9"),
-    ("mixtral_t512_skew40", "down"): (983391232, "c849555c80d424e9"),
-    ("mixtral_t4096", "gateup_swiglu"): (2628528640, "c849555c80d424e9"),
-    ("mixtral_t4096", "down"): (1527778304, "c849555c80d424e9"),
-    ("deepseek_t2048", "gateup_swiglu"): (8076621056, "c849555c80d424e9"),
-    ("deepseek_t2048", "down"): (4063829248, "c849555c80d424e9"),
-    ("deepseek_e32_t256", "gateup_swiglu"): (1920173312, "c849555c80d424e9"),
-    ("deepseek_e32_t256", "down"): (1008944128, "c849555c80d424e9"),
+    ("mixtral_t32", "gateup_swiglu"): (1884901632, "6755e621afd0d8bc"),
+    ("mixtral_t32", "down"): (945057024, "6755e621afd0d8bc"),
+    ("mixtral_t512", "gateup_swiglu"): (1917181440, "6755e621afd0d8bc"),
+    ("mixtral_t512", "down"): (982833408, "6755e621afd0d8bc"),
+    ("mixtral_t512_skew40", "gateup_swiglu"): (1917549312, "6755e621afd0d8bc"),
+    ("mixtral_t512_skew40", "down"): (983505152, "6755e621afd0d8bc"),
+    ("mixtral_t4096", "gateup_swiglu"): (3706759424, "6755e621afd0d8bc"),
+    ("mixtral_t4096", "down"): (1843701248, "6755e621afd0d8bc"),
+    ("deepseek_t2048", "gateup_swiglu"): (8107921152, "6755e621afd0d8bc"),
+    ("deepseek_t2048", "down"): (4197169152, "6755e621afd0d8bc"),
+    ("deepseek_v3_t2048", "gateup_swiglu"): (4813871872, "6755e621afd0d8bc"),
+    ("deepseek_v3_t2048", "down"): (2482596608, "6755e621afd0d8bc"),
+    ("deepseek_e32_t256", "gateup_swiglu"): (1920039168, "6755e621afd0d8bc"),
+    ("deepseek_e32_t256", "down"): (1008817664, "6755e621afd0d8bc"),
 }
 GEMM_SOURCES = ("mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm.cu",
                 "mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm_2sm.cu",

@@ -153,9 +153,9 @@ MOE_API int moe_grouped_gemm_down(const void* h, const void* w_down, const int32
  *      (M = 256 weight columns x N = rows; up to 64 or 128 rows, by the shared-memory layout the
  *      kernel picks on the device from the row counts);
  *  -1  invalid shape or kind.
- * Policy: with T*top_k >= 128*E (the average expert holds >= 128 rows) SM pairs, mode 1 for the
- * down GEMM below 512 rows per expert and mode 2 otherwise; gate+up also runs in mode 2 from 32
- * rows per expert when E * ceil(f/256) >= 608 (many-expert layers); else mode 0.
+ * Policy: with T*top_k >= 128*E (the average expert holds >= 128 rows) SM pairs, mode 2 for
+ * gate+up and mode 1 for the down GEMM; from 32 rows per expert, mode 2 for a many-expert layer
+ * (E * ceil(f/256) >= 608 for gate+up, E * ceil(d/512) >= 608 for down); else mode 0.
  * The environment variable MOE_GEMM_2SM=0/1/2 overrides both GEMMs, MOE_GEMM_2SM_DOWN the down
  * GEMM alone, MOE_GEMM_PAIR_SWAP_MAX the swap threshold of mode 2 (0..128).  Results agree with
  * the oracle in every mode. */

@@ -13,11 +13,13 @@
 //   swap    a chunk of at most C rows of one expert with the operands swapped (DeepGEMM write-up,
 //           section 3.2, "dynamic swap A/B"): the weights are the UMMA A operand, M = 256 weight
 //           columns (CTA r loads columns n0 + 128 r .. +127), and the tokens are B, N = rows
-//           rounded up to 16 (CTA r loads its N/2 rows).  Kind 0 issues two such UMMAs per K step,
-//           gate into accumulator columns [0, N) and up into [128, 128 + N), so an item covers 256
-//           h columns and one tensor-memory lane holds the gate and up value of one column; kind 1
-//           issues one, covering 256 y columns.  The MMA work is the chunk's rows, not a 256-row
-//           tile, so a small expert streams its weights with the tensor pipe mostly idle.
+//           rounded up to 16 (CTA r loads its N/2 rows).  Two such UMMAs per K step, into
+//           accumulator columns [0, N) and [128, 128 + N): for kind 0 gate and up, so an item
+//           covers 256 h columns and one tensor-memory lane holds the gate and up value of one
+//           column; for kind 1 output columns n0 + 128 r.. and n0 + 256 + 128 r.., so an item
+//           covers 512 y columns.  Either way a pair streams 2 x 32 KB of weights per 64-deep K
+//           block, and the MMA work is the chunk's rows, not a 256-row tile, so a small expert
+//           streams its weights with the tensor pipe mostly idle.
 //
 // The normal-only form (SWAPCAP false) runs six 32 KB pipeline stages.  The swapping form picks
 // one of two shared-memory layouts on the device, from the expert row counts, identically in
@@ -35,15 +37,16 @@
 //                                full tile becomes one swapped chunk, a larger one one more (partly
 //                                empty) normal tile.
 //
-// Schedule.  Items are numbered expert-major; inside an expert by 256-column super tile s (kind 0:
-// the normal N-tiles 2s and 2s+1, kind 1: N-tile s), then normal items (N-tile, pair, K-slice), then
-// the swapped chunk (K-slice) — items that read the same weight columns run at about the same time
-// and share them through L2.  A static round-robin over the persistent grid of CTA pairs balances
+// Schedule.  Items are numbered expert-major; inside an expert by super tile s (the columns of a
+// swapped item: normal N-tiles 2s and 2s+1), then normal items (N-tile, pair, K-slice), then the
+// swapped chunk (K-slice) — items that read the same weight columns run at about the same time and
+// share them through L2.  A static round-robin over the persistent grid of CTA pairs balances
 // skewed loads ("Triton MoE 核心擊敗 Megablocks", setupai.cc, section 關鍵要點, block-scheduled
-// grouped GEMM).  In the swapping form of kind 0 a swapped item reads 512 weight columns and a
-// normal one 256, so there one schedule slot is either a swapped item or the two normal items of
-// N-tiles 2s and 2s+1 for one M-tile pair, run back to back: every slot streams the same weight
-// bytes and the round-robin stays balanced.
+// grouped GEMM).  In the swapping form a swapped item reads twice the weight columns of a normal
+// one, so there one schedule slot is either a swapped item or the two normal items of N-tiles 2s
+// and 2s+1 for one M-tile pair, run back to back: every slot streams the same weight bytes and
+// the round-robin stays balanced.  The swapping form can also split its CTA pairs between the two
+// kinds of slot (see the split schedule below).
 //
 // Shared-memory stage (1024-byte aligned regions, 128-byte swizzle as written by TMA):
 //   X (16 KB)  normal: the CTA's 128 activation rows x 64 K (K-major);
@@ -88,7 +91,10 @@ constexpr int TMEM_COLS = NUM_ACC * ACC_COLS;
 constexpr int NUM_THREADS = 192;
 constexpr int MAX_E = 256;
 constexpr int SMEM_BYTES = 232448;
-constexpr int SUPER_N = 256;                     // output columns of a swapped item
+// Output columns of a swapped item = of a super tile: kind 0 256 h columns (512 gate+up weight
+// columns), kind 1 512 y columns; either way 2 x 32 KB of weights per pair per 64-deep K block.
+template <int KIND>
+constexpr int super_n() { return KIND == 0 ? 256 : 512; }
 constexpr int PAIR_SWAP_MAX_ROWS = 128;
 constexpr uint16_t BOTH_CTAS = 0x3;
 constexpr int kMixedSplit = 1 << 20;  // split_req value selecting the proportional merge
@@ -163,13 +169,13 @@ __device__ __forceinline__ RowSplit split_rows(int cnt, int swap_max, int chunk)
 }
 
 // Column tiling of one launch.  Normal N-tiles are BN_OUT output columns (kind 0: 128 h columns,
-// kind 1: 256 y columns); R of them make one 256-column super tile; the last super tile may hold
-// fewer (r_last).
+// kind 1: 256 y columns); R = 2 of them make one super tile (the columns of a swapped item); the
+// last super tile may hold fewer (r_last).
 template <int KIND>
 struct Tiling {
     int n_super, r_last;
     static constexpr int BN_OUT = KIND == 0 ? 128 : 256;
-    static constexpr int R = SUPER_N / BN_OUT;
+    static constexpr int R = super_n<KIND>() / BN_OUT;
     __device__ __forceinline__ explicit Tiling(int N) {
         const int n_tiles = (N + BN_OUT - 1) / BN_OUT;
         n_super = (n_tiles + R - 1) / R;
@@ -180,7 +186,7 @@ struct Tiling {
 // Whether one schedule slot holds the normal items of a whole super tile (see the header).
 template <int KIND, bool SWAPCAP>
 struct Sched {
-    static constexpr bool GROUP = SWAPCAP && KIND == 0;
+    static constexpr bool GROUP = SWAPCAP;
 };
 
 template <int KIND, bool SWAPCAP>
@@ -241,15 +247,20 @@ __device__ __forceinline__ PairItem decode_pair_item(const Ctl& c, const Tiling<
     return it;
 }
 
-// Split schedule (swapping form only): the normal slots and the swapped slots are numbered
-// separately, each expert-major.  Normal slot numbering inside an expert: super tile, M-tile pair,
+// Split schedule (swapping form only).  In a many-expert layer the large experts' normal tiles are
+// bound by the tensor pipe (2+ tile pairs reuse their weights from L2) and the small experts'
+// swapped chunks by the weight bytes a pair keeps in flight; one round-robin in expert order runs
+// the two kinds one after the other.  Instead, P CTA pairs run the normal slots and the others the
+// swapped slots, at the same time; P comes from a cost model of both kinds' work, evaluated on the
+// device from the row counts (kernel argument split_req: 0 off, P, kMixedSplit, kAutoSplit).  For
+// this the normal slots and the swapped slots are numbered separately, each expert-major.  Normal slot numbering inside an expert: super tile, M-tile pair,
 // K-slice (kind 0: one slot = N-tiles 2s and 2s+1, as in the round-robin order); swapped: super
 // tile, K-slice.
 template <int KIND>
 __device__ __forceinline__ int expert_normal_slots(int cnt, const Tiling<KIND>& t, int ksplit, int swap_max,
                                                    int chunk) {
     const RowSplit s = split_rows<true>(cnt, swap_max, chunk);
-    return (KIND == 0 ? t.n_super : (t.n_super - 1) * Tiling<KIND>::R + t.r_last) * s.np * ksplit;
+    return t.n_super * s.np * ksplit;
 }
 template <int KIND>
 __device__ __forceinline__ int expert_swap_slots(int cnt, const Tiling<KIND>& t, int ksplit, int swap_max,
@@ -278,12 +289,8 @@ __device__ __forceinline__ PairItem decode_split_item(const Ctl& c, const Tiling
         const int r = j - st * per_st;
         const int mpair = r / ksplit;
         it.kslice = r - mpair * ksplit;
-        if (KIND == 0) {
-            it.n_tile = 2 * st;
-            it.nsub = st == t.n_super - 1 ? t.r_last : 2;
-        } else {
-            it.n_tile = st;
-        }
+        it.n_tile = Tiling<KIND>::R * st;
+        it.nsub = st == t.n_super - 1 ? t.r_last : Tiling<KIND>::R;
         const int mtile = 2 * mpair + rank;
         it.row0 = c.seg[lo] + mtile * BM;
         it.rows = min(BM, cnt - mtile * BM);
@@ -339,7 +346,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                         int K, int N, int E, int ksplit, int swap_max, int layout_mode, int split_req,
                         void* __restrict__ out, int32_t* __restrict__ status) {
     constexpr int BN_OUT = Tiling<KIND>::BN_OUT;
-    constexpr int SW_BOXES = KIND == 0 ? 4 : 2;  // weight boxes per CTA in a swapped item
+    constexpr int SW_BOXES = 4;  // weight boxes per CTA in a swapped item (two MMAs)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     uint8_t* tiles = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -545,15 +552,15 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 const uint32_t full_leader = ptx::map_to_cta(ptx::smem_u32(&c.full[stage]), 0);
                 if (leader) ptx::mbar_arrive_expect_tx(&c.full[stage], pair_tx);
                 if (SWAPCAP && it.swap) {
-                    const int n0 = it.n_tile * SUPER_N + 128 * rank;
+                    const int n0 = it.n_tile * super_n<KIND>() + 128 * rank;
                     uint8_t* st = tiles + ring.tok_off(stage);
                     for (int q = 0; q < ntb; ++q)
                         ptx::tma_load_2d_pair(st + q * TOK_BOX_BYTES, &tmA32, full_leader, kb * BK,
                                               it.row0 + rank * half + q * TOK_BOX_ROWS, pol_act);
 #pragma unroll
                     for (int q = 0; q < SW_BOXES; ++q) {
-                        // kind 0: gate n0, n0+64, up f+n0, f+n0+64; kind 1: n0, n0+64.
-                        const int col = (KIND == 0 && q >= 2) ? N + n0 + 64 * (q - 2) : n0 + 64 * (q & 1);
+                        // kind 0: gate n0, n0+64, up f+n0, f+n0+64; kind 1: n0, n0+64, n0+256, n0+320.
+                        const int col = q < 2 ? n0 + 64 * q : (KIND == 0 ? N : 256) + n0 + 64 * (q - 2);
                         ptx::tma_load_2d_pair(sa + q * B_BOX_BYTES, &tmB, full_leader, col, brow + kb * BK,
                                               pol_wgt);
                     }
@@ -617,9 +624,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                         const uint64_t w_off = static_cast<uint64_t>((kk * 2048) >> 4);
                         const uint64_t t_off = static_cast<uint64_t>((kk * 32) >> 4);
                         ptx::mma_bf16_ss_pair(d_tmem, wx_desc + w_off, tok_desc + t_off, idesc_swap, accum);
-                        if (KIND == 0)
-                            ptx::mma_bf16_ss_pair(d_tmem + 128, wy_desc + w_off, tok_desc + t_off, idesc_swap,
-                                                  accum);
+                        ptx::mma_bf16_ss_pair(d_tmem + 128, wy_desc + w_off, tok_desc + t_off, idesc_swap, accum);
                     }
                 } else {
                     const uint64_t a_desc = ptx::smem_desc_sw128(sa, 16, 1024);
@@ -664,30 +669,36 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * ACC_COLS;
             const bool kfull = it.kslice * kb_per < num_kb;  // an empty K slice contributes zeros
             if (SWAPCAP && it.swap) {
-                // Accumulator lane = weight column col0 of this CTA's half, accumulator column = row.
-                const int col0 = it.n_tile * SUPER_N + 128 * rank + r_local;
+                // Accumulator lane = weight column col0 of this CTA's half, accumulator column = row;
+                // the second MMA's accumulator (at +128) holds kind 0's up column / kind 1's column
+                // col0 + 256.
+                const int col0 = it.n_tile * super_n<KIND>() + 128 * rank + r_local;
                 const int nchunk = (it.rows + 31) / 32;
 #pragma unroll 1
                 for (int cc = 0; cc < nchunk; ++cc) {
                     uint32_t a0[32], a1[32];
                     ptx::tmem_ld_32x32b_x32(taddr + cc * 32, a0);
-                    if (KIND == 0) ptx::tmem_ld_32x32b_x32(taddr + 128 + cc * 32, a1);
+                    ptx::tmem_ld_32x32b_x32(taddr + 128 + cc * 32, a1);
                     ptx::tmem_ld_wait();
                     const int nrow = min(32, it.rows - cc * 32);
                     const size_t row_base = static_cast<size_t>(it.row0 + cc * 32);
-                    if (col0 < N) {
-                        if (KIND == 0) {
+                    if (KIND == 1) {
+                        float* y = reinterpret_cast<float*>(out) + static_cast<size_t>(it.kslice) * M * N;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nrow) {
+                                if (col0 < N) y[(row_base + j) * N + col0] = kfull ? __uint_as_float(a0[j]) : 0.0f;
+                                if (col0 + 256 < N)
+                                    y[(row_base + j) * N + col0 + 256] = kfull ? __uint_as_float(a1[j]) : 0.0f;
+                            }
+                    } else if (col0 < N) {
+                        {
                             uint16_t* h = reinterpret_cast<uint16_t*>(out);
 #pragma unroll
                             for (int j = 0; j < 32; ++j)
                                 if (j < nrow)
                                     h[(row_base + j) * N + col0] =
                                         bf16_bits(silu_mul(__uint_as_float(a0[j]), __uint_as_float(a1[j])));
-                        } else {
-                            float* y = reinterpret_cast<float*>(out) + static_cast<size_t>(it.kslice) * M * N;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (j < nrow) y[(row_base + j) * N + col0] = kfull ? __uint_as_float(a0[j]) : 0.0f;
                         }
                     }
                 }

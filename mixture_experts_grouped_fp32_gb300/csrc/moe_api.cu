@@ -106,14 +106,17 @@ int swap_max_rows() {
 // Which grouped-GEMM kernel a layer shape runs on, per GEMM (kind 0 gate+up with N = f output
 // columns, 1 down with N = d): 0 the 1-SM kernel (128-row tiles, experts with <= swap_max_rows()
 // rows swapped), 1 the SM-pair kernel with 256-row tiles only, 2 the SM-pair kernel that also
-// swaps small experts and the short remainders of large ones.
+// swaps small experts and the short remainders of large ones (and splits its CTA pairs between
+// the two kinds of work where that pays).
 //   * average expert >= 128 rows (M >= 128 E): SM pairs, so sibling M-tiles share one weight load;
-//     mode 2, except the down GEMM below 512 rows per expert, measured faster in mode 1;
-//   * gate+up, 32..127 rows per expert on average, and at least 608 schedule slots (E x N/256:
-//     eight rounds over GB300's 76 SM pairs): mode 2 — many-expert layers mix a few large experts,
-//     which pair tiles run faster, with many small ones, which stream swapped (DeepSeek-V3 shape:
-//     gate+up 1.458 -> 1.415 ms); with fewer slots the round-robin's last round runs mostly empty
-//     (a 32-expert layer of the same shape: 0.289 -> 0.340 ms);
+//     gate+up in mode 2, the down GEMM in mode 1 (measured faster: Mixtral T=512 0.174 vs 0.185 ms,
+//     T=4096 0.650 vs 0.665 — its 512-column swapped slots are coarser than its 256-column tiles);
+//   * 32..127 rows per expert on average and at least 608 schedule slots (E x N/256 for gate+up,
+//     E x N/512 for down: eight rounds over GB300's 76 SM pairs): mode 2 — many-expert layers mix
+//     a few large experts, which pair tiles run faster, with many small ones, which stream swapped
+//     (DeepSeek-V3 shape: gate+up 1.458 -> 1.197 ms, down 0.835 -> 0.764 ms); with fewer slots the
+//     round-robin's last round runs mostly empty (a 32-expert layer of the same shape: gate+up
+//     0.289 -> 0.340 ms);
 //   * otherwise the 1-SM kernel.
 // MOE_GEMM_2SM=0/1/2 overrides both GEMMs, MOE_GEMM_2SM_DOWN the down GEMM alone.
 int use_pair(long long M, int E, int N, int kind) {
@@ -121,8 +124,9 @@ int use_pair(long long M, int E, int N, int kind) {
     if (kind == 1)
         if (const char* v = std::getenv("MOE_GEMM_2SM_DOWN")) return parse(v);
     if (const char* v = std::getenv("MOE_GEMM_2SM")) return parse(v);
-    if (M >= 128ll * E) return (kind == 1 && M < 512ll * E) ? 1 : 2;
-    if (kind == 0 && M >= 32ll * E && static_cast<long long>(E) * ((N + 255) / 256) >= 608) return 2;
+    if (M >= 128ll * E) return kind == 1 ? 1 : 2;
+    const int super_cols = kind == 0 ? 256 : 512;
+    if (M >= 32ll * E && static_cast<long long>(E) * ((N + super_cols - 1) / super_cols) >= 608) return 2;
     return 0;
 }
 

@@ -194,19 +194,15 @@ def test_down_ksplit_policy(lib):
 def test_gemm_pair_mode_policy(lib):
     from mixture_experts_grouped_fp32_gb300 import moe
     mx = (4096, 14336)  # Mixtral-8x7B-shaped d, f
-    for kind in (0, 1):
-        assert moe.gemm_pair_mode(4096, *mx, 8, 2, kind) == 2    # 1024 rows per expert on average
-        assert moe.gemm_pair_mode(2048, *mx, 8, 2, kind) == 2    # 512
-        assert moe.gemm_pair_mode(32, *mx, 8, 2, kind) == 0      # 8
+    for kind, big in ((0, 2), (1, 1)):
+        assert moe.gemm_pair_mode(4096, *mx, 8, 2, kind) == big   # 1024 rows per expert on average
+        assert moe.gemm_pair_mode(512, *mx, 8, 2, kind) == big    # 128
+        assert moe.gemm_pair_mode(32, *mx, 8, 2, kind) == 0       # 8
         assert moe.gemm_pair_mode(4, *mx, 8, 9, kind) == -1
-        assert moe.gemm_pair_mode(256, 7168, 2048, 32, 8, kind) == 0  # 64 rows, 256 slots
-    assert moe.gemm_pair_mode(512, *mx, 8, 2, 0) == 2     # 128: pairs, small experts swapped
-    assert moe.gemm_pair_mode(512, *mx, 8, 2, 1) == 1     # down GEMM: 256-row tiles
-    assert moe.gemm_pair_mode(2047, *mx, 8, 2, 1) == 1    # 511.75
+        assert moe.gemm_pair_mode(256, 7168, 2048, 32, 8, kind) == 0   # 64 rows, few slots
+        assert moe.gemm_pair_mode(2048, 7168, 2048, 256, 8, kind) == 2  # 64 rows, many slots
+        assert moe.gemm_pair_mode(1000, 7168, 2048, 256, 8, kind) == 0  # 31.25 rows
     assert moe.gemm_pair_mode(512, *mx, 8, 2, 2) == -1
-    assert moe.gemm_pair_mode(2048, 7168, 2048, 256, 8, 0) == 2  # 64 rows, 2048 slots
-    assert moe.gemm_pair_mode(2048, 7168, 2048, 256, 8, 1) == 0
-    assert moe.gemm_pair_mode(1000, 7168, 2048, 256, 8, 0) == 0  # 31.25 rows
     os.environ["MOE_GEMM_2SM_DOWN"] = "0"
     try:
         assert moe.gemm_pair_mode(4096, *mx, 8, 2, 1) == 0 and moe.gemm_pair_mode(4096, *mx, 8, 2, 0) == 2
