@@ -58,6 +58,7 @@ extern "C" {
 #define MOE_STATUS_BAD_OFFSETS 0x2   /* grouped GEMM: offsets not 0 <= ... nondecreasing <= M */
 #define MOE_STATUS_BAD_DEST 0x4      /* combine: a dest row outside [0, T*top_k) */
 #define MOE_STATUS_WAIT_TIMEOUT 0x8  /* grouped GEMM: a pipeline wait gave up after ~1 s */
+#define MOE_STATUS_BAD_SRC 0x10      /* gathering gate+up GEMM: a src index outside [0, T) (row zeroed) */
 
 typedef void* moe_stream_t; /* a cudaStream_t */
 
@@ -133,6 +134,22 @@ MOE_API int moe_permute(const int32_t* idx, const void* x, int T, int d, int E, 
 MOE_API int moe_grouped_gemm_gateup_swiglu(const void* x_perm, const void* w_gate_up,
                                    const int32_t* offsets, int M, int d, int f, int E, void* h,
                                    int32_t* status, moe_stream_t stream);
+
+/* Step 3 with the gather fused in: the same operation as moe_grouped_gemm_gateup_swiglu, but row r
+ * of the grouped operand is x[src[r]] — the kernel gathers the rows of x itself (16-byte cp.async
+ * copies into the tensor-core operand layout), so x_perm never exists in global memory.  moe_forward
+ * runs it when the environment sets MOE_GATHER=1 (the permute then only computes the indices); by
+ * default it writes x_perm and reads it with TMA, which measured faster.
+ *   x [T,d] bf16 in;  src [M] int32 in (row -> token, from moe_permute; an index outside [0, T) is
+ *   read as a zero row and sets MOE_STATUS_BAD_SRC);
+ *   other arguments as for moe_grouped_gemm_gateup_swiglu.
+ * The pages fuse the dispatch steps to cut kernel launches and passes over the activations
+ * ("Triton-MoE-Dispatch-Kernel erreicht 131 % von Megablocks", lumeric.app, its bullet list: 24+
+ * launches down to 5); folding the row gather into the GEMM removes one more write and read of
+ * the T*top_k x d activations. */
+MOE_API int moe_grouped_gemm_gateup_swiglu_gather(const void* x, const int32_t* src, int T, const void* w_gate_up,
+                                          const int32_t* offsets, int M, int d, int f, int E, void* h,
+                                          int32_t* status, moe_stream_t stream);
 
 /* Step 4 — grouped down-projection GEMM: y_perm[r] = h[r] . W_down[e] (fp32 accumulation) for
  * r in expert e's segment.  With ksplit > 1 the reduction over f is split into ksplit contiguous

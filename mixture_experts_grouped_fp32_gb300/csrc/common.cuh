@@ -89,6 +89,10 @@ struct GemmArgs {
     int pair_split = 0;    // SM-pair kernel (pair == 2): CTA pairs given to normal tiles when the
                            // kinds are split between pairs; 0 = one round-robin over all slots
     int inject_stall = 0;  // test hook (1-SM kernel): make one pipeline wait run out, see moe_api.cu
+    // Gate+up only: when set, A is x [gather_T, K] and row r of the grouped operand is
+    // x[gather_src[r]] (gathered by the kernel); x_perm is never materialised.
+    const int32_t* gather_src = nullptr;
+    int gather_T = 0;
 };
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                 const char** why);

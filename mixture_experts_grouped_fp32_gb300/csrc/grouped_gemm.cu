@@ -68,6 +68,12 @@ constexpr int ACC_COLS = UMMA_N;                // fp32 columns per accumulator
 constexpr int NUM_ACC = 2;
 constexpr int TMEM_COLS = NUM_ACC * ACC_COLS;   // 512
 constexpr int NUM_THREADS = 192;
+// GATHER launches add kGatherWarps warps (6..9) that gather the activation rows, one per ring
+// slot: a warp then never waits on a slot's `empty` barrier more than one phase ahead (which its
+// parity wait requires).
+constexpr int kGatherWarps = STAGES;
+constexpr int kGatherWarp0 = NUM_THREADS / 32;
+constexpr int GATHER_THREADS = NUM_THREADS + 32 * kGatherWarps;
 constexpr int MAX_E = 256;
 constexpr int SWAP_MAX_ROWS = 128;              // swap mode needs N = rows16 <= 128
 // The whole opt-in shared memory of an SM: one CTA per SM, and any descriptor mistake would
@@ -132,11 +138,17 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
 
 // KIND 0: gate+up+SwiGLU (output tile = 128 h columns; weight boxes gate n0, n0+64, up f+n0, f+n0+64)
 // KIND 1: down             (output tile = 256 y columns; weight boxes n0 + 64 q)
-template <int KIND>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// GATHER (kind 0 only): the activation rows are not read from x_perm with TMA but gathered from x
+// by the permutation's src[] with 16-byte cp.async copies, issued by four extra warps into the
+// 128-byte-swizzled positions TMA would have written; rows past the expert's end are zero-filled.
+// Each stage's `full` barrier then expects two arrivals: the TMA weight bytes' and its gather
+// warp's.  x_perm then never exists in global memory.
+template <int KIND, bool GATHER>
+__global__ void __launch_bounds__(GATHER ? GATHER_THREADS : NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
                     const __grid_constant__ CUtensorMap tmB, const int32_t* __restrict__ offsets, int M,
-                    int K, int N, int E, int ksplit, int swap_max, int inject_stall, void* __restrict__ out,
+                    int K, int N, int E, int ksplit, int swap_max, int inject_stall,
+                    const int4* __restrict__ xg, const int32_t* __restrict__ gsrc, int gT, void* __restrict__ out,
                     int32_t* __restrict__ status) {
     constexpr int BN_OUT = KIND == 0 ? 128 : 256;
     extern __shared__ uint8_t smem_raw[];
@@ -152,7 +164,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(&c.full[s], 1);
+            ptx::mbar_init(&c.full[s], GATHER ? 2 : 1);
             ptx::mbar_init(&c.empty[s], 1);
         }
         for (int a = 0; a < NUM_ACC; ++a) {
@@ -165,7 +177,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         ptx::fence_proxy_async_smem();
     }
     if (warp == 0 && lane == 0) {
-        ptx::prefetch_tensormap(&tmA);
+        if (!GATHER) ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmA32);
         ptx::prefetch_tensormap(&tmB);
     }
@@ -228,7 +240,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int n0 = it.n_tile * BN_OUT;
             const int brow = it.e * K;
             const int nbox32 = (it.rows + A_BOX32_ROWS - 1) / A_BOX32_ROWS;
-            const uint32_t tx = it.swap ? B_BYTES + nbox32 * A_BOX32_BYTES : STAGE_BYTES;
+            // With GATHER the activation rows come from the gather warps; TMA brings the weights.
+            const uint32_t tx = GATHER ? B_BYTES : (it.swap ? B_BYTES + nbox32 * A_BOX32_BYTES : STAGE_BYTES);
             const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (!ptx::mbar_wait(&c.empty[stage], phase ^ 1u, abort_flag)) {
@@ -243,12 +256,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 // must expire (status MOE_STATUS_WAIT_TIMEOUT).
                 const uint32_t extra = (inject_stall && blockIdx.x == 0 && filled_mask == 0) ? 16u : 0u;
                 ptx::mbar_arrive_expect_tx(&c.full[stage], tx + extra);
-                if (it.swap) {
-                    for (int q = 0; q < nbox32; ++q)
-                        ptx::tma_load_2d(sa + q * A_BOX32_BYTES, &tmA32, &c.full[stage], kb * BK,
-                                         it.row0 + q * A_BOX32_ROWS, pol_act);
-                } else {
-                    ptx::tma_load_2d(sa, &tmA, &c.full[stage], kb * BK, it.row0, pol_act);
+                if (!GATHER) {
+                    if (it.swap) {
+                        for (int q = 0; q < nbox32; ++q)
+                            ptx::tma_load_2d(sa + q * A_BOX32_BYTES, &tmA32, &c.full[stage], kb * BK,
+                                             it.row0 + q * A_BOX32_ROWS, pol_act);
+                    } else {
+                        ptx::tma_load_2d(sa, &tmA, &c.full[stage], kb * BK, it.row0, pol_act);
+                    }
                 }
 #pragma unroll
                 for (int q = 0; q < B_BOXES; ++q) {
@@ -265,6 +280,70 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     phase ^= 1u;
                 }
             }
+        }
+    } else if (GATHER && warp >= kGatherWarp0) {
+        // ------------------- gather warps (GATHER): activation rows by src[] -------------------
+        // Warp g fills ring slot g each time round (positions g, g + STAGES, ... of the sequence):
+        // it waits until the stage is free, issues its 128-byte rows as 16-byte cp.async copies into
+        // the swizzled positions (chunk ch of tile row r at r * 128 + ((ch ^ (r & 7)) * 16)), waits
+        // for its own copies, fences them for the tensor cores' (async-proxy) reads, and one lane
+        // arrives on the stage's `full` barrier.  kGatherWarps stages are gathered at once.
+        const int g = warp - kGatherWarp0;
+        const uint64_t pol_x = ptx::policy_evict_last();  // x rows are gathered by many tiles: keep them in L2
+        uint32_t stage = 0, phase = 0;
+        int m = 0;  // position in the ring sequence
+        bool aborted = false;
+        for (int i = blockIdx.x; i < total && !aborted; i += gridDim.x) {
+            const Item it = decode_item(c, E, ksplit, swap_max, i);
+            const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
+            const int nst = kb1 - kb0;
+            // Does this warp fill any stage of this item?
+            const int first = (g - m % kGatherWarps + kGatherWarps) % kGatherWarps;
+            if (first < nst) {
+                const int tile_rows = it.swap ? ((it.rows + 15) & ~15) : BM;  // rows the MMA reads
+                // Lane l copies 16-byte chunk (l & 7) of tile rows (l >> 3) + 4 t: eight adjacent
+                // lanes cover one 128-byte row, so each warp instruction moves four whole rows.
+                const int ch = lane & 7, rs = lane >> 3;
+                int tok[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const int r = rs + 4 * t;
+                    tok[t] = r < it.rows ? __ldg(gsrc + it.row0 + r) : -1;
+                    if (r < it.rows && (tok[t] < 0 || tok[t] >= gT)) {  // bad src: zero row, reported
+                        flag_status(status, MOE_STATUS_BAD_SRC);
+                        tok[t] = -1;
+                    }
+                }
+                for (int j = first; j < nst; j += kGatherWarps) {
+                    const int mm = m + j;
+                    const uint32_t st = static_cast<uint32_t>(mm % STAGES);
+                    const uint32_t ph = static_cast<uint32_t>((mm / STAGES) & 1);
+                    const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&c.empty[st], ph ^ 1u, abort_flag));
+                    if (!ok) {
+                        if (lane == 0) raise_abort(c, status);
+                        aborted = true;
+                        break;
+                    }
+                    const int kb = kb0 + j;
+                    const uint32_t sa_u = ptx::smem_u32(tiles + st * STAGE_BYTES);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const int r = rs + 4 * t;
+                        if (r < tile_rows)
+                            ptx::cp_async_16_hint(sa_u + r * 128 + ((ch ^ (r & 7)) << 4),
+                                             tok[t] >= 0 ? xg + static_cast<size_t>(tok[t]) * (K / 8) + kb * 8 + ch : xg,
+                                             tok[t] >= 0 ? 16u : 0u, pol_x);
+                    }
+                    ptx::cp_async_commit();
+                    ptx::cp_async_wait_all();
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&c.full[st]);
+                }
+            }
+            m += nst;
+            (void)stage;
+            (void)phase;
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------ MMA issuer ------------------------------
@@ -320,7 +399,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 acc_phase ^= 1u;
             }
         }
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < kGatherWarp0) {
         // ------------------------------ epilogue ------------------------------
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
         const int r_local = quarter * 32 + lane;
@@ -426,6 +505,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
 
     // ------------------------------ teardown ------------------------------
+    if (GATHER && warp >= kGatherWarp0) ptx::cp_async_wait_all();  // no gather copy outlives the CTA
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0 && lane == 0 && c.abort_flag) {
@@ -446,13 +526,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 // ---------------------------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // ---------------------------------------------------------------------------------------------
-template <int KIND>
+template <int KIND, bool GATHER>
 cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const char** why) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<KIND>,
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<KIND, GATHER>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) {
             *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
@@ -462,16 +542,18 @@ cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const ch
     }
     CUtensorMap mA, mA32, mB;
     const uint64_t bcols = KIND == 0 ? 2ull * a.N : static_cast<uint64_t>(a.N);
-    if (!make_tensor_map_bf16(&mA, a.A, a.K, a.M, BM) || !make_tensor_map_bf16(&mA32, a.A, a.K, a.M, A_BOX32_ROWS) ||
+    // With GATHER, A is x [gather_T, K] (the maps over it are then unused).
+    const uint64_t arows = GATHER ? static_cast<uint64_t>(a.gather_T) : static_cast<uint64_t>(a.M);
+    if (!make_tensor_map_bf16(&mA, a.A, a.K, arows, BM) || !make_tensor_map_bf16(&mA32, a.A, a.K, arows, A_BOX32_ROWS) ||
         !make_tensor_map_bf16(&mB, a.B, bcols, static_cast<uint64_t>(a.E) * a.K, BK)) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or bad operand)";
         return cudaErrorInvalidValue;
     }
     const int swap_max = a.swap_max < 0 ? 0 : (a.swap_max > SWAP_MAX_ROWS ? SWAP_MAX_ROWS : a.swap_max);
     const int ksplit = KIND == 0 ? 1 : a.ksplit;
-    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_kernel<KIND>, dim3(num_sms), dim3(NUM_THREADS),
-                    SMEM_BYTES, s, mA, mA32, mB, a.offsets, a.M, a.K, a.N, a.E, ksplit, swap_max, a.inject_stall,
-                    a.out, a.status);
+    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_kernel<KIND, GATHER>, dim3(num_sms),
+                    dim3(GATHER ? GATHER_THREADS : NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB, a.offsets, a.M, a.K, a.N, a.E, ksplit, swap_max,
+                    a.inject_stall, reinterpret_cast<const int4*>(a.A), a.gather_src, a.gather_T, a.out, a.status);
 }
 
 }  // namespace
@@ -511,7 +593,9 @@ cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaSt
         return cudaErrorInvalidValue;
     }
     if (a.pair && num_sms >= 2 && !a.inject_stall) return launch_grouped_gemm_pair(kind, a, num_sms, s, why);
-    return kind == 0 ? launch_kind<0>(a, num_sms, s, why) : launch_kind<1>(a, num_sms, s, why);
+    if (kind == 0)
+        return a.gather_src ? launch_kind<0, true>(a, num_sms, s, why) : launch_kind<0, false>(a, num_sms, s, why);
+    return launch_kind<1, false>(a, num_sms, s, why);
 }
 
 }  // namespace moe

@@ -89,6 +89,11 @@ constexpr int ACC_COLS = 256;
 constexpr int NUM_ACC = 2;
 constexpr int TMEM_COLS = NUM_ACC * ACC_COLS;
 constexpr int NUM_THREADS = 192;
+// GATHER launches add kGatherWarps warps (6..11) that gather the activation rows: one per
+// pipeline stage, so every free stage's rows are in flight at once.
+constexpr int kGatherWarps = STAGES_MAX;
+constexpr int kGatherWarp0 = NUM_THREADS / 32;
+constexpr int GATHER_THREADS = NUM_THREADS + 32 * kGatherWarps;
 constexpr int MAX_E = 256;
 constexpr int SMEM_BYTES = 232448;
 // Output columns of a swapped item = of a super tile: kind 0 256 h columns (512 gate+up weight
@@ -339,12 +344,16 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
     return *reinterpret_cast<uint16_t*>(&b);
 }
 
-template <int KIND, bool SWAPCAP>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+// GATHER (kind 0 only): each CTA's six extra warps gather its own activation rows from x by
+// src[] with cp.async, as in grouped_gemm.cu; CTA 0's `full` barrier then expects three arrivals:
+// the TMA weight bytes', and one per CTA when its gathered rows have landed (CTA 1's remotely).
+template <int KIND, bool SWAPCAP, bool GATHER>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? GATHER_THREADS : NUM_THREADS, 1)
 grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
                         const __grid_constant__ CUtensorMap tmB, const int32_t* __restrict__ offsets, int M,
                         int K, int N, int E, int ksplit, int swap_max, int layout_mode, int split_req,
-                        void* __restrict__ out, int32_t* __restrict__ status) {
+                        const int4* __restrict__ xg, const int32_t* __restrict__ gsrc, int gT, void* __restrict__ out,
+                        int32_t* __restrict__ status) {
     constexpr int BN_OUT = Tiling<KIND>::BN_OUT;
     constexpr int SW_BOXES = 4;  // weight boxes per CTA in a swapped item (two MMAs)
     extern __shared__ uint8_t smem_raw[];
@@ -363,7 +372,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
 
     if (tid == 0) {
         for (int s = 0; s < STAGES_MAX; ++s) {
-            ptx::mbar_init(&c.full[s], 1);
+            ptx::mbar_init(&c.full[s], GATHER ? 3 : 1);
             ptx::mbar_init(&c.empty[s], 1);
         }
         for (int a = 0; a < NUM_ACC; ++a) {
@@ -376,8 +385,8 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         ptx::fence_proxy_async_smem();
     }
     if (warp == 0 && lane == 0) {
-        ptx::prefetch_tensormap(&tmA);
-        if (SWAPCAP) ptx::prefetch_tensormap(&tmA32);
+        if (!GATHER) ptx::prefetch_tensormap(&tmA);
+        if (SWAPCAP && !GATHER) ptx::prefetch_tensormap(&tmA32);
         ptx::prefetch_tensormap(&tmB);
     }
     if (warp == 1) {
@@ -540,8 +549,10 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             // Swapped items: this CTA's token rows start N/2 into the chunk for CTA 1.
             const int half = it.ntok >> 1;
             const int ntb = (half + TOK_BOX_ROWS - 1) / TOK_BOX_ROWS;  // 1 (layout A) or up to 2 (B)
-            const uint32_t pair_tx = it.swap ? 2u * (SW_BOXES * B_BOX_BYTES + ntb * TOK_BOX_BYTES)
-                                             : 2u * NORMAL_CTA_BYTES;
+            // With GATHER the activation rows come from the gather warps; TMA brings the weights.
+            const uint32_t pair_tx = GATHER ? (it.swap ? 2u * SW_BOXES * B_BOX_BYTES : 2u * BH_BOXES * B_BOX_BYTES)
+                                            : (it.swap ? 2u * (SW_BOXES * B_BOX_BYTES + ntb * TOK_BOX_BYTES)
+                                                       : 2u * NORMAL_CTA_BYTES);
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (!ptx::mbar_wait(&c.empty[stage], phase ^ 1u, abort_flag)) {
                     raise_abort(c, status);
@@ -553,10 +564,12 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 if (leader) ptx::mbar_arrive_expect_tx(&c.full[stage], pair_tx);
                 if (SWAPCAP && it.swap) {
                     const int n0 = it.n_tile * super_n<KIND>() + 128 * rank;
-                    uint8_t* st = tiles + ring.tok_off(stage);
-                    for (int q = 0; q < ntb; ++q)
-                        ptx::tma_load_2d_pair(st + q * TOK_BOX_BYTES, &tmA32, full_leader, kb * BK,
-                                              it.row0 + rank * half + q * TOK_BOX_ROWS, pol_act);
+                    if (!GATHER) {
+                        uint8_t* st = tiles + ring.tok_off(stage);
+                        for (int q = 0; q < ntb; ++q)
+                            ptx::tma_load_2d_pair(st + q * TOK_BOX_BYTES, &tmA32, full_leader, kb * BK,
+                                                  it.row0 + rank * half + q * TOK_BOX_ROWS, pol_act);
+                    }
 #pragma unroll
                     for (int q = 0; q < SW_BOXES; ++q) {
                         // kind 0: gate n0, n0+64, up f+n0, f+n0+64; kind 1: n0, n0+64, n0+256, n0+320.
@@ -566,7 +579,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                     }
                 } else {
                     const int n0 = it.n_tile * BN_OUT;
-                    ptx::tma_load_2d_pair(sa, &tmA, full_leader, kb * BK, it.row0, pol_act);
+                    if (!GATHER) ptx::tma_load_2d_pair(sa, &tmA, full_leader, kb * BK, it.row0, pol_act);
 #pragma unroll
                     for (int q = 0; q < BH_BOXES; ++q) {
                         // kind 0: CTA r holds gate columns n0+64r.. and up columns f+n0+64r..;
@@ -584,6 +597,78 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                     phase ^= 1u;
                 }
             }
+          }
+        }
+    } else if (GATHER && warp >= kGatherWarp0) {
+        // ------------------- gather warps (GATHER, both CTAs): activation rows by src[] -------------------
+        // As in grouped_gemm.cu: warp g fills ring slot g each time round (positions g, g + stages,
+        // ... of the ring sequence) with this CTA's rows (normal: its 128-row M-tile; swapped: its
+        // N/2 token rows), waits for its own copies, fences them, and one lane arrives on CTA 0's
+        // `full` barrier of the stage (CTA 1 remotely).
+        const int g = warp - kGatherWarp0;
+        const uint64_t pol_x = ptx::policy_evict_last();  // x rows are gathered by many tiles: keep them in L2
+        int m = 0;  // position in the ring sequence
+        bool aborted = false;
+        for (int i = walk.first; i < walk.count && !aborted; i += walk.stride) {
+          const PairItem slot = slot_at(i);
+          for (int sub = 0; sub < slot.nsub && !aborted; ++sub) {
+            PairItem it = slot;
+            it.n_tile += sub;
+            const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
+            const int nst = kb1 - kb0;
+            // Warp g owns ring slot g: positions mm with mm % stages == g.  One warp per slot keeps
+            // every waiter on a slot's `empty` barrier at most one phase ahead, which its parity wait
+            // needs (warps g >= stages have nothing to do).
+            const int first = (g - m % ring.nst + ring.nst) % ring.nst;
+            if (g < ring.nst && first < nst) {
+                const int half = it.ntok >> 1;
+                const int tile_rows = it.swap ? half : BM;
+                // Lane l copies 16-byte chunk (l & 7) of tile rows (l >> 3) + 4 t: eight adjacent
+                // lanes cover one 128-byte row, so each warp instruction moves four whole rows.
+                const int ch = lane & 7, rs = lane >> 3;
+                int tok[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const int r = rs + 4 * t;
+                    const int rr = it.swap ? rank * half + r : r;  // row within the item's rows
+                    const bool valid = r < tile_rows && rr < it.rows;
+                    tok[t] = valid ? __ldg(gsrc + it.row0 + (it.swap ? rank * half : 0) + r) : -1;
+                    if (valid && (tok[t] < 0 || tok[t] >= gT)) {  // bad src: zero row, reported
+                        flag_status(status, MOE_STATUS_BAD_SRC);
+                        tok[t] = -1;
+                    }
+                }
+                for (int j = first; j < nst; j += ring.nst) {
+                    const int mm = m + j;
+                    const int st = mm % ring.nst;  // == g
+                    const uint32_t ph = static_cast<uint32_t>((mm / ring.nst) & 1);
+                    const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&c.empty[st], ph ^ 1u, abort_flag));
+                    if (!ok) {
+                        if (lane == 0) raise_abort(c, status);
+                        aborted = true;
+                        break;
+                    }
+                    const int kb = kb0 + j;
+                    const uint32_t dst = ptx::smem_u32(it.swap ? tiles + ring.tok_off(st) : tiles + st * ring.stride);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const int r = rs + 4 * t;
+                        if (r < tile_rows)
+                            ptx::cp_async_16_hint(dst + r * 128 + ((ch ^ (r & 7)) << 4),
+                                             tok[t] >= 0 ? xg + static_cast<size_t>(tok[t]) * (K / 8) + kb * 8 + ch : xg,
+                                             tok[t] >= 0 ? 16u : 0u, pol_x);
+                    }
+                    ptx::cp_async_commit();
+                    ptx::cp_async_wait_all();
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (leader) ptx::mbar_arrive(&c.full[st]);
+                        else ptx::mbar_arrive_cluster(ptx::map_to_cta(ptx::smem_u32(&c.full[st]), 0));
+                    }
+                }
+            }
+            m += nst;
           }
         }
     } else if (warp == 1 && lane == 0 && leader) {
@@ -649,7 +734,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             }
           }
         }
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < kGatherWarp0) {
         // ------------------------------ epilogue (both CTAs) ------------------------------
         const int quarter = warp & 3;
         const int r_local = quarter * 32 + lane;
@@ -764,6 +849,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
     }
 
     // ------------------------------ teardown ------------------------------
+    if (GATHER && warp >= kGatherWarp0) ptx::cp_async_wait_all();  // no gather copy outlives the CTA
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0 && lane == 0 && c.abort_flag) {
@@ -788,13 +874,13 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
     ptx::cluster_sync();
 }
 
-template <int KIND, bool SWAPCAP>
+template <int KIND, bool SWAPCAP, bool GATHER>
 cudaError_t launch_pair_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const char** why) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_2sm_kernel<KIND, SWAPCAP>,
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_2sm_kernel<KIND, SWAPCAP, GATHER>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) {
             *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
@@ -804,8 +890,10 @@ cudaError_t launch_pair_kind(const GemmArgs& a, int num_sms, cudaStream_t s, con
     }
     CUtensorMap mA, mA32, mB;
     const uint64_t bcols = KIND == 0 ? 2ull * a.N : static_cast<uint64_t>(a.N);
-    if (!make_tensor_map_bf16(&mA, a.A, a.K, a.M, BM) ||
-        !make_tensor_map_bf16(&mA32, a.A, a.K, a.M, TOK_BOX_ROWS) ||
+    // With GATHER, A is x [gather_T, K] (the maps over it are then unused).
+    const uint64_t arows = GATHER ? static_cast<uint64_t>(a.gather_T) : static_cast<uint64_t>(a.M);
+    if (!make_tensor_map_bf16(&mA, a.A, a.K, arows, BM) ||
+        !make_tensor_map_bf16(&mA32, a.A, a.K, arows, TOK_BOX_ROWS) ||
         !make_tensor_map_bf16(&mB, a.B, bcols, static_cast<uint64_t>(a.E) * a.K, BK)) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or bad operand)";
         return cudaErrorInvalidValue;
@@ -814,18 +902,24 @@ cudaError_t launch_pair_kind(const GemmArgs& a, int num_sms, cudaStream_t s, con
     const int ksplit = KIND == 0 ? 1 : a.ksplit;
     const int swap_max = a.pair_swap_max < 0 ? 0 : (a.pair_swap_max > PAIR_SWAP_MAX_ROWS ? PAIR_SWAP_MAX_ROWS
                                                                                       : a.pair_swap_max);
-    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_2sm_kernel<KIND, SWAPCAP>, dim3(grid),
-                    dim3(NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB, a.offsets, a.M, a.K, a.N, a.E, ksplit,
-                    swap_max, a.pair_layout, a.pair_split, a.out, a.status);
+    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_2sm_kernel<KIND, SWAPCAP, GATHER>, dim3(grid),
+                    dim3(GATHER ? GATHER_THREADS : NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB, a.offsets, a.M, a.K, a.N, a.E, ksplit,
+                    swap_max, a.pair_layout, a.pair_split, reinterpret_cast<const int4*>(a.A), a.gather_src,
+                    a.gather_T, a.out, a.status);
 }
 
 }  // namespace
 
 cudaError_t launch_grouped_gemm_pair(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                      const char** why) {
-    if (a.pair == 2)
-        return kind == 0 ? launch_pair_kind<0, true>(a, num_sms, s, why) : launch_pair_kind<1, true>(a, num_sms, s, why);
-    return kind == 0 ? launch_pair_kind<0, false>(a, num_sms, s, why) : launch_pair_kind<1, false>(a, num_sms, s, why);
+    if (kind == 1)
+        return a.pair == 2 ? launch_pair_kind<1, true, false>(a, num_sms, s, why)
+                           : launch_pair_kind<1, false, false>(a, num_sms, s, why);
+    if (a.gather_src)
+        return a.pair == 2 ? launch_pair_kind<0, true, true>(a, num_sms, s, why)
+                           : launch_pair_kind<0, false, true>(a, num_sms, s, why);
+    return a.pair == 2 ? launch_pair_kind<0, true, false>(a, num_sms, s, why)
+                       : launch_pair_kind<0, false, false>(a, num_sms, s, why);
 }
 
 }  // namespace moe

@@ -160,6 +160,14 @@ int pair_swap_max_rows() {
     return x < 0 ? 0 : (x > 128 ? 128 : x);
 }
 
+// Whether moe_forward's gate+up GEMM gathers its activation rows from x by src[] (the permute then
+// writes no x_perm).  Off by default: measured slower than writing x_perm and reading it with TMA
+// (Mixtral shape T=4096 2.81 vs 2.04 ms per layer, T=512 0.68 vs 0.53); MOE_GATHER=1 turns it on.
+bool gather_rows() {
+    const char* v = std::getenv("MOE_GATHER");
+    return v && v[0] == '1';
+}
+
 // Whether moe_forward runs routing and the permutation as one launch (softmax router, E <= 32,
 // T*E <= 8192: every block can afford to route all tokens itself).  MOE_FUSE_ROUTE_PERMUTE=0
 // turns it off.
@@ -276,9 +284,11 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
     float* y = at<float>(ws, L.y_perm);
     const int M = T * k;
     cudaError_t e;
+    const bool gather = gather_rows();
+    __nv_bfloat16* xp = gather ? nullptr : x_perm;  // no x_perm when the GEMM gathers
     if (!router.grouped && fuse_route_permute(T, E)) {
         if ((e = launch_route_permute(logits, static_cast<const __nv_bfloat16*>(x), T, d, E, k, idx, w, counts,
-                                      offsets, src, dest, x_perm, status, num_sms, s)) != cudaSuccess)
+                                      offsets, src, dest, xp, status, num_sms, s)) != cudaSuccess)
             return launched(e, "route+permute");
     } else {
         e = router.grouped ? launch_route_grouped(logits, router.bias, T, E, k, router.n_group, router.topk_group,
@@ -286,13 +296,17 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
                            : launch_route(logits, T, E, k, idx, w, status, s);
         if (e != cudaSuccess) return launched(e, "route");
         if ((e = launch_permute(idx, static_cast<const __nv_bfloat16*>(x), T, d, E, k, counts, offsets, src,
-                                dest, x_perm, status, num_sms, s)) != cudaSuccess)
+                                dest, xp, status, num_sms, s)) != cudaSuccess)
             return launched(e, "permute");
     }
     const char* why = "";
     const int swap_max = swap_max_rows(), ksplit = down_ksplit(T, d, f, E, k);
-    GemmArgs g1{x_perm, wgu, offsets, M, d, f, E, h, status, 1, swap_max, use_pair(M, E, f, 0), pair_swap_max_rows(),
-                pair_layout(), pair_split()};
+    GemmArgs g1{gather ? x : x_perm, wgu, offsets, M, d, f, E, h, status, 1, swap_max, use_pair(M, E, f, 0),
+                pair_swap_max_rows(), pair_layout(), pair_split()};
+    if (gather) {
+        g1.gather_src = src;
+        g1.gather_T = T;
+    }
     if ((e = launch_grouped_gemm(0, g1, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "gate+up GEMM: %s (%s)", why, cudaGetErrorString(e));
     GemmArgs g2{h, wd, offsets, M, f, d, E, y, status, ksplit, swap_max, use_pair(M, E, d, 1), pair_swap_max_rows(),
@@ -429,7 +443,8 @@ int moe_permute(const int32_t* idx, const void* x, int T, int d, int E, int top_
 }
 
 static int gemm_entry(int kind, const void* A, const void* B, const int32_t* offsets, int M, int d, int f,
-                      int E, int ksplit, void* out, int32_t* status, moe_stream_t stream, const char* name) {
+                      int E, int ksplit, void* out, int32_t* status, moe_stream_t stream, const char* name,
+                      const int32_t* gather_src = nullptr, int gather_T = 0) {
     int rc = check_shape(0, d, f, E, 1, true);
     if (rc) return rc;
     if (M < 0) return fail(MOE_ERR_INVALID_ARG, "%s: M = %d must be >= 0", name, M);
@@ -448,6 +463,8 @@ static int gemm_entry(int kind, const void* A, const void* B, const int32_t* off
     g.pair_layout = pair_layout();
     g.pair_split = pair_split();
     g.inject_stall = inject_stall();
+    g.gather_src = gather_src;
+    g.gather_T = gather_T;
     const char* why = "";
     cudaError_t e = launch_grouped_gemm(kind, g, sms, static_cast<cudaStream_t>(stream), &why);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s (%s)", name, why, cudaGetErrorString(e));
@@ -458,6 +475,16 @@ int moe_grouped_gemm_gateup_swiglu(const void* x_perm, const void* w_gate_up, co
                                    int d, int f, int E, void* h, int32_t* status, moe_stream_t stream) {
     return gemm_entry(0, x_perm, w_gate_up, offsets, M, d, f, E, 1, h, status, stream,
                       "moe_grouped_gemm_gateup_swiglu");
+}
+
+int moe_grouped_gemm_gateup_swiglu_gather(const void* x, const int32_t* src, int T, const void* w_gate_up,
+                                          const int32_t* offsets, int M, int d, int f, int E, void* h,
+                                          int32_t* status, moe_stream_t stream) {
+    if (T < 0) return fail(MOE_ERR_INVALID_ARG, "moe_grouped_gemm_gateup_swiglu_gather: T = %d must be >= 0", T);
+    if (M > 0 && (!src || T == 0))
+        return fail(MOE_ERR_INVALID_ARG, "moe_grouped_gemm_gateup_swiglu_gather: null src or empty x");
+    return gemm_entry(0, x, w_gate_up, offsets, M, d, f, E, 1, h, status, stream,
+                      "moe_grouped_gemm_gateup_swiglu_gather", src, T);
 }
 
 int moe_grouped_gemm_down(const void* h, const void* w_down, const int32_t* offsets, int M, int d, int f,

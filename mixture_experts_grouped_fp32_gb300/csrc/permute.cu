@@ -147,6 +147,7 @@ permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int
     // Row copies: x[t] -> x_perm[row(t, j)] for each slot j, 16 bytes per access.  Each thread
     // first issues kCopyBatch independent loads, then their k stores each, so that enough reads
     // are in flight to cover the memory latency.
+    if (x_perm == nullptr) return;  // the gate+up GEMM gathers x rows itself
     const int dv = d / 8;  // uint4 per row
     const int nvec = (t1 - t0) * dv;
     for (int base = tid; base < nvec; base += kPermThreads * kCopyBatch) {
@@ -303,6 +304,7 @@ route_permute_kernel(const float* __restrict__ logits, const uint4* __restrict__
         crow[tid] = row;
     }
     __syncthreads();
+    if (x_perm == nullptr) return;  // the gate+up GEMM gathers x rows itself
     const int dv = d / 8;
     const int nvec = (t1 - t0) * dv;
     for (int base = tid; base < nvec; base += kPermThreads * kCopyBatch) {

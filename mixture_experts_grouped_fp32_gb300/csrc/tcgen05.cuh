@@ -52,6 +52,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// ---------------------------------------------------------------------------------------------
+// cp.async (16-byte global -> shared copies issued per thread; used to gather rows)
+// ---------------------------------------------------------------------------------------------
+// Copies 16 bytes from global `src` to shared `dst_smem`; with src_bytes = 0 nothing is read and
+// the 16 destination bytes are zero-filled.  `src` must be a valid, 16-byte aligned address.
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+// The same with an L2 cache-eviction policy for the source line (policy from createpolicy).
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst_smem, const void* src, uint32_t src_bytes,
+                                                 uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst_smem), "l"(src),
+                 "r"(src_bytes), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Longest a pipeline wait may take before the kernel gives up (a correct kernel waits at most
 // one tile's main loop, microseconds).
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s

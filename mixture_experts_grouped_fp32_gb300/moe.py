@@ -32,6 +32,7 @@ _SIGS = {
                             _I),
     "moe_permute": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_gateup_swiglu": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "moe_grouped_gemm_gateup_swiglu_gather": ([_P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gemm_down": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_down_ksplit": ([_I, _I, _I, _I, _I], _I),
     "moe_gemm_pair_mode": ([_I, _I, _I, _I, _I, _I], _I),
@@ -48,6 +49,7 @@ STATUS_BAD_EXPERT_ID = 0x1
 STATUS_BAD_OFFSETS = 0x2
 STATUS_BAD_DEST = 0x4
 STATUS_WAIT_TIMEOUT = 0x8
+STATUS_BAD_SRC = 0x10
 
 
 class MoeError(RuntimeError):
@@ -173,6 +175,21 @@ def grouped_gemm_gateup_swiglu(x_perm, w_gate_up, offsets, h=None, status=None, 
     h = h if h is not None else torch.empty(M, f2 // 2, dtype=torch.bfloat16, device=x_perm.device)
     _call("moe_grouped_gemm_gateup_swiglu", _ptr(x_perm), _ptr(w_gate_up), _ptr(offsets), M, d, f2 // 2, E,
           _ptr(h), _ptr(status), _stream(stream))
+    return h
+
+
+def grouped_gemm_gateup_swiglu_gather(x, src, w_gate_up, offsets, h=None, status=None, stream=None):
+    """Step 3 reading row r of the grouped operand as x[src[r]] (the kernel gathers the rows)."""
+    _dev(x, torch.bfloat16, "x")
+    _dev(src, torch.int32, "src")
+    _dev(w_gate_up, torch.bfloat16, "w_gate_up")
+    _dev(offsets, torch.int32, "offsets")
+    T, d = x.shape
+    M = src.numel()
+    E, _, f2 = w_gate_up.shape
+    h = h if h is not None else torch.empty(M, f2 // 2, dtype=torch.bfloat16, device=x.device)
+    _call("moe_grouped_gemm_gateup_swiglu_gather", _ptr(x), _ptr(src), T, _ptr(w_gate_up), _ptr(offsets), M, d,
+          f2 // 2, E, _ptr(h), _ptr(status), _stream(stream))
     return h
 
 

@@ -48,7 +48,8 @@ def test_full_size_forward(oracle, name, path, monkeypatch):
     assert np.array_equal(v["src"].cpu().numpy(), src)
     assert np.array_equal(v["dest"].cpu().numpy(), dest)
     xb = to_np_bits(x)
-    assert np.array_equal(to_np_bits(v["x_perm"].cpu()), xb[src])
+    if os.environ.get("MOE_GATHER") != "1":  # with MOE_GATHER=1 the gate+up GEMM gathers x rows itself
+        assert np.array_equal(to_np_bits(v["x_perm"].cpu()), xb[src])
 
     rng = np.random.default_rng(1)
     hot = int(np.argmax(counts))

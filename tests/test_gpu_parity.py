@@ -64,9 +64,10 @@ MODES = {"default": {}, "noswap": {"MOE_GEMM_SWAP_MAX": "0", "MOE_GEMM_2SM": "0"
          "pairsplit": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_SPLIT": "30"},
          "pairmix": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_SPLIT": "mix"},
          "pairauto": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_SPLIT": "auto"},
-         "ksplit3": {"MOE_DOWN_KSPLIT": "3"}, "nofuse": {"MOE_FUSE_ROUTE_PERMUTE": "0"}}
+         "ksplit3": {"MOE_DOWN_KSPLIT": "3"}, "nofuse": {"MOE_FUSE_ROUTE_PERMUTE": "0"},
+         "gather": {"MOE_GATHER": "1"}}
 ENV_KNOBS = ("MOE_GEMM_SWAP_MAX", "MOE_DOWN_KSPLIT", "MOE_GEMM_2SM", "MOE_GEMM_PAIR_SWAP_MAX", "MOE_GEMM_2SM_DOWN",
-             "MOE_FUSE_ROUTE_PERMUTE", "MOE_GEMM_PAIR_LAYOUT", "MOE_GEMM_PAIR_SPLIT")
+             "MOE_FUSE_ROUTE_PERMUTE", "MOE_GEMM_PAIR_LAYOUT", "MOE_GEMM_PAIR_SPLIT", "MOE_GATHER")
 
 
 @pytest.fixture(params=sorted(MODES))
@@ -92,7 +93,8 @@ def test_forward_matches_oracle(moe, oracle, w, mode):
     assert np.array_equal(v["offsets"].cpu().numpy(), offsets)
     assert np.array_equal(v["src"].cpu().numpy(), src)
     assert np.array_equal(v["dest"].cpu().numpy(), dest)
-    assert np.array_equal(to_np_bits(v["x_perm"].cpu()), to_np_bits(x)[src])
+    if mode != "gather":  # with MOE_GATHER=1 the gate+up GEMM gathers x rows itself; x_perm is unused
+        assert np.array_equal(to_np_bits(v["x_perm"].cpu()), to_np_bits(x)[src])
     ref = oracle.forward(to_np_bits(x), ln, to_np_bits(wgu), to_np_bits(wd), w.k)
     assert_layer_close(out.float().cpu().numpy(), ref, w.name)
 
@@ -200,6 +202,35 @@ def test_gateup_swiglu_parity(moe, oracle, T, d, f, E, k, bias, swap_max, pair, 
     assert_close(got, ref, 2.0 ** -7, 2e-3, "h")
 
 
+@pytest.mark.parametrize("swap_max,pair", [("128", "0"), ("0", "0"), ("64", "1"), ("64", "2:128:0"),
+                                           ("64", "2:64:0"), ("64", "2:128:auto"), ("64", "2:64:40")])
+@pytest.mark.parametrize("T,d,f,E,k,bias", GEMM_CASES)
+def test_gateup_swiglu_gather_parity(moe, oracle, T, d, f, E, k, bias, swap_max, pair, monkeypatch):
+    """The gate+up GEMM gathering its rows from x by src (what moe_forward runs) against the oracle
+    applied to x[src]: every kernel form, with src a random permutation-with-repeats of x's rows."""
+    _set_gemm_env(monkeypatch, swap_max, pair)
+    offsets = _segments(oracle, T, E, k, seed=11, bias=bias)
+    M = T * k
+    x = random_bf16((T, d), seed=15)
+    g = torch.Generator("cpu").manual_seed(T + d)
+    src = torch.randint(0, T, (M,), generator=g, dtype=torch.int32)
+    _, _, wgu, _ = case_inputs(Workload("g", 1, d, f, E, 1), seed=2)
+    extra = 3
+    h = torch.full((M + extra, f), float("nan"), dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    moe.grouped_gemm_gateup_swiglu_gather(x.to(DEV), src.to(DEV), wgu.to(DEV), torch.from_numpy(offsets).to(DEV),
+                                          h=h, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    xb = to_np_bits(x)
+    ref = oracle.gateup_swiglu(oracle.gather_rows(xb, src.numpy()), offsets, to_np_bits(wgu))
+    got = h[:M].float().cpu().numpy()
+    assert np.isfinite(got).all(), "some h rows were not written"
+    assert torch.isnan(h[M:].float()).all(), "rows past offsets[E] were written"
+    assert float(np.abs(got - ref).max()) <= 1e-2 * float(np.abs(ref).max())
+    assert_close(got, ref, 2.0 ** -7, 2e-3, "h (gathered)")
+
+
 @pytest.mark.parametrize("swap_max,ksplit,pair", [("128", 1, "0"), ("0", 1, "0"), ("128", 3, "0"), ("0", 5, "0"),
                                                   ("128", 8, "0"), ("64", 1, "1"), ("64", 3, "1"), ("64", 1, "2:128"),
                                                   ("64", 3, "2:64"), ("64", 2, "2:0"), ("64", 1, "2:128:40"),
@@ -268,6 +299,24 @@ def test_status_flags_bad_offsets(moe):
         moe.grouped_gemm_gateup_swiglu(x_perm, wgu, offs, h=h, status=status)
         torch.cuda.synchronize()
         assert int(status.item()) & moe.STATUS_BAD_OFFSETS
+
+
+def test_status_flags_bad_src(moe):
+    """A gathering gate+up GEMM given src indices outside [0, T) reads zero rows for them and sets
+    MOE_STATUS_BAD_SRC instead of reading out of bounds."""
+    E, d, f, T = 2, 64, 128, 8
+    x = torch.ones(T, d, dtype=torch.bfloat16, device=DEV)
+    wgu = torch.zeros(E, d, 2 * f, dtype=torch.bfloat16, device=DEV)
+    h = torch.zeros(16, f, dtype=torch.bfloat16, device=DEV)
+    offs = torch.tensor([0, 8, 16], dtype=torch.int32, device=DEV)
+    for bad in (T, -1, 1 << 30):
+        src = torch.arange(16, dtype=torch.int32, device=DEV) % T
+        src[5] = bad
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        moe.grouped_gemm_gateup_swiglu_gather(x, src, wgu, offs, h=h, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) & moe.STATUS_BAD_SRC
+        assert torch.isfinite(h.float()).all()
 
 
 def test_status_flags_bad_dest(moe):
