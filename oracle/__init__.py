@@ -44,6 +44,7 @@ def _needs_build() -> bool:
 _I32P = ctypes.POINTER(ctypes.c_int32)
 _F32P = ctypes.POINTER(ctypes.c_float)
 _U16P = ctypes.POINTER(ctypes.c_uint16)
+_U8P = ctypes.POINTER(ctypes.c_uint8)
 _INT = ctypes.c_int
 
 _SIGS = {
@@ -62,6 +63,12 @@ _SIGS = {
     "oracle_forward_routed": ([_U16P, _I32P, _F32P, _U16P, _U16P, _INT, _INT, _INT, _INT, _INT, _F32P], _INT),
     "oracle_forward_tokens_routed": ([_U16P, _I32P, _F32P, _U16P, _U16P, _INT, _INT, _INT, _INT, _INT, _I32P,
                                       _INT, _F32P], _INT),
+    "oracle_e4m3_encode_array": ([_F32P, _INT, _U8P], None),
+    "oracle_e4m3_decode_array": ([_U8P, _INT, _F32P], None),
+    "oracle_quantize_rows_fp8": ([_U16P, _INT, _INT, _U8P, _F32P], None),
+    "oracle_quantize_weights_fp8": ([_U16P, _INT, _INT, _INT, _U8P, _F32P], None),
+    "oracle_forward_fp8_tokens_routed": ([_U16P, _I32P, _F32P, _U8P, _F32P, _U8P, _F32P, _INT, _INT, _INT, _INT,
+                                          _INT, _I32P, _INT, _F32P], _INT),
 }
 
 
@@ -250,6 +257,60 @@ class Oracle:
         if rc:
             raise ValueError(f"oracle_forward_tokens_routed failed (rc={rc})")
         return out
+
+    # ---- FP8 variant ----
+    def e4m3_encode(self, x):
+        x = _c(x, np.float32)
+        out = np.empty(x.shape, np.uint8)
+        self.L.oracle_e4m3_encode_array(_p(x.reshape(-1), _F32P), x.size, _p(out.reshape(-1), _U8P))
+        return out
+
+    def e4m3_decode(self, codes):
+        codes = _c(codes, np.uint8)
+        out = np.empty(codes.shape, np.float32)
+        self.L.oracle_e4m3_decode_array(_p(codes.reshape(-1), _U8P), codes.size, _p(out.reshape(-1), _F32P))
+        return out
+
+    def quantize_rows_fp8(self, a_bits):
+        a_bits = _c(a_bits, np.uint16)
+        R, C = a_bits.shape
+        q = np.empty((R, C), np.uint8)
+        sc = np.empty(R, np.float32)
+        self.L.oracle_quantize_rows_fp8(_p(a_bits, _U16P), R, C, _p(q, _U8P), _p(sc, _F32P))
+        return q, sc
+
+    def quantize_weights_fp8(self, w_bits):
+        """W [E, K, N] bf16 bits -> (codes [E, N, K], scales [E, N])."""
+        w_bits = _c(w_bits, np.uint16)
+        E, K, N = w_bits.shape
+        q = np.empty((E, N, K), np.uint8)
+        sc = np.empty((E, N), np.float32)
+        self.L.oracle_quantize_weights_fp8(_p(w_bits, _U16P), E, K, N, _p(q, _U8P), _p(sc, _F32P))
+        return q, sc
+
+    def forward_fp8_tokens_routed(self, x_bits, idx_rows, w_rows, wgu8, sgu, wd8, sd, tokens):
+        x_bits = _c(x_bits, np.uint16)
+        idx_rows = _c(idx_rows, np.int32)
+        w_rows = _c(w_rows, np.float32)
+        wgu8, wd8 = _c(wgu8, np.uint8), _c(wd8, np.uint8)
+        sgu, sd = _c(sgu, np.float32), _c(sd, np.float32)
+        tokens = _c(tokens, np.int32)
+        T, d = x_bits.shape
+        E, f2, _ = wgu8.shape
+        k = idx_rows.shape[1]
+        out = np.empty((tokens.shape[0], d), np.float32)
+        rc = self.L.oracle_forward_fp8_tokens_routed(
+            _p(x_bits, _U16P), _p(idx_rows, _I32P), _p(w_rows, _F32P), _p(wgu8, _U8P), _p(sgu, _F32P),
+            _p(wd8, _U8P), _p(sd, _F32P), T, d, f2 // 2, E, k, _p(tokens, _I32P), tokens.shape[0], _p(out, _F32P))
+        if rc:
+            raise ValueError(f"oracle_forward_fp8_tokens_routed failed (rc={rc})")
+        return out
+
+    def forward_fp8(self, x_bits, logits, wgu8, sgu, wd8, sd, k):
+        """The whole FP8 layer with the softmax router (every token)."""
+        idx, w = self.route(logits, k)
+        T = idx.shape[0]
+        return self.forward_fp8_tokens_routed(x_bits, idx, w, wgu8, sgu, wd8, sd, np.arange(T, dtype=np.int32))
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:

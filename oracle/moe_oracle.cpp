@@ -62,6 +62,67 @@ inline float bf16_to_f32(uint16_t b) {
 
 inline float silu(float z) { return z / (1.0f + std::exp(-z)); }
 
+// fp32 -> bf16, round to nearest even (finite inputs).
+inline uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u;
+    std::memcpy(&u, &f, sizeof u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return static_cast<uint16_t>(u >> 16);
+}
+
+// FP8 E4M3 (the OCP 8-bit floating-point format's E4M3 variant): 1 sign bit, 4 exponent bits
+// with bias 7, 3 mantissa bits; no infinities; S.1111.111 is NaN; largest finite 448 = 1.75 * 2^8;
+// normals 1.m * 2^(e-7) for e = 1..15 (e = 15 with m = 7 excluded); subnormals m/8 * 2^-6.
+inline float e4m3_decode(uint8_t c) {
+    const int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return std::nanf("");
+    const double v = e == 0 ? std::ldexp(m / 8.0, -6) : std::ldexp(1.0 + m / 8.0, e - 7);
+    return static_cast<float>(sgn ? -v : v);
+}
+
+// Round to the nearest E4M3 value, ties to even mantissa; magnitudes that round above 448 become
+// 448 (saturation to the largest finite value).  NaN maps to the NaN code.
+inline uint8_t e4m3_encode(float x) {
+    if (std::isnan(x)) return 0x7F;
+    const uint8_t sgn = std::signbit(x) ? 0x80 : 0x00;
+    const double a = std::fabs(static_cast<double>(x));
+    // Quantum of the binade holding a (subnormal range: 2^-9).
+    int ex = 0;
+    std::frexp(a, &ex);                  // a = f * 2^ex, f in [0.5, 1)
+    const int e_unb = a > 0 ? std::max(ex - 1, -6) : -6;  // unbiased exponent, floor at the subnormal one
+    const double quantum = std::ldexp(1.0, e_unb - 3);
+    const double q = std::nearbyint(a / quantum);  // default rounding mode: to nearest, ties to even
+    double v = q * quantum;
+    if (v > 448.0) v = 448.0;
+    // Encode v (exactly representable by construction).
+    if (v == 0.0) return sgn;
+    int e2 = 0;
+    const double f2 = std::frexp(v, &e2);  // v = f2 * 2^e2
+    int exp_field = (e2 - 1) + 7;
+    int man;
+    if (exp_field <= 0) {  // subnormal: v = m/8 * 2^-6
+        exp_field = 0;
+        man = static_cast<int>(std::lround(v / std::ldexp(1.0, -9)));
+    } else {
+        man = static_cast<int>(std::lround((f2 * 2.0 - 1.0) * 8.0));
+    }
+    return static_cast<uint8_t>(sgn | (exp_field << 3) | man);
+}
+
+// Per-row FP8 quantisation of a [R, C] matrix: absmax over the row, inv = 448 / absmax (fp32),
+// code = e4m3(value * inv), dequantisation scale = absmax / 448 (fp32); an all-zero row gets
+// scale 1 and zero codes.
+template <class GetF>
+void quantize_rows_fp8(GetF get, int R, int C, uint8_t* q, float* scale) {
+    for (int r = 0; r < R; ++r) {
+        float amax = 0.0f;
+        for (int c = 0; c < C; ++c) amax = std::max(amax, std::fabs(get(r, c)));
+        const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
+        scale[r] = amax > 0.0f ? amax / 448.0f : 1.0f;
+        for (int c = 0; c < C; ++c) q[static_cast<size_t>(r) * C + c] = e4m3_encode(get(r, c) * inv);
+    }
+}
+
 // One permuted row through expert e: g, u over i = 0..d-1 ascending; h = silu(g) * u.
 void gateup_row(const float* x, const uint16_t* Wgu_e, int d, int f, float* h, float* g, float* u) {
     for (int n = 0; n < f; ++n) { g[n] = 0.0f; u[n] = 0.0f; }
@@ -371,6 +432,102 @@ int oracle_forward_tokens(const uint16_t* x, const float* logits, const uint16_t
                      w.data() + s * k);
     return oracle_forward_tokens_routed(x, idx.data(), w.data(), Wgu, Wd, T, d, f, E, k, tokens, ntok,
                                         out_rows);
+}
+
+// ---------------------------------------------------------------------------------------------
+// FP8 variant of the layer (the grouped GEMMs on E4M3 operands).  Scaling: per token for the
+// activations (x and h rows), per output channel for the weights (for expert e and output column
+// n, over the K dimension) — scales that factor out of each dot product, so
+//   g[n] = (sum_i dec(x8[t][i]) * dec(Wgu8[e][n][i])) * (sx[t] * sgu[e][n])    (n < f: gate, f.. up)
+//   h    = bf16(silu(g) * u), then quantised per row:  h8, sh[r]
+//   y[m] = (sum_n dec(h8[r][n]) * dec(Wd8[e][m][n])) * (sh[r] * sd[e][m])
+//   out  = sum_j w_j * y   (slot order)
+// Weights are stored transposed, [E, N, K] (K contiguous).
+// ---------------------------------------------------------------------------------------------
+uint8_t oracle_e4m3_encode(float x) { return e4m3_encode(x); }
+float oracle_e4m3_decode(uint8_t c) { return e4m3_decode(c); }
+
+void oracle_e4m3_encode_array(const float* x, int n, uint8_t* out) {
+    for (int i = 0; i < n; ++i) out[i] = e4m3_encode(x[i]);
+}
+void oracle_e4m3_decode_array(const uint8_t* c, int n, float* out) {
+    for (int i = 0; i < n; ++i) out[i] = e4m3_decode(c[i]);
+}
+
+// Rows of a bf16 matrix [R, C] -> codes [R, C] and scales [R] (see quantize_rows_fp8).
+void oracle_quantize_rows_fp8(const uint16_t* a, int R, int C, uint8_t* q, float* scale) {
+    quantize_rows_fp8([&](int r, int c) { return bf16_to_f32(a[static_cast<size_t>(r) * C + c]); }, R, C, q,
+                      scale);
+}
+
+// Weights W [E, K, N] bf16 -> Wq [E, N, K] codes (transposed) and scales [E, N]: output column n
+// of expert e is quantised over its K values like a row.
+void oracle_quantize_weights_fp8(const uint16_t* W, int E, int K, int N, uint8_t* Wq, float* scale) {
+    for (int e = 0; e < E; ++e) {
+        const uint16_t* We = W + static_cast<size_t>(e) * K * N;
+        quantize_rows_fp8([&](int n, int k) { return bf16_to_f32(We[static_cast<size_t>(k) * N + n]); }, N, K,
+                          Wq + static_cast<size_t>(e) * N * K, scale + static_cast<size_t>(e) * N);
+    }
+}
+
+// The FP8 layer's output for the given tokens (all T of them for the whole layer) with their
+// routing idx_rows/w_rows [ntok, k]; out_rows [ntok, d] fp32.  Returns 0 or a negative code.
+int oracle_forward_fp8_tokens_routed(const uint16_t* x, const int32_t* idx_rows, const float* w_rows,
+                                     const uint8_t* Wgu8, const float* sgu, const uint8_t* Wd8, const float* sd,
+                                     int T, int d, int f, int E, int k, const int32_t* tokens, int ntok,
+                                     float* out_rows) {
+    if (!valid_shape(T, E, k) || d < 1 || f < 1) return -1;
+    for (int s = 0; s < ntok; ++s)
+        if (tokens[s] < 0 || tokens[s] >= T) return -1;
+    const size_t npairs = static_cast<size_t>(ntok) * k;
+    for (size_t q = 0; q < npairs; ++q)
+        if (idx_rows[q] < 0 || idx_rows[q] >= E) return -2;
+    std::vector<float> ys(npairs * d);
+#pragma omp parallel
+    {
+        std::vector<uint8_t> x8(d), h8(f);
+        std::vector<float> xd(d), g(f), u(f), hd(f);
+        std::vector<uint16_t> hb(f);
+        float sx = 0.0f, sh = 0.0f;
+#pragma omp for schedule(dynamic, 1)
+        for (long long q = 0; q < static_cast<long long>(npairs); ++q) {
+            const int s = static_cast<int>(q / k);
+            const int e = idx_rows[q];
+            oracle_quantize_rows_fp8(x + static_cast<size_t>(tokens[s]) * d, 1, d, x8.data(), &sx);
+            for (int i = 0; i < d; ++i) xd[i] = e4m3_decode(x8[i]);
+            const uint8_t* We = Wgu8 + static_cast<size_t>(e) * 2 * f * d;
+            const float* se = sgu + static_cast<size_t>(e) * 2 * f;
+            for (int n = 0; n < 2 * f; ++n) {
+                const uint8_t* wrow = We + static_cast<size_t>(n) * d;
+                float acc = 0.0f;
+                for (int i = 0; i < d; ++i) acc += xd[i] * e4m3_decode(wrow[i]);
+                const float v = acc * (sx * se[n]);
+                if (n < f) g[n] = v; else u[n - f] = v;
+            }
+            for (int n = 0; n < f; ++n) hb[n] = f32_to_bf16_rne(silu(g[n]) * u[n]);
+            oracle_quantize_rows_fp8(hb.data(), 1, f, h8.data(), &sh);
+            for (int n = 0; n < f; ++n) hd[n] = e4m3_decode(h8[n]);
+            const uint8_t* Wde = Wd8 + static_cast<size_t>(e) * d * f;
+            const float* sde = sd + static_cast<size_t>(e) * d;
+            float* yr = ys.data() + q * d;
+            for (int m = 0; m < d; ++m) {
+                const uint8_t* wrow = Wde + static_cast<size_t>(m) * f;
+                float acc = 0.0f;
+                for (int n = 0; n < f; ++n) acc += hd[n] * e4m3_decode(wrow[n]);
+                yr[m] = acc * (sh * sde[m]);
+            }
+        }
+    }
+    for (int s = 0; s < ntok; ++s) {
+        float* o = out_rows + static_cast<size_t>(s) * d;
+        for (int m = 0; m < d; ++m) o[m] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const float wj = w_rows[static_cast<size_t>(s) * k + j];
+            const float* yr = ys.data() + (static_cast<size_t>(s) * k + j) * d;
+            for (int m = 0; m < d; ++m) o[m] += wj * yr[m];
+        }
+    }
+    return 0;
 }
 
 }  // extern "C"

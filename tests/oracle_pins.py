@@ -391,6 +391,129 @@ def pin_grouped_invariants(O, seed=29):
         assert max(c[t, kept]) <= min(c[t, ids]) + 1e-7
 
 
+# --------------------------------------------------------------------------------------------
+# The FP8 variant: E4M3 (OCP 8-bit float, E4M3: bias 7, 3 mantissa bits, no infinities, S.1111.111
+# NaN, largest finite 448), per-row / per-output-channel scales absmax / 448.
+# --------------------------------------------------------------------------------------------
+def e4m3_table():
+    """Value of every code, written from the format definition (float64; NaN for the two NaN codes)."""
+    vals = np.empty(256)
+    for c in range(256):
+        sgn, e, m = c >> 7, (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            vals[c] = np.nan
+        elif e == 0:
+            vals[c] = (m / 8) * 2.0 ** -6
+        else:
+            vals[c] = (1 + m / 8) * 2.0 ** (e - 7)
+        if sgn:
+            vals[c] = -vals[c]
+    return vals
+
+
+def pin_e4m3_decode_table(O):
+    """All 256 codes decode to the format's values; the landmarks of the format."""
+    tab = e4m3_table()
+    dec = O.e4m3_decode(np.arange(256, dtype=np.uint8)).astype(np.float64)
+    assert np.array_equal(np.isnan(dec), np.isnan(tab))
+    ok = ~np.isnan(tab)
+    assert np.array_equal(dec[ok], tab[ok])
+    assert dec[0x7E] == 448 and dec[0x08] == 2.0 ** -6 and dec[0x01] == 2.0 ** -9 and dec[0x38] == 1.0
+    assert np.isnan(dec[0x7F]) and np.isnan(dec[0xFF])
+
+
+def e4m3_brute_encode(x):
+    """Nearest E4M3 code by search over every finite value, ties to the even (lsb 0) code, values
+    above 448 saturating to +-448; NaN -> 0x7F."""
+    tab = e4m3_table()
+    pos = [c for c in range(128) if not np.isnan(tab[c])]
+    pv = np.array([tab[c] for c in pos])
+    out = np.empty(x.shape, np.uint8)
+    for i, v in enumerate(np.asarray(x, np.float64).reshape(-1)):
+        if np.isnan(v):
+            out.reshape(-1)[i] = 0x7F
+            continue
+        a = min(abs(v), 448.0)
+        dist = np.abs(pv - a)
+        best = np.flatnonzero(dist == dist.min())
+        c = pos[best[0]] if len(best) == 1 else next(pos[b] for b in best if pos[b] % 2 == 0)
+        out.reshape(-1)[i] = c | (0x80 if np.signbit(v) else 0)
+    return out
+
+
+def pin_e4m3_encode_rne(O, seed=41):
+    """Encoding = nearest-value search with ties to even and saturation: on every representable
+    value, every midpoint between neighbours (the ties), just above and below each midpoint, and
+    random magnitudes across the whole range (subnormals and saturation included)."""
+    tab = e4m3_table()
+    fin = np.array(sorted({abs(v) for v in tab if not np.isnan(v)}))
+    mids = (fin[:-1] + fin[1:]) / 2
+    rng = np.random.default_rng(seed)
+    rand = np.exp(rng.uniform(np.log(2.0 ** -12), np.log(600.0), 4000)) * rng.choice([-1, 1], 4000)
+    xs = np.concatenate([fin, -fin, mids, -mids, np.nextafter(mids.astype(np.float32), np.float32(np.inf)),
+                         np.nextafter(mids.astype(np.float32), np.float32(0)), rand, [460.0, 464.0, 470.0, 1e6]])
+    xs = xs.astype(np.float32)
+    assert np.array_equal(O.e4m3_encode(xs), e4m3_brute_encode(xs))
+
+
+def pin_quantize_rows_fp8(O, seed=43):
+    """Per-row quantisation: scale = absmax / 448, the absmax element maps to +-448 exactly, every
+    value is within half a quantum of its code's value times the scale, and a zero row gives
+    scale 1 and zero codes."""
+    rng = np.random.default_rng(seed)
+    a = rng.standard_normal((20, 300)).astype(np.float32) * np.exp(rng.uniform(-6, 6, (20, 1))).astype(np.float32)
+    a[3] = 0.0
+    bits = f32_to_bf16_bits(a)
+    af = bf16_bits_to_f32(bits).astype(np.float64)
+    q, sc = O.quantize_rows_fp8(bits)
+    tab = e4m3_table()
+    for r in range(a.shape[0]):
+        amax = np.abs(af[r]).max()
+        if amax == 0:
+            assert sc[r] == 1.0 and not q[r].any()
+            continue
+        assert sc[r] == np.float32(np.float32(amax) / np.float32(448.0))
+        j = int(np.argmax(np.abs(af[r])))
+        assert abs(tab[q[r, j]]) == 448.0
+        rec = tab[q[r]] * sc[r]
+        # half a quantum: 2^-4 relative for normals, 2^-10 * scale in the subnormal range
+        bound = np.maximum(np.abs(af[r]) * 2.0 ** -4, 2.0 ** -10 * sc[r]) * (1 + 1e-6)
+        assert np.all(np.abs(rec - af[r]) <= bound), r
+
+
+def pin_fp8_forward(O, seed=47):
+    """The FP8 layer against a float64 statement of it built from the pinned pieces (router,
+    E4M3 quantiser): dequantised operands, per-row and per-channel scales, h rounded to bf16 and
+    requantised per row, slot-ordered combine."""
+    rng = np.random.default_rng(seed)
+    T, d, f, E, k = 9, 32, 48, 4, 2
+    logits, x_bits, wgu, wd = random_layer(rng, T, d, f, E)
+    wgu8, sgu = O.quantize_weights_fp8(wgu)
+    wd8, sdn = O.quantize_weights_fp8(wd)
+    # The weight quantiser is the row quantiser on the transposed weights.
+    for e in range(E):
+        q, sc = O.quantize_rows_fp8(np.ascontiguousarray(wgu[e].T))
+        assert np.array_equal(q, wgu8[e]) and np.array_equal(sc, sgu[e])
+    out = O.forward_fp8(x_bits, logits, wgu8, sgu, wd8, sdn, k)
+    idx, w = O.route(logits, k)
+    tab = e4m3_table()
+    ref = np.zeros((T, d))
+    for t in range(T):
+        x8, sx = O.quantize_rows_fp8(x_bits[t:t + 1])
+        xd = tab[x8[0]]
+        for j in range(k):
+            e = idx[t, j]
+            gu = (tab[wgu8[e]] @ xd) * (np.float64(sx[0]) * sgu[e].astype(np.float64))
+            g, u = gu[:f], gu[f:]
+            hb = f32_to_bf16_bits((g / (1 + np.exp(-g)) * u).astype(np.float32))[None, :]
+            h8, sh = O.quantize_rows_fp8(hb)
+            y = (tab[wd8[e]] @ tab[h8[0]]) * (np.float64(sh[0]) * sdn[e].astype(np.float64))
+            ref[t] += w[t, j] * y
+    err = np.abs(out - ref).max()
+    assert err <= 2e-3 * np.abs(ref).max(), err
+
+
 ALL_PINS = [pin_hand_example, pin_brute_force, pin_dense_e1_k1, pin_route_library,
             pin_permute_library, pin_invariants, pin_stages, pin_grouped_hand_example,
-            pin_grouped_reduces_to_topk, pin_grouped_brute_force, pin_grouped_invariants]
+            pin_grouped_reduces_to_topk, pin_grouped_brute_force, pin_grouped_invariants,
+            pin_e4m3_decode_table, pin_e4m3_encode_rne, pin_quantize_rows_fp8, pin_fp8_forward]

@@ -46,6 +46,13 @@ MUTANTS = {
     "grouped_group_ties_higher": ("return gscore[a] > gscore[b]; });",
                                   "return gscore[a] > gscore[b] || (gscore[a] == gscore[b] && a > b); });"),
     "grouped_affinity_sign": ("sc[e] = 1.0f / (1.0f + std::exp(-l[e]));", "sc[e] = 1.0f / (1.0f + std::exp(l[e]));"),
+    # the FP8 variant
+    "e4m3_ties_away": ("const double q = std::nearbyint(a / quantum);", "const double q = std::round(a / quantum);"),
+    "e4m3_no_saturation": ("if (v > 448.0) v = 448.0;", "if (v > 480.0) v = 480.0;"),
+    "fp8_row_scale_dropped": ("scale[r] = amax > 0.0f ? amax / 448.0f : 1.0f;", "scale[r] = 1.0f;"),
+    "fp8_weight_scale_dropped": ("const float v = acc * (sx * se[n]);", "const float v = acc * sx;"),
+    "fp8_h_unquantised": ("for (int n = 0; n < f; ++n) hd[n] = e4m3_decode(h8[n]);",
+                          "for (int n = 0; n < f; ++n) hd[n] = bf16_to_f32(hb[n]) / sh;"),
 }
 
 _CHILD = textwrap.dedent("""
