@@ -20,6 +20,9 @@ ours (default):
 reference:
   the CPU oracle as the reference arm: each step is the oracle's forward on a bounded token
   sample of the same workload, timed on the host cores.
+--dtype e4m3 times the FP8 variant instead (moe_forward_fp8: the grouped GEMMs on E4M3 codes with
+per-row / per-output-channel scales; weights quantised once before the timed region), with the
+same metric, and the FP8 oracle as CPU baseline and reference arm.
 Under torchrun (N > 1) each rank runs an independent replica of the layer on its own GPU (the
 layer has no cross-rank exchange); value = tokens of all ranks / max-over-ranks time.
 """
@@ -52,6 +55,11 @@ STAGES = ("route", "permute", "gateup_swiglu", "down", "combine")
 KERNEL_NAMES = {"route": "route_kernel", "permute": "permute_kernel",
                 "gateup_swiglu": "grouped_gemm_kernel<0>", "down": "grouped_gemm_kernel<1>",
                 "combine": "combine_kernel"}
+# The FP8 layer's stages (moe_forward_fp8) and its GEMM kernels' template instances <KIND, GATHER, FP8>.
+STAGES_FP8 = ("route", "permute", "quantize_x", "gateup_swiglu", "quantize_h", "down", "combine")
+KERNEL_NAMES_FP8 = {"gateup_swiglu": "grouped_gemm_kernel<0, false, true>",
+                    "down": "grouped_gemm_kernel<1, false, true>"}
+FP8_OVER_BF16 = 2.0  # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s) applied to the measured bf16 peak
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum per launch) from ncu captures of the
 # kernel source with the recorded hash (profiles/grouped_gemm_*.md); reported only while the GEMM
@@ -108,9 +116,20 @@ def load_peaks():
 # ----------------------------------------------------------------------------------------------
 # Algorithmic work per stage (what the layer must move / compute, not what the kernels happen to)
 # ----------------------------------------------------------------------------------------------
-def stage_work(w: Workload, n_active: int) -> dict:
+def stage_work(w: Workload, n_active: int, fp8: bool = False) -> dict:
     T, d, f, E, k = w.T, w.d, w.f, w.E, w.k
     M = T * k
+    if fp8:  # 1-byte codes; weight scales 4 bytes per output column, activation scales per row
+        return {
+            "route": {"bytes": T * E * 4 + M * 8, "flops": 0},
+            "permute": {"bytes": M * 4 + (E + E + 1 + 2 * M) * 4, "flops": 0},
+            "quantize_x": {"bytes": M * 4 + T * d * 2 + M * d + M * 4, "flops": 0},
+            "gateup_swiglu": {"bytes": n_active * (d * 2 * f + 2 * f * 4) + M * d + M * 4 + M * f * 2,
+                              "flops": 4 * M * d * f},
+            "quantize_h": {"bytes": M * f * 2 + M * f + M * 4, "flops": 0},
+            "down": {"bytes": n_active * (f * d + d * 4) + M * f + M * 4 + M * d * 4, "flops": 2 * M * d * f},
+            "combine": {"bytes": M * d * 4 + M * 8 + T * d * 2, "flops": 2 * M * d},
+        }
     return {
         "route": {"bytes": T * E * 4 + M * 8, "flops": 0},
         "permute": {"bytes": M * 4 + T * d * 2 + M * d * 2 + (E + E + 1 + 2 * M) * 4, "flops": 0},
@@ -120,8 +139,9 @@ def stage_work(w: Workload, n_active: int) -> dict:
     }
 
 
-def layer_work(w: Workload, n_active: int) -> dict:
-    return {"bytes": n_active * 3 * w.d * w.f * 2 + w.T * w.d * 2 + w.T * w.E * 4 + w.T * w.d * 2,
+def layer_work(w: Workload, n_active: int, fp8: bool = False) -> dict:
+    wbytes = n_active * (3 * w.d * w.f + 4 * (2 * w.f + w.d)) if fp8 else n_active * 3 * w.d * w.f * 2
+    return {"bytes": wbytes + w.T * w.d * 2 + w.T * w.E * 4 + w.T * w.d * 2,
             "flops": 6 * w.T * w.k * w.d * w.f}
 
 
@@ -217,10 +237,18 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     torch.cuda.set_device(dev)
     moe.load()
 
+    fp8 = args.dtype == "e4m3"
     logits, x, wgu, wd = make_inputs(w, seed=args.seed + rank, weight_device=str(dev))
     x_d, l_d = x.to(dev), logits.to(dev)
-    ws = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k) + moe.host_staging_size(w.T, w.d, w.E),
-                     dtype=torch.uint8, device=dev)
+    if fp8:
+        if w.router[0] == "grouped":
+            raise SystemExit("--dtype e4m3 runs the softmax router only")
+        w8 = moe.quantize_weights_fp8(wgu) + moe.quantize_weights_fp8(wd)  # (wgu8, sgu, wd8, sd), once
+        torch.cuda.synchronize(dev)
+        ws = torch.empty(moe.workspace_size_fp8(w.T, w.d, w.f, w.E, w.k), dtype=torch.uint8, device=dev)
+    else:
+        ws = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k) + moe.host_staging_size(w.T, w.d, w.E),
+                         dtype=torch.uint8, device=dev)
     out = torch.empty(w.T, w.d, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if args.flush_l2 else None
     stream = torch.cuda.current_stream(dev)
@@ -229,7 +257,9 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     bias_d = draw_router_bias(w, seed=args.seed + rank).to(dev)
 
     def step():
-        if grouped:  # DeepSeek-V3's router as step 1
+        if fp8:
+            moe.forward_fp8(x_d, l_d, *w8, w.k, out=out, workspace=ws)
+        elif grouped:  # DeepSeek-V3's router as step 1
             _, G, tg, scale, _ = w.router
             moe.forward_grouped(x_d, l_d, bias_d, wgu, wd, w.k, G, tg, scale, out=out, workspace=ws)
         else:
@@ -252,7 +282,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         est = max_over_ranks(e0.elapsed_time(e1) / 3, dist, dev)
         args.steps = int(min(AUTO_STEPS_MAX, max(AUTO_STEPS_MIN, math.ceil(AUTO_TIMED_S * 1e3 / est))))
 
-    v = moe.workspace_views(ws, w.T, w.d, w.f, w.E, w.k)
+    v = (moe.workspace_views_fp8 if fp8 else moe.workspace_views)(ws, w.T, w.d, w.f, w.E, w.k)
     counts = v["counts"].cpu().numpy()
     n_active = int((counts > 0).sum())
 
@@ -286,18 +316,32 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
 
     # ---- per-stage timing: the five stage entry points, events between launches ---------------
     idx, wts = v["idx"], v["w"]
-    counts_d, offs, src, dest, xp, h, y = (v["counts"], v["offsets"], v["src"], v["dest"], v["x_perm"],
-                                          v["h"], v["y_perm"])
+    counts_d, offs, src, dest, h, y = (v["counts"], v["offsets"], v["src"], v["dest"], v["h"], v["y_perm"])
     st = v["status"]
-    calls = [
-        (lambda: moe.route_grouped(l_d, bias_d, w.k, *w.router[1:4], idx=idx, w=wts)) if grouped else
-        (lambda: moe.route(l_d, w.k, idx=idx, w=wts)),
-        lambda: moe.permute(idx, x_d, w.E, status=st, out=(counts_d, offs, src, dest, xp)),
-        lambda: moe.grouped_gemm_gateup_swiglu(xp, wgu, offs, h=h, status=st),
-        lambda: moe.grouped_gemm_down(h, wd, offs, y_perm=y, status=st, ksplit=v["ksplit"]),
-        lambda: moe.combine(y, wts, dest, out=out, status=st, ksplit=v["ksplit"]),
-    ]
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    stages = STAGES_FP8 if fp8 else STAGES
+    if fp8:
+        x8, sx, h8, sh = v["x8"], v["sx"], v["h8"], v["sh"]
+        calls = [
+            lambda: moe.route(l_d, w.k, idx=idx, w=wts),
+            lambda: moe.permute(idx, x_d, w.E, status=st, out=(counts_d, offs, src, dest, None)),
+            lambda: moe.quantize_rows_fp8(x_d, src, status=st, out=(x8, sx)),
+            lambda: moe.grouped_gemm_gateup_swiglu_fp8(x8, sx, w8[0], w8[1], offs, h=h, status=st),
+            lambda: moe.quantize_rows_fp8(h, status=st, out=(h8, sh)),
+            lambda: moe.grouped_gemm_down_fp8(h8, sh, w8[2], w8[3], offs, y_perm=y, status=st, ksplit=v["ksplit"]),
+            lambda: moe.combine(y, wts, dest, out=out, status=st, ksplit=v["ksplit"]),
+        ]
+    else:
+        xp = v["x_perm"]
+        calls = [
+            (lambda: moe.route_grouped(l_d, bias_d, w.k, *w.router[1:4], idx=idx, w=wts)) if grouped else
+            (lambda: moe.route(l_d, w.k, idx=idx, w=wts)),
+            lambda: moe.permute(idx, x_d, w.E, status=st, out=(counts_d, offs, src, dest, xp)),
+            lambda: moe.grouped_gemm_gateup_swiglu(xp, wgu, offs, h=h, status=st),
+            lambda: moe.grouped_gemm_down(h, wd, offs, y_perm=y, status=st, ksplit=v["ksplit"]),
+            lambda: moe.combine(y, wts, dest, out=out, status=st, ksplit=v["ksplit"]),
+        ]
+    ns = len(stages)
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(args.steps)]
     torch.cuda.synchronize(dev)
     for i in range(args.steps):
         if flush is not None:
@@ -308,8 +352,8 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
             sev[i][j + 1].record(stream)
     torch.cuda.synchronize(dev)
     stage_ms = {name: statistics.mean(sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(args.steps))
-                for j, name in enumerate(STAGES)}
-    staged_step_ms = statistics.mean(sev[i][0].elapsed_time(sev[i][5]) for i in range(args.steps))
+                for j, name in enumerate(stages)}
+    staged_step_ms = statistics.mean(sev[i][0].elapsed_time(sev[i][ns]) for i in range(args.steps))
 
     # ---- e2e through moe_forward_host ---------------------------------------------------------
     # (grouped router: the same host->device copies, moe_forward_grouped and the copy back, each
@@ -318,7 +362,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     oh = torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory()
 
     def e2e_step():
-        if grouped:
+        if grouped or fp8:
             x_d.copy_(xh, non_blocking=True)
             l_d.copy_(lh, non_blocking=True)
             step()
@@ -342,30 +386,32 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         raise RuntimeError("device status word set during the timed region")
 
     peaks, peak_src = load_peaks()
-    sw = stage_work(w, n_active)
-    lw = layer_work(w, n_active)
+    sw = stage_work(w, n_active, fp8)
+    lw = layer_work(w, n_active, fp8)
     dom = max(("gateup_swiglu", "down"), key=lambda n: stage_ms[n])
     dom_ms = stage_ms[dom]
+    tensor_peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if fp8 else 1.0)
     t_mem = sw[dom]["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_cmp = sw[dom]["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_cmp = sw[dom]["flops"] / (tensor_peak * 1e12)
     if t_cmp > t_mem:
         achieved = sw[dom]["flops"] / (dom_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(tensor_peak, 1),
                 "unit": "TFLOP/s"}
     else:
         achieved = sw[dom]["bytes"] / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = measured_traffic(w.name, dom)
-    kname = KERNEL_NAMES[dom]
-    pair_mode = moe.gemm_pair_mode(w.T, w.d, w.f, w.E, w.k, 0 if dom == "gateup_swiglu" else 1)
+    roof["traffic"] = measured_traffic(w.name, dom + ("_fp8" if fp8 else ""))
+    kname = KERNEL_NAMES_FP8[dom] if fp8 else KERNEL_NAMES[dom]
+    pair_mode = 0 if fp8 else moe.gemm_pair_mode(w.T, w.d, w.f, w.E, w.k, 0 if dom == "gateup_swiglu" else 1)
     if pair_mode >= 1:  # SM-pair kernel, template <KIND, swapping form>
         kname = kname.replace("grouped_gemm_kernel", "grouped_gemm_2sm_kernel").replace(
             ">", ", true>" if pair_mode == 2 else ", false>")
-    roof.update({"kernel": kname, "peak_source": peak_src + " (burst)",
+    psrc = peak_src + " (burst)" + (" x 2 (nominal fp8 / bf16 dense rate)" if fp8 and roof["bound"] == "tensor" else "")
+    roof.update({"kernel": kname, "peak_source": psrc,
                  "algorithmic_per_launch": sw[dom]["flops"] if roof["bound"] == "tensor" else sw[dom]["bytes"],
                  "launch_ms": round(dom_ms, 4)})
-    layer_roof_ms = 1e3 * max(lw["bytes"] / (peaks["hbm_gbs"] * 1e9), lw["flops"] / (peaks["bf16_tflops"] * 1e12))
+    layer_roof_ms = 1e3 * max(lw["bytes"] / (peaks["hbm_gbs"] * 1e9), lw["flops"] / (tensor_peak * 1e12))
 
     return {
         "ms": ms_max, "tokens_per_rank": w.T, "t_wall": t_wall, "clocks": clocks, "stage_ms": stage_ms,
@@ -374,24 +420,28 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         "host_weights": (wgu, wd), "inputs": (logits, x), "step_ms_p10_p90": (
             float(np.percentile(step_ms, 10)), float(np.percentile(step_ms, 90))),
         "peak_src": peak_src, "peaks": peaks, "ksplit": v["ksplit"],
-        "launches_per_step": 5 if grouped else moe.forward_launch_count(w.T, w.E, w.k),
+        "launches_per_step": (moe.forward_fp8_launch_count(w.T, w.E, w.k) if fp8 else
+                              5 if grouped else moe.forward_launch_count(w.T, w.E, w.k)),
     }
 
 
 # ----------------------------------------------------------------------------------------------
 # Oracle timing (CPU baseline and the reference arm)
 # ----------------------------------------------------------------------------------------------
-def oracle_sample_runner(w: Workload, logits, x, wgu, wd, seed: int = 0):
+def oracle_sample_runner(w: Workload, logits, x, wgu, wd, seed: int = 0, fp8: bool = False):
     import oracle as oracle_pkg
     O = oracle_pkg.Oracle()
     xb = bf16_bits(x)
     ln = logits.numpy()
     wgub, wdb = bf16_bits(wgu), bf16_bits(wd)
     bias = draw_router_bias(w, seed).numpy()
+    w8 = O.quantize_weights_fp8(wgub) + O.quantize_weights_fp8(wdb) if fp8 else None  # once, untimed
 
     def run(S: int) -> float:
         t0 = time.perf_counter()
-        if w.router[0] == "grouped":
+        if fp8:
+            O.forward_fp8(xb[:S], ln[:S], *w8, w.k)
+        elif w.router[0] == "grouped":
             idx, wts = O.route_grouped(ln[:S], bias, w.k, *w.router[1:4])
             O.forward_routed(xb[:S], idx, wts, wgub, wdb)
         else:
@@ -412,13 +462,15 @@ def pick_sample(run, T: int, budget_s: float) -> int:
     return S
 
 
-def cpu_baseline(w, logits, x, wgu, wd, budget_s: float, seed: int = 0):
-    O, run = oracle_sample_runner(w, logits, x, wgu, wd, seed)
+def cpu_baseline(w, logits, x, wgu, wd, budget_s: float, seed: int = 0, fp8: bool = False):
+    O, run = oracle_sample_runner(w, logits, x, wgu, wd, seed, fp8)
     S = pick_sample(run, w.T, budget_s)
     dt = run(S)
+    what = ("FP8 oracle forward (route, permute, x/h quantisation, E4M3 gate+up/SwiGLU and down, combine; "
+            "weights quantised beforehand, untimed)" if fp8 else
+            "oracle forward (route, permute, gate+up/SwiGLU, down, combine)")
     return {"value": round(S / dt, 3), "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
-            "sample": f"oracle forward (route, permute, gate+up/SwiGLU, down, combine) on the first {S} of "
-                      f"{w.T} tokens of the same seeded batch, full weights, {dt:.1f} s"}
+            "sample": f"{what} on the first {S} of {w.T} tokens of the same seeded batch, full weights, {dt:.1f} s"}
 
 
 def run_reference(args, w: Workload, rank: int, world: int):
@@ -426,7 +478,8 @@ def run_reference(args, w: Workload, rank: int, world: int):
         return None
     logits, x, wgu, wd = make_inputs(w, seed=args.seed, weight_device="cuda" if torch.cuda.is_available() else "cpu")
     wgu, wd = wgu.cpu(), wd.cpu()
-    O, run = oracle_sample_runner(w, logits, x, wgu, wd, args.seed)
+    fp8 = args.dtype == "e4m3"
+    O, run = oracle_sample_runner(w, logits, x, wgu, wd, args.seed, fp8)
     n = args.steps + args.warmup
     per_step = max(0.5, min(20.0, 150.0 / max(1, n)))
     S = pick_sample(run, w.T, per_step)
@@ -435,8 +488,8 @@ def run_reference(args, w: Workload, rank: int, world: int):
     times = [run(S) for _ in range(args.steps)]
     ms = 1e3 * statistics.mean(times)
     value = S / (ms * 1e-3)
-    sample = (f"each step: oracle forward on the first {S} of {w.T} tokens of the seeded batch, full weights, "
-              f"{O.num_threads()} host threads")
+    sample = (f"each step: {'FP8 ' if fp8 else ''}oracle forward on the first {S} of {w.T} tokens of the seeded "
+              f"batch, full weights, {O.num_threads()} host threads")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
@@ -451,6 +504,8 @@ def run_reference(args, w: Workload, rank: int, world: int):
 def config_of(w: Workload, args) -> dict:
     return {"workload": w.name, "T": w.T, "d_model": w.d, "d_ff": w.f, "experts": w.E, "top_k": w.k,
             "logit_bias": list(w.bias), "router": list(w.router), "seed": args.seed, "parallelism": "replicas",
+            "gemm_operands": ("e4m3, per-row activation and per-output-channel weight scales" if args.dtype == "e4m3"
+                              else "bf16"),
             "l2": ("flushed between steps (512 MB write, outside the step events)" if args.flush_l2 else
                    "not flushed: inputs larger than L2 (the active experts' weights, >= 2.8 GB, stream "
                    "from HBM every step; L2 is 129 MB)")}
@@ -467,6 +522,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0, help="oracle CPU-baseline sample size, seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3"],
+                    help="operands of the grouped GEMMs: bf16 (moe_forward) or e4m3 (moe_forward_fp8)")
     ap.add_argument("--flush-l2", action="store_true",
                     help="write a 512 MB buffer between steps (default: rely on inputs larger than L2)")
     args = ap.parse_args()
@@ -497,7 +554,7 @@ def main():
         line = {
             "metric": METRIC, "value": round(tok_s, 2), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"], 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
             "data": "synthetic (seeded)", "config": config_of(w, args),
             "tflops": round(tflops, 2),
             "layer_roofline": {"ms": round(r["layer_roof_ms"], 4), "frac": round(r["layer_roof_ms"] / r["ms"], 4),
@@ -517,7 +574,8 @@ def main():
         if world == 1 and not args.no_cpu_baseline:
             logits, x = r["inputs"]
             wgu, wd = (t.cpu() for t in r["host_weights"])
-            line["cpu_baseline"] = cpu_baseline(w, logits, x, wgu, wd, args.cpu_budget_s, args.seed)
+            line["cpu_baseline"] = cpu_baseline(w, logits, x, wgu, wd, args.cpu_budget_s, args.seed,
+                                                args.dtype == "e4m3")
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

@@ -58,7 +58,7 @@ extern "C" {
 #define MOE_STATUS_BAD_OFFSETS 0x2   /* grouped GEMM: offsets not 0 <= ... nondecreasing <= M */
 #define MOE_STATUS_BAD_DEST 0x4      /* combine: a dest row outside [0, T*top_k) */
 #define MOE_STATUS_WAIT_TIMEOUT 0x8  /* grouped GEMM: a pipeline wait gave up after ~1 s */
-#define MOE_STATUS_BAD_SRC 0x10      /* gathering gate+up GEMM: a src index outside [0, T) (row zeroed) */
+#define MOE_STATUS_BAD_SRC 0x10      /* gathering gate+up GEMM or FP8 row quantiser: a src index out of range (row zeroed) */
 
 typedef void* moe_stream_t; /* a cudaStream_t */
 
@@ -111,7 +111,8 @@ MOE_API int moe_route_grouped(const float* logits, const float* bias, int T, int
  *   counts [E] int32 out (assignments per expert);  offsets [E+1] int32 out (exclusive scan;
  *   expert e owns rows offsets[e] .. offsets[e+1]-1);  src [T*top_k] int32 out (row -> token);
  *   dest [T,top_k] int32 out ((token, slot) -> row);  x_perm [T*top_k, d] bf16 out (x_perm[r] =
- *   x[src[r]]);  status: device int32 or NULL, gets MOE_STATUS_BAD_EXPERT_ID.
+ *   x[src[r]]), or NULL to compute the indices only (for a consumer that gathers or quantises the
+ *   rows by src itself);  status: device int32 or NULL, gets MOE_STATUS_BAD_EXPERT_ID.
  * DeepGEMM PR #304 write-up, section 3.1 (m-grouped contiguous layout: activations contiguous by
  * token, grouped per expert); HPC-Ops page, FusedMoE paragraph (the preceding rearrangement). */
 MOE_API int moe_permute(const int32_t* idx, const void* x, int T, int d, int E, int top_k,
@@ -248,6 +249,65 @@ MOE_API int moe_forward_host(const void* x_host, const float* logits_host, const
 MOE_API int moe_forward_noalloc(const void* x, const float* logits, const void* w_gate_up,
                                 const void* w_down, int T, int d, int f, int E, int top_k,
                                 void* out, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * FP8 (E4M3) variant of the layer.  The grouped GEMMs run on 8-bit E4M3 codes (the OCP FP8
+ * format: bias 7, 3 mantissa bits, largest finite 448) on the tensor cores (tcgen05 kind::f8f6f4,
+ * fp32 accumulation).  Quantisation: absmax over a row (activations: each x_perm row and each h
+ * row) or over an output column's K values (weights), inv = 448 / absmax, code = E4M3(v * inv)
+ * rounded to nearest even, saturating at 448; dequantisation scale = absmax / 448 (an all-zero
+ * row or column: scale 1, zero codes).  The scales factor out of each dot product, so
+ *   g[n] = (sum_i x8[r][i] * W8[e][n][i]) * (sx[r] * s_gate_up[e][n])   (likewise u, y),
+ * applied in the GEMM epilogue.  DeepGEMM PR #304 write-up, section 5.3 (an FP8 grouped GEMM on
+ * SM100) and its Mega MoE figure (SwiGLU then FP8 quantisation inside the fused layer) are the
+ * pages' FP8 context; they scale 128-wide blocks, this variant scales whole rows and columns (its
+ * scales then need no per-block promotion of the accumulator).  d and f must be multiples of 128.
+ * ------------------------------------------------------------------------------------------- */
+
+/* Weights, once per model: W [E,K,N] bf16 (as w_gate_up [E,d,2f] or w_down [E,f,d]) -> Wq [E,N,K]
+ * E4M3 codes (transposed: K contiguous) and scale [E,N] fp32, one per output column.
+ * Requires 1 <= E <= 256, K a multiple of 128 and N of 64, both <= 65536. */
+MOE_API int moe_quantize_weights_fp8(const void* W, int E, int K, int N, void* Wq, float* scale,
+                                     moe_stream_t stream);
+
+/* Rows: q[r] = E4M3 codes of row src[r] of a (row r when src is NULL), scale[r] its scale.
+ *   a [src_rows, C] bf16 in (16-byte aligned), C a multiple of 8;  src [R] int32 in or NULL (then
+ *   src_rows >= R);  q [R, C] codes out (8-byte aligned);  scale [R] fp32 out;
+ *   status: device int32 or NULL (a src value outside [0, src_rows) quantises a zero row and sets
+ *   MOE_STATUS_BAD_SRC).
+ * moe_forward_fp8 uses it with src from the permutation (x8_perm[r] = quantised x[src[r]]) and on h. */
+MOE_API int moe_quantize_rows_fp8(const void* a, const int32_t* src, int R, int C, int src_rows, void* q,
+                                  float* scale, int32_t* status, moe_stream_t stream);
+
+/* Step 3 on E4M3 operands: h[r] = bf16(silu(g) * u) with g, u as above.
+ *   x8_perm [M,d] codes, sx [M] fp32;  w8_gate_up [E,2f,d] codes (gate rows 0..f-1, up rows
+ *   f..2f-1 of each expert), s_gate_up [E,2f] fp32 (moe_quantize_weights_fp8 of w_gate_up);
+ *   offsets [E+1];  h [M,f] bf16 out;  status as for step 3. */
+MOE_API int moe_grouped_gemm_gateup_swiglu_fp8(const void* x8_perm, const float* sx, const void* w8_gate_up,
+                                               const float* s_gate_up, const int32_t* offsets, int M, int d,
+                                               int f, int E, void* h, int32_t* status, moe_stream_t stream);
+
+/* Step 4 on E4M3 operands: y_perm[r][m] = (sum_n h8[r][n] * W8[e][m][n]) * (sh[r] * s_down[e][m]).
+ *   h8 [M,f] codes, sh [M] fp32;  w8_down [E,d,f] codes, s_down [E,d] fp32;  ksplit in [1, 8]
+ *   (K slices of 128-wide blocks, as in moe_grouped_gemm_down);  y_perm [ksplit,M,d] fp32 out. */
+MOE_API int moe_grouped_gemm_down_fp8(const void* h8, const float* sh, const void* w8_down, const float* s_down,
+                                      const int32_t* offsets, int M, int d, int f, int E, int ksplit,
+                                      float* y_perm, int32_t* status, moe_stream_t stream);
+
+/* The FP8 layer in one call: route (+ permute), quantise x rows by src, FP8 gate+up GEMM
+ * (+ SwiGLU), quantise h rows, FP8 down GEMM, combine — 6 launches (7 when routing and the
+ * permutation run apart, see moe_forward_launch_count).  Inputs as for moe_forward, with the
+ * weights given as moe_quantize_weights_fp8 codes and scales; workspace >=
+ * moe_workspace_size_fp8() bytes, 256-byte aligned, its pieces at moe_workspace_layout_fp8()'s
+ * offsets: status, idx, w, counts, offsets, src, dest, x8 [M,d], sx [M], h [M,f] bf16, h8 [M,f],
+ * sh [M], y_perm [moe_down_ksplit_fp8(), M, d], total (14 values). */
+MOE_API size_t moe_workspace_size_fp8(int T, int d, int f, int E, int top_k);
+MOE_API int moe_workspace_layout_fp8(int T, int d, int f, int E, int top_k, size_t* offsets_out);
+MOE_API int moe_down_ksplit_fp8(int T, int d, int f, int E, int top_k);
+MOE_API int moe_forward_fp8_launch_count(int T, int E, int top_k);
+MOE_API int moe_forward_fp8(const void* x, const float* logits, const void* w8_gate_up, const float* s_gate_up,
+                            const void* w8_down, const float* s_down, int T, int d, int f, int E, int top_k,
+                            void* out, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /* Reads (synchronously: cudaMemcpy) a device status word — a stage call's `status` pointer, or
  * the workspace of moe_forward — into *code (0 = no device-side error). */

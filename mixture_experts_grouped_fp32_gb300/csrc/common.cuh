@@ -30,7 +30,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Kernels of the layer, as bits of the programmatic-launch mask.
-enum PdlKernel { kPdlRoute = 1, kPdlPermute = 2, kPdlGateUp = 4, kPdlDown = 8, kPdlCombine = 16 };
+enum PdlKernel { kPdlRoute = 1, kPdlPermute = 2, kPdlGateUp = 4, kPdlDown = 8, kPdlCombine = 16, kPdlQuant = 32 };
 
 // Whether a kernel is launched with the programmatic-stream-serialization attribute (see
 // pdl_wait).  The environment variable MOE_PDL, a bit mask of PdlKernel, overrides the default.
@@ -93,6 +93,11 @@ struct GemmArgs {
     // x[gather_src[r]] (gathered by the kernel); x_perm is never materialised.
     const int32_t* gather_src = nullptr;
     int gather_T = 0;
+    // FP8 variant (1-SM kernel): A is [M, K] E4M3 codes with a_scale [M] (one per row), B is
+    // [E, N_total, K] E4M3 codes (transposed) with b_scale [E, N_total]; K % 128 == 0.
+    bool fp8 = false;
+    const float* a_scale = nullptr;
+    const float* b_scale = nullptr;
 };
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                 const char** why);
@@ -103,5 +108,15 @@ cudaError_t launch_grouped_gemm_pair(int kind, const GemmArgs& a, int num_sms, c
 // swizzle; false if the driver's encoder is unavailable or rejects the operand.
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
                           uint32_t box_rows);
+// The same over bytes (FP8 codes): box = [box_rows, 128 cols].
+bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows);
+
+// FP8 quantisation (fp8.cu).  Rows: row r of the bf16 [*, C] matrix a (row src[r] when src is
+// given, src values checked against src_rows) -> E4M3 codes q [R, C] and scale [R].  Weights:
+// W [E, K, N] bf16 -> Wq [E, N, K] codes (transposed) and scale [E, N], one per output column.
+cudaError_t launch_quantize_rows_fp8(const __nv_bfloat16* a, const int32_t* src, int R, int C, int src_rows,
+                                     uint8_t* q, float* scale, int32_t* status, cudaStream_t s);
+cudaError_t launch_quantize_weights_fp8(const __nv_bfloat16* W, int E, int K, int N, uint8_t* Wq, float* scale,
+                                        cudaStream_t s);
 
 }  // namespace moe

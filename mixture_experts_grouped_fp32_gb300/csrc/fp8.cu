@@ -1,0 +1,146 @@
+// fp8.cu — FP8 (E4M3) quantisation for the FP8 variant of the layer's grouped GEMMs.
+//
+// Scaling: per row for activations (each x_perm row, each h row), per output channel for the
+// weights (expert e, output column n, over K): absmax over the row / channel, inv = 448 / absmax,
+// code = E4M3(value * inv) rounded to nearest even with saturation, dequantisation scale =
+// absmax / 448 (an all-zero row: scale 1, zero codes).  These scales factor out of every dot
+// product, so the FP8 GEMMs accumulate decoded codes in fp32 and apply scale_row * scale_col in
+// their epilogue.  DeepGEMM PR #304 write-up, section 5.3 (an FP8 grouped GEMM on SM100) and its
+// Mega MoE epilogue (SwiGLU then FP8 quantisation) are the pages' FP8 context; their 128-wide
+// blockwise scales are not used here (they need per-K-block promotion of the accumulator).
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kQThreads = 256;
+
+__device__ __forceinline__ uint8_t to_e4m3(float v) {
+    return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Block-wide max of non-negative floats (every thread gets the result).
+__device__ __forceinline__ float block_max(float v, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();  // red may still be read from a previous call
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float m = 0.0f;
+    for (int i = 0; i < kQThreads / 32; ++i) m = fmaxf(m, red[i]);
+    return m;
+}
+
+// One block per output row r: source row src[r] (or r when src is null) of a bf16 matrix with C
+// columns (C % 8 == 0) -> codes [r, C] and scale[r].
+__global__ void __launch_bounds__(kQThreads)
+quantize_rows_kernel(const uint4* __restrict__ a, const int32_t* __restrict__ src, int R, int C, int src_rows,
+                     uint2* __restrict__ q, float* __restrict__ scale, int32_t* __restrict__ status) {
+    __shared__ float red[kQThreads / 32];
+    pdl_wait();
+    pdl_trigger();
+    const int r = blockIdx.x;
+    if (r >= R) return;
+    int s = src ? __ldg(src + r) : r;
+    if (s < 0 || s >= src_rows) {  // bad src: a zero row, reported
+        flag_status(status, MOE_STATUS_BAD_SRC);
+        s = -1;
+    }
+    const int cv = C / 8;  // uint4 (8 bf16) per row
+    const uint4* row = a + static_cast<size_t>(s < 0 ? 0 : s) * cv;
+    float m = 0.0f;
+    if (s >= 0)
+        for (int v = threadIdx.x; v < cv; v += kQThreads) {
+            const uint4 p = __ldg(row + v);
+            const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+        }
+    const float amax = block_max(m, red);
+    const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
+    if (threadIdx.x == 0) scale[r] = amax > 0.0f ? amax / 448.0f : 1.0f;
+    uint2* out = q + static_cast<size_t>(r) * cv;
+    for (int v = threadIdx.x; v < cv; v += kQThreads) {
+        uint4 p = make_uint4(0, 0, 0, 0);
+        if (s >= 0) p = __ldg(row + v);
+        const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+        uint32_t o[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t c0 = to_e4m3(bf16_lo(w[i]) * inv), c1 = to_e4m3(bf16_hi(w[i]) * inv);
+            o[i >> 1] |= (c0 | (c1 << 8)) << (16 * (i & 1));
+        }
+        out[v] = make_uint2(o[0], o[1]);
+    }
+}
+
+// Weights W [E, K, N] bf16 -> Wq [E, N, K] codes and scale [E, N]; block (e, 64-column group).
+// Pass 1: per-column absmax over K.  Pass 2: 64 x 64 tiles transposed through shared memory, so
+// reads (64 columns of a K-row) and writes (64 K-bytes of an output row) are both contiguous.
+constexpr int kWCols = 64;
+__global__ void __launch_bounds__(kQThreads)
+quantize_weights_kernel(const uint16_t* __restrict__ W, int K, int N, uint8_t* __restrict__ Wq,
+                        float* __restrict__ scale) {
+    __shared__ float cmax[kQThreads / kWCols][kWCols];
+    __shared__ float inv[kWCols];
+    __shared__ uint8_t tile[kWCols][kWCols + 4];
+    const int e = blockIdx.y, n0 = blockIdx.x * kWCols;
+    const int c = threadIdx.x % kWCols, rr = threadIdx.x / kWCols;  // 4 row phases x 64 columns
+    const uint16_t* We = W + static_cast<size_t>(e) * K * N;
+    const bool col_ok = n0 + c < N;
+    float m = 0.0f;
+    if (col_ok)
+        for (int k = rr; k < K; k += kQThreads / kWCols)
+            m = fmaxf(m, fabsf(__uint_as_float(static_cast<uint32_t>(__ldg(We + static_cast<size_t>(k) * N + n0 + c)) << 16)));
+    cmax[rr][c] = m;
+    __syncthreads();
+    if (threadIdx.x < kWCols) {
+        float a = 0.0f;
+        for (int i = 0; i < kQThreads / kWCols; ++i) a = fmaxf(a, cmax[i][threadIdx.x]);
+        inv[threadIdx.x] = a > 0.0f ? 448.0f / a : 1.0f;
+        if (n0 + static_cast<int>(threadIdx.x) < N)
+            scale[static_cast<size_t>(e) * N + n0 + threadIdx.x] = a > 0.0f ? a / 448.0f : 1.0f;
+    }
+    __syncthreads();
+    uint8_t* Wqe = Wq + static_cast<size_t>(e) * N * K;
+    for (int k0 = 0; k0 < K; k0 += kWCols) {
+        for (int i = threadIdx.x; i < kWCols * kWCols; i += kQThreads) {
+            const int kk = i / kWCols, cc = i % kWCols;  // read: row k0+kk, column n0+cc
+            uint8_t code = 0;
+            if (k0 + kk < K && n0 + cc < N)
+                code = to_e4m3(__uint_as_float(static_cast<uint32_t>(__ldg(We + static_cast<size_t>(k0 + kk) * N + n0 + cc)) << 16) * inv[cc]);
+            tile[cc][kk] = code;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < kWCols * kWCols; i += kQThreads) {
+            const int cc = i / kWCols, kk = i % kWCols;  // write: output row n0+cc, K-byte k0+kk
+            if (k0 + kk < K && n0 + cc < N) Wqe[static_cast<size_t>(n0 + cc) * K + k0 + kk] = tile[cc][kk];
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_rows_fp8(const __nv_bfloat16* a, const int32_t* src, int R, int C, int src_rows,
+                                     uint8_t* q, float* scale, int32_t* status, cudaStream_t s) {
+    if (R == 0) return cudaSuccess;
+    return launch_k(kPdlQuant, quantize_rows_kernel, dim3(R), dim3(kQThreads), 0, s,
+                    reinterpret_cast<const uint4*>(a), src, R, C, src_rows, reinterpret_cast<uint2*>(q), scale,
+                    status);
+}
+
+cudaError_t launch_quantize_weights_fp8(const __nv_bfloat16* W, int E, int K, int N, uint8_t* Wq, float* scale,
+                                        cudaStream_t s) {
+    const dim3 grid((N + kWCols - 1) / kWCols, E);
+    quantize_weights_kernel<<<grid, kQThreads, 0, s>>>(reinterpret_cast<const uint16_t*>(W), K, N, Wq, scale);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -43,6 +43,14 @@
 //   swap mode: two M=128 x N=rows16 MMAs per K step, weight boxes 0-1 and 2-3 as A, into
 //     accumulator columns [0, N) and [128, 128+N) (kind 0: gate and up; kind 1: output columns
 //     n0..n0+127 and n0+128..n0+255).
+//
+// FP8 variant (E4M3 codes, kind::f8f6f4 MMAs with K = 32): the activations are [M, K] codes with a
+// scale per row, the weights are stored transposed, [E, N_total, K] codes (K contiguous) with a
+// scale per output column, so both operands are K-major and one 128-byte swizzle row holds 128 K
+// values: a stage is 128 K deep.  Its weight part is two 128-row boxes (kind 0: gate rows n0.. and
+// up rows f+n0..; kind 1: rows n0.. and n0+128..), 16 KB each, and the accumulator columns keep the
+// BF16 kernel's meaning.  The scales factor out of the K sum, so the epilogue multiplies each
+// accumulator by scale_row * scale_col before SwiGLU (kind 0) or the store (kind 1).
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -143,14 +151,18 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
 // 128-byte-swizzled positions TMA would have written; rows past the expert's end are zero-filled.
 // Each stage's `full` barrier then expects two arrivals: the TMA weight bytes' and its gather
 // warp's.  x_perm then never exists in global memory.
-template <int KIND, bool GATHER>
+template <int KIND, bool GATHER, bool FP8>
 __global__ void __launch_bounds__(GATHER ? GATHER_THREADS : NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
                     const __grid_constant__ CUtensorMap tmB, const int32_t* __restrict__ offsets, int M,
                     int K, int N, int E, int ksplit, int swap_max, int inject_stall,
-                    const int4* __restrict__ xg, const int32_t* __restrict__ gsrc, int gT, void* __restrict__ out,
+                    const int4* __restrict__ xg, const int32_t* __restrict__ gsrc, int gT,
+                    const float* __restrict__ a_scale, const float* __restrict__ b_scale, void* __restrict__ out,
                     int32_t* __restrict__ status) {
+    static_assert(!(GATHER && FP8), "the FP8 variant reads its activation codes with TMA");
     constexpr int BN_OUT = KIND == 0 ? 128 : 256;
+    constexpr int BKE = FP8 ? 128 : BK;  // K values per stage (one 128-byte swizzle row)
+    constexpr int W8_BOX_BYTES = 128 * 128;  // FP8 weight box: 128 rows x 128 K codes
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     uint8_t* tiles = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -159,7 +171,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_tiles = (N + BN_OUT - 1) / BN_OUT;
-    const int num_kb = K / BK;
+    const int num_kb = K / BKE;
     const int kb_per = (num_kb + ksplit - 1) / ksplit;  // K blocks per slice (host: no empty slice)
 
     if (tid == 0) {
@@ -259,19 +271,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (!GATHER) {
                     if (it.swap) {
                         for (int q = 0; q < nbox32; ++q)
-                            ptx::tma_load_2d(sa + q * A_BOX32_BYTES, &tmA32, &c.full[stage], kb * BK,
+                            ptx::tma_load_2d(sa + q * A_BOX32_BYTES, &tmA32, &c.full[stage], kb * BKE,
                                              it.row0 + q * A_BOX32_ROWS, pol_act);
                     } else {
-                        ptx::tma_load_2d(sa, &tmA, &c.full[stage], kb * BK, it.row0, pol_act);
+                        ptx::tma_load_2d(sa, &tmA, &c.full[stage], kb * BKE, it.row0, pol_act);
                     }
                 }
+                if (FP8) {
+                    // Weight rows (output columns) of expert e: [e * 2N, e * 2N + 2N) for gate+up
+                    // (gate then up), [e * N, e * N + N) for down.
+                    const int wrow0 = KIND == 0 ? it.e * 2 * N + n0 : it.e * N + n0;
+                    const int wrow1 = KIND == 0 ? wrow0 + N : wrow0 + 128;
+                    ptx::tma_load_2d(sb, &tmB, &c.full[stage], kb * BKE, wrow0, pol_wgt);
+                    ptx::tma_load_2d(sb + W8_BOX_BYTES, &tmB, &c.full[stage], kb * BKE, wrow1, pol_wgt);
+                } else {
 #pragma unroll
-                for (int q = 0; q < B_BOXES; ++q) {
-                    int col;
-                    if (KIND == 0) col = (q < 2) ? n0 + q * B_BOX_N : N + n0 + (q - 2) * B_BOX_N;
-                    else col = n0 + q * B_BOX_N;
-                    ptx::tma_load_2d(sb + q * B_BOX_BYTES, &tmB, &c.full[stage], col, brow + kb * BK,
-                                     pol_wgt);
+                    for (int q = 0; q < B_BOXES; ++q) {
+                        int col;
+                        if (KIND == 0) col = (q < 2) ? n0 + q * B_BOX_N : N + n0 + (q - 2) * B_BOX_N;
+                        else col = n0 + q * B_BOX_N;
+                        ptx::tma_load_2d(sb + q * B_BOX_BYTES, &tmB, &c.full[stage], col, brow + kb * BK,
+                                         pol_wgt);
+                    }
                 }
                 fill_parity[stage] = phase;
                 filled_mask |= 1 << stage;
@@ -372,6 +393,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 // Activations: K-major, +32 B per 16 K.  Weights: MN-major (atoms 8 KB apart along
                 // N/M, 8-row K groups 1 KB apart), +16 rows * 128 B = 2 KB per 16 K.
                 const uint64_t act_desc = ptx::smem_desc_sw128(sa, 16, 1024);
+                if (FP8) {
+                    // Both operands K-major: +32 B (32 codes) per MMA; 8-row groups 1 KB apart.
+                    const uint64_t w8_desc = ptx::smem_desc_sw128(sa + A_BYTES, 16, 1024);
+                    const uint64_t w8_hi_desc = ptx::smem_desc_sw128(sa + A_BYTES + W8_BOX_BYTES, 16, 1024);
+                    constexpr uint32_t idesc8_normal = ptx::idesc_e4m3_f32(BM, UMMA_N, 0, 0);
+                    const uint32_t idesc8_swap = ptx::idesc_e4m3_f32(BM, ntok, 0, 0);
+#pragma unroll
+                    for (int kk = 0; kk < BKE / 32; ++kk) {
+                        const uint32_t accum = (kb != kb0 || kk != 0) ? 1u : 0u;
+                        const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+                        if (it.swap) {
+                            ptx::mma_f8_ss(d_tmem, w8_desc + off, act_desc + off, idesc8_swap, accum);
+                            ptx::mma_f8_ss(d_tmem + 128, w8_hi_desc + off, act_desc + off, idesc8_swap, accum);
+                        } else {
+                            ptx::mma_f8_ss(d_tmem, act_desc + off, w8_desc + off, idesc8_normal, accum);
+                        }
+                    }
+                    ptx::mma_commit(&c.empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    continue;
+                }
                 const uint64_t wgt_desc = ptx::smem_desc_sw128(sa + A_BYTES, B_BOX_BYTES, 1024);
                 const uint64_t wgt_hi_desc = ptx::smem_desc_sw128(sa + A_BYTES + 2 * B_BOX_BYTES, B_BOX_BYTES, 1024);
 #pragma unroll
@@ -419,6 +464,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 // Accumulator lane = weight column (n0 + r_local [+128]), accumulator column = row.
                 const int nchunk = (it.rows + 31) / 32;
                 const int col0 = n0 + r_local;
+                // FP8: column scales of this lane's two weight columns (gate/up, or col0/col0+128).
+                float sc0 = 1.0f, sc1 = 1.0f;
+                if (FP8) {
+                    const float* sbe = b_scale + static_cast<size_t>(it.e) * (KIND == 0 ? 2 * N : N);
+                    if (col0 < N) sc0 = __ldg(sbe + col0);
+                    if (KIND == 0 ? col0 < N : col0 + 128 < N) sc1 = __ldg(sbe + col0 + (KIND == 0 ? N : 128));
+                }
 #pragma unroll 1
                 for (int cc = 0; cc < nchunk; ++cc) {
                     uint32_t a0[32], a1[32];
@@ -427,6 +479,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     ptx::tmem_ld_wait();
                     const int nrow = min(32, it.rows - cc * 32);
                     const size_t row_base = static_cast<size_t>(it.row0 + cc * 32);
+                    if (FP8) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nrow) {
+                                const float sr = __ldg(a_scale + row_base + j);  // same row in every lane
+                                a0[j] = __float_as_uint(__uint_as_float(a0[j]) * (sr * sc0));
+                                a1[j] = __float_as_uint(__uint_as_float(a1[j]) * (sr * sc1));
+                            }
+                    }
                     if (KIND == 0) {
                         uint16_t* h = reinterpret_cast<uint16_t*>(out);
                         if (col0 < N) {
@@ -450,6 +511,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 // Accumulator lane = row (row0 + r_local), accumulator column = output column.
                 const bool row_ok = r_local < it.rows;
                 const size_t grow = static_cast<size_t>(it.row0 + r_local);
+                // FP8: this lane's row scale and the expert's column scales.
+                const float srow = (FP8 && row_ok) ? __ldg(a_scale + grow) : 1.0f;
+                const float* sbe = FP8 ? b_scale + static_cast<size_t>(it.e) * (KIND == 0 ? 2 * N : N) : nullptr;
                 if (KIND == 0) {
                     __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(out);
 #pragma unroll 1
@@ -459,6 +523,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         ptx::tmem_ld_32x32b_x32(taddr + 128 + cc * 32, u);
                         ptx::tmem_ld_wait();
                         const int col = n0 + cc * 32;
+                        if (FP8 && row_ok && col < N) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {  // the column scales are the same in every lane
+                                g[j] = __float_as_uint(__uint_as_float(g[j]) * (srow * __ldg(sbe + col + j)));
+                                u[j] = __float_as_uint(__uint_as_float(u[j]) * (srow * __ldg(sbe + N + col + j)));
+                            }
+                        }
                         if (row_ok && col < N) {
                             uint4* dst = reinterpret_cast<uint4*>(h + grow * N + col);
 #pragma unroll
@@ -482,6 +553,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         ptx::tmem_ld_32x32b_x32(taddr + cc * 32, v32);
                         ptx::tmem_ld_wait();
                         const int col = n0 + cc * 32;
+                        if (FP8 && row_ok && col < N) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                v32[j] = __float_as_uint(__uint_as_float(v32[j]) * (srow * __ldg(sbe + col + j)));
+                        }
                         if (row_ok && col < N) {
                             float4* dst = reinterpret_cast<float4*>(y + grow * N + col);
 #pragma unroll
@@ -526,13 +602,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 // ---------------------------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // ---------------------------------------------------------------------------------------------
-template <int KIND, bool GATHER>
+template <int KIND, bool GATHER, bool FP8>
 cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const char** why) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<KIND, GATHER>,
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<KIND, GATHER, FP8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) {
             *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
@@ -544,16 +620,23 @@ cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const ch
     const uint64_t bcols = KIND == 0 ? 2ull * a.N : static_cast<uint64_t>(a.N);
     // With GATHER, A is x [gather_T, K] (the maps over it are then unused).
     const uint64_t arows = GATHER ? static_cast<uint64_t>(a.gather_T) : static_cast<uint64_t>(a.M);
-    if (!make_tensor_map_bf16(&mA, a.A, a.K, arows, BM) || !make_tensor_map_bf16(&mA32, a.A, a.K, arows, A_BOX32_ROWS) ||
-        !make_tensor_map_bf16(&mB, a.B, bcols, static_cast<uint64_t>(a.E) * a.K, BK)) {
+    // FP8: activation codes [M, K] and transposed weight codes [E * N_total, K], K contiguous.
+    const bool maps_ok =
+        FP8 ? make_tensor_map_u8(&mA, a.A, a.K, arows, BM) && make_tensor_map_u8(&mA32, a.A, a.K, arows, A_BOX32_ROWS) &&
+                  make_tensor_map_u8(&mB, a.B, a.K, static_cast<uint64_t>(a.E) * bcols, 128)
+            : make_tensor_map_bf16(&mA, a.A, a.K, arows, BM) &&
+                  make_tensor_map_bf16(&mA32, a.A, a.K, arows, A_BOX32_ROWS) &&
+                  make_tensor_map_bf16(&mB, a.B, bcols, static_cast<uint64_t>(a.E) * a.K, BK);
+    if (!maps_ok) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or bad operand)";
         return cudaErrorInvalidValue;
     }
     const int swap_max = a.swap_max < 0 ? 0 : (a.swap_max > SWAP_MAX_ROWS ? SWAP_MAX_ROWS : a.swap_max);
     const int ksplit = KIND == 0 ? 1 : a.ksplit;
-    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_kernel<KIND, GATHER>, dim3(num_sms),
-                    dim3(GATHER ? GATHER_THREADS : NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB, a.offsets, a.M, a.K, a.N, a.E, ksplit, swap_max,
-                    a.inject_stall, reinterpret_cast<const int4*>(a.A), a.gather_src, a.gather_T, a.out, a.status);
+    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_kernel<KIND, GATHER, FP8>, dim3(num_sms),
+                    dim3(GATHER ? GATHER_THREADS : NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB, a.offsets, a.M, a.K,
+                    a.N, a.E, ksplit, swap_max, a.inject_stall, reinterpret_cast<const int4*>(a.A), a.gather_src,
+                    a.gather_T, a.a_scale, a.b_scale, a.out, a.status);
 }
 
 }  // namespace
@@ -586,16 +669,37 @@ bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint6
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte tensor [rows, cols] (FP8 codes, cols contiguous), box = [box_rows, 128 cols], 128-byte swizzle.
+bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                 const char** why) {
     if (a.ksplit < 1 || a.ksplit > kMaxKSplit || (kind == 0 && a.ksplit != 1)) {
         *why = "ksplit must be 1 for gate+up and in [1, 8] for down";
         return cudaErrorInvalidValue;
     }
+    if (a.fp8) {
+        if (a.K % 128 != 0 || a.gather_src || !a.a_scale || !a.b_scale) {
+            *why = "FP8 grouped GEMM: K must be a multiple of 128, scales given, no row gather";
+            return cudaErrorInvalidValue;
+        }
+        return kind == 0 ? launch_kind<0, false, true>(a, num_sms, s, why) : launch_kind<1, false, true>(a, num_sms, s, why);
+    }
     if (a.pair && num_sms >= 2 && !a.inject_stall) return launch_grouped_gemm_pair(kind, a, num_sms, s, why);
     if (kind == 0)
-        return a.gather_src ? launch_kind<0, true>(a, num_sms, s, why) : launch_kind<0, false>(a, num_sms, s, why);
-    return launch_kind<1, false>(a, num_sms, s, why);
+        return a.gather_src ? launch_kind<0, true, false>(a, num_sms, s, why)
+                            : launch_kind<0, false, false>(a, num_sms, s, why);
+    return launch_kind<1, false, false>(a, num_sms, s, why);
 }
 
 }  // namespace moe

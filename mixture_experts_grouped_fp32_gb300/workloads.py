@@ -153,3 +153,18 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
 def bits_to_bf16(bits: np.ndarray) -> torch.Tensor:
     """numpy uint16 bit patterns -> bf16 CPU tensor."""
     return torch.from_numpy(np.ascontiguousarray(bits, np.uint16).view(np.int16)).view(torch.bfloat16)
+
+
+def draw_e4m3_codes(shape, seed: int) -> np.ndarray:
+    """Uniformly random 8-bit E4M3 codes of the given shape, NaN codes (0x7F, 0xFF) excluded: raw
+    operands for the FP8 GEMM stages (no quantisation involved)."""
+    rng = np.random.default_rng(seed)
+    c = rng.integers(0, 254, size=shape, dtype=np.uint16)  # 254 values: skip 0x7F and 0xFF
+    c = c + (c >= 0x7F)
+    return c.astype(np.uint8)
+
+
+def draw_scales(shape, seed: int, lo: float = 1e-3, hi: float = 1e-2) -> np.ndarray:
+    """Positive fp32 dequantisation scales, log-uniform in [lo, hi]."""
+    rng = np.random.default_rng(seed)
+    return np.exp(rng.uniform(np.log(lo), np.log(hi), size=shape)).astype(np.float32)

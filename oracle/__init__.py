@@ -67,6 +67,8 @@ _SIGS = {
     "oracle_e4m3_decode_array": ([_U8P, _INT, _F32P], None),
     "oracle_quantize_rows_fp8": ([_U16P, _INT, _INT, _U8P, _F32P], None),
     "oracle_quantize_weights_fp8": ([_U16P, _INT, _INT, _INT, _U8P, _F32P], None),
+    "oracle_gateup_swiglu_fp8": ([_U8P, _F32P, _I32P, _INT, _U8P, _F32P, _INT, _INT, _U16P], None),
+    "oracle_down_fp8": ([_U8P, _F32P, _I32P, _INT, _U8P, _F32P, _INT, _INT, _F32P], None),
     "oracle_forward_fp8_tokens_routed": ([_U16P, _I32P, _F32P, _U8P, _F32P, _U8P, _F32P, _INT, _INT, _INT, _INT,
                                           _INT, _I32P, _INT, _F32P], _INT),
 }
@@ -287,6 +289,31 @@ class Oracle:
         sc = np.empty((E, N), np.float32)
         self.L.oracle_quantize_weights_fp8(_p(w_bits, _U16P), E, K, N, _p(q, _U8P), _p(sc, _F32P))
         return q, sc
+
+    def gateup_swiglu_fp8(self, x8_perm, sx, offsets, wgu8, sgu):
+        """FP8 step 3: codes x8_perm [M, d] + sx [M], wgu8 [E, 2f, d] + sgu [E, 2f] -> h [M, f] bf16 bits
+        (rows past offsets[E] zero)."""
+        x8_perm, sx = _c(x8_perm, np.uint8), _c(sx, np.float32)
+        offsets = _c(offsets, np.int32)
+        wgu8, sgu = _c(wgu8, np.uint8), _c(sgu, np.float32)
+        E, f2, d = wgu8.shape
+        M = x8_perm.shape[0]
+        h = np.zeros((M, f2 // 2), np.uint16)
+        self.L.oracle_gateup_swiglu_fp8(_p(x8_perm, _U8P), _p(sx, _F32P), _p(offsets, _I32P), E, _p(wgu8, _U8P),
+                                        _p(sgu, _F32P), d, f2 // 2, _p(h, _U16P))
+        return h
+
+    def down_fp8(self, h8, sh, offsets, wd8, sd):
+        """FP8 step 4: codes h8 [M, f] + sh [M], wd8 [E, d, f] + sd [E, d] -> y [M, d] fp32."""
+        h8, sh = _c(h8, np.uint8), _c(sh, np.float32)
+        offsets = _c(offsets, np.int32)
+        wd8, sd = _c(wd8, np.uint8), _c(sd, np.float32)
+        E, d, f = wd8.shape
+        M = h8.shape[0]
+        y = np.zeros((M, d), np.float32)
+        self.L.oracle_down_fp8(_p(h8, _U8P), _p(sh, _F32P), _p(offsets, _I32P), E, _p(wd8, _U8P), _p(sd, _F32P), d,
+                               f, _p(y, _F32P))
+        return y
 
     def forward_fp8_tokens_routed(self, x_bits, idx_rows, w_rows, wgu8, sgu, wd8, sd, tokens):
         x_bits = _c(x_bits, np.uint16)

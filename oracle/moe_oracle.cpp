@@ -444,6 +444,37 @@ int oracle_forward_tokens(const uint16_t* x, const float* logits, const uint16_t
 //   out  = sum_j w_j * y   (slot order)
 // Weights are stored transposed, [E, N, K] (K contiguous).
 // ---------------------------------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+// One row r of the FP8 gate+up GEMM through expert e: decoded codes xd [d] with row scale sx;
+// for each of the 2f output columns n (gate n < f, then up), the K sum in ascending i, then the
+// product with (sx * se[n]); h = bf16(silu(g) * u).
+void gateup_row_fp8(const float* xd, float sx, const uint8_t* We8, const float* se, int d, int f, float* g,
+                    float* u, uint16_t* hb) {
+    for (int n = 0; n < 2 * f; ++n) {
+        const uint8_t* wrow = We8 + static_cast<size_t>(n) * d;
+        float acc = 0.0f;
+        for (int i = 0; i < d; ++i) acc += xd[i] * e4m3_decode(wrow[i]);
+        const float v = acc * (sx * se[n]);
+        if (n < f) g[n] = v; else u[n - f] = v;
+    }
+    for (int n = 0; n < f; ++n) hb[n] = f32_to_bf16_rne(silu(g[n]) * u[n]);
+}
+
+// One row of the FP8 down GEMM: decoded h codes hd [f] with row scale sh -> yr [d].
+void down_row_fp8(const float* hd, float sh, const uint8_t* Wde8, const float* sde, int d, int f, float* yr) {
+    for (int m = 0; m < d; ++m) {
+        const uint8_t* wrow = Wde8 + static_cast<size_t>(m) * f;
+        float acc = 0.0f;
+        for (int n = 0; n < f; ++n) acc += hd[n] * e4m3_decode(wrow[n]);
+        yr[m] = acc * (sh * sde[m]);
+    }
+}
+}  // namespace
+
+extern "C" {
+
 uint8_t oracle_e4m3_encode(float x) { return e4m3_encode(x); }
 float oracle_e4m3_decode(uint8_t c) { return e4m3_decode(c); }
 
@@ -463,6 +494,7 @@ void oracle_quantize_rows_fp8(const uint16_t* a, int R, int C, uint8_t* q, float
 // Weights W [E, K, N] bf16 -> Wq [E, N, K] codes (transposed) and scales [E, N]: output column n
 // of expert e is quantised over its K values like a row.
 void oracle_quantize_weights_fp8(const uint16_t* W, int E, int K, int N, uint8_t* Wq, float* scale) {
+#pragma omp parallel for schedule(dynamic, 1)
     for (int e = 0; e < E; ++e) {
         const uint16_t* We = W + static_cast<size_t>(e) * K * N;
         quantize_rows_fp8([&](int n, int k) { return bf16_to_f32(We[static_cast<size_t>(k) * N + n]); }, N, K,
@@ -495,27 +527,12 @@ int oracle_forward_fp8_tokens_routed(const uint16_t* x, const int32_t* idx_rows,
             const int e = idx_rows[q];
             oracle_quantize_rows_fp8(x + static_cast<size_t>(tokens[s]) * d, 1, d, x8.data(), &sx);
             for (int i = 0; i < d; ++i) xd[i] = e4m3_decode(x8[i]);
-            const uint8_t* We = Wgu8 + static_cast<size_t>(e) * 2 * f * d;
-            const float* se = sgu + static_cast<size_t>(e) * 2 * f;
-            for (int n = 0; n < 2 * f; ++n) {
-                const uint8_t* wrow = We + static_cast<size_t>(n) * d;
-                float acc = 0.0f;
-                for (int i = 0; i < d; ++i) acc += xd[i] * e4m3_decode(wrow[i]);
-                const float v = acc * (sx * se[n]);
-                if (n < f) g[n] = v; else u[n - f] = v;
-            }
-            for (int n = 0; n < f; ++n) hb[n] = f32_to_bf16_rne(silu(g[n]) * u[n]);
+            gateup_row_fp8(xd.data(), sx, Wgu8 + static_cast<size_t>(e) * 2 * f * d, sgu + static_cast<size_t>(e) * 2 * f,
+                           d, f, g.data(), u.data(), hb.data());
             oracle_quantize_rows_fp8(hb.data(), 1, f, h8.data(), &sh);
             for (int n = 0; n < f; ++n) hd[n] = e4m3_decode(h8[n]);
-            const uint8_t* Wde = Wd8 + static_cast<size_t>(e) * d * f;
-            const float* sde = sd + static_cast<size_t>(e) * d;
-            float* yr = ys.data() + q * d;
-            for (int m = 0; m < d; ++m) {
-                const uint8_t* wrow = Wde + static_cast<size_t>(m) * f;
-                float acc = 0.0f;
-                for (int n = 0; n < f; ++n) acc += hd[n] * e4m3_decode(wrow[n]);
-                yr[m] = acc * (sh * sde[m]);
-            }
+            down_row_fp8(hd.data(), sh, Wd8 + static_cast<size_t>(e) * d * f, sd + static_cast<size_t>(e) * d, d, f,
+                         ys.data() + q * d);
         }
     }
     for (int s = 0; s < ntok; ++s) {
@@ -528,6 +545,43 @@ int oracle_forward_fp8_tokens_routed(const uint16_t* x, const int32_t* idx_rows,
         }
     }
     return 0;
+}
+
+// Step 3 of the FP8 layer on its own, over rows 0..offsets[E]-1 of a grouped operand:
+// x8_perm [M, d] codes with sx [M], Wgu8 [E, 2f, d] with sgu [E, 2f] -> h [M, f] bf16.
+void oracle_gateup_swiglu_fp8(const uint8_t* x8_perm, const float* sx, const int32_t* offsets, int E,
+                              const uint8_t* Wgu8, const float* sgu, int d, int f, uint16_t* h) {
+    for (int e = 0; e < E; ++e) {
+#pragma omp parallel
+        {
+            std::vector<float> xd(d), g(f), u(f);
+#pragma omp for schedule(dynamic, 1)
+            for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
+                for (int i = 0; i < d; ++i) xd[i] = e4m3_decode(x8_perm[static_cast<size_t>(r) * d + i]);
+                gateup_row_fp8(xd.data(), sx[r], Wgu8 + static_cast<size_t>(e) * 2 * f * d,
+                               sgu + static_cast<size_t>(e) * 2 * f, d, f, g.data(), u.data(),
+                               h + static_cast<size_t>(r) * f);
+            }
+        }
+    }
+}
+
+// Step 4 of the FP8 layer on its own: h8 [M, f] codes with sh [M], Wd8 [E, d, f] with sd [E, d]
+// -> y [M, d] fp32.
+void oracle_down_fp8(const uint8_t* h8, const float* sh, const int32_t* offsets, int E, const uint8_t* Wd8,
+                     const float* sd, int d, int f, float* y) {
+    for (int e = 0; e < E; ++e) {
+#pragma omp parallel
+        {
+            std::vector<float> hd(f);
+#pragma omp for schedule(dynamic, 1)
+            for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
+                for (int n = 0; n < f; ++n) hd[n] = e4m3_decode(h8[static_cast<size_t>(r) * f + n]);
+                down_row_fp8(hd.data(), sh[r], Wd8 + static_cast<size_t>(e) * d * f, sd + static_cast<size_t>(e) * d,
+                             d, f, y + static_cast<size_t>(r) * d);
+            }
+        }
+    }
 }
 
 }  // extern "C"

@@ -513,7 +513,30 @@ def pin_fp8_forward(O, seed=47):
     assert err <= 2e-3 * np.abs(ref).max(), err
 
 
+def pin_fp8_stages(O, seed=53):
+    """The FP8 stage functions composed in the layer's order (permute, quantise x_perm rows,
+    gate+up, quantise h rows, down, combine) give the FP8 layer's output exactly (the same fp32
+    operations in the same order), on a layer where one expert receives no token."""
+    rng = np.random.default_rng(seed)
+    T, d, f, E, k = 11, 32, 48, 5, 2
+    logits, x_bits, wgu, wd = random_layer(rng, T, d, f, E)
+    logits[:, 3] = -30.0  # expert 3 never chosen: an empty segment
+    wgu8, sgu = O.quantize_weights_fp8(wgu)
+    wd8, sdn = O.quantize_weights_fp8(wd)
+    out = O.forward_fp8(x_bits, logits, wgu8, sgu, wd8, sdn, k)
+    idx, w = O.route(logits, k)
+    counts, offsets, src, dest = O.permute(idx, E)
+    assert counts[3] == 0
+    x8, sx = O.quantize_rows_fp8(x_bits[src])
+    h = O.gateup_swiglu_fp8(x8, sx, offsets, wgu8, sgu)
+    h8, sh = O.quantize_rows_fp8(h)
+    y = O.down_fp8(h8, sh, offsets, wd8, sdn)
+    got = O.combine(y, w, dest)
+    assert np.array_equal(got, out)
+
+
 ALL_PINS = [pin_hand_example, pin_brute_force, pin_dense_e1_k1, pin_route_library,
             pin_permute_library, pin_invariants, pin_stages, pin_grouped_hand_example,
             pin_grouped_reduces_to_topk, pin_grouped_brute_force, pin_grouped_invariants,
-            pin_e4m3_decode_table, pin_e4m3_encode_rne, pin_quantize_rows_fp8, pin_fp8_forward]
+            pin_e4m3_decode_table, pin_e4m3_encode_rne, pin_quantize_rows_fp8, pin_fp8_forward,
+            pin_fp8_stages]

@@ -208,3 +208,44 @@ def test_gemm_pair_mode_policy(lib):
         assert moe.gemm_pair_mode(4096, *mx, 8, 2, 1) == 0 and moe.gemm_pair_mode(4096, *mx, 8, 2, 0) == 2
     finally:
         del os.environ["MOE_GEMM_2SM_DOWN"]
+
+
+def test_fp8_workspace_layout_and_validation(lib):
+    from mixture_experts_grouped_fp32_gb300 import moe
+    T, d, f, E, k = 300, 512, 768, 8, 2
+    L = moe.workspace_layout_fp8(T, d, f, E, k)
+    M = T * k
+
+    def up(v):
+        return (v + 255) // 256 * 256
+
+    S = moe.down_ksplit_fp8(T, d, f, E, k)
+    assert 1 <= S <= 8
+    expect, o = {}, 0
+    for name, nbytes in [("status", 256), ("idx", M * 4), ("w", M * 4), ("counts", E * 4),
+                         ("offsets", (E + 1) * 4), ("src", M * 4), ("dest", M * 4), ("x8", M * d),
+                         ("sx", M * 4), ("h", M * f * 2), ("h8", M * f), ("sh", M * 4),
+                         ("y_perm", S * M * d * 4)]:
+        expect[name] = o
+        o = up(o + nbytes)
+    expect["total"] = o
+    assert L == expect
+    assert moe.workspace_size_fp8(T, d, f, E, k) == o
+    assert moe.workspace_size_fp8(T, 192, f, E, k) == 0       # d not a multiple of 128
+    assert lib.moe_forward_fp8_launch_count(32, 8, 2) == 6
+    assert lib.moe_forward_fp8_launch_count(2048, 256, 8) == 7
+    assert lib.moe_forward_fp8_launch_count(0, 8, 2) == 0
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.moe_forward_fp8(p, p, p, p, p, p, 4, 192, 256, 8, 2, p, p, 1 << 40, None) == -1
+    assert "multiples of 128" in _err(lib)
+    assert lib.moe_forward_fp8(p, p, None, p, p, p, 4, 256, 256, 8, 2, p, p, 1 << 40, None) == -1
+    assert lib.moe_forward_fp8(p, p, p, p, p, p, 4, 256, 256, 8, 2, p, p, 16, None) == -3
+    assert lib.moe_forward_fp8(p, p, p, p, p, p, 0, 256, 256, 8, 2, p, p, 1 << 40, None) == 0
+    assert lib.moe_quantize_weights_fp8(p, 8, 192, 256, p, p, None) == -1        # K % 128
+    assert lib.moe_quantize_weights_fp8(None, 8, 256, 256, p, p, None) == -1
+    assert lib.moe_quantize_rows_fp8(p, None, 4, 12, 4, p, p, None, None) == -1   # C % 8
+    assert lib.moe_quantize_rows_fp8(p, None, 4, 64, 3, p, p, None, None) == -1   # src_rows < R, no src
+    assert lib.moe_quantize_rows_fp8(p, None, 0, 64, 0, p, p, None, None) == 0    # nothing to do
+    assert lib.moe_grouped_gemm_gateup_swiglu_fp8(p, None, p, p, p, 8, 256, 256, 8, p, None, None) == -1
+    assert lib.moe_grouped_gemm_down_fp8(p, p, p, p, p, 8, 256, 256, 8, 9, p, None, None) == -1
+    assert lib.moe_grouped_gemm_down_fp8(p, p, p, p, p, 0, 256, 256, 8, 1, p, None, None) == 0
