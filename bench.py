@@ -56,7 +56,7 @@ KERNEL_NAMES = {"route": "route_kernel", "permute": "permute_kernel",
                 "gateup_swiglu": "grouped_gemm_kernel<0>", "down": "grouped_gemm_kernel<1>",
                 "combine": "combine_kernel"}
 # The FP8 layer's stages (moe_forward_fp8) and its GEMM kernels' template instances <KIND, GATHER, FP8>.
-STAGES_FP8 = ("route", "permute", "quantize_x", "gateup_swiglu", "quantize_h", "down", "combine")
+STAGES_FP8 = ("route", "permute", "gateup_swiglu", "quantize_h", "down", "combine")
 KERNEL_NAMES_FP8 = {"gateup_swiglu": "grouped_gemm_kernel<0, false, true>",
                     "down": "grouped_gemm_kernel<1, false, true>"}
 FP8_OVER_BF16 = 2.0  # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s) applied to the measured bf16 peak
@@ -68,21 +68,34 @@ FP8_OVER_BF16 = 2.0  # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s) appl
 AUTO_TIMED_S = 0.5
 AUTO_STEPS_MIN, AUTO_STEPS_MAX = 50, 4000
 
+_TRAFFIC_HASH = "4b383edeb4f77185"  # GEMM source hash the captures below were taken at
 MEASURED_TRAFFIC = {
-    ("mixtral_t32", "gateup_swiglu"): (1884901632, "6755e621afd0d8bc"),
-    ("mixtral_t32", "down"): (945057024, "6755e621afd0d8bc"),
-    ("mixtral_t512", "gateup_swiglu"): (1917181440, "6755e621afd0d8bc"),
-    ("mixtral_t512", "down"): (982833408, "6755e621afd0d8bc"),
-    ("mixtral_t512_skew40", "gateup_swiglu"): (1917549312, "6755e621afd0d8bc"),
-    ("mixtral_t512_skew40", "down"): (983505152, "6755e621afd0d8bc"),
-    ("mixtral_t4096", "gateup_swiglu"): (3706759424, "6755e621afd0d8bc"),
-    ("mixtral_t4096", "down"): (1843701248, "6755e621afd0d8bc"),
-    ("deepseek_t2048", "gateup_swiglu"): (8107921152, "6755e621afd0d8bc"),
-    ("deepseek_t2048", "down"): (4197169152, "6755e621afd0d8bc"),
-    ("deepseek_v3_t2048", "gateup_swiglu"): (4813871872, "6755e621afd0d8bc"),
-    ("deepseek_v3_t2048", "down"): (2482596608, "6755e621afd0d8bc"),
-    ("deepseek_e32_t256", "gateup_swiglu"): (1920039168, "6755e621afd0d8bc"),
-    ("deepseek_e32_t256", "down"): (1008817664, "6755e621afd0d8bc"),
+    ("mixtral_t32", "gateup_swiglu"): (1884874752, _TRAFFIC_HASH),
+    ("mixtral_t32", "down"): (944451840, _TRAFFIC_HASH),
+    ("mixtral_t512", "gateup_swiglu"): (1917088768, _TRAFFIC_HASH),
+    ("mixtral_t512", "down"): (982745856, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "gateup_swiglu"): (1917344256, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "down"): (983449344, _TRAFFIC_HASH),
+    ("mixtral_t4096", "gateup_swiglu"): (2596496384, _TRAFFIC_HASH),
+    ("mixtral_t4096", "down"): (1552656640, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "gateup_swiglu"): (1920297728, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "down"): (1008994816, _TRAFFIC_HASH),
+    ("deepseek_t2048", "gateup_swiglu"): (8110466304, _TRAFFIC_HASH),
+    ("deepseek_t2048", "down"): (4196724480, _TRAFFIC_HASH),
+    ("deepseek_v3_t2048", "gateup_swiglu"): (4703464960, _TRAFFIC_HASH),
+    ("deepseek_v3_t2048", "down"): (2482137600, _TRAFFIC_HASH),
+    ("mixtral_t32", "gateup_swiglu_fp8"): (945577216, _TRAFFIC_HASH),
+    ("mixtral_t32", "down_fp8"): (474084352, _TRAFFIC_HASH),
+    ("mixtral_t512", "gateup_swiglu_fp8"): (971990272, _TRAFFIC_HASH),
+    ("mixtral_t512", "down_fp8"): (497739008, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "gateup_swiglu_fp8"): (971613696, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "down_fp8"): (498119168, _TRAFFIC_HASH),
+    ("mixtral_t4096", "gateup_swiglu_fp8"): (1201340928, _TRAFFIC_HASH),
+    ("mixtral_t4096", "down_fp8"): (781184000, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "gateup_swiglu_fp8"): (965993216, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "down_fp8"): (534342144, _TRAFFIC_HASH),
+    ("deepseek_t2048", "gateup_swiglu_fp8"): (3891759104, _TRAFFIC_HASH),
+    ("deepseek_t2048", "down_fp8"): (2295916544, _TRAFFIC_HASH),
 }
 GEMM_SOURCES = ("mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm.cu",
                 "mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm_2sm.cu",
@@ -122,8 +135,7 @@ def stage_work(w: Workload, n_active: int, fp8: bool = False) -> dict:
     if fp8:  # 1-byte codes; weight scales 4 bytes per output column, activation scales per row
         return {
             "route": {"bytes": T * E * 4 + M * 8, "flops": 0},
-            "permute": {"bytes": M * 4 + (E + E + 1 + 2 * M) * 4, "flops": 0},
-            "quantize_x": {"bytes": M * 4 + T * d * 2 + M * d + M * 4, "flops": 0},
+            "permute": {"bytes": M * 4 + T * d * 2 + M * d + M * 4 + (E + E + 1 + 2 * M) * 4, "flops": 0},
             "gateup_swiglu": {"bytes": n_active * (d * 2 * f + 2 * f * 4) + M * d + M * 4 + M * f * 2,
                               "flops": 4 * M * d * f},
             "quantize_h": {"bytes": M * f * 2 + M * f + M * 4, "flops": 0},
@@ -323,8 +335,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         x8, sx, h8, sh = v["x8"], v["sx"], v["h8"], v["sh"]
         calls = [
             lambda: moe.route(l_d, w.k, idx=idx, w=wts),
-            lambda: moe.permute(idx, x_d, w.E, status=st, out=(counts_d, offs, src, dest, None)),
-            lambda: moe.quantize_rows_fp8(x_d, src, status=st, out=(x8, sx)),
+            lambda: moe.permute_fp8(idx, x_d, w.E, status=st, out=(counts_d, offs, src, dest, x8, sx)),
             lambda: moe.grouped_gemm_gateup_swiglu_fp8(x8, sx, w8[0], w8[1], offs, h=h, status=st),
             lambda: moe.quantize_rows_fp8(h, status=st, out=(h8, sh)),
             lambda: moe.grouped_gemm_down_fp8(h8, sh, w8[2], w8[3], offs, y_perm=y, status=st, ksplit=v["ksplit"]),
@@ -403,10 +414,12 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = measured_traffic(w.name, dom + ("_fp8" if fp8 else ""))
     kname = KERNEL_NAMES_FP8[dom] if fp8 else KERNEL_NAMES[dom]
-    pair_mode = 0 if fp8 else moe.gemm_pair_mode(w.T, w.d, w.f, w.E, w.k, 0 if dom == "gateup_swiglu" else 1)
-    if pair_mode >= 1:  # SM-pair kernel, template <KIND, swapping form>
-        kname = kname.replace("grouped_gemm_kernel", "grouped_gemm_2sm_kernel").replace(
-            ">", ", true>" if pair_mode == 2 else ", false>")
+    pair_mode = (moe.gemm_pair_mode_fp8 if fp8 else moe.gemm_pair_mode)(w.T, w.d, w.f, w.E, w.k,
+                                                                       0 if dom == "gateup_swiglu" else 1)
+    if pair_mode >= 1:  # SM-pair kernel, template <KIND, SWAPCAP, GATHER, FP8>
+        kname = "grouped_gemm_2sm_kernel<%d, %s, false, %s>" % (0 if dom == "gateup_swiglu" else 1,
+                                                                "true" if pair_mode == 2 else "false",
+                                                                "true" if fp8 else "false")
     psrc = peak_src + " (burst)" + (" x 2 (nominal fp8 / bf16 dense rate)" if fp8 and roof["bound"] == "tensor" else "")
     roof.update({"kernel": kname, "peak_source": psrc,
                  "algorithmic_per_launch": sw[dom]["flops"] if roof["bound"] == "tensor" else sw[dom]["bytes"],

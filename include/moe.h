@@ -264,38 +264,50 @@ MOE_API int moe_forward_noalloc(const void* x, const float* logits, const void* 
  * scales then need no per-block promotion of the accumulator).  d and f must be multiples of 128.
  * ------------------------------------------------------------------------------------------- */
 
-/* Weights, once per model: W [E,K,N] bf16 (as w_gate_up [E,d,2f] or w_down [E,f,d]) -> Wq [E,N,K]
- * E4M3 codes (transposed: K contiguous) and scale [E,N] fp32, one per output column.
- * Requires 1 <= E <= 256, K a multiple of 128 and N of 64, both <= 65536. */
+/* Weights, once per model: W [E,K,N] bf16 (as w_gate_up [E,d,2f] or w_down [E,f,d]) -> Wq E4M3
+ * codes, transposed and blocked: [E, N/64, K/128, 64, 128], the code of (expert e, output column n,
+ * reduction index k) at [e][n/64][k/128][n%64][k%128] — contiguous 8 KB blocks of 64 output
+ * columns x 128 K values, which the FP8 GEMMs read as whole blocks — and scale [E,N] fp32, one per
+ * output column.  Requires 1 <= E <= 256, K a multiple of 128 and N of 64, both <= 65536. */
 MOE_API int moe_quantize_weights_fp8(const void* W, int E, int K, int N, void* Wq, float* scale,
                                      moe_stream_t stream);
+
+/* Step 2 of the FP8 layer: moe_permute, with the permuted rows written as E4M3 codes instead of
+ * bf16 — each token's row quantised once (absmax over its d values) and its codes and scale written
+ * to each of its top_k rows: x8_perm [T*top_k, d] codes (8-byte aligned), sx [T*top_k] fp32; the
+ * other arguments and outputs as for moe_permute. */
+MOE_API int moe_permute_fp8(const int32_t* idx, const void* x, int T, int d, int E, int top_k, int32_t* counts,
+                            int32_t* offsets, int32_t* src, int32_t* dest, void* x8_perm, float* sx,
+                            int32_t* status, moe_stream_t stream);
 
 /* Rows: q[r] = E4M3 codes of row src[r] of a (row r when src is NULL), scale[r] its scale.
  *   a [src_rows, C] bf16 in (16-byte aligned), C a multiple of 8;  src [R] int32 in or NULL (then
  *   src_rows >= R);  q [R, C] codes out (8-byte aligned);  scale [R] fp32 out;
  *   status: device int32 or NULL (a src value outside [0, src_rows) quantises a zero row and sets
  *   MOE_STATUS_BAD_SRC).
- * moe_forward_fp8 uses it with src from the permutation (x8_perm[r] = quantised x[src[r]]) and on h. */
+ * moe_forward_fp8 uses it on h. */
 MOE_API int moe_quantize_rows_fp8(const void* a, const int32_t* src, int R, int C, int src_rows, void* q,
                                   float* scale, int32_t* status, moe_stream_t stream);
 
 /* Step 3 on E4M3 operands: h[r] = bf16(silu(g) * u) with g, u as above.
- *   x8_perm [M,d] codes, sx [M] fp32;  w8_gate_up [E,2f,d] codes (gate rows 0..f-1, up rows
- *   f..2f-1 of each expert), s_gate_up [E,2f] fp32 (moe_quantize_weights_fp8 of w_gate_up);
+ *   x8_perm [M,d] codes, sx [M] fp32;  w8_gate_up: blocked codes of the [E,2f,d] transposed
+ *   weights (gate columns 0..f-1, up f..2f-1 of each expert), s_gate_up [E,2f] fp32, both from
+ *   moe_quantize_weights_fp8 of w_gate_up;
  *   offsets [E+1];  h [M,f] bf16 out;  status as for step 3. */
 MOE_API int moe_grouped_gemm_gateup_swiglu_fp8(const void* x8_perm, const float* sx, const void* w8_gate_up,
                                                const float* s_gate_up, const int32_t* offsets, int M, int d,
                                                int f, int E, void* h, int32_t* status, moe_stream_t stream);
 
 /* Step 4 on E4M3 operands: y_perm[r][m] = (sum_n h8[r][n] * W8[e][m][n]) * (sh[r] * s_down[e][m]).
- *   h8 [M,f] codes, sh [M] fp32;  w8_down [E,d,f] codes, s_down [E,d] fp32;  ksplit in [1, 8]
+ *   h8 [M,f] codes, sh [M] fp32;  w8_down: blocked codes of the [E,d,f] transposed weights and
+ *   s_down [E,d] fp32 (moe_quantize_weights_fp8 of w_down);  ksplit in [1, 8]
  *   (K slices of 128-wide blocks, as in moe_grouped_gemm_down);  y_perm [ksplit,M,d] fp32 out. */
 MOE_API int moe_grouped_gemm_down_fp8(const void* h8, const float* sh, const void* w8_down, const float* s_down,
                                       const int32_t* offsets, int M, int d, int f, int E, int ksplit,
                                       float* y_perm, int32_t* status, moe_stream_t stream);
 
-/* The FP8 layer in one call: route (+ permute), quantise x rows by src, FP8 gate+up GEMM
- * (+ SwiGLU), quantise h rows, FP8 down GEMM, combine — 6 launches (7 when routing and the
+/* The FP8 layer in one call: route (+ permute writing quantised x rows), FP8 gate+up GEMM
+ * (+ SwiGLU), quantise h rows, FP8 down GEMM, combine — 5 launches (6 when routing and the
  * permutation run apart, see moe_forward_launch_count).  Inputs as for moe_forward, with the
  * weights given as moe_quantize_weights_fp8 codes and scales; workspace >=
  * moe_workspace_size_fp8() bytes, 256-byte aligned, its pieces at moe_workspace_layout_fp8()'s
@@ -304,6 +316,10 @@ MOE_API int moe_grouped_gemm_down_fp8(const void* h8, const float* sh, const voi
 MOE_API size_t moe_workspace_size_fp8(int T, int d, int f, int E, int top_k);
 MOE_API int moe_workspace_layout_fp8(int T, int d, int f, int E, int top_k, size_t* offsets_out);
 MOE_API int moe_down_ksplit_fp8(int T, int d, int f, int E, int top_k);
+/* As moe_gemm_pair_mode, for moe_forward_fp8's GEMMs.  Policy (the same environment overrides):
+ * gate+up as for moe_forward; the down GEMM on normal-only SM pairs (1) from 128 rows per expert on
+ * average, else single SMs (0). */
+MOE_API int moe_gemm_pair_mode_fp8(int T, int d, int f, int E, int top_k, int kind);
 MOE_API int moe_forward_fp8_launch_count(int T, int E, int top_k);
 MOE_API int moe_forward_fp8(const void* x, const float* logits, const void* w8_gate_up, const float* s_gate_up,
                             const void* w8_down, const float* s_down, int T, int d, int f, int E, int top_k,

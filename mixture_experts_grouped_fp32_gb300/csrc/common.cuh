@@ -57,15 +57,18 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx,
 cudaError_t launch_route_grouped(const float* logits, const float* bias, int T, int E, int k, int n_group,
                                  int topk_group, float scale, int32_t* idx, float* w, int32_t* status_reset,
                                  cudaStream_t s);
+// x8/sx (FP8 layer): when x8 is given, the permuted rows are written as E4M3 codes x8 [T*k, d] with
+// a scale per row sx [T*k] (each token quantised once, fp8.cuh) instead of the bf16 x_perm.
 cudaError_t launch_permute(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
                            int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest,
-                           __nv_bfloat16* x_perm, int32_t* status, int num_sms, cudaStream_t s);
+                           __nv_bfloat16* x_perm, int32_t* status, int num_sms, cudaStream_t s,
+                           uint8_t* x8 = nullptr, float* sx = nullptr);
 // Steps 1+2 in one launch (softmax router): only when route_permute_fusable(T, E).
 bool route_permute_fusable(int T, int E);
 cudaError_t launch_route_permute(const float* logits, const __nv_bfloat16* x, int T, int d, int E, int k,
                                  int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* src,
                                  int32_t* dest, __nv_bfloat16* x_perm, int32_t* status, int num_sms,
-                                 cudaStream_t s);
+                                 cudaStream_t s, uint8_t* x8 = nullptr, float* sx = nullptr);
 cudaError_t launch_combine(const float* y, const float* w, const int32_t* dest, int T, int d, int k,
                            int ksplit, __nv_bfloat16* out, int32_t* status, cudaStream_t s);
 
@@ -110,10 +113,14 @@ bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint6
                           uint32_t box_rows);
 // The same over bytes (FP8 codes): box = [box_rows, 128 cols].
 bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows);
+// Blocked FP8 weight codes (rows x K in 8 KB blocks of 64 rows x 128 K, see moe.h): a box of
+// box_rows (a multiple of 64) rows x 128 K codes.
+bool make_tensor_map_w8(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows);
 
 // FP8 quantisation (fp8.cu).  Rows: row r of the bf16 [*, C] matrix a (row src[r] when src is
 // given, src values checked against src_rows) -> E4M3 codes q [R, C] and scale [R].  Weights:
-// W [E, K, N] bf16 -> Wq [E, N, K] codes (transposed) and scale [E, N], one per output column.
+// W [E, K, N] bf16 -> Wq codes, transposed and blocked ([E, N/64, K/128, 64, 128]: code (e, n, k) at
+// [e][n / 64][k / 128][n % 64][k % 128]), and scale [E, N], one per output column.
 cudaError_t launch_quantize_rows_fp8(const __nv_bfloat16* a, const int32_t* src, int R, int C, int src_rows,
                                      uint8_t* q, float* scale, int32_t* status, cudaStream_t s);
 cudaError_t launch_quantize_weights_fp8(const __nv_bfloat16* W, int E, int K, int N, uint8_t* Wq, float* scale,

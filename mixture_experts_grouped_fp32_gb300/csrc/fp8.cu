@@ -8,21 +8,13 @@
 // their epilogue.  DeepGEMM PR #304 write-up, section 5.3 (an FP8 grouped GEMM on SM100) and its
 // Mega MoE epilogue (SwiGLU then FP8 quantisation) are the pages' FP8 context; their 128-wide
 // blockwise scales are not used here (they need per-K-block promotion of the accumulator).
-#include <cuda_fp8.h>
-
 #include "common.cuh"
+#include "fp8.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kQThreads = 256;
-
-__device__ __forceinline__ uint8_t to_e4m3(float v) {
-    return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Block-wide max of non-negative floats (every thread gets the result).
 __device__ __forceinline__ float block_max(float v, float* red) {
@@ -56,31 +48,20 @@ quantize_rows_kernel(const uint4* __restrict__ a, const int32_t* __restrict__ sr
     const uint4* row = a + static_cast<size_t>(s < 0 ? 0 : s) * cv;
     float m = 0.0f;
     if (s >= 0)
-        for (int v = threadIdx.x; v < cv; v += kQThreads) {
-            const uint4 p = __ldg(row + v);
-            const uint32_t w[4] = {p.x, p.y, p.z, p.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
-        }
+        for (int v = threadIdx.x; v < cv; v += kQThreads) m = fmaxf(m, absmax8(__ldg(row + v)));
     const float amax = block_max(m, red);
-    const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
-    if (threadIdx.x == 0) scale[r] = amax > 0.0f ? amax / 448.0f : 1.0f;
+    const float inv = fp8_inv(amax);
+    if (threadIdx.x == 0) scale[r] = fp8_scale(amax);
     uint2* out = q + static_cast<size_t>(r) * cv;
     for (int v = threadIdx.x; v < cv; v += kQThreads) {
         uint4 p = make_uint4(0, 0, 0, 0);
         if (s >= 0) p = __ldg(row + v);
-        const uint32_t w[4] = {p.x, p.y, p.z, p.w};
-        uint32_t o[2] = {0u, 0u};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t c0 = to_e4m3(bf16_lo(w[i]) * inv), c1 = to_e4m3(bf16_hi(w[i]) * inv);
-            o[i >> 1] |= (c0 | (c1 << 8)) << (16 * (i & 1));
-        }
-        out[v] = make_uint2(o[0], o[1]);
+        out[v] = codes8(p, inv);
     }
 }
 
-// Weights W [E, K, N] bf16 -> Wq [E, N, K] codes and scale [E, N]; block (e, 64-column group).
+// Weights W [E, K, N] bf16 -> Wq blocked codes (code (e, n, k) at [e][n / 64][k / 128][n % 64]
+// [k % 128]: 8 KB blocks of 64 output columns x 128 K) and scale [E, N]; block (e, 64-column group).
 // Pass 1: per-column absmax over K.  Pass 2: 64 x 64 tiles transposed through shared memory, so
 // reads (64 columns of a K-row) and writes (64 K-bytes of an output row) are both contiguous.
 constexpr int kWCols = 64;
@@ -103,12 +84,12 @@ quantize_weights_kernel(const uint16_t* __restrict__ W, int K, int N, uint8_t* _
     if (threadIdx.x < kWCols) {
         float a = 0.0f;
         for (int i = 0; i < kQThreads / kWCols; ++i) a = fmaxf(a, cmax[i][threadIdx.x]);
-        inv[threadIdx.x] = a > 0.0f ? 448.0f / a : 1.0f;
-        if (n0 + static_cast<int>(threadIdx.x) < N)
-            scale[static_cast<size_t>(e) * N + n0 + threadIdx.x] = a > 0.0f ? a / 448.0f : 1.0f;
+        inv[threadIdx.x] = fp8_inv(a);
+        if (n0 + static_cast<int>(threadIdx.x) < N) scale[static_cast<size_t>(e) * N + n0 + threadIdx.x] = fp8_scale(a);
     }
     __syncthreads();
-    uint8_t* Wqe = Wq + static_cast<size_t>(e) * N * K;
+    // This block's 64 columns form one 64-row group of the blocked layout: K / 128 blocks of 8 KB.
+    uint8_t* Wqg = Wq + static_cast<size_t>(e) * N * K + static_cast<size_t>(n0) * K;
     for (int k0 = 0; k0 < K; k0 += kWCols) {
         for (int i = threadIdx.x; i < kWCols * kWCols; i += kQThreads) {
             const int kk = i / kWCols, cc = i % kWCols;  // read: row k0+kk, column n0+cc
@@ -120,7 +101,8 @@ quantize_weights_kernel(const uint16_t* __restrict__ W, int K, int N, uint8_t* _
         __syncthreads();
         for (int i = threadIdx.x; i < kWCols * kWCols; i += kQThreads) {
             const int cc = i / kWCols, kk = i % kWCols;  // write: output row n0+cc, K-byte k0+kk
-            if (k0 + kk < K && n0 + cc < N) Wqe[static_cast<size_t>(n0 + cc) * K + k0 + kk] = tile[cc][kk];
+            const int k = k0 + kk;
+            if (k < K && n0 + cc < N) Wqg[static_cast<size_t>(k >> 7) * 8192 + cc * 128 + (k & 127)] = tile[cc][kk];
         }
         __syncthreads();
     }

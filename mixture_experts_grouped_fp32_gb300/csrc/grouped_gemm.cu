@@ -45,9 +45,13 @@
 //     n0..n0+127 and n0+128..n0+255).
 //
 // FP8 variant (E4M3 codes, kind::f8f6f4 MMAs with K = 32): the activations are [M, K] codes with a
-// scale per row, the weights are stored transposed, [E, N_total, K] codes (K contiguous) with a
-// scale per output column, so both operands are K-major and one 128-byte swizzle row holds 128 K
-// values: a stage is 128 K deep.  Its weight part is two 128-row boxes (kind 0: gate rows n0.. and
+// scale per row, the weights are stored transposed and blocked, [E * N_total / 64, K / 128, 64, 128]
+// codes (64 output columns x 128 K values per contiguous 8 KB block) with a scale per output
+// column, so both operands are K-major and one 128-byte swizzle row holds 128 K values: a stage is
+// 128 K deep, and each weight box is one or two whole 8 KB blocks of HBM rather than 128 rows of
+// 128 bytes a power-of-two stride apart.  (Row-major [N, K] codes with K = 4096 streamed ~10 %
+// slower even in the pure weight-streaming case, and up to ~25 % slower at 128-256 rows per
+// expert.)  Its weight part is two 128-row boxes (kind 0: gate rows n0.. and
 // up rows f+n0..; kind 1: rows n0.. and n0+128..), 16 KB each, and the accumulator columns keep the
 // BF16 kernel's meaning.  The scales factor out of the K sum, so the epilogue multiplies each
 // accumulator by scale_row * scale_col before SwiGLU (kind 0) or the store (kind 1).
@@ -279,11 +283,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 if (FP8) {
                     // Weight rows (output columns) of expert e: [e * 2N, e * 2N + 2N) for gate+up
-                    // (gate then up), [e * N, e * N + N) for down.
+                    // (gate then up), [e * N, e * N + N) for down; two 64-row blocks per box.
                     const int wrow0 = KIND == 0 ? it.e * 2 * N + n0 : it.e * N + n0;
                     const int wrow1 = KIND == 0 ? wrow0 + N : wrow0 + 128;
-                    ptx::tma_load_2d(sb, &tmB, &c.full[stage], kb * BKE, wrow0, pol_wgt);
-                    ptx::tma_load_2d(sb + W8_BOX_BYTES, &tmB, &c.full[stage], kb * BKE, wrow1, pol_wgt);
+                    ptx::tma_load_4d(sb, &tmB, &c.full[stage], 0, 0, kb, wrow0 / 64, pol_wgt);
+                    ptx::tma_load_4d(sb + W8_BOX_BYTES, &tmB, &c.full[stage], 0, 0, kb, wrow1 / 64, pol_wgt);
                 } else {
 #pragma unroll
                     for (int q = 0; q < B_BOXES; ++q) {
@@ -623,7 +627,7 @@ cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const ch
     // FP8: activation codes [M, K] and transposed weight codes [E * N_total, K], K contiguous.
     const bool maps_ok =
         FP8 ? make_tensor_map_u8(&mA, a.A, a.K, arows, BM) && make_tensor_map_u8(&mA32, a.A, a.K, arows, A_BOX32_ROWS) &&
-                  make_tensor_map_u8(&mB, a.B, a.K, static_cast<uint64_t>(a.E) * bcols, 128)
+                  make_tensor_map_w8(&mB, a.B, a.K, static_cast<uint64_t>(a.E) * bcols, 128)
             : make_tensor_map_bf16(&mA, a.A, a.K, arows, BM) &&
                   make_tensor_map_bf16(&mA32, a.A, a.K, arows, A_BOX32_ROWS) &&
                   make_tensor_map_bf16(&mB, a.B, bcols, static_cast<uint64_t>(a.E) * a.K, BK);
@@ -669,6 +673,21 @@ bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint6
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Blocked FP8 weight codes [rows / 64, K / 128, 64, 128] as a 4-D tensor (innermost first: 128 K
+// codes, 64 rows, K block, 64-row group); box = 128 codes x 64 rows x 1 K block x box_rows / 64
+// groups, which lands in shared memory as box_rows K-major rows of 128 bytes, 128-byte swizzled.
+bool make_tensor_map_w8(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {128, 64, K / 128, rows / 64};
+    cuuint64_t strides[3] = {128, 64 * 128, (K / 128) * 64 * 128};
+    cuuint32_t box[4] = {128, 64, 1, box_rows / 64};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D byte tensor [rows, cols] (FP8 codes, cols contiguous), box = [box_rows, 128 cols], 128-byte swizzle.
 bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
     auto enc = get_encode_fn();
@@ -688,14 +707,13 @@ cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaSt
         *why = "ksplit must be 1 for gate+up and in [1, 8] for down";
         return cudaErrorInvalidValue;
     }
-    if (a.fp8) {
-        if (a.K % 128 != 0 || a.gather_src || !a.a_scale || !a.b_scale) {
-            *why = "FP8 grouped GEMM: K must be a multiple of 128, scales given, no row gather";
-            return cudaErrorInvalidValue;
-        }
-        return kind == 0 ? launch_kind<0, false, true>(a, num_sms, s, why) : launch_kind<1, false, true>(a, num_sms, s, why);
+    if (a.fp8 && (a.K % 128 != 0 || a.gather_src || !a.a_scale || !a.b_scale)) {
+        *why = "FP8 grouped GEMM: K must be a multiple of 128, scales given, no row gather";
+        return cudaErrorInvalidValue;
     }
     if (a.pair && num_sms >= 2 && !a.inject_stall) return launch_grouped_gemm_pair(kind, a, num_sms, s, why);
+    if (a.fp8)
+        return kind == 0 ? launch_kind<0, false, true>(a, num_sms, s, why) : launch_kind<1, false, true>(a, num_sms, s, why);
     if (kind == 0)
         return a.gather_src ? launch_kind<0, true, false>(a, num_sms, s, why)
                             : launch_kind<0, false, false>(a, num_sms, s, why);

@@ -55,6 +55,14 @@
 //   T (4/8 KB) swap only: the CTA's N/2 token rows x 64 K (K-major), as 32-row boxes; after the
 //              six stages in layout A, after X and Y of the stage in layout B.
 //
+// FP8 variant (E4M3 codes, kind::f8f6f4 pair MMAs, as in grouped_gemm.cu's FP8 instance): the
+// weights are transposed, blocked codes (8 KB blocks of 64 output columns x 128 K), so each
+// 64-column weight box above becomes one such block — 64 K-major rows of 128 K codes, the same
+// 8 KB at the same place in shared memory — every operand is K-major,
+// a stage is 128 K deep, and the epilogue multiplies by scale_row * scale_col.  Schedule, layouts
+// and synchronisation are unchanged: a stage still moves the same bytes and MMA work per CTA pair
+// (twice the FLOPs at twice the tensor rate).
+//
 // Synchronisation across the pair:
 //   full[s]   lives in CTA 0: its producer arms it with the bytes of both CTAs; both producers'
 //             TMA loads complete on it (cp.async.bulk.tensor .cta_group::2).
@@ -347,14 +355,18 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
 // GATHER (kind 0 only): each CTA's six extra warps gather its own activation rows from x by
 // src[] with cp.async, as in grouped_gemm.cu; CTA 0's `full` barrier then expects three arrivals:
 // the TMA weight bytes', and one per CTA when its gathered rows have landed (CTA 1's remotely).
-template <int KIND, bool SWAPCAP, bool GATHER>
+template <int KIND, bool SWAPCAP, bool GATHER, bool FP8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? GATHER_THREADS : NUM_THREADS, 1)
 grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
                         const __grid_constant__ CUtensorMap tmB, const int32_t* __restrict__ offsets, int M,
                         int K, int N, int E, int ksplit, int swap_max, int layout_mode, int split_req,
-                        const int4* __restrict__ xg, const int32_t* __restrict__ gsrc, int gT, void* __restrict__ out,
+                        const int4* __restrict__ xg, const int32_t* __restrict__ gsrc, int gT,
+                        const float* __restrict__ a_scale, const float* __restrict__ b_scale, void* __restrict__ out,
                         int32_t* __restrict__ status) {
+    static_assert(!(GATHER && FP8), "the FP8 variant reads its activation codes with TMA");
     constexpr int BN_OUT = Tiling<KIND>::BN_OUT;
+    constexpr int BKE = FP8 ? 128 : BK;  // K values per stage (one 128-byte swizzle row)
+    const int wrows = KIND == 0 ? 2 * N : N;  // FP8: weight rows (output columns) per expert
     constexpr int SW_BOXES = 4;  // weight boxes per CTA in a swapped item (two MMAs)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -367,7 +379,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
     const bool leader = rank == 0;
     const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
     const Tiling<KIND> tiling(N);
-    const int num_kb = K / BK;
+    const int num_kb = K / BKE;
     const int kb_per = (num_kb + ksplit - 1) / ksplit;
 
     if (tid == 0) {
@@ -567,27 +579,36 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                     if (!GATHER) {
                         uint8_t* st = tiles + ring.tok_off(stage);
                         for (int q = 0; q < ntb; ++q)
-                            ptx::tma_load_2d_pair(st + q * TOK_BOX_BYTES, &tmA32, full_leader, kb * BK,
+                            ptx::tma_load_2d_pair(st + q * TOK_BOX_BYTES, &tmA32, full_leader, kb * BKE,
                                                   it.row0 + rank * half + q * TOK_BOX_ROWS, pol_act);
                     }
 #pragma unroll
                     for (int q = 0; q < SW_BOXES; ++q) {
                         // kind 0: gate n0, n0+64, up f+n0, f+n0+64; kind 1: n0, n0+64, n0+256, n0+320.
+                        // (FP8: the same output columns as 64-row boxes of the transposed codes.)
                         const int col = q < 2 ? n0 + 64 * q : (KIND == 0 ? N : 256) + n0 + 64 * (q - 2);
-                        ptx::tma_load_2d_pair(sa + q * B_BOX_BYTES, &tmB, full_leader, col, brow + kb * BK,
-                                              pol_wgt);
+                        if (FP8)
+                            ptx::tma_load_4d_pair(sa + q * B_BOX_BYTES, &tmB, full_leader, 0, 0, kb,
+                                                  (it.e * wrows + col) / 64, pol_wgt);
+                        else
+                            ptx::tma_load_2d_pair(sa + q * B_BOX_BYTES, &tmB, full_leader, col, brow + kb * BK,
+                                                  pol_wgt);
                     }
                 } else {
                     const int n0 = it.n_tile * BN_OUT;
-                    if (!GATHER) ptx::tma_load_2d_pair(sa, &tmA, full_leader, kb * BK, it.row0, pol_act);
+                    if (!GATHER) ptx::tma_load_2d_pair(sa, &tmA, full_leader, kb * BKE, it.row0, pol_act);
 #pragma unroll
                     for (int q = 0; q < BH_BOXES; ++q) {
                         // kind 0: CTA r holds gate columns n0+64r.. and up columns f+n0+64r..;
                         // kind 1: CTA r holds output columns n0+128r .. n0+128r+127.
                         const int col = KIND == 0 ? (q == 0 ? n0 + 64 * rank : N + n0 + 64 * rank)
                                                   : n0 + 128 * rank + 64 * q;
-                        ptx::tma_load_2d_pair(sa + REGION_Y + q * B_BOX_BYTES, &tmB, full_leader, col,
-                                              brow + kb * BK, pol_wgt);
+                        if (FP8)
+                            ptx::tma_load_4d_pair(sa + REGION_Y + q * B_BOX_BYTES, &tmB, full_leader, 0, 0, kb,
+                                                  (it.e * wrows + col) / 64, pol_wgt);
+                        else
+                            ptx::tma_load_2d_pair(sa + REGION_Y + q * B_BOX_BYTES, &tmB, full_leader, col,
+                                                  brow + kb * BK, pol_wgt);
                     }
                 }
                 fill_parity[stage] = phase;
@@ -673,7 +694,8 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------ pair MMA issuer (CTA 0) ------------------------------
-        constexpr uint32_t idesc_normal = ptx::idesc_bf16_f32(2 * BM, ACC_COLS, /*a_mn=*/0, /*b_mn=*/1);
+        constexpr uint32_t idesc_normal = FP8 ? ptx::idesc_e4m3_f32(2 * BM, ACC_COLS, 0, 0)
+                                              : ptx::idesc_bf16_f32(2 * BM, ACC_COLS, /*a_mn=*/0, /*b_mn=*/1);
         int stage = 0;
         uint32_t phase = 0, acc = 0, acc_phase = 0;
         bool aborted = false;
@@ -681,7 +703,8 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
           const PairItem slot = slot_at(i);
           for (int sub = 0; sub < slot.nsub && !aborted; ++sub) {
             const PairItem& it = slot;
-            const uint32_t idesc_swap = ptx::idesc_bf16_f32(2 * BM, static_cast<uint32_t>(it.ntok), 1, 0);
+            const uint32_t idesc_swap = FP8 ? ptx::idesc_e4m3_f32(2 * BM, static_cast<uint32_t>(it.ntok), 0, 0)
+                                            : ptx::idesc_bf16_f32(2 * BM, static_cast<uint32_t>(it.ntok), 1, 0);
             const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
             if (!ptx::mbar_wait(&c.tempty[acc], acc_phase ^ 1u, abort_flag)) {
                 raise_abort(c, status);
@@ -698,7 +721,30 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 }
                 ptx::tc_fence_after();
                 const uint32_t sa = ptx::smem_u32(tiles + stage * ring.stride);
-                if (SWAPCAP && it.swap) {
+                if (FP8) {
+                    // Every operand K-major: +32 B (32 codes) per MMA, 8-row groups 1 KB apart.
+                    if (SWAPCAP && it.swap) {
+                        const uint64_t wx_desc = ptx::smem_desc_sw128(sa, 16, 1024);
+                        const uint64_t wy_desc = ptx::smem_desc_sw128(sa + REGION_Y, 16, 1024);
+                        const uint64_t tok_desc = ptx::smem_desc_sw128(ptx::smem_u32(tiles + ring.tok_off(stage)), 16, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < BKE / 32; ++kk) {
+                            const uint32_t accum = (kb != kb0 || kk != 0) ? 1u : 0u;
+                            const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+                            ptx::mma_f8_ss_pair(d_tmem, wx_desc + off, tok_desc + off, idesc_swap, accum);
+                            ptx::mma_f8_ss_pair(d_tmem + 128, wy_desc + off, tok_desc + off, idesc_swap, accum);
+                        }
+                    } else {
+                        const uint64_t a_desc = ptx::smem_desc_sw128(sa, 16, 1024);
+                        const uint64_t b_desc = ptx::smem_desc_sw128(sa + REGION_Y, 16, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < BKE / 32; ++kk) {
+                            const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+                            ptx::mma_f8_ss_pair(d_tmem, a_desc + off, b_desc + off, idesc_normal,
+                                                (kb != kb0 || kk != 0) ? 1u : 0u);
+                        }
+                    }
+                } else if (SWAPCAP && it.swap) {
                     // Weights MN-major (A, 64-column atoms 8 KB apart), tokens K-major (B).
                     const uint64_t wx_desc = ptx::smem_desc_sw128(sa, B_BOX_BYTES, 1024);
                     const uint64_t wy_desc = ptx::smem_desc_sw128(sa + REGION_Y, B_BOX_BYTES, 1024);
@@ -759,6 +805,13 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 // col0 + 256.
                 const int col0 = it.n_tile * super_n<KIND>() + 128 * rank + r_local;
                 const int nchunk = (it.rows + 31) / 32;
+                // FP8: column scales of this lane's two columns (gate/up, or col0/col0+256).
+                float sc0 = 1.0f, sc1 = 1.0f;
+                if (FP8) {
+                    const float* sbe = b_scale + static_cast<size_t>(it.e) * wrows;
+                    if (col0 < N) sc0 = __ldg(sbe + col0);
+                    if (KIND == 0 ? col0 < N : col0 + 256 < N) sc1 = __ldg(sbe + col0 + (KIND == 0 ? N : 256));
+                }
 #pragma unroll 1
                 for (int cc = 0; cc < nchunk; ++cc) {
                     uint32_t a0[32], a1[32];
@@ -767,6 +820,15 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                     ptx::tmem_ld_wait();
                     const int nrow = min(32, it.rows - cc * 32);
                     const size_t row_base = static_cast<size_t>(it.row0 + cc * 32);
+                    if (FP8) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nrow) {
+                                const float sr = __ldg(a_scale + row_base + j);  // same row in every lane
+                                a0[j] = __float_as_uint(__uint_as_float(a0[j]) * (sr * sc0));
+                                a1[j] = __float_as_uint(__uint_as_float(a1[j]) * (sr * sc1));
+                            }
+                    }
                     if (KIND == 1) {
                         float* y = reinterpret_cast<float*>(out) + static_cast<size_t>(it.kslice) * M * N;
 #pragma unroll
@@ -791,6 +853,9 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 const int n0 = it.n_tile * BN_OUT;
                 const bool row_ok = r_local < it.rows;
                 const size_t grow = static_cast<size_t>(it.row0 + r_local);
+                // FP8: this lane's row scale and the expert's column scales.
+                const float srow = (FP8 && row_ok) ? __ldg(a_scale + grow) : 1.0f;
+                const float* sbe = FP8 ? b_scale + static_cast<size_t>(it.e) * wrows : nullptr;
                 if (KIND == 0) {
                     // Accumulator columns: [gate n0..+63 | up n0..+63 | gate n0+64..+127 | up n0+64..+127].
                     __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(out);
@@ -802,6 +867,13 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                         ptx::tmem_ld_32x32b_x32(taddr + gcol + 64, u);
                         ptx::tmem_ld_wait();
                         const int col = n0 + cc * 32;
+                        if (FP8 && row_ok && col < N) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {  // the column scales are the same in every lane
+                                g[j] = __float_as_uint(__uint_as_float(g[j]) * (srow * __ldg(sbe + col + j)));
+                                u[j] = __float_as_uint(__uint_as_float(u[j]) * (srow * __ldg(sbe + N + col + j)));
+                            }
+                        }
                         if (row_ok && col < N) {
                             uint4* dst = reinterpret_cast<uint4*>(h + grow * N + col);
 #pragma unroll
@@ -825,6 +897,11 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                         ptx::tmem_ld_32x32b_x32(taddr + cc * 32, v32);
                         ptx::tmem_ld_wait();
                         const int col = n0 + cc * 32;
+                        if (FP8 && row_ok && col < N) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                v32[j] = __float_as_uint(__uint_as_float(v32[j]) * (srow * __ldg(sbe + col + j)));
+                        }
                         if (row_ok && col < N) {
                             float4* dst = reinterpret_cast<float4*>(y + grow * N + col);
 #pragma unroll
@@ -874,13 +951,13 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
     ptx::cluster_sync();
 }
 
-template <int KIND, bool SWAPCAP, bool GATHER>
+template <int KIND, bool SWAPCAP, bool GATHER, bool FP8>
 cudaError_t launch_pair_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const char** why) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_2sm_kernel<KIND, SWAPCAP, GATHER>,
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_2sm_kernel<KIND, SWAPCAP, GATHER, FP8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) {
             *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
@@ -892,9 +969,14 @@ cudaError_t launch_pair_kind(const GemmArgs& a, int num_sms, cudaStream_t s, con
     const uint64_t bcols = KIND == 0 ? 2ull * a.N : static_cast<uint64_t>(a.N);
     // With GATHER, A is x [gather_T, K] (the maps over it are then unused).
     const uint64_t arows = GATHER ? static_cast<uint64_t>(a.gather_T) : static_cast<uint64_t>(a.M);
-    if (!make_tensor_map_bf16(&mA, a.A, a.K, arows, BM) ||
-        !make_tensor_map_bf16(&mA32, a.A, a.K, arows, TOK_BOX_ROWS) ||
-        !make_tensor_map_bf16(&mB, a.B, bcols, static_cast<uint64_t>(a.E) * a.K, BK)) {
+    // FP8: activation codes [M, K] and blocked transposed weight codes (one 8 KB block per box).
+    const bool maps_ok =
+        FP8 ? make_tensor_map_u8(&mA, a.A, a.K, arows, BM) && make_tensor_map_u8(&mA32, a.A, a.K, arows, TOK_BOX_ROWS) &&
+                  make_tensor_map_w8(&mB, a.B, a.K, static_cast<uint64_t>(a.E) * bcols, 64)
+            : make_tensor_map_bf16(&mA, a.A, a.K, arows, BM) &&
+                  make_tensor_map_bf16(&mA32, a.A, a.K, arows, TOK_BOX_ROWS) &&
+                  make_tensor_map_bf16(&mB, a.B, bcols, static_cast<uint64_t>(a.E) * a.K, BK);
+    if (!maps_ok) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or bad operand)";
         return cudaErrorInvalidValue;
     }
@@ -902,24 +984,32 @@ cudaError_t launch_pair_kind(const GemmArgs& a, int num_sms, cudaStream_t s, con
     const int ksplit = KIND == 0 ? 1 : a.ksplit;
     const int swap_max = a.pair_swap_max < 0 ? 0 : (a.pair_swap_max > PAIR_SWAP_MAX_ROWS ? PAIR_SWAP_MAX_ROWS
                                                                                       : a.pair_swap_max);
-    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_2sm_kernel<KIND, SWAPCAP, GATHER>, dim3(grid),
-                    dim3(GATHER ? GATHER_THREADS : NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB, a.offsets, a.M, a.K, a.N, a.E, ksplit,
-                    swap_max, a.pair_layout, a.pair_split, reinterpret_cast<const int4*>(a.A), a.gather_src,
-                    a.gather_T, a.out, a.status);
+    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_2sm_kernel<KIND, SWAPCAP, GATHER, FP8>,
+                    dim3(grid), dim3(GATHER ? GATHER_THREADS : NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB, a.offsets,
+                    a.M, a.K, a.N, a.E, ksplit, swap_max, a.pair_layout, a.pair_split,
+                    reinterpret_cast<const int4*>(a.A), a.gather_src, a.gather_T, a.a_scale, a.b_scale, a.out,
+                    a.status);
 }
 
 }  // namespace
 
 cudaError_t launch_grouped_gemm_pair(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                      const char** why) {
+    if (a.fp8) {
+        if (kind == 1)
+            return a.pair == 2 ? launch_pair_kind<1, true, false, true>(a, num_sms, s, why)
+                               : launch_pair_kind<1, false, false, true>(a, num_sms, s, why);
+        return a.pair == 2 ? launch_pair_kind<0, true, false, true>(a, num_sms, s, why)
+                           : launch_pair_kind<0, false, false, true>(a, num_sms, s, why);
+    }
     if (kind == 1)
-        return a.pair == 2 ? launch_pair_kind<1, true, false>(a, num_sms, s, why)
-                           : launch_pair_kind<1, false, false>(a, num_sms, s, why);
+        return a.pair == 2 ? launch_pair_kind<1, true, false, false>(a, num_sms, s, why)
+                           : launch_pair_kind<1, false, false, false>(a, num_sms, s, why);
     if (a.gather_src)
-        return a.pair == 2 ? launch_pair_kind<0, true, true>(a, num_sms, s, why)
-                           : launch_pair_kind<0, false, true>(a, num_sms, s, why);
-    return a.pair == 2 ? launch_pair_kind<0, true, false>(a, num_sms, s, why)
-                       : launch_pair_kind<0, false, false>(a, num_sms, s, why);
+        return a.pair == 2 ? launch_pair_kind<0, true, true, false>(a, num_sms, s, why)
+                           : launch_pair_kind<0, false, true, false>(a, num_sms, s, why);
+    return a.pair == 2 ? launch_pair_kind<0, true, false, false>(a, num_sms, s, why)
+                       : launch_pair_kind<0, false, false, false>(a, num_sms, s, why);
 }
 
 }  // namespace moe

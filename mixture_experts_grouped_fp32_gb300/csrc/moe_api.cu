@@ -119,11 +119,18 @@ int swap_max_rows() {
 //     0.289 -> 0.340 ms);
 //   * otherwise the 1-SM kernel.
 // MOE_GEMM_2SM=0/1/2 overrides both GEMMs, MOE_GEMM_2SM_DOWN the down GEMM alone.
-int use_pair(long long M, int E, int N, int kind) {
+//
+// The FP8 layer (fp8 = true) follows the same rules for gate+up (Mixtral shape, T=512: 0.196 ms on
+// swapping pairs against 0.185 normal-only, but 0.183 against 0.209 with expert 0 drawing 40 % of
+// the assignments; T=4096: 0.684 against 0.728; DeepSeek-V3 shape: 0.638 against 0.753 on single
+// SMs); its down GEMM runs on normal-only pairs from 128 rows per expert and on single SMs below
+// (DeepSeek-V3 shape: 0.499 ms against 0.576 on swapping pairs).
+int use_pair(long long M, int E, int N, int kind, bool fp8 = false) {
     auto parse = [](const char* v) { return v[0] == '2' ? 2 : (v[0] == '1' ? 1 : 0); };
     if (kind == 1)
         if (const char* v = std::getenv("MOE_GEMM_2SM_DOWN")) return parse(v);
     if (const char* v = std::getenv("MOE_GEMM_2SM")) return parse(v);
+    if (fp8 && kind == 1) return M >= 128ll * E ? 1 : 0;
     if (M >= 128ll * E) return kind == 1 ? 1 : 2;
     const int super_cols = kind == 0 ? 256 : 512;
     if (M >= 32ll * E && static_cast<long long>(E) * ((N + super_cols - 1) / super_cols) >= 608) return 2;
@@ -193,14 +200,14 @@ int inject_stall() {
 // already saturate HBM, and a split only adds partial-sum traffic (T=32: 0.138 -> 0.142 ms);
 // above two waves the tail is small.  MOE_DOWN_KSPLIT overrides the choice.  The result never
 // leaves a slice without K blocks.
-// The FP8 layer (fp8 = true) runs the 1-SM kernel with 128-deep K blocks.
+// The FP8 layer (fp8 = true) has 128-deep K blocks.
 int down_ksplit(int T, int d, int f, int E, int k, bool fp8 = false) {
     const long long M = static_cast<long long>(T) * k;
     const int num_kb = f / (fp8 ? 128 : 64);
     int S;
     if (const char* v = std::getenv("MOE_DOWN_KSPLIT")) {
         S = std::atoi(v);
-    } else if (!fp8 && use_pair(M, E, d, 1)) {
+    } else if (use_pair(M, E, d, 1, fp8)) {
         S = 1;  // 256-row pair items: measured best unsplit (Mixtral T=512: 0.510 ms/layer vs 0.524 at 2)
     } else {
         const long long mtiles = (M + 127) / 128 + (M < E ? M : E);
@@ -347,8 +354,8 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
     return ok();
 }
 
-// The FP8 layer: route (+ permute), x rows gathered by src[] and quantised, gate+up FP8 GEMM
-// (+ SwiGLU, bf16 h), h quantised per row, down FP8 GEMM, combine.
+// The FP8 layer: route (+ permute, writing the x rows quantised), gate+up FP8 GEMM (+ SwiGLU,
+// bf16 h), h quantised per row, down FP8 GEMM, combine.
 int run_layer_fp8(const void* x, const float* logits, const void* wgu8, const float* sgu, const void* wd8,
                   const float* sd, int T, int d, int f, int E, int k, void* out, void* ws, int num_sms,
                   cudaStream_t s) {
@@ -369,21 +376,21 @@ int run_layer_fp8(const void* x, const float* logits, const void* wgu8, const fl
     const int M = T * k;
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
     cudaError_t e;
+    // The permutation writes the quantised x rows (x8, sx) directly.
     if (fuse_route_permute(T, E)) {
         if ((e = launch_route_permute(logits, xb, T, d, E, k, idx, w, counts, offsets, src, dest, nullptr, status,
-                                      num_sms, s)) != cudaSuccess)
+                                      num_sms, s, x8, sx)) != cudaSuccess)
             return launched(e, "route+permute");
     } else {
         if ((e = launch_route(logits, T, E, k, idx, w, status, s)) != cudaSuccess) return launched(e, "route");
-        if ((e = launch_permute(idx, xb, T, d, E, k, counts, offsets, src, dest, nullptr, status, num_sms, s)) !=
-            cudaSuccess)
+        if ((e = launch_permute(idx, xb, T, d, E, k, counts, offsets, src, dest, nullptr, status, num_sms, s, x8,
+                                sx)) != cudaSuccess)
             return launched(e, "permute");
     }
-    if ((e = launch_quantize_rows_fp8(xb, src, M, d, T, x8, sx, status, s)) != cudaSuccess)
-        return launched(e, "quantize x");
     const char* why = "";
     const int ksplit = down_ksplit(T, d, f, E, k, true);
-    GemmArgs g1{x8, wgu8, offsets, M, d, f, E, h, status, 1, swap_max_rows(), 0};
+    GemmArgs g1{x8, wgu8, offsets, M, d, f, E, h, status, 1, swap_max_rows(), use_pair(M, E, f, 0, true),
+                pair_swap_max_rows(), pair_layout(), pair_split()};
     g1.fp8 = true;
     g1.a_scale = sx;
     g1.b_scale = sgu;
@@ -391,7 +398,8 @@ int run_layer_fp8(const void* x, const float* logits, const void* wgu8, const fl
         return fail(MOE_ERR_CUDA, "FP8 gate+up GEMM: %s (%s)", why, cudaGetErrorString(e));
     if ((e = launch_quantize_rows_fp8(h, nullptr, M, f, M, h8, sh, status, s)) != cudaSuccess)
         return launched(e, "quantize h");
-    GemmArgs g2{h8, wd8, offsets, M, f, d, E, y, status, ksplit, swap_max_rows(), 0};
+    GemmArgs g2{h8, wd8, offsets, M, f, d, E, y, status, ksplit, swap_max_rows(), use_pair(M, E, d, 1, true),
+                pair_swap_max_rows(), pair_layout(), pair_split()};
     g2.fp8 = true;
     g2.a_scale = sh;
     g2.b_scale = sd;
@@ -738,10 +746,33 @@ int moe_down_ksplit_fp8(int T, int d, int f, int E, int top_k) {
     return down_ksplit(T, d, f, E, top_k, true);
 }
 
+int moe_gemm_pair_mode_fp8(int T, int d, int f, int E, int top_k, int kind) {
+    if (check_shape_fp8(T, d, f, E, top_k, "moe_gemm_pair_mode_fp8") != MOE_OK || (kind != 0 && kind != 1)) return -1;
+    return use_pair(static_cast<long long>(T) * top_k, E, kind == 0 ? f : d, kind, true);
+}
+
 int moe_forward_fp8_launch_count(int T, int E, int top_k) {
     if (check_shape(T, -1, 0, E, top_k, false) != MOE_OK) return -1;
     if (T == 0) return 0;
-    return fuse_route_permute(T, E) ? 6 : 7;
+    return fuse_route_permute(T, E) ? 5 : 6;
+}
+
+int moe_permute_fp8(const int32_t* idx, const void* x, int T, int d, int E, int top_k, int32_t* counts,
+                    int32_t* offsets, int32_t* src, int32_t* dest, void* x8_perm, float* sx, int32_t* status,
+                    moe_stream_t stream) {
+    int rc = check_shape(T, d, 0, E, top_k, false);
+    if (rc) return rc;
+    if (T == 0) return ok();
+    if (!idx || !x || !counts || !offsets || !src || !dest || !x8_perm || !sx)
+        return fail(MOE_ERR_INVALID_ARG, "moe_permute_fp8: null pointer");
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(x8_perm) & 7u) || (reinterpret_cast<uintptr_t>(sx) & 3u))
+        return fail(MOE_ERR_INVALID_ARG, "moe_permute_fp8: x must be 16-byte, x8_perm 8-byte, sx 4-byte aligned");
+    int sms;
+    if ((rc = check_device(&sms))) return rc;
+    return launched(launch_permute(idx, static_cast<const __nv_bfloat16*>(x), T, d, E, top_k, counts, offsets, src,
+                                   dest, nullptr, status, sms, static_cast<cudaStream_t>(stream),
+                                   static_cast<uint8_t*>(x8_perm), sx),
+                    "permute");
 }
 
 int moe_quantize_weights_fp8(const void* W, int E, int K, int N, void* Wq, float* scale, moe_stream_t stream) {
@@ -792,8 +823,12 @@ static int gemm8_entry(int kind, const void* A, const float* sa, const void* B, 
         return fail(MOE_ERR_INVALID_ARG, "%s: scales must be 4-byte aligned", name);
     int sms;
     if ((rc = check_device(&sms))) return rc;
-    GemmArgs g = kind == 0 ? GemmArgs{A, B, offsets, M, d, f, E, out, status, 1, swap_max_rows(), 0}
-                           : GemmArgs{A, B, offsets, M, f, d, E, out, status, ksplit, swap_max_rows(), 0};
+    const int pair = use_pair(M, E, kind == 0 ? f : d, kind, true);
+    GemmArgs g = kind == 0 ? GemmArgs{A, B, offsets, M, d, f, E, out, status, 1, swap_max_rows(), pair}
+                           : GemmArgs{A, B, offsets, M, f, d, E, out, status, ksplit, swap_max_rows(), pair};
+    g.pair_swap_max = pair_swap_max_rows();
+    g.pair_layout = pair_layout();
+    g.pair_split = pair_split();
     g.fp8 = true;
     g.a_scale = sa;
     g.b_scale = sb;

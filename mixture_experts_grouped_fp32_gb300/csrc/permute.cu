@@ -11,6 +11,7 @@
 // assignments, writes src/dest, and copies its tokens' x rows to their k destinations with
 // 16-byte vector loads and stores.
 #include "common.cuh"
+#include "fp8.cuh"
 
 namespace moe {
 namespace {
@@ -22,12 +23,57 @@ constexpr int kMaxTokPerBlock = 16;
 constexpr int kCopyBatch = 4;
 constexpr long long kFuseMaxLogits = 8192;  // route+permute fusion: T*E at most this
 
+// FP8 layer: instead of copying x rows, quantise each of the chunk's tokens once (absmax over its d
+// values, fp8.cuh's per-row arithmetic) and write its codes and scale to each of its k permuted
+// rows (rows < 0, from an invalid expert id, are skipped).  The block splits into 1, 2, 4 or 8
+// teams, one token per team at a time, so a block with a single token still spreads its row over
+// all 256 threads: a pass for the absmax (team reduction through shared memory), a second (from
+// L1) for the codes.  Called by every thread of the block.
+__device__ __forceinline__ void quantize_perm_rows(const uint4* __restrict__ x, int t0, int t1, int d, int k,
+                                                   const int* crow, uint2* __restrict__ x8, float* __restrict__ sx,
+                                                   float* red) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ntok = t1 - t0, dv = d / 8;
+    int teams = 1;
+    while (teams < ntok && teams < kPermThreads / 32) teams <<= 1;
+    const int team_threads = kPermThreads / teams, team = tid / team_threads, tt = tid % team_threads;
+    const int wpt = team_threads / 32;  // warps per team
+    for (int base = 0; base < ntok; base += teams) {  // uniform trip count: every thread reaches the barriers
+        const int tl = base + team;
+        const uint4* row = x + static_cast<size_t>(t0 + (tl < ntok ? tl : 0)) * dv;
+        float m = 0.0f;
+        if (tl < ntok)
+            for (int v = tt; v < dv; v += team_threads) m = fmaxf(m, absmax8(__ldg(row + v)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) red[warp] = m;
+        __syncthreads();
+        m = 0.0f;
+        for (int i = 0; i < wpt; ++i) m = fmaxf(m, red[team * wpt + i]);
+        if (tl < ntok) {
+            const float inv = fp8_inv(m);
+            if (tt < k) {
+                const int r = crow[tl * k + tt];
+                if (r >= 0) sx[r] = fp8_scale(m);
+            }
+            for (int v = tt; v < dv; v += team_threads) {
+                const uint2 c = codes8(__ldg(row + v), inv);
+                for (int j = 0; j < k; ++j) {
+                    const int r = crow[tl * k + j];
+                    if (r >= 0) x8[static_cast<size_t>(r) * dv + v] = c;
+                }
+            }
+        }
+        __syncthreads();  // red is rewritten next round
+    }
+}
+
 __global__ void __launch_bounds__(kPermThreads)
 permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int T, int d, int E,
                int k, int tok_per_block, int32_t* __restrict__ counts,
                int32_t* __restrict__ offsets, int32_t* __restrict__ src,
-               int32_t* __restrict__ dest, uint4* __restrict__ x_perm,
-               int32_t* __restrict__ status) {
+               int32_t* __restrict__ dest, uint4* __restrict__ x_perm, uint2* __restrict__ x8,
+               float* __restrict__ sx, int32_t* __restrict__ status) {
     __shared__ int tot[kMaxE];      // assignments per expert, all tokens
     __shared__ int before[kMaxE];   // ... from tokens before this block's chunk
     __shared__ int off[kMaxE + 1];  // exclusive scan of tot
@@ -144,6 +190,11 @@ permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int
     __syncthreads();
     if (bad && tid == 0) flag_status(status, MOE_STATUS_BAD_EXPERT_ID);
 
+    if (x8 != nullptr) {
+        __shared__ float red[kPermThreads / 32];
+        quantize_perm_rows(x, t0, t1, d, k, crow, x8, sx, red);
+        return;
+    }
     // Row copies: x[t] -> x_perm[row(t, j)] for each slot j, 16 bytes per access.  Each thread
     // first issues kCopyBatch independent loads, then their k stores each, so that enough reads
     // are in flight to cover the memory latency.
@@ -194,7 +245,8 @@ __global__ void __launch_bounds__(kPermThreads)
 route_permute_kernel(const float* __restrict__ logits, const uint4* __restrict__ x, int T, int d, int E, int k,
                      int tok_per_block, int32_t* __restrict__ idx, float* __restrict__ w,
                      int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ src,
-                     int32_t* __restrict__ dest, uint4* __restrict__ x_perm, int32_t* __restrict__ status) {
+                     int32_t* __restrict__ dest, uint4* __restrict__ x_perm, uint2* __restrict__ x8,
+                     float* __restrict__ sx, int32_t* __restrict__ status) {
     __shared__ int tot[kFuseMaxE];
     __shared__ int before[kFuseMaxE];
     __shared__ int off[kFuseMaxE + 1];
@@ -304,6 +356,11 @@ route_permute_kernel(const float* __restrict__ logits, const uint4* __restrict__
         crow[tid] = row;
     }
     __syncthreads();
+    if (x8 != nullptr) {
+        __shared__ float red[kPermThreads / 32];
+        quantize_perm_rows(x, t0, t1, d, k, crow, x8, sx, red);
+        return;
+    }
     if (x_perm == nullptr) return;  // the gate+up GEMM gathers x rows itself
     const int dv = d / 8;
     const int nvec = (t1 - t0) * dv;
@@ -337,25 +394,26 @@ bool route_permute_fusable(int T, int E) {
 cudaError_t launch_route_permute(const float* logits, const __nv_bfloat16* x, int T, int d, int E, int k,
                                  int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* src,
                                  int32_t* dest, __nv_bfloat16* x_perm, int32_t* status, int num_sms,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, uint8_t* x8, float* sx) {
     int tpb = (T + 4 * num_sms - 1) / (4 * num_sms);
     tpb = tpb < 1 ? 1 : (tpb > kMaxTokPerBlock ? kMaxTokPerBlock : tpb);
     const int blocks = (T + tpb - 1) / tpb;
     return launch_k(kPdlRoute, route_permute_kernel, dim3(blocks), dim3(kPermThreads), 0, s, logits,
                     reinterpret_cast<const uint4*>(x), T, d, E, k, tpb, idx, w, counts, offsets, src, dest,
-                    reinterpret_cast<uint4*>(x_perm), status);
+                    reinterpret_cast<uint4*>(x_perm), reinterpret_cast<uint2*>(x8), sx, status);
 }
 
 cudaError_t launch_permute(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
                            int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest,
-                           __nv_bfloat16* x_perm, int32_t* status, int num_sms, cudaStream_t s) {
+                           __nv_bfloat16* x_perm, int32_t* status, int num_sms, cudaStream_t s, uint8_t* x8,
+                           float* sx) {
     // About four blocks per SM for the row copies, at most kMaxTokPerBlock tokens per block.
     int tpb = (T + 4 * num_sms - 1) / (4 * num_sms);
     tpb = tpb < 1 ? 1 : (tpb > kMaxTokPerBlock ? kMaxTokPerBlock : tpb);
     const int blocks = (T + tpb - 1) / tpb;
     return launch_k(kPdlPermute, permute_kernel, dim3(blocks), dim3(kPermThreads), 0, s, idx,
                     reinterpret_cast<const uint4*>(x), T, d, E, k, tpb, counts, offsets, src, dest,
-                    reinterpret_cast<uint4*>(x_perm), status);
+                    reinterpret_cast<uint4*>(x_perm), reinterpret_cast<uint2*>(x8), sx, status);
 }
 
 }  // namespace moe

@@ -42,12 +42,14 @@ _SIGS = {
     "moe_forward_host": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "moe_get_device_error": ([_P, ctypes.POINTER(ctypes.c_int32)], _I),
     "moe_quantize_weights_fp8": ([_P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_permute_fp8": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_quantize_rows_fp8": ([_P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_gateup_swiglu_fp8": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gemm_down_fp8": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_workspace_size_fp8": ([_I, _I, _I, _I, _I], _SZ),
     "moe_workspace_layout_fp8": ([_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _I),
     "moe_down_ksplit_fp8": ([_I, _I, _I, _I, _I], _I),
+    "moe_gemm_pair_mode_fp8": ([_I, _I, _I, _I, _I, _I], _I),
     "moe_forward_fp8_launch_count": ([_I, _I, _I], _I),
     "moe_forward_fp8": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
 }
@@ -359,14 +361,62 @@ class MoELayer:
 # FP8 (E4M3) variant: codes are torch.uint8 tensors, scales float32.
 # ---------------------------------------------------------------------------------------------
 def quantize_weights_fp8(W: torch.Tensor, stream=None, out: tuple | None = None):
-    """W [E, K, N] bf16 -> (Wq [E, N, K] uint8 E4M3 codes, scale [E, N] fp32): one scale per output
-    column (absmax over K / 448)."""
+    """W [E, K, N] bf16 -> (Wq uint8 E4M3 codes [E, N/64, K/128, 64, 128], scale [E, N] fp32): the
+    transposed codes in 8 KB blocks of 64 output columns x 128 K (see ``fp8_unblock``), one scale
+    per output column (absmax over K / 448)."""
     _dev(W, torch.bfloat16, "W")
     E, K, N = W.shape
-    Wq, scale = out if out is not None else (torch.empty(E, N, K, dtype=torch.uint8, device=W.device),
-                                             torch.empty(E, N, dtype=torch.float32, device=W.device))
+    Wq, scale = out if out is not None else (
+        torch.empty(E, N // 64, K // 128, 64, 128, dtype=torch.uint8, device=W.device),
+        torch.empty(E, N, dtype=torch.float32, device=W.device))
     _call("moe_quantize_weights_fp8", _ptr(W), E, K, N, _ptr(Wq), _ptr(scale), _stream(stream))
     return Wq, scale
+
+
+def _w8_dims(w8: torch.Tensor, name: str):
+    """(E, N, K) of blocked FP8 weight codes [E, N/64, K/128, 64, 128]."""
+    _dev(w8, torch.uint8, name)
+    if w8.dim() != 5 or w8.shape[3:] != (64, 128):
+        raise ValueError(f"{name} must be blocked FP8 codes [E, N/64, K/128, 64, 128], got {tuple(w8.shape)}")
+    return w8.shape[0], w8.shape[1] * 64, w8.shape[2] * 128
+
+
+def fp8_unblock(w8):
+    """Blocked codes [E, N/64, K/128, 64, 128] (tensor or array) -> [E, N, K] (index work only)."""
+    E, G, B = w8.shape[:3]
+    return w8.transpose(2, 3).reshape(E, G * 64, B * 128) if isinstance(w8, torch.Tensor) else \
+        w8.transpose(0, 1, 3, 2, 4).reshape(E, G * 64, B * 128)
+
+
+def fp8_block(w):
+    """[E, N, K] codes (tensor or array) -> the blocked layout [E, N/64, K/128, 64, 128]."""
+    E, N, K = w.shape
+    v = w.reshape(E, N // 64, 64, K // 128, 128)
+    return v.transpose(2, 3).contiguous() if isinstance(w, torch.Tensor) else \
+        v.transpose(0, 1, 3, 2, 4).copy()
+
+
+def permute_fp8(idx: torch.Tensor, x: torch.Tensor, E: int, status: torch.Tensor | None = None, stream=None,
+                out: tuple | None = None):
+    """Step 2 of the FP8 layer: returns (counts, offsets, src, dest, x8_perm, sx) with x8_perm [T*k, d]
+    uint8 E4M3 codes and sx [T*k] fp32; ``out`` may supply those six buffers."""
+    _dev(idx, torch.int32, "idx")
+    _dev(x, torch.bfloat16, "x")
+    T, k = idx.shape
+    d = x.shape[1]
+    dev = x.device
+    if out is not None:
+        counts, offsets, src, dest, x8, sx = out
+    else:
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+        offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        src = torch.empty(T * k, dtype=torch.int32, device=dev)
+        dest = torch.empty(T, k, dtype=torch.int32, device=dev)
+        x8 = torch.empty(T * k, d, dtype=torch.uint8, device=dev)
+        sx = torch.empty(T * k, dtype=torch.float32, device=dev)
+    _call("moe_permute_fp8", _ptr(idx), _ptr(x), T, d, E, k, _ptr(counts), _ptr(offsets), _ptr(src), _ptr(dest),
+          _ptr(x8), _ptr(sx), _ptr(status), _stream(stream))
+    return counts, offsets, src, dest, x8, sx
 
 
 def quantize_rows_fp8(a: torch.Tensor, src: torch.Tensor | None = None, status=None, stream=None,
@@ -389,11 +439,10 @@ def grouped_gemm_gateup_swiglu_fp8(x8_perm, sx, w8_gate_up, s_gate_up, offsets, 
     """Step 3 on E4M3 codes: x8_perm [M, d] uint8 + sx [M]; w8_gate_up [E, 2f, d] uint8 + s_gate_up [E, 2f]."""
     _dev(x8_perm, torch.uint8, "x8_perm")
     _dev(sx, torch.float32, "sx")
-    _dev(w8_gate_up, torch.uint8, "w8_gate_up")
     _dev(s_gate_up, torch.float32, "s_gate_up")
     _dev(offsets, torch.int32, "offsets")
     M, d = x8_perm.shape
-    E, f2, _ = w8_gate_up.shape
+    E, f2, _ = _w8_dims(w8_gate_up, "w8_gate_up")
     h = h if h is not None else torch.empty(M, f2 // 2, dtype=torch.bfloat16, device=x8_perm.device)
     _call("moe_grouped_gemm_gateup_swiglu_fp8", _ptr(x8_perm), _ptr(sx), _ptr(w8_gate_up), _ptr(s_gate_up),
           _ptr(offsets), M, d, f2 // 2, E, _ptr(h), _ptr(status), _stream(stream))
@@ -404,11 +453,10 @@ def grouped_gemm_down_fp8(h8, sh, w8_down, s_down, offsets, y_perm=None, status=
     """Step 4 on E4M3 codes: h8 [M, f] uint8 + sh [M]; w8_down [E, d, f] uint8 + s_down [E, d]."""
     _dev(h8, torch.uint8, "h8")
     _dev(sh, torch.float32, "sh")
-    _dev(w8_down, torch.uint8, "w8_down")
     _dev(s_down, torch.float32, "s_down")
     _dev(offsets, torch.int32, "offsets")
     M, f = h8.shape
-    E, d, _ = w8_down.shape
+    E, d, _ = _w8_dims(w8_down, "w8_down")
     if y_perm is None:
         y_perm = torch.empty(ksplit, M, d, dtype=torch.float32, device=h8.device)
         if ksplit == 1:
@@ -434,8 +482,13 @@ def down_ksplit_fp8(T: int, d: int, f: int, E: int, top_k: int) -> int:
     return int(load().moe_down_ksplit_fp8(T, d, f, E, top_k))
 
 
+def gemm_pair_mode_fp8(T: int, d: int, f: int, E: int, top_k: int, kind: int = 0) -> int:
+    """As gemm_pair_mode, for moe_forward_fp8's grouped GEMMs."""
+    return int(load().moe_gemm_pair_mode_fp8(T, d, f, E, top_k, kind))
+
+
 def forward_fp8_launch_count(T: int, E: int, top_k: int) -> int:
-    """Kernel launches of one moe_forward_fp8 call (6 with route+permute fused, else 7)."""
+    """Kernel launches of one moe_forward_fp8 call (5 with route+permute fused, else 6)."""
     return int(load().moe_forward_fp8_launch_count(T, E, top_k))
 
 
@@ -444,12 +497,11 @@ def forward_fp8(x, logits, w8_gate_up, s_gate_up, w8_down, s_down, top_k, out=No
     and w_down [E, f, d].  Returns ``out`` bf16 [T, d]."""
     _dev(x, torch.bfloat16, "x")
     _dev(logits, torch.float32, "logits")
-    _dev(w8_gate_up, torch.uint8, "w8_gate_up")
     _dev(s_gate_up, torch.float32, "s_gate_up")
-    _dev(w8_down, torch.uint8, "w8_down")
     _dev(s_down, torch.float32, "s_down")
     T, d = x.shape
-    E, f2, _ = w8_gate_up.shape
+    E, f2, _ = _w8_dims(w8_gate_up, "w8_gate_up")
+    _w8_dims(w8_down, "w8_down")
     if workspace is None:
         workspace = torch.empty(workspace_size_fp8(T, d, f2 // 2, E, top_k), dtype=torch.uint8, device=x.device)
     out = out if out is not None else torch.empty(T, d, dtype=torch.bfloat16, device=x.device)

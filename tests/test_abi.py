@@ -232,8 +232,8 @@ def test_fp8_workspace_layout_and_validation(lib):
     assert L == expect
     assert moe.workspace_size_fp8(T, d, f, E, k) == o
     assert moe.workspace_size_fp8(T, 192, f, E, k) == 0       # d not a multiple of 128
-    assert lib.moe_forward_fp8_launch_count(32, 8, 2) == 6
-    assert lib.moe_forward_fp8_launch_count(2048, 256, 8) == 7
+    assert lib.moe_forward_fp8_launch_count(32, 8, 2) == 5
+    assert lib.moe_forward_fp8_launch_count(2048, 256, 8) == 6
     assert lib.moe_forward_fp8_launch_count(0, 8, 2) == 0
     p = ctypes.c_void_p(1 << 20)
     assert lib.moe_forward_fp8(p, p, p, p, p, p, 4, 192, 256, 8, 2, p, p, 1 << 40, None) == -1
@@ -249,3 +249,32 @@ def test_fp8_workspace_layout_and_validation(lib):
     assert lib.moe_grouped_gemm_gateup_swiglu_fp8(p, None, p, p, p, 8, 256, 256, 8, p, None, None) == -1
     assert lib.moe_grouped_gemm_down_fp8(p, p, p, p, p, 8, 256, 256, 8, 9, p, None, None) == -1
     assert lib.moe_grouped_gemm_down_fp8(p, p, p, p, p, 0, 256, 256, 8, 1, p, None, None) == 0
+
+
+def test_fp8_block_layout_round_trip():
+    """The blocked FP8 weight layout helpers are inverse index permutations, and the block of
+    (n, k) is at [n // 64][k // 128][n % 64][k % 128]."""
+    import numpy as np
+    import torch
+    from mixture_experts_grouped_fp32_gb300.moe import fp8_block, fp8_unblock
+    a = np.random.default_rng(0).integers(0, 255, (3, 192, 256), dtype=np.uint8)
+    b = fp8_block(a)
+    assert b.shape == (3, 3, 2, 64, 128)
+    assert np.array_equal(fp8_unblock(b), a)
+    for e, n, k in [(0, 0, 0), (1, 65, 130), (2, 191, 255)]:
+        assert b[e, n // 64, k // 128, n % 64, k % 128] == a[e, n, k]
+    t = torch.from_numpy(a)
+    assert torch.equal(fp8_unblock(fp8_block(t)), t)
+    assert np.array_equal(fp8_block(t).numpy(), b)
+
+
+def test_gemm_pair_mode_fp8_policy(lib):
+    for v in ("MOE_GEMM_2SM", "MOE_GEMM_2SM_DOWN"):
+        os.environ.pop(v, None)
+    f = lib.moe_gemm_pair_mode_fp8
+    assert f(32, 4096, 14336, 8, 2, 0) == 0 and f(32, 4096, 14336, 8, 2, 1) == 0       # Mixtral, T=32
+    assert f(512, 4096, 14336, 8, 2, 0) == 2 and f(512, 4096, 14336, 8, 2, 1) == 1     # 128 rows per expert
+    assert f(4096, 4096, 14336, 8, 2, 0) == 2 and f(4096, 4096, 14336, 8, 2, 1) == 1   # 1024 rows per expert
+    assert f(2048, 7168, 2048, 256, 8, 0) == 2 and f(2048, 7168, 2048, 256, 8, 1) == 0  # DeepSeek-V3 shape
+    assert f(256, 7168, 2048, 32, 8, 0) == 0 and f(256, 7168, 2048, 32, 8, 1) == 0     # 32 experts
+    assert f(32, 4096, 14336, 8, 2, 2) == -1 and f(32, 4000, 14336, 8, 2, 0) == -1

@@ -25,7 +25,21 @@ from mixture_experts_grouped_fp32_gb300.workloads import (WORKLOADS, Workload, d
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-KNOBS = ("MOE_GEMM_SWAP_MAX", "MOE_DOWN_KSPLIT", "MOE_FUSE_ROUTE_PERMUTE")
+KNOBS = ("MOE_GEMM_SWAP_MAX", "MOE_DOWN_KSPLIT", "MOE_FUSE_ROUTE_PERMUTE", "MOE_GEMM_2SM", "MOE_GEMM_2SM_DOWN",
+         "MOE_GEMM_PAIR_LAYOUT", "MOE_GEMM_PAIR_SPLIT", "MOE_GEMM_PAIR_SWAP_MAX")
+# Grouped-GEMM kernel configurations: the 1-SM kernel (swap thresholds 64, 0, 128) and the SM-pair
+# kernel (normal-only; swapping with either shared-memory layout, round-robin or split schedule).
+GEMM_MODES = {
+    "1sm": {"MOE_GEMM_2SM": "0"},
+    "1sm_noswap": {"MOE_GEMM_2SM": "0", "MOE_GEMM_SWAP_MAX": "0"},
+    "1sm_swap128": {"MOE_GEMM_2SM": "0", "MOE_GEMM_SWAP_MAX": "128"},
+    "pair1": {"MOE_GEMM_2SM": "1"},
+    "pair2": {"MOE_GEMM_2SM": "2"},
+    "pair2_A": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_LAYOUT": "A", "MOE_GEMM_PAIR_SPLIT": "0"},
+    "pair2_B": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_LAYOUT": "B", "MOE_GEMM_PAIR_SPLIT": "0"},
+    "pair2_split": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_SPLIT": "30"},
+    "pair2_swap64": {"MOE_GEMM_2SM": "2", "MOE_GEMM_PAIR_SWAP_MAX": "64"},
+}
 
 
 @pytest.fixture(scope="module")
@@ -39,6 +53,17 @@ def moe():
 def _clean_env(monkeypatch):
     for k in KNOBS:
         monkeypatch.delenv(k, raising=False)
+
+
+def w8(a: np.ndarray) -> torch.Tensor:
+    """[E, N, K] codes -> the library's blocked weight layout, on the GPU."""
+    from mixture_experts_grouped_fp32_gb300.moe import fp8_block
+    return u8(fp8_block(a))
+
+
+def unblock(t: torch.Tensor) -> np.ndarray:
+    from mixture_experts_grouped_fp32_gb300.moe import fp8_unblock
+    return fp8_unblock(t.cpu().numpy())
 
 
 def u8(a: np.ndarray) -> torch.Tensor:
@@ -73,7 +98,7 @@ def test_quantize_weights_fp8_bit_exact(moe, oracle, E, K, N):
     q, sc = moe.quantize_weights_fp8(Wt)
     torch.cuda.synchronize()
     rq, rsc = oracle.quantize_weights_fp8(bits)
-    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(unblock(q), rq)
     assert np.array_equal(sc.cpu().numpy().view(np.uint32), rsc.view(np.uint32))
 
 
@@ -110,6 +135,29 @@ def test_quantize_rows_fp8_bad_src(moe, oracle):
     assert np.array_equal(q[[0, 1, 4]], rq) and np.array_equal(sc[[0, 1, 4]], rsc)
 
 
+@pytest.mark.parametrize("T,d,E,k", [(1, 256, 8, 2), (300, 256, 8, 2), (2000, 4096, 64, 6), (77, 7168, 16, 4)])
+def test_permute_fp8_parity(moe, oracle, T, d, E, k):
+    """Step 2 of the FP8 layer: the permutation bit for bit, and each permuted row's codes and
+    scale equal to the oracle's quantisation of x[src[r]]."""
+    g = torch.Generator("cpu").manual_seed(T + d)
+    logits = torch.randn(T, E, generator=g)
+    idx, _ = oracle.route(logits.numpy(), k)
+    bits = to_np_bits(random_bf16((T, d), seed=T * 3 + E))
+    if T >= 5:
+        bits = special_rows(bits)
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    counts, offsets, src, dest, x8, sx = moe.permute_fp8(torch.from_numpy(idx).to(DEV), x, E, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rc, ro, rs, rd = oracle.permute(idx, E)
+    assert np.array_equal(counts.cpu().numpy(), rc) and np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(src.cpu().numpy(), rs) and np.array_equal(dest.cpu().numpy(), rd)
+    rq, rsc = oracle.quantize_rows_fp8(bits[rs])
+    assert np.array_equal(x8.cpu().numpy(), rq)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), rsc.view(np.uint32))
+
+
 def segments(counts):
     offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     return offsets
@@ -123,23 +171,24 @@ GEMM_CASES = [  # (counts per expert, d, f); rows beyond offsets[E] exist in the
 ]
 
 
-@pytest.mark.parametrize("swap_max", ["64", "0", "128"])
+@pytest.mark.parametrize("mode", sorted(GEMM_MODES))
 @pytest.mark.parametrize("ci", range(len(GEMM_CASES)))
-def test_gemm_fp8_parity(moe, oracle, monkeypatch, ci, swap_max):
-    monkeypatch.setenv("MOE_GEMM_SWAP_MAX", swap_max)
+def test_gemm_fp8_parity(moe, oracle, monkeypatch, ci, mode):
+    for k, v in GEMM_MODES[mode].items():
+        monkeypatch.setenv(k, v)
     counts, d, f = GEMM_CASES[ci]
     E = len(counts)
     offsets = segments(counts)
     M = int(offsets[-1]) + 3
-    seed = 100 * ci + int(swap_max)
+    seed = 100 * ci + sorted(GEMM_MODES).index(mode)
     x8, sx = draw_e4m3_codes((M, d), seed), draw_scales(M, seed + 1)
     wgu8, sgu = draw_e4m3_codes((E, 2 * f, d), seed + 2), draw_scales((E, 2 * f), seed + 3)
     h8, sh = draw_e4m3_codes((M, f), seed + 4), draw_scales(M, seed + 5)
     wd8, sd = draw_e4m3_codes((E, d, f), seed + 6), draw_scales((E, d), seed + 7)
     off_t = torch.from_numpy(offsets).to(DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    h = moe.grouped_gemm_gateup_swiglu_fp8(u8(x8), f32(sx), u8(wgu8), f32(sgu), off_t, status=status)
-    y = moe.grouped_gemm_down_fp8(u8(h8), f32(sh), u8(wd8), f32(sd), off_t, status=status)
+    h = moe.grouped_gemm_gateup_swiglu_fp8(u8(x8), f32(sx), w8(wgu8), f32(sgu), off_t, status=status)
+    y = moe.grouped_gemm_down_fp8(u8(h8), f32(sh), w8(wd8), f32(sd), off_t, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     n = int(offsets[-1])
@@ -151,15 +200,18 @@ def test_gemm_fp8_parity(moe, oracle, monkeypatch, ci, swap_max):
     assert_close(y.cpu().numpy()[:n], ref_y[:n], 1e-3, 1e-4, "fp8 down y")
 
 
+@pytest.mark.parametrize("mode", ["1sm", "pair1", "pair2"])
 @pytest.mark.parametrize("ksplit", [2, 3])
-def test_gemm_down_fp8_ksplit(moe, oracle, ksplit):
+def test_gemm_down_fp8_ksplit(moe, oracle, monkeypatch, ksplit, mode):
+    for k, v in GEMM_MODES[mode].items():
+        monkeypatch.setenv(k, v)
     counts, d, f = [40, 300, 0, 77], 256, 640  # f = 5 blocks of 128: ksplit 3 leaves slices of 2, 2, 1
     E = len(counts)
     offsets = segments(counts)
     M = int(offsets[-1])
     h8, sh = draw_e4m3_codes((M, f), 11), draw_scales(M, 12)
     wd8, sd = draw_e4m3_codes((E, d, f), 13), draw_scales((E, d), 14)
-    y = moe.grouped_gemm_down_fp8(u8(h8), f32(sh), u8(wd8), f32(sd), torch.from_numpy(offsets).to(DEV),
+    y = moe.grouped_gemm_down_fp8(u8(h8), f32(sh), w8(wd8), f32(sd), torch.from_numpy(offsets).to(DEV),
                                   ksplit=ksplit)
     torch.cuda.synchronize()
     ref_y = oracle.down_fp8(h8, sh, offsets, wd8, sd)
@@ -183,15 +235,18 @@ def quantized_weights(moe, oracle, wgu, wd):
     wd8, sd = moe.quantize_weights_fp8(wd.to(DEV))
     r = oracle.quantize_weights_fp8(to_np_bits(wgu)) + oracle.quantize_weights_fp8(to_np_bits(wd))
     torch.cuda.synchronize()
-    assert np.array_equal(wgu8.cpu().numpy(), r[0]) and np.array_equal(sgu.cpu().numpy(), r[1])
-    assert np.array_equal(wd8.cpu().numpy(), r[2]) and np.array_equal(sd.cpu().numpy(), r[3])
+    assert np.array_equal(unblock(wgu8), r[0]) and np.array_equal(sgu.cpu().numpy(), r[1])
+    assert np.array_equal(unblock(wd8), r[2]) and np.array_equal(sd.cpu().numpy(), r[3])
     return (wgu8, sgu, wd8, sd), r
 
 
-@pytest.mark.parametrize("mode", ["default", "noswap", "ksplit3", "nofuse"])
+@pytest.mark.parametrize("mode", ["default", "noswap", "ksplit3", "nofuse", "pair1", "pair2"])
 @pytest.mark.parametrize("w", LAYER_CASES, ids=lambda w: w.name)
 def test_forward_fp8_matches_oracle(moe, oracle, monkeypatch, w, mode):
-    if mode == "noswap":
+    if mode in GEMM_MODES:
+        for k, v in GEMM_MODES[mode].items():
+            monkeypatch.setenv(k, v)
+    elif mode == "noswap":
         monkeypatch.setenv("MOE_GEMM_SWAP_MAX", "0")
     elif mode == "ksplit3":
         monkeypatch.setenv("MOE_DOWN_KSPLIT", "3")
@@ -221,18 +276,25 @@ def test_forward_fp8_matches_oracle(moe, oracle, monkeypatch, w, mode):
 
 
 def test_forward_fp8_launch_count(moe):
-    assert moe.forward_fp8_launch_count(64, 8, 2) == 6
-    assert moe.forward_fp8_launch_count(2048, 256, 8) == 7
+    assert moe.forward_fp8_launch_count(64, 8, 2) == 5
+    assert moe.forward_fp8_launch_count(2048, 256, 8) == 6
     assert moe.forward_fp8_launch_count(0, 8, 2) == 0
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["mixtral_t512", "mixtral_t4096", "deepseek_t2048"])
-def test_forward_fp8_full_size(moe, oracle, name):
-    """The FP8 layer at full size in the configuration bench.py times: the weight codes and scales
-    bit for bit against the oracle's quantiser, routing, permutation and x codes bit for bit, the
-    output on sampled tokens that the oracle computes one by one."""
+@pytest.mark.parametrize("path", ["policy", "other"])
+@pytest.mark.parametrize("name", ["mixtral_t32", "mixtral_t512", "mixtral_t4096", "deepseek_t2048"])
+def test_forward_fp8_full_size(moe, oracle, monkeypatch, name, path):
+    """The FP8 layer at full size in the configuration bench.py times (`policy`), and with another
+    grouped-GEMM kernel forced (`other`: single SMs -> swapping SM pairs -> normal-only SM pairs ->
+    single SMs): the weight codes and scales bit for bit against the oracle's quantiser, routing,
+    permutation and x codes bit for bit, the output on sampled tokens that the oracle computes one
+    by one."""
     w = WORKLOADS[name]
+    if path == "other":
+        rot = {0: "2", 2: "1", 1: "0"}
+        monkeypatch.setenv("MOE_GEMM_2SM", rot[moe.gemm_pair_mode_fp8(w.T, w.d, w.f, w.E, w.k, 0)])
+        monkeypatch.setenv("MOE_GEMM_2SM_DOWN", rot[moe.gemm_pair_mode_fp8(w.T, w.d, w.f, w.E, w.k, 1)])
     dev = torch.device(DEV)
     logits, x, wgu, wd = make_inputs(w, seed=0, weight_device="cuda")
     wgu8, sgu = moe.quantize_weights_fp8(wgu)
@@ -247,10 +309,10 @@ def test_forward_fp8_full_size(moe, oracle, name):
     assert moe.get_device_error(ws) == 0
     v = moe.workspace_views_fp8(ws, w.T, w.d, w.f, w.E, w.k)
     r_wgu8, r_sgu = oracle.quantize_weights_fp8(wgu_bits)
-    assert np.array_equal(wgu8.cpu().numpy(), r_wgu8) and np.array_equal(sgu.cpu().numpy(), r_sgu)
+    assert np.array_equal(unblock(wgu8), r_wgu8) and np.array_equal(sgu.cpu().numpy(), r_sgu)
     del wgu_bits
     r_wd8, r_sd = oracle.quantize_weights_fp8(wd_bits)
-    assert np.array_equal(wd8.cpu().numpy(), r_wd8) and np.array_equal(sd.cpu().numpy(), r_sd)
+    assert np.array_equal(unblock(wd8), r_wd8) and np.array_equal(sd.cpu().numpy(), r_sd)
     del wd_bits
     ln, xb = logits.numpy(), to_np_bits(x)
     idx, wt = oracle.route(ln, w.k)
