@@ -68,6 +68,13 @@ _SIGS = {
     "oracle_quantize_rows_fp8": ([_U16P, _INT, _INT, _U8P, _F32P], None),
     "oracle_quantize_weights_fp8": ([_U16P, _INT, _INT, _INT, _U8P, _F32P], None),
     "oracle_gateup_swiglu_fp8": ([_U8P, _F32P, _I32P, _INT, _U8P, _F32P, _INT, _INT, _U16P], None),
+    "oracle_pow2_block_scale": ([ctypes.c_float], ctypes.c_float),
+    "oracle_quantize_rows_fp8b": ([_U16P, _INT, _INT, _U8P, _F32P], None),
+    "oracle_quantize_weights_fp8b": ([_U16P, _INT, _INT, _INT, _U8P, _F32P], None),
+    "oracle_forward_fp8b_tokens_routed": ([_U16P, _I32P, _F32P, _U8P, _F32P, _U8P, _F32P, _INT, _INT, _INT, _INT,
+                                           _INT, _I32P, _INT, _F32P], _INT),
+    "oracle_gateup_swiglu_fp8b": ([_U8P, _F32P, _I32P, _INT, _U8P, _F32P, _INT, _INT, _U16P], None),
+    "oracle_down_fp8b": ([_U8P, _F32P, _I32P, _INT, _U8P, _F32P, _INT, _INT, _F32P], None),
     "oracle_down_fp8": ([_U8P, _F32P, _I32P, _INT, _U8P, _F32P, _INT, _INT, _F32P], None),
     "oracle_forward_fp8_tokens_routed": ([_U16P, _I32P, _F32P, _U8P, _F32P, _U8P, _F32P, _INT, _INT, _INT, _INT,
                                           _INT, _I32P, _INT, _F32P], _INT),
@@ -338,6 +345,75 @@ class Oracle:
         idx, w = self.route(logits, k)
         T = idx.shape[0]
         return self.forward_fp8_tokens_routed(x_bits, idx, w, wgu8, sgu, wd8, sd, np.arange(T, dtype=np.int32))
+
+
+    # ---- blockwise FP8 (1 x 128 activation blocks, 128 x 128 weight blocks, power-of-two scales) ----
+    def pow2_block_scale(self, amax: float) -> float:
+        return float(self.L.oracle_pow2_block_scale(float(amax)))
+
+    def quantize_rows_fp8b(self, a_bits):
+        """[R, C] bf16 bits -> (codes [R, C], block scales [R, C/128])."""
+        a_bits = _c(a_bits, np.uint16)
+        R, C = a_bits.shape
+        q = np.empty((R, C), np.uint8)
+        sc = np.empty((R, C // 128), np.float32)
+        self.L.oracle_quantize_rows_fp8b(_p(a_bits, _U16P), R, C, _p(q, _U8P), _p(sc, _F32P))
+        return q, sc
+
+    def quantize_weights_fp8b(self, w_bits):
+        """W [E, K, N] bf16 bits -> (codes [E, N, K], block scales [E, N/128, K/128])."""
+        w_bits = _c(w_bits, np.uint16)
+        E, K, N = w_bits.shape
+        q = np.empty((E, N, K), np.uint8)
+        sc = np.empty((E, N // 128, K // 128), np.float32)
+        self.L.oracle_quantize_weights_fp8b(_p(w_bits, _U16P), E, K, N, _p(q, _U8P), _p(sc, _F32P))
+        return q, sc
+
+    def gateup_swiglu_fp8b(self, x8_perm, sx, offsets, wgu8, sgu):
+        x8_perm, sx = _c(x8_perm, np.uint8), _c(sx, np.float32)
+        offsets = _c(offsets, np.int32)
+        wgu8, sgu = _c(wgu8, np.uint8), _c(sgu, np.float32)
+        E, f2, d = wgu8.shape
+        M = x8_perm.shape[0]
+        h = np.zeros((M, f2 // 2), np.uint16)
+        self.L.oracle_gateup_swiglu_fp8b(_p(x8_perm, _U8P), _p(sx, _F32P), _p(offsets, _I32P), E, _p(wgu8, _U8P),
+                                         _p(sgu, _F32P), d, f2 // 2, _p(h, _U16P))
+        return h
+
+    def down_fp8b(self, h8, sh, offsets, wd8, sd):
+        h8, sh = _c(h8, np.uint8), _c(sh, np.float32)
+        offsets = _c(offsets, np.int32)
+        wd8, sd = _c(wd8, np.uint8), _c(sd, np.float32)
+        E, d, f = wd8.shape
+        M = h8.shape[0]
+        y = np.zeros((M, d), np.float32)
+        self.L.oracle_down_fp8b(_p(h8, _U8P), _p(sh, _F32P), _p(offsets, _I32P), E, _p(wd8, _U8P), _p(sd, _F32P), d,
+                                f, _p(y, _F32P))
+        return y
+
+    def forward_fp8b_tokens_routed(self, x_bits, idx_rows, w_rows, wgu8, sgu, wd8, sd, tokens):
+        x_bits = _c(x_bits, np.uint16)
+        idx_rows = _c(idx_rows, np.int32)
+        w_rows = _c(w_rows, np.float32)
+        wgu8, wd8 = _c(wgu8, np.uint8), _c(wd8, np.uint8)
+        sgu, sd = _c(sgu, np.float32), _c(sd, np.float32)
+        tokens = _c(tokens, np.int32)
+        T, d = x_bits.shape
+        E, f2, _ = wgu8.shape
+        k = idx_rows.shape[1]
+        out = np.empty((tokens.shape[0], d), np.float32)
+        rc = self.L.oracle_forward_fp8b_tokens_routed(
+            _p(x_bits, _U16P), _p(idx_rows, _I32P), _p(w_rows, _F32P), _p(wgu8, _U8P), _p(sgu, _F32P),
+            _p(wd8, _U8P), _p(sd, _F32P), T, d, f2 // 2, E, k, _p(tokens, _I32P), tokens.shape[0], _p(out, _F32P))
+        if rc:
+            raise ValueError(f"oracle_forward_fp8b_tokens_routed failed (rc={rc})")
+        return out
+
+    def forward_fp8b(self, x_bits, logits, wgu8, sgu, wd8, sd, k):
+        """The whole blockwise FP8 layer with the softmax router (every token)."""
+        idx, w = self.route(logits, k)
+        T = idx.shape[0]
+        return self.forward_fp8b_tokens_routed(x_bits, idx, w, wgu8, sgu, wd8, sd, np.arange(T, dtype=np.int32))
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:

@@ -123,6 +123,33 @@ void quantize_rows_fp8(GetF get, int R, int C, uint8_t* q, float* scale) {
     }
 }
 
+// Blockwise FP8 scale of a block with absolute maximum amax: the smallest power of two P with
+// fl(amax / 448) <= P (a UE8M0-representable scale), at least 2^-126 so that 1/P is a finite fp32
+// power of two; an all-zero block gets P = 1.  Codes are e4m3(v * (1/P)) (exact scaling), the
+// dequantised value code * P.
+inline float pow2_block_scale(float amax) {
+    if (!(amax > 0.0f)) return 1.0f;
+    const float q = amax / 448.0f;
+    int e = 0;
+    const float m = std::frexp(q, &e);  // q = m * 2^e, m in [0.5, 1)
+    const float p = (m == 0.5f) ? q : std::ldexp(1.0f, e);
+    return std::max(p, std::ldexp(1.0f, -126));
+}
+
+// Quantise the C values get(c), c in [0, C), in consecutive blocks of B (C % B == 0): codes q[c],
+// one scale per block.
+template <class GetF>
+void quantize_blocks_fp8(GetF get, int C, int B, uint8_t* q, float* scale) {
+    for (int b = 0; b < C / B; ++b) {
+        float amax = 0.0f;
+        for (int c = b * B; c < (b + 1) * B; ++c) amax = std::max(amax, std::fabs(get(c)));
+        const float P = pow2_block_scale(amax);
+        const float inv = 1.0f / P;  // exact: P is a power of two in [2^-126, 2^128)
+        scale[b] = P;
+        for (int c = b * B; c < (b + 1) * B; ++c) q[c] = e4m3_encode(get(c) * inv);
+    }
+}
+
 // One permuted row through expert e: g, u over i = 0..d-1 ascending; h = silu(g) * u.
 void gateup_row(const float* x, const uint16_t* Wgu_e, int d, int f, float* h, float* g, float* u) {
     for (int n = 0; n < f; ++n) { g[n] = 0.0f; u[n] = 0.0f; }
@@ -471,6 +498,40 @@ void down_row_fp8(const float* hd, float sh, const uint8_t* Wde8, const float* s
         yr[m] = acc * (sh * sde[m]);
     }
 }
+// Blockwise FP8 (128-wide K blocks): one row r through expert e.  xd [d] decoded codes with block
+// scales sx[d/128]; weight codes We8 [2f, d] with block scales se[(2f/128) x (d/128)] (row-major by
+// output block).  For each output column n the 128-element partial sums are taken block by block
+// (i ascending), each multiplied by (sx[b] * se[n/128][b]) and added in block order.
+void gateup_row_fp8b(const float* xd, const float* sx, const uint8_t* We8, const float* se, int d, int f,
+                     float* g, float* u, uint16_t* hb) {
+    const int nb = d / 128;
+    for (int n = 0; n < 2 * f; ++n) {
+        const uint8_t* wrow = We8 + static_cast<size_t>(n) * d;
+        float acc = 0.0f;
+        for (int b = 0; b < nb; ++b) {
+            float part = 0.0f;
+            for (int i = b * 128; i < (b + 1) * 128; ++i) part += xd[i] * e4m3_decode(wrow[i]);
+            acc += part * (sx[b] * se[static_cast<size_t>(n / 128) * nb + b]);
+        }
+        if (n < f) g[n] = acc; else u[n - f] = acc;
+    }
+    for (int n = 0; n < f; ++n) hb[n] = f32_to_bf16_rne(silu(g[n]) * u[n]);
+}
+
+void down_row_fp8b(const float* hd, const float* sh, const uint8_t* Wde8, const float* sde, int d, int f,
+                   float* yr) {
+    const int nb = f / 128;
+    for (int m = 0; m < d; ++m) {
+        const uint8_t* wrow = Wde8 + static_cast<size_t>(m) * f;
+        float acc = 0.0f;
+        for (int b = 0; b < nb; ++b) {
+            float part = 0.0f;
+            for (int n = b * 128; n < (b + 1) * 128; ++n) part += hd[n] * e4m3_decode(wrow[n]);
+            acc += part * (sh[b] * sde[static_cast<size_t>(m / 128) * nb + b]);
+        }
+        yr[m] = acc;
+    }
+}
 }  // namespace
 
 extern "C" {
@@ -545,6 +606,128 @@ int oracle_forward_fp8_tokens_routed(const uint16_t* x, const int32_t* idx_rows,
         }
     }
     return 0;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Blockwise FP8 variant: 1 x 128 blocks for the activations (x and h rows), 128 x 128 blocks
+// (128 output columns x 128 K values) for the weights, power-of-two block scales (see
+// pow2_block_scale).  Per output element, the 128-wide partial sums are scaled block by block:
+//   g[n] = sum_b (sum_{i in b} dec(x8[i]) * dec(W8[e][n][i])) * (sx[b] * sw[e][n/128][b])
+// ---------------------------------------------------------------------------------------------
+float oracle_pow2_block_scale(float amax) { return pow2_block_scale(amax); }
+
+// Rows of a bf16 matrix [R, C] (C % 128 == 0) -> codes [R, C] and scales [R, C/128].
+void oracle_quantize_rows_fp8b(const uint16_t* a, int R, int C, uint8_t* q, float* scale) {
+    for (int r = 0; r < R; ++r) {
+        const uint16_t* row = a + static_cast<size_t>(r) * C;
+        quantize_blocks_fp8([&](int c) { return bf16_to_f32(row[c]); }, C, 128, q + static_cast<size_t>(r) * C,
+                            scale + static_cast<size_t>(r) * (C / 128));
+    }
+}
+
+// Weights W [E, K, N] bf16 (K, N multiples of 128) -> codes Wq [E, N, K] (transposed) and scales
+// [E, N/128, K/128], one per 128 x 128 block of (output column, K).
+void oracle_quantize_weights_fp8b(const uint16_t* W, int E, int K, int N, uint8_t* Wq, float* scale) {
+    const int nbn = N / 128, nbk = K / 128;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int e = 0; e < E; ++e)
+        for (int bn = 0; bn < nbn; ++bn) {
+            const uint16_t* We = W + static_cast<size_t>(e) * K * N;
+            for (int bk = 0; bk < nbk; ++bk) {
+                float amax = 0.0f;
+                for (int n = bn * 128; n < (bn + 1) * 128; ++n)
+                    for (int k = bk * 128; k < (bk + 1) * 128; ++k)
+                        amax = std::max(amax, std::fabs(bf16_to_f32(We[static_cast<size_t>(k) * N + n])));
+                const float P = pow2_block_scale(amax);
+                const float inv = 1.0f / P;
+                scale[(static_cast<size_t>(e) * nbn + bn) * nbk + bk] = P;
+                for (int n = bn * 128; n < (bn + 1) * 128; ++n)
+                    for (int k = bk * 128; k < (bk + 1) * 128; ++k)
+                        Wq[(static_cast<size_t>(e) * N + n) * K + k] =
+                            e4m3_encode(bf16_to_f32(We[static_cast<size_t>(k) * N + n]) * inv);
+            }
+        }
+}
+
+// The blockwise FP8 layer's output for the given tokens with their routing (as
+// oracle_forward_fp8_tokens_routed): x rows quantised in 1 x 128 blocks, h likewise.
+int oracle_forward_fp8b_tokens_routed(const uint16_t* x, const int32_t* idx_rows, const float* w_rows,
+                                      const uint8_t* Wgu8, const float* sgu, const uint8_t* Wd8, const float* sd,
+                                      int T, int d, int f, int E, int k, const int32_t* tokens, int ntok,
+                                      float* out_rows) {
+    if (!valid_shape(T, E, k) || d < 128 || f < 128 || d % 128 || f % 128) return -1;
+    for (int s = 0; s < ntok; ++s)
+        if (tokens[s] < 0 || tokens[s] >= T) return -1;
+    const size_t npairs = static_cast<size_t>(ntok) * k;
+    for (size_t q = 0; q < npairs; ++q)
+        if (idx_rows[q] < 0 || idx_rows[q] >= E) return -2;
+    std::vector<float> ys(npairs * d);
+#pragma omp parallel
+    {
+        std::vector<uint8_t> x8(d), h8(f);
+        std::vector<float> xd(d), g(f), u(f), hd(f), sx(d / 128), sh(f / 128);
+        std::vector<uint16_t> hb(f);
+#pragma omp for schedule(dynamic, 1)
+        for (long long q = 0; q < static_cast<long long>(npairs); ++q) {
+            const int s = static_cast<int>(q / k);
+            const int e = idx_rows[q];
+            oracle_quantize_rows_fp8b(x + static_cast<size_t>(tokens[s]) * d, 1, d, x8.data(), sx.data());
+            for (int i = 0; i < d; ++i) xd[i] = e4m3_decode(x8[i]);
+            gateup_row_fp8b(xd.data(), sx.data(), Wgu8 + static_cast<size_t>(e) * 2 * f * d,
+                            sgu + static_cast<size_t>(e) * (2 * f / 128) * (d / 128), d, f, g.data(), u.data(),
+                            hb.data());
+            oracle_quantize_rows_fp8b(hb.data(), 1, f, h8.data(), sh.data());
+            for (int n = 0; n < f; ++n) hd[n] = e4m3_decode(h8[n]);
+            down_row_fp8b(hd.data(), sh.data(), Wd8 + static_cast<size_t>(e) * d * f,
+                          sd + static_cast<size_t>(e) * (d / 128) * (f / 128), d, f, ys.data() + q * d);
+        }
+    }
+    for (int s = 0; s < ntok; ++s) {
+        float* o = out_rows + static_cast<size_t>(s) * d;
+        for (int m = 0; m < d; ++m) o[m] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const float wj = w_rows[static_cast<size_t>(s) * k + j];
+            const float* yr = ys.data() + (static_cast<size_t>(s) * k + j) * d;
+            for (int m = 0; m < d; ++m) o[m] += wj * yr[m];
+        }
+    }
+    return 0;
+}
+
+// Blockwise FP8 steps 3 and 4 on their own (as oracle_gateup_swiglu_fp8 / oracle_down_fp8), with
+// block scales sx [M, d/128], sgu [E, 2f/128, d/128], sh [M, f/128], sd [E, d/128, f/128].
+void oracle_gateup_swiglu_fp8b(const uint8_t* x8_perm, const float* sx, const int32_t* offsets, int E,
+                               const uint8_t* Wgu8, const float* sgu, int d, int f, uint16_t* h) {
+    for (int e = 0; e < E; ++e) {
+#pragma omp parallel
+        {
+            std::vector<float> xd(d), g(f), u(f);
+#pragma omp for schedule(dynamic, 1)
+            for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
+                for (int i = 0; i < d; ++i) xd[i] = e4m3_decode(x8_perm[static_cast<size_t>(r) * d + i]);
+                gateup_row_fp8b(xd.data(), sx + static_cast<size_t>(r) * (d / 128),
+                                Wgu8 + static_cast<size_t>(e) * 2 * f * d,
+                                sgu + static_cast<size_t>(e) * (2 * f / 128) * (d / 128), d, f, g.data(), u.data(),
+                                h + static_cast<size_t>(r) * f);
+            }
+        }
+    }
+}
+
+void oracle_down_fp8b(const uint8_t* h8, const float* sh, const int32_t* offsets, int E, const uint8_t* Wd8,
+                      const float* sd, int d, int f, float* y) {
+    for (int e = 0; e < E; ++e) {
+#pragma omp parallel
+        {
+            std::vector<float> hd(f);
+#pragma omp for schedule(dynamic, 1)
+            for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
+                for (int n = 0; n < f; ++n) hd[n] = e4m3_decode(h8[static_cast<size_t>(r) * f + n]);
+                down_row_fp8b(hd.data(), sh + static_cast<size_t>(r) * (f / 128), Wd8 + static_cast<size_t>(e) * d * f,
+                              sd + static_cast<size_t>(e) * (d / 128) * (f / 128), d, f, y + static_cast<size_t>(r) * d);
+            }
+        }
+    }
 }
 
 // Step 3 of the FP8 layer on its own, over rows 0..offsets[E]-1 of a grouped operand:

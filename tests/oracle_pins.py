@@ -535,8 +535,149 @@ def pin_fp8_stages(O, seed=53):
     assert np.array_equal(got, out)
 
 
+# --------------------------------------------------------------------------------------------
+# Blockwise FP8: 1 x 128 activation blocks, 128 x 128 weight blocks, power-of-two block scales.
+# --------------------------------------------------------------------------------------------
+def pow2_scale_ref(amax):
+    """The block scale stated on its own: the smallest power of two P with fl32(amax / 448) <= P,
+    clamped below at 2^-126; 1 for amax == 0 (float64 search over exponents)."""
+    if amax == 0:
+        return 1.0
+    q = float(np.float32(np.float32(amax) / np.float32(448.0)))
+    e = -126
+    while 2.0 ** e < q:
+        e += 1
+    return 2.0 ** e
+
+
+def pin_pow2_block_scale(O, seed=59):
+    """Powers of two times 448 (exact ratios), their neighbours, tiny and huge magnitudes, random ones."""
+    rng = np.random.default_rng(seed)
+    vals = [0.0, 448.0, 224.0, 896.0, 1.0, 3.0e38, 1e-30, 1e-40]
+    for e in range(-20, 21, 5):
+        v = np.float32(448.0 * 2.0 ** e)
+        vals += [float(v), float(np.nextafter(v, np.float32(np.inf))), float(np.nextafter(v, np.float32(0)))]
+    vals += list(np.exp(rng.uniform(-60, 60, 40)).astype(np.float32).astype(float))
+    for a in vals:
+        a32 = float(np.float32(a))
+        assert O.pow2_block_scale(a32) == pow2_scale_ref(a32), a32
+
+
+def block_quantise_ref(O, vals, B=128):
+    """Rows of float values quantised in consecutive blocks of B: the pinned scale rule per block,
+    the pinned E4M3 encoder on value / scale."""
+    R, C = vals.shape
+    q = np.empty((R, C), np.uint8)
+    sc = np.empty((R, C // B))
+    for r in range(R):
+        for b in range(C // B):
+            blk = vals[r, b * B:(b + 1) * B]
+            P = pow2_scale_ref(float(np.abs(blk).max()))
+            sc[r, b] = P
+            q[r, b * B:(b + 1) * B] = O.e4m3_encode((blk.astype(np.float32) * np.float32(1.0 / P)).astype(np.float32))
+    return q, sc
+
+
+def pin_quantize_fp8b(O, seed=61):
+    """Row blocks and weight blocks against the block rule stated with numpy: each 128-wide block of
+    a row (each 128 x 128 block of a weight matrix) gets its own power-of-two scale; codes are the
+    encoder's on value / scale; a zero block gets scale 1; dequantised values are within half a
+    quantum."""
+    rng = np.random.default_rng(seed)
+    a = rng.standard_normal((6, 384)).astype(np.float32)
+    a[:, 128:256] *= 1000.0   # blocks of very different magnitude in one row
+    a[2, 256:] = 0.0          # a zero block
+    a[3, :128] *= 1e-20
+    bits = f32_to_bf16_bits(a)
+    af = bf16_bits_to_f32(bits)
+    q, sc = O.quantize_rows_fp8b(bits)
+    rq, rsc = block_quantise_ref(O, af)
+    assert np.array_equal(q, rq) and np.array_equal(sc.astype(np.float64), rsc)
+    tab = e4m3_table()
+    rec = tab[q] * np.repeat(sc.astype(np.float64), 128, axis=1)
+    bound = np.maximum(np.abs(af) * 2.0 ** -4, 2.0 ** -10 * np.repeat(sc, 128, axis=1)) * (1 + 1e-6)
+    assert np.all(np.abs(rec - af) <= bound)
+    # weights: W [E, K, N] -> codes [E, N, K], scales [E, N/128, K/128]
+    W = (0.05 * rng.standard_normal((2, 256, 384))).astype(np.float32)
+    W[1, :128, 128:256] *= 64.0
+    wbits = f32_to_bf16_bits(W)
+    wf = bf16_bits_to_f32(wbits)
+    wq, wsc = O.quantize_weights_fp8b(wbits)
+    assert wq.shape == (2, 384, 256) and wsc.shape == (2, 3, 2)
+    for e in range(2):
+        for bn in range(3):
+            for bk in range(2):
+                blk = wf[e, bk * 128:(bk + 1) * 128, bn * 128:(bn + 1) * 128].T  # [n, k]
+                P = pow2_scale_ref(float(np.abs(blk).max()))
+                assert wsc[e, bn, bk] == P
+                codes = O.e4m3_encode((blk.astype(np.float32) * np.float32(1.0 / P)).astype(np.float32))
+                assert np.array_equal(wq[e, bn * 128:(bn + 1) * 128, bk * 128:(bk + 1) * 128], codes)
+
+
+def pin_fp8b_forward(O, seed=67):
+    """The blockwise FP8 layer against a float64 statement built from dequantised operands (codes
+    times their block scales), h rounded to bf16 and requantised in 128-wide blocks, slot-ordered
+    combine."""
+    rng = np.random.default_rng(seed)
+    T, d, f, E, k = 7, 256, 384, 3, 2
+    logits, x_bits, wgu, wd = random_layer(rng, T, d, f, E)
+    # Give every 128 x 128 weight block (and every 128-wide x block) its own magnitude, so that the
+    # block scales differ and a wrongly indexed scale changes the result.
+    def spread(bits, axes, lo=-6, hi=6):
+        v = bf16_bits_to_f32(bits).astype(np.float32)
+        for ax in axes:
+            fac = (2.0 ** rng.integers(lo, hi, v.shape[ax] // 128)).repeat(128).astype(np.float32)
+            shape = [1] * v.ndim
+            shape[ax] = -1
+            v = v * fac.reshape(shape)
+        return f32_to_bf16_bits(v)
+    wgu, wd, x_bits = spread(wgu, (1, 2)), spread(wd, (1, 2)), spread(x_bits, (1,), -3, 3)
+    wgu8, sgu = O.quantize_weights_fp8b(wgu)   # [E, 2f, d], [E, 2f/128, d/128]
+    wd8, sdn = O.quantize_weights_fp8b(wd)     # [E, d, f], [E, d/128, f/128]
+    assert len(np.unique(sgu)) > 4 and len(np.unique(sdn)) > 2
+    out = O.forward_fp8b(x_bits, logits, wgu8, sgu, wd8, sdn, k)
+    idx, w = O.route(logits, k)
+    tab = e4m3_table()
+
+    def deq_w(codes, sc):  # [N, K] codes, [N/128, K/128] scales
+        return tab[codes] * np.kron(sc.astype(np.float64), np.ones((128, 128)))
+
+    ref = np.zeros((T, d))
+    for t in range(T):
+        x8, sx = O.quantize_rows_fp8b(x_bits[t:t + 1])
+        xd = tab[x8[0]] * np.repeat(sx[0].astype(np.float64), 128)
+        for j in range(k):
+            e = idx[t, j]
+            gu = deq_w(wgu8[e], sgu[e]) @ xd
+            g, u = gu[:f], gu[f:]
+            hb = f32_to_bf16_bits((g / (1 + np.exp(-g)) * u).astype(np.float32))[None, :]
+            h8, sh = O.quantize_rows_fp8b(hb)
+            hd = tab[h8[0]] * np.repeat(sh[0].astype(np.float64), 128)
+            ref[t] += w[t, j] * (deq_w(wd8[e], sdn[e]) @ hd)
+    err = np.abs(out - ref).max()
+    assert err <= 2e-3 * np.abs(ref).max(), err
+
+
+def pin_fp8b_stages(O, seed=71):
+    """The blockwise FP8 stage functions composed in the layer's order give its output exactly."""
+    rng = np.random.default_rng(seed)
+    T, d, f, E, k = 9, 256, 256, 4, 2
+    logits, x_bits, wgu, wd = random_layer(rng, T, d, f, E)
+    logits[:, 1] = -30.0  # expert 1 never chosen: an empty segment
+    wgu8, sgu = O.quantize_weights_fp8b(wgu)
+    wd8, sdn = O.quantize_weights_fp8b(wd)
+    out = O.forward_fp8b(x_bits, logits, wgu8, sgu, wd8, sdn, k)
+    idx, w = O.route(logits, k)
+    counts, offsets, src, dest = O.permute(idx, E)
+    x8, sx = O.quantize_rows_fp8b(x_bits[src])
+    h = O.gateup_swiglu_fp8b(x8, sx, offsets, wgu8, sgu)
+    h8, sh = O.quantize_rows_fp8b(h)
+    y = O.down_fp8b(h8, sh, offsets, wd8, sdn)
+    assert np.array_equal(O.combine(y, w, dest), out)
+
+
 ALL_PINS = [pin_hand_example, pin_brute_force, pin_dense_e1_k1, pin_route_library,
             pin_permute_library, pin_invariants, pin_stages, pin_grouped_hand_example,
             pin_grouped_reduces_to_topk, pin_grouped_brute_force, pin_grouped_invariants,
             pin_e4m3_decode_table, pin_e4m3_encode_rne, pin_quantize_rows_fp8, pin_fp8_forward,
-            pin_fp8_stages]
+            pin_fp8_stages, pin_pow2_block_scale, pin_quantize_fp8b, pin_fp8b_forward, pin_fp8b_stages]

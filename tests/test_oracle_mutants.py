@@ -51,8 +51,21 @@ MUTANTS = {
     "e4m3_no_saturation": ("if (v > 448.0) v = 448.0;", "if (v > 480.0) v = 480.0;"),
     "fp8_row_scale_dropped": ("scale[r] = amax > 0.0f ? amax / 448.0f : 1.0f;", "scale[r] = 1.0f;"),
     "fp8_weight_scale_dropped": ("const float v = acc * (sx * se[n]);", "const float v = acc * sx;"),
-    "fp8_h_unquantised": ("for (int n = 0; n < f; ++n) hd[n] = e4m3_decode(h8[n]);",
-                          "for (int n = 0; n < f; ++n) hd[n] = bf16_to_f32(hb[n]) / sh;"),
+    "fp8_h_unquantised": ("oracle_quantize_rows_fp8(hb.data(), 1, f, h8.data(), &sh);\n"
+                          "            for (int n = 0; n < f; ++n) hd[n] = e4m3_decode(h8[n]);",
+                          "oracle_quantize_rows_fp8(hb.data(), 1, f, h8.data(), &sh);\n"
+                          "            for (int n = 0; n < f; ++n) hd[n] = bf16_to_f32(hb[n]) / sh;"),
+    # the blockwise FP8 variant
+    "fp8b_scale_rounds_down": ("const float p = (m == 0.5f) ? q : std::ldexp(1.0f, e);",
+                               "const float p = (m == 0.5f) ? q : std::ldexp(1.0f, e - 1);"),
+    "fp8b_weight_scale_transposed": ("acc += part * (sx[b] * se[static_cast<size_t>(n / 128) * nb + b]);",
+                                     "acc += part * (sx[b] * se[static_cast<size_t>(b) * (2 * f / 128) + n / 128]);"),
+    "fp8b_first_block_scale_only": ("acc += part * (sh[b] * sde[static_cast<size_t>(m / 128) * nb + b]);",
+                                    "acc += part * (sh[0] * sde[static_cast<size_t>(m / 128) * nb + b]);"),
+    "fp8b_weight_block_one_row": ("for (int n = bn * 128; n < (bn + 1) * 128; ++n)\n                    for (int k = bk * 128; k < (bk + 1) * 128; ++k)\n                        amax",
+                                  "for (int n = bn * 128; n < bn * 128 + 1; ++n)\n                    for (int k = bk * 128; k < (bk + 1) * 128; ++k)\n                        amax"),
+    "fp8b_block_absmax_half": ("for (int c = b * B; c < (b + 1) * B; ++c) amax",
+                               "for (int c = b * B; c < b * B + B / 2; ++c) amax"),
 }
 
 _CHILD = textwrap.dedent("""
