@@ -59,6 +59,9 @@ KERNEL_NAMES = {"route": "route_kernel", "permute": "permute_kernel",
 STAGES_FP8 = ("route", "permute", "gateup_swiglu", "quantize_h", "down", "combine")
 KERNEL_NAMES_FP8 = {"gateup_swiglu": "grouped_gemm_kernel<0, false, true>",
                     "down": "grouped_gemm_kernel<1, false, true>"}
+STAGES_FP8B = ("route", "permute", "quantize_x", "gateup_swiglu", "quantize_h", "down", "combine")
+KERNEL_NAMES_FP8B = {"gateup_swiglu": "grouped_gemm_kernel<0, false, true, true>",
+                     "down": "grouped_gemm_kernel<1, false, true, true>"}
 FP8_OVER_BF16 = 2.0  # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s) applied to the measured bf16 peak
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum per launch) from ncu captures of the
@@ -129,9 +132,21 @@ def load_peaks():
 # ----------------------------------------------------------------------------------------------
 # Algorithmic work per stage (what the layer must move / compute, not what the kernels happen to)
 # ----------------------------------------------------------------------------------------------
-def stage_work(w: Workload, n_active: int, fp8: bool = False) -> dict:
+def stage_work(w: Workload, n_active: int, fp8: bool = False, blocks: bool = False) -> dict:
     T, d, f, E, k = w.T, w.d, w.f, w.E, w.k
     M = T * k
+    if blocks:  # 1-byte codes; one 4-byte scale per 128 x 128 weight block and per 128 activation values
+        return {
+            "route": {"bytes": T * E * 4 + M * 8, "flops": 0},
+            "permute": {"bytes": M * 4 + (E + E + 1 + 2 * M) * 4, "flops": 0},
+            "quantize_x": {"bytes": M * 4 + T * d * 2 + M * d + M * d // 32, "flops": 0},
+            "gateup_swiglu": {"bytes": n_active * (d * 2 * f + d * 2 * f // 4096) + M * d + M * d // 32 + M * f * 2,
+                              "flops": 4 * M * d * f},
+            "quantize_h": {"bytes": M * f * 2 + M * f + M * f // 32, "flops": 0},
+            "down": {"bytes": n_active * (f * d + f * d // 4096) + M * f + M * f // 32 + M * d * 4,
+                     "flops": 2 * M * d * f},
+            "combine": {"bytes": M * d * 4 + M * 8 + T * d * 2, "flops": 2 * M * d},
+        }
     if fp8:  # 1-byte codes; weight scales 4 bytes per output column, activation scales per row
         return {
             "route": {"bytes": T * E * 4 + M * 8, "flops": 0},
@@ -151,8 +166,13 @@ def stage_work(w: Workload, n_active: int, fp8: bool = False) -> dict:
     }
 
 
-def layer_work(w: Workload, n_active: int, fp8: bool = False) -> dict:
-    wbytes = n_active * (3 * w.d * w.f + 4 * (2 * w.f + w.d)) if fp8 else n_active * 3 * w.d * w.f * 2
+def layer_work(w: Workload, n_active: int, fp8: bool = False, blocks: bool = False) -> dict:
+    if blocks:
+        wbytes = n_active * (3 * w.d * w.f + 3 * w.d * w.f // 4096)
+    elif fp8:
+        wbytes = n_active * (3 * w.d * w.f + 4 * (2 * w.f + w.d))
+    else:
+        wbytes = n_active * 3 * w.d * w.f * 2
     return {"bytes": wbytes + w.T * w.d * 2 + w.T * w.E * 4 + w.T * w.d * 2,
             "flops": 6 * w.T * w.k * w.d * w.f}
 
@@ -249,15 +269,18 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     torch.cuda.set_device(dev)
     moe.load()
 
-    fp8 = args.dtype == "e4m3"
+    blocks = args.dtype == "e4m3b"
+    fp8 = args.dtype == "e4m3" or blocks
     logits, x, wgu, wd = make_inputs(w, seed=args.seed + rank, weight_device=str(dev))
     x_d, l_d = x.to(dev), logits.to(dev)
     if fp8:
         if w.router[0] == "grouped":
-            raise SystemExit("--dtype e4m3 runs the softmax router only")
-        w8 = moe.quantize_weights_fp8(wgu) + moe.quantize_weights_fp8(wd)  # (wgu8, sgu, wd8, sd), once
+            raise SystemExit("--dtype e4m3/e4m3b run the softmax router only")
+        quant = moe.quantize_weights_fp8b if blocks else moe.quantize_weights_fp8
+        w8 = quant(wgu) + quant(wd)  # (wgu8, sgu, wd8, sd), once
         torch.cuda.synchronize(dev)
-        ws = torch.empty(moe.workspace_size_fp8(w.T, w.d, w.f, w.E, w.k), dtype=torch.uint8, device=dev)
+        wsize = moe.workspace_size_fp8b if blocks else moe.workspace_size_fp8
+        ws = torch.empty(wsize(w.T, w.d, w.f, w.E, w.k), dtype=torch.uint8, device=dev)
     else:
         ws = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k) + moe.host_staging_size(w.T, w.d, w.E),
                          dtype=torch.uint8, device=dev)
@@ -269,7 +292,9 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     bias_d = draw_router_bias(w, seed=args.seed + rank).to(dev)
 
     def step():
-        if fp8:
+        if blocks:
+            moe.forward_fp8b(x_d, l_d, *w8, w.k, out=out, workspace=ws)
+        elif fp8:
             moe.forward_fp8(x_d, l_d, *w8, w.k, out=out, workspace=ws)
         elif grouped:  # DeepSeek-V3's router as step 1
             _, G, tg, scale, _ = w.router
@@ -294,7 +319,8 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         est = max_over_ranks(e0.elapsed_time(e1) / 3, dist, dev)
         args.steps = int(min(AUTO_STEPS_MAX, max(AUTO_STEPS_MIN, math.ceil(AUTO_TIMED_S * 1e3 / est))))
 
-    v = (moe.workspace_views_fp8 if fp8 else moe.workspace_views)(ws, w.T, w.d, w.f, w.E, w.k)
+    views = moe.workspace_views_fp8b if blocks else (moe.workspace_views_fp8 if fp8 else moe.workspace_views)
+    v = views(ws, w.T, w.d, w.f, w.E, w.k)
     counts = v["counts"].cpu().numpy()
     n_active = int((counts > 0).sum())
 
@@ -330,8 +356,19 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     idx, wts = v["idx"], v["w"]
     counts_d, offs, src, dest, h, y = (v["counts"], v["offsets"], v["src"], v["dest"], v["h"], v["y_perm"])
     st = v["status"]
-    stages = STAGES_FP8 if fp8 else STAGES
-    if fp8:
+    stages = STAGES_FP8B if blocks else (STAGES_FP8 if fp8 else STAGES)
+    if blocks:
+        x8, sx, h8, sh = v["x8"], v["sx"], v["h8"], v["sh"]
+        calls = [
+            lambda: moe.route(l_d, w.k, idx=idx, w=wts),
+            lambda: moe.permute(idx, x_d, w.E, status=st, out=(counts_d, offs, src, dest, None)),
+            lambda: moe.quantize_rows_fp8b(x_d, src, status=st, out=(x8, sx)),
+            lambda: moe.grouped_gemm_gateup_swiglu_fp8b(x8, sx, w8[0], w8[1], offs, h=h, status=st),
+            lambda: moe.quantize_rows_fp8b(h, status=st, out=(h8, sh)),
+            lambda: moe.grouped_gemm_down_fp8b(h8, sh, w8[2], w8[3], offs, y_perm=y, status=st, ksplit=v["ksplit"]),
+            lambda: moe.combine(y, wts, dest, out=out, status=st, ksplit=v["ksplit"]),
+        ]
+    elif fp8:
         x8, sx, h8, sh = v["x8"], v["sx"], v["h8"], v["sh"]
         calls = [
             lambda: moe.route(l_d, w.k, idx=idx, w=wts),
@@ -397,8 +434,8 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         raise RuntimeError("device status word set during the timed region")
 
     peaks, peak_src = load_peaks()
-    sw = stage_work(w, n_active, fp8)
-    lw = layer_work(w, n_active, fp8)
+    sw = stage_work(w, n_active, fp8, blocks)
+    lw = layer_work(w, n_active, fp8, blocks)
     dom = max(("gateup_swiglu", "down"), key=lambda n: stage_ms[n])
     dom_ms = stage_ms[dom]
     tensor_peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if fp8 else 1.0)
@@ -412,10 +449,10 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         achieved = sw[dom]["bytes"] / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = measured_traffic(w.name, dom + ("_fp8" if fp8 else ""))
-    kname = KERNEL_NAMES_FP8[dom] if fp8 else KERNEL_NAMES[dom]
-    pair_mode = (moe.gemm_pair_mode_fp8 if fp8 else moe.gemm_pair_mode)(w.T, w.d, w.f, w.E, w.k,
-                                                                       0 if dom == "gateup_swiglu" else 1)
+    roof["traffic"] = measured_traffic(w.name, dom + ("_fp8b" if blocks else "_fp8" if fp8 else ""))
+    kname = KERNEL_NAMES_FP8B[dom] if blocks else (KERNEL_NAMES_FP8[dom] if fp8 else KERNEL_NAMES[dom])
+    pair_mode = 0 if blocks else (moe.gemm_pair_mode_fp8 if fp8 else moe.gemm_pair_mode)(
+        w.T, w.d, w.f, w.E, w.k, 0 if dom == "gateup_swiglu" else 1)
     if pair_mode >= 1:  # SM-pair kernel, template <KIND, SWAPCAP, GATHER, FP8>
         kname = "grouped_gemm_2sm_kernel<%d, %s, false, %s>" % (0 if dom == "gateup_swiglu" else 1,
                                                                 "true" if pair_mode == 2 else "false",
@@ -433,7 +470,8 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         "host_weights": (wgu, wd), "inputs": (logits, x), "step_ms_p10_p90": (
             float(np.percentile(step_ms, 10)), float(np.percentile(step_ms, 90))),
         "peak_src": peak_src, "peaks": peaks, "ksplit": v["ksplit"],
-        "launches_per_step": (moe.forward_fp8_launch_count(w.T, w.E, w.k) if fp8 else
+        "launches_per_step": (moe.forward_fp8b_launch_count(w.T, w.E, w.k) if blocks else
+                              moe.forward_fp8_launch_count(w.T, w.E, w.k) if fp8 else
                               5 if grouped else moe.forward_launch_count(w.T, w.E, w.k)),
     }
 
@@ -441,18 +479,23 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
 # ----------------------------------------------------------------------------------------------
 # Oracle timing (CPU baseline and the reference arm)
 # ----------------------------------------------------------------------------------------------
-def oracle_sample_runner(w: Workload, logits, x, wgu, wd, seed: int = 0, fp8: bool = False):
+def oracle_sample_runner(w: Workload, logits, x, wgu, wd, seed: int = 0, fp8: bool = False, blocks: bool = False):
     import oracle as oracle_pkg
     O = oracle_pkg.Oracle()
     xb = bf16_bits(x)
     ln = logits.numpy()
     wgub, wdb = bf16_bits(wgu), bf16_bits(wd)
     bias = draw_router_bias(w, seed).numpy()
-    w8 = O.quantize_weights_fp8(wgub) + O.quantize_weights_fp8(wdb) if fp8 else None  # once, untimed
+    if blocks:
+        w8 = O.quantize_weights_fp8b(wgub) + O.quantize_weights_fp8b(wdb)  # once, untimed
+    else:
+        w8 = O.quantize_weights_fp8(wgub) + O.quantize_weights_fp8(wdb) if fp8 else None
 
     def run(S: int) -> float:
         t0 = time.perf_counter()
-        if fp8:
+        if blocks:
+            O.forward_fp8b(xb[:S], ln[:S], *w8, w.k)
+        elif fp8:
             O.forward_fp8(xb[:S], ln[:S], *w8, w.k)
         elif w.router[0] == "grouped":
             idx, wts = O.route_grouped(ln[:S], bias, w.k, *w.router[1:4])
@@ -475,12 +518,13 @@ def pick_sample(run, T: int, budget_s: float) -> int:
     return S
 
 
-def cpu_baseline(w, logits, x, wgu, wd, budget_s: float, seed: int = 0, fp8: bool = False):
-    O, run = oracle_sample_runner(w, logits, x, wgu, wd, seed, fp8)
+def cpu_baseline(w, logits, x, wgu, wd, budget_s: float, seed: int = 0, fp8: bool = False, blocks: bool = False):
+    O, run = oracle_sample_runner(w, logits, x, wgu, wd, seed, fp8, blocks)
     S = pick_sample(run, w.T, budget_s)
     dt = run(S)
     what = ("FP8 oracle forward (route, permute, x/h quantisation, E4M3 gate+up/SwiGLU and down, combine; "
-            "weights quantised beforehand, untimed)" if fp8 else
+            f"{'128-wide block' if blocks else 'per-row / per-channel'} scales; weights quantised beforehand, "
+            "untimed)" if fp8 else
             "oracle forward (route, permute, gate+up/SwiGLU, down, combine)")
     return {"value": round(S / dt, 3), "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
             "sample": f"{what} on the first {S} of {w.T} tokens of the same seeded batch, full weights, {dt:.1f} s"}
@@ -491,8 +535,9 @@ def run_reference(args, w: Workload, rank: int, world: int):
         return None
     logits, x, wgu, wd = make_inputs(w, seed=args.seed, weight_device="cuda" if torch.cuda.is_available() else "cpu")
     wgu, wd = wgu.cpu(), wd.cpu()
-    fp8 = args.dtype == "e4m3"
-    O, run = oracle_sample_runner(w, logits, x, wgu, wd, args.seed, fp8)
+    blocks = args.dtype == "e4m3b"
+    fp8 = args.dtype == "e4m3" or blocks
+    O, run = oracle_sample_runner(w, logits, x, wgu, wd, args.seed, fp8, blocks)
     n = args.steps + args.warmup
     per_step = max(0.5, min(20.0, 150.0 / max(1, n)))
     S = pick_sample(run, w.T, per_step)
@@ -517,8 +562,9 @@ def run_reference(args, w: Workload, rank: int, world: int):
 def config_of(w: Workload, args) -> dict:
     return {"workload": w.name, "T": w.T, "d_model": w.d, "d_ff": w.f, "experts": w.E, "top_k": w.k,
             "logit_bias": list(w.bias), "router": list(w.router), "seed": args.seed, "parallelism": "replicas",
-            "gemm_operands": ("e4m3, per-row activation and per-output-channel weight scales" if args.dtype == "e4m3"
-                              else "bf16"),
+            "gemm_operands": {"e4m3": "e4m3, per-row activation and per-output-channel weight scales",
+                              "e4m3b": "e4m3, power-of-two scales per 1x128 activation and 128x128 weight block"}
+                             .get(args.dtype, "bf16"),
             "l2": ("flushed between steps (512 MB write, outside the step events)" if args.flush_l2 else
                    "not flushed: inputs larger than L2 (the active experts' weights, >= 2.8 GB, stream "
                    "from HBM every step; L2 is 129 MB)")}
@@ -535,8 +581,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0, help="oracle CPU-baseline sample size, seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3"],
-                    help="operands of the grouped GEMMs: bf16 (moe_forward) or e4m3 (moe_forward_fp8)")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3", "e4m3b"],
+                    help="operands of the grouped GEMMs: bf16 (moe_forward), e4m3 (moe_forward_fp8) or e4m3 with "
+                         "block scales (moe_forward_fp8b)")
     ap.add_argument("--flush-l2", action="store_true",
                     help="write a 512 MB buffer between steps (default: rely on inputs larger than L2)")
     args = ap.parse_args()
@@ -588,7 +635,7 @@ def main():
             logits, x = r["inputs"]
             wgu, wd = (t.cpu() for t in r["host_weights"])
             line["cpu_baseline"] = cpu_baseline(w, logits, x, wgu, wd, args.cpu_budget_s, args.seed,
-                                                args.dtype == "e4m3")
+                                                args.dtype != "bf16", args.dtype == "e4m3b")
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

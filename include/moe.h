@@ -325,6 +325,53 @@ MOE_API int moe_forward_fp8(const void* x, const float* logits, const void* w8_g
                             const void* w8_down, const float* s_down, int T, int d, int f, int E, int top_k,
                             void* out, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Blockwise FP8 variant: the scales vary along K.  Activations (x and h rows) are scaled per
+ * 1 x 128 block (one scale per 128 consecutive values of a row), weights per 128 x 128 block of
+ * (output column, K).  Block scales are powers of two — the smallest power of two P with
+ * fl(absmax / 448) <= P, at least 2^-126, 1 for an all-zero block (representable as UE8M0, the
+ * scale encoding of the DeepGEMM write-up's SM100 path, section on the FP4 indexer) — and codes
+ * are E4M3(v / P) (exact scaling; round to nearest even, saturating).  The GEMM sums each 128-deep
+ * block on the tensor cores and adds block b's partial times (scale_row[b] * scale_col[b]) in block
+ * order:  g[n] = sum_b (sum_{i in b} x8[i] * W8[e][n][i]) * (sx[r][b] * sw[e][n/128][b]).
+ * "Blockwise FP8" (HPC-Ops page) and the Mega MoE epilogue's FP8 quantisation (DeepGEMM write-up,
+ * section 1.2) are the pages' context.  d and f must be multiples of 128; the GEMMs run on single
+ * SMs (each 128-deep partial product is promoted into fp32 registers by eight warps).
+ * ------------------------------------------------------------------------------------------- */
+
+/* Weights: W [E,K,N] bf16 (K, N multiples of 128) -> Wq blocked codes exactly as
+ * moe_quantize_weights_fp8 lays them out, and scale [E, N/128, K/128] fp32 (powers of two).
+ * W and Wq 16-byte aligned. */
+MOE_API int moe_quantize_weights_fp8b(const void* W, int E, int K, int N, void* Wq, float* scale,
+                                      moe_stream_t stream);
+
+/* Rows in 128-wide blocks: q[r] = codes of row src[r] of a (row r when src is NULL), scale [R, C/128].
+ * C a multiple of 128; other arguments as for moe_quantize_rows_fp8. */
+MOE_API int moe_quantize_rows_fp8b(const void* a, const int32_t* src, int R, int C, int src_rows, void* q,
+                                   float* scale, int32_t* status, moe_stream_t stream);
+
+/* Blockwise steps 3 and 4: as moe_grouped_gemm_gateup_swiglu_fp8 / moe_grouped_gemm_down_fp8 with
+ * block scales sx [M, d/128], s_gate_up [E, 2f/128, d/128], sh [M, f/128], s_down [E, d/128, f/128]. */
+MOE_API int moe_grouped_gemm_gateup_swiglu_fp8b(const void* x8_perm, const float* sx, const void* w8_gate_up,
+                                                const float* s_gate_up, const int32_t* offsets, int M, int d,
+                                                int f, int E, void* h, int32_t* status, moe_stream_t stream);
+MOE_API int moe_grouped_gemm_down_fp8b(const void* h8, const float* sh, const void* w8_down, const float* s_down,
+                                       const int32_t* offsets, int M, int d, int f, int E, int ksplit,
+                                       float* y_perm, int32_t* status, moe_stream_t stream);
+
+/* The blockwise FP8 layer in one call: route (+ permute, indices only), x rows quantised in blocks
+ * (gathered by src), blockwise gate+up GEMM (+ SwiGLU), h quantised in blocks, blockwise down GEMM,
+ * combine — 6 launches (7 when routing and the permutation run apart).  Workspace as for
+ * moe_forward_fp8 (14 offsets from moe_workspace_layout_fp8b), with sx [T*top_k, d/128] and
+ * sh [T*top_k, f/128]. */
+MOE_API size_t moe_workspace_size_fp8b(int T, int d, int f, int E, int top_k);
+MOE_API int moe_workspace_layout_fp8b(int T, int d, int f, int E, int top_k, size_t* offsets_out);
+MOE_API int moe_down_ksplit_fp8b(int T, int d, int f, int E, int top_k);
+MOE_API int moe_forward_fp8b_launch_count(int T, int E, int top_k);
+MOE_API int moe_forward_fp8b(const void* x, const float* logits, const void* w8_gate_up, const float* s_gate_up,
+                             const void* w8_down, const float* s_down, int T, int d, int f, int E, int top_k,
+                             void* out, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* Reads (synchronously: cudaMemcpy) a device status word — a stage call's `status` pointer, or
  * the workspace of moe_forward — into *code (0 = no device-side error). */
 MOE_API int moe_get_device_error(const void* status_or_workspace, int32_t* code);

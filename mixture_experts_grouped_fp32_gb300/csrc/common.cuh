@@ -101,11 +101,16 @@ struct GemmArgs {
     bool fp8 = false;
     const float* a_scale = nullptr;
     const float* b_scale = nullptr;
+    // Blockwise FP8 (with fp8): a_scale [M, K/128] (one per 128-wide row block), b_scale
+    // [E, N_total/128, K/128] (one per 128 x 128 block); its own kernel, N % 128 == 0.
+    bool fp8_blocks = false;
 };
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                 const char** why);
 cudaError_t launch_grouped_gemm_pair(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                      const char** why);
+// Blockwise FP8 (a.fp8_blocks): grouped_gemm_fp8b.cu.
+cudaError_t launch_grouped_gemm_fp8b(int kind, const GemmArgs& a, int num_sms, cudaStream_t s, const char** why);
 
 // 2-D bf16 tensor map over [rows, cols] (cols contiguous), box = [box_rows, 64 cols], 128-byte
 // swizzle; false if the driver's encoder is unavailable or rejects the operand.
@@ -125,5 +130,11 @@ cudaError_t launch_quantize_rows_fp8(const __nv_bfloat16* a, const int32_t* src,
                                      uint8_t* q, float* scale, int32_t* status, cudaStream_t s);
 cudaError_t launch_quantize_weights_fp8(const __nv_bfloat16* W, int E, int K, int N, uint8_t* Wq, float* scale,
                                         cudaStream_t s);
+// Blockwise FP8 (fp8.cu): 128-wide row blocks (scale [R, C/128]) and 128 x 128 weight blocks
+// (scale [E, N/128, K/128]; codes in the same blocked layout), power-of-two scales.
+cudaError_t launch_quantize_rows_fp8b(const __nv_bfloat16* a, const int32_t* src, int R, int C, int src_rows,
+                                      uint8_t* q, float* scale, int32_t* status, cudaStream_t s);
+cudaError_t launch_quantize_weights_fp8b(const __nv_bfloat16* W, int E, int K, int N, uint8_t* Wq, float* scale,
+                                         cudaStream_t s);
 
 }  // namespace moe

@@ -108,7 +108,98 @@ quantize_weights_kernel(const uint16_t* __restrict__ W, int K, int N, uint8_t* _
     }
 }
 
+// Blockwise rows: one CTA per output row r (source row src[r], or r), 128-wide blocks of C
+// (C % 128 == 0) -> codes and one power-of-two scale per block, scale [R, C/128].  Half a warp per
+// block (16 lanes x 8 values); a warp takes two blocks at a time.
+__global__ void __launch_bounds__(kQThreads)
+quantize_rows_blocks_kernel(const uint4* __restrict__ a, const int32_t* __restrict__ src, int R, int C,
+                            int src_rows, uint2* __restrict__ q, float* __restrict__ scale,
+                            int32_t* __restrict__ status) {
+    pdl_wait();
+    pdl_trigger();
+    const int r = blockIdx.x;
+    if (r >= R) return;
+    int s = src ? __ldg(src + r) : r;
+    if (s < 0 || s >= src_rows) {  // bad src: a zero row, reported
+        if (threadIdx.x == 0) flag_status(status, MOE_STATUS_BAD_SRC);
+        s = -1;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int cv = C / 8, nblk = C / 128;
+    const uint4* row = a + static_cast<size_t>(s < 0 ? 0 : s) * cv;
+    for (int bp = warp; bp < (nblk + 1) / 2; bp += kQThreads / 32) {  // warp-uniform trip count
+        const int b = 2 * bp + (lane >> 4);
+        const bool valid = b < nblk;
+        const int v = b * 16 + (lane & 15);
+        uint4 p = make_uint4(0, 0, 0, 0);
+        if (valid && s >= 0) p = __ldg(row + v);
+        float m = absmax8(p);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));  // within 16 lanes
+        const float P = pow2_block_scale(m);
+        if (valid) {
+            q[static_cast<size_t>(r) * cv + v] = codes8(p, 1.0f / P);
+            if ((lane & 15) == 0) scale[static_cast<size_t>(r) * nblk + b] = P;
+        }
+    }
+}
+
+// Blockwise weights: W [E, K, N] bf16 -> blocked codes (as quantize_weights_kernel) and one
+// power-of-two scale per 128 x 128 block of (output column, K), scale [E, N/128, K/128].  CTA
+// (n block, k block, e): the block through shared memory, its absmax, then 64 codes per thread
+// (one output column, half of the K block) written as 64 contiguous bytes.
+constexpr int kWB = 128;
+__global__ void __launch_bounds__(kQThreads)
+quantize_weights_blocks_kernel(const uint16_t* __restrict__ W, int K, int N, uint8_t* __restrict__ Wq,
+                               float* __restrict__ scale) {
+    __shared__ uint16_t tile[kWB][kWB + 2];  // [k][n], padded against bank conflicts in the column reads
+    __shared__ float red[kQThreads / 32];
+    const int nb = blockIdx.x, kb = blockIdx.y, e = blockIdx.z;
+    const uint16_t* We = W + static_cast<size_t>(e) * K * N;
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < kWB * kWB / 2; i += kQThreads) {  // bf16 pairs
+        const int k = i / (kWB / 2), n2 = i % (kWB / 2);
+        const uint32_t w2 = __ldg(reinterpret_cast<const uint32_t*>(We + static_cast<size_t>(kb * kWB + k) * N + nb * kWB) + n2);
+        tile[k][2 * n2] = static_cast<uint16_t>(w2 & 0xFFFFu);
+        tile[k][2 * n2 + 1] = static_cast<uint16_t>(w2 >> 16);
+        m = fmaxf(m, fmaxf(fabsf(bf16_lo(w2)), fabsf(bf16_hi(w2))));
+    }
+    const float amax = block_max(m, red);
+    const float P = pow2_block_scale(amax), inv = 1.0f / P;
+    if (threadIdx.x == 0) scale[(static_cast<size_t>(e) * (N / kWB) + nb) * (K / kWB) + kb] = P;
+    __syncthreads();
+    const int n = threadIdx.x >> 1, k0 = (threadIdx.x & 1) * 64;  // output column, K half
+    const int gn = nb * kWB + n;
+    uint8_t* dst = Wq + static_cast<size_t>(e) * N * K + static_cast<size_t>(gn >> 6) * K * 64 +
+                   static_cast<size_t>(kb) * 8192 + (gn & 63) * 128 + k0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {  // 4 x 16 codes
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float v = __uint_as_float(static_cast<uint32_t>(tile[k0 + c * 16 + j][n]) << 16) * inv;
+            o[j >> 2] |= static_cast<uint32_t>(to_e4m3(v)) << (8 * (j & 3));
+        }
+        reinterpret_cast<uint4*>(dst)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_rows_fp8b(const __nv_bfloat16* a, const int32_t* src, int R, int C, int src_rows,
+                                      uint8_t* q, float* scale, int32_t* status, cudaStream_t s) {
+    if (R == 0) return cudaSuccess;
+    return launch_k(kPdlQuant, quantize_rows_blocks_kernel, dim3(R), dim3(kQThreads), 0, s,
+                    reinterpret_cast<const uint4*>(a), src, R, C, src_rows, reinterpret_cast<uint2*>(q), scale,
+                    status);
+}
+
+cudaError_t launch_quantize_weights_fp8b(const __nv_bfloat16* W, int E, int K, int N, uint8_t* Wq, float* scale,
+                                         cudaStream_t s) {
+    const dim3 grid(N / kWB, K / kWB, E);
+    quantize_weights_blocks_kernel<<<grid, kQThreads, 0, s>>>(reinterpret_cast<const uint16_t*>(W), K, N, Wq, scale);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_rows_fp8(const __nv_bfloat16* a, const int32_t* src, int R, int C, int src_rows,
                                      uint8_t* q, float* scale, int32_t* status, cudaStream_t s) {

@@ -29,6 +29,18 @@ __device__ __forceinline__ float absmax8(uint4 p) {
 __device__ __forceinline__ float fp8_inv(float amax) { return amax > 0.0f ? 448.0f / amax : 1.0f; }
 __device__ __forceinline__ float fp8_scale(float amax) { return amax > 0.0f ? amax / 448.0f : 1.0f; }
 
+// Blockwise scale of a block with absolute maximum amax: the smallest power of two P with
+// fl(amax / 448) <= P, at least 2^-126 (so 1/P is a finite power of two), 1 for an all-zero block.
+// frexpf / ldexpf are exact; the division is IEEE (no fast-math), so host and device agree.
+__device__ __forceinline__ float pow2_block_scale(float amax) {
+    if (!(amax > 0.0f)) return 1.0f;
+    const float q = amax / 448.0f;
+    int e = 0;
+    const float m = frexpf(q, &e);
+    const float p = (m == 0.5f) ? q : ldexpf(1.0f, e);
+    return fmaxf(p, 1.1754943508222875e-38f);  // 2^-126
+}
+
 // Eight bf16 values -> eight E4M3 codes (byte i = code of value i).
 __device__ __forceinline__ uint2 codes8(uint4 p, float inv) {
     const uint32_t w[4] = {p.x, p.y, p.z, p.w};

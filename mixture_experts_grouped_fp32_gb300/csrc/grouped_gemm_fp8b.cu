@@ -1,0 +1,497 @@
+// grouped_gemm_fp8b.cu — the two grouped GEMMs of the blockwise FP8 layer on the sm_103a tensor
+// cores: E4M3 operands whose scales vary along K — one per 128-wide block of an activation row and
+// one per 128 x 128 block of (output column, K) of the weights, all powers of two.
+//
+//   kind 0: for the rows r of expert e, g[n] = sum_b P_b[r][n] * (sx[r][b] * sw[e][n/128][b]) with
+//           P_b the 128-deep partial product of K block b (likewise u), h[r] = bf16(silu(g) * u);
+//   kind 1: y[r][m] = sum_b P_b[r][m] * (sh[r][b] * sw[e][m/128][b]), fp32, optionally split over K.
+//
+// The scales do not factor out of the K sum, so the accumulation over K blocks cannot stay on the
+// tensor cores: a stage is exactly one K block (128 codes, one 128-byte swizzle row), the MMA
+// thread writes each block's partial product into one of four 128-column tensor-memory buffers
+// (fresh, not accumulated), and eight promotion warps read it, multiply it by that block's
+// scale_row * scale_col and add it into fp32 registers (a fused multiply-add: the scales are powers
+// of two, so the product is exact and the add rounds once, as in the block-by-block sum it
+// restates).  The item's epilogue (SwiGLU or the fp32 store) then runs from those registers.
+// Blockwise FP8 is named on the HPC-Ops page; the DeepGEMM PR #304 write-up's SM100 path encodes
+// its block scale factors as UE8M0 (powers of two), which these scales are.
+//
+// Tiles are sized for the promotion: every item covers 128 accumulator columns, 64 per promotion
+// thread (two warps per tensor-memory lane quarter):
+//   normal   UMMA M = 128 rows x N = 128 weight columns; kind 0: gate n0..n0+63 and up f+n0..f+n0+63
+//            (64 h columns), kind 1: 128 y columns.  Weights arrive as whole 8 KB blocks of the
+//            blocked layout (64 rows x 128 K).
+//   swapped  (experts with at most 64 rows) UMMA M = 128 weight columns x N = rows rounded to 16,
+//            two MMAs per K step into columns [0, N) and [64, 64 + N): kind 0 gate and up of 128 h
+//            columns, kind 1 y columns n0.. and n0+128.. — so a swapped item spans two normal
+//            N-tiles and streams 32 KB of weights per stage.
+// Ring: five 40 KB stages (normal: 16 KB activations + 16 KB weights; swapped: up to 8 KB of
+// tokens, then 32 KB of weights).  Scheduling as in grouped_gemm.cu: (expert, N-tile, M-tile,
+// K-slice) items, expert-major, static round-robin over one persistent CTA per SM.  Every wait is
+// bounded (1 s) and reports MOE_STATUS_WAIT_TIMEOUT.
+#include "common.cuh"
+#include "tcgen05.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BKE = 128;                           // K codes per stage = one scale block
+constexpr int STAGES = 5;
+constexpr int STAGE_BYTES = 40 * 1024;
+constexpr int TOK_BOX_ROWS = 32;
+constexpr int TOK_BOX_BYTES = TOK_BOX_ROWS * BKE;  // 4 KB
+constexpr int A_BYTES = BM * BKE;                  // 16 KB
+constexpr int WBOX64 = 64 * BKE;                   // one weight block, 8 KB
+constexpr int WBOX128 = 128 * BKE;                 // two weight blocks, 16 KB
+constexpr int SWAP_W_OFF = 2 * TOK_BOX_BYTES;      // swapped stage: tokens (<= 64 rows), then weights
+constexpr int SWAP_MAX_ROWS = 64;
+constexpr int PART_COLS = 128;                     // tensor-memory columns per partial buffer
+constexpr int NUM_PART = 4;
+constexpr int TMEM_COLS = NUM_PART * PART_COLS;    // 512
+constexpr int EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;   // warp 0 TMA, warp 1 MMA, warps 2-9 promotion
+constexpr int MAX_E = 256;
+constexpr int SMEM_BYTES = 232448;
+static_assert(SWAP_W_OFF + 2 * WBOX128 <= STAGE_BYTES && A_BYTES + WBOX128 <= STAGE_BYTES, "stage layout");
+
+// Output columns of a normal item (a swapped one covers twice as many).
+template <int KIND>
+constexpr int bn_normal() { return KIND == 0 ? 64 : 128; }
+
+struct Ctl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t pfull[NUM_PART];   // a K block's partial product is in buffer p
+    uint64_t pempty[NUM_PART];  // the promotion warps have read buffer p
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int total_items;
+    int seg[MAX_E + 1];
+    int item_start[MAX_E + 1];
+};
+static_assert(STAGES * STAGE_BYTES + 1024 + sizeof(Ctl) <= SMEM_BYTES, "shared memory budget");
+
+struct Item {
+    int e, n_tile, m_tile, kslice, row0, rows;
+    bool swap;
+};
+
+// Work items of an expert with cnt rows.
+__device__ __forceinline__ int expert_items(int cnt, int N, int bn, int ksplit, int swap_max) {
+    if (cnt == 0) return 0;
+    if (cnt <= swap_max) return ((N + 2 * bn - 1) / (2 * bn)) * ksplit;
+    return ((N + bn - 1) / bn) * ((cnt + BM - 1) / BM) * ksplit;
+}
+
+// Item i: expert by binary search over item_start, then N-tile, M-tile, K-slice.
+__device__ __forceinline__ Item decode_item(const Ctl& c, int E, int ksplit, int swap_max, int i) {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (c.item_start[mid] <= i) lo = mid; else hi = mid;
+    }
+    Item it;
+    it.e = lo;
+    const int cnt = c.seg[lo + 1] - c.seg[lo];
+    it.swap = cnt <= swap_max;
+    const int mt = it.swap ? 1 : (cnt + BM - 1) / BM;
+    const int j = i - c.item_start[lo];
+    const int per_n = mt * ksplit;
+    it.n_tile = j / per_n;
+    const int r = j - it.n_tile * per_n;
+    it.m_tile = r / ksplit;
+    it.kslice = r - it.m_tile * ksplit;
+    it.row0 = c.seg[lo] + it.m_tile * BM;
+    it.rows = min(BM, cnt - it.m_tile * BM);
+    return it;
+}
+
+__device__ __forceinline__ void raise_abort(Ctl& c, int32_t* status) {
+    *reinterpret_cast<volatile int*>(&c.abort_flag) = 1;
+    flag_status(status, MOE_STATUS_WAIT_TIMEOUT);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+    __nv_bfloat16 b = __float2bfloat16_rn(v);
+    return *reinterpret_cast<uint16_t*>(&b);
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
+                         const __grid_constant__ CUtensorMap tmB128, const __grid_constant__ CUtensorMap tmB64,
+                         const int32_t* __restrict__ offsets, int M, int K, int N, int E, int ksplit, int swap_max,
+                         const float* __restrict__ a_scale, const float* __restrict__ b_scale, void* __restrict__ out,
+                         int32_t* __restrict__ status) {
+    constexpr int BN = bn_normal<KIND>();
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    uint8_t* tiles = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    Ctl& c = *reinterpret_cast<Ctl*>(tiles + STAGES * STAGE_BYTES);
+    const volatile int* abort_flag = &c.abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int num_kb = K / BKE;
+    const int kb_per = (num_kb + ksplit - 1) / ksplit;
+    const int wrows = KIND == 0 ? 2 * N : N;  // weight rows (output columns) per expert
+    const int nbw = wrows / 128;              // weight scale blocks per expert along N
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(&c.full[s], 1);
+            ptx::mbar_init(&c.empty[s], 1);
+        }
+        for (int p = 0; p < NUM_PART; ++p) {
+            ptx::mbar_init(&c.pfull[p], 1);
+            ptx::mbar_init(&c.pempty[p], EPI_WARPS);
+        }
+        ptx::mbar_init(&c.drain, 1);
+        c.abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmA32);
+        ptx::prefetch_tensormap(&tmB128);
+        ptx::prefetch_tensormap(&tmB64);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&c.tmem_base, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (warp == 2) {
+        // Validate offsets and build the per-expert item prefix.
+        for (int e = lane; e <= E; e += 32) c.seg[e] = __ldg(offsets + e);
+        __syncwarp();
+        bool ok = true;
+        for (int e = lane; e < E; e += 32) ok = ok && c.seg[e] <= c.seg[e + 1];
+        if (lane == 0) ok = ok && c.seg[0] >= 0 && c.seg[E] <= M;
+        ok = __all_sync(0xffffffffu, ok);
+        const int per = (E + 31) / 32;
+        const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+        int sum = 0;
+        if (ok)
+            for (int e = e0; e < e1; ++e) sum += expert_items(c.seg[e + 1] - c.seg[e], N, BN, ksplit, swap_max);
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+        for (int e = e0; e < e1; ++e) {
+            c.item_start[e] = run;
+            if (ok) run += expert_items(c.seg[e + 1] - c.seg[e], N, BN, ksplit, swap_max);
+        }
+        if (lane == 31) {
+            c.item_start[E] = incl;
+            c.total_items = incl;
+        }
+        if (!ok && lane == 0) flag_status(status, MOE_STATUS_BAD_OFFSETS);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+
+    const uint32_t tmem_base = c.tmem_base;
+    const int total = c.total_items;
+    uint32_t fill_parity[STAGES];
+    int filled_mask = 0;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        const uint64_t pol_act = ptx::policy_evict_last();
+        const uint64_t pol_wgt = ptx::policy_evict_normal();
+        uint32_t stage = 0, phase = 0;
+        bool aborted = false;
+        for (int i = blockIdx.x; i < total && !aborted; i += gridDim.x) {
+            const Item it = decode_item(c, E, ksplit, swap_max, i);
+            const int n0 = it.n_tile * (it.swap ? 2 * BN : BN);
+            const int nbox32 = (it.rows + TOK_BOX_ROWS - 1) / TOK_BOX_ROWS;
+            const uint32_t tx = it.swap ? 2 * WBOX128 + nbox32 * TOK_BOX_BYTES : A_BYTES + 2 * WBOX64;
+            // Weight rows (output columns) of the item's blocks.
+            const int wr0 = it.e * wrows + n0;
+            const int wr1 = KIND == 0 ? wr0 + N : wr0 + 128;  // swapped kind 0: up; kind 1: the second half
+            const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!ptx::mbar_wait(&c.empty[stage], phase ^ 1u, abort_flag)) {
+                    raise_abort(c, status);
+                    aborted = true;
+                    break;
+                }
+                uint8_t* st = tiles + stage * STAGE_BYTES;
+                ptx::mbar_arrive_expect_tx(&c.full[stage], tx);
+                if (it.swap) {
+                    for (int q = 0; q < nbox32; ++q)
+                        ptx::tma_load_2d(st + q * TOK_BOX_BYTES, &tmA32, &c.full[stage], kb * BKE,
+                                         it.row0 + q * TOK_BOX_ROWS, pol_act);
+                    ptx::tma_load_4d(st + SWAP_W_OFF, &tmB128, &c.full[stage], 0, 0, kb, wr0 / 64, pol_wgt);
+                    ptx::tma_load_4d(st + SWAP_W_OFF + WBOX128, &tmB128, &c.full[stage], 0, 0, kb, wr1 / 64, pol_wgt);
+                } else {
+                    ptx::tma_load_2d(st, &tmA, &c.full[stage], kb * BKE, it.row0, pol_act);
+                    if (KIND == 0) {  // gate n0..n0+63, then up f+n0..f+n0+63: one block each
+                        ptx::tma_load_4d(st + A_BYTES, &tmB64, &c.full[stage], 0, 0, kb, wr0 / 64, pol_wgt);
+                        ptx::tma_load_4d(st + A_BYTES + WBOX64, &tmB64, &c.full[stage], 0, 0, kb, (wr0 + N) / 64,
+                                         pol_wgt);
+                    } else {  // 128 output columns: two blocks
+                        ptx::tma_load_4d(st + A_BYTES, &tmB128, &c.full[stage], 0, 0, kb, wr0 / 64, pol_wgt);
+                    }
+                }
+                fill_parity[stage] = phase;
+                filled_mask |= 1 << stage;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer: one partial product per K block, four buffers ----------------
+        constexpr uint32_t idesc_normal = ptx::idesc_e4m3_f32(BM, PART_COLS, 0, 0);
+        uint32_t stage = 0, phase = 0, pb = 0, pph = 0;
+        bool aborted = false;
+        for (int i = blockIdx.x; i < total && !aborted; i += gridDim.x) {
+            const Item it = decode_item(c, E, ksplit, swap_max, i);
+            const uint32_t ntok = (static_cast<uint32_t>(it.rows) + 15u) & ~15u;
+            const uint32_t idesc_swap = ptx::idesc_e4m3_f32(BM, ntok, 0, 0);
+            const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!ptx::mbar_wait(&c.full[stage], phase, abort_flag) ||
+                    !ptx::mbar_wait(&c.pempty[pb], pph ^ 1u, abort_flag)) {
+                    raise_abort(c, status);
+                    aborted = true;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + pb * PART_COLS;
+                const uint32_t sa = ptx::smem_u32(tiles + stage * STAGE_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BKE / 32; ++kk) {
+                    const uint32_t accum = kk != 0 ? 1u : 0u;  // a fresh partial per K block
+                    const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+                    if (it.swap) {
+                        // Weights (K-major, 128 rows) as A, the tokens (K-major) as B.
+                        const uint64_t tok = ptx::smem_desc_sw128(sa, 16, 1024);
+                        const uint64_t w0 = ptx::smem_desc_sw128(sa + SWAP_W_OFF, 16, 1024);
+                        const uint64_t w1 = ptx::smem_desc_sw128(sa + SWAP_W_OFF + WBOX128, 16, 1024);
+                        ptx::mma_f8_ss(d_tmem, w0 + off, tok + off, idesc_swap, accum);
+                        ptx::mma_f8_ss(d_tmem + 64, w1 + off, tok + off, idesc_swap, accum);
+                    } else {
+                        const uint64_t a = ptx::smem_desc_sw128(sa, 16, 1024);
+                        const uint64_t b = ptx::smem_desc_sw128(sa + A_BYTES, 16, 1024);
+                        ptx::mma_f8_ss(d_tmem, a + off, b + off, idesc_normal, accum);
+                    }
+                }
+                ptx::mma_commit(&c.empty[stage]);
+                ptx::mma_commit(&c.pfull[pb]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (++pb == NUM_PART) {
+                    pb = 0;
+                    pph ^= 1u;
+                }
+            }
+        }
+    } else if (warp >= 2) {
+        // ---------------- promotion + epilogue: per-block scales into fp32 registers ----------------
+        // Warp w: tensor-memory lane quarter (w & 3), half hh = (w - 2) >> 2 of the 128 partial
+        // columns, as two 32-column groups c0, c1:
+        //   normal kind 0: gate [32hh, +32) and up [64 + 32hh, +32) — the same 32 h columns;
+        //   normal kind 1: [64hh, +32) and [64hh + 32, +32);
+        //   swapped: tokens [32hh, +32) of the two MMAs, [32hh, +32) and [64 + 32hh, +32).
+        const int quarter = warp & 3, hh = (warp - 2) >> 2;
+        const int r_local = quarter * 32 + lane;
+        uint32_t pb = 0, pph = 0;
+        bool aborted = false;
+        for (int i = blockIdx.x; i < total && !aborted; i += gridDim.x) {
+            const Item it = decode_item(c, E, ksplit, swap_max, i);
+            const int n0 = it.n_tile * (it.swap ? 2 * BN : BN);
+            const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
+            const bool normal1 = KIND == 1 && !it.swap;
+            const uint32_t c0 = normal1 ? 64 * hh : 32 * hh, c1 = normal1 ? 64 * hh + 32 : 64 + 32 * hh;
+            // Weight scale blocks of the two groups (a group past N is computed, never stored).
+            int wb0, wb1;
+            if (KIND == 0) {
+                wb0 = n0 / 128;
+                wb1 = (N + n0) / 128;
+            } else {
+                wb0 = n0 / 128;
+                wb1 = it.swap ? min(nbw - 1, (n0 + 128) / 128) : wb0;
+            }
+            const float* sw0p = b_scale + (static_cast<size_t>(it.e) * nbw + wb0) * num_kb;
+            const float* sw1p = b_scale + (static_cast<size_t>(it.e) * nbw + wb1) * num_kb;
+            const bool row_ok = r_local < it.rows;
+            const size_t grow = static_cast<size_t>(it.row0 + r_local);
+            // Does this warp hold any result column?  (Warp-uniform.)
+            const bool active = it.swap ? 32 * hh < it.rows : quarter * 32 < it.rows;
+            // The row / token scale this lane loads: its row (normal) or token 32hh + lane (swapped).
+            const int tok = 32 * hh + lane;
+            const bool sc_ok = it.swap ? tok < it.rows : row_ok;
+            const float* srp = a_scale + (it.swap ? static_cast<size_t>(it.row0 + (sc_ok ? tok : 0)) : (sc_ok ? grow : 0)) *
+                                             num_kb;
+            float A0[32], A1[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                A0[j] = 0.0f;
+                A1[j] = 0.0f;
+            }
+            float sw0 = 0.0f, sw1 = 0.0f, sr = 0.0f;
+            if (kb0 < kb1) {
+                sw0 = __ldg(sw0p + kb0);
+                sw1 = __ldg(sw1p + kb0);
+                sr = sc_ok ? __ldg(srp + kb0) : 0.0f;
+            }
+            for (int kb = kb0; kb < kb1; ++kb) {
+                // The next K block's scales, loaded before this block's partial is waited for.
+                const bool more = kb + 1 < kb1;
+                const float nsw0 = more ? __ldg(sw0p + kb + 1) : 0.0f;
+                const float nsw1 = more ? __ldg(sw1p + kb + 1) : 0.0f;
+                const float nsr = (more && sc_ok) ? __ldg(srp + kb + 1) : 0.0f;
+                if (!ptx::mbar_wait(&c.pfull[pb], pph, abort_flag)) {
+                    raise_abort(c, status);
+                    aborted = true;
+                    break;
+                }
+                ptx::tc_fence_after();
+                if (active) {
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + pb * PART_COLS;
+                    uint32_t v0[32], v1[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + c0, v0);
+                    ptx::tmem_ld_32x32b_x32(taddr + c1, v1);
+                    ptx::tmem_ld_wait();
+                    if (!it.swap) {
+                        const float s0 = sr * sw0, s1 = sr * sw1;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            A0[j] = fmaf(__uint_as_float(v0[j]), s0, A0[j]);
+                            A1[j] = fmaf(__uint_as_float(v1[j]), s1, A1[j]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {  // column j is token 32hh + j: lane j's scale
+                            const float sj = __shfl_sync(0xffffffffu, sr, j);
+                            A0[j] = fmaf(__uint_as_float(v0[j]), sj * sw0, A0[j]);
+                            A1[j] = fmaf(__uint_as_float(v1[j]), sj * sw1, A1[j]);
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&c.pempty[pb]);
+                if (++pb == NUM_PART) {
+                    pb = 0;
+                    pph ^= 1u;
+                }
+                sw0 = nsw0;
+                sw1 = nsw1;
+                sr = nsr;
+            }
+            if (aborted) break;
+            // ------------------------------ epilogue from registers ------------------------------
+            if (!it.swap) {
+                if (!row_ok) continue;
+                if (KIND == 0) {
+                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + grow * N + n0 + 32 * hh);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t p[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            p[q] = pack_bf16x2(silu_mul(A0[8 * v + 2 * q], A1[8 * v + 2 * q]),
+                                               silu_mul(A0[8 * v + 2 * q + 1], A1[8 * v + 2 * q + 1]));
+                        dst[v] = make_uint4(p[0], p[1], p[2], p[3]);
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) +
+                                                            static_cast<size_t>(it.kslice) * M * N + grow * N + n0 + 64 * hh);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        dst[v] = make_float4(A0[4 * v], A0[4 * v + 1], A0[4 * v + 2], A0[4 * v + 3]);
+                        dst[8 + v] = make_float4(A1[4 * v], A1[4 * v + 1], A1[4 * v + 2], A1[4 * v + 3]);
+                    }
+                }
+            } else {
+                // Lane = weight column n0 + r_local (kind 1: and n0 + 128 + r_local), column j = token.
+                const int col0 = n0 + r_local;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int t = 32 * hh + j;
+                    if (t < it.rows) {
+                        const size_t rr = static_cast<size_t>(it.row0 + t);
+                        if (KIND == 0) {
+                            reinterpret_cast<uint16_t*>(out)[rr * N + col0] = bf16_bits(silu_mul(A0[j], A1[j]));
+                        } else {
+                            float* y = reinterpret_cast<float*>(out) + static_cast<size_t>(it.kslice) * M * N;
+                            if (col0 < N) y[rr * N + col0] = A0[j];
+                            if (col0 + 128 < N) y[rr * N + col0 + 128] = A1[j];
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ------------------------------ teardown ------------------------------
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0 && lane == 0 && c.abort_flag) {
+        for (int s = 0; s < STAGES; ++s)
+            if (filled_mask & (1 << s)) ptx::mbar_wait_ns(&c.full[s], fill_parity[s], 100000000ull);
+    }
+    if (warp == 1 && lane == 0) {
+        ptx::mma_commit(&c.drain);
+        ptx::mbar_wait_ns(&c.drain, 0, 100000000ull);
+    }
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+template <int KIND>
+cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const char** why) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_fp8b_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_BYTES);
+        if (e != cudaSuccess) {
+            *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+            return e;
+        }
+        attr_set[dev] = true;
+    }
+    CUtensorMap mA, mA32, mB128, mB64;
+    const uint64_t wrows = static_cast<uint64_t>(a.E) * (KIND == 0 ? 2ull * a.N : static_cast<uint64_t>(a.N));
+    if (!make_tensor_map_u8(&mA, a.A, a.K, a.M, BM) || !make_tensor_map_u8(&mA32, a.A, a.K, a.M, TOK_BOX_ROWS) ||
+        !make_tensor_map_w8(&mB128, a.B, a.K, wrows, 128) || !make_tensor_map_w8(&mB64, a.B, a.K, wrows, 64)) {
+        *why = "cuTensorMapEncodeTiled failed (driver entry point missing or bad operand)";
+        return cudaErrorInvalidValue;
+    }
+    const int swap_max = a.swap_max < 0 ? 0 : (a.swap_max > SWAP_MAX_ROWS ? SWAP_MAX_ROWS : a.swap_max);
+    const int ksplit = KIND == 0 ? 1 : a.ksplit;
+    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_fp8b_kernel<KIND>, dim3(num_sms),
+                    dim3(NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB128, mB64, a.offsets, a.M, a.K, a.N, a.E, ksplit,
+                    swap_max, a.a_scale, a.b_scale, a.out, a.status);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_fp8b(int kind, const GemmArgs& a, int num_sms, cudaStream_t s, const char** why) {
+    if (a.N % 128 != 0 || a.K % 128 != 0 || !a.a_scale || !a.b_scale) {
+        *why = "blockwise FP8 grouped GEMM: N and K must be multiples of 128, scales given";
+        return cudaErrorInvalidValue;
+    }
+    return kind == 0 ? launch_kind<0>(a, num_sms, s, why) : launch_kind<1>(a, num_sms, s, why);
+}
+
+}  // namespace moe

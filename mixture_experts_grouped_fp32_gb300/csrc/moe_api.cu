@@ -200,14 +200,15 @@ int inject_stall() {
 // already saturate HBM, and a split only adds partial-sum traffic (T=32: 0.138 -> 0.142 ms);
 // above two waves the tail is small.  MOE_DOWN_KSPLIT overrides the choice.  The result never
 // leaves a slice without K blocks.
-// The FP8 layer (fp8 = true) has 128-deep K blocks.
-int down_ksplit(int T, int d, int f, int E, int k, bool fp8 = false) {
+// The FP8 layers (fp8 = true) have 128-deep K blocks; the blockwise one (blocks = true) always
+// runs the 1-SM kernel.
+int down_ksplit(int T, int d, int f, int E, int k, bool fp8 = false, bool blocks = false) {
     const long long M = static_cast<long long>(T) * k;
     const int num_kb = f / (fp8 ? 128 : 64);
     int S;
     if (const char* v = std::getenv("MOE_DOWN_KSPLIT")) {
         S = std::atoi(v);
-    } else if (use_pair(M, E, d, 1, fp8)) {
+    } else if (!blocks && use_pair(M, E, d, 1, fp8)) {
         S = 1;  // 256-row pair items: measured best unsplit (Mixtral T=512: 0.510 ms/layer vs 0.524 at 2)
     } else {
         const long long mtiles = (M + 127) / 128 + (M < E ? M : E);
@@ -251,8 +252,10 @@ struct Layout8 {
     size_t status, idx, w, counts, offsets, src, dest, x8, sx, h, h8, sh, y_perm, total;
 };
 
-Layout8 layout_fp8(int T, int d, int f, int E, int k) {
+// blocks = true: the blockwise layer, whose sx and sh hold one scale per 128-wide block.
+Layout8 layout_fp8(int T, int d, int f, int E, int k, bool blocks = false) {
     const size_t M = static_cast<size_t>(T) * k;
+    const size_t nsx = blocks ? static_cast<size_t>(d / 128) : 1, nsh = blocks ? static_cast<size_t>(f / 128) : 1;
     Layout8 L;
     size_t o = 0;
     L.status = o; o += 256;
@@ -263,11 +266,11 @@ Layout8 layout_fp8(int T, int d, int f, int E, int k) {
     L.src = o; o = align256(o + M * 4);
     L.dest = o; o = align256(o + M * 4);
     L.x8 = o; o = align256(o + M * d);
-    L.sx = o; o = align256(o + M * 4);
+    L.sx = o; o = align256(o + M * nsx * 4);
     L.h = o; o = align256(o + M * f * 2);
     L.h8 = o; o = align256(o + M * f);
-    L.sh = o; o = align256(o + M * 4);
-    L.y_perm = o; o = align256(o + static_cast<size_t>(down_ksplit(T, d, f, E, k, true)) * M * d * 4);
+    L.sh = o; o = align256(o + M * nsh * 4);
+    L.y_perm = o; o = align256(o + static_cast<size_t>(down_ksplit(T, d, f, E, k, true, blocks)) * M * d * 4);
     L.total = o;
     return L;
 }
@@ -405,6 +408,63 @@ int run_layer_fp8(const void* x, const float* logits, const void* wgu8, const fl
     g2.b_scale = sd;
     if ((e = launch_grouped_gemm(1, g2, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "FP8 down GEMM: %s (%s)", why, cudaGetErrorString(e));
+    if ((e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) !=
+        cudaSuccess)
+        return launched(e, "combine");
+    return ok();
+}
+
+// The blockwise FP8 layer: route (+ permute, indices only), x rows gathered by src and quantised
+// in 128-wide blocks, blockwise gate+up GEMM (+ SwiGLU, bf16 h), h quantised in blocks, blockwise
+// down GEMM, combine.
+int run_layer_fp8b(const void* x, const float* logits, const void* wgu8, const float* sgu, const void* wd8,
+                   const float* sd, int T, int d, int f, int E, int k, void* out, void* ws, int num_sms,
+                   cudaStream_t s) {
+    const Layout8 L = layout_fp8(T, d, f, E, k, true);
+    int32_t* status = at<int32_t>(ws, L.status);
+    int32_t* idx = at<int32_t>(ws, L.idx);
+    float* w = at<float>(ws, L.w);
+    int32_t* counts = at<int32_t>(ws, L.counts);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* src = at<int32_t>(ws, L.src);
+    int32_t* dest = at<int32_t>(ws, L.dest);
+    uint8_t* x8 = at<uint8_t>(ws, L.x8);
+    float* sx = at<float>(ws, L.sx);
+    auto* h = at<__nv_bfloat16>(ws, L.h);
+    uint8_t* h8 = at<uint8_t>(ws, L.h8);
+    float* sh = at<float>(ws, L.sh);
+    float* y = at<float>(ws, L.y_perm);
+    const int M = T * k;
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    cudaError_t e;
+    if (fuse_route_permute(T, E)) {
+        if ((e = launch_route_permute(logits, xb, T, d, E, k, idx, w, counts, offsets, src, dest, nullptr, status,
+                                      num_sms, s)) != cudaSuccess)
+            return launched(e, "route+permute");
+    } else {
+        if ((e = launch_route(logits, T, E, k, idx, w, status, s)) != cudaSuccess) return launched(e, "route");
+        if ((e = launch_permute(idx, xb, T, d, E, k, counts, offsets, src, dest, nullptr, status, num_sms, s)) !=
+            cudaSuccess)
+            return launched(e, "permute");
+    }
+    if ((e = launch_quantize_rows_fp8b(xb, src, M, d, T, x8, sx, status, s)) != cudaSuccess)
+        return launched(e, "quantize x");
+    const char* why = "";
+    const int ksplit = down_ksplit(T, d, f, E, k, true, true);
+    GemmArgs g1{x8, wgu8, offsets, M, d, f, E, h, status, 1, swap_max_rows(), 0};
+    g1.fp8 = g1.fp8_blocks = true;
+    g1.a_scale = sx;
+    g1.b_scale = sgu;
+    if ((e = launch_grouped_gemm(0, g1, num_sms, s, &why)) != cudaSuccess)
+        return fail(MOE_ERR_CUDA, "blockwise FP8 gate+up GEMM: %s (%s)", why, cudaGetErrorString(e));
+    if ((e = launch_quantize_rows_fp8b(h, nullptr, M, f, M, h8, sh, status, s)) != cudaSuccess)
+        return launched(e, "quantize h");
+    GemmArgs g2{h8, wd8, offsets, M, f, d, E, y, status, ksplit, swap_max_rows(), 0};
+    g2.fp8 = g2.fp8_blocks = true;
+    g2.a_scale = sh;
+    g2.b_scale = sd;
+    if ((e = launch_grouped_gemm(1, g2, num_sms, s, &why)) != cudaSuccess)
+        return fail(MOE_ERR_CUDA, "blockwise FP8 down GEMM: %s (%s)", why, cudaGetErrorString(e));
     if ((e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) !=
         cudaSuccess)
         return launched(e, "combine");
@@ -872,6 +932,133 @@ int moe_forward_fp8(const void* x, const float* logits, const void* w8_gate_up, 
     if ((rc = check_device(&sms))) return rc;
     return run_layer_fp8(x, logits, w8_gate_up, s_gate_up, w8_down, s_down, T, d, f, E, top_k, out, workspace, sms,
                          static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------------------------
+// Blockwise FP8 variant (1 x 128 activation blocks, 128 x 128 weight blocks, power-of-two scales)
+// ---------------------------------------------------------------------------------------------
+size_t moe_workspace_size_fp8b(int T, int d, int f, int E, int top_k) {
+    if (check_shape_fp8(T, d, f, E, top_k, "moe_workspace_size_fp8b") != MOE_OK) return 0;
+    return layout_fp8(T, d, f, E, top_k, true).total;
+}
+
+int moe_workspace_layout_fp8b(int T, int d, int f, int E, int top_k, size_t* offsets_out) {
+    int rc = check_shape_fp8(T, d, f, E, top_k, "moe_workspace_layout_fp8b");
+    if (rc) return rc;
+    if (!offsets_out) return fail(MOE_ERR_INVALID_ARG, "moe_workspace_layout_fp8b: null pointer");
+    const Layout8 L = layout_fp8(T, d, f, E, top_k, true);
+    const size_t v[14] = {L.status, L.idx, L.w, L.counts, L.offsets, L.src, L.dest,
+                          L.x8, L.sx, L.h, L.h8, L.sh, L.y_perm, L.total};
+    for (int i = 0; i < 14; ++i) offsets_out[i] = v[i];
+    return ok();
+}
+
+int moe_down_ksplit_fp8b(int T, int d, int f, int E, int top_k) {
+    if (check_shape_fp8(T, d, f, E, top_k, "moe_down_ksplit_fp8b") != MOE_OK) return 0;
+    return down_ksplit(T, d, f, E, top_k, true, true);
+}
+
+int moe_forward_fp8b_launch_count(int T, int E, int top_k) {
+    if (check_shape(T, -1, 0, E, top_k, false) != MOE_OK) return -1;
+    if (T == 0) return 0;
+    return fuse_route_permute(T, E) ? 6 : 7;
+}
+
+int moe_quantize_weights_fp8b(const void* W, int E, int K, int N, void* Wq, float* scale, moe_stream_t stream) {
+    if (E < 1 || E > kMaxE || !dim_ok(K) || !dim_ok(N) || K % 128 != 0 || N % 128 != 0)
+        return fail(MOE_ERR_INVALID_ARG,
+                    "moe_quantize_weights_fp8b: E = %d in [1, %d], K = %d and N = %d multiples of 128 "
+                    "(<= %d) required",
+                    E, kMaxE, K, N, kMaxDim);
+    if (!W || !Wq || !scale) return fail(MOE_ERR_INVALID_ARG, "moe_quantize_weights_fp8b: null pointer");
+    if (!aligned16(W) || !aligned16(Wq) || (reinterpret_cast<uintptr_t>(scale) & 3u))
+        return fail(MOE_ERR_INVALID_ARG, "moe_quantize_weights_fp8b: W and Wq 16-byte, scale 4-byte aligned");
+    int sms, rc;
+    if ((rc = check_device(&sms))) return rc;
+    return launched(launch_quantize_weights_fp8b(static_cast<const __nv_bfloat16*>(W), E, K, N,
+                                                 static_cast<uint8_t*>(Wq), scale, static_cast<cudaStream_t>(stream)),
+                    "quantize weights (blockwise)");
+}
+
+int moe_quantize_rows_fp8b(const void* a, const int32_t* src, int R, int C, int src_rows, void* q, float* scale,
+                           int32_t* status, moe_stream_t stream) {
+    if (R < 0 || C < 128 || C % 128 != 0 || C > kMaxDim || src_rows < 0 || (!src && src_rows < R))
+        return fail(MOE_ERR_INVALID_ARG,
+                    "moe_quantize_rows_fp8b: R = %d >= 0, C = %d a multiple of 128 in [128, %d], src_rows = %d "
+                    "(>= R without src) required",
+                    R, C, kMaxDim, src_rows);
+    if (R == 0) return ok();
+    if (!a || !q || !scale) return fail(MOE_ERR_INVALID_ARG, "moe_quantize_rows_fp8b: null pointer");
+    if (!aligned16(a) || (reinterpret_cast<uintptr_t>(q) & 7u) || (reinterpret_cast<uintptr_t>(scale) & 3u))
+        return fail(MOE_ERR_INVALID_ARG, "moe_quantize_rows_fp8b: a 16-byte, q 8-byte, scale 4-byte aligned");
+    int sms, rc;
+    if ((rc = check_device(&sms))) return rc;
+    return launched(launch_quantize_rows_fp8b(static_cast<const __nv_bfloat16*>(a), src, R, C, src_rows,
+                                              static_cast<uint8_t*>(q), scale, status,
+                                              static_cast<cudaStream_t>(stream)),
+                    "quantize rows (blockwise)");
+}
+
+static int gemm8b_entry(int kind, const void* A, const float* sa, const void* B, const float* sb,
+                        const int32_t* offsets, int M, int d, int f, int E, int ksplit, void* out, int32_t* status,
+                        moe_stream_t stream, const char* name) {
+    int rc = check_shape_fp8(0, d, f, E, 1, name);
+    if (rc) return rc;
+    if (M < 0) return fail(MOE_ERR_INVALID_ARG, "%s: M = %d must be >= 0", name, M);
+    if (ksplit < 1 || ksplit > kMaxKSplit)
+        return fail(MOE_ERR_INVALID_ARG, "%s: ksplit = %d outside [1, %d]", name, ksplit, kMaxKSplit);
+    if (M == 0) return ok();
+    if (!A || !sa || !B || !sb || !offsets || !out) return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
+    if (!aligned16(A) || !aligned16(B) || !aligned16(out) || (reinterpret_cast<uintptr_t>(sa) & 3u) ||
+        (reinterpret_cast<uintptr_t>(sb) & 3u))
+        return fail(MOE_ERR_INVALID_ARG, "%s: operands must be 16-byte (scales 4-byte) aligned", name);
+    int sms;
+    if ((rc = check_device(&sms))) return rc;
+    GemmArgs g = kind == 0 ? GemmArgs{A, B, offsets, M, d, f, E, out, status, 1, swap_max_rows(), 0}
+                           : GemmArgs{A, B, offsets, M, f, d, E, out, status, ksplit, swap_max_rows(), 0};
+    g.fp8 = g.fp8_blocks = true;
+    g.a_scale = sa;
+    g.b_scale = sb;
+    const char* why = "";
+    cudaError_t e = launch_grouped_gemm(kind, g, sms, static_cast<cudaStream_t>(stream), &why);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s (%s)", name, why, cudaGetErrorString(e));
+    return ok();
+}
+
+int moe_grouped_gemm_gateup_swiglu_fp8b(const void* x8_perm, const float* sx, const void* w8_gate_up,
+                                        const float* s_gate_up, const int32_t* offsets, int M, int d, int f, int E,
+                                        void* h, int32_t* status, moe_stream_t stream) {
+    return gemm8b_entry(0, x8_perm, sx, w8_gate_up, s_gate_up, offsets, M, d, f, E, 1, h, status, stream,
+                        "moe_grouped_gemm_gateup_swiglu_fp8b");
+}
+
+int moe_grouped_gemm_down_fp8b(const void* h8, const float* sh, const void* w8_down, const float* s_down,
+                               const int32_t* offsets, int M, int d, int f, int E, int ksplit, float* y_perm,
+                               int32_t* status, moe_stream_t stream) {
+    return gemm8b_entry(1, h8, sh, w8_down, s_down, offsets, M, d, f, E, ksplit, y_perm, status, stream,
+                        "moe_grouped_gemm_down_fp8b");
+}
+
+int moe_forward_fp8b(const void* x, const float* logits, const void* w8_gate_up, const float* s_gate_up,
+                     const void* w8_down, const float* s_down, int T, int d, int f, int E, int top_k, void* out,
+                     void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    int rc = check_shape_fp8(T, d, f, E, top_k, "moe_forward_fp8b");
+    if (rc) return rc;
+    if (T == 0) return ok();
+    if (!x || !logits || !w8_gate_up || !s_gate_up || !w8_down || !s_down || !out)
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_fp8b: null pointer");
+    if (!aligned16(x) || !aligned16(w8_gate_up) || !aligned16(w8_down) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(s_gate_up) & 3u) || (reinterpret_cast<uintptr_t>(s_down) & 3u))
+        return fail(MOE_ERR_INVALID_ARG, "moe_forward_fp8b: tensors must be 16-byte (scales 4-byte) aligned");
+    const size_t need = layout_fp8(T, d, f, E, top_k, true).total;
+    if (!workspace || workspace_bytes < need)
+        return fail(MOE_ERR_WORKSPACE, "moe_forward_fp8b: workspace %zu bytes < %zu needed", workspace_bytes, need);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(MOE_ERR_WORKSPACE, "moe_forward_fp8b: workspace must be 256-byte aligned");
+    int sms;
+    if ((rc = check_device(&sms))) return rc;
+    return run_layer_fp8b(x, logits, w8_gate_up, s_gate_up, w8_down, s_down, T, d, f, E, top_k, out, workspace, sms,
+                          static_cast<cudaStream_t>(stream));
 }
 
 int moe_get_device_error(const void* status_or_workspace, int32_t* code) {

@@ -52,6 +52,15 @@ _SIGS = {
     "moe_gemm_pair_mode_fp8": ([_I, _I, _I, _I, _I, _I], _I),
     "moe_forward_fp8_launch_count": ([_I, _I, _I], _I),
     "moe_forward_fp8": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
+    "moe_quantize_weights_fp8b": ([_P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_quantize_rows_fp8b": ([_P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_grouped_gemm_gateup_swiglu_fp8b": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "moe_grouped_gemm_down_fp8b": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
+    "moe_workspace_size_fp8b": ([_I, _I, _I, _I, _I], _SZ),
+    "moe_workspace_layout_fp8b": ([_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _I),
+    "moe_down_ksplit_fp8b": ([_I, _I, _I, _I, _I], _I),
+    "moe_forward_fp8b_launch_count": ([_I, _I, _I], _I),
+    "moe_forward_fp8b": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
 }
 
 WS_FIELDS = ("status", "idx", "w", "counts", "offsets", "src", "dest", "x_perm", "h", "y_perm", "total")
@@ -533,6 +542,132 @@ def workspace_views_fp8(ws: torch.Tensor, T: int, d: int, f: int, E: int, top_k:
         "h": view("h", M * f, torch.bfloat16, (M, f)),
         "h8": view("h8", M * f, torch.uint8, (M, f)),
         "sh": view("sh", M, torch.float32, (M,)),
+        "y_perm": view("y_perm", S * M * d, torch.float32, (S, M, d)),
+        "ksplit": S,
+    }
+
+
+# ---------------------------------------------------------------------------------------------
+# Blockwise FP8: 1 x 128 activation blocks, 128 x 128 weight blocks, power-of-two scales.
+# ---------------------------------------------------------------------------------------------
+def quantize_weights_fp8b(W: torch.Tensor, stream=None, out: tuple | None = None):
+    """W [E, K, N] bf16 -> (Wq blocked codes [E, N/64, K/128, 64, 128], scale [E, N/128, K/128])."""
+    _dev(W, torch.bfloat16, "W")
+    E, K, N = W.shape
+    Wq, scale = out if out is not None else (
+        torch.empty(E, N // 64, K // 128, 64, 128, dtype=torch.uint8, device=W.device),
+        torch.empty(E, N // 128, K // 128, dtype=torch.float32, device=W.device))
+    _call("moe_quantize_weights_fp8b", _ptr(W), E, K, N, _ptr(Wq), _ptr(scale), _stream(stream))
+    return Wq, scale
+
+
+def quantize_rows_fp8b(a: torch.Tensor, src: torch.Tensor | None = None, status=None, stream=None,
+                       out: tuple | None = None):
+    """Rows of a [R0, C] bf16 in 128-wide blocks -> (codes [R, C] uint8, scale [R, C/128] fp32)."""
+    _dev(a, torch.bfloat16, "a")
+    if src is not None:
+        _dev(src, torch.int32, "src")
+    R0, C = a.shape
+    R = R0 if src is None else src.numel()
+    q, scale = out if out is not None else (torch.empty(R, C, dtype=torch.uint8, device=a.device),
+                                            torch.empty(R, C // 128, dtype=torch.float32, device=a.device))
+    _call("moe_quantize_rows_fp8b", _ptr(a), _ptr(src), R, C, R0, _ptr(q), _ptr(scale), _ptr(status),
+          _stream(stream))
+    return q, scale
+
+
+def grouped_gemm_gateup_swiglu_fp8b(x8_perm, sx, w8_gate_up, s_gate_up, offsets, h=None, status=None, stream=None):
+    """Blockwise step 3: sx [M, d/128], s_gate_up [E, 2f/128, d/128]."""
+    _dev(x8_perm, torch.uint8, "x8_perm")
+    _dev(sx, torch.float32, "sx")
+    _dev(s_gate_up, torch.float32, "s_gate_up")
+    _dev(offsets, torch.int32, "offsets")
+    M, d = x8_perm.shape
+    E, f2, _ = _w8_dims(w8_gate_up, "w8_gate_up")
+    h = h if h is not None else torch.empty(M, f2 // 2, dtype=torch.bfloat16, device=x8_perm.device)
+    _call("moe_grouped_gemm_gateup_swiglu_fp8b", _ptr(x8_perm), _ptr(sx), _ptr(w8_gate_up), _ptr(s_gate_up),
+          _ptr(offsets), M, d, f2 // 2, E, _ptr(h), _ptr(status), _stream(stream))
+    return h
+
+
+def grouped_gemm_down_fp8b(h8, sh, w8_down, s_down, offsets, y_perm=None, status=None, stream=None, ksplit: int = 1):
+    """Blockwise step 4: sh [M, f/128], s_down [E, d/128, f/128]."""
+    _dev(h8, torch.uint8, "h8")
+    _dev(sh, torch.float32, "sh")
+    _dev(s_down, torch.float32, "s_down")
+    _dev(offsets, torch.int32, "offsets")
+    M, f = h8.shape
+    E, d, _ = _w8_dims(w8_down, "w8_down")
+    if y_perm is None:
+        y_perm = torch.empty(ksplit, M, d, dtype=torch.float32, device=h8.device)
+        if ksplit == 1:
+            y_perm = y_perm[0]
+    if y_perm.numel() < ksplit * M * d:
+        raise ValueError("y_perm must hold ksplit * M * d floats")
+    _call("moe_grouped_gemm_down_fp8b", _ptr(h8), _ptr(sh), _ptr(w8_down), _ptr(s_down), _ptr(offsets), M, d, f, E,
+          ksplit, _ptr(y_perm), _ptr(status), _stream(stream))
+    return y_perm
+
+
+def workspace_size_fp8b(T: int, d: int, f: int, E: int, top_k: int) -> int:
+    return int(load().moe_workspace_size_fp8b(T, d, f, E, top_k))
+
+
+def workspace_layout_fp8b(T: int, d: int, f: int, E: int, top_k: int) -> dict:
+    out = (_SZ * 14)()
+    _call("moe_workspace_layout_fp8b", T, d, f, E, top_k, out)
+    return dict(zip(WS8_FIELDS, [int(v) for v in out]))
+
+
+def down_ksplit_fp8b(T: int, d: int, f: int, E: int, top_k: int) -> int:
+    return int(load().moe_down_ksplit_fp8b(T, d, f, E, top_k))
+
+
+def forward_fp8b_launch_count(T: int, E: int, top_k: int) -> int:
+    """Kernel launches of one moe_forward_fp8b call (6 with route+permute fused, else 7)."""
+    return int(load().moe_forward_fp8b_launch_count(T, E, top_k))
+
+
+def forward_fp8b(x, logits, w8_gate_up, s_gate_up, w8_down, s_down, top_k, out=None, workspace=None, stream=None):
+    """The blockwise FP8 layer in one call (weights from quantize_weights_fp8b).  Returns ``out``."""
+    _dev(x, torch.bfloat16, "x")
+    _dev(logits, torch.float32, "logits")
+    _dev(s_gate_up, torch.float32, "s_gate_up")
+    _dev(s_down, torch.float32, "s_down")
+    T, d = x.shape
+    E, f2, _ = _w8_dims(w8_gate_up, "w8_gate_up")
+    _w8_dims(w8_down, "w8_down")
+    if workspace is None:
+        workspace = torch.empty(workspace_size_fp8b(T, d, f2 // 2, E, top_k), dtype=torch.uint8, device=x.device)
+    out = out if out is not None else torch.empty(T, d, dtype=torch.bfloat16, device=x.device)
+    _call("moe_forward_fp8b", _ptr(x), _ptr(logits), _ptr(w8_gate_up), _ptr(s_gate_up), _ptr(w8_down), _ptr(s_down),
+          T, d, f2 // 2, E, top_k, _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    return out
+
+
+def workspace_views_fp8b(ws: torch.Tensor, T: int, d: int, f: int, E: int, top_k: int) -> dict:
+    """Typed views of moe_forward_fp8b's intermediates inside ``ws``."""
+    L = workspace_layout_fp8b(T, d, f, E, top_k)
+    M = T * top_k
+    S = down_ksplit_fp8b(T, d, f, E, top_k)
+
+    def view(name, n, dtype, shape):
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return ws[L[name]:L[name] + nbytes].view(dtype).view(*shape)
+
+    return {
+        "status": view("status", 1, torch.int32, (1,)),
+        "idx": view("idx", M, torch.int32, (T, top_k)),
+        "w": view("w", M, torch.float32, (T, top_k)),
+        "counts": view("counts", E, torch.int32, (E,)),
+        "offsets": view("offsets", E + 1, torch.int32, (E + 1,)),
+        "src": view("src", M, torch.int32, (M,)),
+        "dest": view("dest", M, torch.int32, (T, top_k)),
+        "x8": view("x8", M * d, torch.uint8, (M, d)),
+        "sx": view("sx", M * (d // 128), torch.float32, (M, d // 128)),
+        "h": view("h", M * f, torch.bfloat16, (M, f)),
+        "h8": view("h8", M * f, torch.uint8, (M, f)),
+        "sh": view("sh", M * (f // 128), torch.float32, (M, f // 128)),
         "y_perm": view("y_perm", S * M * d, torch.float32, (S, M, d)),
         "ksplit": S,
     }

@@ -168,3 +168,9 @@ def draw_scales(shape, seed: int, lo: float = 1e-3, hi: float = 1e-2) -> np.ndar
     """Positive fp32 dequantisation scales, log-uniform in [lo, hi]."""
     rng = np.random.default_rng(seed)
     return np.exp(rng.uniform(np.log(lo), np.log(hi), size=shape)).astype(np.float32)
+
+
+def draw_pow2_scales(shape, seed: int, lo: int = -12, hi: int = -4) -> np.ndarray:
+    """fp32 powers of two 2^e, e uniform in [lo, hi]: raw block scales for the blockwise FP8 stages."""
+    rng = np.random.default_rng(seed)
+    return np.ldexp(1.0, rng.integers(lo, hi + 1, size=shape)).astype(np.float32)

@@ -278,3 +278,21 @@ def test_gemm_pair_mode_fp8_policy(lib):
     assert f(2048, 7168, 2048, 256, 8, 0) == 2 and f(2048, 7168, 2048, 256, 8, 1) == 0  # DeepSeek-V3 shape
     assert f(256, 7168, 2048, 32, 8, 0) == 0 and f(256, 7168, 2048, 32, 8, 1) == 0     # 32 experts
     assert f(32, 4096, 14336, 8, 2, 2) == -1 and f(32, 4000, 14336, 8, 2, 0) == -1
+
+
+def test_fp8b_entry_points_validate(lib):
+    from mixture_experts_grouped_fp32_gb300 import moe
+    T, d, f, E, k = 300, 512, 768, 8, 2
+    L = moe.workspace_layout_fp8b(T, d, f, E, k)
+    M = T * k
+    assert L["sh"] - L["h8"] >= M * f and L["y_perm"] - L["sh"] >= M * (f // 128) * 4
+    assert L["h"] - L["sx"] >= M * (d // 128) * 4
+    assert moe.workspace_size_fp8b(T, d, f, E, k) == L["total"]
+    assert moe.down_ksplit_fp8b(T, d, f, E, k) >= 1
+    assert lib.moe_forward_fp8b_launch_count(32, 8, 2) == 6
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.moe_quantize_weights_fp8b(p, 8, 256, 192, p, p, None) == -1      # N % 128
+    assert lib.moe_quantize_rows_fp8b(p, None, 4, 64, 4, p, p, None, None) == -1  # C % 128
+    assert lib.moe_forward_fp8b(p, p, p, p, p, p, 4, 192, 256, 8, 2, p, p, 1 << 40, None) == -1
+    assert lib.moe_forward_fp8b(p, p, p, p, p, p, 4, 256, 256, 8, 2, p, p, 16, None) == -3
+    assert lib.moe_grouped_gemm_down_fp8b(p, p, p, p, p, 0, 256, 256, 8, 1, p, None, None) == 0
