@@ -72,6 +72,7 @@ AUTO_TIMED_S = 0.5
 AUTO_STEPS_MIN, AUTO_STEPS_MAX = 50, 4000
 
 _TRAFFIC_HASH = "4b383edeb4f77185"  # GEMM source hash the captures below were taken at
+_TRAFFIC_HASH_FP8B = "637ecc65f4d2dad2"  # ... and that of the blockwise FP8 kernel's sources
 MEASURED_TRAFFIC = {
     ("mixtral_t32", "gateup_swiglu"): (1884874752, _TRAFFIC_HASH),
     ("mixtral_t32", "down"): (944451840, _TRAFFIC_HASH),
@@ -99,16 +100,29 @@ MEASURED_TRAFFIC = {
     ("deepseek_e32_t256", "down_fp8"): (534342144, _TRAFFIC_HASH),
     ("deepseek_t2048", "gateup_swiglu_fp8"): (3891759104, _TRAFFIC_HASH),
     ("deepseek_t2048", "down_fp8"): (2295916544, _TRAFFIC_HASH),
+    ("mixtral_t32", "gateup_swiglu_fp8b"): (945041664, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t32", "down_fp8b"): (474054656, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512", "gateup_swiglu_fp8b"): (1294983680, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512", "down_fp8b"): (616183040, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t4096", "gateup_swiglu_fp8b"): (1199375616, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t4096", "down_fp8b"): (728358656, _TRAFFIC_HASH_FP8B),
+    ("deepseek_t2048", "gateup_swiglu_fp8b"): (3747385088, _TRAFFIC_HASH_FP8B),
+    ("deepseek_t2048", "down_fp8b"): (2315257600, _TRAFFIC_HASH_FP8B),
 }
 GEMM_SOURCES = ("mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm.cu",
                 "mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm_2sm.cu",
                 "mixture_experts_grouped_fp32_gb300/csrc/tcgen05.cuh")
 
 
-def gemm_source_hash() -> str:
+# The blockwise FP8 GEMMs' own kernel (their traffic entries carry this source set's hash).
+FP8B_SOURCES = ("mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm_fp8b.cu",
+                "mixture_experts_grouped_fp32_gb300/csrc/tcgen05.cuh")
+
+
+def gemm_source_hash(sources=GEMM_SOURCES) -> str:
     import hashlib
     h = hashlib.sha256()
-    for p in GEMM_SOURCES:
+    for p in sources:
         with open(os.path.join(ROOT, p), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -116,7 +130,8 @@ def gemm_source_hash() -> str:
 
 def measured_traffic(workload: str, stage: str):
     rec = MEASURED_TRAFFIC.get((workload, stage))
-    return rec[0] if rec and rec[1] == gemm_source_hash() else None
+    sources = FP8B_SOURCES if stage.endswith("_fp8b") else GEMM_SOURCES
+    return rec[0] if rec and rec[1] == gemm_source_hash(sources) else None
 
 
 def load_peaks():

@@ -101,8 +101,8 @@ struct GemmArgs {
     bool fp8 = false;
     const float* a_scale = nullptr;
     const float* b_scale = nullptr;
-    // Blockwise FP8 (with fp8): a_scale [M, K/128] (one per 128-wide row block), b_scale
-    // [E, N_total/128, K/128] (one per 128 x 128 block); its own kernel, N % 128 == 0.
+    // Blockwise FP8 (with fp8; launched by launch_grouped_gemm_fp8b): a_scale [M, K/128] (one per
+    // 128-wide row block), b_scale [E, N_total/128, K/128] (one per 128 x 128 block), N % 128 == 0.
     bool fp8_blocks = false;
 };
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,

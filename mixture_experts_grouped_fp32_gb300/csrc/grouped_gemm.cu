@@ -711,7 +711,6 @@ cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaSt
         *why = "FP8 grouped GEMM: K must be a multiple of 128, scales given, no row gather";
         return cudaErrorInvalidValue;
     }
-    if (a.fp8_blocks) return launch_grouped_gemm_fp8b(kind, a, num_sms, s, why);
     if (a.pair && num_sms >= 2 && !a.inject_stall) return launch_grouped_gemm_pair(kind, a, num_sms, s, why);
     if (a.fp8)
         return kind == 0 ? launch_kind<0, false, true>(a, num_sms, s, why) : launch_kind<1, false, true>(a, num_sms, s, why);

@@ -344,18 +344,20 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 A0[j] = 0.0f;
                 A1[j] = 0.0f;
             }
-            float sw0 = 0.0f, sw1 = 0.0f, sr = 0.0f;
-            if (kb0 < kb1) {
-                sw0 = __ldg(sw0p + kb0);
-                sw1 = __ldg(sw1p + kb0);
-                sr = sc_ok ? __ldg(srp + kb0) : 0.0f;
-            }
+            // Scales of K blocks kb (s*), kb + 1 (n*) and kb + 2 (m*): each is loaded two blocks
+            // ahead of its use, so the load's latency hides behind two partial products.
+            auto ld_sc = [&](int b, float& w0, float& w1, float& r) {
+                const bool in = b < kb1;
+                w0 = in ? __ldg(sw0p + b) : 0.0f;
+                w1 = in ? __ldg(sw1p + b) : 0.0f;
+                r = (in && sc_ok) ? __ldg(srp + b) : 0.0f;
+            };
+            float sw0, sw1, sr, nsw0, nsw1, nsr;
+            ld_sc(kb0, sw0, sw1, sr);
+            ld_sc(kb0 + 1, nsw0, nsw1, nsr);
             for (int kb = kb0; kb < kb1; ++kb) {
-                // The next K block's scales, loaded before this block's partial is waited for.
-                const bool more = kb + 1 < kb1;
-                const float nsw0 = more ? __ldg(sw0p + kb + 1) : 0.0f;
-                const float nsw1 = more ? __ldg(sw1p + kb + 1) : 0.0f;
-                const float nsr = (more && sc_ok) ? __ldg(srp + kb + 1) : 0.0f;
+                float msw0, msw1, msr;
+                ld_sc(kb + 2, msw0, msw1, msr);
                 if (!ptx::mbar_wait(&c.pfull[pb], pph, abort_flag)) {
                     raise_abort(c, status);
                     aborted = true;
@@ -394,6 +396,9 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 sw0 = nsw0;
                 sw1 = nsw1;
                 sr = nsr;
+                nsw0 = msw0;
+                nsw1 = msw1;
+                nsr = msr;
             }
             if (aborted) break;
             // ------------------------------ epilogue from registers ------------------------------

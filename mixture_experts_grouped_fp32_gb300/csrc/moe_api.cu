@@ -455,7 +455,7 @@ int run_layer_fp8b(const void* x, const float* logits, const void* wgu8, const f
     g1.fp8 = g1.fp8_blocks = true;
     g1.a_scale = sx;
     g1.b_scale = sgu;
-    if ((e = launch_grouped_gemm(0, g1, num_sms, s, &why)) != cudaSuccess)
+    if ((e = launch_grouped_gemm_fp8b(0, g1, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "blockwise FP8 gate+up GEMM: %s (%s)", why, cudaGetErrorString(e));
     if ((e = launch_quantize_rows_fp8b(h, nullptr, M, f, M, h8, sh, status, s)) != cudaSuccess)
         return launched(e, "quantize h");
@@ -463,7 +463,7 @@ int run_layer_fp8b(const void* x, const float* logits, const void* wgu8, const f
     g2.fp8 = g2.fp8_blocks = true;
     g2.a_scale = sh;
     g2.b_scale = sd;
-    if ((e = launch_grouped_gemm(1, g2, num_sms, s, &why)) != cudaSuccess)
+    if ((e = launch_grouped_gemm_fp8b(1, g2, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "blockwise FP8 down GEMM: %s (%s)", why, cudaGetErrorString(e));
     if ((e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) !=
         cudaSuccess)
@@ -1020,7 +1020,7 @@ static int gemm8b_entry(int kind, const void* A, const float* sa, const void* B,
     g.a_scale = sa;
     g.b_scale = sb;
     const char* why = "";
-    cudaError_t e = launch_grouped_gemm(kind, g, sms, static_cast<cudaStream_t>(stream), &why);
+    cudaError_t e = launch_grouped_gemm_fp8b(kind, g, sms, static_cast<cudaStream_t>(stream), &why);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s (%s)", name, why, cudaGetErrorString(e));
     return ok();
 }
