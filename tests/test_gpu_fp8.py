@@ -331,3 +331,71 @@ def test_forward_fp8_full_size(moe, oracle, monkeypatch, name, path):
                                            sample.astype(np.int32))
     got = out[torch.from_numpy(sample).to(dev)].float().cpu().numpy()
     assert_layer_close(got, ref, f"{name} fp8 sampled tokens {sample.tolist()}")
+
+
+@pytest.mark.parametrize("variant", ["fp8", "fp8b"])
+def test_forward_fp8_graph_capture(moe, variant):
+    """Capture one FP8 layer in a CUDA graph: the kernel nodes equal the stated launch count and
+    replaying reproduces the eager result bit for bit."""
+    from test_gpu_parity import _graph_node_types
+    w = WORKLOADS["tiny"]
+    logits, x, wgu, wd = case_inputs(w)
+    dev = torch.device(DEV)
+    quant = moe.quantize_weights_fp8b if variant == "fp8b" else moe.quantize_weights_fp8
+    fwd = moe.forward_fp8b if variant == "fp8b" else moe.forward_fp8
+    wsize = moe.workspace_size_fp8b if variant == "fp8b" else moe.workspace_size_fp8
+    count = moe.forward_fp8b_launch_count if variant == "fp8b" else moe.forward_fp8_launch_count
+    w8 = quant(wgu.to(dev)) + quant(wd.to(dev))
+    args = (x.to(dev), logits.to(dev), *w8, w.k)
+    ws = torch.empty(wsize(w.T, w.d, w.f, w.E, w.k), dtype=torch.uint8, device=dev)
+    eager = fwd(*args, workspace=ws).clone()
+    out = torch.zeros_like(eager)
+    torch.cuda.synchronize()
+    try:
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+    except TypeError:
+        g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fwd(*args, out=out, workspace=ws)
+    raw = None
+    try:
+        raw = g.raw_cuda_graph()
+    except (AttributeError, RuntimeError):
+        pass
+    kinds = _graph_node_types(raw) if raw else None
+    if raw is not None and hasattr(g, "instantiate"):
+        g.instantiate()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    if kinds is None:
+        pytest.skip("no libcudart / raw_cuda_graph to count graph nodes")
+    assert kinds.count(0) == count(w.T, w.E, w.k), kinds
+
+
+def test_fp8_status_flags(moe):
+    """Bad offsets reach the FP8 and blockwise FP8 GEMMs' status bit; a bad expert id reaches the
+    FP8 permute's; nothing is read out of bounds."""
+    E, d, f = 4, 128, 128
+    M = 16
+    x8 = torch.zeros(M, d, dtype=torch.uint8, device=DEV)
+    sx = torch.ones(M, dtype=torch.float32, device=DEV)
+    sxb = torch.ones(M, d // 128, dtype=torch.float32, device=DEV)
+    w8 = torch.zeros(E, 2 * f // 64, d // 128, 64, 128, dtype=torch.uint8, device=DEV)
+    sw = torch.ones(E, 2 * f, dtype=torch.float32, device=DEV)
+    swb = torch.ones(E, 2 * f // 128, d // 128, dtype=torch.float32, device=DEV)
+    h = torch.zeros(M, f, dtype=torch.bfloat16, device=DEV)
+    for bad in ([0, 5, 3, 8, 16], [0, 4, 8, 12, 17]):
+        offs = torch.tensor(bad, dtype=torch.int32, device=DEV)
+        for call in (lambda st: moe.grouped_gemm_gateup_swiglu_fp8(x8, sx, w8, sw, offs, h=h, status=st),
+                     lambda st: moe.grouped_gemm_gateup_swiglu_fp8b(x8, sxb, w8, swb, offs, h=h, status=st)):
+            status = torch.zeros(1, dtype=torch.int32, device=DEV)
+            call(status)
+            torch.cuda.synchronize()
+            assert int(status.item()) & moe.STATUS_BAD_OFFSETS
+    idx = torch.tensor([[0, 1], [2, 9], [3, 3]], dtype=torch.int32, device=DEV)
+    x = torch.zeros(3, 128, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    moe.permute_fp8(idx, x, 4, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & moe.STATUS_BAD_EXPERT_ID
