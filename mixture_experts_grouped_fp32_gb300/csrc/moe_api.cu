@@ -357,12 +357,15 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
     return ok();
 }
 
-// The FP8 layer: route (+ permute, writing the x rows quantised), gate+up FP8 GEMM (+ SwiGLU,
-// bf16 h), h quantised per row, down FP8 GEMM, combine.
+// The FP8 layers.  Per-row / per-channel scales (blocks = false): route (+ permute writing the x
+// rows quantised), gate+up FP8 GEMM (+ SwiGLU, bf16 h), h quantised per row, down FP8 GEMM,
+// combine.  Blockwise scales (blocks = true): the permutation computes indices only and x rows are
+// gathered by src and quantised in 128-wide blocks by their own launch; the GEMMs are the
+// blockwise kernel's.
 int run_layer_fp8(const void* x, const float* logits, const void* wgu8, const float* sgu, const void* wd8,
                   const float* sd, int T, int d, int f, int E, int k, void* out, void* ws, int num_sms,
-                  cudaStream_t s) {
-    const Layout8 L = layout_fp8(T, d, f, E, k);
+                  cudaStream_t s, bool blocks) {
+    const Layout8 L = layout_fp8(T, d, f, E, k, blocks);
     int32_t* status = at<int32_t>(ws, L.status);
     int32_t* idx = at<int32_t>(ws, L.idx);
     float* w = at<float>(ws, L.w);
@@ -378,93 +381,46 @@ int run_layer_fp8(const void* x, const float* logits, const void* wgu8, const fl
     float* y = at<float>(ws, L.y_perm);
     const int M = T * k;
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    uint8_t* perm_x8 = blocks ? nullptr : x8;  // per-row scales: the permutation quantises x itself
+    float* perm_sx = blocks ? nullptr : sx;
     cudaError_t e;
-    // The permutation writes the quantised x rows (x8, sx) directly.
     if (fuse_route_permute(T, E)) {
         if ((e = launch_route_permute(logits, xb, T, d, E, k, idx, w, counts, offsets, src, dest, nullptr, status,
-                                      num_sms, s, x8, sx)) != cudaSuccess)
+                                      num_sms, s, perm_x8, perm_sx)) != cudaSuccess)
             return launched(e, "route+permute");
     } else {
         if ((e = launch_route(logits, T, E, k, idx, w, status, s)) != cudaSuccess) return launched(e, "route");
-        if ((e = launch_permute(idx, xb, T, d, E, k, counts, offsets, src, dest, nullptr, status, num_sms, s, x8,
-                                sx)) != cudaSuccess)
+        if ((e = launch_permute(idx, xb, T, d, E, k, counts, offsets, src, dest, nullptr, status, num_sms, s, perm_x8,
+                                perm_sx)) != cudaSuccess)
             return launched(e, "permute");
     }
-    const char* why = "";
-    const int ksplit = down_ksplit(T, d, f, E, k, true);
-    GemmArgs g1{x8, wgu8, offsets, M, d, f, E, h, status, 1, swap_max_rows(), use_pair(M, E, f, 0, true),
+    if (blocks && (e = launch_quantize_rows_fp8b(xb, src, M, d, T, x8, sx, status, s)) != cudaSuccess)
+        return launched(e, "quantize x");
+    auto gemm = [&](int kind, GemmArgs& g, const char* what) -> int {
+        const char* why = "";
+        const cudaError_t ge = blocks ? launch_grouped_gemm_fp8b(kind, g, num_sms, s, &why)
+                                      : launch_grouped_gemm(kind, g, num_sms, s, &why);
+        return ge == cudaSuccess ? MOE_OK : fail(MOE_ERR_CUDA, "%s: %s (%s)", what, why, cudaGetErrorString(ge));
+    };
+    const int ksplit = down_ksplit(T, d, f, E, k, true, blocks);
+    GemmArgs g1{x8, wgu8, offsets, M, d, f, E, h, status, 1, swap_max_rows(), blocks ? 0 : use_pair(M, E, f, 0, true),
                 pair_swap_max_rows(), pair_layout(), pair_split()};
     g1.fp8 = true;
+    g1.fp8_blocks = blocks;
     g1.a_scale = sx;
     g1.b_scale = sgu;
-    if ((e = launch_grouped_gemm(0, g1, num_sms, s, &why)) != cudaSuccess)
-        return fail(MOE_ERR_CUDA, "FP8 gate+up GEMM: %s (%s)", why, cudaGetErrorString(e));
-    if ((e = launch_quantize_rows_fp8(h, nullptr, M, f, M, h8, sh, status, s)) != cudaSuccess)
-        return launched(e, "quantize h");
-    GemmArgs g2{h8, wd8, offsets, M, f, d, E, y, status, ksplit, swap_max_rows(), use_pair(M, E, d, 1, true),
-                pair_swap_max_rows(), pair_layout(), pair_split()};
+    int rc = gemm(0, g1, blocks ? "blockwise FP8 gate+up GEMM" : "FP8 gate+up GEMM");
+    if (rc) return rc;
+    e = blocks ? launch_quantize_rows_fp8b(h, nullptr, M, f, M, h8, sh, status, s)
+               : launch_quantize_rows_fp8(h, nullptr, M, f, M, h8, sh, status, s);
+    if (e != cudaSuccess) return launched(e, "quantize h");
+    GemmArgs g2{h8, wd8, offsets, M, f, d, E, y, status, ksplit, swap_max_rows(),
+                blocks ? 0 : use_pair(M, E, d, 1, true), pair_swap_max_rows(), pair_layout(), pair_split()};
     g2.fp8 = true;
+    g2.fp8_blocks = blocks;
     g2.a_scale = sh;
     g2.b_scale = sd;
-    if ((e = launch_grouped_gemm(1, g2, num_sms, s, &why)) != cudaSuccess)
-        return fail(MOE_ERR_CUDA, "FP8 down GEMM: %s (%s)", why, cudaGetErrorString(e));
-    if ((e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) !=
-        cudaSuccess)
-        return launched(e, "combine");
-    return ok();
-}
-
-// The blockwise FP8 layer: route (+ permute, indices only), x rows gathered by src and quantised
-// in 128-wide blocks, blockwise gate+up GEMM (+ SwiGLU, bf16 h), h quantised in blocks, blockwise
-// down GEMM, combine.
-int run_layer_fp8b(const void* x, const float* logits, const void* wgu8, const float* sgu, const void* wd8,
-                   const float* sd, int T, int d, int f, int E, int k, void* out, void* ws, int num_sms,
-                   cudaStream_t s) {
-    const Layout8 L = layout_fp8(T, d, f, E, k, true);
-    int32_t* status = at<int32_t>(ws, L.status);
-    int32_t* idx = at<int32_t>(ws, L.idx);
-    float* w = at<float>(ws, L.w);
-    int32_t* counts = at<int32_t>(ws, L.counts);
-    int32_t* offsets = at<int32_t>(ws, L.offsets);
-    int32_t* src = at<int32_t>(ws, L.src);
-    int32_t* dest = at<int32_t>(ws, L.dest);
-    uint8_t* x8 = at<uint8_t>(ws, L.x8);
-    float* sx = at<float>(ws, L.sx);
-    auto* h = at<__nv_bfloat16>(ws, L.h);
-    uint8_t* h8 = at<uint8_t>(ws, L.h8);
-    float* sh = at<float>(ws, L.sh);
-    float* y = at<float>(ws, L.y_perm);
-    const int M = T * k;
-    const auto* xb = static_cast<const __nv_bfloat16*>(x);
-    cudaError_t e;
-    if (fuse_route_permute(T, E)) {
-        if ((e = launch_route_permute(logits, xb, T, d, E, k, idx, w, counts, offsets, src, dest, nullptr, status,
-                                      num_sms, s)) != cudaSuccess)
-            return launched(e, "route+permute");
-    } else {
-        if ((e = launch_route(logits, T, E, k, idx, w, status, s)) != cudaSuccess) return launched(e, "route");
-        if ((e = launch_permute(idx, xb, T, d, E, k, counts, offsets, src, dest, nullptr, status, num_sms, s)) !=
-            cudaSuccess)
-            return launched(e, "permute");
-    }
-    if ((e = launch_quantize_rows_fp8b(xb, src, M, d, T, x8, sx, status, s)) != cudaSuccess)
-        return launched(e, "quantize x");
-    const char* why = "";
-    const int ksplit = down_ksplit(T, d, f, E, k, true, true);
-    GemmArgs g1{x8, wgu8, offsets, M, d, f, E, h, status, 1, swap_max_rows(), 0};
-    g1.fp8 = g1.fp8_blocks = true;
-    g1.a_scale = sx;
-    g1.b_scale = sgu;
-    if ((e = launch_grouped_gemm_fp8b(0, g1, num_sms, s, &why)) != cudaSuccess)
-        return fail(MOE_ERR_CUDA, "blockwise FP8 gate+up GEMM: %s (%s)", why, cudaGetErrorString(e));
-    if ((e = launch_quantize_rows_fp8b(h, nullptr, M, f, M, h8, sh, status, s)) != cudaSuccess)
-        return launched(e, "quantize h");
-    GemmArgs g2{h8, wd8, offsets, M, f, d, E, y, status, ksplit, swap_max_rows(), 0};
-    g2.fp8 = g2.fp8_blocks = true;
-    g2.a_scale = sh;
-    g2.b_scale = sd;
-    if ((e = launch_grouped_gemm_fp8b(1, g2, num_sms, s, &why)) != cudaSuccess)
-        return fail(MOE_ERR_CUDA, "blockwise FP8 down GEMM: %s (%s)", why, cudaGetErrorString(e));
+    if ((rc = gemm(1, g2, blocks ? "blockwise FP8 down GEMM" : "FP8 down GEMM"))) return rc;
     if ((e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) !=
         cudaSuccess)
         return launched(e, "combine");
@@ -867,9 +823,10 @@ int moe_quantize_rows_fp8(const void* a, const int32_t* src, int R, int C, int s
                     "quantize rows");
 }
 
+// The FP8 GEMM stage calls; blocks = true for the blockwise kernel.
 static int gemm8_entry(int kind, const void* A, const float* sa, const void* B, const float* sb,
                        const int32_t* offsets, int M, int d, int f, int E, int ksplit, void* out, int32_t* status,
-                       moe_stream_t stream, const char* name) {
+                       moe_stream_t stream, const char* name, bool blocks = false) {
     int rc = check_shape_fp8(0, d, f, E, 1, name);
     if (rc) return rc;
     if (M < 0) return fail(MOE_ERR_INVALID_ARG, "%s: M = %d must be >= 0", name, M);
@@ -883,17 +840,19 @@ static int gemm8_entry(int kind, const void* A, const float* sa, const void* B, 
         return fail(MOE_ERR_INVALID_ARG, "%s: scales must be 4-byte aligned", name);
     int sms;
     if ((rc = check_device(&sms))) return rc;
-    const int pair = use_pair(M, E, kind == 0 ? f : d, kind, true);
+    const int pair = blocks ? 0 : use_pair(M, E, kind == 0 ? f : d, kind, true);
     GemmArgs g = kind == 0 ? GemmArgs{A, B, offsets, M, d, f, E, out, status, 1, swap_max_rows(), pair}
                            : GemmArgs{A, B, offsets, M, f, d, E, out, status, ksplit, swap_max_rows(), pair};
     g.pair_swap_max = pair_swap_max_rows();
     g.pair_layout = pair_layout();
     g.pair_split = pair_split();
     g.fp8 = true;
+    g.fp8_blocks = blocks;
     g.a_scale = sa;
     g.b_scale = sb;
     const char* why = "";
-    cudaError_t e = launch_grouped_gemm(kind, g, sms, static_cast<cudaStream_t>(stream), &why);
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = blocks ? launch_grouped_gemm_fp8b(kind, g, sms, cs, &why) : launch_grouped_gemm(kind, g, sms, cs, &why);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s (%s)", name, why, cudaGetErrorString(e));
     return ok();
 }
@@ -912,26 +871,35 @@ int moe_grouped_gemm_down_fp8(const void* h8, const float* sh, const void* w8_do
                        "moe_grouped_gemm_down_fp8");
 }
 
-int moe_forward_fp8(const void* x, const float* logits, const void* w8_gate_up, const float* s_gate_up,
-                    const void* w8_down, const float* s_down, int T, int d, int f, int E, int top_k, void* out,
-                    void* workspace, size_t workspace_bytes, moe_stream_t stream) {
-    int rc = check_shape_fp8(T, d, f, E, top_k, "moe_forward_fp8");
+// moe_forward_fp8 and moe_forward_fp8b: argument checks, then the layer.
+static int forward8_entry(const void* x, const float* logits, const void* w8_gate_up, const float* s_gate_up,
+                          const void* w8_down, const float* s_down, int T, int d, int f, int E, int top_k, void* out,
+                          void* workspace, size_t workspace_bytes, moe_stream_t stream, bool blocks) {
+    const char* name = blocks ? "moe_forward_fp8b" : "moe_forward_fp8";
+    int rc = check_shape_fp8(T, d, f, E, top_k, name);
     if (rc) return rc;
     if (T == 0) return ok();
     if (!x || !logits || !w8_gate_up || !s_gate_up || !w8_down || !s_down || !out)
-        return fail(MOE_ERR_INVALID_ARG, "moe_forward_fp8: null pointer");
+        return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
     if (!aligned16(x) || !aligned16(w8_gate_up) || !aligned16(w8_down) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(s_gate_up) & 3u) || (reinterpret_cast<uintptr_t>(s_down) & 3u))
-        return fail(MOE_ERR_INVALID_ARG, "moe_forward_fp8: tensors must be 16-byte (scales 4-byte) aligned");
-    const size_t need = layout_fp8(T, d, f, E, top_k).total;
+        return fail(MOE_ERR_INVALID_ARG, "%s: tensors must be 16-byte (scales 4-byte) aligned", name);
+    const size_t need = layout_fp8(T, d, f, E, top_k, blocks).total;
     if (!workspace || workspace_bytes < need)
-        return fail(MOE_ERR_WORKSPACE, "moe_forward_fp8: workspace %zu bytes < %zu needed", workspace_bytes, need);
+        return fail(MOE_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", name, workspace_bytes, need);
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
-        return fail(MOE_ERR_WORKSPACE, "moe_forward_fp8: workspace must be 256-byte aligned");
+        return fail(MOE_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", name);
     int sms;
     if ((rc = check_device(&sms))) return rc;
     return run_layer_fp8(x, logits, w8_gate_up, s_gate_up, w8_down, s_down, T, d, f, E, top_k, out, workspace, sms,
-                         static_cast<cudaStream_t>(stream));
+                         static_cast<cudaStream_t>(stream), blocks);
+}
+
+int moe_forward_fp8(const void* x, const float* logits, const void* w8_gate_up, const float* s_gate_up,
+                    const void* w8_down, const float* s_down, int T, int d, int f, int E, int top_k, void* out,
+                    void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    return forward8_entry(x, logits, w8_gate_up, s_gate_up, w8_down, s_down, T, d, f, E, top_k, out, workspace,
+                          workspace_bytes, stream, false);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -999,66 +967,25 @@ int moe_quantize_rows_fp8b(const void* a, const int32_t* src, int R, int C, int 
                     "quantize rows (blockwise)");
 }
 
-static int gemm8b_entry(int kind, const void* A, const float* sa, const void* B, const float* sb,
-                        const int32_t* offsets, int M, int d, int f, int E, int ksplit, void* out, int32_t* status,
-                        moe_stream_t stream, const char* name) {
-    int rc = check_shape_fp8(0, d, f, E, 1, name);
-    if (rc) return rc;
-    if (M < 0) return fail(MOE_ERR_INVALID_ARG, "%s: M = %d must be >= 0", name, M);
-    if (ksplit < 1 || ksplit > kMaxKSplit)
-        return fail(MOE_ERR_INVALID_ARG, "%s: ksplit = %d outside [1, %d]", name, ksplit, kMaxKSplit);
-    if (M == 0) return ok();
-    if (!A || !sa || !B || !sb || !offsets || !out) return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
-    if (!aligned16(A) || !aligned16(B) || !aligned16(out) || (reinterpret_cast<uintptr_t>(sa) & 3u) ||
-        (reinterpret_cast<uintptr_t>(sb) & 3u))
-        return fail(MOE_ERR_INVALID_ARG, "%s: operands must be 16-byte (scales 4-byte) aligned", name);
-    int sms;
-    if ((rc = check_device(&sms))) return rc;
-    GemmArgs g = kind == 0 ? GemmArgs{A, B, offsets, M, d, f, E, out, status, 1, swap_max_rows(), 0}
-                           : GemmArgs{A, B, offsets, M, f, d, E, out, status, ksplit, swap_max_rows(), 0};
-    g.fp8 = g.fp8_blocks = true;
-    g.a_scale = sa;
-    g.b_scale = sb;
-    const char* why = "";
-    cudaError_t e = launch_grouped_gemm_fp8b(kind, g, sms, static_cast<cudaStream_t>(stream), &why);
-    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s (%s)", name, why, cudaGetErrorString(e));
-    return ok();
-}
-
 int moe_grouped_gemm_gateup_swiglu_fp8b(const void* x8_perm, const float* sx, const void* w8_gate_up,
                                         const float* s_gate_up, const int32_t* offsets, int M, int d, int f, int E,
                                         void* h, int32_t* status, moe_stream_t stream) {
-    return gemm8b_entry(0, x8_perm, sx, w8_gate_up, s_gate_up, offsets, M, d, f, E, 1, h, status, stream,
-                        "moe_grouped_gemm_gateup_swiglu_fp8b");
+    return gemm8_entry(0, x8_perm, sx, w8_gate_up, s_gate_up, offsets, M, d, f, E, 1, h, status, stream,
+                       "moe_grouped_gemm_gateup_swiglu_fp8b", true);
 }
 
 int moe_grouped_gemm_down_fp8b(const void* h8, const float* sh, const void* w8_down, const float* s_down,
                                const int32_t* offsets, int M, int d, int f, int E, int ksplit, float* y_perm,
                                int32_t* status, moe_stream_t stream) {
-    return gemm8b_entry(1, h8, sh, w8_down, s_down, offsets, M, d, f, E, ksplit, y_perm, status, stream,
-                        "moe_grouped_gemm_down_fp8b");
+    return gemm8_entry(1, h8, sh, w8_down, s_down, offsets, M, d, f, E, ksplit, y_perm, status, stream,
+                       "moe_grouped_gemm_down_fp8b", true);
 }
 
 int moe_forward_fp8b(const void* x, const float* logits, const void* w8_gate_up, const float* s_gate_up,
                      const void* w8_down, const float* s_down, int T, int d, int f, int E, int top_k, void* out,
                      void* workspace, size_t workspace_bytes, moe_stream_t stream) {
-    int rc = check_shape_fp8(T, d, f, E, top_k, "moe_forward_fp8b");
-    if (rc) return rc;
-    if (T == 0) return ok();
-    if (!x || !logits || !w8_gate_up || !s_gate_up || !w8_down || !s_down || !out)
-        return fail(MOE_ERR_INVALID_ARG, "moe_forward_fp8b: null pointer");
-    if (!aligned16(x) || !aligned16(w8_gate_up) || !aligned16(w8_down) || !aligned16(out) ||
-        (reinterpret_cast<uintptr_t>(s_gate_up) & 3u) || (reinterpret_cast<uintptr_t>(s_down) & 3u))
-        return fail(MOE_ERR_INVALID_ARG, "moe_forward_fp8b: tensors must be 16-byte (scales 4-byte) aligned");
-    const size_t need = layout_fp8(T, d, f, E, top_k, true).total;
-    if (!workspace || workspace_bytes < need)
-        return fail(MOE_ERR_WORKSPACE, "moe_forward_fp8b: workspace %zu bytes < %zu needed", workspace_bytes, need);
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
-        return fail(MOE_ERR_WORKSPACE, "moe_forward_fp8b: workspace must be 256-byte aligned");
-    int sms;
-    if ((rc = check_device(&sms))) return rc;
-    return run_layer_fp8b(x, logits, w8_gate_up, s_gate_up, w8_down, s_down, T, d, f, E, top_k, out, workspace, sms,
-                          static_cast<cudaStream_t>(stream));
+    return forward8_entry(x, logits, w8_gate_up, s_gate_up, w8_down, s_down, T, d, f, E, top_k, out, workspace,
+                          workspace_bytes, stream, true);
 }
 
 int moe_get_device_error(const void* status_or_workspace, int32_t* code) {
