@@ -289,8 +289,6 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     logits, x, wgu, wd = make_inputs(w, seed=args.seed + rank, weight_device=str(dev))
     x_d, l_d = x.to(dev), logits.to(dev)
     if fp8:
-        if w.router[0] == "grouped":
-            raise SystemExit("--dtype e4m3/e4m3b run the softmax router only")
         quant = moe.quantize_weights_fp8b if blocks else moe.quantize_weights_fp8
         w8 = quant(wgu) + quant(wd)  # (wgu8, sgu, wd8, sd), once
         torch.cuda.synchronize(dev)
@@ -307,7 +305,10 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     bias_d = draw_router_bias(w, seed=args.seed + rank).to(dev)
 
     def step():
-        if blocks:
+        if fp8 and grouped:  # an FP8 layer with DeepSeek-V3's router as step 1
+            _, G, tg, scale, _ = w.router
+            moe.forward_grouped_fp8(x_d, l_d, bias_d, *w8, w.k, G, tg, scale, out=out, workspace=ws, blocks=blocks)
+        elif blocks:
             moe.forward_fp8b(x_d, l_d, *w8, w.k, out=out, workspace=ws)
         elif fp8:
             moe.forward_fp8(x_d, l_d, *w8, w.k, out=out, workspace=ws)
@@ -374,8 +375,10 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     stages = STAGES_FP8B if blocks else (STAGES_FP8 if fp8 else STAGES)
     if blocks:
         x8, sx, h8, sh = v["x8"], v["sx"], v["h8"], v["sh"]
+        route_call = ((lambda: moe.route_grouped(l_d, bias_d, w.k, *w.router[1:4], idx=idx, w=wts)) if grouped else
+                      (lambda: moe.route(l_d, w.k, idx=idx, w=wts)))
         calls = [
-            lambda: moe.route(l_d, w.k, idx=idx, w=wts),
+            route_call,
             lambda: moe.permute(idx, x_d, w.E, status=st, out=(counts_d, offs, src, dest, None)),
             lambda: moe.quantize_rows_fp8b(x_d, src, status=st, out=(x8, sx)),
             lambda: moe.grouped_gemm_gateup_swiglu_fp8b(x8, sx, w8[0], w8[1], offs, h=h, status=st),
@@ -385,8 +388,10 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         ]
     elif fp8:
         x8, sx, h8, sh = v["x8"], v["sx"], v["h8"], v["sh"]
+        route_call = ((lambda: moe.route_grouped(l_d, bias_d, w.k, *w.router[1:4], idx=idx, w=wts)) if grouped else
+                      (lambda: moe.route(l_d, w.k, idx=idx, w=wts)))
         calls = [
-            lambda: moe.route(l_d, w.k, idx=idx, w=wts),
+            route_call,
             lambda: moe.permute_fp8(idx, x_d, w.E, status=st, out=(counts_d, offs, src, dest, x8, sx)),
             lambda: moe.grouped_gemm_gateup_swiglu_fp8(x8, sx, w8[0], w8[1], offs, h=h, status=st),
             lambda: moe.quantize_rows_fp8(h, status=st, out=(h8, sh)),
@@ -485,9 +490,11 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         "host_weights": (wgu, wd), "inputs": (logits, x), "step_ms_p10_p90": (
             float(np.percentile(step_ms, 10)), float(np.percentile(step_ms, 90))),
         "peak_src": peak_src, "peaks": peaks, "ksplit": v["ksplit"],
-        "launches_per_step": (moe.forward_fp8b_launch_count(w.T, w.E, w.k) if blocks else
+        # DeepSeek-V3's router never fuses with the permutation: 5 (bf16), 6 (e4m3), 7 (e4m3b).
+        "launches_per_step": ((7 if blocks else 6 if fp8 else 5) if grouped else
+                              moe.forward_fp8b_launch_count(w.T, w.E, w.k) if blocks else
                               moe.forward_fp8_launch_count(w.T, w.E, w.k) if fp8 else
-                              5 if grouped else moe.forward_launch_count(w.T, w.E, w.k)),
+                              moe.forward_launch_count(w.T, w.E, w.k)),
     }
 
 
@@ -508,7 +515,11 @@ def oracle_sample_runner(w: Workload, logits, x, wgu, wd, seed: int = 0, fp8: bo
 
     def run(S: int) -> float:
         t0 = time.perf_counter()
-        if blocks:
+        if fp8 and w.router[0] == "grouped":
+            idx, wts = O.route_grouped(ln[:S], bias, w.k, *w.router[1:4])
+            fwd = O.forward_fp8b_tokens_routed if blocks else O.forward_fp8_tokens_routed
+            fwd(xb, idx, wts, *w8, np.arange(S, dtype=np.int32))
+        elif blocks:
             O.forward_fp8b(xb[:S], ln[:S], *w8, w.k)
         elif fp8:
             O.forward_fp8(xb[:S], ln[:S], *w8, w.k)

@@ -372,6 +372,19 @@ MOE_API int moe_forward_fp8b(const void* x, const float* logits, const void* w8_
                              const void* w8_down, const float* s_down, int T, int d, int f, int E, int top_k,
                              void* out, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* The FP8 layers with DeepSeek-V3's router (moe_route_grouped) as step 1: bias [E] fp32, n_group,
+ * topk_group and scale as for moe_route_grouped; everything else as for moe_forward_fp8 /
+ * moe_forward_fp8b, with the same workspaces.  6 launches (per-row / per-channel scales) or 7
+ * (blockwise): routing and the permutation never fuse with this router. */
+MOE_API int moe_forward_grouped_fp8(const void* x, const float* logits, const float* bias, const void* w8_gate_up,
+                                    const float* s_gate_up, const void* w8_down, const float* s_down, int T, int d,
+                                    int f, int E, int top_k, int n_group, int topk_group, float scale, void* out,
+                                    void* workspace, size_t workspace_bytes, moe_stream_t stream);
+MOE_API int moe_forward_grouped_fp8b(const void* x, const float* logits, const float* bias, const void* w8_gate_up,
+                                     const float* s_gate_up, const void* w8_down, const float* s_down, int T, int d,
+                                     int f, int E, int top_k, int n_group, int topk_group, float scale, void* out,
+                                     void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* Reads (synchronously: cudaMemcpy) a device status word — a stage call's `status` pointer, or
  * the workspace of moe_forward — into *code (0 = no device-side error). */
 MOE_API int moe_get_device_error(const void* status_or_workspace, int32_t* code);

@@ -364,7 +364,7 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
 // blockwise kernel's.
 int run_layer_fp8(const void* x, const float* logits, const void* wgu8, const float* sgu, const void* wd8,
                   const float* sd, int T, int d, int f, int E, int k, void* out, void* ws, int num_sms,
-                  cudaStream_t s, bool blocks) {
+                  cudaStream_t s, bool blocks, const Router& router = Router()) {
     const Layout8 L = layout_fp8(T, d, f, E, k, blocks);
     int32_t* status = at<int32_t>(ws, L.status);
     int32_t* idx = at<int32_t>(ws, L.idx);
@@ -384,12 +384,15 @@ int run_layer_fp8(const void* x, const float* logits, const void* wgu8, const fl
     uint8_t* perm_x8 = blocks ? nullptr : x8;  // per-row scales: the permutation quantises x itself
     float* perm_sx = blocks ? nullptr : sx;
     cudaError_t e;
-    if (fuse_route_permute(T, E)) {
+    if (!router.grouped && fuse_route_permute(T, E)) {
         if ((e = launch_route_permute(logits, xb, T, d, E, k, idx, w, counts, offsets, src, dest, nullptr, status,
                                       num_sms, s, perm_x8, perm_sx)) != cudaSuccess)
             return launched(e, "route+permute");
     } else {
-        if ((e = launch_route(logits, T, E, k, idx, w, status, s)) != cudaSuccess) return launched(e, "route");
+        e = router.grouped ? launch_route_grouped(logits, router.bias, T, E, k, router.n_group, router.topk_group,
+                                                  router.scale, idx, w, status, s)
+                           : launch_route(logits, T, E, k, idx, w, status, s);
+        if (e != cudaSuccess) return launched(e, "route");
         if ((e = launch_permute(idx, xb, T, d, E, k, counts, offsets, src, dest, nullptr, status, num_sms, s, perm_x8,
                                 perm_sx)) != cudaSuccess)
             return launched(e, "permute");
@@ -874,10 +877,13 @@ int moe_grouped_gemm_down_fp8(const void* h8, const float* sh, const void* w8_do
 // moe_forward_fp8 and moe_forward_fp8b: argument checks, then the layer.
 static int forward8_entry(const void* x, const float* logits, const void* w8_gate_up, const float* s_gate_up,
                           const void* w8_down, const float* s_down, int T, int d, int f, int E, int top_k, void* out,
-                          void* workspace, size_t workspace_bytes, moe_stream_t stream, bool blocks) {
-    const char* name = blocks ? "moe_forward_fp8b" : "moe_forward_fp8";
+                          void* workspace, size_t workspace_bytes, moe_stream_t stream, bool blocks,
+                          const Router& router = Router()) {
+    const char* name = router.grouped ? (blocks ? "moe_forward_grouped_fp8b" : "moe_forward_grouped_fp8")
+                                      : (blocks ? "moe_forward_fp8b" : "moe_forward_fp8");
     int rc = check_shape_fp8(T, d, f, E, top_k, name);
     if (rc) return rc;
+    if ((rc = check_router(router, E, top_k, name))) return rc;
     if (T == 0) return ok();
     if (!x || !logits || !w8_gate_up || !s_gate_up || !w8_down || !s_down || !out)
         return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
@@ -892,7 +898,33 @@ static int forward8_entry(const void* x, const float* logits, const void* w8_gat
     int sms;
     if ((rc = check_device(&sms))) return rc;
     return run_layer_fp8(x, logits, w8_gate_up, s_gate_up, w8_down, s_down, T, d, f, E, top_k, out, workspace, sms,
-                         static_cast<cudaStream_t>(stream), blocks);
+                         static_cast<cudaStream_t>(stream), blocks, router);
+}
+
+static Router grouped_router(const float* bias, int n_group, int topk_group, float scale) {
+    Router r;
+    r.grouped = true;
+    r.bias = bias;
+    r.n_group = n_group;
+    r.topk_group = topk_group;
+    r.scale = scale;
+    return r;
+}
+
+int moe_forward_grouped_fp8(const void* x, const float* logits, const float* bias, const void* w8_gate_up,
+                            const float* s_gate_up, const void* w8_down, const float* s_down, int T, int d, int f,
+                            int E, int top_k, int n_group, int topk_group, float scale, void* out, void* workspace,
+                            size_t workspace_bytes, moe_stream_t stream) {
+    return forward8_entry(x, logits, w8_gate_up, s_gate_up, w8_down, s_down, T, d, f, E, top_k, out, workspace,
+                          workspace_bytes, stream, false, grouped_router(bias, n_group, topk_group, scale));
+}
+
+int moe_forward_grouped_fp8b(const void* x, const float* logits, const float* bias, const void* w8_gate_up,
+                             const float* s_gate_up, const void* w8_down, const float* s_down, int T, int d, int f,
+                             int E, int top_k, int n_group, int topk_group, float scale, void* out, void* workspace,
+                             size_t workspace_bytes, moe_stream_t stream) {
+    return forward8_entry(x, logits, w8_gate_up, s_gate_up, w8_down, s_down, T, d, f, E, top_k, out, workspace,
+                          workspace_bytes, stream, true, grouped_router(bias, n_group, topk_group, scale));
 }
 
 int moe_forward_fp8(const void* x, const float* logits, const void* w8_gate_up, const float* s_gate_up,

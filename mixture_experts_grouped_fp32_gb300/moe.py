@@ -61,6 +61,10 @@ _SIGS = {
     "moe_down_ksplit_fp8b": ([_I, _I, _I, _I, _I], _I),
     "moe_forward_fp8b_launch_count": ([_I, _I, _I], _I),
     "moe_forward_fp8b": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
+    "moe_forward_grouped_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P,
+                                 _SZ, _P], _I),
+    "moe_forward_grouped_fp8b": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P,
+                                  _SZ, _P], _I),
 }
 
 WS_FIELDS = ("status", "idx", "w", "counts", "offsets", "src", "dest", "x_perm", "h", "y_perm", "total")
@@ -671,3 +675,25 @@ def workspace_views_fp8b(ws: torch.Tensor, T: int, d: int, f: int, E: int, top_k
         "y_perm": view("y_perm", S * M * d, torch.float32, (S, M, d)),
         "ksplit": S,
     }
+
+
+def forward_grouped_fp8(x, logits, bias, w8_gate_up, s_gate_up, w8_down, s_down, top_k, n_group, topk_group,
+                        scale=1.0, out=None, workspace=None, stream=None, blocks: bool = False):
+    """An FP8 layer (per-row / per-channel scales, or blockwise with ``blocks``) with DeepSeek-V3's
+    router as step 1.  Weights as returned by quantize_weights_fp8 / quantize_weights_fp8b."""
+    _dev(x, torch.bfloat16, "x")
+    _dev(logits, torch.float32, "logits")
+    _dev(bias, torch.float32, "bias")
+    _dev(s_gate_up, torch.float32, "s_gate_up")
+    _dev(s_down, torch.float32, "s_down")
+    T, d = x.shape
+    E, f2, _ = _w8_dims(w8_gate_up, "w8_gate_up")
+    _w8_dims(w8_down, "w8_down")
+    if workspace is None:
+        size = workspace_size_fp8b if blocks else workspace_size_fp8
+        workspace = torch.empty(size(T, d, f2 // 2, E, top_k), dtype=torch.uint8, device=x.device)
+    out = out if out is not None else torch.empty(T, d, dtype=torch.bfloat16, device=x.device)
+    _call("moe_forward_grouped_fp8b" if blocks else "moe_forward_grouped_fp8", _ptr(x), _ptr(logits), _ptr(bias),
+          _ptr(w8_gate_up), _ptr(s_gate_up), _ptr(w8_down), _ptr(s_down), T, d, f2 // 2, E, top_k, n_group,
+          topk_group, float(scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    return out

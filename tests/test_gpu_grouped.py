@@ -170,3 +170,86 @@ def test_forward_grouped_full_size(moe, oracle):
                                        to_np_bits(wd), sample.astype(np.int32))
     got = out[torch.from_numpy(sample).to(dev)].float().cpu().numpy()
     assert_layer_close(got, ref, f"deepseek_v3_t2048 sampled tokens {sample.tolist()}")
+
+
+def _quantised(moe, oracle, wgu, wd, blocks):
+    """GPU weight codes and the oracle's (checked equal, so that both sides use the same weights)."""
+    from mixture_experts_grouped_fp32_gb300.moe import fp8_unblock
+    gq = moe.quantize_weights_fp8b if blocks else moe.quantize_weights_fp8
+    oq = oracle.quantize_weights_fp8b if blocks else oracle.quantize_weights_fp8
+    g = gq(wgu.to(DEV)) + gq(wd.to(DEV))
+    r = oq(to_np_bits(wgu)) + oq(to_np_bits(wd))
+    torch.cuda.synchronize()
+    assert np.array_equal(fp8_unblock(g[0].cpu().numpy()), r[0]) and np.array_equal(g[1].cpu().numpy(), r[1])
+    assert np.array_equal(fp8_unblock(g[2].cpu().numpy()), r[2]) and np.array_equal(g[3].cpu().numpy(), r[3])
+    return g, r
+
+
+@pytest.mark.parametrize("blocks", [False, True], ids=["fp8", "fp8b"])
+@pytest.mark.parametrize("w", LAYER_CASES, ids=lambda w: w.name)
+def test_forward_grouped_fp8_matches_oracle(moe, oracle, w, blocks):
+    """The FP8 layers with DeepSeek-V3's router: routing as for the bf16 layer, the output of every
+    token routed like the oracle's against the FP8 oracle at the layer tolerance."""
+    _, G, tg, scale, _ = w.router
+    logits, x, wgu, wd = case_inputs(w, seed=4)
+    bias = draw_router_bias(w, seed=4)
+    gw, rw = _quantised(moe, oracle, wgu, wd, blocks)
+    size = moe.workspace_size_fp8b if blocks else moe.workspace_size_fp8
+    views = moe.workspace_views_fp8b if blocks else moe.workspace_views_fp8
+    ws = torch.empty(size(w.T, w.d, w.f, w.E, w.k), dtype=torch.uint8, device=DEV)
+    out = moe.forward_grouped_fp8(x.to(DEV), logits.to(DEV), bias.to(DEV), *gw, w.k, G, tg, scale, workspace=ws,
+                                  blocks=blocks)
+    torch.cuda.synchronize()
+    assert moe.get_device_error(ws) == 0
+    v = views(ws, w.T, w.d, w.f, w.E, w.k)
+    ln, bn = logits.numpy(), bias.numpy()
+    ref_idx, ref_w = oracle.route_grouped(ln, bn, w.k, G, tg, scale)
+    same = check_routing(v["idx"].cpu().numpy(), v["w"].cpu().numpy(), ref_idx, ref_w, ln, bn, w.k, G, tg)
+    fwd = oracle.forward_fp8b_tokens_routed if blocks else oracle.forward_fp8_tokens_routed
+    tokens = np.nonzero(same)[0].astype(np.int32)
+    ref = fwd(to_np_bits(x), ref_idx[tokens], ref_w[tokens], *rw, tokens)
+    assert_layer_close(out.float().cpu().numpy()[tokens], ref, f"{w.name} grouped router, {'fp8b' if blocks else 'fp8'}")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("blocks", [False, True], ids=["fp8", "fp8b"])
+def test_forward_grouped_fp8_full_size(moe, oracle, blocks):
+    """DeepSeek-V3's layer shape and router at full size on the FP8 layers: weight codes bit for bit,
+    routing checked for every token, the output on sampled tokens against the FP8 oracle."""
+    from mixture_experts_grouped_fp32_gb300.moe import fp8_unblock
+    from mixture_experts_grouped_fp32_gb300.workloads import make_inputs
+    w = WORKLOADS["deepseek_v3_t2048"]
+    _, G, tg, scale, _ = w.router
+    logits, x, wgu, wd = make_inputs(w, seed=0, weight_device="cuda")
+    bias = draw_router_bias(w, seed=0)
+    gq = moe.quantize_weights_fp8b if blocks else moe.quantize_weights_fp8
+    gw = gq(wgu) + gq(wd)
+    torch.cuda.synchronize()
+    wgu_bits, wd_bits = to_np_bits(wgu), to_np_bits(wd)
+    del wgu, wd
+    torch.cuda.empty_cache()
+    size = moe.workspace_size_fp8b if blocks else moe.workspace_size_fp8
+    views = moe.workspace_views_fp8b if blocks else moe.workspace_views_fp8
+    ws = torch.empty(size(w.T, w.d, w.f, w.E, w.k), dtype=torch.uint8, device=DEV)
+    out = moe.forward_grouped_fp8(x.to(DEV), logits.to(DEV), bias.to(DEV), *gw, w.k, G, tg, scale, workspace=ws,
+                                  blocks=blocks)
+    torch.cuda.synchronize()
+    assert moe.get_device_error(ws) == 0
+    v = views(ws, w.T, w.d, w.f, w.E, w.k)
+    oq = oracle.quantize_weights_fp8b if blocks else oracle.quantize_weights_fp8
+    r_gu = oq(wgu_bits)
+    assert np.array_equal(fp8_unblock(gw[0].cpu().numpy()), r_gu[0]) and np.array_equal(gw[1].cpu().numpy(), r_gu[1])
+    del wgu_bits
+    r_d = oq(wd_bits)
+    assert np.array_equal(fp8_unblock(gw[2].cpu().numpy()), r_d[0]) and np.array_equal(gw[3].cpu().numpy(), r_d[1])
+    del wd_bits
+    ln, bn = logits.numpy(), bias.numpy()
+    ref_idx, ref_w = oracle.route_grouped(ln, bn, w.k, G, tg, scale)
+    same = check_routing(v["idx"].cpu().numpy(), v["w"].cpu().numpy(), ref_idx, ref_w, ln, bn, w.k, G, tg)
+    rng = np.random.default_rng(7)
+    sample = np.unique(np.concatenate([[0, w.T - 1], rng.integers(0, w.T, 6)]))
+    sample = sample[same[sample]].astype(np.int32)
+    fwd = oracle.forward_fp8b_tokens_routed if blocks else oracle.forward_fp8_tokens_routed
+    ref = fwd(to_np_bits(x), ref_idx[sample], ref_w[sample], *r_gu, *r_d, sample)
+    got = out[torch.from_numpy(sample).long().to(DEV)].float().cpu().numpy()
+    assert_layer_close(got, ref, f"deepseek_v3_t2048 {'fp8b' if blocks else 'fp8'} sampled tokens {sample.tolist()}")
