@@ -164,6 +164,9 @@ LAYER_CASES = [
     Workload("fp8b_many_rows", 700, 256, 384, 4, 2),
     Workload("fp8b_skewed", 300, 384, 256, 16, 4, ("zipf", 1.2)),
     Workload("fp8b_one_token", 1, 512, 256, 8, 2),
+    Workload("fp8b_dense_e1_k1", 70, 128, 256, 1, 1),
+    Workload("fp8b_k_eq_e", 37, 256, 384, 4, 4),
+    Workload("fp8b_many_experts", 96, 128, 128, 256, 8, ("zipf", 1.2)),
     Workload("fp8b_deepseek_like", 48, 1024, 256, 64, 8, ("zipf", 1.2)),
 ]
 
