@@ -261,7 +261,8 @@ MOE_API int moe_forward_noalloc(const void* x, const float* logits, const void* 
  * applied in the GEMM epilogue.  DeepGEMM PR #304 write-up, section 5.3 (an FP8 grouped GEMM on
  * SM100) and its Mega MoE figure (SwiGLU then FP8 quantisation inside the fused layer) are the
  * pages' FP8 context; they scale 128-wide blocks, this variant scales whole rows and columns (its
- * scales then need no per-block promotion of the accumulator).  d and f must be multiples of 128.
+ * scales then need no per-block promotion of the accumulator).  d and f must be multiples of 128; codes
+ * and weight scales 16-byte aligned, row scales 4-byte aligned.
  * ------------------------------------------------------------------------------------------- */
 
 /* Weights, once per model: W [E,K,N] bf16 (as w_gate_up [E,d,2f] or w_down [E,f,d]) -> Wq E4M3

@@ -343,8 +343,11 @@ __device__ __forceinline__ void raise_abort(Ctl& c, int32_t* status) {
     flag_status(status, MOE_STATUS_WAIT_TIMEOUT);
 }
 
+// silu(g) * u = g / (1 + e^-g) * u, with CUDA's fast-divide intrinsic: its error (~2 ulp) is far
+// below the bf16 rounding of h that follows (for g below about -88, 1 + e^-g is infinite and the
+// quotient is -0, as silu's limit).
 __device__ __forceinline__ float silu_mul(float g, float u) {
-    return g / (1.0f + __expf(-g)) * u;
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 __device__ __forceinline__ uint16_t bf16_bits(float v) {
@@ -869,9 +872,16 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                         const int col = n0 + cc * 32;
                         if (FP8 && row_ok && col < N) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {  // the column scales are the same in every lane
-                                g[j] = __float_as_uint(__uint_as_float(g[j]) * (srow * __ldg(sbe + col + j)));
-                                u[j] = __float_as_uint(__uint_as_float(u[j]) * (srow * __ldg(sbe + N + col + j)));
+                            for (int j4 = 0; j4 < 8; ++j4) {  // the column scales are the same in every lane
+                                const float4 sg = __ldg(reinterpret_cast<const float4*>(sbe + col) + j4);
+                                const float4 su = __ldg(reinterpret_cast<const float4*>(sbe + N + col) + j4);
+                                const float sgv[4] = {sg.x, sg.y, sg.z, sg.w}, suv[4] = {su.x, su.y, su.z, su.w};
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    const int j = 4 * j4 + q;
+                                    g[j] = __float_as_uint(__uint_as_float(g[j]) * (srow * sgv[q]));
+                                    u[j] = __float_as_uint(__uint_as_float(u[j]) * (srow * suv[q]));
+                                }
                             }
                         }
                         if (row_ok && col < N) {
@@ -899,8 +909,13 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                         const int col = n0 + cc * 32;
                         if (FP8 && row_ok && col < N) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                v32[j] = __float_as_uint(__uint_as_float(v32[j]) * (srow * __ldg(sbe + col + j)));
+                            for (int j4 = 0; j4 < 8; ++j4) {
+                                const float4 sc = __ldg(reinterpret_cast<const float4*>(sbe + col) + j4);
+                                const float scv[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    v32[4 * j4 + q] = __float_as_uint(__uint_as_float(v32[4 * j4 + q]) * (srow * scv[q]));
+                            }
                         }
                         if (row_ok && col < N) {
                             float4* dst = reinterpret_cast<float4*>(y + grow * N + col);

@@ -113,7 +113,8 @@ __device__ __forceinline__ void raise_abort(Ctl& c, int32_t* status) {
     flag_status(status, MOE_STATUS_WAIT_TIMEOUT);
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+// silu(g) * u with the fast-divide intrinsic (its ~2 ulp error is far below h's bf16 rounding).
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 __device__ __forceinline__ uint16_t bf16_bits(float v) {
     __nv_bfloat16 b = __float2bfloat16_rn(v);

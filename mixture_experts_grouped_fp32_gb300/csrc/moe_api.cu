@@ -839,8 +839,8 @@ static int gemm8_entry(int kind, const void* A, const float* sa, const void* B, 
     if (!A || !sa || !B || !sb || !offsets || !out) return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
     if (!aligned16(A) || !aligned16(B) || !aligned16(out))
         return fail(MOE_ERR_INVALID_ARG, "%s: operands must be 16-byte aligned", name);
-    if ((reinterpret_cast<uintptr_t>(sb) & 3u) || (reinterpret_cast<uintptr_t>(sa) & 3u))
-        return fail(MOE_ERR_INVALID_ARG, "%s: scales must be 4-byte aligned", name);
+    if (!aligned16(sb) || (reinterpret_cast<uintptr_t>(sa) & 3u))
+        return fail(MOE_ERR_INVALID_ARG, "%s: weight scales must be 16-byte, row scales 4-byte aligned", name);
     int sms;
     if ((rc = check_device(&sms))) return rc;
     const int pair = blocks ? 0 : use_pair(M, E, kind == 0 ? f : d, kind, true);
@@ -887,9 +887,9 @@ static int forward8_entry(const void* x, const float* logits, const void* w8_gat
     if (T == 0) return ok();
     if (!x || !logits || !w8_gate_up || !s_gate_up || !w8_down || !s_down || !out)
         return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
-    if (!aligned16(x) || !aligned16(w8_gate_up) || !aligned16(w8_down) || !aligned16(out) ||
-        (reinterpret_cast<uintptr_t>(s_gate_up) & 3u) || (reinterpret_cast<uintptr_t>(s_down) & 3u))
-        return fail(MOE_ERR_INVALID_ARG, "%s: tensors must be 16-byte (scales 4-byte) aligned", name);
+    if (!aligned16(x) || !aligned16(w8_gate_up) || !aligned16(w8_down) || !aligned16(out) || !aligned16(s_gate_up) ||
+        !aligned16(s_down))
+        return fail(MOE_ERR_INVALID_ARG, "%s: tensors and weight scales must be 16-byte aligned", name);
     const size_t need = layout_fp8(T, d, f, E, top_k, blocks).total;
     if (!workspace || workspace_bytes < need)
         return fail(MOE_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", name, workspace_bytes, need);
