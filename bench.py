@@ -53,15 +53,16 @@ L2_FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 STAGES = ("route", "permute", "gateup_swiglu", "down", "combine")
 KERNEL_NAMES = {"route": "route_kernel", "permute": "permute_kernel",
-                "gateup_swiglu": "grouped_gemm_kernel<0>", "down": "grouped_gemm_kernel<1>",
+                "gateup_swiglu": "grouped_gemm_kernel<0, false, false>",
+                "down": "grouped_gemm_kernel<1, false, false>",
                 "combine": "combine_kernel"}
 # The FP8 layer's stages (moe_forward_fp8) and its GEMM kernels' template instances <KIND, GATHER, FP8>.
 STAGES_FP8 = ("route", "permute", "gateup_swiglu", "quantize_h", "down", "combine")
 KERNEL_NAMES_FP8 = {"gateup_swiglu": "grouped_gemm_kernel<0, false, true>",
                     "down": "grouped_gemm_kernel<1, false, true>"}
 STAGES_FP8B = ("route", "permute", "quantize_x", "gateup_swiglu", "quantize_h", "down", "combine")
-KERNEL_NAMES_FP8B = {"gateup_swiglu": "grouped_gemm_kernel<0, false, true, true>",
-                     "down": "grouped_gemm_kernel<1, false, true, true>"}
+KERNEL_NAMES_FP8B = {"gateup_swiglu": "grouped_gemm_fp8b_kernel<0>",
+                     "down": "grouped_gemm_fp8b_kernel<1>"}
 FP8_OVER_BF16 = 2.0  # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s) applied to the measured bf16 peak
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum per launch) from ncu captures of the
@@ -71,43 +72,47 @@ FP8_OVER_BF16 = 2.0  # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s) appl
 AUTO_TIMED_S = 0.5
 AUTO_STEPS_MIN, AUTO_STEPS_MAX = 50, 4000
 
-_TRAFFIC_HASH = "4b383edeb4f77185"  # GEMM source hash the captures below were taken at
-_TRAFFIC_HASH_FP8B = "637ecc65f4d2dad2"  # ... and that of the blockwise FP8 kernel's sources
+_TRAFFIC_HASH = "a8d3a7a96e328c09"  # GEMM source hash the captures below were taken at
+_TRAFFIC_HASH_FP8B = "5f6734ae94ec4ddf"  # ... and that of the blockwise FP8 kernel's sources
 MEASURED_TRAFFIC = {
-    ("mixtral_t32", "gateup_swiglu"): (1884874752, _TRAFFIC_HASH),
-    ("mixtral_t32", "down"): (944451840, _TRAFFIC_HASH),
-    ("mixtral_t512", "gateup_swiglu"): (1917088768, _TRAFFIC_HASH),
-    ("mixtral_t512", "down"): (982745856, _TRAFFIC_HASH),
-    ("mixtral_t512_skew40", "gateup_swiglu"): (1917344256, _TRAFFIC_HASH),
-    ("mixtral_t512_skew40", "down"): (983449344, _TRAFFIC_HASH),
-    ("mixtral_t4096", "gateup_swiglu"): (2596496384, _TRAFFIC_HASH),
-    ("mixtral_t4096", "down"): (1552656640, _TRAFFIC_HASH),
-    ("deepseek_e32_t256", "gateup_swiglu"): (1920297728, _TRAFFIC_HASH),
-    ("deepseek_e32_t256", "down"): (1008994816, _TRAFFIC_HASH),
-    ("deepseek_t2048", "gateup_swiglu"): (8110466304, _TRAFFIC_HASH),
-    ("deepseek_t2048", "down"): (4196724480, _TRAFFIC_HASH),
-    ("deepseek_v3_t2048", "gateup_swiglu"): (4703464960, _TRAFFIC_HASH),
-    ("deepseek_v3_t2048", "down"): (2482137600, _TRAFFIC_HASH),
-    ("mixtral_t32", "gateup_swiglu_fp8"): (945577216, _TRAFFIC_HASH),
-    ("mixtral_t32", "down_fp8"): (474084352, _TRAFFIC_HASH),
-    ("mixtral_t512", "gateup_swiglu_fp8"): (971990272, _TRAFFIC_HASH),
-    ("mixtral_t512", "down_fp8"): (497739008, _TRAFFIC_HASH),
-    ("mixtral_t512_skew40", "gateup_swiglu_fp8"): (971613696, _TRAFFIC_HASH),
-    ("mixtral_t512_skew40", "down_fp8"): (498119168, _TRAFFIC_HASH),
-    ("mixtral_t4096", "gateup_swiglu_fp8"): (1201340928, _TRAFFIC_HASH),
-    ("mixtral_t4096", "down_fp8"): (781184000, _TRAFFIC_HASH),
-    ("deepseek_e32_t256", "gateup_swiglu_fp8"): (965993216, _TRAFFIC_HASH),
-    ("deepseek_e32_t256", "down_fp8"): (534342144, _TRAFFIC_HASH),
-    ("deepseek_t2048", "gateup_swiglu_fp8"): (3891759104, _TRAFFIC_HASH),
-    ("deepseek_t2048", "down_fp8"): (2295916544, _TRAFFIC_HASH),
-    ("mixtral_t32", "gateup_swiglu_fp8b"): (945041664, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t32", "down_fp8b"): (474054656, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512", "gateup_swiglu_fp8b"): (1294983680, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512", "down_fp8b"): (616183040, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t4096", "gateup_swiglu_fp8b"): (1199375616, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t4096", "down_fp8b"): (728358656, _TRAFFIC_HASH_FP8B),
-    ("deepseek_t2048", "gateup_swiglu_fp8b"): (3747385088, _TRAFFIC_HASH_FP8B),
-    ("deepseek_t2048", "down_fp8b"): (2315257600, _TRAFFIC_HASH_FP8B),
+    ("deepseek_e32_t256", "gateup_swiglu"): (1919914752, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "down"): (1008838144, _TRAFFIC_HASH),
+    ("mixtral_t32", "gateup_swiglu"): (1884825088, _TRAFFIC_HASH),
+    ("mixtral_t32", "down"): (944483328, _TRAFFIC_HASH),
+    ("mixtral_t4096", "gateup_swiglu"): (3337290496, _TRAFFIC_HASH),
+    ("mixtral_t4096", "down"): (1656340992, _TRAFFIC_HASH),
+    ("mixtral_t512", "gateup_swiglu"): (1917540864, _TRAFFIC_HASH),
+    ("mixtral_t512", "down"): (982737664, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "gateup_swiglu"): (1917613056, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "down"): (983452672, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "gateup_swiglu_fp8"): (966500352, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "down_fp8"): (534014976, _TRAFFIC_HASH),
+    ("mixtral_t32", "gateup_swiglu_fp8"): (945943296, _TRAFFIC_HASH),
+    ("mixtral_t32", "down_fp8"): (474108672, _TRAFFIC_HASH),
+    ("mixtral_t4096", "gateup_swiglu_fp8"): (1211593984, _TRAFFIC_HASH),
+    ("mixtral_t4096", "down_fp8"): (785332480, _TRAFFIC_HASH),
+    ("mixtral_t512", "gateup_swiglu_fp8"): (972093696, _TRAFFIC_HASH),
+    ("mixtral_t512", "down_fp8"): (498120704, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "gateup_swiglu_fp8"): (971906304, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "down_fp8"): (498307328, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "gateup_swiglu_fp8b"): (966419200, _TRAFFIC_HASH_FP8B),
+    ("deepseek_e32_t256", "down_fp8b"): (533735168, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t32", "gateup_swiglu_fp8b"): (944920576, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t32", "down_fp8b"): (474286336, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t4096", "gateup_swiglu_fp8b"): (1199317760, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t4096", "down_fp8b"): (728835072, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512", "gateup_swiglu_fp8b"): (1312394240, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512", "down_fp8b"): (614131200, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512_skew40", "gateup_swiglu_fp8b"): (973773824, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512_skew40", "down_fp8b"): (515848704, _TRAFFIC_HASH_FP8B),
+    ("deepseek_t2048", "gateup_swiglu"): (8108204800, _TRAFFIC_HASH),
+    ("deepseek_t2048", "down"): (4196736768, _TRAFFIC_HASH),
+    ("deepseek_v3_t2048", "gateup_swiglu"): (4711750656, _TRAFFIC_HASH),
+    ("deepseek_v3_t2048", "down"): (2483243008, _TRAFFIC_HASH),
+    ("deepseek_t2048", "gateup_swiglu_fp8"): (3892582656, _TRAFFIC_HASH),
+    ("deepseek_t2048", "down_fp8"): (2288754688, _TRAFFIC_HASH),
+    ("deepseek_t2048", "gateup_swiglu_fp8b"): (3759550976, _TRAFFIC_HASH_FP8B),
+    ("deepseek_t2048", "down_fp8b"): (2315701504, _TRAFFIC_HASH_FP8B),
 }
 GEMM_SOURCES = ("mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm.cu",
                 "mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm_2sm.cu",
