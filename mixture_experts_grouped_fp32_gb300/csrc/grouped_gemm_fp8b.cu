@@ -8,7 +8,7 @@
 //
 // The scales do not factor out of the K sum, so the accumulation over K blocks cannot stay on the
 // tensor cores: a stage is exactly one K block (128 codes, one 128-byte swizzle row), the MMA
-// thread writes each block's partial product into one of four 128-column tensor-memory buffers
+// thread writes each block's partial product into one of two 256-column tensor-memory buffers
 // (fresh, not accumulated), and eight promotion warps read it, multiply it by that block's
 // scale_row * scale_col and add it into fp32 registers (a fused multiply-add: the scales are powers
 // of two, so the product is exact and the add rounds once, as in the block-by-block sum it
@@ -16,19 +16,23 @@
 // Blockwise FP8 is named on the HPC-Ops page; the DeepGEMM PR #304 write-up's SM100 path encodes
 // its block scale factors as UE8M0 (powers of two), which these scales are.
 //
-// Tiles are sized for the promotion: every item covers 128 accumulator columns, 64 per promotion
-// thread (two warps per tensor-memory lane quarter):
-//   normal   UMMA M = 128 rows x N = 128 weight columns; kind 0: gate n0..n0+63 and up f+n0..f+n0+63
-//            (64 h columns), kind 1: 128 y columns.  Weights arrive as whole 8 KB blocks of the
-//            blocked layout (64 rows x 128 K).
+// Tiles are sized for the tensor cores: one UMMA of M = 128 x N = 256 takes as long as one of
+// N = 128 (measured on this kernel's hand-over loop: 0.32 us per K block either way), so every
+// normal item issues N = 256 MMAs into one of two 256-column tensor-memory buffers, and eight
+// promotion warps (two per tensor-memory lane quarter) each keep 128 fp32 accumulators.  For
+// those registers the block's warpgroups split its register file with setmaxnreg: warpgroup 0
+// (TMA producer, MMA issuer, two idle warps) drops to 40 registers a thread, the two promotion
+// warpgroups rise to 232 (per SM sub-partition: 40 x 32 + 2 x 232 x 32 <= 16384).
+//   normal   UMMA M = 128 rows x N = 256 weight columns; kind 0: gate n0..n0+127 and up
+//            f+n0..f+n0+127 (128 h columns), kind 1: 256 y columns.  Weights arrive as whole
+//            8 KB blocks of the blocked layout (64 rows x 128 K), 32 KB per stage.
 //   swapped  (experts with at most 64 rows) UMMA M = 128 weight columns x N = rows rounded to 16,
-//            two MMAs per K step into columns [0, N) and [64, 64 + N): kind 0 gate and up of 128 h
-//            columns, kind 1 y columns n0.. and n0+128.. — so a swapped item spans two normal
-//            N-tiles and streams 32 KB of weights per stage.
-// Ring: five 40 KB stages (normal: 16 KB activations + 16 KB weights; swapped: up to 8 KB of
-// tokens, then 32 KB of weights).  Scheduling as in grouped_gemm.cu: (expert, N-tile, M-tile,
-// K-slice) items, expert-major, static round-robin over one persistent CTA per SM.  Every wait is
-// bounded (1 s) and reports MOE_STATUS_WAIT_TIMEOUT.
+//            two MMAs per K step (the two 128-row weight groups of the same stage) into columns
+//            [0, N) and [64, 64 + N): the same weight columns as a normal item of that N-tile.
+// Ring: four 48 KB stages (16 KB activations or up to 8 KB of tokens, then 32 KB of weights).
+// Scheduling as in grouped_gemm.cu: (expert, N-tile, M-tile, K-slice) items, expert-major, static
+// round-robin over one persistent CTA per SM.  Every wait is bounded (1 s) and reports
+// MOE_STATUS_WAIT_TIMEOUT.
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -37,27 +41,34 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BKE = 128;                           // K codes per stage = one scale block
-constexpr int STAGES = 5;
-constexpr int STAGE_BYTES = 40 * 1024;
+constexpr int STAGES = 4;
+constexpr int STAGE_BYTES = 48 * 1024;
 constexpr int TOK_BOX_ROWS = 32;
 constexpr int TOK_BOX_BYTES = TOK_BOX_ROWS * BKE;  // 4 KB
-constexpr int A_BYTES = BM * BKE;                  // 16 KB
-constexpr int WBOX64 = 64 * BKE;                   // one weight block, 8 KB
+constexpr int A_BYTES = BM * BKE;                  // 16 KB: activations, or tokens (<= 8 KB)
 constexpr int WBOX128 = 128 * BKE;                 // two weight blocks, 16 KB
-constexpr int SWAP_W_OFF = 2 * TOK_BOX_BYTES;      // swapped stage: tokens (<= 64 rows), then weights
+constexpr int W_OFF = A_BYTES;                     // weights: two 128-row groups from here
 constexpr int SWAP_MAX_ROWS = 64;
-constexpr int PART_COLS = 128;                     // tensor-memory columns per partial buffer
-constexpr int NUM_PART = 4;
+constexpr int PART_COLS = 256;                     // tensor-memory columns per partial buffer
+constexpr int NUM_PART = 2;
 constexpr int TMEM_COLS = NUM_PART * PART_COLS;    // 512
 constexpr int EPI_WARPS = 8;
-constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;   // warp 0 TMA, warp 1 MMA, warps 2-9 promotion
+constexpr int NUM_THREADS = 128 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA, warps 4-11 promotion
+// Registers a thread: at launch (three warps per SM sub-partition: 16384 / 96 rounded down to a
+// multiple of 8), then warpgroup 0 and the promotion warpgroups after setmaxnreg.  The split must
+// not exceed what the block was launched with, or the increase would wait for registers forever;
+// the launcher also checks the compiled count before every launch.
+constexpr int REGS_LAUNCH = 168;
+constexpr int REGS_CTL = 40;
+constexpr int REGS_PROMO = 232;
+static_assert(REGS_CTL * 128 + REGS_PROMO * 32 * EPI_WARPS <= REGS_LAUNCH * NUM_THREADS, "register split");
 constexpr int MAX_E = 256;
 constexpr int SMEM_BYTES = 232448;
-static_assert(SWAP_W_OFF + 2 * WBOX128 <= STAGE_BYTES && A_BYTES + WBOX128 <= STAGE_BYTES, "stage layout");
+static_assert(W_OFF + 2 * WBOX128 <= STAGE_BYTES && 2 * TOK_BOX_BYTES <= A_BYTES, "stage layout");
 
-// Output columns of a normal item (a swapped one covers twice as many).
+// Output columns of an item: kind 0 h columns, kind 1 y columns.
 template <int KIND>
-constexpr int bn_normal() { return KIND == 0 ? 64 : 128; }
+constexpr int bn_item() { return KIND == 0 ? 128 : 256; }
 
 struct Ctl {
     uint64_t full[STAGES];
@@ -78,11 +89,11 @@ struct Item {
     bool swap;
 };
 
-// Work items of an expert with cnt rows.
+// Work items of an expert with cnt rows (a swapped expert takes one M-tile).
 __device__ __forceinline__ int expert_items(int cnt, int N, int bn, int ksplit, int swap_max) {
     if (cnt == 0) return 0;
-    if (cnt <= swap_max) return ((N + 2 * bn - 1) / (2 * bn)) * ksplit;
-    return ((N + bn - 1) / bn) * ((cnt + BM - 1) / BM) * ksplit;
+    const int mt = cnt <= swap_max ? 1 : (cnt + BM - 1) / BM;
+    return ((N + bn - 1) / bn) * mt * ksplit;
 }
 
 // Item i: expert by binary search over item_start, then N-tile, M-tile, K-slice.
@@ -124,11 +135,10 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
-                         const __grid_constant__ CUtensorMap tmB128, const __grid_constant__ CUtensorMap tmB64,
-                         const int32_t* __restrict__ offsets, int M, int K, int N, int E, int ksplit, int swap_max,
-                         const float* __restrict__ a_scale, const float* __restrict__ b_scale, void* __restrict__ out,
-                         int32_t* __restrict__ status) {
-    constexpr int BN = bn_normal<KIND>();
+                         const __grid_constant__ CUtensorMap tmB128, const int32_t* __restrict__ offsets, int M,
+                         int K, int N, int E, int ksplit, int swap_max, const float* __restrict__ a_scale,
+                         const float* __restrict__ b_scale, void* __restrict__ out, int32_t* __restrict__ status) {
+    constexpr int BN = bn_item<KIND>();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     uint8_t* tiles = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -159,7 +169,6 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmA32);
         ptx::prefetch_tensormap(&tmB128);
-        ptx::prefetch_tensormap(&tmB64);
     }
     if (warp == 1) {
         ptx::tmem_alloc(&c.tmem_base, TMEM_COLS);
@@ -206,127 +215,132 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     uint32_t fill_parity[STAGES];
     int filled_mask = 0;
 
-    if (warp == 0 && lane == 0) {
-        // ------------------------------ TMA producer ------------------------------
-        const uint64_t pol_act = ptx::policy_evict_last();
-        const uint64_t pol_wgt = ptx::policy_evict_normal();
-        uint32_t stage = 0, phase = 0;
-        bool aborted = false;
-        for (int i = blockIdx.x; i < total && !aborted; i += gridDim.x) {
-            const Item it = decode_item(c, E, ksplit, swap_max, i);
-            const int n0 = it.n_tile * (it.swap ? 2 * BN : BN);
-            const int nbox32 = (it.rows + TOK_BOX_ROWS - 1) / TOK_BOX_ROWS;
-            const uint32_t tx = it.swap ? 2 * WBOX128 + nbox32 * TOK_BOX_BYTES : A_BYTES + 2 * WBOX64;
-            // Weight rows (output columns) of the item's blocks.
-            const int wr0 = it.e * wrows + n0;
-            const int wr1 = KIND == 0 ? wr0 + N : wr0 + 128;  // swapped kind 0: up; kind 1: the second half
-            const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
-            for (int kb = kb0; kb < kb1; ++kb) {
-                if (!ptx::mbar_wait(&c.empty[stage], phase ^ 1u, abort_flag)) {
-                    raise_abort(c, status);
-                    aborted = true;
-                    break;
-                }
-                uint8_t* st = tiles + stage * STAGE_BYTES;
-                ptx::mbar_arrive_expect_tx(&c.full[stage], tx);
-                if (it.swap) {
-                    for (int q = 0; q < nbox32; ++q)
-                        ptx::tma_load_2d(st + q * TOK_BOX_BYTES, &tmA32, &c.full[stage], kb * BKE,
-                                         it.row0 + q * TOK_BOX_ROWS, pol_act);
-                    ptx::tma_load_4d(st + SWAP_W_OFF, &tmB128, &c.full[stage], 0, 0, kb, wr0 / 64, pol_wgt);
-                    ptx::tma_load_4d(st + SWAP_W_OFF + WBOX128, &tmB128, &c.full[stage], 0, 0, kb, wr1 / 64, pol_wgt);
-                } else {
-                    ptx::tma_load_2d(st, &tmA, &c.full[stage], kb * BKE, it.row0, pol_act);
-                    if (KIND == 0) {  // gate n0..n0+63, then up f+n0..f+n0+63: one block each
-                        ptx::tma_load_4d(st + A_BYTES, &tmB64, &c.full[stage], 0, 0, kb, wr0 / 64, pol_wgt);
-                        ptx::tma_load_4d(st + A_BYTES + WBOX64, &tmB64, &c.full[stage], 0, 0, kb, (wr0 + N) / 64,
-                                         pol_wgt);
-                    } else {  // 128 output columns: two blocks
-                        ptx::tma_load_4d(st + A_BYTES, &tmB128, &c.full[stage], 0, 0, kb, wr0 / 64, pol_wgt);
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTL));
+        if (warp == 0 && lane == 0) {
+            // ------------------------------ TMA producer ------------------------------
+            const uint64_t pol_act = ptx::policy_evict_last();
+            const uint64_t pol_wgt = ptx::policy_evict_normal();
+            uint32_t stage = 0, phase = 0;
+            bool aborted = false;
+            for (int i = blockIdx.x; i < total && !aborted; i += gridDim.x) {
+                const Item it = decode_item(c, E, ksplit, swap_max, i);
+                const int n0 = it.n_tile * BN;
+                const int nbox32 = (it.rows + TOK_BOX_ROWS - 1) / TOK_BOX_ROWS;
+                const uint32_t tx = (it.swap ? nbox32 * TOK_BOX_BYTES : A_BYTES) + 2 * WBOX128;
+                // The two 128-row weight groups: kind 0 gate rows n0.. and up rows f+n0..; kind 1
+                // output columns n0.. and n0+128.. (past the expert's last group: the next expert's
+                // rows or the map's zero fill, computed and never stored).
+                const int wr0 = it.e * wrows + n0;
+                const int wr1 = KIND == 0 ? wr0 + N : wr0 + 128;
+                const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!ptx::mbar_wait(&c.empty[stage], phase ^ 1u, abort_flag)) {
+                        raise_abort(c, status);
+                        aborted = true;
+                        break;
                     }
-                }
-                fill_parity[stage] = phase;
-                filled_mask |= 1 << stage;
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-        }
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer: one partial product per K block, four buffers ----------------
-        constexpr uint32_t idesc_normal = ptx::idesc_e4m3_f32(BM, PART_COLS, 0, 0);
-        uint32_t stage = 0, phase = 0, pb = 0, pph = 0;
-        bool aborted = false;
-        for (int i = blockIdx.x; i < total && !aborted; i += gridDim.x) {
-            const Item it = decode_item(c, E, ksplit, swap_max, i);
-            const uint32_t ntok = (static_cast<uint32_t>(it.rows) + 15u) & ~15u;
-            const uint32_t idesc_swap = ptx::idesc_e4m3_f32(BM, ntok, 0, 0);
-            const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
-            for (int kb = kb0; kb < kb1; ++kb) {
-                if (!ptx::mbar_wait(&c.full[stage], phase, abort_flag) ||
-                    !ptx::mbar_wait(&c.pempty[pb], pph ^ 1u, abort_flag)) {
-                    raise_abort(c, status);
-                    aborted = true;
-                    break;
-                }
-                ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + pb * PART_COLS;
-                const uint32_t sa = ptx::smem_u32(tiles + stage * STAGE_BYTES);
-#pragma unroll
-                for (int kk = 0; kk < BKE / 32; ++kk) {
-                    const uint32_t accum = kk != 0 ? 1u : 0u;  // a fresh partial per K block
-                    const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+                    uint8_t* st = tiles + stage * STAGE_BYTES;
+                    ptx::mbar_arrive_expect_tx(&c.full[stage], tx);
                     if (it.swap) {
-                        // Weights (K-major, 128 rows) as A, the tokens (K-major) as B.
-                        const uint64_t tok = ptx::smem_desc_sw128(sa, 16, 1024);
-                        const uint64_t w0 = ptx::smem_desc_sw128(sa + SWAP_W_OFF, 16, 1024);
-                        const uint64_t w1 = ptx::smem_desc_sw128(sa + SWAP_W_OFF + WBOX128, 16, 1024);
-                        ptx::mma_f8_ss(d_tmem, w0 + off, tok + off, idesc_swap, accum);
-                        ptx::mma_f8_ss(d_tmem + 64, w1 + off, tok + off, idesc_swap, accum);
+                        for (int q = 0; q < nbox32; ++q)
+                            ptx::tma_load_2d(st + q * TOK_BOX_BYTES, &tmA32, &c.full[stage], kb * BKE,
+                                             it.row0 + q * TOK_BOX_ROWS, pol_act);
                     } else {
-                        const uint64_t a = ptx::smem_desc_sw128(sa, 16, 1024);
-                        const uint64_t b = ptx::smem_desc_sw128(sa + A_BYTES, 16, 1024);
-                        ptx::mma_f8_ss(d_tmem, a + off, b + off, idesc_normal, accum);
+                        ptx::tma_load_2d(st, &tmA, &c.full[stage], kb * BKE, it.row0, pol_act);
+                    }
+                    ptx::tma_load_4d(st + W_OFF, &tmB128, &c.full[stage], 0, 0, kb, wr0 / 64, pol_wgt);
+                    ptx::tma_load_4d(st + W_OFF + WBOX128, &tmB128, &c.full[stage], 0, 0, kb, wr1 / 64, pol_wgt);
+                    fill_parity[stage] = phase;
+                    filled_mask |= 1 << stage;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
                 }
-                ptx::mma_commit(&c.empty[stage]);
-                ptx::mma_commit(&c.pfull[pb]);
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                if (++pb == NUM_PART) {
-                    pb = 0;
-                    pph ^= 1u;
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ---------------- MMA issuer: one partial product per K block, two buffers ----------------
+            constexpr uint32_t idesc_normal = ptx::idesc_e4m3_f32(BM, PART_COLS, 0, 0);
+            uint32_t stage = 0, phase = 0, pb = 0, pph = 0;
+            bool aborted = false;
+            for (int i = blockIdx.x; i < total && !aborted; i += gridDim.x) {
+                const Item it = decode_item(c, E, ksplit, swap_max, i);
+                const uint32_t ntok = (static_cast<uint32_t>(it.rows) + 15u) & ~15u;
+                const uint32_t idesc_swap = ptx::idesc_e4m3_f32(BM, ntok, 0, 0);
+                const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!ptx::mbar_wait(&c.full[stage], phase, abort_flag) ||
+                        !ptx::mbar_wait(&c.pempty[pb], pph ^ 1u, abort_flag)) {
+                        raise_abort(c, status);
+                        aborted = true;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + pb * PART_COLS;
+                    const uint32_t sa = ptx::smem_u32(tiles + stage * STAGE_BYTES);
+    #pragma unroll
+                    for (int kk = 0; kk < BKE / 32; ++kk) {
+                        const uint32_t accum = kk != 0 ? 1u : 0u;  // a fresh partial per K block
+                        const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+                        if (it.swap) {
+                            // Each weight group (K-major, 128 rows) as A, the tokens (K-major) as B.
+                            const uint64_t tok = ptx::smem_desc_sw128(sa, 16, 1024);
+                            const uint64_t w0 = ptx::smem_desc_sw128(sa + W_OFF, 16, 1024);
+                            const uint64_t w1 = ptx::smem_desc_sw128(sa + W_OFF + WBOX128, 16, 1024);
+                            ptx::mma_f8_ss(d_tmem, w0 + off, tok + off, idesc_swap, accum);
+                            ptx::mma_f8_ss(d_tmem + 64, w1 + off, tok + off, idesc_swap, accum);
+                        } else {
+                            // The activations as A, both weight groups as one 256-row B.
+                            const uint64_t a = ptx::smem_desc_sw128(sa, 16, 1024);
+                            const uint64_t b = ptx::smem_desc_sw128(sa + W_OFF, 16, 1024);
+                            ptx::mma_f8_ss(d_tmem, a + off, b + off, idesc_normal, accum);
+                        }
+                    }
+                    ptx::mma_commit(&c.empty[stage]);
+                    ptx::mma_commit(&c.pfull[pb]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    if (++pb == NUM_PART) {
+                        pb = 0;
+                        pph ^= 1u;
+                    }
                 }
             }
         }
-    } else if (warp >= 2) {
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_PROMO));
         // ---------------- promotion + epilogue: per-block scales into fp32 registers ----------------
-        // Warp w: tensor-memory lane quarter (w & 3), half hh = (w - 2) >> 2 of the 128 partial
-        // columns, as two 32-column groups c0, c1:
-        //   normal kind 0: gate [32hh, +32) and up [64 + 32hh, +32) — the same 32 h columns;
-        //   normal kind 1: [64hh, +32) and [64hh + 32, +32);
-        //   swapped: tokens [32hh, +32) of the two MMAs, [32hh, +32) and [64 + 32hh, +32).
-        const int quarter = warp & 3, hh = (warp - 2) >> 2;
+        // Warp w: tensor-memory lane quarter (w & 3), half hh = (w - 4) >> 2 of the buffer's columns.
+        // acc[] holds 128 fp32 sums:
+        //   normal kind 0: gate columns [64hh, +64) in acc[0..63], up [128 + 64hh, +64) in
+        //                  acc[64..127] (the same 64 h columns);
+        //   normal kind 1: columns [128hh, +128);
+        //   swapped: tokens [32hh, +32) of the two MMAs, columns [32hh, +32) and [64 + 32hh, +32), in
+        //            acc[0..31] and acc[32..63].
+        // A K block's columns come in rounds of two 32-column loads (64 columns per wait: the
+        // tensor-memory load latency, not the FMAs, sets the pace of a round).
+        const int quarter = warp & 3, hh = (warp - 4) >> 2;
         const int r_local = quarter * 32 + lane;
         uint32_t pb = 0, pph = 0;
         bool aborted = false;
         for (int i = blockIdx.x; i < total && !aborted; i += gridDim.x) {
             const Item it = decode_item(c, E, ksplit, swap_max, i);
-            const int n0 = it.n_tile * (it.swap ? 2 * BN : BN);
+            const int n0 = it.n_tile * BN;
             const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
-            const bool normal1 = KIND == 1 && !it.swap;
-            const uint32_t c0 = normal1 ? 64 * hh : 32 * hh, c1 = normal1 ? 64 * hh + 32 : 64 + 32 * hh;
-            // Weight scale blocks of the two groups (a group past N is computed, never stored).
+            // Weight scale blocks of the loaded columns (a block past N is computed, never stored).
             int wb0, wb1;
             if (KIND == 0) {
                 wb0 = n0 / 128;
                 wb1 = (N + n0) / 128;
-            } else {
+            } else if (it.swap) {
                 wb0 = n0 / 128;
-                wb1 = it.swap ? min(nbw - 1, (n0 + 128) / 128) : wb0;
+                wb1 = min(nbw - 1, wb0 + 1);
+            } else {
+                wb0 = min(nbw - 1, (n0 + 128 * hh) / 128);
+                wb1 = wb0;
             }
             const float* sw0p = b_scale + (static_cast<size_t>(it.e) * nbw + wb0) * num_kb;
             const float* sw1p = b_scale + (static_cast<size_t>(it.e) * nbw + wb1) * num_kb;
@@ -337,14 +351,11 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             // The row / token scale this lane loads: its row (normal) or token 32hh + lane (swapped).
             const int tok = 32 * hh + lane;
             const bool sc_ok = it.swap ? tok < it.rows : row_ok;
-            const float* srp = a_scale + (it.swap ? static_cast<size_t>(it.row0 + (sc_ok ? tok : 0)) : (sc_ok ? grow : 0)) *
-                                             num_kb;
-            float A0[32], A1[32];
+            const float* srp =
+                a_scale + (it.swap ? static_cast<size_t>(it.row0 + (sc_ok ? tok : 0)) : (sc_ok ? grow : 0)) * num_kb;
+            float acc[128];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                A0[j] = 0.0f;
-                A1[j] = 0.0f;
-            }
+            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
             // Scales of K blocks kb (s*), kb + 1 (n*) and kb + 2 (m*): each is loaded two blocks
             // ahead of its use, so the load's latency hides behind two partial products.
             auto ld_sc = [&](int b, float& w0, float& w1, float& r) {
@@ -368,22 +379,33 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 if (active) {
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + pb * PART_COLS;
                     uint32_t v0[32], v1[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + c0, v0);
-                    ptx::tmem_ld_32x32b_x32(taddr + c1, v1);
-                    ptx::tmem_ld_wait();
-                    if (!it.swap) {
-                        const float s0 = sr * sw0, s1 = sr * sw1;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            A0[j] = fmaf(__uint_as_float(v0[j]), s0, A0[j]);
-                            A1[j] = fmaf(__uint_as_float(v1[j]), s1, A1[j]);
-                        }
-                    } else {
+                    if (it.swap) {
+                        ptx::tmem_ld_32x32b_x32(taddr + 32 * hh, v0);
+                        ptx::tmem_ld_32x32b_x32(taddr + 64 + 32 * hh, v1);
+                        ptx::tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {  // column j is token 32hh + j: lane j's scale
                             const float sj = __shfl_sync(0xffffffffu, sr, j);
-                            A0[j] = fmaf(__uint_as_float(v0[j]), sj * sw0, A0[j]);
-                            A1[j] = fmaf(__uint_as_float(v1[j]), sj * sw1, A1[j]);
+                            acc[j] = fmaf(__uint_as_float(v0[j]), sj * sw0, acc[j]);
+                            acc[32 + j] = fmaf(__uint_as_float(v1[j]), sj * sw1, acc[32 + j]);
+                        }
+                    } else {
+                        const float s0 = sr * sw0, s1 = sr * sw1;
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            // kind 0: gate and up columns 32q.. of this warp's 64 -> acc[32q..],
+                            // acc[64 + 32q..]; kind 1: columns 64q.. and 64q + 32.. of its 128.
+                            const uint32_t ca = KIND == 0 ? 64 * hh + 32 * q : 128 * hh + 64 * q;
+                            const uint32_t cb = KIND == 0 ? 128 + 64 * hh + 32 * q : 128 * hh + 64 * q + 32;
+                            ptx::tmem_ld_32x32b_x32(taddr + ca, v0);
+                            ptx::tmem_ld_32x32b_x32(taddr + cb, v1);
+                            ptx::tmem_ld_wait();
+                            const int oa = KIND == 0 ? 32 * q : 64 * q, ob = KIND == 0 ? 64 + 32 * q : 64 * q + 32;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                acc[oa + j] = fmaf(__uint_as_float(v0[j]), s0, acc[oa + j]);
+                                acc[ob + j] = fmaf(__uint_as_float(v1[j]), s1, acc[ob + j]);
+                            }
                         }
                     }
                 }
@@ -406,24 +428,23 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             if (!it.swap) {
                 if (!row_ok) continue;
                 if (KIND == 0) {
-                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + grow * N + n0 + 32 * hh);
+                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + grow * N + n0 + 64 * hh);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
+                    for (int v = 0; v < 8; ++v) {
                         uint32_t p[4];
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            p[q] = pack_bf16x2(silu_mul(A0[8 * v + 2 * q], A1[8 * v + 2 * q]),
-                                               silu_mul(A0[8 * v + 2 * q + 1], A1[8 * v + 2 * q + 1]));
+                            p[q] = pack_bf16x2(silu_mul(acc[8 * v + 2 * q], acc[64 + 8 * v + 2 * q]),
+                                               silu_mul(acc[8 * v + 2 * q + 1], acc[64 + 8 * v + 2 * q + 1]));
                         dst[v] = make_uint4(p[0], p[1], p[2], p[3]);
                     }
                 } else {
+                    if (n0 + 128 * hh >= N) continue;  // the half of a last, 128-column tile past N
                     float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) +
-                                                            static_cast<size_t>(it.kslice) * M * N + grow * N + n0 + 64 * hh);
+                                                            static_cast<size_t>(it.kslice) * M * N + grow * N + n0 + 128 * hh);
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        dst[v] = make_float4(A0[4 * v], A0[4 * v + 1], A0[4 * v + 2], A0[4 * v + 3]);
-                        dst[8 + v] = make_float4(A1[4 * v], A1[4 * v + 1], A1[4 * v + 2], A1[4 * v + 3]);
-                    }
+                    for (int v = 0; v < 32; ++v)
+                        dst[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
                 }
             } else {
                 // Lane = weight column n0 + r_local (kind 1: and n0 + 128 + r_local), column j = token.
@@ -434,11 +455,11 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     if (t < it.rows) {
                         const size_t rr = static_cast<size_t>(it.row0 + t);
                         if (KIND == 0) {
-                            reinterpret_cast<uint16_t*>(out)[rr * N + col0] = bf16_bits(silu_mul(A0[j], A1[j]));
+                            reinterpret_cast<uint16_t*>(out)[rr * N + col0] = bf16_bits(silu_mul(acc[j], acc[32 + j]));
                         } else {
                             float* y = reinterpret_cast<float*>(out) + static_cast<size_t>(it.kslice) * M * N;
-                            if (col0 < N) y[rr * N + col0] = A0[j];
-                            if (col0 + 128 < N) y[rr * N + col0 + 128] = A1[j];
+                            if (col0 < N) y[rr * N + col0] = acc[j];
+                            if (col0 + 128 < N) y[rr * N + col0 + 128] = acc[32 + j];
                         }
                     }
                 }
@@ -476,17 +497,23 @@ cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const ch
         }
         attr_set[dev] = true;
     }
-    CUtensorMap mA, mA32, mB128, mB64;
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8b_kernel<KIND>) != cudaSuccess ||
+        fa.numRegs * NUM_THREADS < REGS_CTL * 128 + REGS_PROMO * 32 * EPI_WARPS) {
+        *why = "blockwise FP8 GEMM: the kernel was compiled with fewer registers than its setmaxnreg split needs";
+        return cudaErrorInvalidValue;
+    }
+    CUtensorMap mA, mA32, mB128;
     const uint64_t wrows = static_cast<uint64_t>(a.E) * (KIND == 0 ? 2ull * a.N : static_cast<uint64_t>(a.N));
     if (!make_tensor_map_u8(&mA, a.A, a.K, a.M, BM) || !make_tensor_map_u8(&mA32, a.A, a.K, a.M, TOK_BOX_ROWS) ||
-        !make_tensor_map_w8(&mB128, a.B, a.K, wrows, 128) || !make_tensor_map_w8(&mB64, a.B, a.K, wrows, 64)) {
+        !make_tensor_map_w8(&mB128, a.B, a.K, wrows, 128)) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or bad operand)";
         return cudaErrorInvalidValue;
     }
     const int swap_max = a.swap_max < 0 ? 0 : (a.swap_max > SWAP_MAX_ROWS ? SWAP_MAX_ROWS : a.swap_max);
     const int ksplit = KIND == 0 ? 1 : a.ksplit;
     return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_fp8b_kernel<KIND>, dim3(num_sms),
-                    dim3(NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB128, mB64, a.offsets, a.M, a.K, a.N, a.E, ksplit,
+                    dim3(NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB128, a.offsets, a.M, a.K, a.N, a.E, ksplit,
                     swap_max, a.a_scale, a.b_scale, a.out, a.status);
 }
 
