@@ -216,7 +216,7 @@ def test_forward_fp8b_launch_count(moe):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["mixtral_t32", "mixtral_t512", "deepseek_t2048"])
+@pytest.mark.parametrize("name", ["mixtral_t32", "mixtral_t512", "mixtral_t4096", "deepseek_t2048"])
 def test_forward_fp8b_full_size(moe, oracle, name):
     """The blockwise FP8 layer at full size in the configuration bench.py times: weight codes and
     block scales bit for bit, routing and x codes bit for bit, sampled tokens against the oracle."""
