@@ -73,7 +73,7 @@ AUTO_TIMED_S = 0.5
 AUTO_STEPS_MIN, AUTO_STEPS_MAX = 50, 4000
 
 _TRAFFIC_HASH = "a8d3a7a96e328c09"  # GEMM source hash the captures below were taken at
-_TRAFFIC_HASH_FP8B = "5f6734ae94ec4ddf"  # ... and that of the blockwise FP8 kernel's sources
+_TRAFFIC_HASH_FP8B = "55d0627b99641536"  # ... and that of the blockwise FP8 kernel's sources
 MEASURED_TRAFFIC = {
     ("deepseek_e32_t256", "gateup_swiglu"): (1919914752, _TRAFFIC_HASH),
     ("deepseek_e32_t256", "down"): (1008838144, _TRAFFIC_HASH),
@@ -95,24 +95,26 @@ MEASURED_TRAFFIC = {
     ("mixtral_t512", "down_fp8"): (498120704, _TRAFFIC_HASH),
     ("mixtral_t512_skew40", "gateup_swiglu_fp8"): (971906304, _TRAFFIC_HASH),
     ("mixtral_t512_skew40", "down_fp8"): (498307328, _TRAFFIC_HASH),
-    ("deepseek_e32_t256", "gateup_swiglu_fp8b"): (966419200, _TRAFFIC_HASH_FP8B),
-    ("deepseek_e32_t256", "down_fp8b"): (533735168, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t32", "gateup_swiglu_fp8b"): (944920576, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t32", "down_fp8b"): (474286336, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t4096", "gateup_swiglu_fp8b"): (1199317760, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t4096", "down_fp8b"): (728835072, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512", "gateup_swiglu_fp8b"): (1312394240, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512", "down_fp8b"): (614131200, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512_skew40", "gateup_swiglu_fp8b"): (973773824, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512_skew40", "down_fp8b"): (515848704, _TRAFFIC_HASH_FP8B),
     ("deepseek_t2048", "gateup_swiglu"): (8108204800, _TRAFFIC_HASH),
     ("deepseek_t2048", "down"): (4196736768, _TRAFFIC_HASH),
     ("deepseek_v3_t2048", "gateup_swiglu"): (4711750656, _TRAFFIC_HASH),
     ("deepseek_v3_t2048", "down"): (2483243008, _TRAFFIC_HASH),
     ("deepseek_t2048", "gateup_swiglu_fp8"): (3892582656, _TRAFFIC_HASH),
     ("deepseek_t2048", "down_fp8"): (2288754688, _TRAFFIC_HASH),
-    ("deepseek_t2048", "gateup_swiglu_fp8b"): (3759550976, _TRAFFIC_HASH_FP8B),
-    ("deepseek_t2048", "down_fp8b"): (2315701504, _TRAFFIC_HASH_FP8B),
+    ("deepseek_e32_t256", "gateup_swiglu_fp8b"): (966384640, _TRAFFIC_HASH_FP8B),
+    ("deepseek_e32_t256", "down_fp8b"): (534975488, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t32", "gateup_swiglu_fp8b"): (944954880, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t32", "down_fp8b"): (474785536, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t4096", "gateup_swiglu_fp8b"): (1197870080, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t4096", "down_fp8b"): (780931072, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512", "gateup_swiglu_fp8b"): (1358057216, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512", "down_fp8b"): (616780288, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512_skew40", "gateup_swiglu_fp8b"): (973863680, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512_skew40", "down_fp8b"): (513936896, _TRAFFIC_HASH_FP8B),
+    ("deepseek_t2048", "gateup_swiglu_fp8b"): (3789366016, _TRAFFIC_HASH_FP8B),
+    ("deepseek_t2048", "down_fp8b"): (2342260224, _TRAFFIC_HASH_FP8B),
+    ("deepseek_v3_t2048", "gateup_swiglu_fp8b"): (2074135296, _TRAFFIC_HASH_FP8B),
+    ("deepseek_v3_t2048", "down_fp8b"): (1408561920, _TRAFFIC_HASH_FP8B),
 }
 GEMM_SOURCES = ("mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm.cu",
                 "mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm_2sm.cu",
