@@ -14,8 +14,10 @@ ours (default):
   roofline     the dominant kernel: its algorithmic bytes (or FLOPs) per launch / its mean duration,
                from a second K-step loop that calls the five stage entry points with events between
                them (the same kernels moe_forward launches).
-  e2e          tokens/s through moe_forward_host: x and logits copied from page-locked host memory,
-               the layer, out copied back — all inside the timed region.
+  e2e          tokens/s with x and logits copied from page-locked host memory, the layer and out
+               copied back, every step, all inside the timed region: through moe_forward_host_batches
+               (bf16, softmax router: the K steps as K batches, copies overlapped with the layers on
+               two copy streams), else the binding's copies and layer per step on one stream.
   cpu_baseline the CPU oracle on a bounded sample of the same workload (rank 0, N=1 only).
 reference:
   the CPU oracle as the reference arm: each step is the oracle's forward on a bounded token
@@ -430,33 +432,59 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
                 for j, name in enumerate(stages)}
     staged_step_ms = statistics.mean(sev[i][0].elapsed_time(sev[i][ns]) for i in range(args.steps))
 
-    # ---- e2e through moe_forward_host ---------------------------------------------------------
-    # (grouped router: the same host->device copies, moe_forward_grouped and the copy back, each
-    # enqueued on the stream by the binding)
+    # ---- e2e: host buffers in, layer, host buffer out, every step ---------------------------------
+    # bf16 softmax router: one moe_forward_host_batches call over the K steps (each step's x and
+    # logits copied in and its out copied back, on two copy streams beside the layers).  Grouped
+    # router and FP8: per step, the host->device copies, the layer and the copy back, each
+    # enqueued on the stream by the binding.
     xh, lh = x.pin_memory(), logits.pin_memory()
     oh = torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory()
+    batched = not (grouped or fp8) and flush is None
+    if batched:
+        ohs = [oh, torch.empty_like(oh).pin_memory()]
+        ws_b = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k) + 2 * moe.host_staging_size(w.T, w.d, w.E),
+                           dtype=torch.uint8, device=dev)
+        h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
-    def e2e_step():
-        if grouped or fp8:
-            x_d.copy_(xh, non_blocking=True)
-            l_d.copy_(lh, non_blocking=True)
-            step()
-            oh.copy_(out, non_blocking=True)
-        else:
-            moe.forward_host(xh, lh, wgu, wd, w.k, oh, ws)
+        def e2e_run(n):
+            moe.forward_host_batches([xh] * n, [lh] * n, wgu, wd, w.k, [ohs[i & 1] for i in range(n)], ws_b,
+                                     stream, h2d, d2h)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps):
-        if flush is not None:
-            flush.zero_()
-        eev[i][0].record(stream)
-        e2e_step()
-        eev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
+        e2e_run(max(1, args.warmup))
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_run(args.steps)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        e2e_api = "moe_forward_host_batches: K batches, copies on two copy streams beside the layers"
+        if moe.get_device_error(ws_b) != 0:
+            raise RuntimeError("device status word set during the e2e run")
+    else:
+        def e2e_step():
+            if grouped or fp8:
+                x_d.copy_(xh, non_blocking=True)
+                l_d.copy_(lh, non_blocking=True)
+                step()
+                oh.copy_(out, non_blocking=True)
+            else:
+                moe.forward_host(xh, lh, wgu, wd, w.k, oh, ws)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            eev[i][0].record(stream)
+            e2e_step()
+            eev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
+        e2e_api = ("per step on one stream: host-to-device copies, the layer, the copy back" if (grouped or fp8)
+                   else "moe_forward_host, one call per step")
     if moe.get_device_error(ws) != 0:
         raise RuntimeError("device status word set during the timed region")
 
@@ -492,7 +520,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
 
     return {
         "ms": ms_max, "tokens_per_rank": w.T, "t_wall": t_wall, "clocks": clocks, "stage_ms": stage_ms,
-        "staged_step_ms": staged_step_ms, "e2e_ms": e2e_ms, "roofline": roof, "layer": lw,
+        "staged_step_ms": staged_step_ms, "e2e_ms": e2e_ms, "e2e_api": e2e_api, "roofline": roof, "layer": lw,
         "layer_roof_ms": layer_roof_ms, "n_active": n_active, "max_load": int(counts.max()),
         "host_weights": (wgu, wd), "inputs": (logits, x), "step_ms_p10_p90": (
             float(np.percentile(step_ms, 10)), float(np.percentile(step_ms, 90))),
@@ -668,7 +696,7 @@ def main():
             "active_experts": r["n_active"], "max_expert_load": r["max_load"], "down_ksplit": r["ksplit"],
             "e2e": {"value": round(w.T / (r["e2e_ms"] * 1e-3), 2), "unit": "tokens/s",
                     "h2d_bytes_per_step": w.T * w.d * 2 + w.T * w.E * 4, "d2h_bytes_per_step": w.T * w.d * 2,
-                    "ms_per_step": round(r["e2e_ms"], 4)},
+                    "ms_per_step": round(r["e2e_ms"], 4), "api": r["e2e_api"]},
             "gpu_launches": r["launches_per_step"] * args.steps,
             "clocks": r["clocks"],
         }

@@ -224,6 +224,25 @@ MOE_API int moe_forward_host(const void* x_host, const float* logits_host, const
                      const void* w_down, int T, int d, int f, int E, int top_k, void* out_host,
                      void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* moe_forward_host over n_batches batches of T tokens each, with the copies overlapped with the
+ * layers: batch i's x [T,d] bf16 and logits [T,E] fp32 are read from x_hosts[i] and
+ * logits_hosts[i] and its out [T,d] bf16 is written to out_hosts[i] (page-locked host memory, or
+ * the copies do not overlap).  The layers run one after another on `stream`; the host-to-device
+ * copies are issued on h2d_stream and the device-to-host copies on d2h_stream (two streams other
+ * than `stream`, so that both copy directions run beside the layers), ordered by events: batch
+ * i+1's inputs and batch i-1's output move while batch i computes.  Inputs and outputs are staged
+ * in two slots after the layer's workspace: workspace_bytes >= moe_workspace_size() +
+ * 2 * moe_host_staging_size().  All work is ordered after what `stream` already holds, and
+ * `stream` completes only after the last copy back: synchronise `stream` before reading
+ * out_hosts.  The call creates seven CUDA events and releases them before returning (the driver
+ * frees them once the recorded work completes); it allocates no device memory.  Errors as
+ * moe_forward_host; n_batches = 0 does nothing. */
+MOE_API int moe_forward_host_batches(const void* const* x_hosts, const float* const* logits_hosts,
+                                     const void* w_gate_up, const void* w_down, int n_batches, int T, int d, int f,
+                                     int E, int top_k, void* const* out_hosts, void* workspace,
+                                     size_t workspace_bytes, moe_stream_t stream, moe_stream_t h2d_stream,
+                                     moe_stream_t d2h_stream);
+
 /* Size of the fixed scratch array that moe_forward_noalloc uses (64 MiB). */
 #define MOE_NOALLOC_SCRATCH_BYTES (64ull * 1024ull * 1024ull)
 

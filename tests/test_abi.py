@@ -106,6 +106,22 @@ def test_forward_rejects_null_and_small_workspace(lib):
                            None) == -1
 
 
+def test_forward_host_batches_validates(lib):
+    p = ctypes.c_void_p(1 << 20)
+    arr = (ctypes.c_void_p * 2)(1 << 20, 1 << 21)
+    nul = (ctypes.c_void_p * 2)(1 << 20, None)
+    f = lib.moe_forward_host_batches
+    assert f(arr, arr, p, p, 0, 4, 64, 128, 8, 2, arr, p, 1 << 40, None, None, None) == 0   # no batches
+    assert f(arr, arr, p, p, 2, 0, 64, 128, 8, 2, arr, p, 1 << 40, None, None, None) == 0   # T = 0
+    assert f(arr, arr, p, p, -1, 4, 64, 128, 8, 2, arr, p, 1 << 40, None, None, None) == -1
+    assert f(None, arr, p, p, 2, 4, 64, 128, 8, 2, arr, p, 1 << 40, None, None, None) == -1
+    assert f(arr, nul, p, p, 2, 4, 64, 128, 8, 2, arr, p, 1 << 40, None, None, None) == -1
+    assert "batch 1" in _err(lib)
+    need = lib.moe_workspace_size(4, 64, 128, 8, 2) + 2 * lib.moe_host_staging_size(4, 64, 8)
+    assert f(arr, arr, p, p, 2, 4, 64, 128, 8, 2, arr, p, need - 1, None, None, None) == -3
+    assert f(arr, arr, p, p, 2, 4, 64, 100, 8, 2, arr, p, 1 << 40, None, None, None) == -1   # f % 64
+
+
 def test_stage_calls_reject_bad_arguments(lib):
     p = ctypes.c_void_p(1 << 20)
     assert lib.moe_route(None, 4, 8, 2, p, p, None) == -1

@@ -345,6 +345,29 @@ def test_forward_host_matches_forward(moe):
     assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))
 
 
+@pytest.mark.parametrize("n", [1, 2, 5])
+def test_forward_host_batches_matches_forward(moe, n):
+    """Batches with copies overlapped on two copy streams give each batch's moe_forward output."""
+    w = Workload("host_batches", 97, 256, 512, 8, 2)
+    dev = torch.device(DEV)
+    _, _, wgu, wd = case_inputs(w, seed=11)
+    wgu_d, wd_d = wgu.to(dev), wd.to(dev)
+    xs, ls, refs = [], [], []
+    for i in range(n):
+        logits, x, _, _ = case_inputs(w, seed=20 + i)
+        xs.append(x.pin_memory())
+        ls.append(logits.pin_memory())
+        refs.append(moe.forward(x.to(dev), logits.to(dev), wgu_d, wd_d, w.k).cpu())
+    outs = [torch.full((w.T, w.d), -1.0, dtype=torch.bfloat16).pin_memory() for _ in range(n)]
+    ws = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k) + 2 * moe.host_staging_size(w.T, w.d, w.E),
+                     dtype=torch.uint8, device=dev)
+    moe.forward_host_batches(xs, ls, wgu_d, wd_d, w.k, outs, ws)
+    torch.cuda.current_stream().synchronize()  # the call orders its copies before the stream's end
+    assert moe.get_device_error(ws) == 0
+    for i in range(n):
+        assert torch.equal(outs[i].view(torch.int16), refs[i].view(torch.int16)), f"batch {i}"
+
+
 def _cudart():
     import ctypes
     import glob
