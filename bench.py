@@ -16,8 +16,9 @@ ours (default):
                them (the same kernels moe_forward launches).
   e2e          tokens/s with x and logits copied from page-locked host memory, the layer and out
                copied back, every step, all inside the timed region: through moe_forward_host_batches
-               (bf16, softmax router: the K steps as K batches, copies overlapped with the layers on
-               two copy streams), else the binding's copies and layer per step on one stream.
+               or its FP8 forms (softmax router: the K steps as K batches, copies overlapped with the
+               layers on two copy streams), else (DeepSeek-V3's router, or --flush-l2) the binding's
+               copies and layer per step on one stream.
   cpu_baseline the CPU oracle on a bounded sample of the same workload (rank 0, N=1 only).
 reference:
   the CPU oracle as the reference arm: each step is the oracle's forward on a bounded token
@@ -439,16 +440,21 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     # enqueued on the stream by the binding.
     xh, lh = x.pin_memory(), logits.pin_memory()
     oh = torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory()
-    batched = not (grouped or fp8) and flush is None
+    batched = not grouped and flush is None
     if batched:
         ohs = [oh, torch.empty_like(oh).pin_memory()]
-        ws_b = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k) + 2 * moe.host_staging_size(w.T, w.d, w.E),
+        wsize = moe.workspace_size_fp8b if blocks else moe.workspace_size_fp8 if fp8 else moe.workspace_size
+        ws_b = torch.empty(wsize(w.T, w.d, w.f, w.E, w.k) + 2 * moe.host_staging_size(w.T, w.d, w.E),
                            dtype=torch.uint8, device=dev)
         h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
         def e2e_run(n):
-            moe.forward_host_batches([xh] * n, [lh] * n, wgu, wd, w.k, [ohs[i & 1] for i in range(n)], ws_b,
-                                     stream, h2d, d2h)
+            outs = [ohs[i & 1] for i in range(n)]
+            if fp8:
+                fwd = moe.forward_fp8b_host_batches if blocks else moe.forward_fp8_host_batches
+                fwd([xh] * n, [lh] * n, *w8, w.k, outs, ws_b, stream, h2d, d2h)
+            else:
+                moe.forward_host_batches([xh] * n, [lh] * n, wgu, wd, w.k, outs, ws_b, stream, h2d, d2h)
 
         e2e_run(max(1, args.warmup))
         torch.cuda.synchronize(dev)
@@ -458,7 +464,8 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / args.steps
-        e2e_api = "moe_forward_host_batches: K batches, copies on two copy streams beside the layers"
+        e2e_api = ("moe_forward_" + ("fp8b_" if blocks else "fp8_" if fp8 else "") +
+                   "host_batches: K batches, copies on two copy streams beside the layers")
         if moe.get_device_error(ws_b) != 0:
             raise RuntimeError("device status word set during the e2e run")
     else:

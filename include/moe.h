@@ -392,6 +392,20 @@ MOE_API int moe_forward_fp8b(const void* x, const float* logits, const void* w8_
                              const void* w8_down, const float* s_down, int T, int d, int f, int E, int top_k,
                              void* out, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* moe_forward_host_batches with moe_forward_fp8 / moe_forward_fp8b as the layer: the same
+ * overlapped copies over two staging slots, weights as those calls take them; workspace_bytes >=
+ * moe_workspace_size_fp8() (resp. moe_workspace_size_fp8b()) + 2 * moe_host_staging_size(). */
+MOE_API int moe_forward_fp8_host_batches(const void* const* x_hosts, const float* const* logits_hosts,
+                                         const void* w8_gate_up, const float* s_gate_up, const void* w8_down,
+                                         const float* s_down, int n_batches, int T, int d, int f, int E, int top_k,
+                                         void* const* out_hosts, void* workspace, size_t workspace_bytes,
+                                         moe_stream_t stream, moe_stream_t h2d_stream, moe_stream_t d2h_stream);
+MOE_API int moe_forward_fp8b_host_batches(const void* const* x_hosts, const float* const* logits_hosts,
+                                          const void* w8_gate_up, const float* s_gate_up, const void* w8_down,
+                                          const float* s_down, int n_batches, int T, int d, int f, int E, int top_k,
+                                          void* const* out_hosts, void* workspace, size_t workspace_bytes,
+                                          moe_stream_t stream, moe_stream_t h2d_stream, moe_stream_t d2h_stream);
+
 /* The FP8 layers with DeepSeek-V3's router (moe_route_grouped) as step 1: bias [E] fp32, n_group,
  * topk_group and scale as for moe_route_grouped; everything else as for moe_forward_fp8 /
  * moe_forward_fp8b, with the same workspaces.  6 launches (per-row / per-channel scales) or 7

@@ -472,6 +472,82 @@ int noalloc_scratch(int dev, void** out) {
 
 using namespace moe;
 
+// Null checks of the *_host_batches calls' per-batch host pointers.
+static int check_host_batches(const char* name, const void* const* x_hosts, const float* const* logits_hosts,
+                              void* const* out_hosts, int n_batches) {
+    if (!x_hosts || !logits_hosts || !out_hosts) return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
+    for (int b = 0; b < n_batches; ++b)
+        if (!x_hosts[b] || !logits_hosts[b] || !out_hosts[b])
+            return fail(MOE_ERR_INVALID_ARG, "%s: null host pointer for batch %d", name, b);
+    return MOE_OK;
+}
+
+// The copy/compute pipeline of the *_host_batches calls (arguments already checked): two staging
+// slots (x, out, logits, as moe_forward_host lays them out) after the layer's `need` bytes of
+// workspace; batch b's inputs go to slot b & 1 on `si` once the layer of batch b-2 has read it,
+// its layer runs on `s` (run(x_dev, logits_dev, out_dev)) once they have landed and batch b-2's
+// output has left the slot, and its output goes back on `so`.
+template <typename Run>
+static int run_host_batches(const char* name, const void* const* x_hosts, const float* const* logits_hosts,
+                            void* const* out_hosts, int n_batches, int T, int d, int E, size_t need, void* workspace,
+                            cudaStream_t s, cudaStream_t si, cudaStream_t so, Run run) {
+    const size_t stage = moe_host_staging_size(T, d, E);
+    const size_t xb = static_cast<size_t>(T) * d * 2, lb = static_cast<size_t>(T) * E * 4;
+    void* x_dev[2];
+    void* out_dev[2];
+    float* logits_dev[2];
+    for (int k = 0; k < 2; ++k) {
+        const size_t base = need + k * stage;
+        x_dev[k] = at<char>(workspace, base);
+        out_dev[k] = at<char>(workspace, base + align256(xb));
+        logits_dev[k] = at<float>(workspace, base + 2 * align256(xb));
+    }
+    // Events: start (prior work on `s`), and per slot: inputs landed, layer done, output read.
+    cudaEvent_t ev[7] = {};
+    cudaError_t e = cudaSuccess;
+    for (int k = 0; k < 7 && e == cudaSuccess; ++k) e = cudaEventCreateWithFlags(&ev[k], cudaEventDisableTiming);
+    cudaEvent_t start = ev[0], in_ready[2] = {ev[1], ev[2]}, layer_done[2] = {ev[3], ev[4]},
+                out_done[2] = {ev[5], ev[6]};
+    auto cleanup = [&]() {
+        for (int k = 0; k < 7; ++k)
+            if (ev[k]) cudaEventDestroy(ev[k]);  // released once the recorded work completes
+    };
+    if (e != cudaSuccess) {
+        cleanup();
+        return fail(MOE_ERR_CUDA, "%s: event creation: %s", name, cudaGetErrorString(e));
+    }
+    // Everything below is ordered after the work already enqueued on `s` (which may still be
+    // using the staging slots or the layer's workspace).
+    if ((e = cudaEventRecord(start, s)) != cudaSuccess || (e = cudaStreamWaitEvent(si, start, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(so, start, 0)) != cudaSuccess) {
+        cleanup();
+        return fail(MOE_ERR_CUDA, "%s: stream ordering: %s", name, cudaGetErrorString(e));
+    }
+    int rc = MOE_OK;
+    for (int b = 0; b < n_batches && e == cudaSuccess && rc == MOE_OK; ++b) {
+        const int k = b & 1;
+        if (b >= 2 && (e = cudaStreamWaitEvent(si, layer_done[k], 0)) != cudaSuccess) break;
+        if ((e = cudaMemcpyAsync(x_dev[k], x_hosts[b], xb, cudaMemcpyHostToDevice, si)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(logits_dev[k], logits_hosts[b], lb, cudaMemcpyHostToDevice, si)) != cudaSuccess ||
+            (e = cudaEventRecord(in_ready[k], si)) != cudaSuccess)
+            break;
+        if ((e = cudaStreamWaitEvent(s, in_ready[k], 0)) != cudaSuccess) break;
+        if (b >= 2 && (e = cudaStreamWaitEvent(s, out_done[k], 0)) != cudaSuccess) break;
+        if ((rc = run(x_dev[k], logits_dev[k], out_dev[k])) != MOE_OK) break;
+        if ((e = cudaEventRecord(layer_done[k], s)) != cudaSuccess) break;
+        if ((e = cudaStreamWaitEvent(so, layer_done[k], 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(out_hosts[b], out_dev[k], xb, cudaMemcpyDeviceToHost, so)) != cudaSuccess ||
+            (e = cudaEventRecord(out_done[k], so)) != cudaSuccess)
+            break;
+    }
+    // `s` completes only after the last copy back (the copies on `so` run in order).
+    if (e == cudaSuccess && rc == MOE_OK) e = cudaStreamWaitEvent(s, out_done[(n_batches - 1) & 1], 0);
+    cleanup();
+    if (rc != MOE_OK) return rc;
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", name, cudaGetErrorString(e));
+    return ok();
+}
+
 extern "C" {
 
 int moe_version(void) { return 100; }
@@ -724,11 +800,8 @@ int moe_forward_host_batches(const void* const* x_hosts, const float* const* log
     if (rc) return rc;
     if (n_batches < 0) return fail(MOE_ERR_INVALID_ARG, "%s: n_batches = %d < 0", name, n_batches);
     if (T == 0 || n_batches == 0) return ok();
-    if (!x_hosts || !logits_hosts || !out_hosts || !w_gate_up || !w_down)
-        return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
-    for (int b = 0; b < n_batches; ++b)
-        if (!x_hosts[b] || !logits_hosts[b] || !out_hosts[b])
-            return fail(MOE_ERR_INVALID_ARG, "%s: null host pointer for batch %d", name, b);
+    if ((rc = check_host_batches(name, x_hosts, logits_hosts, out_hosts, n_batches))) return rc;
+    if (!w_gate_up || !w_down) return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
     const size_t need = layout(T, d, f, E, top_k).total;
     const size_t stage = moe_host_staging_size(T, d, E);
     if (!workspace || workspace_bytes < need + 2 * stage)
@@ -740,66 +813,11 @@ int moe_forward_host_batches(const void* const* x_hosts, const float* const* log
     int sms;
     if ((rc = check_device(&sms))) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaStream_t si = static_cast<cudaStream_t>(h2d_stream), so = static_cast<cudaStream_t>(d2h_stream);
-    const size_t xb = static_cast<size_t>(T) * d * 2, lb = static_cast<size_t>(T) * E * 4;
-    // Per staging slot: x, out, logits (the layout moe_forward_host uses), two slots.
-    void* x_dev[2];
-    void* out_dev[2];
-    float* logits_dev[2];
-    for (int k = 0; k < 2; ++k) {
-        const size_t base = need + k * stage;
-        x_dev[k] = at<char>(workspace, base);
-        out_dev[k] = at<char>(workspace, base + align256(xb));
-        logits_dev[k] = at<float>(workspace, base + 2 * align256(xb));
-    }
-    // Events: start (prior work on `stream`), and per slot: inputs landed, layer done, output read.
-    cudaEvent_t ev[7] = {};
-    cudaError_t e = cudaSuccess;
-    for (int k = 0; k < 7 && e == cudaSuccess; ++k) e = cudaEventCreateWithFlags(&ev[k], cudaEventDisableTiming);
-    cudaEvent_t start = ev[0], in_ready[2] = {ev[1], ev[2]}, layer_done[2] = {ev[3], ev[4]},
-                out_done[2] = {ev[5], ev[6]};
-    auto cleanup = [&]() {
-        for (int k = 0; k < 7; ++k)
-            if (ev[k]) cudaEventDestroy(ev[k]);  // released once the recorded work completes
-    };
-    if (e != cudaSuccess) {
-        cleanup();
-        return fail(MOE_ERR_CUDA, "%s: event creation: %s", name, cudaGetErrorString(e));
-    }
-    // Everything below is ordered after the work already enqueued on `stream` (which may still be
-    // using the staging slots or the layer's workspace).
-    if ((e = cudaEventRecord(start, s)) != cudaSuccess || (e = cudaStreamWaitEvent(si, start, 0)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(so, start, 0)) != cudaSuccess) {
-        cleanup();
-        return fail(MOE_ERR_CUDA, "%s: stream ordering: %s", name, cudaGetErrorString(e));
-    }
-    for (int b = 0; b < n_batches && e == cudaSuccess && rc == MOE_OK; ++b) {
-        const int k = b & 1;
-        // Inputs of batch b into slot k once the layer of batch b-2 has read it.
-        if (b >= 2 && (e = cudaStreamWaitEvent(si, layer_done[k], 0)) != cudaSuccess) break;
-        if ((e = cudaMemcpyAsync(x_dev[k], x_hosts[b], xb, cudaMemcpyHostToDevice, si)) != cudaSuccess ||
-            (e = cudaMemcpyAsync(logits_dev[k], logits_hosts[b], lb, cudaMemcpyHostToDevice, si)) != cudaSuccess ||
-            (e = cudaEventRecord(in_ready[k], si)) != cudaSuccess)
-            break;
-        // The layer once they have landed and batch b-2's output has been copied out of slot k.
-        if ((e = cudaStreamWaitEvent(s, in_ready[k], 0)) != cudaSuccess) break;
-        if (b >= 2 && (e = cudaStreamWaitEvent(s, out_done[k], 0)) != cudaSuccess) break;
-        if ((rc = run_layer(x_dev[k], logits_dev[k], w_gate_up, w_down, T, d, f, E, top_k, out_dev[k], workspace, sms,
-                            s)) != MOE_OK)
-            break;
-        if ((e = cudaEventRecord(layer_done[k], s)) != cudaSuccess) break;
-        // The output back to the host.
-        if ((e = cudaStreamWaitEvent(so, layer_done[k], 0)) != cudaSuccess ||
-            (e = cudaMemcpyAsync(out_hosts[b], out_dev[k], xb, cudaMemcpyDeviceToHost, so)) != cudaSuccess ||
-            (e = cudaEventRecord(out_done[k], so)) != cudaSuccess)
-            break;
-    }
-    // `stream` completes only after the last copy back (the copies on d2h_stream run in order).
-    if (e == cudaSuccess && rc == MOE_OK) e = cudaStreamWaitEvent(s, out_done[(n_batches - 1) & 1], 0);
-    cleanup();
-    if (rc != MOE_OK) return rc;
-    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", name, cudaGetErrorString(e));
-    return ok();
+    return run_host_batches(name, x_hosts, logits_hosts, out_hosts, n_batches, T, d, E, need, workspace, s,
+                            static_cast<cudaStream_t>(h2d_stream), static_cast<cudaStream_t>(d2h_stream),
+                            [&](const void* x, const float* l, void* o) {
+                                return run_layer(x, l, w_gate_up, w_down, T, d, f, E, top_k, o, workspace, sms, s);
+                            });
 }
 
 int moe_forward_noalloc(const void* x, const float* logits, const void* w_gate_up, const void* w_down, int T,
@@ -986,6 +1004,56 @@ static int forward8_entry(const void* x, const float* logits, const void* w8_gat
     if ((rc = check_device(&sms))) return rc;
     return run_layer_fp8(x, logits, w8_gate_up, s_gate_up, w8_down, s_down, T, d, f, E, top_k, out, workspace, sms,
                          static_cast<cudaStream_t>(stream), blocks, router);
+}
+
+// The FP8 layers over host batches (moe_forward_host_batches with moe_forward_fp8[b] as the layer).
+static int forward8_host_batches(const void* const* x_hosts, const float* const* logits_hosts, const void* w8_gate_up,
+                                 const float* s_gate_up, const void* w8_down, const float* s_down, int n_batches, int T,
+                                 int d, int f, int E, int top_k, void* const* out_hosts, void* workspace,
+                                 size_t workspace_bytes, moe_stream_t stream, moe_stream_t h2d_stream,
+                                 moe_stream_t d2h_stream, bool blocks) {
+    const char* name = blocks ? "moe_forward_fp8b_host_batches" : "moe_forward_fp8_host_batches";
+    int rc = check_shape_fp8(T, d, f, E, top_k, name);
+    if (rc) return rc;
+    if (n_batches < 0) return fail(MOE_ERR_INVALID_ARG, "%s: n_batches = %d < 0", name, n_batches);
+    if (T == 0 || n_batches == 0) return ok();
+    if ((rc = check_host_batches(name, x_hosts, logits_hosts, out_hosts, n_batches))) return rc;
+    if (!w8_gate_up || !s_gate_up || !w8_down || !s_down) return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
+    if (!aligned16(w8_gate_up) || !aligned16(w8_down) || !aligned16(s_gate_up) || !aligned16(s_down))
+        return fail(MOE_ERR_INVALID_ARG, "%s: weights and weight scales must be 16-byte aligned", name);
+    const size_t need = layout_fp8(T, d, f, E, top_k, blocks).total;
+    const size_t stage = moe_host_staging_size(T, d, E);
+    if (!workspace || workspace_bytes < need + 2 * stage)
+        return fail(MOE_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", name, workspace_bytes, need + 2 * stage);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(MOE_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", name);
+    int sms;
+    if ((rc = check_device(&sms))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return run_host_batches(name, x_hosts, logits_hosts, out_hosts, n_batches, T, d, E, need, workspace, s,
+                            static_cast<cudaStream_t>(h2d_stream), static_cast<cudaStream_t>(d2h_stream),
+                            [&](const void* x, const float* l, void* o) {
+                                return run_layer_fp8(x, l, w8_gate_up, s_gate_up, w8_down, s_down, T, d, f, E, top_k,
+                                                     o, workspace, sms, s, blocks, Router());
+                            });
+}
+
+int moe_forward_fp8_host_batches(const void* const* x_hosts, const float* const* logits_hosts, const void* w8_gate_up,
+                                 const float* s_gate_up, const void* w8_down, const float* s_down, int n_batches, int T,
+                                 int d, int f, int E, int top_k, void* const* out_hosts, void* workspace,
+                                 size_t workspace_bytes, moe_stream_t stream, moe_stream_t h2d_stream,
+                                 moe_stream_t d2h_stream) {
+    return forward8_host_batches(x_hosts, logits_hosts, w8_gate_up, s_gate_up, w8_down, s_down, n_batches, T, d, f, E,
+                                 top_k, out_hosts, workspace, workspace_bytes, stream, h2d_stream, d2h_stream, false);
+}
+
+int moe_forward_fp8b_host_batches(const void* const* x_hosts, const float* const* logits_hosts,
+                                  const void* w8_gate_up, const float* s_gate_up, const void* w8_down,
+                                  const float* s_down, int n_batches, int T, int d, int f, int E, int top_k,
+                                  void* const* out_hosts, void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                                  moe_stream_t h2d_stream, moe_stream_t d2h_stream) {
+    return forward8_host_batches(x_hosts, logits_hosts, w8_gate_up, s_gate_up, w8_down, s_down, n_batches, T, d, f, E,
+                                 top_k, out_hosts, workspace, workspace_bytes, stream, h2d_stream, d2h_stream, true);
 }
 
 static Router grouped_router(const float* bias, int n_group, int topk_group, float scale) {

@@ -41,6 +41,8 @@ _SIGS = {
     "moe_forward": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "moe_forward_host": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "moe_forward_host_batches": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P, _P], _I),
+    "moe_forward_fp8_host_batches": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P, _P], _I),
+    "moe_forward_fp8b_host_batches": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P, _P], _I),
     "moe_get_device_error": ([_P, ctypes.POINTER(ctypes.c_int32)], _I),
     "moe_quantize_weights_fp8": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_permute_fp8": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
@@ -321,27 +323,60 @@ def forward_host_batches(x_hosts, logits_hosts, w_gate_up, w_down, top_k, out_ho
     layers: the layers run on ``stream``, the copies on ``h2d_stream`` / ``d2h_stream`` (created
     here when not given).  The workspace holds workspace_size() + 2 * host_staging_size() bytes.
     Synchronise ``stream`` before reading ``out_hosts``."""
+    if len(x_hosts) == 0:
+        return out_hosts
+    _dev(w_gate_up, torch.bfloat16, "w_gate_up")
+    _dev(w_down, torch.bfloat16, "w_down")
+    E, _, f2 = w_gate_up.shape
+    n, T, d, xa, la, oa, h2d, d2h = _host_batch_args(x_hosts, logits_hosts, out_hosts, w_gate_up.device,
+                                                     h2d_stream, d2h_stream)
+    _call("moe_forward_host_batches", xa, la, _ptr(w_gate_up), _ptr(w_down), n, T, d, f2 // 2, E, top_k, oa,
+          _ptr(workspace), workspace.numel(), _stream(stream), _stream(h2d), _stream(d2h))
+    return out_hosts
+
+
+def _host_batch_args(x_hosts, logits_hosts, out_hosts, device, h2d_stream, d2h_stream):
     n = len(x_hosts)
     if len(logits_hosts) != n or len(out_hosts) != n:
         raise ValueError("x_hosts, logits_hosts and out_hosts must have one tensor per batch")
-    if n == 0:
-        return out_hosts
     T, d = x_hosts[0].shape
     for i in range(n):
         for t, nm, shape in ((x_hosts[i], "x_hosts", (T, d)), (logits_hosts[i], "logits_hosts", None),
                              (out_hosts[i], "out_hosts", (T, d))):
             if t.is_cuda or not t.is_contiguous() or (shape is not None and tuple(t.shape) != shape):
                 raise ValueError(f"{nm}[{i}] must be a contiguous host tensor of the first batch's shape")
-    _dev(w_gate_up, torch.bfloat16, "w_gate_up")
-    _dev(w_down, torch.bfloat16, "w_down")
-    E, _, f2 = w_gate_up.shape
-    h2d = h2d_stream if h2d_stream is not None else torch.cuda.Stream(device=w_gate_up.device)
-    d2h = d2h_stream if d2h_stream is not None else torch.cuda.Stream(device=w_gate_up.device)
+    h2d = h2d_stream if h2d_stream is not None else torch.cuda.Stream(device=device)
+    d2h = d2h_stream if d2h_stream is not None else torch.cuda.Stream(device=device)
     arr = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])
-    _call("moe_forward_host_batches", arr(x_hosts), arr(logits_hosts), _ptr(w_gate_up), _ptr(w_down), n, T, d,
-          f2 // 2, E, top_k, arr(out_hosts), _ptr(workspace), workspace.numel(), _stream(stream), _stream(h2d),
-          _stream(d2h))
+    return n, T, d, arr(x_hosts), arr(logits_hosts), arr(out_hosts), h2d, d2h
+
+
+def _forward8_host_batches(sym, x_hosts, logits_hosts, w8_gate_up, s_gate_up, w8_down, s_down, top_k, out_hosts,
+                           workspace, stream, h2d_stream, d2h_stream):
+    if len(x_hosts) == 0:
+        return out_hosts
+    E, f2, _ = _w8_dims(w8_gate_up, "w8_gate_up")
+    n, T, d, xa, la, oa, h2d, d2h = _host_batch_args(x_hosts, logits_hosts, out_hosts, w8_gate_up.device,
+                                                     h2d_stream, d2h_stream)
+    _call(sym, xa, la, _ptr(w8_gate_up), _ptr(s_gate_up), _ptr(w8_down), _ptr(s_down), n, T, d, f2 // 2, E, top_k,
+          oa, _ptr(workspace), workspace.numel(), _stream(stream), _stream(h2d), _stream(d2h))
     return out_hosts
+
+
+def forward_fp8_host_batches(x_hosts, logits_hosts, w8_gate_up, s_gate_up, w8_down, s_down, top_k, out_hosts,
+                             workspace, stream=None, h2d_stream=None, d2h_stream=None):
+    """forward_host_batches with the FP8 layer (per-row / per-channel scales); the workspace holds
+    workspace_size_fp8() + 2 * host_staging_size() bytes."""
+    return _forward8_host_batches("moe_forward_fp8_host_batches", x_hosts, logits_hosts, w8_gate_up, s_gate_up,
+                                  w8_down, s_down, top_k, out_hosts, workspace, stream, h2d_stream, d2h_stream)
+
+
+def forward_fp8b_host_batches(x_hosts, logits_hosts, w8_gate_up, s_gate_up, w8_down, s_down, top_k, out_hosts,
+                              workspace, stream=None, h2d_stream=None, d2h_stream=None):
+    """forward_host_batches with the blockwise FP8 layer; the workspace holds workspace_size_fp8b() +
+    2 * host_staging_size() bytes."""
+    return _forward8_host_batches("moe_forward_fp8b_host_batches", x_hosts, logits_hosts, w8_gate_up, s_gate_up,
+                                  w8_down, s_down, top_k, out_hosts, workspace, stream, h2d_stream, d2h_stream)
 
 
 def get_device_error(status_or_workspace: torch.Tensor) -> int:

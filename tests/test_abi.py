@@ -122,6 +122,19 @@ def test_forward_host_batches_validates(lib):
     assert f(arr, arr, p, p, 2, 4, 64, 100, 8, 2, arr, p, 1 << 40, None, None, None) == -1   # f % 64
 
 
+@pytest.mark.parametrize("sym", ["moe_forward_fp8_host_batches", "moe_forward_fp8b_host_batches"])
+def test_forward_fp8_host_batches_validates(lib, sym):
+    p = ctypes.c_void_p(1 << 20)
+    arr = (ctypes.c_void_p * 2)(1 << 20, 1 << 21)
+    f = getattr(lib, sym)
+    assert f(arr, arr, p, p, p, p, 0, 4, 128, 128, 8, 2, arr, p, 1 << 40, None, None, None) == 0
+    assert f(arr, arr, p, p, p, p, -1, 4, 128, 128, 8, 2, arr, p, 1 << 40, None, None, None) == -1
+    assert f(arr, arr, p, None, p, p, 2, 4, 128, 128, 8, 2, arr, p, 1 << 40, None, None, None) == -1
+    assert f(arr, arr, p, p, p, p, 2, 4, 64, 128, 8, 2, arr, p, 1 << 40, None, None, None) == -1    # d % 128
+    assert f(arr, arr, p, p, p, p, 2, 4, 128, 128, 8, 2, arr, p, 4096, None, None, None) == -3
+    assert "workspace" in _err(lib)
+
+
 def test_stage_calls_reject_bad_arguments(lib):
     p = ctypes.c_void_p(1 << 20)
     assert lib.moe_route(None, 4, 8, 2, p, p, None) == -1

@@ -376,6 +376,33 @@ def test_forward_fp8_graph_capture(moe, variant):
     assert kinds.count(0) == count(w.T, w.E, w.k), kinds
 
 
+@pytest.mark.parametrize("variant", ["fp8", "fp8b"])
+def test_forward_fp8_host_batches_matches_forward(moe, variant):
+    """FP8 layers over host batches with overlapped copies give each batch's device-call output."""
+    w = Workload("fp8_host_batches", 97, 256, 512, 8, 2)
+    dev = torch.device(DEV)
+    _, _, wgu, wd = case_inputs(w, seed=31)
+    quant = moe.quantize_weights_fp8b if variant == "fp8b" else moe.quantize_weights_fp8
+    fwd = moe.forward_fp8b if variant == "fp8b" else moe.forward_fp8
+    batches = moe.forward_fp8b_host_batches if variant == "fp8b" else moe.forward_fp8_host_batches
+    wsize = moe.workspace_size_fp8b if variant == "fp8b" else moe.workspace_size_fp8
+    w8 = quant(wgu.to(dev)) + quant(wd.to(dev))
+    xs, ls, refs = [], [], []
+    for i in range(3):
+        logits, x, _, _ = case_inputs(w, seed=40 + i)
+        xs.append(x.pin_memory())
+        ls.append(logits.pin_memory())
+        refs.append(fwd(x.to(dev), logits.to(dev), *w8, w.k).cpu())
+    outs = [torch.full((w.T, w.d), -1.0, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    ws = torch.empty(wsize(w.T, w.d, w.f, w.E, w.k) + 2 * moe.host_staging_size(w.T, w.d, w.E),
+                     dtype=torch.uint8, device=dev)
+    batches(xs, ls, *w8, w.k, outs, ws)
+    torch.cuda.current_stream().synchronize()
+    assert moe.get_device_error(ws) == 0
+    for i in range(3):
+        assert torch.equal(outs[i].view(torch.int16), refs[i].view(torch.int16)), f"{variant} batch {i}"
+
+
 def test_fp8_status_flags(moe):
     """Bad offsets reach the FP8 and blockwise FP8 GEMMs' status bit; a bad expert id reaches the
     FP8 permute's; nothing is read out of bounds."""
