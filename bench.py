@@ -64,6 +64,8 @@ STAGES_FP8 = ("route", "permute", "gateup_swiglu", "quantize_h", "down", "combin
 KERNEL_NAMES_FP8 = {"gateup_swiglu": "grouped_gemm_kernel<0, false, true>",
                     "down": "grouped_gemm_kernel<1, false, true>"}
 STAGES_FP8B = ("route", "permute", "quantize_x", "gateup_swiglu", "quantize_h", "down", "combine")
+# ... when the gate+up GEMM quantises h in its epilogue (moe_fp8b_gemm_quantizes_h).
+STAGES_FP8B_FUSED = ("route", "permute", "quantize_x", "gateup_swiglu", "down", "combine")
 KERNEL_NAMES_FP8B = {"gateup_swiglu": "grouped_gemm_fp8b_kernel<0>",
                      "down": "grouped_gemm_fp8b_kernel<1>"}
 FP8_OVER_BF16 = 2.0  # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s) applied to the measured bf16 peak
@@ -157,21 +159,25 @@ def load_peaks():
 # ----------------------------------------------------------------------------------------------
 # Algorithmic work per stage (what the layer must move / compute, not what the kernels happen to)
 # ----------------------------------------------------------------------------------------------
-def stage_work(w: Workload, n_active: int, fp8: bool = False, blocks: bool = False) -> dict:
+def stage_work(w: Workload, n_active: int, fp8: bool = False, blocks: bool = False, fuse_h: bool = False) -> dict:
     T, d, f, E, k = w.T, w.d, w.f, w.E, w.k
     M = T * k
     if blocks:  # 1-byte codes; one 4-byte scale per 128 x 128 weight block and per 128 activation values
-        return {
+        h_out = M * f + M * f // 32 if fuse_h else M * f * 2  # codes + block scales, or bf16 h
+        work = {
             "route": {"bytes": T * E * 4 + M * 8, "flops": 0},
             "permute": {"bytes": M * 4 + (E + E + 1 + 2 * M) * 4, "flops": 0},
             "quantize_x": {"bytes": M * 4 + T * d * 2 + M * d + M * d // 32, "flops": 0},
-            "gateup_swiglu": {"bytes": n_active * (d * 2 * f + d * 2 * f // 4096) + M * d + M * d // 32 + M * f * 2,
+            "gateup_swiglu": {"bytes": n_active * (d * 2 * f + d * 2 * f // 4096) + M * d + M * d // 32 + h_out,
                               "flops": 4 * M * d * f},
             "quantize_h": {"bytes": M * f * 2 + M * f + M * f // 32, "flops": 0},
             "down": {"bytes": n_active * (f * d + f * d // 4096) + M * f + M * f // 32 + M * d * 4,
                      "flops": 2 * M * d * f},
             "combine": {"bytes": M * d * 4 + M * 8 + T * d * 2, "flops": 2 * M * d},
         }
+        if fuse_h:
+            del work["quantize_h"]
+        return work
     if fp8:  # 1-byte codes; weight scales 4 bytes per output column, activation scales per row
         return {
             "route": {"bytes": T * E * 4 + M * 8, "flops": 0},
@@ -382,7 +388,8 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     idx, wts = v["idx"], v["w"]
     counts_d, offs, src, dest, h, y = (v["counts"], v["offsets"], v["src"], v["dest"], v["h"], v["y_perm"])
     st = v["status"]
-    stages = STAGES_FP8B if blocks else (STAGES_FP8 if fp8 else STAGES)
+    fuse_h = blocks and moe.fp8b_gemm_quantizes_h(w.T, w.E, w.k)
+    stages = (STAGES_FP8B_FUSED if fuse_h else STAGES_FP8B) if blocks else (STAGES_FP8 if fp8 else STAGES)
     if blocks:
         x8, sx, h8, sh = v["x8"], v["sx"], v["h8"], v["sh"]
         route_call = ((lambda: moe.route_grouped(l_d, bias_d, w.k, *w.router[1:4], idx=idx, w=wts)) if grouped else
@@ -391,8 +398,12 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
             route_call,
             lambda: moe.permute(idx, x_d, w.E, status=st, out=(counts_d, offs, src, dest, None)),
             lambda: moe.quantize_rows_fp8b(x_d, src, status=st, out=(x8, sx)),
+        ] + ([
+            lambda: moe.grouped_gemm_gateup_swiglu_fp8b_q(x8, sx, w8[0], w8[1], offs, h8=h8, sh=sh, status=st),
+        ] if fuse_h else [
             lambda: moe.grouped_gemm_gateup_swiglu_fp8b(x8, sx, w8[0], w8[1], offs, h=h, status=st),
             lambda: moe.quantize_rows_fp8b(h, status=st, out=(h8, sh)),
+        ]) + [
             lambda: moe.grouped_gemm_down_fp8b(h8, sh, w8[2], w8[3], offs, y_perm=y, status=st, ksplit=v["ksplit"]),
             lambda: moe.combine(y, wts, dest, out=out, status=st, ksplit=v["ksplit"]),
         ]
@@ -496,7 +507,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         raise RuntimeError("device status word set during the timed region")
 
     peaks, peak_src = load_peaks()
-    sw = stage_work(w, n_active, fp8, blocks)
+    sw = stage_work(w, n_active, fp8, blocks, fuse_h)
     lw = layer_work(w, n_active, fp8, blocks)
     dom = max(("gateup_swiglu", "down"), key=lambda n: stage_ms[n])
     dom_ms = stage_ms[dom]
@@ -532,8 +543,8 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         "host_weights": (wgu, wd), "inputs": (logits, x), "step_ms_p10_p90": (
             float(np.percentile(step_ms, 10)), float(np.percentile(step_ms, 90))),
         "peak_src": peak_src, "peaks": peaks, "ksplit": v["ksplit"],
-        # DeepSeek-V3's router never fuses with the permutation: 5 (bf16), 6 (e4m3), 7 (e4m3b).
-        "launches_per_step": ((7 if blocks else 6 if fp8 else 5) if grouped else
+        # DeepSeek-V3's router never fuses with the permutation: 5 (bf16), 6 (e4m3), 6 or 7 (e4m3b).
+        "launches_per_step": (((7 - int(fuse_h)) if blocks else 6 if fp8 else 5) if grouped else
                               moe.forward_fp8b_launch_count(w.T, w.E, w.k) if blocks else
                               moe.forward_fp8_launch_count(w.T, w.E, w.k) if fp8 else
                               moe.forward_launch_count(w.T, w.E, w.k)),

@@ -375,15 +375,29 @@ MOE_API int moe_quantize_rows_fp8b(const void* a, const int32_t* src, int R, int
 MOE_API int moe_grouped_gemm_gateup_swiglu_fp8b(const void* x8_perm, const float* sx, const void* w8_gate_up,
                                                 const float* s_gate_up, const int32_t* offsets, int M, int d,
                                                 int f, int E, void* h, int32_t* status, moe_stream_t stream);
+/* moe_grouped_gemm_gateup_swiglu_fp8b with h quantised in the GEMM's epilogue, as
+ * moe_quantize_rows_fp8b would quantise its bf16 output: h8 [M, f] E4M3 codes (the bf16-rounded
+ * h divided by its block's scale) and sh [M, f/128] power-of-two block scales; h in bf16 is never
+ * written.  moe_forward_fp8b runs this form.  sh 4-byte aligned; other arguments and errors as the
+ * call above. */
+MOE_API int moe_grouped_gemm_gateup_swiglu_fp8b_q(const void* x8_perm, const float* sx, const void* w8_gate_up,
+                                                  const float* s_gate_up, const int32_t* offsets, int M, int d,
+                                                  int f, int E, void* h8, float* sh, int32_t* status,
+                                                  moe_stream_t stream);
 MOE_API int moe_grouped_gemm_down_fp8b(const void* h8, const float* sh, const void* w8_down, const float* s_down,
                                        const int32_t* offsets, int M, int d, int f, int E, int ksplit,
                                        float* y_perm, int32_t* status, moe_stream_t stream);
 
 /* The blockwise FP8 layer in one call: route (+ permute, indices only), x rows quantised in blocks
  * (gathered by src), blockwise gate+up GEMM (+ SwiGLU), h quantised in blocks, blockwise down GEMM,
- * combine — 6 launches (7 when routing and the permutation run apart).  Workspace as for
+ * combine.  When the experts hold more than 64 rows on average (T*top_k > 64*E), h is quantised in
+ * the gate+up GEMM's epilogue (moe_grouped_gemm_gateup_swiglu_fp8b_q; h in bf16 is not written),
+ * else by its own launch: 5 or 6 launches, one more when routing and the permutation run apart
+ * (moe_forward_fp8b_launch_count; moe_fp8b_gemm_quantizes_h tells which form, 1 = in the GEMM,
+ * -1 for a bad shape; MOE_FP8B_FUSE_H=0/1 overrides the choice).  Workspace as for
  * moe_forward_fp8 (14 offsets from moe_workspace_layout_fp8b), with sx [T*top_k, d/128] and
  * sh [T*top_k, f/128]. */
+MOE_API int moe_fp8b_gemm_quantizes_h(int T, int E, int top_k);
 MOE_API size_t moe_workspace_size_fp8b(int T, int d, int f, int E, int top_k);
 MOE_API int moe_workspace_layout_fp8b(int T, int d, int f, int E, int top_k, size_t* offsets_out);
 MOE_API int moe_down_ksplit_fp8b(int T, int d, int f, int E, int top_k);

@@ -104,6 +104,9 @@ struct GemmArgs {
     // Blockwise FP8 (with fp8; launched by launch_grouped_gemm_fp8b): a_scale [M, K/128] (one per
     // 128-wide row block), b_scale [E, N_total/128, K/128] (one per 128 x 128 block), N % 128 == 0.
     bool fp8_blocks = false;
+    // Blockwise gate+up only: when set, out receives h's E4M3 codes [M, N] (uint8) and h_scale
+    // [M, N/128] the power-of-two scale of each 128-wide block, h quantised in the epilogue.
+    float* h_scale = nullptr;
 };
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                 const char** why);

@@ -34,6 +34,7 @@
 // round-robin over one persistent CTA per SM.  Every wait is bounded (1 s) and reports
 // MOE_STATUS_WAIT_TIMEOUT.
 #include "common.cuh"
+#include "fp8.cuh"
 #include "tcgen05.cuh"
 
 namespace moe {
@@ -81,6 +82,12 @@ struct Ctl {
     int total_items;
     int seg[MAX_E + 1];
     int item_start[MAX_E + 1];
+    // Quantised h (kind 0 with h_scale): the absolute maxima of each 128-wide h block are shared
+    // between the warps that hold its columns, in two slots used by alternate items.
+    float xn[2][2][BM];         // normal items: [slot][half hh][row] max over the half's 64 columns
+    float xs[2][2][4][32];      // swapped items: [slot][hh][lane quarter][token] max over 32 columns
+    uint64_t xbar_n[2][4];      // [slot][quarter]: the quarter's two warps wrote (64 arrivals)
+    uint64_t xbar_s[2][2];      // [slot][hh]: the four quarters' warps wrote (128 arrivals)
 };
 static_assert(STAGES * STAGE_BYTES + 1024 + sizeof(Ctl) <= SMEM_BYTES, "shared memory budget");
 
@@ -127,17 +134,25 @@ __device__ __forceinline__ void raise_abort(Ctl& c, int32_t* status) {
 // silu(g) * u with the fast-divide intrinsic (its ~2 ulp error is far below h's bf16 rounding).
 __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
+// Two values -> two E4M3 codes (a in the low byte), rounded as to_e4m3 rounds each.
+__device__ __forceinline__ uint16_t e4m3x2(float a, float b) {
+    return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
 __device__ __forceinline__ uint16_t bf16_bits(float v) {
     __nv_bfloat16 b = __float2bfloat16_rn(v);
     return *reinterpret_cast<uint16_t*>(&b);
 }
 
-template <int KIND>
+// QH (kind 0 only): h quantised in the epilogue, a separate instance so that the plain one keeps
+// its register allocation.
+template <int KIND, bool QH>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
                          const __grid_constant__ CUtensorMap tmB128, const int32_t* __restrict__ offsets, int M,
                          int K, int N, int E, int ksplit, int swap_max, const float* __restrict__ a_scale,
-                         const float* __restrict__ b_scale, void* __restrict__ out, int32_t* __restrict__ status) {
+                         const float* __restrict__ b_scale, void* __restrict__ out, float* __restrict__ h_scale,
+                         int32_t* __restrict__ status) {
     constexpr int BN = bn_item<KIND>();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -161,6 +176,10 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             ptx::mbar_init(&c.pempty[p], EPI_WARPS);
         }
         ptx::mbar_init(&c.drain, 1);
+        for (int k = 0; k < 2; ++k) {
+            for (int q = 0; q < 4; ++q) ptx::mbar_init(&c.xbar_n[k][q], 64);
+            for (int q = 0; q < 2; ++q) ptx::mbar_init(&c.xbar_s[k][q], 128);
+        }
         c.abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
@@ -325,6 +344,8 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         const int quarter = warp & 3, hh = (warp - 4) >> 2;
         const int r_local = quarter * 32 + lane;
         uint32_t pb = 0, pph = 0;
+        uint32_t xn_count = 0, xs_count = 0;  // exchanges done (quantised h), per item kind
+        constexpr bool quant_h = KIND == 0 && QH;
         bool aborted = false;
         for (int i = blockIdx.x; i < total && !aborted; i += gridDim.x) {
             const Item it = decode_item(c, E, ksplit, swap_max, i);
@@ -425,6 +446,80 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             }
             if (aborted) break;
             // ------------------------------ epilogue from registers ------------------------------
+            if constexpr (quant_h) {
+                // h rounded to bf16 (the values the block quantiser reads), then E4M3 codes with the
+                // power-of-two scale of its 128-wide block, whose absolute maximum spans two warps
+                // (normal items: halves hh of the row) or four (swapped: lane quarters of a column
+                // block): each warp's partial maximum goes through shared memory; a slot is rewritten
+                // two items later, after every warp of the exchange has passed the next one.
+                uint8_t* h8 = reinterpret_cast<uint8_t*>(out);
+                const int nb = N / 128;
+                if (!it.swap) {
+                    float m = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        acc[j] = __bfloat162float(__float2bfloat16_rn(silu_mul(acc[j], acc[64 + j])));
+                        m = fmaxf(m, fabsf(acc[j]));
+                    }
+                    const uint32_t slot = xn_count & 1u, par = (xn_count >> 1) & 1u;
+                    ++xn_count;
+                    c.xn[slot][hh][r_local] = row_ok ? m : 0.0f;
+                    ptx::mbar_arrive(&c.xbar_n[slot][quarter]);
+                    if (!ptx::mbar_wait(&c.xbar_n[slot][quarter], par, abort_flag)) {
+                        raise_abort(c, status);
+                        break;
+                    }
+                    if (!row_ok) continue;
+                    const float P = pow2_block_scale(fmaxf(m, c.xn[slot][hh ^ 1][r_local]));
+                    const float inv = 1.0f / P;
+                    uint4* dst = reinterpret_cast<uint4*>(h8 + grow * N + n0 + 64 * hh);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int j = 16 * v + 4 * q;
+                            w[q] = static_cast<uint32_t>(e4m3x2(acc[j] * inv, acc[j + 1] * inv)) |
+                                   (static_cast<uint32_t>(e4m3x2(acc[j + 2] * inv, acc[j + 3] * inv)) << 16);
+                        }
+                        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    if (hh == 0) h_scale[grow * nb + n0 / 128] = P;
+                } else {
+                    // Lane = h column n0 + r_local, acc[j] = token 32hh + j.
+                    float mine = 0.0f;  // this warp's maximum for token 32hh + lane
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        acc[j] = __bfloat162float(__float2bfloat16_rn(silu_mul(acc[j], acc[32 + j])));
+                        float v = fabsf(acc[j]);
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                        if (lane == j) mine = v;
+                    }
+                    const uint32_t slot = xs_count & 1u, par = (xs_count >> 1) & 1u;
+                    ++xs_count;
+                    c.xs[slot][hh][quarter][lane] = mine;
+                    ptx::mbar_arrive(&c.xbar_s[slot][hh]);
+                    if (!ptx::mbar_wait(&c.xbar_s[slot][hh], par, abort_flag)) {
+                        raise_abort(c, status);
+                        break;
+                    }
+                    // Lane j: the scale of token 32hh + j, then every lane takes 1/P of each token.
+                    const float P = pow2_block_scale(fmaxf(fmaxf(c.xs[slot][hh][0][lane], c.xs[slot][hh][1][lane]),
+                                                           fmaxf(c.xs[slot][hh][2][lane], c.xs[slot][hh][3][lane])));
+                    const float inv_mine = 1.0f / P;
+                    if (quarter == 0 && 32 * hh + lane < it.rows)
+                        h_scale[static_cast<size_t>(it.row0 + 32 * hh + lane) * nb + n0 / 128] = P;
+                    const int col = n0 + r_local;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float inv = __shfl_sync(0xffffffffu, inv_mine, j);
+                        const int t = 32 * hh + j;
+                        if (t < it.rows) h8[static_cast<size_t>(it.row0 + t) * N + col] = to_e4m3(acc[j] * inv);
+                    }
+                }
+                continue;
+            }
             if (!it.swap) {
                 if (!row_ok) continue;
                 if (KIND == 0) {
@@ -483,14 +578,14 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     if (warp == 1) ptx::tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
-template <int KIND>
+template <int KIND, bool QH>
 cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const char** why) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_fp8b_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_fp8b_kernel<KIND, QH>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) {
             *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
             return e;
@@ -498,7 +593,7 @@ cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const ch
         attr_set[dev] = true;
     }
     cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8b_kernel<KIND>) != cudaSuccess ||
+    if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8b_kernel<KIND, QH>) != cudaSuccess ||
         fa.numRegs * NUM_THREADS < REGS_CTL * 128 + REGS_PROMO * 32 * EPI_WARPS) {
         *why = "blockwise FP8 GEMM: the kernel was compiled with fewer registers than its setmaxnreg split needs";
         return cudaErrorInvalidValue;
@@ -512,9 +607,9 @@ cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const ch
     }
     const int swap_max = a.swap_max < 0 ? 0 : (a.swap_max > SWAP_MAX_ROWS ? SWAP_MAX_ROWS : a.swap_max);
     const int ksplit = KIND == 0 ? 1 : a.ksplit;
-    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_fp8b_kernel<KIND>, dim3(num_sms),
+    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_fp8b_kernel<KIND, QH>, dim3(num_sms),
                     dim3(NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB128, a.offsets, a.M, a.K, a.N, a.E, ksplit,
-                    swap_max, a.a_scale, a.b_scale, a.out, a.status);
+                    swap_max, a.a_scale, a.b_scale, a.out, QH ? a.h_scale : nullptr, a.status);
 }
 
 }  // namespace
@@ -524,7 +619,8 @@ cudaError_t launch_grouped_gemm_fp8b(int kind, const GemmArgs& a, int num_sms, c
         *why = "blockwise FP8 grouped GEMM: N and K must be multiples of 128, scales given";
         return cudaErrorInvalidValue;
     }
-    return kind == 0 ? launch_kind<0>(a, num_sms, s, why) : launch_kind<1>(a, num_sms, s, why);
+    if (kind == 1) return launch_kind<1, false>(a, num_sms, s, why);
+    return a.h_scale ? launch_kind<0, true>(a, num_sms, s, why) : launch_kind<0, false>(a, num_sms, s, why);
 }
 
 }  // namespace moe

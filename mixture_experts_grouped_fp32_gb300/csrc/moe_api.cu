@@ -137,6 +137,18 @@ int use_pair(long long M, int E, int N, int kind, bool fp8 = false) {
     return 0;
 }
 
+// Blockwise FP8: whether the gate+up GEMM quantises h in its epilogue (codes + 128-wide block
+// scales; the separate quantisation launch goes) — when the experts hold more than 64 rows on
+// average, so that most items are normal 128-row tiles.  The swapped items' epilogue shares each
+// token's block maximum across four warps and costs more than the launch it saves (Mixtral shape,
+// T=32, all items swapped: 0.253 vs 0.242 ms/layer; T=512 0.417 vs 0.430, T=4096 1.902 vs
+// 1.944; DeepSeek-V3 shape, 64 rows per expert on average, 1.852 vs 1.846).
+// MOE_FP8B_FUSE_H=0/1 overrides.
+bool fp8b_fuse_h(long long M, int E) {
+    if (const char* v = std::getenv("MOE_FP8B_FUSE_H")) return v[0] == '1';
+    return M > 64ll * E;
+}
+
 // Swap threshold of the SM-pair kernel in mode 2: experts with at most this many rows run as one
 // swapped chunk (further capped on the device at 64 or 128 rows by the shared-memory layout the
 // kernel picks).  MOE_GEMM_PAIR_SWAP_MAX overrides (clamped to [0, 128]).
@@ -406,17 +418,24 @@ int run_layer_fp8(const void* x, const float* logits, const void* wgu8, const fl
         return ge == cudaSuccess ? MOE_OK : fail(MOE_ERR_CUDA, "%s: %s (%s)", what, why, cudaGetErrorString(ge));
     };
     const int ksplit = down_ksplit(T, d, f, E, k, true, blocks);
-    GemmArgs g1{x8, wgu8, offsets, M, d, f, E, h, status, 1, swap_max_rows(), blocks ? 0 : use_pair(M, E, f, 0, true),
-                pair_swap_max_rows(), pair_layout(), pair_split()};
+    // Blockwise, by fp8b_fuse_h: the gate+up GEMM writes h's codes and 128-wide block scales itself
+    // (h in bf16 never exists).  Otherwise, and always for per-row scales (which need the whole
+    // row), h is quantised by a launch of its own.
+    const bool fuse_h = blocks && fp8b_fuse_h(M, E);
+    GemmArgs g1{x8, wgu8, offsets, M, d, f, E, fuse_h ? static_cast<void*>(h8) : h, status, 1, swap_max_rows(),
+                blocks ? 0 : use_pair(M, E, f, 0, true), pair_swap_max_rows(), pair_layout(), pair_split()};
     g1.fp8 = true;
     g1.fp8_blocks = blocks;
     g1.a_scale = sx;
     g1.b_scale = sgu;
+    if (fuse_h) g1.h_scale = sh;
     int rc = gemm(0, g1, blocks ? "blockwise FP8 gate+up GEMM" : "FP8 gate+up GEMM");
     if (rc) return rc;
-    e = blocks ? launch_quantize_rows_fp8b(h, nullptr, M, f, M, h8, sh, status, s)
-               : launch_quantize_rows_fp8(h, nullptr, M, f, M, h8, sh, status, s);
-    if (e != cudaSuccess) return launched(e, "quantize h");
+    if (!fuse_h) {
+        e = blocks ? launch_quantize_rows_fp8b(h, nullptr, M, f, M, h8, sh, status, s)
+                   : launch_quantize_rows_fp8(h, nullptr, M, f, M, h8, sh, status, s);
+        if (e != cudaSuccess) return launched(e, "quantize h");
+    }
     GemmArgs g2{h8, wd8, offsets, M, f, d, E, y, status, ksplit, swap_max_rows(),
                 blocks ? 0 : use_pair(M, E, d, 1, true), pair_swap_max_rows(), pair_layout(), pair_split()};
     g2.fp8 = true;
@@ -934,7 +953,7 @@ int moe_quantize_rows_fp8(const void* a, const int32_t* src, int R, int C, int s
 // The FP8 GEMM stage calls; blocks = true for the blockwise kernel.
 static int gemm8_entry(int kind, const void* A, const float* sa, const void* B, const float* sb,
                        const int32_t* offsets, int M, int d, int f, int E, int ksplit, void* out, int32_t* status,
-                       moe_stream_t stream, const char* name, bool blocks = false) {
+                       moe_stream_t stream, const char* name, bool blocks = false, float* h_scale = nullptr) {
     int rc = check_shape_fp8(0, d, f, E, 1, name);
     if (rc) return rc;
     if (M < 0) return fail(MOE_ERR_INVALID_ARG, "%s: M = %d must be >= 0", name, M);
@@ -944,7 +963,7 @@ static int gemm8_entry(int kind, const void* A, const float* sa, const void* B, 
     if (!A || !sa || !B || !sb || !offsets || !out) return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
     if (!aligned16(A) || !aligned16(B) || !aligned16(out))
         return fail(MOE_ERR_INVALID_ARG, "%s: operands must be 16-byte aligned", name);
-    if (!aligned16(sb) || (reinterpret_cast<uintptr_t>(sa) & 3u))
+    if (!aligned16(sb) || (reinterpret_cast<uintptr_t>(sa) & 3u) || (reinterpret_cast<uintptr_t>(h_scale) & 3u))
         return fail(MOE_ERR_INVALID_ARG, "%s: weight scales must be 16-byte, row scales 4-byte aligned", name);
     int sms;
     if ((rc = check_device(&sms))) return rc;
@@ -958,6 +977,7 @@ static int gemm8_entry(int kind, const void* A, const float* sa, const void* B, 
     g.fp8_blocks = blocks;
     g.a_scale = sa;
     g.b_scale = sb;
+    g.h_scale = h_scale;
     const char* why = "";
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = blocks ? launch_grouped_gemm_fp8b(kind, g, sms, cs, &why) : launch_grouped_gemm(kind, g, sms, cs, &why);
@@ -1116,7 +1136,12 @@ int moe_down_ksplit_fp8b(int T, int d, int f, int E, int top_k) {
 int moe_forward_fp8b_launch_count(int T, int E, int top_k) {
     if (check_shape(T, -1, 0, E, top_k, false) != MOE_OK) return -1;
     if (T == 0) return 0;
-    return fuse_route_permute(T, E) ? 6 : 7;
+    return (fuse_route_permute(T, E) ? 5 : 6) + (fp8b_fuse_h(static_cast<long long>(T) * top_k, E) ? 0 : 1);
+}
+
+int moe_fp8b_gemm_quantizes_h(int T, int E, int top_k) {
+    if (check_shape(T, -1, 0, E, top_k, false) != MOE_OK) return -1;
+    return fp8b_fuse_h(static_cast<long long>(T) * top_k, E) ? 1 : 0;
 }
 
 int moe_quantize_weights_fp8b(const void* W, int E, int K, int N, void* Wq, float* scale, moe_stream_t stream) {
@@ -1159,6 +1184,15 @@ int moe_grouped_gemm_gateup_swiglu_fp8b(const void* x8_perm, const float* sx, co
                                         void* h, int32_t* status, moe_stream_t stream) {
     return gemm8_entry(0, x8_perm, sx, w8_gate_up, s_gate_up, offsets, M, d, f, E, 1, h, status, stream,
                        "moe_grouped_gemm_gateup_swiglu_fp8b", true);
+}
+
+int moe_grouped_gemm_gateup_swiglu_fp8b_q(const void* x8_perm, const float* sx, const void* w8_gate_up,
+                                          const float* s_gate_up, const int32_t* offsets, int M, int d, int f, int E,
+                                          void* h8, float* sh, int32_t* status, moe_stream_t stream) {
+    const char* name = "moe_grouped_gemm_gateup_swiglu_fp8b_q";
+    if (M > 0 && !sh) return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
+    return gemm8_entry(0, x8_perm, sx, w8_gate_up, s_gate_up, offsets, M, d, f, E, 1, h8, status, stream, name, true,
+                       sh);
 }
 
 int moe_grouped_gemm_down_fp8b(const void* h8, const float* sh, const void* w8_down, const float* s_down,

@@ -58,6 +58,8 @@ _SIGS = {
     "moe_quantize_weights_fp8b": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_quantize_rows_fp8b": ([_P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_gateup_swiglu_fp8b": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "moe_grouped_gemm_gateup_swiglu_fp8b_q": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_fp8b_gemm_quantizes_h": ([_I, _I, _I], _I),
     "moe_grouped_gemm_down_fp8b": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_workspace_size_fp8b": ([_I, _I, _I, _I, _I], _SZ),
     "moe_workspace_layout_fp8b": ([_I, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _I),
@@ -659,6 +661,23 @@ def grouped_gemm_gateup_swiglu_fp8b(x8_perm, sx, w8_gate_up, s_gate_up, offsets,
     return h
 
 
+def grouped_gemm_gateup_swiglu_fp8b_q(x8_perm, sx, w8_gate_up, s_gate_up, offsets, h8=None, sh=None, status=None,
+                                      stream=None):
+    """Blockwise step 3 with h quantised in the epilogue: (h8 [M, f] codes, sh [M, f/128] scales)."""
+    _dev(x8_perm, torch.uint8, "x8_perm")
+    _dev(sx, torch.float32, "sx")
+    _dev(s_gate_up, torch.float32, "s_gate_up")
+    _dev(offsets, torch.int32, "offsets")
+    M, d = x8_perm.shape
+    E, f2, _ = _w8_dims(w8_gate_up, "w8_gate_up")
+    f = f2 // 2
+    h8 = h8 if h8 is not None else torch.empty(M, f, dtype=torch.uint8, device=x8_perm.device)
+    sh = sh if sh is not None else torch.empty(M, f // 128, dtype=torch.float32, device=x8_perm.device)
+    _call("moe_grouped_gemm_gateup_swiglu_fp8b_q", _ptr(x8_perm), _ptr(sx), _ptr(w8_gate_up), _ptr(s_gate_up),
+          _ptr(offsets), M, d, f, E, _ptr(h8), _ptr(sh), _ptr(status), _stream(stream))
+    return h8, sh
+
+
 def grouped_gemm_down_fp8b(h8, sh, w8_down, s_down, offsets, y_perm=None, status=None, stream=None, ksplit: int = 1):
     """Blockwise step 4: sh [M, f/128], s_down [E, d/128, f/128]."""
     _dev(h8, torch.uint8, "h8")
@@ -693,8 +712,14 @@ def down_ksplit_fp8b(T: int, d: int, f: int, E: int, top_k: int) -> int:
 
 
 def forward_fp8b_launch_count(T: int, E: int, top_k: int) -> int:
-    """Kernel launches of one moe_forward_fp8b call (6 with route+permute fused, else 7)."""
+    """Kernel launches of one moe_forward_fp8b call (5 or 6 with route+permute fused, one more
+    otherwise; see fp8b_gemm_quantizes_h)."""
     return int(load().moe_forward_fp8b_launch_count(T, E, top_k))
+
+
+def fp8b_gemm_quantizes_h(T: int, E: int, top_k: int) -> bool:
+    """Whether moe_forward_fp8b's gate+up GEMM quantises h itself (T*top_k > 64*E, or MOE_FP8B_FUSE_H)."""
+    return int(load().moe_fp8b_gemm_quantizes_h(T, E, top_k)) == 1
 
 
 def forward_fp8b(x, logits, w8_gate_up, s_gate_up, w8_down, s_down, top_k, out=None, workspace=None, stream=None):

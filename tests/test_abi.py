@@ -309,6 +309,20 @@ def test_gemm_pair_mode_fp8_policy(lib):
     assert f(32, 4096, 14336, 8, 2, 2) == -1 and f(32, 4000, 14336, 8, 2, 0) == -1
 
 
+def test_fp8b_quantised_h_policy(lib, monkeypatch):
+    monkeypatch.delenv("MOE_FP8B_FUSE_H", raising=False)
+    f = lib.moe_fp8b_gemm_quantizes_h
+    assert f(32, 8, 2) == 0 and f(256, 8, 2) == 0        # 8 / 64 rows per expert on average
+    assert f(512, 8, 2) == 1 and f(4096, 8, 2) == 1      # 128 / 1024
+    assert f(2048, 256, 8) == 0                          # DeepSeek-V3 shape: 64
+    assert f(4, 8, 9) == -1
+    assert lib.moe_forward_fp8b_launch_count(4096, 8, 2) == 6 and lib.moe_forward_fp8b_launch_count(2048, 256, 8) == 7
+    monkeypatch.setenv("MOE_FP8B_FUSE_H", "1")
+    assert f(32, 8, 2) == 1 and lib.moe_forward_fp8b_launch_count(32, 8, 2) == 5
+    monkeypatch.setenv("MOE_FP8B_FUSE_H", "0")
+    assert f(4096, 8, 2) == 0
+
+
 def test_fp8b_entry_points_validate(lib):
     from mixture_experts_grouped_fp32_gb300 import moe
     T, d, f, E, k = 300, 512, 768, 8, 2
@@ -318,7 +332,8 @@ def test_fp8b_entry_points_validate(lib):
     assert L["h"] - L["sx"] >= M * (d // 128) * 4
     assert moe.workspace_size_fp8b(T, d, f, E, k) == L["total"]
     assert moe.down_ksplit_fp8b(T, d, f, E, k) >= 1
-    assert lib.moe_forward_fp8b_launch_count(32, 8, 2) == 6
+    assert lib.moe_forward_fp8b_launch_count(32, 8, 2) == 6      # h quantised by its own launch
+    assert lib.moe_forward_fp8b_launch_count(512, 8, 2) == 5     # h quantised in the gate+up GEMM
     p = ctypes.c_void_p(1 << 20)
     assert lib.moe_quantize_weights_fp8b(p, 8, 256, 192, p, p, None) == -1      # N % 128
     assert lib.moe_quantize_rows_fp8b(p, None, 4, 64, 4, p, p, None, None) == -1  # C % 128

@@ -144,6 +144,34 @@ def test_gemm_fp8b_parity(moe, oracle, monkeypatch, ci, swap_max):
     assert_close(y.cpu().numpy()[:n], ref_y[:n], 1e-3, 1e-4, "blockwise fp8 down y")
 
 
+@pytest.mark.parametrize("swap_max", ["64", "0"])
+@pytest.mark.parametrize("ci", range(len(GEMM_CASES)))
+def test_gemm_gateup_fp8b_quantised_h(moe, oracle, monkeypatch, ci, swap_max):
+    """The gate+up GEMM quantising h in its epilogue gives, bit for bit, the codes and block scales
+    that quantising its bf16 output gives (normal and swapped items; rows past the experts' untouched)."""
+    monkeypatch.setenv("MOE_GEMM_SWAP_MAX", swap_max)
+    counts, d, f = GEMM_CASES[ci]
+    E = len(counts)
+    offsets = segments(counts)
+    n = int(offsets[-1])
+    M = n + 3
+    seed = 2000 + 10 * ci + int(swap_max)
+    x8, sx = draw_e4m3_codes((M, d), seed), draw_pow2_scales((M, d // 128), seed + 1)
+    wgu8, sgu = draw_e4m3_codes((E, 2 * f, d), seed + 2), draw_pow2_scales((E, 2 * f // 128, d // 128), seed + 3)
+    off_t = torch.from_numpy(offsets).to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    h = moe.grouped_gemm_gateup_swiglu_fp8b(u8(x8), f32(sx), w8(wgu8), f32(sgu), off_t, status=status)
+    h8 = torch.full((M, f), 0x7E, dtype=torch.uint8, device=DEV)
+    sh = torch.full((M, f // 128), -1.0, dtype=torch.float32, device=DEV)
+    moe.grouped_gemm_gateup_swiglu_fp8b_q(u8(x8), f32(sx), w8(wgu8), f32(sgu), off_t, h8=h8, sh=sh, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref8, refs = oracle.quantize_rows_fp8b(to_np_bits(h[:n].cpu()))
+    assert np.array_equal(h8[:n].cpu().numpy(), ref8)
+    assert np.array_equal(sh[:n].cpu().numpy(), refs)
+    assert bool((h8[n:] == 0x7E).all()) and bool((sh[n:] == -1.0).all())
+
+
 @pytest.mark.parametrize("ksplit", [2, 3])
 def test_gemm_down_fp8b_ksplit(moe, oracle, ksplit):
     counts, d, f = [40, 300, 0, 77], 256, 640
@@ -181,10 +209,16 @@ def quantized_weights(moe, oracle, wgu, wd):
     return (wgu8, sgu, wd8, sd), r
 
 
-@pytest.mark.parametrize("mode", ["default", "noswap", "ksplit3", "nofuse"])
+@pytest.mark.parametrize("mode", ["default", "noswap", "ksplit3", "nofuse", "fuse_h", "fuse_h_noswap", "unfused_h"])
 @pytest.mark.parametrize("w", LAYER_CASES, ids=lambda w: w.name)
 def test_forward_fp8b_matches_oracle(moe, oracle, monkeypatch, w, mode):
-    if mode == "noswap":
+    if mode.startswith("fuse_h"):  # h quantised in the gate+up GEMM's epilogue whatever the shape
+        monkeypatch.setenv("MOE_FP8B_FUSE_H", "1")
+        if mode == "fuse_h_noswap":
+            monkeypatch.setenv("MOE_GEMM_SWAP_MAX", "0")
+    elif mode == "unfused_h":
+        monkeypatch.setenv("MOE_FP8B_FUSE_H", "0")
+    elif mode == "noswap":
         monkeypatch.setenv("MOE_GEMM_SWAP_MAX", "0")
     elif mode == "ksplit3":
         monkeypatch.setenv("MOE_DOWN_KSPLIT", "3")
@@ -211,8 +245,10 @@ def test_forward_fp8b_matches_oracle(moe, oracle, monkeypatch, w, mode):
 
 
 def test_forward_fp8b_launch_count(moe):
-    assert moe.forward_fp8b_launch_count(64, 8, 2) == 6
+    assert moe.forward_fp8b_launch_count(64, 8, 2) == 6       # 16 rows per expert: h quantised apart
     assert moe.forward_fp8b_launch_count(2048, 256, 8) == 7
+    assert moe.forward_fp8b_launch_count(512, 8, 2) == 5      # 128 rows: in the gate+up GEMM
+    assert moe.forward_fp8b_launch_count(4096, 8, 2) == 6
 
 
 @pytest.mark.slow
