@@ -66,8 +66,9 @@ KERNEL_NAMES_FP8 = {"gateup_swiglu": "grouped_gemm_kernel<0, false, true>",
 STAGES_FP8B = ("route", "permute", "quantize_x", "gateup_swiglu", "quantize_h", "down", "combine")
 # ... when the gate+up GEMM quantises h in its epilogue (moe_fp8b_gemm_quantizes_h).
 STAGES_FP8B_FUSED = ("route", "permute", "quantize_x", "gateup_swiglu", "down", "combine")
-KERNEL_NAMES_FP8B = {"gateup_swiglu": "grouped_gemm_fp8b_kernel<0>",
-                     "down": "grouped_gemm_fp8b_kernel<1>"}
+# <KIND, QH>: QH = h quantised in the gate+up epilogue.
+KERNEL_NAMES_FP8B = {"gateup_swiglu": "grouped_gemm_fp8b_kernel<0, false>",
+                     "down": "grouped_gemm_fp8b_kernel<1, false>"}
 FP8_OVER_BF16 = 2.0  # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s) applied to the measured bf16 peak
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum per launch) from ncu captures of the
@@ -78,7 +79,7 @@ AUTO_TIMED_S = 0.5
 AUTO_STEPS_MIN, AUTO_STEPS_MAX = 50, 4000
 
 _TRAFFIC_HASH = "a8d3a7a96e328c09"  # GEMM source hash the captures below were taken at
-_TRAFFIC_HASH_FP8B = "55d0627b99641536"  # ... and that of the blockwise FP8 kernel's sources
+_TRAFFIC_HASH_FP8B = "f00c09d6f20a7ae5"  # ... and that of the blockwise FP8 kernel's sources
 MEASURED_TRAFFIC = {
     ("deepseek_e32_t256", "gateup_swiglu"): (1919914752, _TRAFFIC_HASH),
     ("deepseek_e32_t256", "down"): (1008838144, _TRAFFIC_HASH),
@@ -106,20 +107,20 @@ MEASURED_TRAFFIC = {
     ("deepseek_v3_t2048", "down"): (2483243008, _TRAFFIC_HASH),
     ("deepseek_t2048", "gateup_swiglu_fp8"): (3892582656, _TRAFFIC_HASH),
     ("deepseek_t2048", "down_fp8"): (2288754688, _TRAFFIC_HASH),
-    ("deepseek_e32_t256", "gateup_swiglu_fp8b"): (966384640, _TRAFFIC_HASH_FP8B),
-    ("deepseek_e32_t256", "down_fp8b"): (534975488, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t32", "gateup_swiglu_fp8b"): (944954880, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t32", "down_fp8b"): (474785536, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t4096", "gateup_swiglu_fp8b"): (1197870080, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t4096", "down_fp8b"): (780931072, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512", "gateup_swiglu_fp8b"): (1358057216, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512", "down_fp8b"): (616780288, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512_skew40", "gateup_swiglu_fp8b"): (973863680, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512_skew40", "down_fp8b"): (513936896, _TRAFFIC_HASH_FP8B),
-    ("deepseek_t2048", "gateup_swiglu_fp8b"): (3789366016, _TRAFFIC_HASH_FP8B),
-    ("deepseek_t2048", "down_fp8b"): (2342260224, _TRAFFIC_HASH_FP8B),
-    ("deepseek_v3_t2048", "gateup_swiglu_fp8b"): (2074135296, _TRAFFIC_HASH_FP8B),
-    ("deepseek_v3_t2048", "down_fp8b"): (1408561920, _TRAFFIC_HASH_FP8B),
+    ("deepseek_e32_t256", "gateup_swiglu_fp8b"): (966599936, _TRAFFIC_HASH_FP8B),
+    ("deepseek_e32_t256", "down_fp8b"): (535245568, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t32", "gateup_swiglu_fp8b"): (944946688, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t32", "down_fp8b"): (474656768, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t4096", "gateup_swiglu_fp8b"): (1091124480, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t4096", "down_fp8b"): (781382400, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512", "gateup_swiglu_fp8b"): (1188105984, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512", "down_fp8b"): (614691072, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512_skew40", "gateup_swiglu_fp8b"): (962396928, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512_skew40", "down_fp8b"): (514285056, _TRAFFIC_HASH_FP8B),
+    ("deepseek_t2048", "gateup_swiglu_fp8b"): (3806213120, _TRAFFIC_HASH_FP8B),
+    ("deepseek_t2048", "down_fp8b"): (2343941632, _TRAFFIC_HASH_FP8B),
+    ("deepseek_v3_t2048", "gateup_swiglu_fp8b"): (2076622848, _TRAFFIC_HASH_FP8B),
+    ("deepseek_v3_t2048", "down_fp8b"): (1408621312, _TRAFFIC_HASH_FP8B),
 }
 GEMM_SOURCES = ("mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm.cu",
                 "mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm_2sm.cu",
@@ -524,6 +525,8 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = measured_traffic(w.name, dom + ("_fp8b" if blocks else "_fp8" if fp8 else ""))
     kname = KERNEL_NAMES_FP8B[dom] if blocks else (KERNEL_NAMES_FP8[dom] if fp8 else KERNEL_NAMES[dom])
+    if blocks and fuse_h and dom == "gateup_swiglu":
+        kname = "grouped_gemm_fp8b_kernel<0, true>"
     pair_mode = 0 if blocks else (moe.gemm_pair_mode_fp8 if fp8 else moe.gemm_pair_mode)(
         w.T, w.d, w.f, w.E, w.k, 0 if dom == "gateup_swiglu" else 1)
     if pair_mode >= 1:  # SM-pair kernel, template <KIND, SWAPCAP, GATHER, FP8>
