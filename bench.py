@@ -16,9 +16,9 @@ ours (default):
                them (the same kernels moe_forward launches).
   e2e          tokens/s with x and logits copied from page-locked host memory, the layer and out
                copied back, every step, all inside the timed region: through moe_forward_host_batches
-               or its FP8 forms (softmax router: the K steps as K batches, copies overlapped with the
-               layers on two copy streams), else (DeepSeek-V3's router, or --flush-l2) the binding's
-               copies and layer per step on one stream.
+               or its FP8 / DeepSeek-V3-router forms (the K steps as K batches, copies overlapped with
+               the layers on two copy streams); with --flush-l2 the binding's copies and layer per
+               step on one stream.
   cpu_baseline the CPU oracle on a bounded sample of the same workload (rank 0, N=1 only).
 reference:
   the CPU oracle as the reference arm: each step is the oracle's forward on a bounded token
@@ -452,7 +452,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     # enqueued on the stream by the binding.
     xh, lh = x.pin_memory(), logits.pin_memory()
     oh = torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory()
-    batched = not grouped and flush is None
+    batched = flush is None
     if batched:
         ohs = [oh, torch.empty_like(oh).pin_memory()]
         wsize = moe.workspace_size_fp8b if blocks else moe.workspace_size_fp8 if fp8 else moe.workspace_size
@@ -462,7 +462,15 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
 
         def e2e_run(n):
             outs = [ohs[i & 1] for i in range(n)]
-            if fp8:
+            if grouped:
+                G, tg, sc = w.router[1:4]
+                if fp8:
+                    moe.forward_grouped_fp8_host_batches([xh] * n, [lh] * n, bias_d, *w8, w.k, G, tg, sc, outs, ws_b,
+                                                         stream, h2d, d2h, blocks=blocks)
+                else:
+                    moe.forward_grouped_host_batches([xh] * n, [lh] * n, bias_d, wgu, wd, w.k, G, tg, sc, outs, ws_b,
+                                                     stream, h2d, d2h)
+            elif fp8:
                 fwd = moe.forward_fp8b_host_batches if blocks else moe.forward_fp8_host_batches
                 fwd([xh] * n, [lh] * n, *w8, w.k, outs, ws_b, stream, h2d, d2h)
             else:
@@ -476,7 +484,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / args.steps
-        e2e_api = ("moe_forward_" + ("fp8b_" if blocks else "fp8_" if fp8 else "") +
+        e2e_api = ("moe_forward_" + ("grouped_" if grouped else "") + ("fp8b_" if blocks else "fp8_" if fp8 else "") +
                    "host_batches: K batches, copies on two copy streams beside the layers")
         if moe.get_device_error(ws_b) != 0:
             raise RuntimeError("device status word set during the e2e run")

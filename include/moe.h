@@ -243,6 +243,16 @@ MOE_API int moe_forward_host_batches(const void* const* x_hosts, const float* co
                                      size_t workspace_bytes, moe_stream_t stream, moe_stream_t h2d_stream,
                                      moe_stream_t d2h_stream);
 
+/* moe_forward_host_batches with DeepSeek-V3's router (moe_forward_grouped as the layer): bias [E]
+ * fp32 on the device and n_group, topk_group, scale as for moe_route_grouped; the rest as
+ * moe_forward_host_batches. */
+MOE_API int moe_forward_grouped_host_batches(const void* const* x_hosts, const float* const* logits_hosts,
+                                             const float* bias, const void* w_gate_up, const void* w_down,
+                                             int n_batches, int T, int d, int f, int E, int top_k, int n_group,
+                                             int topk_group, float scale, void* const* out_hosts, void* workspace,
+                                             size_t workspace_bytes, moe_stream_t stream, moe_stream_t h2d_stream,
+                                             moe_stream_t d2h_stream);
+
 /* Size of the fixed scratch array that moe_forward_noalloc uses (64 MiB). */
 #define MOE_NOALLOC_SCRATCH_BYTES (64ull * 1024ull * 1024ull)
 
@@ -419,6 +429,22 @@ MOE_API int moe_forward_fp8b_host_batches(const void* const* x_hosts, const floa
                                           const float* s_down, int n_batches, int T, int d, int f, int E, int top_k,
                                           void* const* out_hosts, void* workspace, size_t workspace_bytes,
                                           moe_stream_t stream, moe_stream_t h2d_stream, moe_stream_t d2h_stream);
+/* The same two with DeepSeek-V3's router (moe_forward_grouped_fp8 / moe_forward_grouped_fp8b as the
+ * layer; bias, n_group, topk_group, scale as for moe_route_grouped). */
+MOE_API int moe_forward_grouped_fp8_host_batches(const void* const* x_hosts, const float* const* logits_hosts,
+                                                 const float* bias, const void* w8_gate_up, const float* s_gate_up,
+                                                 const void* w8_down, const float* s_down, int n_batches, int T,
+                                                 int d, int f, int E, int top_k, int n_group, int topk_group,
+                                                 float scale, void* const* out_hosts, void* workspace,
+                                                 size_t workspace_bytes, moe_stream_t stream, moe_stream_t h2d_stream,
+                                                 moe_stream_t d2h_stream);
+MOE_API int moe_forward_grouped_fp8b_host_batches(const void* const* x_hosts, const float* const* logits_hosts,
+                                                  const float* bias, const void* w8_gate_up, const float* s_gate_up,
+                                                  const void* w8_down, const float* s_down, int n_batches, int T,
+                                                  int d, int f, int E, int top_k, int n_group, int topk_group,
+                                                  float scale, void* const* out_hosts, void* workspace,
+                                                  size_t workspace_bytes, moe_stream_t stream,
+                                                  moe_stream_t h2d_stream, moe_stream_t d2h_stream);
 
 /* The FP8 layers with DeepSeek-V3's router (moe_route_grouped) as step 1: bias [E] fp32, n_group,
  * topk_group and scale as for moe_route_grouped; everything else as for moe_forward_fp8 /

@@ -810,13 +810,14 @@ int moe_forward_host(const void* x_host, const float* logits_host, const void* w
     return ok();
 }
 
-int moe_forward_host_batches(const void* const* x_hosts, const float* const* logits_hosts, const void* w_gate_up,
-                             const void* w_down, int n_batches, int T, int d, int f, int E, int top_k,
-                             void* const* out_hosts, void* workspace, size_t workspace_bytes, moe_stream_t stream,
-                             moe_stream_t h2d_stream, moe_stream_t d2h_stream) {
-    const char* name = "moe_forward_host_batches";
+static int forward_host_batches(const void* const* x_hosts, const float* const* logits_hosts, const void* w_gate_up,
+                                const void* w_down, int n_batches, int T, int d, int f, int E, int top_k,
+                                void* const* out_hosts, void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                                moe_stream_t h2d_stream, moe_stream_t d2h_stream, const Router& router) {
+    const char* name = router.grouped ? "moe_forward_grouped_host_batches" : "moe_forward_host_batches";
     int rc = check_shape(T, d, f, E, top_k, true);
     if (rc) return rc;
+    if ((rc = check_router(router, E, top_k, name))) return rc;
     if (n_batches < 0) return fail(MOE_ERR_INVALID_ARG, "%s: n_batches = %d < 0", name, n_batches);
     if (T == 0 || n_batches == 0) return ok();
     if ((rc = check_host_batches(name, x_hosts, logits_hosts, out_hosts, n_batches))) return rc;
@@ -835,8 +836,32 @@ int moe_forward_host_batches(const void* const* x_hosts, const float* const* log
     return run_host_batches(name, x_hosts, logits_hosts, out_hosts, n_batches, T, d, E, need, workspace, s,
                             static_cast<cudaStream_t>(h2d_stream), static_cast<cudaStream_t>(d2h_stream),
                             [&](const void* x, const float* l, void* o) {
-                                return run_layer(x, l, w_gate_up, w_down, T, d, f, E, top_k, o, workspace, sms, s);
+                                return run_layer(x, l, w_gate_up, w_down, T, d, f, E, top_k, o, workspace, sms, s,
+                                                 router);
                             });
+}
+
+int moe_forward_host_batches(const void* const* x_hosts, const float* const* logits_hosts, const void* w_gate_up,
+                             const void* w_down, int n_batches, int T, int d, int f, int E, int top_k,
+                             void* const* out_hosts, void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                             moe_stream_t h2d_stream, moe_stream_t d2h_stream) {
+    return forward_host_batches(x_hosts, logits_hosts, w_gate_up, w_down, n_batches, T, d, f, E, top_k, out_hosts,
+                                workspace, workspace_bytes, stream, h2d_stream, d2h_stream, Router());
+}
+
+int moe_forward_grouped_host_batches(const void* const* x_hosts, const float* const* logits_hosts, const float* bias,
+                                     const void* w_gate_up, const void* w_down, int n_batches, int T, int d, int f,
+                                     int E, int top_k, int n_group, int topk_group, float scale,
+                                     void* const* out_hosts, void* workspace, size_t workspace_bytes,
+                                     moe_stream_t stream, moe_stream_t h2d_stream, moe_stream_t d2h_stream) {
+    Router r;
+    r.grouped = true;
+    r.bias = bias;
+    r.n_group = n_group;
+    r.topk_group = topk_group;
+    r.scale = scale;
+    return forward_host_batches(x_hosts, logits_hosts, w_gate_up, w_down, n_batches, T, d, f, E, top_k, out_hosts,
+                                workspace, workspace_bytes, stream, h2d_stream, d2h_stream, r);
 }
 
 int moe_forward_noalloc(const void* x, const float* logits, const void* w_gate_up, const void* w_down, int T,
@@ -1031,10 +1056,13 @@ static int forward8_host_batches(const void* const* x_hosts, const float* const*
                                  const float* s_gate_up, const void* w8_down, const float* s_down, int n_batches, int T,
                                  int d, int f, int E, int top_k, void* const* out_hosts, void* workspace,
                                  size_t workspace_bytes, moe_stream_t stream, moe_stream_t h2d_stream,
-                                 moe_stream_t d2h_stream, bool blocks) {
-    const char* name = blocks ? "moe_forward_fp8b_host_batches" : "moe_forward_fp8_host_batches";
+                                 moe_stream_t d2h_stream, bool blocks, const Router& router = Router()) {
+    const char* name = router.grouped ? (blocks ? "moe_forward_grouped_fp8b_host_batches"
+                                                : "moe_forward_grouped_fp8_host_batches")
+                                      : (blocks ? "moe_forward_fp8b_host_batches" : "moe_forward_fp8_host_batches");
     int rc = check_shape_fp8(T, d, f, E, top_k, name);
     if (rc) return rc;
+    if ((rc = check_router(router, E, top_k, name))) return rc;
     if (n_batches < 0) return fail(MOE_ERR_INVALID_ARG, "%s: n_batches = %d < 0", name, n_batches);
     if (T == 0 || n_batches == 0) return ok();
     if ((rc = check_host_batches(name, x_hosts, logits_hosts, out_hosts, n_batches))) return rc;
@@ -1054,7 +1082,7 @@ static int forward8_host_batches(const void* const* x_hosts, const float* const*
                             static_cast<cudaStream_t>(h2d_stream), static_cast<cudaStream_t>(d2h_stream),
                             [&](const void* x, const float* l, void* o) {
                                 return run_layer_fp8(x, l, w8_gate_up, s_gate_up, w8_down, s_down, T, d, f, E, top_k,
-                                                     o, workspace, sms, s, blocks, Router());
+                                                     o, workspace, sms, s, blocks, router);
                             });
 }
 
@@ -1084,6 +1112,28 @@ static Router grouped_router(const float* bias, int n_group, int topk_group, flo
     r.topk_group = topk_group;
     r.scale = scale;
     return r;
+}
+
+int moe_forward_grouped_fp8_host_batches(const void* const* x_hosts, const float* const* logits_hosts,
+                                         const float* bias, const void* w8_gate_up, const float* s_gate_up,
+                                         const void* w8_down, const float* s_down, int n_batches, int T, int d, int f,
+                                         int E, int top_k, int n_group, int topk_group, float scale,
+                                         void* const* out_hosts, void* workspace, size_t workspace_bytes,
+                                         moe_stream_t stream, moe_stream_t h2d_stream, moe_stream_t d2h_stream) {
+    return forward8_host_batches(x_hosts, logits_hosts, w8_gate_up, s_gate_up, w8_down, s_down, n_batches, T, d, f, E,
+                                 top_k, out_hosts, workspace, workspace_bytes, stream, h2d_stream, d2h_stream, false,
+                                 grouped_router(bias, n_group, topk_group, scale));
+}
+
+int moe_forward_grouped_fp8b_host_batches(const void* const* x_hosts, const float* const* logits_hosts,
+                                          const float* bias, const void* w8_gate_up, const float* s_gate_up,
+                                          const void* w8_down, const float* s_down, int n_batches, int T, int d,
+                                          int f, int E, int top_k, int n_group, int topk_group, float scale,
+                                          void* const* out_hosts, void* workspace, size_t workspace_bytes,
+                                          moe_stream_t stream, moe_stream_t h2d_stream, moe_stream_t d2h_stream) {
+    return forward8_host_batches(x_hosts, logits_hosts, w8_gate_up, s_gate_up, w8_down, s_down, n_batches, T, d, f, E,
+                                 top_k, out_hosts, workspace, workspace_bytes, stream, h2d_stream, d2h_stream, true,
+                                 grouped_router(bias, n_group, topk_group, scale));
 }
 
 int moe_forward_grouped_fp8(const void* x, const float* logits, const float* bias, const void* w8_gate_up,

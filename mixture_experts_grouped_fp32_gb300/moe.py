@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
+_F = ctypes.c_float
 _SIGS = {
     "moe_version": ([], _I),
     "moe_forward_launch_count": ([_I, _I, _I], _I),
@@ -43,6 +44,12 @@ _SIGS = {
     "moe_forward_host_batches": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P, _P], _I),
     "moe_forward_fp8_host_batches": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P, _P], _I),
     "moe_forward_fp8b_host_batches": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P, _P], _I),
+    "moe_forward_grouped_host_batches": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _SZ, _P,
+                                          _P, _P], _I),
+    "moe_forward_grouped_fp8_host_batches": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P,
+                                              _SZ, _P, _P, _P], _I),
+    "moe_forward_grouped_fp8b_host_batches": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P,
+                                               _SZ, _P, _P, _P], _I),
     "moe_get_device_error": ([_P, ctypes.POINTER(ctypes.c_int32)], _I),
     "moe_quantize_weights_fp8": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_permute_fp8": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
@@ -379,6 +386,40 @@ def forward_fp8b_host_batches(x_hosts, logits_hosts, w8_gate_up, s_gate_up, w8_d
     2 * host_staging_size() bytes."""
     return _forward8_host_batches("moe_forward_fp8b_host_batches", x_hosts, logits_hosts, w8_gate_up, s_gate_up,
                                   w8_down, s_down, top_k, out_hosts, workspace, stream, h2d_stream, d2h_stream)
+
+
+def forward_grouped_host_batches(x_hosts, logits_hosts, bias, w_gate_up, w_down, top_k, n_group, topk_group, scale,
+                                 out_hosts, workspace, stream=None, h2d_stream=None, d2h_stream=None):
+    """forward_host_batches with DeepSeek-V3's router (bias [E] fp32 on the device)."""
+    if len(x_hosts) == 0:
+        return out_hosts
+    _dev(w_gate_up, torch.bfloat16, "w_gate_up")
+    _dev(w_down, torch.bfloat16, "w_down")
+    _dev(bias, torch.float32, "bias")
+    E, _, f2 = w_gate_up.shape
+    n, T, d, xa, la, oa, h2d, d2h = _host_batch_args(x_hosts, logits_hosts, out_hosts, w_gate_up.device,
+                                                     h2d_stream, d2h_stream)
+    _call("moe_forward_grouped_host_batches", xa, la, _ptr(bias), _ptr(w_gate_up), _ptr(w_down), n, T, d, f2 // 2, E,
+          top_k, n_group, topk_group, float(scale), oa, _ptr(workspace), workspace.numel(), _stream(stream),
+          _stream(h2d), _stream(d2h))
+    return out_hosts
+
+
+def forward_grouped_fp8_host_batches(x_hosts, logits_hosts, bias, w8_gate_up, s_gate_up, w8_down, s_down, top_k,
+                                     n_group, topk_group, scale, out_hosts, workspace, stream=None, h2d_stream=None,
+                                     d2h_stream=None, blocks: bool = False):
+    """The FP8 layers (blocks=True: block scales) over host batches with DeepSeek-V3's router."""
+    if len(x_hosts) == 0:
+        return out_hosts
+    _dev(bias, torch.float32, "bias")
+    E, f2, _ = _w8_dims(w8_gate_up, "w8_gate_up")
+    n, T, d, xa, la, oa, h2d, d2h = _host_batch_args(x_hosts, logits_hosts, out_hosts, w8_gate_up.device,
+                                                     h2d_stream, d2h_stream)
+    sym = "moe_forward_grouped_fp8b_host_batches" if blocks else "moe_forward_grouped_fp8_host_batches"
+    _call(sym, xa, la, _ptr(bias), _ptr(w8_gate_up), _ptr(s_gate_up), _ptr(w8_down), _ptr(s_down), n, T, d, f2 // 2,
+          E, top_k, n_group, topk_group, float(scale), oa, _ptr(workspace), workspace.numel(), _stream(stream),
+          _stream(h2d), _stream(d2h))
+    return out_hosts
 
 
 def get_device_error(status_or_workspace: torch.Tensor) -> int:

@@ -135,6 +135,18 @@ def test_forward_fp8_host_batches_validates(lib, sym):
     assert "workspace" in _err(lib)
 
 
+def test_forward_grouped_host_batches_validates(lib):
+    p = ctypes.c_void_p(1 << 20)
+    arr = (ctypes.c_void_p * 2)(1 << 20, 1 << 21)
+    f = lib.moe_forward_grouped_host_batches
+    assert f(arr, arr, p, p, p, 0, 4, 64, 128, 8, 2, 4, 2, 1.0, arr, p, 1 << 40, None, None, None) == 0
+    assert f(arr, arr, None, p, p, 2, 4, 64, 128, 8, 2, 4, 2, 1.0, arr, p, 1 << 40, None, None, None) == -1  # bias
+    assert f(arr, arr, p, p, p, 2, 4, 64, 128, 8, 2, 3, 2, 1.0, arr, p, 1 << 40, None, None, None) == -1  # 8 % 3
+    g8 = lib.moe_forward_grouped_fp8b_host_batches
+    assert g8(arr, arr, p, p, p, p, p, 2, 4, 128, 128, 8, 2, 4, 5, 1.0, arr, p, 1 << 40, None, None, None) == -1
+    assert g8(arr, arr, p, p, p, p, p, 2, 4, 128, 128, 8, 2, 4, 2, 1.0, arr, p, 4096, None, None, None) == -3
+
+
 def test_stage_calls_reject_bad_arguments(lib):
     p = ctypes.c_void_p(1 << 20)
     assert lib.moe_route(None, 4, 8, 2, p, p, None) == -1

@@ -253,3 +253,41 @@ def test_forward_grouped_fp8_full_size(moe, oracle, blocks):
     ref = fwd(to_np_bits(x), ref_idx[sample], ref_w[sample], *r_gu, *r_d, sample)
     got = out[torch.from_numpy(sample).long().to(DEV)].float().cpu().numpy()
     assert_layer_close(got, ref, f"deepseek_v3_t2048 {'fp8b' if blocks else 'fp8'} sampled tokens {sample.tolist()}")
+
+
+@pytest.mark.parametrize("variant", ["bf16", "fp8", "fp8b"])
+def test_forward_grouped_host_batches_matches_forward(moe, variant):
+    """DeepSeek-V3's router over host batches with overlapped copies: each batch's output equals
+    the device call's."""
+    w = LAYER_CASES[0]
+    _, G, tg, scale, _ = w.router
+    dev = torch.device(DEV)
+    _, _, wgu, wd = case_inputs(w, seed=50)
+    bias = draw_router_bias(w, seed=50).to(dev)
+    if variant == "bf16":
+        wts = (wgu.to(dev), wd.to(dev))
+        fwd = lambda x, l: moe.forward_grouped(x, l, bias, *wts, w.k, G, tg, scale)
+        size = moe.workspace_size
+    else:
+        blocks = variant == "fp8b"
+        quant = moe.quantize_weights_fp8b if blocks else moe.quantize_weights_fp8
+        wts = quant(wgu.to(dev)) + quant(wd.to(dev))
+        fwd = lambda x, l: moe.forward_grouped_fp8(x, l, bias, *wts, w.k, G, tg, scale, blocks=blocks)
+        size = moe.workspace_size_fp8b if blocks else moe.workspace_size_fp8
+    xs, ls, refs = [], [], []
+    for i in range(3):
+        logits, x, _, _ = case_inputs(w, seed=60 + i)
+        xs.append(x.pin_memory())
+        ls.append(logits.pin_memory())
+        refs.append(fwd(x.to(dev), logits.to(dev)).cpu())
+    outs = [torch.full((w.T, w.d), -1.0, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    ws = torch.empty(size(w.T, w.d, w.f, w.E, w.k) + 2 * moe.host_staging_size(w.T, w.d, w.E), dtype=torch.uint8,
+                     device=dev)
+    if variant == "bf16":
+        moe.forward_grouped_host_batches(xs, ls, bias, *wts, w.k, G, tg, scale, outs, ws)
+    else:
+        moe.forward_grouped_fp8_host_batches(xs, ls, bias, *wts, w.k, G, tg, scale, outs, ws, blocks=variant == "fp8b")
+    torch.cuda.current_stream().synchronize()
+    assert moe.get_device_error(ws) == 0
+    for i in range(3):
+        assert torch.equal(outs[i].view(torch.int16), refs[i].view(torch.int16)), f"{variant} batch {i}"
