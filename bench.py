@@ -636,7 +636,7 @@ def run_reference(args, w: Workload, rank: int, world: int):
     fp8 = args.dtype == "e4m3" or blocks
     O, run = oracle_sample_runner(w, logits, x, wgu, wd, args.seed, fp8, blocks)
     n = args.steps + args.warmup
-    per_step = max(0.5, min(20.0, 150.0 / max(1, n)))
+    per_step = args.ref_step_s if args.ref_step_s else max(0.5, min(20.0, 150.0 / max(1, n)))
     S = pick_sample(run, w.T, per_step)
     R = passes_for(run, S, per_step)
     for _ in range(args.warmup):
@@ -678,6 +678,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0, help="oracle CPU-baseline sample size, seconds")
+    ap.add_argument("--ref-step-s", type=float, default=None,
+                    help="--impl reference: CPU seconds per step (default: ~150 s over all steps, 0.5..20 per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3", "e4m3b"],
                     help="operands of the grouped GEMMs: bf16 (moe_forward), e4m3 (moe_forward_fp8) or e4m3 with "
