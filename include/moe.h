@@ -21,8 +21,10 @@
  *     never frees anything and keeps no pointer after a call returns.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls enqueue work on it
  *     and return without synchronising, except moe_get_device_error, which reads back.
- *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code.  On any error nothing is launched
- *     and moe_last_error_string() (per calling thread) says why.
+ *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code, and moe_last_error_string() (per
+ *     calling thread) says why.  On an argument, shape, workspace or device error nothing is
+ *     launched; a *_host_batches call whose enqueueing fails at batch b has enqueued the batches
+ *     before b.
  *   - Shape limits: 1 <= E <= 256, 1 <= top_k <= min(E, 8), T >= 0 (T = 0 launches nothing),
  *     d and f multiples of 64 in [64, 65536], T * top_k < 2^31 and every buffer < 2^31 rows.
  *   - Only devices of compute capability 10.3 (GB300) are supported: MOE_ERR_UNSUPPORTED else.
