@@ -108,6 +108,82 @@ quantize_weights_kernel(const uint16_t* __restrict__ W, int K, int N, uint8_t* _
     }
 }
 
+// The same quantisation of W [E, K, N] bf16 (16-byte aligned; N % 64 == 0, K % 128 == 0) in three
+// steps with 16-byte loads.  1) Column maxima over K chunks: CTA (256 columns, 256 K rows, e), a
+// thread 8 columns of every 8th row, the chunk's maxima merged into colmax[e][n] (zeroed first) by
+// an integer atomicMax on the float bits, which orders non-negative floats as floats.
+constexpr int kCmCols = 256, kCmRows = 256;
+__global__ void __launch_bounds__(kQThreads)
+weights_colmax_kernel(const uint4* __restrict__ W, int K, int N, unsigned int* __restrict__ colmax) {
+    __shared__ float red[kQThreads / 32][kCmCols];
+    const int e = blockIdx.z, n0 = blockIdx.x * kCmCols, k0 = blockIdx.y * kCmRows;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // column group, row phase
+    const int c8 = n0 + 8 * tx;
+    float m[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    if (c8 < N) {
+        const int k1 = min(K, k0 + kCmRows);
+        const uint4* col = W + (static_cast<size_t>(e) * K * N + c8) / 8;
+        for (int k = k0 + ty; k < k1; k += kQThreads / 32) {
+            const uint4 p = __ldg(col + static_cast<size_t>(k) * (N / 8));
+            const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                m[2 * i] = fmaxf(m[2 * i], fabsf(bf16_lo(w[i])));
+                m[2 * i + 1] = fmaxf(m[2 * i + 1], fabsf(bf16_hi(w[i])));
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red[ty][8 * tx + i] = m[i];
+    __syncthreads();
+    const int c = threadIdx.x;  // one column of the CTA's 256
+    if (n0 + c < N) {
+        float a = 0.0f;
+#pragma unroll
+        for (int r = 0; r < kQThreads / 32; ++r) a = fmaxf(a, red[r][c]);
+        atomicMax(colmax + static_cast<size_t>(e) * N + n0 + c, __float_as_uint(a));
+    }
+}
+
+// 2) One 8 KB output block per CTA (64 output columns x 128 K of expert e): the 128 x 64 tile read
+// row by row (16-byte loads), converted with its columns' 448 / max, transposed through shared
+// memory and written as 64 contiguous 128-byte rows.
+__global__ void __launch_bounds__(kQThreads)
+weights_tile_kernel(const uint4* __restrict__ W, int K, int N, const float* __restrict__ colmax,
+                    uint8_t* __restrict__ Wq) {
+    __shared__ float inv[64];
+    __shared__ __align__(16) uint8_t tile[64][128 + 16];
+    const int e = blockIdx.z, n0 = blockIdx.x * 64, k0 = blockIdx.y * 128;
+    if (threadIdx.x < 64) inv[threadIdx.x] = fp8_inv(colmax[static_cast<size_t>(e) * N + n0 + threadIdx.x]);
+    __syncthreads();
+    const uint4* src = W + (static_cast<size_t>(e) * K * N + static_cast<size_t>(k0) * N + n0) / 8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // 128 rows x 8 uint4 = 1024 loads, 4 a thread
+        const int v = threadIdx.x + j * kQThreads, kk = v >> 3, g = v & 7;
+        const uint4 p = __ldg(src + static_cast<size_t>(kk) * (N / 8) + g);
+        const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            tile[8 * g + 2 * i][kk] = to_e4m3(bf16_lo(w[i]) * inv[8 * g + 2 * i]);
+            tile[8 * g + 2 * i + 1][kk] = to_e4m3(bf16_hi(w[i]) * inv[8 * g + 2 * i + 1]);
+        }
+    }
+    __syncthreads();
+    uint8_t* dst = Wq + static_cast<size_t>(e) * N * K + static_cast<size_t>(n0) * K + static_cast<size_t>(k0 >> 7) * 8192;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {  // 512 uint4 of output, 2 a thread
+        const int v = threadIdx.x + j * kQThreads, c = v >> 3, q = v & 7;
+        reinterpret_cast<uint4*>(dst)[v] = *reinterpret_cast<const uint4*>(&tile[c][16 * q]);
+    }
+}
+
+// 3) Column maxima -> scales in place.
+__global__ void __launch_bounds__(kQThreads)
+colmax_to_scale_kernel(float* __restrict__ scale, int n) {
+    const int i = blockIdx.x * kQThreads + threadIdx.x;
+    if (i < n) scale[i] = fp8_scale(scale[i]);
+}
+
 // Blockwise rows: one CTA per output row r (source row src[r], or r), 128-wide blocks of C
 // (C % 128 == 0) -> codes and one power-of-two scale per block, scale [R, C/128].  Half a warp per
 // block (16 lanes x 8 values); a warp takes two blocks at a time.
@@ -211,8 +287,22 @@ cudaError_t launch_quantize_rows_fp8(const __nv_bfloat16* a, const int32_t* src,
 
 cudaError_t launch_quantize_weights_fp8(const __nv_bfloat16* W, int E, int K, int N, uint8_t* Wq, float* scale,
                                         cudaStream_t s) {
-    const dim3 grid((N + kWCols - 1) / kWCols, E);
-    quantize_weights_kernel<<<grid, kQThreads, 0, s>>>(reinterpret_cast<const uint16_t*>(W), K, N, Wq, scale);
+    if (reinterpret_cast<uintptr_t>(W) & 15u) {  // 16-byte loads need an aligned W: the two-pass kernel
+        const dim3 grid((N + kWCols - 1) / kWCols, E);
+        quantize_weights_kernel<<<grid, kQThreads, 0, s>>>(reinterpret_cast<const uint16_t*>(W), K, N, Wq, scale);
+        return cudaGetLastError();
+    }
+    // scale holds the column maxima (as bits) until the last step turns them into scales.
+    cudaError_t e = cudaMemsetAsync(scale, 0, static_cast<size_t>(E) * N * sizeof(float), s);
+    if (e != cudaSuccess) return e;
+    const uint4* W4 = reinterpret_cast<const uint4*>(W);
+    weights_colmax_kernel<<<dim3((N + kCmCols - 1) / kCmCols, (K + kCmRows - 1) / kCmRows, E), kQThreads, 0, s>>>(
+        W4, K, N, reinterpret_cast<unsigned int*>(scale));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    weights_tile_kernel<<<dim3(N / 64, K / 128, E), kQThreads, 0, s>>>(W4, K, N, scale, Wq);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int n = E * N;
+    colmax_to_scale_kernel<<<(n + kQThreads - 1) / kQThreads, kQThreads, 0, s>>>(scale, n);
     return cudaGetLastError();
 }
 
