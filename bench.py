@@ -1,6 +1,7 @@
 """Benchmark of the MoE layer forward on GB300: prints ONE JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--dtype bf16|e4m3|e4m3b] [--flush-l2] [--no-cpu-baseline]
 
 A step is one pass of the whole layer (route -> permute -> gate+up/SwiGLU GEMM -> down GEMM ->
 combine) over one batch of seeded synthetic input.  Default workload: the Mixtral-8x7B-shaped
@@ -9,8 +10,9 @@ decode-like batch (T=32, d=4096, f=14336, E=8, top-2).
 ours (default):
   value        tokens/s with inputs resident in HBM: K steps of moe_forward, CUDA events around each
                step on its stream (K defaults to ~0.5 s of device time; nvidia-smi samples the SM
-               clock and throttle reasons every 20 ms during that region).  The weights of every workload (>= 2.8 GB) exceed the 129 MB L2,
-               so they stream from HBM each step; --flush-l2 also writes 512 MB between steps.
+               clock and throttle reasons every 20 ms during that region).  The weights of every
+               workload (>= 2.8 GB) exceed the 129 MB L2, so they stream from HBM each step;
+               --flush-l2 also writes 512 MB between steps.
   roofline     the dominant kernel: its algorithmic bytes (or FLOPs) per launch / its mean duration,
                from a second K-step loop that calls the five stage entry points with events between
                them (the same kernels moe_forward launches).
@@ -22,10 +24,12 @@ ours (default):
   cpu_baseline the CPU oracle on a bounded sample of the same workload (rank 0, N=1 only).
 reference:
   the CPU oracle as the reference arm: each step is the oracle's forward on a bounded token
-  sample of the same workload, timed on the host cores.
+  sample of the same workload (repeated to fill --ref-step-s seconds, by default ~150 s over
+  all steps), timed on the host cores.
 --dtype e4m3 times the FP8 variant instead (moe_forward_fp8: the grouped GEMMs on E4M3 codes with
 per-row / per-output-channel scales; weights quantised once before the timed region), with the
-same metric, and the FP8 oracle as CPU baseline and reference arm.
+same metric, and the FP8 oracle as CPU baseline and reference arm; --dtype e4m3b the blockwise
+variant (moe_forward_fp8b: power-of-two scales per 1x128 activation and 128x128 weight block).
 Under torchrun (N > 1) each rank runs an independent replica of the layer on its own GPU (the
 layer has no cross-rank exchange); value = tokens of all ranks / max-over-ranks time.
 """
