@@ -4,8 +4,14 @@
                     [--dtype bf16|e4m3|e4m3b] [--flush-l2] [--no-cpu-baseline]
 
 A step is one pass of the whole layer (route -> permute -> gate+up/SwiGLU GEMM -> down GEMM ->
-combine) over one batch of seeded synthetic input.  Default workload: the Mixtral-8x7B-shaped
-decode-like batch (T=32, d=4096, f=14336, E=8, top-2).
+combine) over one batch of seeded synthetic input.  Default (headline) workload: the
+Mixtral-8x7B-shaped large batch (T=4096, d=4096, f=14336, E=8, top-2), the largest configuration of
+the metric's T=32..4096 range and the tensor-bound one.  The same JSON line carries `per_workload`:
+the other configurations (Mixtral T=32, T=512, T=512 with 40 % of assignments on one expert, the
+DeepSeek-V3-shaped routed experts with the softmax router and with DeepSeek-V3's own router), each
+measured in the same process the same way (steps, roofline, layer roofline, e2e, clocks), one after
+the other; `--per-workload none` turns them off.  `timed_region_s` is the headline's timed region
+(wall clock), `timed_region_s_all_workloads` the sum over every workload's.
 
 ours (default):
   value        tokens/s with inputs resident in HBM: K steps of moe_forward, CUDA events around each
@@ -15,7 +21,9 @@ ours (default):
                --flush-l2 also writes 512 MB between steps.
   roofline     the dominant kernel: its algorithmic bytes (or FLOPs) per launch / its mean duration,
                from a second K-step loop that calls the five stage entry points with events between
-               them (the same kernels moe_forward launches).
+               them (the same kernels moe_forward launches).  `traffic` is the kernel's DRAM bytes
+               per launch from an earlier ncu capture of the same kernel source (`traffic_source`
+               says so and names the source hash); null once the source has changed since.
   e2e          tokens/s with x and logits copied from page-locked host memory, the layer and out
                copied back, every step, all inside the timed region: through moe_forward_host_batches
                or its FP8 / DeepSeek-V3-router forms (the K steps as K batches, copies overlapped with
@@ -55,7 +63,8 @@ from mixture_experts_grouped_fp32_gb300.workloads import (WORKLOADS, Workload, b
                                                           make_inputs)
 
 METRIC = "MoE-layer tokens/s and TFLOP/s, % of roofline (1×GB300), T=32..4096"
-DEFAULT_WORKLOAD = "mixtral_t32"
+DEFAULT_WORKLOAD = "mixtral_t4096"
+PER_WORKLOAD = ("mixtral_t32", "mixtral_t512", "mixtral_t512_skew40", "deepseek_t2048", "deepseek_v3_t2048")
 L2_FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 STAGES = ("route", "permute", "gateup_swiglu", "down", "combine")
@@ -75,12 +84,13 @@ KERNEL_NAMES_FP8B = {"gateup_swiglu": "grouped_gemm_fp8b_kernel<0, false>",
                      "down": "grouped_gemm_fp8b_kernel<1, false>"}
 FP8_OVER_BF16 = 2.0  # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s) applied to the measured bf16 peak
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum per launch) from ncu captures of the
-# kernel source with the recorded hash (profiles/grouped_gemm_*.md); reported only while the GEMM
-# source still hashes to that value, else null.
 # Default timed region (no --steps): about this much device time, within these step counts.
 AUTO_TIMED_S = 0.5
 AUTO_STEPS_MIN, AUTO_STEPS_MAX = 50, 4000
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum per launch) from ncu captures of the
+# kernel source with the recorded hash; reported only while the GEMM source still hashes to that
+# value, else null.
 
 _TRAFFIC_HASH = "a8d3a7a96e328c09"  # GEMM source hash the captures below were taken at
 _TRAFFIC_HASH_FP8B = "f00c09d6f20a7ae5"  # ... and that of the blockwise FP8 kernel's sources
@@ -146,9 +156,15 @@ def gemm_source_hash(sources=GEMM_SOURCES) -> str:
 
 
 def measured_traffic(workload: str, stage: str):
+    """(bytes per launch, where the figure comes from): a stored ncu capture of this kernel source."""
     rec = MEASURED_TRAFFIC.get((workload, stage))
     sources = FP8B_SOURCES if stage.endswith("_fp8b") else GEMM_SOURCES
-    return rec[0] if rec and rec[1] == gemm_source_hash(sources) else None
+    h = gemm_source_hash(sources)
+    if rec and rec[1] == h:
+        return rec[0], (f"stored ncu capture (dram__bytes_read.sum + dram__bytes_write.sum, one launch) of this "
+                        f"kernel source, hash {h}; not measured in this run")
+    why = "no capture of this workload" if not rec else f"source changed since the capture (hash {rec[1]} -> {h})"
+    return None, f"null: {why}"
 
 
 def load_peaks():
@@ -535,7 +551,8 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         achieved = sw[dom]["bytes"] / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = measured_traffic(w.name, dom + ("_fp8b" if blocks else "_fp8" if fp8 else ""))
+    roof["traffic"], roof["traffic_source"] = measured_traffic(w.name, dom + ("_fp8b" if blocks else "_fp8" if fp8
+                                                                               else ""))
     kname = KERNEL_NAMES_FP8B[dom] if blocks else (KERNEL_NAMES_FP8[dom] if fp8 else KERNEL_NAMES[dom])
     if blocks and fuse_h and dom == "gateup_swiglu":
         kname = "grouped_gemm_fp8b_kernel<0, true>"
@@ -552,7 +569,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     layer_roof_ms = 1e3 * max(lw["bytes"] / (peaks["hbm_gbs"] * 1e9), lw["flops"] / (tensor_peak * 1e12))
 
     return {
-        "ms": ms_max, "tokens_per_rank": w.T, "t_wall": t_wall, "clocks": clocks, "stage_ms": stage_ms,
+        "ms": ms_max, "steps": args.steps, "tokens_per_rank": w.T, "t_wall": t_wall, "clocks": clocks, "stage_ms": stage_ms,
         "staged_step_ms": staged_step_ms, "e2e_ms": e2e_ms, "e2e_api": e2e_api, "roofline": roof, "layer": lw,
         "layer_roof_ms": layer_roof_ms, "n_active": n_active, "max_load": int(counts.max()),
         "host_weights": (wgu, wd), "inputs": (logits, x), "step_ms_p10_p90": (
@@ -688,6 +705,9 @@ def main():
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3", "e4m3b"],
                     help="operands of the grouped GEMMs: bf16 (moe_forward), e4m3 (moe_forward_fp8) or e4m3 with "
                          "block scales (moe_forward_fp8b)")
+    ap.add_argument("--per-workload", default=",".join(PER_WORKLOAD),
+                    help="comma-separated workloads also measured in this process and reported under per_workload "
+                         "(default: %(default)s), or 'none'")
     ap.add_argument("--flush-l2", action="store_true",
                     help="write a 512 MB buffer between steps (default: rely on inputs larger than L2)")
     args = ap.parse_args()
@@ -697,6 +717,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     w = WORKLOADS[args.workload]
+    unknown = [n for n in args.per_workload.split(",") if n and n != "none" and n not in WORKLOADS]
+    if unknown:
+        ap.error(f"--per-workload: unknown workload(s) {unknown}")
 
     if args.impl == "reference":
         if args.steps is None:
@@ -711,39 +734,70 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
+    steps_arg = args.steps
+    t_bench0 = time.perf_counter()
     r = run_ours(args, w, rank, world, dist)
+    line = result_line(r, w, args, world) if rank == 0 else None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        logits, x = r["inputs"]
+        wgu, wd = (t.cpu() for t in r["host_weights"])
+        line["cpu_baseline"] = cpu_baseline(w, logits, x, wgu, wd, args.cpu_budget_s, args.seed,
+                                            args.dtype != "bf16", args.dtype == "e4m3b")
+        del wgu, wd
+    timed_s = r["t_wall"]
+    del r
+    names = [] if args.per_workload == "none" else [n for n in args.per_workload.split(",") if n and n != w.name]
+    per = {}
+    for name in names:
+        torch.cuda.empty_cache()
+        args.steps = steps_arg  # each workload takes its own K when --steps is not given
+        wl = WORKLOADS[name]
+        rr = run_ours(args, wl, rank, world, dist)
+        timed_s += rr["t_wall"]
+        if rank == 0:
+            full = result_line(rr, wl, args, world)
+            per[name] = {key: full[key] for key in (
+                "value", "unit", "ms_per_step", "steps", "tflops", "layer_roofline", "roofline", "e2e", "clocks",
+                "stage_ms", "step_ms_p10_p90", "active_experts", "max_expert_load", "gpu_launches")}
+            per[name]["config"] = {key: full["config"][key] for key in (
+                "T", "d_model", "d_ff", "experts", "top_k", "logit_bias", "router")}
+        del rr
     if rank == 0:
-        tok_s = job_tokens_per_s(r["tokens_per_rank"], world, r["ms"])
-        tflops = r["layer"]["flops"] * world / (r["ms"] * 1e-3) / 1e12
-        line = {
-            "metric": METRIC, "value": round(tok_s, 2), "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"], 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
-            "data": "synthetic (seeded)", "config": config_of(w, args),
-            "tflops": round(tflops, 2),
-            "layer_roofline": {"ms": round(r["layer_roof_ms"], 4), "frac": round(r["layer_roof_ms"] / r["ms"], 4),
-                               "bytes": r["layer"]["bytes"], "flops": r["layer"]["flops"],
-                               "peaks": r["peak_src"]},
-            "roofline": r["roofline"],
-            "stage_ms": {k: round(v, 4) for k, v in r["stage_ms"].items()},
-            "staged_step_ms": round(r["staged_step_ms"], 4),
-            "step_ms_p10_p90": [round(v, 4) for v in r["step_ms_p10_p90"]],
-            "active_experts": r["n_active"], "max_expert_load": r["max_load"], "down_ksplit": r["ksplit"],
-            "e2e": {"value": round(w.T / (r["e2e_ms"] * 1e-3), 2), "unit": "tokens/s",
-                    "h2d_bytes_per_step": w.T * w.d * 2 + w.T * w.E * 4, "d2h_bytes_per_step": w.T * w.d * 2,
-                    "ms_per_step": round(r["e2e_ms"], 4), "api": r["e2e_api"]},
-            "gpu_launches": r["launches_per_step"] * args.steps,
-            "clocks": r["clocks"],
-        }
-        if world == 1 and not args.no_cpu_baseline:
-            logits, x = r["inputs"]
-            wgu, wd = (t.cpu() for t in r["host_weights"])
-            line["cpu_baseline"] = cpu_baseline(w, logits, x, wgu, wd, args.cpu_budget_s, args.seed,
-                                                args.dtype != "bf16", args.dtype == "e4m3b")
+        if per:
+            line["per_workload"] = per
+        line["timed_region_s_all_workloads"] = round(timed_s, 3)
+        line["bench_wall_s"] = round(time.perf_counter() - t_bench0, 1)
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def result_line(r: dict, w: Workload, args, world: int) -> dict:
+    """The JSON fields of one workload's measurement (rank 0)."""
+    tok_s = job_tokens_per_s(r["tokens_per_rank"], world, r["ms"])
+    tflops = r["layer"]["flops"] * world / (r["ms"] * 1e-3) / 1e12
+    return {
+        "metric": METRIC, "value": round(tok_s, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": r["steps"], "warmup": args.warmup, "ms_per_step": round(r["ms"], 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
+        "data": "synthetic (seeded)", "config": config_of(w, args),
+        "tflops": round(tflops, 2),
+        "layer_roofline": {"ms": round(r["layer_roof_ms"], 4), "frac": round(r["layer_roof_ms"] / r["ms"], 4),
+                           "bytes": r["layer"]["bytes"], "flops": r["layer"]["flops"],
+                           "peaks": r["peak_src"]},
+        "roofline": r["roofline"],
+        "stage_ms": {k: round(v, 4) for k, v in r["stage_ms"].items()},
+        "staged_step_ms": round(r["staged_step_ms"], 4),
+        "step_ms_p10_p90": [round(v, 4) for v in r["step_ms_p10_p90"]],
+        "active_experts": r["n_active"], "max_expert_load": r["max_load"], "down_ksplit": r["ksplit"],
+        "e2e": {"value": round(w.T / (r["e2e_ms"] * 1e-3), 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": w.T * w.d * 2 + w.T * w.E * 4, "d2h_bytes_per_step": w.T * w.d * 2,
+                "ms_per_step": round(r["e2e_ms"], 4), "api": r["e2e_api"]},
+        "gpu_launches": r["launches_per_step"] * r["steps"],
+        "clocks": r["clocks"],
+        "timed_region_s": round(r["t_wall"], 3),
+    }
 
 
 if __name__ == "__main__":

@@ -83,7 +83,9 @@ MOE_API int moe_workspace_layout(int T, int d, int f, int E, int top_k, size_t* 
  * Routing on the device with no host synchronisation: "Triton MoE 核心擊敗 Megablocks"
  * (setupai.cc), section 技術深入, the dynamic-routing bullet.  The pages do not define the
  * router function; softmax-then-top-k-renormalised is the reading used throughout.
- * Logits must be finite (NaN/inf are outside the contract). */
+ * Weights are defined for finite logits only.  The ids stay well defined for any input: a NaN
+ * logit ranks below every number (-inf included), NaNs among themselves by ascending id, so no
+ * expert is chosen twice for one token. */
 MOE_API int moe_route(const float* logits, int T, int E, int top_k, int32_t* idx, float* w,
               moe_stream_t stream);
 
@@ -259,23 +261,25 @@ MOE_API int moe_forward_grouped_host_batches(const void* const* x_hosts, const f
 #define MOE_NOALLOC_SCRATCH_BYTES (64ull * 1024ull * 1024ull)
 
 /* moe_forward without a caller-provided workspace and without allocating anything.
- * The pages have no counterpart to this call; it exists for callers that cannot allocate device
- * memory when they run the layer: code that runs while a stream is being captured into a CUDA
- * graph (allocation is not allowed there), inference servers whose device memory is carved up in
- * advance so that no extra pool is available, and plugins inside a host framework whose
- * allocator they cannot reach.  Such callers pass only the layer's inputs and output.
+ * The pages have no counterpart to this call.  It is for callers that cannot allocate device
+ * memory at the moment they run the layer: inference servers that carve all device memory into
+ * fixed pools at start-up and have none left to hand out, plugins inside a host framework whose
+ * allocator they cannot reach, and latency-critical paths where a cudaMalloc (which can
+ * synchronise the device) is not acceptable.  Such callers pass only the layer's inputs and output.
  *   x [T,d] bf16, logits [T,E] fp32, w_gate_up [E,d,2f] bf16, w_down [E,f,d] bf16 in;
  *   out [T,d] bf16 out — device pointers, same meaning and layout as moe_forward.
  * The intermediates live in one file-scope device array of MOE_NOALLOC_SCRATCH_BYTES that every
  * GPU loading this library holds until the process exits.  Shapes whose moe_workspace_size()
  * exceeds it are rejected with MOE_ERR_WORKSPACE (e.g. the Mixtral-8x7B shape fits up to
- * T = 629 tokens with top-2).  The first call on a device looks up the array's device address
+ * T = 629 tokens with top-2).  The first call on a device (and the first after that device's
+ * context was destroyed and created again) looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream
- * capture.  All calls on a device share the one array and it keeps the last call's contents
- * (every intermediate is rewritten before it is read; the status word is reset by the first
- * kernel), so calls whose work overlaps on the GPU — on different streams, or from different
- * threads without ordering — race with each other: serialise them.  The device status word is
- * kept inside the array and is not readable through moe_get_device_error.
+ * capture.  Device ordinals >= 64 are rejected with MOE_ERR_UNSUPPORTED.  All calls on a device
+ * share the one array and it keeps the last call's contents (every intermediate is rewritten
+ * before it is read; the status word is reset by the first kernel), so calls whose work overlaps
+ * on the GPU — on different streams, or from different threads without ordering — race with each
+ * other: serialise them.  The device status word sits at the start of the array;
+ * moe_get_device_error(NULL, &code) reads it for the current device.
  * Returns MOE_OK or an MOE_ERR_* code as moe_forward does. */
 MOE_API int moe_forward_noalloc(const void* x, const float* logits, const void* w_gate_up,
                                 const void* w_down, int T, int d, int f, int E, int top_k,
@@ -462,7 +466,9 @@ MOE_API int moe_forward_grouped_fp8b(const void* x, const float* logits, const f
                                      void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /* Reads (synchronously: cudaMemcpy) a device status word — a stage call's `status` pointer, or
- * the workspace of moe_forward — into *code (0 = no device-side error). */
+ * the workspace of moe_forward — into *code (0 = no device-side error).  With
+ * status_or_workspace = NULL it reads the status word of moe_forward_noalloc's fixed array on the
+ * current device (the last noalloc call's). */
 MOE_API int moe_get_device_error(const void* status_or_workspace, int32_t* code);
 
 /* Number of kernel launches one moe_forward call makes for this shape: 4 when routing and the

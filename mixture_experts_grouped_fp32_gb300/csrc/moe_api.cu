@@ -469,18 +469,51 @@ namespace moe {
 namespace {
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[64] = {};
+constexpr int kNoallocMaxDevices = 64;
+// Per device: the array's device address and the CUDA context it was looked up in.  A context
+// destroyed and created again (cudaDeviceReset, or the primary context released and retained)
+// loads the module again, and the array can move; the address is then looked up afresh.
+void* g_noalloc_ptr[kNoallocMaxDevices] = {};
+void* g_noalloc_ctx[kNoallocMaxDevices] = {};
 
-// Device address of moe_noalloc_scratch on device `dev` (current), looked up once per device.
-// In host code the array's name is only a host-side handle, never a device address.
+// The current thread's CUDA context (driver cuCtxGetCurrent, reached through the runtime's
+// entry-point query so that the library needs no link against libcuda).
+int current_context(void** ctx) {
+    using GetCurrent = int (*)(void**);
+    static GetCurrent fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<GetCurrent>(p);
+    });
+    *ctx = nullptr;
+    if (!fn) return fail(MOE_ERR_CUDA, "moe_forward_noalloc: driver entry point cuCtxGetCurrent not found");
+    if (fn(ctx) != 0 || *ctx == nullptr)
+        return fail(MOE_ERR_CUDA, "moe_forward_noalloc: no current CUDA context");
+    return MOE_OK;
+}
+
+// Device address of moe_noalloc_scratch on device `dev` (current), looked up with that device
+// current the first time a context of it is seen.  In host code the array's name is only a
+// host-side handle, never a device address.
 int noalloc_scratch(int dev, void** out) {
+    if (dev < 0 || dev >= kNoallocMaxDevices)
+        return fail(MOE_ERR_UNSUPPORTED, "moe_forward_noalloc: device ordinal %d is beyond the %d this library tracks",
+                    dev, kNoallocMaxDevices);
+    void* ctx = nullptr;
+    int rc = current_context(&ctx);
+    if (rc) return rc;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_ptr[dev] == nullptr) {
+    if (g_noalloc_ptr[dev] == nullptr || g_noalloc_ctx[dev] != ctx) {
         void* p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, moe_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr)
             return fail(MOE_ERR_CUDA, "moe_forward_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
         g_noalloc_ptr[dev] = p;
+        g_noalloc_ctx[dev] = ctx;
     }
     *out = g_noalloc_ptr[dev];
     return MOE_OK;
@@ -1260,7 +1293,16 @@ int moe_forward_fp8b(const void* x, const float* logits, const void* w8_gate_up,
 }
 
 int moe_get_device_error(const void* status_or_workspace, int32_t* code) {
-    if (!status_or_workspace || !code) return fail(MOE_ERR_INVALID_ARG, "moe_get_device_error: null pointer");
+    if (!code) return fail(MOE_ERR_INVALID_ARG, "moe_get_device_error: null pointer");
+    if (!status_or_workspace) {  // the status word of moe_forward_noalloc's array on the current device
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "moe_get_device_error: %s", cudaGetErrorString(e));
+        void* ws = nullptr;
+        int rc = noalloc_scratch(dev, &ws);
+        if (rc) return rc;
+        status_or_workspace = static_cast<const unsigned char*>(ws) + layout(1, 64, 64, 1, 1).status;
+    }
     cudaError_t e = cudaMemcpy(code, status_or_workspace, sizeof(int32_t), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "moe_get_device_error: %s", cudaGetErrorString(e));
     return ok();

@@ -238,7 +238,9 @@ permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int
 constexpr int kFuseMaxE = 32;
 
 __device__ __forceinline__ bool logit_before(float av, int ai, float bv, int bi) {
-    return av > bv || (av == bv && ai < bi);
+    const bool an = av != av, bn = bv != bv;  // a NaN ranks below every number, NaNs by id
+    if (an != bn) return bn;
+    return av > bv || ((av == bv || an) && ai < bi);
 }
 
 __global__ void __launch_bounds__(kPermThreads)

@@ -19,11 +19,14 @@ constexpr int kRouteWarps = 8;  // tokens per 256-thread block
 constexpr int kMaxK = 8;
 
 // Does candidate (av, ai) rank before (bv, bi)?  Larger logit first, lower id on equal logits;
-// id INT_MAX marks "no candidate".
+// id INT_MAX marks "no candidate".  A NaN ranks below every number (NaNs among themselves by id),
+// so the order stays total and no expert can win two slots of one token.
 __device__ __forceinline__ bool ranks_before(float av, int ai, float bv, int bi) {
     if (ai == INT_MAX) return false;
     if (bi == INT_MAX) return true;
-    return av > bv || (av == bv && ai < bi);
+    const bool an = av != av, bn = bv != bv;
+    if (an != bn) return bn;
+    return av > bv || ((av == bv || an) && ai < bi);
 }
 
 // EPL = experts held per lane (ceil(E / 32)), expert e lives in lane e % 32, register e / 32.
@@ -63,8 +66,8 @@ route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __r
                     bv = v[i];
                     bi = lane + 32 * i;
                 }
-            // Butterfly arg-max: ranks_before is a strict total order on distinct ids, so every
-            // lane ends with the same winner.
+            // Butterfly arg-max: ranks_before is a strict total order on distinct ids (NaN
+            // included), so every lane ends with the same winner.
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
                 const float ov = __shfl_xor_sync(0xffffffffu, bv, off);

@@ -198,8 +198,14 @@ int oracle_route(const float* logits, int T, int E, int k, int32_t* idx, float* 
     for (int t = 0; t < T; ++t) {
         const float* l = logits + static_cast<size_t>(t) * E;
         // Sort expert ids by logit, largest first; stable, so equal logits keep ascending id.
+        // A NaN logit ranks below every number (the NaNs keep ascending id among themselves), which
+        // keeps the comparison a strict weak order; the weights of a row with a NaN are undefined.
         std::iota(order.begin(), order.end(), 0);
-        std::stable_sort(order.begin(), order.end(), [l](int a, int b) { return l[a] > l[b]; });
+        std::stable_sort(order.begin(), order.end(), [l](int a, int b) {
+            if (std::isnan(l[a])) return false;
+            if (std::isnan(l[b])) return true;
+            return l[a] > l[b];
+        });
         // Full softmax over all E experts.
         float mx = l[0];
         for (int e = 1; e < E; ++e) mx = std::max(mx, l[e]);

@@ -59,3 +59,24 @@ def to_np_bits(t: torch.Tensor) -> np.ndarray:
 
 def from_np_bits(a: np.ndarray) -> torch.Tensor:
     return bits_to_bf16(a)
+
+
+def tile_class_tokens(src, offsets, rng, n_random=6, n_extreme=10):
+    """Tokens whose outputs reach every class of GEMM tile at full size: the first and last token,
+    random ones, the last row of every non-empty expert (its last, usually partial, M-tile; for a
+    small expert its swapped chunk), and for the n_extreme largest and smallest non-empty experts
+    also the first row of the segment and of its last 128-row and 256-row tiles (single-SM and
+    SM-pair tiles)."""
+    src = np.asarray(src)
+    offsets = np.asarray(offsets)
+    T = int(src.max()) + 1 if src.size else 0
+    counts = np.diff(offsets)
+    active = np.nonzero(counts > 0)[0]
+    rows = [offsets[e + 1] - 1 for e in active]
+    order = active[np.argsort(counts[active], kind="stable")]
+    for e in np.unique(np.concatenate([order[:n_extreme], order[-n_extreme:]])):
+        n = int(counts[e])
+        rows += [offsets[e], offsets[e] + 128 * ((n - 1) // 128), offsets[e] + 256 * ((n - 1) // 256)]
+    tokens = src[np.asarray(rows, np.int64)]
+    extra = [0, T - 1] + list(rng.integers(0, T, n_random))
+    return np.unique(np.concatenate([tokens, extra])).astype(np.int32)

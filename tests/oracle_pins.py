@@ -196,6 +196,29 @@ def pin_route_library(O, seed=11):
                                        rtol=1e-6, atol=0)
 
 
+def pin_route_nan_order(O, seed=13):
+    """Rows with NaN logits: the ids equal numpy's stable argsort of -logits, which sorts NaN after
+    every number (-inf included) and keeps ascending id among NaNs; rows without a NaN keep their
+    weights.  (The pages define no non-finite logits; this is the order both sides take.)"""
+    rng = np.random.default_rng(seed)
+    T, E, k = 40, 8, 3
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[1:8, 2] = np.nan                      # one NaN
+    logits[8:12, [0, 5]] = np.nan                # two NaNs, below everything
+    logits[12:14, :] = np.nan                    # all NaN -> ids 0, 1, 2
+    logits[14:16, 3] = -np.inf                   # -inf still ranks above NaN
+    logits[14:16, 6] = np.nan
+    logits[16:18, :6] = np.nan                   # only two numbers left for three slots
+    idx, w = O.route(logits, k)
+    ref_idx = np.argsort(-logits.astype(np.float64), axis=1, kind="stable")[:, :k]
+    assert np.array_equal(idx, ref_idx)
+    assert np.array_equal(idx[12], [0, 1, 2]) and np.array_equal(idx[16][:2], [6, 7])
+    clean = ~np.isnan(logits).any(axis=1) & ~np.isinf(logits).any(axis=1)
+    p = softmax(logits[clean].astype(np.float64), axis=1)
+    pk = np.take_along_axis(p, ref_idx[clean], axis=1)
+    np.testing.assert_allclose(w[clean], pk / pk.sum(axis=1, keepdims=True), rtol=1e-6, atol=0)
+
+
 def pin_permute_library(O, seed=5):
     """The permutation equals numpy's stable argsort of the flattened expert ids."""
     rng = np.random.default_rng(seed)
@@ -676,7 +699,7 @@ def pin_fp8b_stages(O, seed=71):
     assert np.array_equal(O.combine(y, w, dest), out)
 
 
-ALL_PINS = [pin_hand_example, pin_brute_force, pin_dense_e1_k1, pin_route_library,
+ALL_PINS = [pin_hand_example, pin_brute_force, pin_dense_e1_k1, pin_route_library, pin_route_nan_order,
             pin_permute_library, pin_invariants, pin_stages, pin_grouped_hand_example,
             pin_grouped_reduces_to_topk, pin_grouped_brute_force, pin_grouped_invariants,
             pin_e4m3_decode_table, pin_e4m3_encode_rne, pin_quantize_rows_fp8, pin_fp8_forward,

@@ -1,7 +1,9 @@
 """GPU parity at the full workload sizes, in the launch configuration bench.py times
 (moe_forward, one call, five launches).  Routing and the permutation are compared in full and bit
 for bit; the layer output is compared on sampled tokens that the oracle computes one by one
-(first, last, random, and tokens routed to the busiest expert)."""
+(first, last, random, tokens routed to the busiest expert, the last row of every expert's segment,
+and the first rows of the segment and of its last 128- and 256-row tiles for the largest and
+smallest experts)."""
 import os
 import sys
 
@@ -10,7 +12,7 @@ import pytest
 import torch
 
 sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
-from gpu_cases import assert_close, assert_layer_close, to_np_bits  # noqa: E402
+from gpu_cases import assert_close, assert_layer_close, tile_class_tokens, to_np_bits  # noqa: E402
 
 from mixture_experts_grouped_fp32_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
 
@@ -54,7 +56,7 @@ def test_full_size_forward(oracle, name, path, monkeypatch):
     rng = np.random.default_rng(1)
     hot = int(np.argmax(counts))
     hot_tokens = src[offsets[hot]:offsets[hot + 1]]
-    sample = np.unique(np.concatenate([[0, w.T - 1], rng.integers(0, w.T, 6),
+    sample = np.unique(np.concatenate([tile_class_tokens(src, offsets, rng),
                                        rng.choice(hot_tokens, min(4, hot_tokens.size), replace=False)]))
     ref = oracle.forward_tokens(xb, ln, to_np_bits(wgu), to_np_bits(wd), w.k, sample.astype(np.int32))
     got = out[torch.from_numpy(sample).to(dev)].float().cpu().numpy()

@@ -4,10 +4,15 @@
 Both sides choose experts by comparing fp32 scores s + bias with s = sigmoid(logit); the GPU's
 expf and the host's expf may round the same affinity one ulp apart, so where two candidates'
 scores lie within that distance the two choices can differ and both are valid top-k selections.
-The tests therefore require the ids to be equal for all but a small fraction of tokens, and check
-every differing token's choice against a float64 evaluation: the GPU's groups and experts must be
-optimal to within 1e-6.  Weights of matching tokens agree to 1e-6 relative (both sides evaluate
-scale * s / sum(s) in fp32).
+How often: a token takes about three such decisions (the kept groups, the top-2 inside a group,
+the k-th expert); with ~128 candidate scores spread over a range of ~1, the chance that a decision's
+gap is under two ulps (1.2e-7) is ~1.2e-7 * 128 ~ 1.5e-5, so ~5e-5 per token, ~0.1 tokens at
+T = 2048 (0 observed in every case here).  The tests allow at most MAX_DIFFERING_TOKENS = 2 (the
+Poisson tail beyond that at 0.1 expected is ~1.5e-4) and print the count.  Every differing token is
+checked in full: its choice against a float64 evaluation (the GPU's groups and experts optimal to
+within 1e-6), its weights against scale * s / sum(s) over the GPU's own ids in float64 (1e-6
+relative), and its layer output against the oracle fed the GPU's routing for that token.  Weights of
+matching tokens agree to 1e-6 relative (both sides evaluate scale * s / sum(s) in fp32).
 """
 import os
 import sys
@@ -17,7 +22,7 @@ import pytest
 import torch
 
 sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
-from gpu_cases import assert_close, assert_layer_close, case_inputs, to_np_bits  # noqa: E402
+from gpu_cases import assert_close, assert_layer_close, case_inputs, tile_class_tokens, to_np_bits  # noqa: E402
 
 from mixture_experts_grouped_fp32_gb300.workloads import WORKLOADS, Workload, draw_router_bias  # noqa: E402
 
@@ -57,14 +62,29 @@ def valid_grouped_choice(logits_row, bias, ids, k, G, tg, tol=1e-6):
     return bool(np.all(np.diff(c[ids]) <= tol))  # slot order: descending score
 
 
-def check_routing(idx, w, ref_idx, ref_w, logits, bias, k, G, tg, max_diff_frac=0.01):
-    """ids equal except near-ties (each differing token validated); weights of equal tokens close."""
+MAX_DIFFERING_TOKENS = 2
+
+
+def check_routing(idx, w, ref_idx, ref_w, logits, bias, k, G, tg, scale):
+    """ids equal except near-ties (each differing token's ids and weights validated); weights of
+    equal tokens close.  Returns the mask of tokens routed like the oracle."""
     same = np.all(idx == ref_idx, axis=1)
-    assert (~same).mean() <= max_diff_frac, f"{int((~same).sum())} of {len(same)} tokens routed differently"
+    n_diff = int((~same).sum())
+    print(f"grouped router: {n_diff} of {len(same)} tokens routed differently from the oracle")
+    assert n_diff <= MAX_DIFFERING_TOKENS, f"{n_diff} of {len(same)} tokens routed differently"
     for t in np.nonzero(~same)[0]:
         assert valid_grouped_choice(logits[t], bias, idx[t], k, G, tg), (t, idx[t], ref_idx[t])
+        s64 = 1.0 / (1.0 + np.exp(-logits[t].astype(np.float64)[idx[t]]))
+        np.testing.assert_allclose(w[t], scale * s64 / s64.sum(), rtol=1e-6, atol=0,
+                                   err_msg=f"weights of differing token {t}")
     assert_close(w[same], ref_w[same], 1e-6, 0, "grouped route weights")
     return same
+
+
+def merged_routing(idx, w, ref_idx, ref_w, same):
+    """The oracle's routing, with the GPU's (validated) routing for the tokens that differ: the
+    routing to feed the oracle's steps 2-5 so that every token's output can be compared."""
+    return np.where(same[:, None], ref_idx, idx).astype(np.int32), np.where(same[:, None], ref_w, w).astype(np.float32)
 
 
 ROUTE_CASES = [  # (T, E, k, n_group, topk_group, scale, bias_std)
@@ -88,7 +108,8 @@ def test_route_grouped_parity(moe, oracle, T, E, k, G, tg, scale, bstd):
     idx, w = moe.route_grouped(logits.to(DEV), bias.to(DEV), k, G, tg, scale)
     torch.cuda.synchronize()
     ref_idx, ref_w = oracle.route_grouped(logits.numpy(), bias.numpy(), k, G, tg, scale)
-    check_routing(idx.cpu().numpy(), w.cpu().numpy(), ref_idx, ref_w, logits.numpy(), bias.numpy(), k, G, tg)
+    check_routing(idx.cpu().numpy(), w.cpu().numpy(), ref_idx, ref_w, logits.numpy(), bias.numpy(), k, G, tg,
+                  scale)
 
 
 def test_route_grouped_exact_ties(moe, oracle):
@@ -127,9 +148,11 @@ def test_forward_grouped_matches_oracle(moe, oracle, w):
     v = moe.workspace_views(ws, w.T, w.d, w.f, w.E, w.k)
     ln, bn = logits.numpy(), bias.numpy()
     ref_idx, ref_w = oracle.route_grouped(ln, bn, w.k, G, tg, scale)
-    same = check_routing(v["idx"].cpu().numpy(), v["w"].cpu().numpy(), ref_idx, ref_w, ln, bn, w.k, G, tg)
-    ref = oracle.forward_routed(to_np_bits(x), ref_idx, ref_w, to_np_bits(wgu), to_np_bits(wd))
-    assert_layer_close(out.float().cpu().numpy()[same], ref[same], w.name)
+    gidx, gw = v["idx"].cpu().numpy(), v["w"].cpu().numpy()
+    same = check_routing(gidx, gw, ref_idx, ref_w, ln, bn, w.k, G, tg, scale)
+    midx, mw = merged_routing(gidx, gw, ref_idx, ref_w, same)
+    ref = oracle.forward_routed(to_np_bits(x), midx, mw, to_np_bits(wgu), to_np_bits(wd))
+    assert_layer_close(out.float().cpu().numpy(), ref, w.name)
 
 
 @pytest.mark.slow
@@ -150,8 +173,8 @@ def test_forward_grouped_full_size(moe, oracle):
     v = moe.workspace_views(ws, w.T, w.d, w.f, w.E, w.k)
     ln, bn = logits.numpy(), bias.numpy()
     ref_idx, ref_w = oracle.route_grouped(ln, bn, w.k, G, tg, scale)
-    gidx = v["idx"].cpu().numpy()
-    same = check_routing(gidx, v["w"].cpu().numpy(), ref_idx, ref_w, ln, bn, w.k, G, tg)
+    gidx, gw = v["idx"].cpu().numpy(), v["w"].cpu().numpy()
+    same = check_routing(gidx, gw, ref_idx, ref_w, ln, bn, w.k, G, tg, scale)
     gc, go, gs, gd = (v[n].cpu().numpy() for n in ("counts", "offsets", "src", "dest"))
     if same.all():  # the permutation is then the oracle's, bit for bit
         counts, offsets, src, dest = oracle.permute(ref_idx, w.E)
@@ -164,9 +187,9 @@ def test_forward_grouped_full_size(moe, oracle):
         assert np.array_equal(gs, np.argsort(flat, kind="stable") // w.k)
         assert np.array_equal(gs[gd.reshape(-1)], np.repeat(np.arange(w.T), w.k))
     rng = np.random.default_rng(2)
-    sample = np.unique(np.concatenate([[0, w.T - 1], rng.integers(0, w.T, 8)]))
-    sample = sample[same[sample]]
-    ref = oracle.forward_tokens_routed(to_np_bits(x), ref_idx[sample], ref_w[sample], to_np_bits(wgu),
+    sample = np.unique(np.concatenate([tile_class_tokens(gs, go, rng, n_random=8), np.nonzero(~same)[0]]))
+    midx, mw = merged_routing(gidx, gw, ref_idx, ref_w, same)
+    ref = oracle.forward_tokens_routed(to_np_bits(x), midx[sample], mw[sample], to_np_bits(wgu),
                                        to_np_bits(wd), sample.astype(np.int32))
     got = out[torch.from_numpy(sample).to(dev)].float().cpu().numpy()
     assert_layer_close(got, ref, f"deepseek_v3_t2048 sampled tokens {sample.tolist()}")
@@ -204,11 +227,13 @@ def test_forward_grouped_fp8_matches_oracle(moe, oracle, w, blocks):
     v = views(ws, w.T, w.d, w.f, w.E, w.k)
     ln, bn = logits.numpy(), bias.numpy()
     ref_idx, ref_w = oracle.route_grouped(ln, bn, w.k, G, tg, scale)
-    same = check_routing(v["idx"].cpu().numpy(), v["w"].cpu().numpy(), ref_idx, ref_w, ln, bn, w.k, G, tg)
+    gidx, gwt = v["idx"].cpu().numpy(), v["w"].cpu().numpy()
+    same = check_routing(gidx, gwt, ref_idx, ref_w, ln, bn, w.k, G, tg, scale)
+    midx, mw = merged_routing(gidx, gwt, ref_idx, ref_w, same)
     fwd = oracle.forward_fp8b_tokens_routed if blocks else oracle.forward_fp8_tokens_routed
-    tokens = np.nonzero(same)[0].astype(np.int32)
-    ref = fwd(to_np_bits(x), ref_idx[tokens], ref_w[tokens], *rw, tokens)
-    assert_layer_close(out.float().cpu().numpy()[tokens], ref, f"{w.name} grouped router, {'fp8b' if blocks else 'fp8'}")
+    tokens = np.arange(w.T, dtype=np.int32)
+    ref = fwd(to_np_bits(x), midx, mw, *rw, tokens)
+    assert_layer_close(out.float().cpu().numpy(), ref, f"{w.name} grouped router, {'fp8b' if blocks else 'fp8'}")
 
 
 @pytest.mark.slow
@@ -245,12 +270,14 @@ def test_forward_grouped_fp8_full_size(moe, oracle, blocks):
     del wd_bits
     ln, bn = logits.numpy(), bias.numpy()
     ref_idx, ref_w = oracle.route_grouped(ln, bn, w.k, G, tg, scale)
-    same = check_routing(v["idx"].cpu().numpy(), v["w"].cpu().numpy(), ref_idx, ref_w, ln, bn, w.k, G, tg)
+    gidx, gwt = v["idx"].cpu().numpy(), v["w"].cpu().numpy()
+    same = check_routing(gidx, gwt, ref_idx, ref_w, ln, bn, w.k, G, tg, scale)
+    midx, mw = merged_routing(gidx, gwt, ref_idx, ref_w, same)
     rng = np.random.default_rng(7)
-    sample = np.unique(np.concatenate([[0, w.T - 1], rng.integers(0, w.T, 6)]))
-    sample = sample[same[sample]].astype(np.int32)
+    go, gs = v["offsets"].cpu().numpy(), v["src"].cpu().numpy()
+    sample = np.unique(np.concatenate([tile_class_tokens(gs, go, rng), np.nonzero(~same)[0]])).astype(np.int32)
     fwd = oracle.forward_fp8b_tokens_routed if blocks else oracle.forward_fp8_tokens_routed
-    ref = fwd(to_np_bits(x), ref_idx[sample], ref_w[sample], *r_gu, *r_d, sample)
+    ref = fwd(to_np_bits(x), midx[sample], mw[sample], *r_gu, *r_d, sample)
     got = out[torch.from_numpy(sample).long().to(DEV)].float().cpu().numpy()
     assert_layer_close(got, ref, f"deepseek_v3_t2048 {'fp8b' if blocks else 'fp8'} sampled tokens {sample.tolist()}")
 

@@ -124,6 +124,50 @@ def test_route_parity(moe, oracle, T, E, k, ties):
     assert_close(w.cpu().numpy(), rw, 1e-6, 0, "route weights")
 
 
+def _nan_logits(T, E, seed):
+    """Logits with NaN rows of every kind: one NaN, several, all NaN, -inf beside a NaN, and fewer
+    numbers than slots.  The pages define no non-finite logits; both sides rank NaN below every
+    number with NaNs by ascending id, so the ids are still compared bit for bit."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    lg = torch.randn(T, E, generator=g)
+    lg[1:9, 2 % E] = float("nan")
+    lg[9:13, [0, E - 1]] = float("nan")
+    lg[13:15, :] = float("nan")
+    lg[15:17, 1] = float("-inf")
+    lg[15:17, E - 2] = float("nan")
+    lg[17:19, :E - 2] = float("nan")
+    return lg
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (8, 3), (64, 6), (256, 8)])
+def test_route_nan_logits_order(moe, oracle, E, k):
+    logits = _nan_logits(64, E, seed=E + k)
+    idx, w = moe.route(logits.to(DEV), k)
+    torch.cuda.synchronize()
+    ridx, rw = oracle.route(logits.numpy(), k)
+    gi = idx.cpu().numpy()
+    assert np.array_equal(gi, ridx)
+    assert all(len(set(r)) == k for r in gi.tolist())  # no expert in two slots of one token
+    clean = torch.isfinite(logits).all(dim=1).numpy()
+    assert_close(w.cpu().numpy()[clean], rw[clean], 1e-6, 0, "route weights, finite rows")
+
+
+def test_fused_route_permute_nan_logits_order(moe, oracle):
+    # E <= 32 and T*E <= 8192: moe_forward routes inside the permute kernel (one thread per token).
+    w = Workload("nan_fused", 64, 128, 128, 8, 2)
+    _, x, wgu, wd = case_inputs(w, seed=5)
+    logits = _nan_logits(w.T, w.E, seed=77)
+    assert moe.forward_launch_count(w.T, w.E, w.k) == 4
+    _, v, ws = _forward_and_views(moe, w, logits, x, wgu, wd)
+    ridx, rw = oracle.route(logits.numpy(), w.k)
+    assert np.array_equal(v["idx"].cpu().numpy(), ridx)
+    counts, offsets, src, dest = oracle.permute(ridx, w.E)
+    assert np.array_equal(v["src"].cpu().numpy(), src)
+    assert np.array_equal(v["dest"].cpu().numpy(), dest)
+    clean = torch.isfinite(logits).all(dim=1).numpy()
+    assert_close(v["w"].cpu().numpy()[clean], rw[clean], 1e-6, 0, "route weights, finite rows")
+
+
 @pytest.mark.parametrize("T,d,E,k", [(4096, 4096, 8, 2), (2048, 256, 256, 8), (37, 64, 4, 4), (1, 128, 8, 2),
                                      (999, 192, 64, 6)])
 def test_permute_parity(moe, oracle, T, d, E, k):

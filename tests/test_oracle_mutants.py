@@ -22,8 +22,8 @@ MUTANTS = {
     "swiglu_swapped": ("h[n] = silu(g[n]) * u[n];", "h[n] = silu(u[n]) * g[n];"),
     "down_transposed": ("y[m] += hn * bf16_to_f32(wrow[m]);",
                         "y[m] += hn * bf16_to_f32(Wd_e[static_cast<size_t>(m) * f + n]);"),
-    "ties_to_higher_id": ("return l[a] > l[b]; });",
-                          "return l[a] > l[b] || (l[a] == l[b] && a > b); });"),
+    "ties_to_higher_id": ("            return l[a] > l[b];\n        });",
+                          "            return l[a] > l[b] || (l[a] == l[b] && a > b);\n        });"),
     "no_renormalise": ("w[static_cast<size_t>(t) * k + j] = p[order[j]] / s;",
                        "w[static_cast<size_t>(t) * k + j] = p[order[j]];"),
     "tokens_descending": ("const int r = cursor[e]++;",
