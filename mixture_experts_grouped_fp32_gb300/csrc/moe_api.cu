@@ -197,9 +197,10 @@ bool fuse_route_permute(int T, int E) {
 }
 
 // Failure-detection test hook, off unless the environment sets MOE_INJECT_STALL=1: the next
-// grouped-GEMM launches run on the 1-SM kernel with one pipeline stage armed for bytes that never
-// arrive, so a bounded wait expires (~1 s), the kernel reports MOE_STATUS_WAIT_TIMEOUT in the
-// status word, releases its tensor memory and returns.  Nothing faults, traps or hangs.
+// grouped-GEMM launches (the stage calls' and the bf16 layer's) run on the 1-SM kernel with one
+// pipeline stage armed for bytes that never arrive, so a bounded wait expires (~1 s), the kernel
+// reports MOE_STATUS_WAIT_TIMEOUT in the status word, releases its tensor memory and returns.
+// Nothing faults, traps or hangs.
 int inject_stall() {
     const char* v = std::getenv("MOE_INJECT_STALL");
     return (v && v[0] == '1') ? 1 : 0;
@@ -357,10 +358,12 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
         g1.gather_src = src;
         g1.gather_T = T;
     }
+    g1.inject_stall = inject_stall();  // failure-detection test hook, off unless MOE_INJECT_STALL=1
     if ((e = launch_grouped_gemm(0, g1, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "gate+up GEMM: %s (%s)", why, cudaGetErrorString(e));
     GemmArgs g2{h, wd, offsets, M, f, d, E, y, status, ksplit, swap_max, use_pair(M, E, d, 1), pair_swap_max_rows(),
                 pair_layout(), pair_split()};
+    g2.inject_stall = g1.inject_stall;
     if ((e = launch_grouped_gemm(1, g2, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "down GEMM: %s (%s)", why, cudaGetErrorString(e));
     if ((e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) !=
