@@ -112,11 +112,18 @@ constexpr int PAIR_SWAP_MAX_ROWS = 128;
 constexpr uint16_t BOTH_CTAS = 0x3;
 constexpr int kMixedSplit = 1 << 20;  // split_req value selecting the proportional merge
 constexpr int kAutoSplit = 1 << 21;   // split_req value: choose the split on the device
-// Cost model of the automatic split (ns per pipeline stage of one CTA pair, fitted to a sweep of
-// the split on the DeepSeek-V3-shaped gate+up GEMM: 0.373 us per 256x256x64 pair MMA stage of a
-// normal tile at the clock the tile phase runs at, 0.465 us per stage of a swapped chunk, which
-// streams 2 x 32 KB of weights and is bound by the bytes one SM pair keeps in flight).
-constexpr long long kNormalStageNs = 373, kSwapStageNs = 465;
+// Cost model of the automatic split (ns per pipeline stage of one CTA pair).  Gate+up: fitted to a
+// sweep of the split on the DeepSeek-V3-shaped gate+up GEMM: 0.373 us per 256x256x64 pair MMA
+// stage of a normal tile at the clock the tile phase runs at, 0.465 us per stage of a swapped
+// chunk, which streams 2 x 32 KB of weights and is bound by the bytes one SM pair keeps in flight.
+// Down: a normal stage costs about as much as a swapped one (0.470 us): its items are only
+// d_ff / 64 stages deep, so the accumulator hand-over and the 128 KB fp32 epilogue of every item
+// weigh more; fitted to the per-pair finishing times of both DeepSeek-shaped down GEMMs (CTA
+// pairs of each kind busy until the same time at P = 57 with DeepSeek-V3's router and P = 45 with
+// the softmax router, against 53 and 41 with the gate+up costs).
+template <int KIND>
+constexpr long long normal_stage_ns() { return KIND == 0 ? 373 : 470; }
+constexpr long long kSwapStageNs = 465;
 
 template <bool SWAPCAP>
 struct Cfg {
@@ -475,7 +482,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 hs_reuse += __shfl_xor_sync(0xffffffffu, hs_reuse, o);
                 ls += __shfl_xor_sync(0xffffffffu, ls, o);
             }
-            const long long wh = hs * kNormalStageNs, wl = ls * kSwapStageNs, wt = wh + wl;
+            const long long wh = hs * normal_stage_ns<KIND>(), wl = ls * kSwapStageNs, wt = wh + wl;
             if (wt > 0 && 100 * wh >= 15 * wt && 100 * wl >= 15 * wt && 2 * hs_reuse >= hs) {
                 auto_p = static_cast<int>((2 * num_pairs * wh + wt) / (2 * wt));  // rounded
                 auto_p = max(1, min(num_pairs - 1, auto_p));

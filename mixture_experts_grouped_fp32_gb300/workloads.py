@@ -71,6 +71,10 @@ WORKLOADS = {
         Workload("deepseek_e32_t256", 256, 7168, 2048, 32, 8, ("zipf", 1.2),
                  note="profiling-scale DeepSeek-V3-shaped layer: same expert shapes and skew, "
                       "32 experts (2.8 GB of weights, small enough for a full ncu capture)"),
+        Workload("deepseek_v3like_e32_t1024", 1024, 7168, 2048, 32, 8, ("zipf", 2.0),
+                 note="profiling-scale stand-in for the DeepSeek-V3-router layer: the same expert "
+                      "shapes and a row distribution of the same kind (a few experts near T rows, "
+                      "a third under 16), 32 experts (2.8 GB of weights)"),
         Workload("deepseek_v3_t2048", 2048, 7168, 2048, 256, 8, ("zipf", 1.2),
                  note="DeepSeek-V3-shaped routed experts with DeepSeek-V3's own router: sigmoid "
                       "affinities, selection bias, 8 groups of 32 experts, 4 groups kept, scale 2.5",
