@@ -21,8 +21,8 @@
 // normal item issues N = 256 MMAs into one of two 256-column tensor-memory buffers, and eight
 // promotion warps (two per tensor-memory lane quarter) each keep 128 fp32 accumulators.  For
 // those registers the block's warpgroups split its register file with setmaxnreg: warpgroup 0
-// (TMA producer, MMA issuer, two idle warps) drops to 40 registers a thread, the two promotion
-// warpgroups rise to 232 (per SM sub-partition: 40 x 32 + 2 x 232 x 32 <= 16384).
+// (TMA producer, one or two MMA issuers, idle warps) drops to 40 registers a thread, the two
+// promotion warpgroups rise to 232 (per SM sub-partition: 40 x 32 + 2 x 232 x 32 <= 16384).
 //   normal   UMMA M = 128 rows x N = 256 weight columns; kind 0: gate n0..n0+127 and up
 //            f+n0..f+n0+127 (128 h columns), kind 1: 256 y columns.  Weights arrive as whole
 //            8 KB blocks of the blocked layout (64 rows x 128 K), 32 KB per stage.
@@ -54,7 +54,7 @@ constexpr int PART_COLS = 256;                     // tensor-memory columns per 
 constexpr int NUM_PART = 2;
 constexpr int TMEM_COLS = NUM_PART * PART_COLS;    // 512
 constexpr int EPI_WARPS = 8;
-constexpr int NUM_THREADS = 128 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA, warps 4-11 promotion
+constexpr int NUM_THREADS = 128 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 (and 2) MMA, warps 4-11 promotion
 // Registers a thread: at launch (three warps per SM sub-partition: 16384 / 96 rounded down to a
 // multiple of 8), then warpgroup 0 and the promotion warpgroups after setmaxnreg.  The split must
 // not exceed what the block was launched with, or the increase would wait for registers forever;
@@ -145,8 +145,8 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
 }
 
 // QH (kind 0 only): h quantised in the epilogue, a separate instance so that the plain one keeps
-// its register allocation.
-template <int KIND, bool QH>
+// its register allocation.  ALT: two MMA threads take alternate K blocks (see the MMA role).
+template <int KIND, bool QH, bool ALT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
                          const __grid_constant__ CUtensorMap tmB128, const int32_t* __restrict__ offsets, int M,
@@ -175,7 +175,7 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             ptx::mbar_init(&c.pfull[p], 1);
             ptx::mbar_init(&c.pempty[p], EPI_WARPS);
         }
-        ptx::mbar_init(&c.drain, 1);
+        ptx::mbar_init(&c.drain, ALT ? 2 : 1);  // one arrival per MMA thread
         for (int k = 0; k < 2; ++k) {
             for (int q = 0; q < 4; ++q) ptx::mbar_init(&c.xbar_n[k][q], 64);
             for (int q = 0; q < 2; ++q) ptx::mbar_init(&c.xbar_s[k][q], 128);
@@ -278,10 +278,20 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     }
                 }
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if ((warp == 1 || (ALT && warp == 2)) && lane == 0) {
             // ---------------- MMA issuer: one partial product per K block, two buffers ----------------
+            // ALT: the CTA's K blocks, in order over its items, alternate between the two partial
+            // buffers and (four stages) between even and odd stages; warp 1 issues the even-numbered
+            // blocks into buffer 0, warp 2 the odd ones into buffer 1.  A block's partial product is
+            // a fresh MMA chain (nothing accumulates across blocks), so the two chains are
+            // independent and every barrier still has a single MMA thread.  A thread spends about
+            // 100 cycles issuing a tcgen05.mma, and with two threads the tensor pipe sees the next
+            // block's MMAs sooner (gate+up, Mixtral shape T=4096: 1.204 -> 1.143 ms).
+            static_assert(STAGES == 2 * NUM_PART, "ALT: each thread owns one buffer and half the stages");
+            const uint32_t t = ALT ? static_cast<uint32_t>(warp - 1) : 0u;
             constexpr uint32_t idesc_normal = ptx::idesc_e4m3_f32(BM, PART_COLS, 0, 0);
-            uint32_t stage = 0, phase = 0, pb = 0, pph = 0;
+            uint32_t stage = t, phase = 0, pb = t, pph = 0;
+            bool mine = t == 0;  // ALT: whether the next K block is this thread's
             bool aborted = false;
             for (int i = blockIdx.x; i < total && !aborted; i += gridDim.x) {
                 const Item it = decode_item(c, E, ksplit, swap_max, i);
@@ -289,6 +299,11 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 const uint32_t idesc_swap = ptx::idesc_e4m3_f32(BM, ntok, 0, 0);
                 const int kb0 = it.kslice * kb_per, kb1 = min(num_kb, kb0 + kb_per);
                 for (int kb = kb0; kb < kb1; ++kb) {
+                    if (ALT) {
+                        const bool m = mine;
+                        mine = !mine;
+                        if (!m) continue;
+                    }
                     if (!ptx::mbar_wait(&c.full[stage], phase, abort_flag) ||
                         !ptx::mbar_wait(&c.pempty[pb], pph ^ 1u, abort_flag)) {
                         raise_abort(c, status);
@@ -318,13 +333,22 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     }
                     ptx::mma_commit(&c.empty[stage]);
                     ptx::mma_commit(&c.pfull[pb]);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                    if (++pb == NUM_PART) {
-                        pb = 0;
+                    if (ALT) {  // this thread's next block: two stages on, the same buffer
+                        stage += 2;
+                        if (stage >= STAGES) {
+                            stage -= STAGES;
+                            phase ^= 1u;
+                        }
                         pph ^= 1u;
+                    } else {
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        if (++pb == NUM_PART) {
+                            pb = 0;
+                            pph ^= 1u;
+                        }
                     }
                 }
             }
@@ -569,7 +593,7 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         for (int s = 0; s < STAGES; ++s)
             if (filled_mask & (1 << s)) ptx::mbar_wait_ns(&c.full[s], fill_parity[s], 100000000ull);
     }
-    if (warp == 1 && lane == 0) {
+    if ((warp == 1 || (ALT && warp == 2)) && lane == 0) {
         ptx::mma_commit(&c.drain);
         ptx::mbar_wait_ns(&c.drain, 0, 100000000ull);
     }
@@ -578,13 +602,13 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     if (warp == 1) ptx::tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
-template <int KIND, bool QH>
-cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const char** why) {
+template <int KIND, bool QH, bool ALT>
+cudaError_t launch_inst(const GemmArgs& a, int num_sms, cudaStream_t s, const char** why) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_fp8b_kernel<KIND, QH>,
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_fp8b_kernel<KIND, QH, ALT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) {
             *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
@@ -593,7 +617,7 @@ cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const ch
         attr_set[dev] = true;
     }
     cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8b_kernel<KIND, QH>) != cudaSuccess ||
+    if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8b_kernel<KIND, QH, ALT>) != cudaSuccess ||
         fa.numRegs * NUM_THREADS < REGS_CTL * 128 + REGS_PROMO * 32 * EPI_WARPS) {
         *why = "blockwise FP8 GEMM: the kernel was compiled with fewer registers than its setmaxnreg split needs";
         return cudaErrorInvalidValue;
@@ -607,9 +631,24 @@ cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const ch
     }
     const int swap_max = a.swap_max < 0 ? 0 : (a.swap_max > SWAP_MAX_ROWS ? SWAP_MAX_ROWS : a.swap_max);
     const int ksplit = KIND == 0 ? 1 : a.ksplit;
-    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_fp8b_kernel<KIND, QH>, dim3(num_sms),
+    return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_fp8b_kernel<KIND, QH, ALT>, dim3(num_sms),
                     dim3(NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB128, a.offsets, a.M, a.K, a.N, a.E, ksplit,
                     swap_max, a.a_scale, a.b_scale, a.out, QH ? a.h_scale : nullptr, a.status);
+}
+
+// Two MMA threads (ALT) for the gate+up GEMM, and for the down GEMM when the experts average 256
+// rows or more: its small-expert launches ran slower with them (Mixtral shape T=32 down 0.080 ->
+// 0.089 ms, DeepSeek-V3 router 0.543 -> 0.559) while T=4096's down gained (0.627 -> 0.612).
+// MOE_FP8B_ALT_ISSUE=0/1 overrides (a measurement knob).
+bool fp8b_alt_issue(int kind, int M, int E) {
+    if (const char* v = std::getenv("MOE_FP8B_ALT_ISSUE")) return v[0] == '1';
+    return kind == 0 || static_cast<long long>(M) >= 256ll * E;
+}
+
+template <int KIND, bool QH>
+cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const char** why) {
+    return fp8b_alt_issue(KIND, a.M, a.E) ? launch_inst<KIND, QH, true>(a, num_sms, s, why)
+                                          : launch_inst<KIND, QH, false>(a, num_sms, s, why);
 }
 
 }  // namespace

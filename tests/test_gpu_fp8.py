@@ -102,7 +102,8 @@ def test_quantize_weights_fp8_bit_exact(moe, oracle, E, K, N):
     assert np.array_equal(sc.cpu().numpy().view(np.uint32), rsc.view(np.uint32))
 
 
-@pytest.mark.parametrize("R,C,src_rows", [(37, 256, None), (300, 4096, 150), (5, 8, 5), (1, 14336, 3)])
+@pytest.mark.parametrize("R,C,src_rows", [(37, 256, None), (300, 4096, 150), (5, 8, 5), (1, 14336, 3),
+                                          (6, 16384, None), (4, 20480, 9)])
 def test_quantize_rows_fp8_bit_exact(moe, oracle, R, C, src_rows):
     n_src = src_rows or R
     bits = to_np_bits(random_bf16((n_src, C), seed=R + C))
