@@ -92,49 +92,45 @@ AUTO_STEPS_MIN, AUTO_STEPS_MAX = 50, 4000
 # kernel source with the recorded hash; reported only while the GEMM source still hashes to that
 # value, else null.
 
-_TRAFFIC_HASH = "a8d3a7a96e328c09"  # GEMM source hash the captures below were taken at
-_TRAFFIC_HASH_FP8B = "f00c09d6f20a7ae5"  # ... and that of the blockwise FP8 kernel's sources
+_TRAFFIC_HASH = "42ce3bbe1c07d68c"  # GEMM source hash the captures below were taken at
+_TRAFFIC_HASH_FP8B = "2cc65fcf7ddc68c6"  # ... and that of the blockwise FP8 kernel's sources
 MEASURED_TRAFFIC = {
-    ("deepseek_e32_t256", "gateup_swiglu"): (1919914752, _TRAFFIC_HASH),
-    ("deepseek_e32_t256", "down"): (1008838144, _TRAFFIC_HASH),
-    ("mixtral_t32", "gateup_swiglu"): (1884825088, _TRAFFIC_HASH),
-    ("mixtral_t32", "down"): (944483328, _TRAFFIC_HASH),
-    ("mixtral_t4096", "gateup_swiglu"): (3337290496, _TRAFFIC_HASH),
-    ("mixtral_t4096", "down"): (1656340992, _TRAFFIC_HASH),
-    ("mixtral_t512", "gateup_swiglu"): (1917540864, _TRAFFIC_HASH),
-    ("mixtral_t512", "down"): (982737664, _TRAFFIC_HASH),
-    ("mixtral_t512_skew40", "gateup_swiglu"): (1917613056, _TRAFFIC_HASH),
-    ("mixtral_t512_skew40", "down"): (983452672, _TRAFFIC_HASH),
-    ("deepseek_e32_t256", "gateup_swiglu_fp8"): (966500352, _TRAFFIC_HASH),
-    ("deepseek_e32_t256", "down_fp8"): (534014976, _TRAFFIC_HASH),
-    ("mixtral_t32", "gateup_swiglu_fp8"): (945943296, _TRAFFIC_HASH),
-    ("mixtral_t32", "down_fp8"): (474108672, _TRAFFIC_HASH),
-    ("mixtral_t4096", "gateup_swiglu_fp8"): (1211593984, _TRAFFIC_HASH),
-    ("mixtral_t4096", "down_fp8"): (785332480, _TRAFFIC_HASH),
-    ("mixtral_t512", "gateup_swiglu_fp8"): (972093696, _TRAFFIC_HASH),
-    ("mixtral_t512", "down_fp8"): (498120704, _TRAFFIC_HASH),
-    ("mixtral_t512_skew40", "gateup_swiglu_fp8"): (971906304, _TRAFFIC_HASH),
-    ("mixtral_t512_skew40", "down_fp8"): (498307328, _TRAFFIC_HASH),
-    ("deepseek_t2048", "gateup_swiglu"): (8108204800, _TRAFFIC_HASH),
-    ("deepseek_t2048", "down"): (4196736768, _TRAFFIC_HASH),
-    ("deepseek_v3_t2048", "gateup_swiglu"): (4711750656, _TRAFFIC_HASH),
-    ("deepseek_v3_t2048", "down"): (2483243008, _TRAFFIC_HASH),
-    ("deepseek_t2048", "gateup_swiglu_fp8"): (3892582656, _TRAFFIC_HASH),
-    ("deepseek_t2048", "down_fp8"): (2288754688, _TRAFFIC_HASH),
-    ("deepseek_e32_t256", "gateup_swiglu_fp8b"): (966599936, _TRAFFIC_HASH_FP8B),
-    ("deepseek_e32_t256", "down_fp8b"): (535245568, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t32", "gateup_swiglu_fp8b"): (944946688, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t32", "down_fp8b"): (474656768, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t4096", "gateup_swiglu_fp8b"): (1091124480, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t4096", "down_fp8b"): (781382400, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512", "gateup_swiglu_fp8b"): (1188105984, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512", "down_fp8b"): (614691072, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512_skew40", "gateup_swiglu_fp8b"): (962396928, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512_skew40", "down_fp8b"): (514285056, _TRAFFIC_HASH_FP8B),
-    ("deepseek_t2048", "gateup_swiglu_fp8b"): (3806213120, _TRAFFIC_HASH_FP8B),
-    ("deepseek_t2048", "down_fp8b"): (2343941632, _TRAFFIC_HASH_FP8B),
-    ("deepseek_v3_t2048", "gateup_swiglu_fp8b"): (2076622848, _TRAFFIC_HASH_FP8B),
-    ("deepseek_v3_t2048", "down_fp8b"): (1408621312, _TRAFFIC_HASH_FP8B),
+    ("deepseek_e32_t256", "gateup_swiglu"): (1919832832, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "down"): (1009043712, _TRAFFIC_HASH),
+    ("deepseek_v3like_e32_t1024", "gateup_swiglu"): (2391786496, _TRAFFIC_HASH),
+    ("deepseek_v3like_e32_t1024", "down"): (1211820544, _TRAFFIC_HASH),
+    ("mixtral_t32", "gateup_swiglu"): (1884708096, _TRAFFIC_HASH),
+    ("mixtral_t32", "down"): (944412160, _TRAFFIC_HASH),
+    ("mixtral_t4096", "gateup_swiglu"): (3664941824, _TRAFFIC_HASH),
+    ("mixtral_t4096", "down"): (1816316160, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "gateup_swiglu"): (1917530368, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "down"): (983433728, _TRAFFIC_HASH),
+    ("mixtral_t512", "gateup_swiglu"): (1917100288, _TRAFFIC_HASH),
+    ("mixtral_t512", "down"): (982793472, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "gateup_swiglu_fp8b"): (966528512, _TRAFFIC_HASH_FP8B),
+    ("deepseek_e32_t256", "down_fp8b"): (535162112, _TRAFFIC_HASH_FP8B),
+    ("deepseek_v3like_e32_t1024", "gateup_swiglu_fp8b"): (1022521856, _TRAFFIC_HASH_FP8B),
+    ("deepseek_v3like_e32_t1024", "down_fp8b"): (730804480, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t32", "gateup_swiglu_fp8b"): (944823296, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t32", "down_fp8b"): (474663936, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t4096", "gateup_swiglu_fp8b"): (1090318080, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t4096", "down_fp8b"): (775504384, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512_skew40", "gateup_swiglu_fp8b"): (962286080, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512_skew40", "down_fp8b"): (515716864, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512", "gateup_swiglu_fp8b"): (963255296, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512", "down_fp8b"): (611966720, _TRAFFIC_HASH_FP8B),
+    ("deepseek_e32_t256", "gateup_swiglu_fp8"): (966083840, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "down_fp8"): (534113792, _TRAFFIC_HASH),
+    ("deepseek_v3like_e32_t1024", "gateup_swiglu_fp8"): (1141912576, _TRAFFIC_HASH),
+    ("deepseek_v3like_e32_t1024", "down_fp8"): (724014080, _TRAFFIC_HASH),
+    ("mixtral_t32", "gateup_swiglu_fp8"): (945154048, _TRAFFIC_HASH),
+    ("mixtral_t32", "down_fp8"): (474109440, _TRAFFIC_HASH),
+    ("mixtral_t4096", "gateup_swiglu_fp8"): (1239584256, _TRAFFIC_HASH),
+    ("mixtral_t4096", "down_fp8"): (799462912, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "gateup_swiglu_fp8"): (972034816, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "down_fp8"): (498305536, _TRAFFIC_HASH),
+    ("mixtral_t512", "gateup_swiglu_fp8"): (971907328, _TRAFFIC_HASH),
+    ("mixtral_t512", "down_fp8"): (497746176, _TRAFFIC_HASH),
 }
 GEMM_SOURCES = ("mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm.cu",
                 "mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm_2sm.cu",
