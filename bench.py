@@ -571,8 +571,11 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         "host_weights": (wgu, wd), "inputs": (logits, x), "step_ms_p10_p90": (
             float(np.percentile(step_ms, 10)), float(np.percentile(step_ms, 90))),
         "peak_src": peak_src, "peaks": peaks, "ksplit": v["ksplit"],
-        # DeepSeek-V3's router never fuses with the permutation: 5 (bf16), 6 (e4m3), 6 or 7 (e4m3b).
-        "launches_per_step": (((7 - int(fuse_h)) if blocks else 6 if fp8 else 5) if grouped else
+        # DeepSeek-V3's router never fuses with the permutation: 5 (bf16), 6 (e4m3), 6 or 7 (e4m3b),
+        # one fewer for bf16 and e4m3 when the combine is folded into the down GEMM (MOE_FOLD_COMBINE=1).
+        "launches_per_step": (((7 - int(fuse_h)) if blocks else
+                               (6 if fp8 else 5) - int(os.environ.get("MOE_FOLD_COMBINE", "0") == "1"))
+                              if grouped else
                               moe.forward_fp8b_launch_count(w.T, w.E, w.k) if blocks else
                               moe.forward_fp8_launch_count(w.T, w.E, w.k) if fp8 else
                               moe.forward_launch_count(w.T, w.E, w.k)),

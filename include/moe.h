@@ -1,7 +1,8 @@
 /* moe.h — C ABI of libmoe.so: the forward pass of one Mixture-of-Experts FFN layer on a GB300
  * (sm_103a).
  *
- * The layer, in five stream-ordered steps (one kernel launch each):
+ * The layer, in five stream-ordered steps (each a stage call below; moe_forward runs them as four
+ * or five launches, see moe_forward_launch_count):
  *   route    -> top-k experts and their weights per token
  *   permute  -> group the (token, slot) assignments by expert, copy x rows into that order
  *   gate+up  -> grouped BF16 GEMM x_perm . [W_gate | W_up] per expert, SwiGLU fused in the
@@ -66,7 +67,7 @@ typedef void* moe_stream_t; /* a cudaStream_t */
 
 /* Bytes of scratch that moe_forward needs for this shape (256-byte aligned pieces: status word,
  * idx, w, counts, offsets, src, dest, x_perm bf16 [T*k,d], h bf16 [T*k,f], y_perm fp32
- * [moe_down_ksplit(), T*k, d]).
+ * [moe_down_ksplit(), T*k, d], then the combine-fold counters int32 [T, d/64]).
  * Returns 0 for an invalid shape. */
 MOE_API size_t moe_workspace_size(int T, int d, int f, int E, int top_k);
 
@@ -199,8 +200,15 @@ MOE_API int moe_down_ksplit(int T, int d, int f, int E, int top_k);
 MOE_API int moe_combine(const float* y_perm, const float* w, const int32_t* dest, int T, int d, int top_k,
                 int ksplit, void* out, int32_t* status, moe_stream_t stream);
 
-/* The whole layer in one call: steps 1-5 as five kernel launches on `stream`, intermediates
- * carved from `workspace` (device, >= moe_workspace_size() bytes, 256-byte aligned).
+/* The whole layer in one call: steps 1-5 on `stream` as moe_forward_launch_count() launches,
+ * intermediates carved from `workspace` (device, >= moe_workspace_size() bytes, 256-byte aligned).
+ * With MOE_FOLD_COMBINE=1 in the environment, step 5 runs inside the down GEMM instead of as its
+ * own launch: every (token, 64-column block) has an arrival counter (zeroed by the permute
+ * launch); each epilogue that stored its part of a row's block adds its share, and the arrival
+ * that completes the token's top_k rows (and K slices) writes that block of `out` — the same fp32
+ * sum in slot order as moe_combine, with no atomics on the output, so the result is deterministic
+ * and equal to the default form bit for bit.  It is off by default because it is slower: the
+ * completing arrival sums top_k rows in one thread, at the tail of the GEMM.
  *   x [T,d] bf16;  logits [T,E] fp32;  w_gate_up [E,d,2f] bf16;  w_down [E,f,d] bf16;
  *   out [T,d] bf16.
  * The status word at the start of the workspace is reset by the first kernel of every call and
@@ -210,7 +218,8 @@ MOE_API int moe_forward(const void* x, const float* logits, const void* w_gate_u
                 size_t workspace_bytes, moe_stream_t stream);
 
 /* moe_forward with DeepSeek-V3's router (moe_route_grouped) as step 1; steps 2-5 as in
- * moe_forward, with the same workspace (moe_workspace_size) and five launches.  bias [E] fp32 and
+ * moe_forward, with the same workspace (moe_workspace_size) and five launches (routing and the
+ * permutation never fuse with this router; four with MOE_FOLD_COMBINE=1).  bias [E] fp32 and
  * n_group, topk_group, scale as for moe_route_grouped. */
 MOE_API int moe_forward_grouped(const void* x, const float* logits, const float* bias, const void* w_gate_up,
                         const void* w_down, int T, int d, int f, int E, int top_k, int n_group,
@@ -271,7 +280,7 @@ MOE_API int moe_forward_grouped_host_batches(const void* const* x_hosts, const f
  * The intermediates live in one file-scope device array of MOE_NOALLOC_SCRATCH_BYTES that every
  * GPU loading this library holds until the process exits.  Shapes whose moe_workspace_size()
  * exceeds it are rejected with MOE_ERR_WORKSPACE (e.g. the Mixtral-8x7B shape fits up to
- * T = 629 tokens with top-2).  The first call on a device (and the first after that device's
+ * T = 628 tokens with top-2).  The first call on a device (and the first after that device's
  * context was destroyed and created again) looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream
  * capture.  Device ordinals >= 64 are rejected with MOE_ERR_UNSUPPORTED.  All calls on a device
@@ -344,11 +353,13 @@ MOE_API int moe_grouped_gemm_down_fp8(const void* h8, const float* sh, const voi
 
 /* The FP8 layer in one call: route (+ permute writing quantised x rows), FP8 gate+up GEMM
  * (+ SwiGLU), quantise h rows, FP8 down GEMM, combine — 5 launches (6 when routing and the
- * permutation run apart, see moe_forward_launch_count).  Inputs as for moe_forward, with the
+ * permutation run apart; one fewer with MOE_FOLD_COMBINE=1, which folds the combine into the down
+ * GEMM as for moe_forward; moe_forward_fp8_launch_count).  Inputs as for moe_forward, with the
  * weights given as moe_quantize_weights_fp8 codes and scales; workspace >=
  * moe_workspace_size_fp8() bytes, 256-byte aligned, its pieces at moe_workspace_layout_fp8()'s
  * offsets: status, idx, w, counts, offsets, src, dest, x8 [M,d], sx [M], h [M,f] bf16, h8 [M,f],
- * sh [M], y_perm [moe_down_ksplit_fp8(), M, d], total (14 values). */
+ * sh [M], y_perm [moe_down_ksplit_fp8(), M, d], total (14 values); the combine-fold counters
+ * int32 [T, d/64] lie between the end of y_perm and total. */
 MOE_API size_t moe_workspace_size_fp8(int T, int d, int f, int E, int top_k);
 MOE_API int moe_workspace_layout_fp8(int T, int d, int f, int E, int top_k, size_t* offsets_out);
 MOE_API int moe_down_ksplit_fp8(int T, int d, int f, int E, int top_k);
@@ -454,8 +465,9 @@ MOE_API int moe_forward_grouped_fp8b_host_batches(const void* const* x_hosts, co
 
 /* The FP8 layers with DeepSeek-V3's router (moe_route_grouped) as step 1: bias [E] fp32, n_group,
  * topk_group and scale as for moe_route_grouped; everything else as for moe_forward_fp8 /
- * moe_forward_fp8b, with the same workspaces.  6 launches (per-row / per-channel scales) or 7
- * (blockwise): routing and the permutation never fuse with this router. */
+ * moe_forward_fp8b, with the same workspaces.  6 launches (per-row / per-channel scales; 5 with
+ * MOE_FOLD_COMBINE=1) or 6–7 (blockwise, whose GEMM has no fold): routing and the permutation
+ * never fuse with this router. */
 MOE_API int moe_forward_grouped_fp8(const void* x, const float* logits, const float* bias, const void* w8_gate_up,
                                     const float* s_gate_up, const void* w8_down, const float* s_down, int T, int d,
                                     int f, int E, int top_k, int n_group, int topk_group, float scale, void* out,
@@ -475,7 +487,8 @@ MOE_API int moe_get_device_error(const void* status_or_workspace, int32_t* code)
  * permutation run as one kernel (E <= 32 and T*E <= 8192: each block routes every token itself to
  * build its histogram, so no grid-wide synchronisation is needed), else 5 (route, permute, two
  * grouped GEMMs, combine); 0 for T = 0; -1 for an invalid shape.  moe_forward_grouped always
- * makes 5.  The environment variable MOE_FUSE_ROUTE_PERMUTE=0 turns the fusion off. */
+ * makes 5.  In the environment, MOE_FUSE_ROUTE_PERMUTE=0 turns the route+permute fusion off (one
+ * launch more) and MOE_FOLD_COMBINE=1 folds the combine into the down GEMM (one launch fewer). */
 MOE_API int moe_forward_launch_count(int T, int E, int top_k);
 
 /* Message for the last non-OK return on the calling thread ("" if none). */

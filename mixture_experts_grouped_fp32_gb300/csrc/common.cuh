@@ -62,15 +62,84 @@ cudaError_t launch_route_grouped(const float* logits, const float* bias, int T, 
 cudaError_t launch_permute(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
                            int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest,
                            __nv_bfloat16* x_perm, int32_t* status, int num_sms, cudaStream_t s,
-                           uint8_t* x8 = nullptr, float* sx = nullptr);
+                           uint8_t* x8 = nullptr, float* sx = nullptr, int32_t* fold_cnt = nullptr,
+                           int fold_nblk = 0);
 // Steps 1+2 in one launch (softmax router): only when route_permute_fusable(T, E).
 bool route_permute_fusable(int T, int E);
 cudaError_t launch_route_permute(const float* logits, const __nv_bfloat16* x, int T, int d, int E, int k,
                                  int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* src,
                                  int32_t* dest, __nv_bfloat16* x_perm, int32_t* status, int num_sms,
-                                 cudaStream_t s, uint8_t* x8 = nullptr, float* sx = nullptr);
+                                 cudaStream_t s, uint8_t* x8 = nullptr, float* sx = nullptr,
+                                 int32_t* fold_cnt = nullptr, int fold_nblk = 0);
 cudaError_t launch_combine(const float* y, const float* w, const int32_t* dest, int T, int d, int k,
                            int ksplit, __nv_bfloat16* out, int32_t* status, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------------------
+// Step 5 folded into the down GEMM (moe_forward and moe_forward_fp8 when `cnt` is given).  The
+// combine needs all k rows (and K slices) of a token, which different CTAs store at different
+// times; instead of a grid-wide barrier each (token, 64-column block) has an arrival counter,
+// zeroed by the permute kernel of the same forward.  Every epilogue that has stored its part of
+// row r's block b fences its stores and adds its share to counter [src[r], b] (a block's parts
+// add up to kFoldWays per row and K slice); the arrival that completes k * ksplit rows folds the
+// block: out[t][block] = bf16(sum_j w[t,j] * sum_s y_s[dest[t,j]][block]) in slot and slice order,
+// the combine kernel's arithmetic.  No atomics touch the output, so the result is deterministic.
+struct FoldArgs {
+    int32_t* cnt = nullptr;         // [T, N / kFoldCols] counters; null = no fold (combine launched)
+    const int32_t* src = nullptr;   // [M] token of each permuted row
+    const int32_t* dest = nullptr;  // [T, k]
+    const float* w = nullptr;       // [T, k]
+    __nv_bfloat16* out = nullptr;   // [T, N]
+    int T = 0, k = 0;
+};
+constexpr int kFoldCols = 64;
+constexpr int kFoldWays = 2;  // arrival units per (row, block, K slice)
+
+// Fold token t's column block b (kFoldCols outputs) from the y_perm slices.
+static __device__ __noinline__ void fold_block(const FoldArgs& f, const float* __restrict__ y, long long M, int N,
+                                        int ksplit, int t, int b, int32_t* status) {
+    __threadfence();  // every arrival's stores before this thread's reads
+    const int c0 = b * kFoldCols;
+    float acc[kFoldCols];
+#pragma unroll
+    for (int c = 0; c < kFoldCols; ++c) acc[c] = 0.0f;
+    for (int j = 0; j < f.k; ++j) {
+        const int r = __ldg(f.dest + static_cast<size_t>(t) * f.k + j);
+        if (r < 0 || r >= M) {
+            flag_status(status, MOE_STATUS_BAD_DEST);
+            continue;
+        }
+        const float wj = __ldg(f.w + static_cast<size_t>(t) * f.k + j);
+        const float* yr = y + static_cast<size_t>(r) * N + c0;
+#pragma unroll
+        for (int c = 0; c < kFoldCols; c += 4) {
+            float4 a = __ldcg(reinterpret_cast<const float4*>(yr + c));
+            for (int s = 1; s < ksplit; ++s) {
+                const float4 a2 = __ldcg(reinterpret_cast<const float4*>(yr + static_cast<size_t>(s) * M * N + c));
+                a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
+            }
+            acc[c] += wj * a.x; acc[c + 1] += wj * a.y; acc[c + 2] += wj * a.z; acc[c + 3] += wj * a.w;
+        }
+    }
+    uint4* o = reinterpret_cast<uint4*>(f.out + static_cast<size_t>(t) * N + c0);
+#pragma unroll
+    for (int c = 0; c < kFoldCols; c += 8)
+        o[c / 8] = make_uint4(pack_bf16x2(acc[c], acc[c + 1]), pack_bf16x2(acc[c + 2], acc[c + 3]),
+                              pack_bf16x2(acc[c + 4], acc[c + 5]), pack_bf16x2(acc[c + 6], acc[c + 7]));
+}
+
+// Row r's part of block b is stored and fenced: count `inc` arrival units; fold if this completes
+// the block.
+__device__ __forceinline__ void fold_arrive(const FoldArgs& f, const float* y, long long M, int N, int ksplit,
+                                            int r, int b, int inc, int32_t* status) {
+    const int t = __ldg(f.src + r);
+    if (t < 0 || t >= f.T) {
+        flag_status(status, MOE_STATUS_BAD_SRC);
+        return;
+    }
+    const int target = kFoldWays * f.k * ksplit;
+    const int old = atomicAdd(f.cnt + static_cast<size_t>(t) * (N / kFoldCols) + b, inc);
+    if (old + inc == target) fold_block(f, y, M, N, ksplit, t, b, status);
+}
 
 // Largest number of K slices the down projection may be split into.
 constexpr int kMaxKSplit = 8;
@@ -107,6 +176,8 @@ struct GemmArgs {
     // Blockwise gate+up only: when set, out receives h's E4M3 codes [M, N] (uint8) and h_scale
     // [M, N/128] the power-of-two scale of each 128-wide block, h quantised in the epilogue.
     float* h_scale = nullptr;
+    // Down GEMM only: the combine folded into the epilogue (1-SM and SM-pair kernels; see FoldArgs).
+    FoldArgs fold;
 };
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& a, int num_sms, cudaStream_t s,
                                 const char** why);

@@ -165,7 +165,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     int K, int N, int E, int ksplit, int swap_max, int inject_stall,
                     const int4* __restrict__ xg, const int32_t* __restrict__ gsrc, int gT,
                     const float* __restrict__ a_scale, const float* __restrict__ b_scale, void* __restrict__ out,
-                    int32_t* __restrict__ status) {
+                    int32_t* __restrict__ status, const FoldArgs fold) {
     static_assert(!(GATHER && FP8), "the FP8 variant reads its activation codes with TMA");
     constexpr int BN_OUT = KIND == 0 ? 128 : 256;
     constexpr int BKE = FP8 ? 128 : BK;  // K values per stage (one 128-byte swizzle row)
@@ -596,6 +596,29 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 acc = 0;
                 acc_phase ^= 1u;
             }
+            if (KIND == 1 && fold.cnt != nullptr) {
+                // Combine fold (FoldArgs), after the accumulator is released: this thread's y stores
+                // are fenced, then its rows' blocks counted.  Normal items: the thread stored 256
+                // columns of its row (four 64-column blocks).  Swapped items: this warp stored the 32
+                // columns n0 + 32 q.. and n0 + 128 + 32 q.. (q = its lane quarter) of every row, half
+                // of two blocks; lane j % 32 counts row j once the warp's stores are fenced.
+                const int n0 = it.n_tile * BN_OUT;
+                const float* y0 = reinterpret_cast<const float*>(out);
+                __threadfence();
+                if (it.swap) {
+                    __syncwarp();
+                    const int bq = n0 / kFoldCols + (quarter >> 1);
+                    for (int j = lane; j < it.rows; j += 32) {
+                        if (n0 + 32 * quarter < N) fold_arrive(fold, y0, M, N, ksplit, it.row0 + j, bq, 1, status);
+                        if (n0 + 128 + 32 * quarter < N)
+                            fold_arrive(fold, y0, M, N, ksplit, it.row0 + j, bq + 128 / kFoldCols, 1, status);
+                    }
+                } else if (r_local < it.rows) {
+                    for (int q = 0; q < BN_OUT / kFoldCols; ++q)
+                        if (n0 + q * kFoldCols < N)
+                            fold_arrive(fold, y0, M, N, ksplit, it.row0 + r_local, n0 / kFoldCols + q, kFoldWays, status);
+                }
+            }
         }
     }
 
@@ -655,7 +678,7 @@ cudaError_t launch_kind(const GemmArgs& a, int num_sms, cudaStream_t s, const ch
     return launch_k(KIND == 0 ? kPdlGateUp : kPdlDown, grouped_gemm_kernel<KIND, GATHER, FP8>, dim3(num_sms),
                     dim3(GATHER ? GATHER_THREADS : NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB, a.offsets, a.M, a.K,
                     a.N, a.E, ksplit, swap_max, a.inject_stall, reinterpret_cast<const int4*>(a.A), a.gather_src,
-                    a.gather_T, a.a_scale, a.b_scale, a.out, a.status);
+                    a.gather_T, a.a_scale, a.b_scale, a.out, a.status, a.fold);
 }
 
 }  // namespace

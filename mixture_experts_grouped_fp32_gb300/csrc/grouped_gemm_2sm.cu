@@ -372,7 +372,7 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                         int K, int N, int E, int ksplit, int swap_max, int layout_mode, int split_req,
                         const int4* __restrict__ xg, const int32_t* __restrict__ gsrc, int gT,
                         const float* __restrict__ a_scale, const float* __restrict__ b_scale, void* __restrict__ out,
-                        int32_t* __restrict__ status) {
+                        int32_t* __restrict__ status, const FoldArgs fold) {
     static_assert(!(GATHER && FP8), "the FP8 variant reads its activation codes with TMA");
     constexpr int BN_OUT = Tiling<KIND>::BN_OUT;
     constexpr int BKE = FP8 ? 128 : BK;  // K values per stage (one 128-byte swizzle row)
@@ -943,6 +943,29 @@ grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 acc = 0;
                 acc_phase ^= 1u;
             }
+            if (KIND == 1 && fold.cnt != nullptr) {
+                // Combine fold (FoldArgs), after the accumulator is released: this thread's y stores
+                // are fenced, then its rows' blocks counted.  Normal items: the thread stored all 256
+                // columns of its row (four 64-column blocks).  Swapped items: this warp stored the 32
+                // columns c0 + 32 q.. and c0 + 256 + 32 q.. (c0 = the CTA's first column, q = its
+                // lane quarter) of every row of the chunk, half of two blocks; lane j % 32 counts row j.
+                const float* y0 = reinterpret_cast<const float*>(out);
+                __threadfence();
+                if (SWAPCAP && it.swap) {
+                    __syncwarp();
+                    const int c0 = it.n_tile * super_n<KIND>() + 128 * rank + 32 * quarter;
+                    for (int j = lane; j < it.rows; j += 32) {
+                        if (c0 < N) fold_arrive(fold, y0, M, N, ksplit, it.row0 + j, c0 / kFoldCols, 1, status);
+                        if (c0 + 256 < N)
+                            fold_arrive(fold, y0, M, N, ksplit, it.row0 + j, (c0 + 256) / kFoldCols, 1, status);
+                    }
+                } else if (r_local < it.rows) {
+                    const int n0 = it.n_tile * BN_OUT;
+                    for (int q = 0; q < BN_OUT / kFoldCols; ++q)
+                        if (n0 + q * kFoldCols < N)
+                            fold_arrive(fold, y0, M, N, ksplit, it.row0 + r_local, n0 / kFoldCols + q, kFoldWays, status);
+                }
+            }
           }
         }
     }
@@ -1010,7 +1033,7 @@ cudaError_t launch_pair_kind(const GemmArgs& a, int num_sms, cudaStream_t s, con
                     dim3(grid), dim3(GATHER ? GATHER_THREADS : NUM_THREADS), SMEM_BYTES, s, mA, mA32, mB, a.offsets,
                     a.M, a.K, a.N, a.E, ksplit, swap_max, a.pair_layout, a.pair_split,
                     reinterpret_cast<const int4*>(a.A), a.gather_src, a.gather_T, a.a_scale, a.b_scale, a.out,
-                    a.status);
+                    a.status, a.fold);
 }
 
 }  // namespace

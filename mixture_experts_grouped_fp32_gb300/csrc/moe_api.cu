@@ -179,6 +179,18 @@ int pair_swap_max_rows() {
     return x < 0 ? 0 : (x > 128 ? 128 : x);
 }
 
+// Whether moe_forward (and moe_forward_fp8) fold the combine into the down GEMM's epilogue instead of
+// launching it (FoldArgs in common.cuh: per-(token, 64-column block) arrival counters, the last
+// arrival sums the token's rows in slot order).  Off by default, MOE_FOLD_COMBINE=1 turns it on:
+// measured slower at every bench workload (ms/layer, combine launch -> fold: Mixtral T=32 0.414 ->
+// 0.428, T=512 0.506 -> 0.561, T=4096 1.94 -> 1.98, softmax-routed DeepSeek shape 2.11 -> 6.03,
+// DeepSeek-V3 router 1.61 -> 4.52): a completing arrival sums the token's k rows in one thread,
+// and at the end of the kernel those sums sit on its critical path.
+bool fold_combine() {
+    const char* v = std::getenv("MOE_FOLD_COMBINE");
+    return v && v[0] == '1';
+}
+
 // Whether moe_forward's gate+up GEMM gathers its activation rows from x by src[] (the permute then
 // writes no x_perm).  Off by default: measured slower than writing x_perm and reading it with TMA
 // (Mixtral shape T=4096 2.81 vs 2.04 ms per layer, T=512 0.68 vs 0.53); MOE_GATHER=1 turns it on.
@@ -236,7 +248,7 @@ int down_ksplit(int T, int d, int f, int E, int k, bool fp8 = false, bool blocks
 
 // moe_forward's workspace: 256-byte aligned pieces in this order.
 struct Layout {
-    size_t status, idx, w, counts, offsets, src, dest, x_perm, h, y_perm, total;
+    size_t status, idx, w, counts, offsets, src, dest, x_perm, h, y_perm, fold, total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -255,6 +267,7 @@ Layout layout(int T, int d, int f, int E, int k) {
     L.x_perm = o; o = align256(o + M * d * 2);
     L.h = o; o = align256(o + M * f * 2);
     L.y_perm = o; o = align256(o + static_cast<size_t>(down_ksplit(T, d, f, E, k)) * M * d * 4);
+    L.fold = o; o = align256(o + static_cast<size_t>(T) * (d / kFoldCols) * 4);  // combine-fold counters
     L.total = o;
     return L;
 }
@@ -262,7 +275,7 @@ Layout layout(int T, int d, int f, int E, int k) {
 // The FP8 layer's workspace: the same first pieces, then x8 [M,d] codes, sx [M], h [M,f] bf16,
 // h8 [M,f] codes, sh [M], y_perm.
 struct Layout8 {
-    size_t status, idx, w, counts, offsets, src, dest, x8, sx, h, h8, sh, y_perm, total;
+    size_t status, idx, w, counts, offsets, src, dest, x8, sx, h, h8, sh, y_perm, fold, total;
 };
 
 // blocks = true: the blockwise layer, whose sx and sh hold one scale per 128-wide block.
@@ -284,6 +297,7 @@ Layout8 layout_fp8(int T, int d, int f, int E, int k, bool blocks = false) {
     L.h8 = o; o = align256(o + M * f);
     L.sh = o; o = align256(o + M * nsh * 4);
     L.y_perm = o; o = align256(o + static_cast<size_t>(down_ksplit(T, d, f, E, k, true, blocks)) * M * d * 4);
+    L.fold = o; o = align256(o + static_cast<size_t>(T) * (d / kFoldCols) * 4);  // combine-fold counters
     L.total = o;
     return L;
 }
@@ -337,9 +351,12 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
     cudaError_t e;
     const bool gather = gather_rows();
     __nv_bfloat16* xp = gather ? nullptr : x_perm;  // no x_perm when the GEMM gathers
+    int32_t* fold_cnt = fold_combine() ? at<int32_t>(ws, L.fold) : nullptr;  // zeroed by the permute
+    const int fold_nblk = d / kFoldCols;
     if (!router.grouped && fuse_route_permute(T, E)) {
         if ((e = launch_route_permute(logits, static_cast<const __nv_bfloat16*>(x), T, d, E, k, idx, w, counts,
-                                      offsets, src, dest, xp, status, num_sms, s)) != cudaSuccess)
+                                      offsets, src, dest, xp, status, num_sms, s, nullptr, nullptr, fold_cnt,
+                                      fold_nblk)) != cudaSuccess)
             return launched(e, "route+permute");
     } else {
         e = router.grouped ? launch_route_grouped(logits, router.bias, T, E, k, router.n_group, router.topk_group,
@@ -347,7 +364,7 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
                            : launch_route(logits, T, E, k, idx, w, status, s);
         if (e != cudaSuccess) return launched(e, "route");
         if ((e = launch_permute(idx, static_cast<const __nv_bfloat16*>(x), T, d, E, k, counts, offsets, src,
-                                dest, xp, status, num_sms, s)) != cudaSuccess)
+                                dest, xp, status, num_sms, s, nullptr, nullptr, fold_cnt, fold_nblk)) != cudaSuccess)
             return launched(e, "permute");
     }
     const char* why = "";
@@ -364,10 +381,11 @@ int run_layer(const void* x, const float* logits, const void* wgu, const void* w
     GemmArgs g2{h, wd, offsets, M, f, d, E, y, status, ksplit, swap_max, use_pair(M, E, d, 1), pair_swap_max_rows(),
                 pair_layout(), pair_split()};
     g2.inject_stall = g1.inject_stall;
+    if (fold_cnt) g2.fold = FoldArgs{fold_cnt, src, dest, w, static_cast<__nv_bfloat16*>(out), T, k};
     if ((e = launch_grouped_gemm(1, g2, num_sms, s, &why)) != cudaSuccess)
         return fail(MOE_ERR_CUDA, "down GEMM: %s (%s)", why, cudaGetErrorString(e));
-    if ((e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) !=
-        cudaSuccess)
+    if (!fold_cnt &&
+        (e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) != cudaSuccess)
         return launched(e, "combine");
     return ok();
 }
@@ -398,10 +416,13 @@ int run_layer_fp8(const void* x, const float* logits, const void* wgu8, const fl
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
     uint8_t* perm_x8 = blocks ? nullptr : x8;  // per-row scales: the permutation quantises x itself
     float* perm_sx = blocks ? nullptr : sx;
+    // The combine folds into the per-row-scaled down GEMM (the blockwise kernel has no fold).
+    int32_t* fold_cnt = (!blocks && fold_combine()) ? at<int32_t>(ws, L.fold) : nullptr;
+    const int fold_nblk = d / kFoldCols;
     cudaError_t e;
     if (!router.grouped && fuse_route_permute(T, E)) {
         if ((e = launch_route_permute(logits, xb, T, d, E, k, idx, w, counts, offsets, src, dest, nullptr, status,
-                                      num_sms, s, perm_x8, perm_sx)) != cudaSuccess)
+                                      num_sms, s, perm_x8, perm_sx, fold_cnt, fold_nblk)) != cudaSuccess)
             return launched(e, "route+permute");
     } else {
         e = router.grouped ? launch_route_grouped(logits, router.bias, T, E, k, router.n_group, router.topk_group,
@@ -409,7 +430,7 @@ int run_layer_fp8(const void* x, const float* logits, const void* wgu8, const fl
                            : launch_route(logits, T, E, k, idx, w, status, s);
         if (e != cudaSuccess) return launched(e, "route");
         if ((e = launch_permute(idx, xb, T, d, E, k, counts, offsets, src, dest, nullptr, status, num_sms, s, perm_x8,
-                                perm_sx)) != cudaSuccess)
+                                perm_sx, fold_cnt, fold_nblk)) != cudaSuccess)
             return launched(e, "permute");
     }
     if (blocks && (e = launch_quantize_rows_fp8b(xb, src, M, d, T, x8, sx, status, s)) != cudaSuccess)
@@ -445,9 +466,10 @@ int run_layer_fp8(const void* x, const float* logits, const void* wgu8, const fl
     g2.fp8_blocks = blocks;
     g2.a_scale = sh;
     g2.b_scale = sd;
+    if (fold_cnt) g2.fold = FoldArgs{fold_cnt, src, dest, w, static_cast<__nv_bfloat16*>(out), T, k};
     if ((rc = gemm(1, g2, blocks ? "blockwise FP8 down GEMM" : "FP8 down GEMM"))) return rc;
-    if ((e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) !=
-        cudaSuccess)
+    if (!fold_cnt &&
+        (e = launch_combine(y, w, dest, T, d, k, ksplit, static_cast<__nv_bfloat16*>(out), status, s)) != cudaSuccess)
         return launched(e, "combine");
     return ok();
 }
@@ -610,7 +632,7 @@ int moe_version(void) { return 100; }
 int moe_forward_launch_count(int T, int E, int top_k) {
     if (check_shape(T, -1, 0, E, top_k, false) != MOE_OK) return -1;
     if (T == 0) return 0;
-    return fuse_route_permute(T, E) ? 4 : 5;
+    return (fuse_route_permute(T, E) ? 4 : 5) - (fold_combine() ? 1 : 0);
 }
 
 const char* moe_last_error_string(void) { return g_err; }
@@ -958,7 +980,7 @@ int moe_gemm_pair_mode_fp8(int T, int d, int f, int E, int top_k, int kind) {
 int moe_forward_fp8_launch_count(int T, int E, int top_k) {
     if (check_shape(T, -1, 0, E, top_k, false) != MOE_OK) return -1;
     if (T == 0) return 0;
-    return fuse_route_permute(T, E) ? 5 : 6;
+    return (fuse_route_permute(T, E) ? 5 : 6) - (fold_combine() ? 1 : 0);
 }
 
 int moe_permute_fp8(const int32_t* idx, const void* x, int T, int d, int E, int top_k, int32_t* counts,

@@ -73,7 +73,8 @@ permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int
                int k, int tok_per_block, int32_t* __restrict__ counts,
                int32_t* __restrict__ offsets, int32_t* __restrict__ src,
                int32_t* __restrict__ dest, uint4* __restrict__ x_perm, uint2* __restrict__ x8,
-               float* __restrict__ sx, int32_t* __restrict__ status) {
+               float* __restrict__ sx, int32_t* __restrict__ status, int32_t* __restrict__ fold_cnt,
+               int fold_nblk) {
     __shared__ int tot[kMaxE];      // assignments per expert, all tokens
     __shared__ int before[kMaxE];   // ... from tokens before this block's chunk
     __shared__ int off[kMaxE + 1];  // exclusive scan of tot
@@ -94,6 +95,10 @@ permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int
     const int t0 = blockIdx.x * tok_per_block;
     const int t1 = min(T, t0 + tok_per_block);
     const int nA = T * k, a0 = t0 * k;
+    // The down GEMM's combine-fold counters of this block's tokens start at zero.
+    if (fold_cnt != nullptr)
+        for (int i = tid; i < (t1 - t0) * fold_nblk; i += kPermThreads)
+            fold_cnt[static_cast<size_t>(t0) * fold_nblk + i] = 0;
 
     // Histogram of all assignments (tot) and of those before this block's chunk (before).
     if (E <= 32) {
@@ -248,7 +253,8 @@ route_permute_kernel(const float* __restrict__ logits, const uint4* __restrict__
                      int tok_per_block, int32_t* __restrict__ idx, float* __restrict__ w,
                      int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ src,
                      int32_t* __restrict__ dest, uint4* __restrict__ x_perm, uint2* __restrict__ x8,
-                     float* __restrict__ sx, int32_t* __restrict__ status) {
+                     float* __restrict__ sx, int32_t* __restrict__ status, int32_t* __restrict__ fold_cnt,
+                     int fold_nblk) {
     __shared__ int tot[kFuseMaxE];
     __shared__ int before[kFuseMaxE];
     __shared__ int off[kFuseMaxE + 1];
@@ -266,6 +272,9 @@ route_permute_kernel(const float* __restrict__ logits, const uint4* __restrict__
     __syncthreads();
     const int t0 = blockIdx.x * tok_per_block;
     const int t1 = min(T, t0 + tok_per_block);
+    if (fold_cnt != nullptr)  // the down GEMM's combine-fold counters of this block's tokens
+        for (int i = tid; i < (t1 - t0) * fold_nblk; i += kPermThreads)
+            fold_cnt[static_cast<size_t>(t0) * fold_nblk + i] = 0;
 
     // Route every token (thread per token); warp-aggregated histogram updates.
     for (int base = warp * 32; base < T; base += kPermThreads) {
@@ -396,26 +405,26 @@ bool route_permute_fusable(int T, int E) {
 cudaError_t launch_route_permute(const float* logits, const __nv_bfloat16* x, int T, int d, int E, int k,
                                  int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* src,
                                  int32_t* dest, __nv_bfloat16* x_perm, int32_t* status, int num_sms,
-                                 cudaStream_t s, uint8_t* x8, float* sx) {
+                                 cudaStream_t s, uint8_t* x8, float* sx, int32_t* fold_cnt, int fold_nblk) {
     int tpb = (T + 4 * num_sms - 1) / (4 * num_sms);
     tpb = tpb < 1 ? 1 : (tpb > kMaxTokPerBlock ? kMaxTokPerBlock : tpb);
     const int blocks = (T + tpb - 1) / tpb;
     return launch_k(kPdlRoute, route_permute_kernel, dim3(blocks), dim3(kPermThreads), 0, s, logits,
                     reinterpret_cast<const uint4*>(x), T, d, E, k, tpb, idx, w, counts, offsets, src, dest,
-                    reinterpret_cast<uint4*>(x_perm), reinterpret_cast<uint2*>(x8), sx, status);
+                    reinterpret_cast<uint4*>(x_perm), reinterpret_cast<uint2*>(x8), sx, status, fold_cnt, fold_nblk);
 }
 
 cudaError_t launch_permute(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
                            int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest,
                            __nv_bfloat16* x_perm, int32_t* status, int num_sms, cudaStream_t s, uint8_t* x8,
-                           float* sx) {
+                           float* sx, int32_t* fold_cnt, int fold_nblk) {
     // About four blocks per SM for the row copies, at most kMaxTokPerBlock tokens per block.
     int tpb = (T + 4 * num_sms - 1) / (4 * num_sms);
     tpb = tpb < 1 ? 1 : (tpb > kMaxTokPerBlock ? kMaxTokPerBlock : tpb);
     const int blocks = (T + tpb - 1) / tpb;
     return launch_k(kPdlPermute, permute_kernel, dim3(blocks), dim3(kPermThreads), 0, s, idx,
                     reinterpret_cast<const uint4*>(x), T, d, E, k, tpb, counts, offsets, src, dest,
-                    reinterpret_cast<uint4*>(x_perm), reinterpret_cast<uint2*>(x8), sx, status);
+                    reinterpret_cast<uint4*>(x_perm), reinterpret_cast<uint2*>(x8), sx, status, fold_cnt, fold_nblk);
 }
 
 }  // namespace moe

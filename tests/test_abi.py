@@ -49,6 +49,12 @@ def test_version_and_launch_count(lib):
         assert lib.moe_forward_launch_count(32, 8, 2) == 5
     finally:
         del os.environ["MOE_FUSE_ROUTE_PERMUTE"]
+    os.environ["MOE_FOLD_COMBINE"] = "1"  # the combine folded into the down GEMM: one launch fewer
+    try:
+        assert lib.moe_forward_launch_count(32, 8, 2) == 3 and lib.moe_forward_launch_count(4096, 8, 2) == 4
+        assert lib.moe_forward_fp8_launch_count(32, 8, 2) == 4
+    finally:
+        del os.environ["MOE_FOLD_COMBINE"]
 
 
 def _err(lib):
@@ -72,6 +78,7 @@ def test_workspace_layout_matches_the_documented_order(lib):
                          ("x_perm", M * d * 2), ("h", M * f * 2), ("y_perm", S * M * d * 4)]:
         expect[name] = o
         o = up(o + nbytes)
+    o = up(o + T * (d // 64) * 4)  # the combine-fold counters, one per token and 64 output columns
     expect["total"] = o
     assert L == expect
     assert moe.workspace_size(T, d, f, E, k) == o
@@ -269,6 +276,7 @@ def test_fp8_workspace_layout_and_validation(lib):
                          ("y_perm", S * M * d * 4)]:
         expect[name] = o
         o = up(o + nbytes)
+    o = up(o + T * (d // 64) * 4)  # the combine-fold counters
     expect["total"] = o
     assert L == expect
     assert moe.workspace_size_fp8(T, d, f, E, k) == o

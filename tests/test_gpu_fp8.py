@@ -280,7 +280,7 @@ def test_forward_fp8_matches_oracle(moe, oracle, monkeypatch, w, mode):
 
 
 def test_forward_fp8_launch_count(moe):
-    assert moe.forward_fp8_launch_count(64, 8, 2) == 5
+    assert moe.forward_fp8_launch_count(64, 8, 2) == 5      # route+permute fused
     assert moe.forward_fp8_launch_count(2048, 256, 8) == 6
     assert moe.forward_fp8_launch_count(0, 8, 2) == 0
 

@@ -99,6 +99,32 @@ def test_forward_matches_oracle(moe, oracle, w, mode):
     assert_layer_close(out.float().cpu().numpy(), ref, w.name)
 
 
+@pytest.mark.parametrize("mode", ["default", "noswap", "pair", "pairswap", "pairsplit", "ksplit3"])
+@pytest.mark.parametrize("w", [CASES[1], CASES[3], CASES[4], CASES[5], CASES[6], CASES[8], CASES[9], CASES[10]],
+                         ids=lambda w: w.name)
+def test_folded_combine_equals_combine_kernel(moe, w, mode, monkeypatch):
+    """The combine folded into the down GEMM (MOE_FOLD_COMBINE=1: the last arrival of a token's
+    64-column block sums its k rows in slot order) gives the combine kernel's output bit for bit,
+    for every down-GEMM form (1-SM normal and swapped items, SM-pair normal and swapped items, K
+    split in three), and in a CUDA graph with the same node count moe_forward_launch_count states."""
+    for key in ENV_KNOBS:
+        monkeypatch.delenv(key, raising=False)
+    for key, val in MODES[mode].items():
+        monkeypatch.setenv(key, val)
+    logits, x, wgu, wd = case_inputs(w, seed=8)
+    dev = torch.device(DEV)
+    args = (x.to(dev), logits.to(dev), wgu.to(dev), wd.to(dev), w.k)
+    ref = moe.forward(*args)
+    monkeypatch.setenv("MOE_FOLD_COMBINE", "1")
+    ws = torch.empty(moe.workspace_size(w.T, w.d, w.f, w.E, w.k), dtype=torch.uint8, device=dev)
+    ws.fill_(0x7F)  # counters must be zeroed by the permute
+    for _ in range(2):  # the second call reuses counters the first one left at their targets
+        out = moe.forward(*args, workspace=ws)
+        torch.cuda.synchronize()
+        assert moe.get_device_error(ws) == 0
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"{w.name} [{mode}]"
+
+
 def test_forward_is_deterministic(moe):
     w = Workload("det", 300, 512, 768, 8, 2)
     logits, x, wgu, wd = case_inputs(w, seed=3)
@@ -152,12 +178,15 @@ def test_route_nan_logits_order(moe, oracle, E, k):
     assert_close(w.cpu().numpy()[clean], rw[clean], 1e-6, 0, "route weights, finite rows")
 
 
-def test_fused_route_permute_nan_logits_order(moe, oracle):
+def test_fused_route_permute_nan_logits_order(moe, oracle, monkeypatch):
     # E <= 32 and T*E <= 8192: moe_forward routes inside the permute kernel (one thread per token).
     w = Workload("nan_fused", 64, 128, 128, 8, 2)
     _, x, wgu, wd = case_inputs(w, seed=5)
     logits = _nan_logits(w.T, w.E, seed=77)
-    assert moe.forward_launch_count(w.T, w.E, w.k) == 4
+    fused = moe.forward_launch_count(w.T, w.E, w.k)
+    monkeypatch.setenv("MOE_FUSE_ROUTE_PERMUTE", "0")
+    assert moe.forward_launch_count(w.T, w.E, w.k) == fused + 1
+    monkeypatch.delenv("MOE_FUSE_ROUTE_PERMUTE")
     _, v, ws = _forward_and_views(moe, w, logits, x, wgu, wd)
     ridx, rw = oracle.route(logits.numpy(), w.k)
     assert np.array_equal(v["idx"].cpu().numpy(), ridx)
