@@ -92,21 +92,21 @@ AUTO_STEPS_MIN, AUTO_STEPS_MAX = 50, 4000
 # kernel source with the recorded hash; reported only while the GEMM source still hashes to that
 # value, else null.
 
-_TRAFFIC_HASH = "42ce3bbe1c07d68c"  # GEMM source hash the captures below were taken at
+_TRAFFIC_HASH = "a50adcb350358d68"  # GEMM source hash the captures below were taken at
 _TRAFFIC_HASH_FP8B = "2cc65fcf7ddc68c6"  # ... and that of the blockwise FP8 kernel's sources
 MEASURED_TRAFFIC = {
-    ("deepseek_e32_t256", "gateup_swiglu"): (1919832832, _TRAFFIC_HASH),
-    ("deepseek_e32_t256", "down"): (1009043712, _TRAFFIC_HASH),
-    ("deepseek_v3like_e32_t1024", "gateup_swiglu"): (2391786496, _TRAFFIC_HASH),
-    ("deepseek_v3like_e32_t1024", "down"): (1211820544, _TRAFFIC_HASH),
-    ("mixtral_t32", "gateup_swiglu"): (1884708096, _TRAFFIC_HASH),
-    ("mixtral_t32", "down"): (944412160, _TRAFFIC_HASH),
-    ("mixtral_t4096", "gateup_swiglu"): (3664941824, _TRAFFIC_HASH),
-    ("mixtral_t4096", "down"): (1816316160, _TRAFFIC_HASH),
-    ("mixtral_t512_skew40", "gateup_swiglu"): (1917530368, _TRAFFIC_HASH),
-    ("mixtral_t512_skew40", "down"): (983433728, _TRAFFIC_HASH),
-    ("mixtral_t512", "gateup_swiglu"): (1917100288, _TRAFFIC_HASH),
-    ("mixtral_t512", "down"): (982793472, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "gateup_swiglu"): (1919805440, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "down"): (1010249216, _TRAFFIC_HASH),
+    ("deepseek_v3like_e32_t1024", "gateup_swiglu"): (2392060160, _TRAFFIC_HASH),
+    ("deepseek_v3like_e32_t1024", "down"): (1213201152, _TRAFFIC_HASH),
+    ("mixtral_t32", "gateup_swiglu"): (1884503296, _TRAFFIC_HASH),
+    ("mixtral_t32", "down"): (946020864, _TRAFFIC_HASH),
+    ("mixtral_t4096", "gateup_swiglu"): (3273731072, _TRAFFIC_HASH),
+    ("mixtral_t4096", "down"): (1626119680, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "gateup_swiglu"): (1917325056, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "down"): (984870656, _TRAFFIC_HASH),
+    ("mixtral_t512", "gateup_swiglu"): (1917185792, _TRAFFIC_HASH),
+    ("mixtral_t512", "down"): (984192000, _TRAFFIC_HASH),
     ("deepseek_e32_t256", "gateup_swiglu_fp8b"): (966528512, _TRAFFIC_HASH_FP8B),
     ("deepseek_e32_t256", "down_fp8b"): (535162112, _TRAFFIC_HASH_FP8B),
     ("deepseek_v3like_e32_t1024", "gateup_swiglu_fp8b"): (1022521856, _TRAFFIC_HASH_FP8B),
@@ -119,18 +119,18 @@ MEASURED_TRAFFIC = {
     ("mixtral_t512_skew40", "down_fp8b"): (515716864, _TRAFFIC_HASH_FP8B),
     ("mixtral_t512", "gateup_swiglu_fp8b"): (963255296, _TRAFFIC_HASH_FP8B),
     ("mixtral_t512", "down_fp8b"): (611966720, _TRAFFIC_HASH_FP8B),
-    ("deepseek_e32_t256", "gateup_swiglu_fp8"): (966083840, _TRAFFIC_HASH),
-    ("deepseek_e32_t256", "down_fp8"): (534113792, _TRAFFIC_HASH),
-    ("deepseek_v3like_e32_t1024", "gateup_swiglu_fp8"): (1141912576, _TRAFFIC_HASH),
-    ("deepseek_v3like_e32_t1024", "down_fp8"): (724014080, _TRAFFIC_HASH),
-    ("mixtral_t32", "gateup_swiglu_fp8"): (945154048, _TRAFFIC_HASH),
-    ("mixtral_t32", "down_fp8"): (474109440, _TRAFFIC_HASH),
-    ("mixtral_t4096", "gateup_swiglu_fp8"): (1239584256, _TRAFFIC_HASH),
-    ("mixtral_t4096", "down_fp8"): (799462912, _TRAFFIC_HASH),
-    ("mixtral_t512_skew40", "gateup_swiglu_fp8"): (972034816, _TRAFFIC_HASH),
-    ("mixtral_t512_skew40", "down_fp8"): (498305536, _TRAFFIC_HASH),
-    ("mixtral_t512", "gateup_swiglu_fp8"): (971907328, _TRAFFIC_HASH),
-    ("mixtral_t512", "down_fp8"): (497746176, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "gateup_swiglu_fp8"): (966086656, _TRAFFIC_HASH),
+    ("deepseek_e32_t256", "down_fp8"): (535560192, _TRAFFIC_HASH),
+    ("deepseek_v3like_e32_t1024", "gateup_swiglu_fp8"): (1142837248, _TRAFFIC_HASH),
+    ("deepseek_v3like_e32_t1024", "down_fp8"): (725435136, _TRAFFIC_HASH),
+    ("mixtral_t32", "gateup_swiglu_fp8"): (946222592, _TRAFFIC_HASH),
+    ("mixtral_t32", "down_fp8"): (475548416, _TRAFFIC_HASH),
+    ("mixtral_t4096", "gateup_swiglu_fp8"): (1215292672, _TRAFFIC_HASH),
+    ("mixtral_t4096", "down_fp8"): (788060672, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "gateup_swiglu_fp8"): (972208384, _TRAFFIC_HASH),
+    ("mixtral_t512_skew40", "down_fp8"): (499746560, _TRAFFIC_HASH),
+    ("mixtral_t512", "gateup_swiglu_fp8"): (971900672, _TRAFFIC_HASH),
+    ("mixtral_t512", "down_fp8"): (499183872, _TRAFFIC_HASH),
 }
 GEMM_SOURCES = ("mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm.cu",
                 "mixture_experts_grouped_fp32_gb300/csrc/grouped_gemm_2sm.cu",

@@ -10,16 +10,17 @@
 // chunk of tokens, how many earlier tokens chose each expert.  It then ranks its chunk's
 // assignments, writes src/dest, and copies its tokens' x rows to their k destinations with
 // 16-byte vector loads and stores.
+#include <cstdlib>
+
 #include "common.cuh"
 #include "fp8.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kPermThreads = 256;
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;
-constexpr int kMaxTokPerBlock = 16;
+constexpr int kMaxTokPerBlock = 64;
 constexpr int kCopyBatch = 4;
 constexpr long long kFuseMaxLogits = 8192;  // route+permute fusion: T*E at most this
 
@@ -27,8 +28,9 @@ constexpr long long kFuseMaxLogits = 8192;  // route+permute fusion: T*E at most
 // values, fp8.cuh's per-row arithmetic) and write its codes and scale to each of its k permuted
 // rows (rows < 0, from an invalid expert id, are skipped).  The block splits into 1, 2, 4 or 8
 // teams, one token per team at a time, so a block with a single token still spreads its row over
-// all 256 threads: a pass for the absmax (team reduction through shared memory), a second (from
+// all the block's threads: a pass for the absmax (team reduction through shared memory), a second (from
 // L1) for the codes.  Called by every thread of the block.
+template <int kPermThreads>
 __device__ __forceinline__ void quantize_perm_rows(const uint4* __restrict__ x, int t0, int t1, int d, int k,
                                                    const int* crow, uint2* __restrict__ x8, float* __restrict__ sx,
                                                    float* red) {
@@ -68,6 +70,7 @@ __device__ __forceinline__ void quantize_perm_rows(const uint4* __restrict__ x, 
     }
 }
 
+template <int kPermThreads>
 __global__ void __launch_bounds__(kPermThreads)
 permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int T, int d, int E,
                int k, int tok_per_block, int32_t* __restrict__ counts,
@@ -197,7 +200,7 @@ permute_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int
 
     if (x8 != nullptr) {
         __shared__ float red[kPermThreads / 32];
-        quantize_perm_rows(x, t0, t1, d, k, crow, x8, sx, red);
+        quantize_perm_rows<kPermThreads>(x, t0, t1, d, k, crow, x8, sx, red);
         return;
     }
     // Row copies: x[t] -> x_perm[row(t, j)] for each slot j, 16 bytes per access.  Each thread
@@ -248,6 +251,7 @@ __device__ __forceinline__ bool logit_before(float av, int ai, float bv, int bi)
     return av > bv || ((av == bv || an) && ai < bi);
 }
 
+template <int kPermThreads>
 __global__ void __launch_bounds__(kPermThreads)
 route_permute_kernel(const float* __restrict__ logits, const uint4* __restrict__ x, int T, int d, int E, int k,
                      int tok_per_block, int32_t* __restrict__ idx, float* __restrict__ w,
@@ -369,7 +373,7 @@ route_permute_kernel(const float* __restrict__ logits, const uint4* __restrict__
     __syncthreads();
     if (x8 != nullptr) {
         __shared__ float red[kPermThreads / 32];
-        quantize_perm_rows(x, t0, t1, d, k, crow, x8, sx, red);
+        quantize_perm_rows<kPermThreads>(x, t0, t1, d, k, crow, x8, sx, red);
         return;
     }
     if (x_perm == nullptr) return;  // the gate+up GEMM gathers x rows itself
@@ -402,15 +406,67 @@ bool route_permute_fusable(int T, int E) {
     return E <= kFuseMaxE && static_cast<long long>(T) * E <= kFuseMaxLogits;
 }
 
+// Threads per permutation block.  Every block histograms all T*k assignments itself, so fewer,
+// larger blocks repeat that work fewer times: with E <= 32 (the warp-aggregated histogram) the
+// kernel uses 1024-thread blocks, one per SM, else 256-thread blocks, four per SM.  Measured
+// (ms/layer, 256 -> 1024 threads): Mixtral shape T=4096 1.938 -> 1.925 (permute 37 -> 27 us), e4m3
+// 1.127 -> 1.116, T=512 and T=32 unchanged; softmax-routed DeepSeek shape (E=256) 2.102 -> 2.155
+// although its permute alone ran 59 -> 53 us, DeepSeek-V3 router 1.574 -> 1.570.
+// MOE_PERM_THREADS=256/512/1024 overrides the choice.
+static int perm_threads(int E) {
+    const char* v = std::getenv("MOE_PERM_THREADS");
+    const int n = v ? std::atoi(v) : 0;
+    if (n == 256 || n == 512 || n == 1024) return n;
+    return E <= 32 ? 1024 : 256;
+}
+
+// Tokens per block: the grid fills the GPU with 256-thread blocks four to an SM (or the same threads
+// as fewer, larger blocks), at most kMaxTokPerBlock tokens and at most one assignment per thread.
+static int perm_tokens_per_block(int T, int num_sms, int nt) {
+    const int per_sm = 1024 / nt;
+    const int cap = nt == 256 ? 16 : kMaxTokPerBlock;
+    int tpb = (T + per_sm * num_sms - 1) / (per_sm * num_sms);
+    return tpb < 1 ? 1 : (tpb > cap ? cap : tpb);
+}
+
+template <int NT>
+static cudaError_t launch_route_permute_nt(const float* logits, const __nv_bfloat16* x, int T, int d, int E, int k,
+                                           int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* src,
+                                           int32_t* dest, __nv_bfloat16* x_perm, int32_t* status, int num_sms,
+                                           cudaStream_t s, uint8_t* x8, float* sx, int32_t* fold_cnt, int fold_nblk) {
+    const int tpb = perm_tokens_per_block(T, num_sms, NT);
+    const int blocks = (T + tpb - 1) / tpb;
+    return launch_k(kPdlRoute, route_permute_kernel<NT>, dim3(blocks), dim3(NT), 0, s, logits,
+                    reinterpret_cast<const uint4*>(x), T, d, E, k, tpb, idx, w, counts, offsets, src, dest,
+                    reinterpret_cast<uint4*>(x_perm), reinterpret_cast<uint2*>(x8), sx, status, fold_cnt, fold_nblk);
+}
+
 cudaError_t launch_route_permute(const float* logits, const __nv_bfloat16* x, int T, int d, int E, int k,
                                  int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* src,
                                  int32_t* dest, __nv_bfloat16* x_perm, int32_t* status, int num_sms,
                                  cudaStream_t s, uint8_t* x8, float* sx, int32_t* fold_cnt, int fold_nblk) {
-    int tpb = (T + 4 * num_sms - 1) / (4 * num_sms);
-    tpb = tpb < 1 ? 1 : (tpb > kMaxTokPerBlock ? kMaxTokPerBlock : tpb);
+    switch (perm_threads(E)) {
+        case 1024:
+            return launch_route_permute_nt<1024>(logits, x, T, d, E, k, idx, w, counts, offsets, src, dest, x_perm,
+                                                 status, num_sms, s, x8, sx, fold_cnt, fold_nblk);
+        case 512:
+            return launch_route_permute_nt<512>(logits, x, T, d, E, k, idx, w, counts, offsets, src, dest, x_perm,
+                                                status, num_sms, s, x8, sx, fold_cnt, fold_nblk);
+        default:
+            return launch_route_permute_nt<256>(logits, x, T, d, E, k, idx, w, counts, offsets, src, dest, x_perm,
+                                                status, num_sms, s, x8, sx, fold_cnt, fold_nblk);
+    }
+}
+
+template <int NT>
+static cudaError_t launch_permute_nt(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
+                                     int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest,
+                                     __nv_bfloat16* x_perm, int32_t* status, int num_sms, cudaStream_t s, uint8_t* x8,
+                                     float* sx, int32_t* fold_cnt, int fold_nblk) {
+    const int tpb = perm_tokens_per_block(T, num_sms, NT);
     const int blocks = (T + tpb - 1) / tpb;
-    return launch_k(kPdlRoute, route_permute_kernel, dim3(blocks), dim3(kPermThreads), 0, s, logits,
-                    reinterpret_cast<const uint4*>(x), T, d, E, k, tpb, idx, w, counts, offsets, src, dest,
+    return launch_k(kPdlPermute, permute_kernel<NT>, dim3(blocks), dim3(NT), 0, s, idx,
+                    reinterpret_cast<const uint4*>(x), T, d, E, k, tpb, counts, offsets, src, dest,
                     reinterpret_cast<uint4*>(x_perm), reinterpret_cast<uint2*>(x8), sx, status, fold_cnt, fold_nblk);
 }
 
@@ -418,13 +474,17 @@ cudaError_t launch_permute(const int32_t* idx, const __nv_bfloat16* x, int T, in
                            int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dest,
                            __nv_bfloat16* x_perm, int32_t* status, int num_sms, cudaStream_t s, uint8_t* x8,
                            float* sx, int32_t* fold_cnt, int fold_nblk) {
-    // About four blocks per SM for the row copies, at most kMaxTokPerBlock tokens per block.
-    int tpb = (T + 4 * num_sms - 1) / (4 * num_sms);
-    tpb = tpb < 1 ? 1 : (tpb > kMaxTokPerBlock ? kMaxTokPerBlock : tpb);
-    const int blocks = (T + tpb - 1) / tpb;
-    return launch_k(kPdlPermute, permute_kernel, dim3(blocks), dim3(kPermThreads), 0, s, idx,
-                    reinterpret_cast<const uint4*>(x), T, d, E, k, tpb, counts, offsets, src, dest,
-                    reinterpret_cast<uint4*>(x_perm), reinterpret_cast<uint2*>(x8), sx, status, fold_cnt, fold_nblk);
+    switch (perm_threads(E)) {
+        case 1024:
+            return launch_permute_nt<1024>(idx, x, T, d, E, k, counts, offsets, src, dest, x_perm, status, num_sms,
+                                           s, x8, sx, fold_cnt, fold_nblk);
+        case 512:
+            return launch_permute_nt<512>(idx, x, T, d, E, k, counts, offsets, src, dest, x_perm, status, num_sms,
+                                          s, x8, sx, fold_cnt, fold_nblk);
+        default:
+            return launch_permute_nt<256>(idx, x, T, d, E, k, counts, offsets, src, dest, x_perm, status, num_sms,
+                                          s, x8, sx, fold_cnt, fold_nblk);
+    }
 }
 
 }  // namespace moe

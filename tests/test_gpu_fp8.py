@@ -136,10 +136,15 @@ def test_quantize_rows_fp8_bad_src(moe, oracle):
     assert np.array_equal(q[[0, 1, 4]], rq) and np.array_equal(sc[[0, 1, 4]], rsc)
 
 
-@pytest.mark.parametrize("T,d,E,k", [(1, 256, 8, 2), (300, 256, 8, 2), (2000, 4096, 64, 6), (77, 7168, 16, 4)])
-def test_permute_fp8_parity(moe, oracle, T, d, E, k):
+@pytest.mark.parametrize("nt", ["", "256", "1024"])
+@pytest.mark.parametrize("T,d,E,k", [(1, 256, 8, 2), (300, 256, 8, 2), (2000, 4096, 64, 6), (77, 7168, 16, 4),
+                                     (12000, 128, 8, 2)])
+def test_permute_fp8_parity(moe, oracle, T, d, E, k, nt, monkeypatch):
     """Step 2 of the FP8 layer: the permutation bit for bit, and each permuted row's codes and
-    scale equal to the oracle's quantisation of x[src[r]]."""
+    scale equal to the oracle's quantisation of x[src[r]], at every block size (MOE_PERM_THREADS;
+    "" = the default rule)."""
+    if nt:
+        monkeypatch.setenv("MOE_PERM_THREADS", nt)
     g = torch.Generator("cpu").manual_seed(T + d)
     logits = torch.randn(T, E, generator=g)
     idx, _ = oracle.route(logits.numpy(), k)

@@ -197,9 +197,14 @@ def test_fused_route_permute_nan_logits_order(moe, oracle, monkeypatch):
     assert_close(v["w"].cpu().numpy()[clean], rw[clean], 1e-6, 0, "route weights, finite rows")
 
 
+@pytest.mark.parametrize("nt", ["", "256", "512", "1024"])
 @pytest.mark.parametrize("T,d,E,k", [(4096, 4096, 8, 2), (2048, 256, 256, 8), (37, 64, 4, 4), (1, 128, 8, 2),
-                                     (999, 192, 64, 6)])
-def test_permute_parity(moe, oracle, T, d, E, k):
+                                     (999, 192, 64, 6), (12000, 64, 8, 2), (16000, 64, 64, 8)])
+def test_permute_parity(moe, oracle, T, d, E, k, nt, monkeypatch):
+    """The permutation bit for bit at every block size (MOE_PERM_THREADS; "" = the default rule),
+    including grids at the tokens-per-block cap (T = 12000 and 16000)."""
+    if nt:
+        monkeypatch.setenv("MOE_PERM_THREADS", nt)
     g = torch.Generator("cpu").manual_seed(T + d)
     idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).int()
     x = random_bf16((T, d), seed=T)
@@ -213,6 +218,23 @@ def test_permute_parity(moe, oracle, T, d, E, k):
     assert np.array_equal(src.cpu().numpy(), rs)
     assert np.array_equal(dest.cpu().numpy(), rd)
     assert np.array_equal(to_np_bits(x_perm.cpu()), oracle.gather_rows(to_np_bits(x), rs))
+
+
+@pytest.mark.parametrize("nt", ["256", "512", "1024"])
+def test_fused_route_permute_block_sizes(moe, oracle, nt, monkeypatch):
+    """Route + permute in one kernel (E <= 32, T*E <= 8192) at every block size: idx, w, src, dest
+    and x_perm against the oracle."""
+    monkeypatch.setenv("MOE_PERM_THREADS", nt)
+    w = Workload("fused_block_sizes", 1000, 128, 128, 8, 2)
+    logits, x, wgu, wd = case_inputs(w, seed=21)
+    _, v, ws = _forward_and_views(moe, w, logits, x, wgu, wd)
+    ridx, rw = oracle.route(logits.numpy(), w.k)
+    assert np.array_equal(v["idx"].cpu().numpy(), ridx)
+    assert_close(v["w"].cpu().numpy(), rw, 1e-6, 0, "route weights")
+    counts, offsets, src, dest = oracle.permute(ridx, w.E)
+    assert np.array_equal(v["src"].cpu().numpy(), src)
+    assert np.array_equal(v["dest"].cpu().numpy(), dest)
+    assert np.array_equal(to_np_bits(v["x_perm"].cpu()), oracle.gather_rows(to_np_bits(x), src))
 
 
 def _segments(oracle, T, E, k, seed, bias=("none", 0.0)):
