@@ -284,9 +284,10 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             // buffers and (four stages) between even and odd stages; warp 1 issues the even-numbered
             // blocks into buffer 0, warp 2 the odd ones into buffer 1.  A block's partial product is
             // a fresh MMA chain (nothing accumulates across blocks), so the two chains are
-            // independent and every barrier still has a single MMA thread.  A thread spends about
-            // 100 cycles issuing a tcgen05.mma, and with two threads the tensor pipe sees the next
-            // block's MMAs sooner (gate+up, Mixtral shape T=4096: 1.204 -> 1.143 ms).
+            // independent and every barrier still has a single MMA thread.  Each K block ends in a
+            // hand-over (commit, then waits for a free partial buffer and the next stage); with two
+            // threads one thread's MMAs are already queued while the other waits (gate+up, Mixtral
+            // shape T=4096: 1.204 -> 1.143 ms).
             static_assert(STAGES == 2 * NUM_PART, "ALT: each thread owns one buffer and half the stages");
             const uint32_t t = ALT ? static_cast<uint32_t>(warp - 1) : 0u;
             constexpr uint32_t idesc_normal = ptx::idesc_e4m3_f32(BM, PART_COLS, 0, 0);
