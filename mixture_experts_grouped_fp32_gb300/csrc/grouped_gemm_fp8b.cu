@@ -131,6 +131,19 @@ __device__ __forceinline__ void raise_abort(Ctl& c, int32_t* status) {
     flag_status(status, MOE_STATUS_WAIT_TIMEOUT);
 }
 
+// tcgen05.wait::ld naming the 32 registers of the load it completes, so that the compiler places
+// no read of them before it (a load into other registers may stay in flight across it).
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+                   "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+                   "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
 // silu(g) * u with the fast-divide intrinsic (its ~2 ulp error is far below h's bf16 rounding).
 __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
@@ -436,23 +449,34 @@ grouped_gemm_fp8b_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                             acc[32 + j] = fmaf(__uint_as_float(v1[j]), sj * sw1, acc[32 + j]);
                         }
                     } else {
+                        // Four 32-column chunks, software-pipelined: chunk r + 1's load is in flight
+                        // while chunk r's FMAs run (each wait names the registers it completes).
+                        // kind 0: chunks gate 0..31, up 0..31, gate 32..63, up 32..63 of this warp's
+                        // 64 h columns -> acc[0..], acc[64..], acc[32..], acc[96..]; kind 1:
+                        // columns 32r.. of its 128 -> acc[32r..].
                         const float s0 = sr * sw0, s1 = sr * sw1;
+                        auto col = [&](int r) -> uint32_t {
+                            return KIND == 0 ? static_cast<uint32_t>((r & 1) * 128 + 64 * hh + 32 * (r >> 1))
+                                             : static_cast<uint32_t>(128 * hh + 32 * r);
+                        };
+                        auto fma_chunk = [&](int r, const uint32_t (&v)[32]) {
+                            const int o = KIND == 0 ? (r & 1) * 64 + (r >> 1) * 32 : 32 * r;
+                            const float sc = KIND == 0 ? ((r & 1) ? s1 : s0) : s0;
 #pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            // kind 0: gate and up columns 32q.. of this warp's 64 -> acc[32q..],
-                            // acc[64 + 32q..]; kind 1: columns 64q.. and 64q + 32.. of its 128.
-                            const uint32_t ca = KIND == 0 ? 64 * hh + 32 * q : 128 * hh + 64 * q;
-                            const uint32_t cb = KIND == 0 ? 128 + 64 * hh + 32 * q : 128 * hh + 64 * q + 32;
-                            ptx::tmem_ld_32x32b_x32(taddr + ca, v0);
-                            ptx::tmem_ld_32x32b_x32(taddr + cb, v1);
-                            ptx::tmem_ld_wait();
-                            const int oa = KIND == 0 ? 32 * q : 64 * q, ob = KIND == 0 ? 64 + 32 * q : 64 * q + 32;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                acc[oa + j] = fmaf(__uint_as_float(v0[j]), s0, acc[oa + j]);
-                                acc[ob + j] = fmaf(__uint_as_float(v1[j]), s1, acc[ob + j]);
-                            }
-                        }
+                            for (int j = 0; j < 32; ++j) acc[o + j] = fmaf(__uint_as_float(v[j]), sc, acc[o + j]);
+                        };
+                        ptx::tmem_ld_32x32b_x32(taddr + col(0), v0);
+                        tmem_ld_wait_regs(v0);
+                        ptx::tmem_ld_32x32b_x32(taddr + col(1), v1);
+                        fma_chunk(0, v0);
+                        tmem_ld_wait_regs(v1);
+                        ptx::tmem_ld_32x32b_x32(taddr + col(2), v0);
+                        fma_chunk(1, v1);
+                        tmem_ld_wait_regs(v0);
+                        ptx::tmem_ld_32x32b_x32(taddr + col(3), v1);
+                        fma_chunk(2, v0);
+                        tmem_ld_wait_regs(v1);
+                        fma_chunk(3, v1);
                     }
                 }
                 ptx::tc_fence_before();
