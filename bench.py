@@ -93,8 +93,7 @@ AUTO_STEPS_MIN, AUTO_STEPS_MAX = 50, 4000
 # value, else null.
 
 _TRAFFIC_HASH = "a50adcb350358d68"  # GEMM source hash the captures below were taken at
-_TRAFFIC_HASH_FP8B = "8d0d363f7c12173c"  # ... and that of the blockwise FP8 kernel's sources
-# (captured at 2cc65fcf7ddc68c6; the source has changed since only in a comment)
+_TRAFFIC_HASH_FP8B = "cb56d74ba1e13f0f"  # ... and that of the blockwise FP8 kernel's sources
 MEASURED_TRAFFIC = {
     ("deepseek_e32_t256", "gateup_swiglu"): (1919805440, _TRAFFIC_HASH),
     ("deepseek_e32_t256", "down"): (1010249216, _TRAFFIC_HASH),
@@ -108,18 +107,18 @@ MEASURED_TRAFFIC = {
     ("mixtral_t512_skew40", "down"): (984870656, _TRAFFIC_HASH),
     ("mixtral_t512", "gateup_swiglu"): (1917185792, _TRAFFIC_HASH),
     ("mixtral_t512", "down"): (984192000, _TRAFFIC_HASH),
-    ("deepseek_e32_t256", "gateup_swiglu_fp8b"): (966528512, _TRAFFIC_HASH_FP8B),
-    ("deepseek_e32_t256", "down_fp8b"): (535162112, _TRAFFIC_HASH_FP8B),
-    ("deepseek_v3like_e32_t1024", "gateup_swiglu_fp8b"): (1022521856, _TRAFFIC_HASH_FP8B),
-    ("deepseek_v3like_e32_t1024", "down_fp8b"): (730804480, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t32", "gateup_swiglu_fp8b"): (944823296, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t32", "down_fp8b"): (474663936, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t4096", "gateup_swiglu_fp8b"): (1090318080, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t4096", "down_fp8b"): (775504384, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512_skew40", "gateup_swiglu_fp8b"): (962286080, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512_skew40", "down_fp8b"): (515716864, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512", "gateup_swiglu_fp8b"): (963255296, _TRAFFIC_HASH_FP8B),
-    ("mixtral_t512", "down_fp8b"): (611966720, _TRAFFIC_HASH_FP8B),
+    ("deepseek_e32_t256", "gateup_swiglu_fp8b"): (966629888, _TRAFFIC_HASH_FP8B),
+    ("deepseek_e32_t256", "down_fp8b"): (534442240, _TRAFFIC_HASH_FP8B),
+    ("deepseek_v3like_e32_t1024", "gateup_swiglu_fp8b"): (1022789120, _TRAFFIC_HASH_FP8B),
+    ("deepseek_v3like_e32_t1024", "down_fp8b"): (728637696, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t32", "gateup_swiglu_fp8b"): (944861440, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t32", "down_fp8b"): (474419968, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t4096", "gateup_swiglu_fp8b"): (1090738176, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t4096", "down_fp8b"): (776733440, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512_skew40", "gateup_swiglu_fp8b"): (962235136, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512_skew40", "down_fp8b"): (514651392, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512", "gateup_swiglu_fp8b"): (963427840, _TRAFFIC_HASH_FP8B),
+    ("mixtral_t512", "down_fp8b"): (591564544, _TRAFFIC_HASH_FP8B),
     ("deepseek_e32_t256", "gateup_swiglu_fp8"): (966086656, _TRAFFIC_HASH),
     ("deepseek_e32_t256", "down_fp8"): (535560192, _TRAFFIC_HASH),
     ("deepseek_v3like_e32_t1024", "gateup_swiglu_fp8"): (1142837248, _TRAFFIC_HASH),
